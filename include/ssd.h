@@ -1,0 +1,137 @@
+/*
+ * ssd.h -- C ABI of the GB300 (sm_103a) Mamba-2 SSD chunked selective scan.
+ *
+ * The operation (burn-mamba, page "combined_backward.rs" under
+ * burn_mamba/mamba2/ssd/serial_recalculated/: the five-kernel chunked scan
+ * K1 chunk cumsum of dt*A, K2 C.B^T per chunk, K3 chunk-end states, K4
+ * inter-chunk state passing, K5 chunk scan with the D skip; and its
+ * recompute-based analytic backward, section "Recompute-based gradient math
+ * for the Mamba-2 SSD") is, per batch b and head h with group g = h/(H/G):
+ *
+ *     S_{-1} = init[b,h];   S_t = exp(dt[b,h,t] * A[h]) * S_{t-1}
+ *                                 + dt[b,h,t] * x[b,t,h,:] (outer) B[b,t,g,:]
+ *     y[b,t,h,p] = sum_r S_t[p,r] C[b,t,g,r] + D[h] x[b,t,h,p]
+ *     final_state[b,h] = S_{V-1}
+ *
+ * where V = valid_len[b] (default L).  Tokens t >= V are absent: no state
+ * update, y = 0, and every per-token gradient there is 0.  ssd_backward
+ * returns the gradient of  Loss = <dy, y> + <d_final_state, final_state>
+ * with respect to x, dt, A, B, C, D and init, recomputing every forward
+ * intermediate from those inputs (nothing is saved between the two calls).
+ *
+ * Layouts: all tensors are dense, row-major, contiguous.
+ *     x, y, dy, dx           [batch, seqlen, nheads, headdim]     (T)
+ *     B, C, dB, dC           [batch, seqlen, ngroups, dstate]     (T)
+ *     dt, ddt                [batch, nheads, seqlen]              (fp32)
+ *     A, D, dA, dD           [nheads]                             (fp32)
+ *     init_state, final_state, d_final_state, d_init_state
+ *                            [batch, nheads, headdim, dstate]     (fp32)
+ *     valid_len              [batch]                              (int32)
+ * T is fp32 for SSD_F32 and bf16 for SSD_BF16.  A is the (negative) decay
+ * rate used as given; dt is the already-discretised step used as given.
+ *
+ * Ownership and memory: every pointer is a DEVICE pointer owned by the
+ * caller.  The library allocates no memory and keeps no state between calls;
+ * scratch lives in the caller's `workspace`, sized by ssd_workspace_bytes().
+ * Outputs are overwritten, never accumulated into.  Tensor pointers and the
+ * workspace must be 16-byte aligned.
+ *
+ * Streams and errors: work is enqueued on `stream` (a cudaStream_t; NULL is
+ * the legacy default stream) and the call returns without synchronising.
+ * Argument errors are detected on the host and returned before anything is
+ * enqueued.  Launch failures return SSD_ERR_CUDA.  Kernels that wait on a
+ * shared-memory barrier give up after a bounded number of polls and record
+ * SSD_ERR_TIMEOUT in a status word inside the workspace, readable with
+ * ssd_workspace_status() after the stream has been synchronised.
+ */
+#ifndef SSD_GB300_H
+#define SSD_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    SSD_OK = 0,
+    SSD_ERR_INVALID_ARG = 1,  /* null required pointer, bad dims, H % G != 0, misalignment */
+    SSD_ERR_UNSUPPORTED = 2,  /* shape outside the supported range (see ssd_supported) */
+    SSD_ERR_WORKSPACE = 3,    /* workspace smaller than ssd_workspace_bytes() */
+    SSD_ERR_CUDA = 4,         /* a CUDA call or kernel launch failed */
+    SSD_ERR_TIMEOUT = 5       /* a bounded device-side wait expired */
+} ssd_status;
+
+typedef enum {
+    SSD_F32 = 0,   /* every tensor fp32; CUDA-core kernels, fp32 arithmetic */
+    SSD_BF16 = 1   /* x, B, C, dy, y, dx, dB, dC bf16; fp32 accumulate and state */
+} ssd_dtype;
+
+/* Execution-path flags (ssd_dims.flags). */
+#define SSD_FLAG_NONE 0u
+#define SSD_FLAG_SIMT 1u   /* SSD_BF16 only: use the CUDA-core kernels instead of
+                              the tcgen05 tensor-core kernels for the contractions */
+
+typedef struct {
+    int64_t batch;      /* b  >= 1 */
+    int64_t seqlen;     /* L  >= 1 (need not be a multiple of chunk_len) */
+    int64_t nheads;     /* H  >= 1 */
+    int64_t headdim;    /* P  (the page's per_head_dim) */
+    int64_t dstate;     /* N  (the page's state_rank) */
+    int64_t ngroups;    /* G, divides H; B and C are shared by the H/G heads of a group */
+    int64_t chunk_len;  /* Q, one of 16, 32, 64, 128, 256 */
+    uint32_t flags;     /* SSD_FLAG_* */
+    uint32_t reserved;  /* must be 0 */
+} ssd_dims;
+
+/* Shape support: returns SSD_OK when (dims, dtype) can run, else
+ * SSD_ERR_INVALID_ARG / SSD_ERR_UNSUPPORTED.  Limits: headdim <= 128 and a
+ * multiple of 4; dstate <= 256 and a multiple of 4.  The tcgen05 path of
+ * SSD_BF16 needs chunk_len in {64, 128, 256}, headdim == 64 and dstate in
+ * {64, 128}; other SSD_BF16 shapes run on the CUDA-core kernels. */
+ssd_status ssd_supported(const ssd_dims *dims, ssd_dtype dtype);
+
+/* Bytes of device workspace ssd_forward (backward = 0) or ssd_backward
+ * (backward = 1) needs; 0 when the arguments are invalid. */
+size_t ssd_workspace_bytes(const ssd_dims *dims, ssd_dtype dtype, int backward);
+
+/* Forward: y (and optionally final_state).
+ *   init_state   may be NULL (zeros);  valid_len may be NULL (= seqlen);
+ *   final_state  may be NULL (not written). */
+ssd_status ssd_forward(const ssd_dims *dims, ssd_dtype dtype,
+                       const void *x, const float *dt, const float *A,
+                       const void *B, const void *C, const float *D,
+                       const float *init_state, const int32_t *valid_len,
+                       void *y, float *final_state,
+                       void *workspace, size_t workspace_bytes, void *stream);
+
+/* Backward with recompute: gradients of <dy,y> + <d_final_state,final_state>.
+ *   d_final_state may be NULL (zeros);  d_init_state may be NULL (not written).
+ *   dA and dD are reduced over batch and time in a fixed order (deterministic). */
+ssd_status ssd_backward(const ssd_dims *dims, ssd_dtype dtype,
+                        const void *x, const float *dt, const float *A,
+                        const void *B, const void *C, const float *D,
+                        const float *init_state, const int32_t *valid_len,
+                        const void *dy, const float *d_final_state,
+                        void *dx, float *ddt, float *dA, void *dB, void *dC, float *dD,
+                        float *d_init_state,
+                        void *workspace, size_t workspace_bytes, void *stream);
+
+/* Reads (synchronously, on `stream`) the device status word that the last
+ * call on this workspace left: SSD_OK or SSD_ERR_TIMEOUT. */
+ssd_status ssd_workspace_status(const void *workspace, size_t workspace_bytes, void *stream);
+
+/* Static description of a status code. */
+const char *ssd_status_str(ssd_status status);
+
+/* Detail of the most recent failure on the calling host thread ("" if none). */
+const char *ssd_last_error(void);
+
+/* ABI version (major * 10000 + minor * 100 + patch). */
+int ssd_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* SSD_GB300_H */

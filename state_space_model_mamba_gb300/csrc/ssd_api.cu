@@ -1,0 +1,305 @@
+// ssd_api.cu -- the C ABI declared in include/ssd.h: argument validation,
+// workspace carving and the launch sequence of the forward and of the
+// recompute backward (burn-mamba, "combined_backward.rs": recompute K1-K4
+// from the leaves, BLUE backward, K4 backward, ORANGE + K3 backward, K2
+// backward, K1 backward and the dA / dD reductions).
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include "ssd.h"
+#include "ssd_internal.cuh"
+#include "ssd_tc.cuh"
+
+namespace ssd {
+namespace {
+
+thread_local char g_last_error[512] = "";
+
+ssd_status fail(ssd_status st, const char *fmt, ...) __attribute__((format(printf, 2, 3)));
+ssd_status fail(ssd_status st, const char *fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_last_error, sizeof(g_last_error), fmt, ap);
+    va_end(ap);
+    return st;
+}
+
+constexpr size_t kAlign = 256;
+size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
+
+struct Layout {
+    size_t status, cumA, endA, CB, states, states_bf, dstates, dstates_bf;
+    size_t dcum_blue, dcum_main, d_delta, ddt_main, d_endA_part, dD_part, dA_part, d_cb, dBC_part;
+    size_t total;
+    int k4_nblk, dD_per, nslice;
+};
+
+bool use_tensor_cores(const ssd_dims &d, ssd_dtype dt) {
+    return dt == SSD_BF16 && !(d.flags & SSD_FLAG_SIMT) && tc_supported(d.headdim, d.dstate, d.chunk_len);
+}
+
+Layout make_layout(const ssd_dims &d, ssd_dtype dt, bool backward) {
+    Layout lo;
+    memset(&lo, 0, sizeof(lo));
+    const size_t b = d.batch, H = d.nheads, P = d.headdim, N = d.dstate, G = d.ngroups,
+                 Q = d.chunk_len;
+    const size_t n = (d.seqlen + d.chunk_len - 1) / d.chunk_len;
+    const bool tc = use_tensor_cores(d, dt);
+    const size_t tok = b * H * n * Q, nst = b * n * H * P * N;
+    lo.k4_nblk = (int)((P * N / 4 + kK4Threads - 1) / kK4Threads);
+    lo.dD_per = tc ? tc_dD_per(d.chunk_len) : (int)(Q / kMainRows);
+    lo.nslice = tc ? tc_group_slices(d) : 1;
+    size_t off = 0;
+    auto take = [&](size_t bytes) { size_t o = off; off += align_up(bytes); return o; };
+    lo.status = take(16);
+    lo.cumA = take(4 * tok);
+    lo.endA = take(4 * b * H * n);
+    lo.CB = take(4 * b * n * G * Q * Q);
+    lo.states = take(4 * nst);
+    lo.states_bf = tc ? take(2 * nst) : 0;
+    if (backward) {
+        lo.dstates = take(4 * nst);
+        lo.dstates_bf = tc ? take(2 * nst) : 0;
+        lo.dcum_blue = take(4 * tok);
+        lo.dcum_main = take(4 * tok);
+        lo.d_delta = take(4 * tok);
+        lo.ddt_main = take(4 * tok);
+        lo.d_endA_part = take(4 * b * H * n * lo.k4_nblk);
+        lo.dD_part = take(4 * b * n * H * lo.dD_per);
+        lo.dA_part = take(4 * b * H * n);
+        lo.d_cb = tc ? 0 : take(4 * b * n * G * Q * Q);
+        lo.dBC_part = tc ? take(4 * (size_t)lo.nslice * 2 * b * n * G * Q * N) : 0;
+    }
+    lo.total = off;
+    return lo;
+}
+
+bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
+
+ssd_status validate_dims(const ssd_dims *d, ssd_dtype dt) {
+    if (!d) return fail(SSD_ERR_INVALID_ARG, "dims is NULL");
+    if (dt != SSD_F32 && dt != SSD_BF16) return fail(SSD_ERR_INVALID_ARG, "unknown dtype %d", (int)dt);
+    if (d->reserved != 0) return fail(SSD_ERR_INVALID_ARG, "dims.reserved must be 0");
+    if (d->flags & ~(uint32_t)SSD_FLAG_SIMT) return fail(SSD_ERR_INVALID_ARG, "unknown flags 0x%x", d->flags);
+    if (d->batch < 1 || d->seqlen < 1 || d->nheads < 1 || d->headdim < 1 || d->dstate < 1 ||
+        d->ngroups < 1 || d->chunk_len < 1)
+        return fail(SSD_ERR_INVALID_ARG, "every dimension must be >= 1");
+    if (d->nheads % d->ngroups != 0)
+        return fail(SSD_ERR_INVALID_ARG, "nheads (%lld) must be a multiple of ngroups (%lld)",
+                    (long long)d->nheads, (long long)d->ngroups);
+    const int64_t q = d->chunk_len;
+    if (!(q == 16 || q == 32 || q == 64 || q == 128 || q == 256))
+        return fail(SSD_ERR_UNSUPPORTED, "chunk_len %lld not in {16,32,64,128,256}", (long long)q);
+    if (d->headdim > 128 || d->headdim % 4 != 0)
+        return fail(SSD_ERR_UNSUPPORTED, "headdim %lld: need a multiple of 4 <= 128", (long long)d->headdim);
+    if (d->dstate > 256 || d->dstate % 4 != 0)
+        return fail(SSD_ERR_UNSUPPORTED, "dstate %lld: need a multiple of 4 <= 256", (long long)d->dstate);
+    // index and grid limits
+    const int64_t n = (d->seqlen + q - 1) / q;
+    const double tok = (double)d->batch * (double)(n * q) * (double)d->nheads;
+    if (tok * (double)d->headdim > 4.0e15 || (double)d->batch * n * d->nheads > 2.0e9 ||
+        d->seqlen > (1LL << 30) || d->nheads > (1LL << 20))
+        return fail(SSD_ERR_UNSUPPORTED, "problem too large");
+    return SSD_OK;
+}
+
+Params base_params(const ssd_dims &d, const Layout &lo, void *ws) {
+    Params p;
+    memset(&p, 0, sizeof(p));
+    p.b = (int)d.batch;
+    p.L = (int)d.seqlen;
+    p.H = (int)d.nheads;
+    p.P = (int)d.headdim;
+    p.N = (int)d.dstate;
+    p.G = (int)d.ngroups;
+    p.Q = (int)d.chunk_len;
+    p.n = (int)((d.seqlen + d.chunk_len - 1) / d.chunk_len);
+    p.hpg = p.H / p.G;
+    char *w = (char *)ws;
+    auto f = [&](size_t off) { return (float *)(w + off); };
+    p.status = (int *)(w + lo.status);
+    p.cumA = f(lo.cumA);
+    p.endA = f(lo.endA);
+    p.CB = f(lo.CB);
+    p.states = f(lo.states);
+    p.states_bf = lo.states_bf ? (bf16 *)(w + lo.states_bf) : nullptr;
+    if (lo.dstates) {
+        p.dstates = f(lo.dstates);
+        p.dstates_bf = lo.dstates_bf ? (bf16 *)(w + lo.dstates_bf) : nullptr;
+        p.dcum_blue = f(lo.dcum_blue);
+        p.dcum_main = f(lo.dcum_main);
+        p.d_delta = f(lo.d_delta);
+        p.ddt_main = f(lo.ddt_main);
+        p.d_endA_part = f(lo.d_endA_part);
+        p.dD_part = f(lo.dD_part);
+        p.dA_part = f(lo.dA_part);
+        p.d_cb = lo.d_cb ? f(lo.d_cb) : nullptr;
+        p.dBC_part = lo.dBC_part ? f(lo.dBC_part) : nullptr;
+    }
+    p.k4_nblk = lo.k4_nblk;
+    p.dD_per = lo.dD_per;
+    p.nslice = lo.nslice;
+    return p;
+}
+
+#define SSD_TRY(expr)                                                                     \
+    do {                                                                                  \
+        cudaError_t e_ = (expr);                                                          \
+        if (e_ != cudaSuccess)                                                            \
+            return fail(SSD_ERR_CUDA, "%s: %s", #expr, cudaGetErrorString(e_));          \
+    } while (0)
+
+template <typename T>
+ssd_status run_forward_chain(const Params &p, bool tc, bool write_final, cudaStream_t s) {
+    SSD_TRY(launch_k1_cumsum(p, s));
+    if (tc) {
+        SSD_TRY(launch_tc_k2(p, s));
+        SSD_TRY(launch_tc_k3(p, s));
+    } else {
+        SSD_TRY(launch_simt_k2<T>(p, s));
+        SSD_TRY(launch_simt_k3<T>(p, s));
+    }
+    SSD_TRY(launch_k4_state_passing(p, write_final, s));
+    return SSD_OK;
+}
+
+}  // namespace
+}  // namespace ssd
+
+using namespace ssd;
+
+extern "C" {
+
+int ssd_version(void) { return 10000; }
+
+const char *ssd_last_error(void) { return g_last_error; }
+
+const char *ssd_status_str(ssd_status st) {
+    switch (st) {
+        case SSD_OK: return "ok";
+        case SSD_ERR_INVALID_ARG: return "invalid argument";
+        case SSD_ERR_UNSUPPORTED: return "unsupported shape";
+        case SSD_ERR_WORKSPACE: return "workspace too small";
+        case SSD_ERR_CUDA: return "CUDA error";
+        case SSD_ERR_TIMEOUT: return "device-side wait timed out";
+    }
+    return "unknown status";
+}
+
+ssd_status ssd_supported(const ssd_dims *dims, ssd_dtype dtype) {
+    g_last_error[0] = 0;
+    return validate_dims(dims, dtype);
+}
+
+size_t ssd_workspace_bytes(const ssd_dims *dims, ssd_dtype dtype, int backward) {
+    if (validate_dims(dims, dtype) != SSD_OK) return 0;
+    return make_layout(*dims, dtype, backward != 0).total;
+}
+
+ssd_status ssd_forward(const ssd_dims *dims, ssd_dtype dtype, const void *x, const float *dt,
+                       const float *A, const void *B, const void *C, const float *D,
+                       const float *init_state, const int32_t *valid_len, void *y,
+                       float *final_state, void *workspace, size_t workspace_bytes, void *stream) {
+    g_last_error[0] = 0;
+    ssd_status st = validate_dims(dims, dtype);
+    if (st != SSD_OK) return st;
+    const void *req[] = {x, dt, A, B, C, D, y, workspace};
+    const char *names[] = {"x", "dt", "A", "B", "C", "D", "y", "workspace"};
+    for (int i = 0; i < 8; ++i) {
+        if (!req[i]) return fail(SSD_ERR_INVALID_ARG, "%s is NULL", names[i]);
+        if (!aligned16(req[i])) return fail(SSD_ERR_INVALID_ARG, "%s is not 16-byte aligned", names[i]);
+    }
+    if ((init_state && !aligned16(init_state)) || (final_state && !aligned16(final_state)))
+        return fail(SSD_ERR_INVALID_ARG, "state pointers must be 16-byte aligned");
+    const Layout lo = make_layout(*dims, dtype, false);
+    if (workspace_bytes < lo.total)
+        return fail(SSD_ERR_WORKSPACE, "workspace %zu < required %zu", workspace_bytes, lo.total);
+    const bool tc = use_tensor_cores(*dims, dtype);
+    Params p = base_params(*dims, lo, workspace);
+    p.x = x; p.dt = dt; p.A = A; p.B = B; p.C = C; p.D = D; p.init = init_state;
+    p.valid_len = valid_len; p.y = y; p.final_state = final_state;
+    cudaStream_t s = (cudaStream_t)stream;
+    SSD_TRY(cudaMemsetAsync(p.status, 0, sizeof(int), s));
+    if (dtype == SSD_F32) {
+        st = run_forward_chain<float>(p, false, true, s);
+        if (st != SSD_OK) return st;
+        SSD_TRY(launch_simt_k5<float>(p, s));
+    } else {
+        st = run_forward_chain<bf16>(p, tc, true, s);
+        if (st != SSD_OK) return st;
+        if (tc) SSD_TRY(launch_tc_k5(p, s));
+        else SSD_TRY(launch_simt_k5<bf16>(p, s));
+    }
+    return SSD_OK;
+}
+
+ssd_status ssd_backward(const ssd_dims *dims, ssd_dtype dtype, const void *x, const float *dt,
+                        const float *A, const void *B, const void *C, const float *D,
+                        const float *init_state, const int32_t *valid_len, const void *dy,
+                        const float *d_final_state, void *dx, float *ddt, float *dA, void *dB,
+                        void *dC, float *dD, float *d_init_state, void *workspace,
+                        size_t workspace_bytes, void *stream) {
+    g_last_error[0] = 0;
+    ssd_status st = validate_dims(dims, dtype);
+    if (st != SSD_OK) return st;
+    const void *req[] = {x, dt, A, B, C, D, dy, dx, ddt, dA, dB, dC, dD, workspace};
+    const char *names[] = {"x", "dt", "A", "B", "C", "D", "dy", "dx", "ddt", "dA", "dB", "dC",
+                           "dD", "workspace"};
+    for (int i = 0; i < 14; ++i) {
+        if (!req[i]) return fail(SSD_ERR_INVALID_ARG, "%s is NULL", names[i]);
+        if (!aligned16(req[i])) return fail(SSD_ERR_INVALID_ARG, "%s is not 16-byte aligned", names[i]);
+    }
+    if ((init_state && !aligned16(init_state)) || (d_final_state && !aligned16(d_final_state)) ||
+        (d_init_state && !aligned16(d_init_state)))
+        return fail(SSD_ERR_INVALID_ARG, "state pointers must be 16-byte aligned");
+    const Layout lo = make_layout(*dims, dtype, true);
+    if (workspace_bytes < lo.total)
+        return fail(SSD_ERR_WORKSPACE, "workspace %zu < required %zu", workspace_bytes, lo.total);
+    const bool tc = use_tensor_cores(*dims, dtype);
+    Params p = base_params(*dims, lo, workspace);
+    p.x = x; p.dt = dt; p.A = A; p.B = B; p.C = C; p.D = D; p.init = init_state;
+    p.valid_len = valid_len; p.dy = dy; p.d_final = d_final_state; p.dx = dx; p.ddt = ddt;
+    p.dA = dA; p.dB = dB; p.dC = dC; p.dD = dD; p.d_init = d_init_state;
+    cudaStream_t s = (cudaStream_t)stream;
+    SSD_TRY(cudaMemsetAsync(p.status, 0, sizeof(int), s));
+    if (dtype == SSD_F32) {
+        st = run_forward_chain<float>(p, false, false, s);
+        if (st != SSD_OK) return st;
+        SSD_TRY(launch_simt_bwd_blue<float>(p, s));
+        SSD_TRY(launch_bwd_k4(p, s));
+        SSD_TRY(launch_simt_bwd_main<float>(p, s));
+        SSD_TRY(launch_simt_bwd_group<float>(p, s));
+    } else {
+        st = run_forward_chain<bf16>(p, tc, false, s);
+        if (st != SSD_OK) return st;
+        if (tc) {
+            SSD_TRY(launch_tc_bwd_blue(p, s));
+            SSD_TRY(launch_bwd_k4(p, s));
+            SSD_TRY(launch_tc_bwd_main(p, s));
+            SSD_TRY(launch_tc_bwd_group(p, s));
+        } else {
+            SSD_TRY(launch_simt_bwd_blue<bf16>(p, s));
+            SSD_TRY(launch_bwd_k4(p, s));
+            SSD_TRY(launch_simt_bwd_main<bf16>(p, s));
+            SSD_TRY(launch_simt_bwd_group<bf16>(p, s));
+        }
+    }
+    SSD_TRY(launch_bwd_k1(p, s));
+    SSD_TRY(launch_bwd_finalize(p, s));
+    return SSD_OK;
+}
+
+ssd_status ssd_workspace_status(const void *workspace, size_t workspace_bytes, void *stream) {
+    g_last_error[0] = 0;
+    if (!workspace || workspace_bytes < 16) return fail(SSD_ERR_INVALID_ARG, "bad workspace");
+    int v = 0;
+    cudaStream_t s = (cudaStream_t)stream;
+    SSD_TRY(cudaMemcpyAsync(&v, workspace, sizeof(int), cudaMemcpyDeviceToHost, s));
+    SSD_TRY(cudaStreamSynchronize(s));
+    if (v == SSD_OK) return SSD_OK;
+    if (v == SSD_ERR_TIMEOUT) return fail(SSD_ERR_TIMEOUT, "a device-side wait gave up");
+    return fail(SSD_ERR_CUDA, "unexpected device status %d", v);
+}
+
+}  // extern "C"

@@ -1,0 +1,125 @@
+// ssd_internal.cuh -- shared definitions of the SSD kernels (not part of the ABI).
+//
+// Index conventions (all row-major):
+//   x/y/dy/dx  [b, L, H, P]      B/C/dB/dC  [b, L, G, N]      dt/ddt [b, H, L]
+//   cumA, per-token chunk quantities     [b, H, n, Q]   (n = ceil(L / Q))
+//   endA                                 [b, H, n]
+//   CB (per chunk and group)             [b, n, G, Q, Q]
+//   chunk states (intra -> s_in, d_s_in -> d_intra)   [b, n, H, P, N]
+#pragma once
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace ssd {
+
+typedef __nv_bfloat16 bf16;
+
+struct Params {
+    // shape
+    int b, L, H, P, N, G, Q, n, hpg;
+    // leaves
+    const void *x;
+    const float *dt, *A, *D, *init;
+    const void *B, *C;
+    const int32_t *valid_len;
+    // forward outputs
+    void *y;
+    float *final_state;
+    // backward inputs / outputs
+    const void *dy;
+    const float *d_final;
+    void *dx, *dB, *dC;
+    float *ddt, *dA, *dD, *d_init;
+    // workspace
+    float *cumA, *endA, *CB, *states, *dstates;
+    bf16 *states_bf, *dstates_bf;
+    float *dcum_blue, *dcum_main, *d_delta, *ddt_main;
+    float *d_endA_part;  // [b, H, n, k4_nblk]
+    int k4_nblk;
+    float *dD_part;      // [b, n, H, dD_per]
+    int dD_per;
+    float *dA_part;      // [b, H, n]
+    float *d_cb;         // [b, n, G, Q, Q]   (CUDA-core group path)
+    float *dBC_part;     // [nslice, 2, b, n, G, Q, N]  (tensor-core group path)
+    int nslice;
+    int *status;         // device status word (SSD_OK / SSD_ERR_TIMEOUT)
+};
+
+// ---------------------------------------------------------------- small helpers
+__device__ __forceinline__ int valid_len_of(const Params &p, int bi) {
+    int V = p.L;
+    if (p.valid_len) {
+        V = p.valid_len[bi];
+        V = V < 0 ? 0 : (V > p.L ? p.L : V);
+    }
+    return V;
+}
+
+__device__ __forceinline__ float ldf(const float *a, size_t i) { return a[i]; }
+__device__ __forceinline__ float ldf(const bf16 *a, size_t i) { return __bfloat162float(a[i]); }
+__device__ __forceinline__ void stf(float *a, size_t i, float v) { a[i] = v; }
+__device__ __forceinline__ void stf(bf16 *a, size_t i, float v) { a[i] = __float2bfloat16_rn(v); }
+
+__device__ __forceinline__ size_t ix_x(const Params &p, int bi, int t, int h, int pp) {
+    return ((size_t)((size_t)bi * p.L + t) * p.H + h) * p.P + pp;
+}
+__device__ __forceinline__ size_t ix_bc(const Params &p, int bi, int t, int g, int r) {
+    return ((size_t)((size_t)bi * p.L + t) * p.G + g) * p.N + r;
+}
+__device__ __forceinline__ size_t ix_dt(const Params &p, int bi, int h, int t) {
+    return ((size_t)bi * p.H + h) * p.L + t;
+}
+__device__ __forceinline__ size_t ix_chunk(const Params &p, int bi, int h, int c) {  // [b,H,n]
+    return ((size_t)bi * p.H + h) * p.n + c;
+}
+__device__ __forceinline__ size_t ix_state(const Params &p, int bi, int c, int h) {  // start of P x N
+    return (((size_t)bi * p.n + c) * p.H + h) * (size_t)p.P * p.N;
+}
+__device__ __forceinline__ size_t ix_cb(const Params &p, int bi, int c, int g) {  // start of Q x Q
+    return (((size_t)bi * p.n + c) * p.G + g) * (size_t)p.Q * p.Q;
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+// Fixed-order block sum (deterministic for a fixed blockDim); red has >= 32 floats.
+__device__ __forceinline__ float block_sum(float v, float *red) {
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    v = warp_sum(v);
+    __syncthreads();
+    if (lane == 0) red[wid] = v;
+    __syncthreads();
+    const int nw = (blockDim.x + 31) >> 5;
+    float s = 0.f;
+    if (wid == 0) {
+        s = lane < nw ? red[lane] : 0.f;
+        s = warp_sum(s);
+    }
+    return s;  // valid in warp 0
+}
+
+// ---------------------------------------------------------------- launchers
+// Shared by both execution paths (ssd_scan.cu).
+cudaError_t launch_k1_cumsum(const Params &p, cudaStream_t s);
+cudaError_t launch_k4_state_passing(const Params &p, bool write_final, cudaStream_t s);
+cudaError_t launch_bwd_k4(const Params &p, cudaStream_t s);
+cudaError_t launch_bwd_k1(const Params &p, cudaStream_t s);
+cudaError_t launch_bwd_finalize(const Params &p, cudaStream_t s);
+
+// CUDA-core kernels for the contractions (ssd_simt.cu), T = float or bf16.
+template <typename T> cudaError_t launch_simt_k2(const Params &p, cudaStream_t s);
+template <typename T> cudaError_t launch_simt_k3(const Params &p, cudaStream_t s);
+template <typename T> cudaError_t launch_simt_k5(const Params &p, cudaStream_t s);
+template <typename T> cudaError_t launch_simt_bwd_blue(const Params &p, cudaStream_t s);
+template <typename T> cudaError_t launch_simt_bwd_main(const Params &p, cudaStream_t s);
+template <typename T> cudaError_t launch_simt_bwd_group(const Params &p, cudaStream_t s);
+
+// Geometry constants of the CUDA-core kernels that size workspace buffers.
+constexpr int kK4Threads = 256;             // threads per block of the state-passing kernels
+constexpr int kMainRows = 16;               // source rows per block of the backward main kernel
+
+}  // namespace ssd

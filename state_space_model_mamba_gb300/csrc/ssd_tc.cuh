@@ -1,0 +1,22 @@
+// ssd_tc.cuh -- tcgen05 tensor-core kernels of the bf16 path (ssd_tc.cu).
+#pragma once
+#include "ssd.h"
+#include "ssd_internal.cuh"
+
+namespace ssd {
+
+// True when the tensor-core kernels cover (headdim, dstate, chunk_len).
+bool tc_supported(int64_t P, int64_t N, int64_t Q);
+// dD partials per (b, chunk, head) written by the tensor-core main backward.
+int tc_dD_per(int64_t Q);
+// Head slices of the group-level backward (partial dB / dC sums).
+int tc_group_slices(const ssd_dims &d);
+
+cudaError_t launch_tc_k2(const Params &p, cudaStream_t s);
+cudaError_t launch_tc_k3(const Params &p, cudaStream_t s);
+cudaError_t launch_tc_k5(const Params &p, cudaStream_t s);
+cudaError_t launch_tc_bwd_blue(const Params &p, cudaStream_t s);
+cudaError_t launch_tc_bwd_main(const Params &p, cudaStream_t s);
+cudaError_t launch_tc_bwd_group(const Params &p, cudaStream_t s);
+
+}  // namespace ssd

@@ -1,0 +1,222 @@
+"""Thin Python binding of ``libssd.so`` (the C ABI in ``include/ssd.h``).
+
+Argument marshalling only: every step of the selective scan runs in the CUDA
+kernels behind the ABI.  Tensors are torch CUDA tensors (PyTorch supplies
+device memory and streams); the binding checks dtypes and shapes, allocates
+outputs and workspace with torch, and passes raw device pointers plus the
+current CUDA stream.  There is no fallback: if the library is missing or a
+call fails, a RuntimeError is raised.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from dataclasses import dataclass
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "lib", "libssd.so")
+
+SSD_F32, SSD_BF16 = 0, 1
+SSD_FLAG_SIMT = 1
+STATUS = {0: "SSD_OK", 1: "SSD_ERR_INVALID_ARG", 2: "SSD_ERR_UNSUPPORTED",
+          3: "SSD_ERR_WORKSPACE", 4: "SSD_ERR_CUDA", 5: "SSD_ERR_TIMEOUT"}
+EXPORTED = ("ssd_supported", "ssd_workspace_bytes", "ssd_forward", "ssd_backward",
+            "ssd_workspace_status", "ssd_status_str", "ssd_last_error", "ssd_version")
+
+
+class SsdDims(ctypes.Structure):
+    _fields_ = [("batch", ctypes.c_int64), ("seqlen", ctypes.c_int64),
+                ("nheads", ctypes.c_int64), ("headdim", ctypes.c_int64),
+                ("dstate", ctypes.c_int64), ("ngroups", ctypes.c_int64),
+                ("chunk_len", ctypes.c_int64), ("flags", ctypes.c_uint32),
+                ("reserved", ctypes.c_uint32)]
+
+
+class SsdError(RuntimeError):
+    def __init__(self, code: int, detail: str):
+        super().__init__(f"{STATUS.get(code, code)}: {detail}")
+        self.code = code
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def load_library(path: str | None = None):
+    """Open libssd.so (once).  Raises if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is not None and path is None:
+            return _lib
+        p = path or LIB_PATH
+        if not os.path.exists(p):
+            raise RuntimeError(f"{p} is missing: build it with "
+                               "`python -m state_space_model_mamba_gb300.build`")
+        import torch.cuda  # noqa: F401  (makes the CUDA runtime PyTorch uses resident first)
+        lib = ctypes.CDLL(p)
+        vp, sz, i32 = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int
+        dims_p = ctypes.POINTER(SsdDims)
+        lib.ssd_supported.argtypes = [dims_p, i32]
+        lib.ssd_supported.restype = i32
+        lib.ssd_workspace_bytes.argtypes = [dims_p, i32, i32]
+        lib.ssd_workspace_bytes.restype = sz
+        lib.ssd_forward.argtypes = [dims_p, i32] + [vp] * 10 + [vp, sz, vp]
+        lib.ssd_forward.restype = i32
+        lib.ssd_backward.argtypes = [dims_p, i32] + [vp] * 17 + [vp, sz, vp]
+        lib.ssd_backward.restype = i32
+        lib.ssd_workspace_status.argtypes = [vp, sz, vp]
+        lib.ssd_workspace_status.restype = i32
+        lib.ssd_status_str.argtypes = [i32]
+        lib.ssd_status_str.restype = ctypes.c_char_p
+        lib.ssd_last_error.restype = ctypes.c_char_p
+        lib.ssd_version.restype = i32
+        if path is None:
+            _lib = lib
+        return lib
+
+
+def _check(code: int):
+    if code != 0:
+        raise SsdError(code, load_library().ssd_last_error().decode())
+
+
+@dataclass(frozen=True)
+class Dims:
+    batch: int
+    seqlen: int
+    nheads: int
+    headdim: int
+    dstate: int
+    ngroups: int
+    chunk_len: int
+    simt: bool = False
+
+    def c(self) -> SsdDims:
+        return SsdDims(self.batch, self.seqlen, self.nheads, self.headdim, self.dstate,
+                       self.ngroups, self.chunk_len, SSD_FLAG_SIMT if self.simt else 0, 0)
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.float32:
+        return SSD_F32
+    if t.dtype == torch.bfloat16:
+        return SSD_BF16
+    raise TypeError(f"x must be float32 or bfloat16, got {t.dtype}")
+
+
+def dims_of(x: torch.Tensor, B: torch.Tensor, chunk_len: int, simt: bool = False) -> Dims:
+    b, L, H, P = x.shape
+    G, N = B.shape[2], B.shape[3]
+    return Dims(b, L, H, P, N, G, int(chunk_len), simt)
+
+
+def supported(dims: Dims, dtype_code: int) -> bool:
+    return load_library().ssd_supported(ctypes.byref(dims.c()), dtype_code) == 0
+
+
+def workspace_bytes(dims: Dims, dtype_code: int, backward: bool) -> int:
+    n = load_library().ssd_workspace_bytes(ctypes.byref(dims.c()), dtype_code, int(backward))
+    if n == 0:
+        _check(load_library().ssd_supported(ctypes.byref(dims.c()), dtype_code) or 1)
+    return int(n)
+
+
+def alloc_workspace(dims: Dims, dtype_code: int, backward: bool, device) -> torch.Tensor:
+    return torch.empty(workspace_bytes(dims, dtype_code, backward), dtype=torch.uint8, device=device)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream_ptr(device) -> ctypes.c_void_p:
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+def _check_inputs(x, dt, A, B, C, D, init_state, valid_len, T):
+    b, L, H, P = x.shape
+    G, N = B.shape[2], B.shape[3]
+    exp = {"dt": (dt, (b, H, L), torch.float32), "A": (A, (H,), torch.float32),
+           "B": (B, (b, L, G, N), T), "C": (C, (b, L, G, N), T), "D": (D, (H,), torch.float32)}
+    if init_state is not None:
+        exp["init_state"] = (init_state, (b, H, P, N), torch.float32)
+    for name, (t, shape, dtype) in exp.items():
+        if tuple(t.shape) != shape or t.dtype != dtype:
+            raise ValueError(f"{name}: expected {shape} {dtype}, got {tuple(t.shape)} {t.dtype}")
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CUDA tensor")
+    if not x.is_cuda or not x.is_contiguous():
+        raise ValueError("x must be a contiguous CUDA tensor")
+    if valid_len is not None and (valid_len.dtype != torch.int32 or tuple(valid_len.shape) != (b,)
+                                  or not valid_len.is_cuda):
+        raise ValueError("valid_len must be a CUDA int32 tensor of shape [batch]")
+
+
+def forward_into(dims: Dims, x, dt, A, B, C, D, init_state, valid_len, y, final_state,
+                 workspace: torch.Tensor):
+    """ssd_forward on caller-provided outputs and workspace (no allocation)."""
+    code = _dtype_code(x)
+    _check(load_library().ssd_forward(
+        ctypes.byref(dims.c()), code, _ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C), _ptr(D),
+        _ptr(init_state), _ptr(valid_len), _ptr(y), _ptr(final_state), _ptr(workspace),
+        workspace.numel(), _stream_ptr(x.device)))
+
+
+def backward_into(dims: Dims, x, dt, A, B, C, D, init_state, valid_len, dy, d_final, dx, ddt,
+                  dA, dB, dC, dD, d_init, workspace: torch.Tensor):
+    """ssd_backward on caller-provided gradients and workspace (no allocation)."""
+    code = _dtype_code(x)
+    _check(load_library().ssd_backward(
+        ctypes.byref(dims.c()), code, _ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C), _ptr(D),
+        _ptr(init_state), _ptr(valid_len), _ptr(dy), _ptr(d_final), _ptr(dx), _ptr(ddt), _ptr(dA),
+        _ptr(dB), _ptr(dC), _ptr(dD), _ptr(d_init), _ptr(workspace), workspace.numel(),
+        _stream_ptr(x.device)))
+
+
+def ssd_forward(x, dt, A, B, C, D, chunk_len, init_state=None, valid_len=None,
+                return_final_state=True, simt=False):
+    """Forward of the chunked selective scan.  Returns ``(y, final_state)``.
+
+    x [b,L,H,P] (fp32 or bf16), dt [b,H,L] fp32, A [H] fp32, B/C [b,L,G,N]
+    (x's dtype), D [H] fp32, init_state [b,H,P,N] fp32 or None,
+    valid_len int32 [b] or None.
+    """
+    _check_inputs(x, dt, A, B, C, D, init_state, valid_len, x.dtype)
+    dims = dims_of(x, B, chunk_len, simt)
+    code = _dtype_code(x)
+    y = torch.empty_like(x)
+    fin = (torch.empty(x.shape[0], x.shape[2], x.shape[3], B.shape[3], device=x.device,
+                       dtype=torch.float32) if return_final_state else None)
+    ws = alloc_workspace(dims, code, False, x.device)
+    forward_into(dims, x, dt, A, B, C, D, init_state, valid_len, y, fin, ws)
+    return y, fin
+
+
+def ssd_backward(x, dt, A, B, C, D, chunk_len, dy, d_final_state=None, init_state=None,
+                 valid_len=None, want_d_init=True, simt=False):
+    """Recompute backward.  Returns a dict with dx, ddt, dA, dB, dC, dD, d_init."""
+    _check_inputs(x, dt, A, B, C, D, init_state, valid_len, x.dtype)
+    if tuple(dy.shape) != tuple(x.shape) or dy.dtype != x.dtype or not dy.is_contiguous():
+        raise ValueError("dy must match x in shape and dtype and be contiguous")
+    dims = dims_of(x, B, chunk_len, simt)
+    code = _dtype_code(x)
+    b, L, H, P = x.shape
+    N = B.shape[3]
+    dev = x.device
+    out = dict(dx=torch.empty_like(x), ddt=torch.empty_like(dt), dA=torch.empty_like(A),
+               dB=torch.empty_like(B), dC=torch.empty_like(C), dD=torch.empty_like(D),
+               d_init=(torch.empty(b, H, P, N, device=dev, dtype=torch.float32)
+                       if want_d_init else None))
+    ws = alloc_workspace(dims, code, True, dev)
+    backward_into(dims, x, dt, A, B, C, D, init_state, valid_len, dy, d_final_state, out["dx"],
+                  out["ddt"], out["dA"], out["dB"], out["dC"], out["dD"], out["d_init"], ws)
+    return out
+
+
+def workspace_status(workspace: torch.Tensor) -> None:
+    """Raise if the last call on ``workspace`` recorded a device-side timeout."""
+    _check(load_library().ssd_workspace_status(_ptr(workspace), workspace.numel(),
+                                               _stream_ptr(workspace.device)))

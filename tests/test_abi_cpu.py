@@ -1,0 +1,116 @@
+"""Host-side checks of the C ABI (no GPU): the library loads, exports every
+function that include/ssd.h declares, sizes workspaces, and rejects bad
+arguments before enqueuing any device work."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from state_space_model_mamba_gb300 import build as ssd_build
+from state_space_model_mamba_gb300 import ssd
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    ssd_build.build()
+    return ssd.load_library()
+
+
+def declared_functions():
+    names = []
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", fn)).read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            names += re.findall(r"\b(ssd_[a-z_]+)\s*\(", text)
+    return sorted(set(names))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert len(names) >= 8
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in include/ but not exported"
+    assert set(ssd.EXPORTED) <= set(names)
+
+
+def test_version_and_status_strings(lib):
+    assert lib.ssd_version() >= 10000
+    for code in range(6):
+        assert lib.ssd_status_str(code)
+    assert lib.ssd_status_str(99) == b"unknown status"
+
+
+def _dims(**kw):
+    base = dict(batch=2, seqlen=8192, nheads=80, headdim=64, dstate=128, ngroups=1, chunk_len=256)
+    base.update(kw)
+    return ssd.SsdDims(base["batch"], base["seqlen"], base["nheads"], base["headdim"],
+                       base["dstate"], base["ngroups"], base["chunk_len"],
+                       base.get("flags", 0), base.get("reserved", 0))
+
+
+def test_workspace_sizes(lib):
+    d = _dims()
+    f = lib.ssd_workspace_bytes(ctypes.byref(d), ssd.SSD_BF16, 0)
+    b = lib.ssd_workspace_bytes(ctypes.byref(d), ssd.SSD_BF16, 1)
+    states = 2 * 32 * 80 * 64 * 128 * 4
+    assert f >= states and b >= 2 * states and b > f
+    assert lib.ssd_workspace_bytes(ctypes.byref(_dims(ngroups=3)), ssd.SSD_BF16, 0) == 0
+    # ragged sequence length rounds the chunk count up
+    r = lib.ssd_workspace_bytes(ctypes.byref(_dims(seqlen=8193)), ssd.SSD_BF16, 0)
+    assert r > f
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(ngroups=3), ssd.SSD_BF16 and 1),
+    (dict(chunk_len=100), 2),
+    (dict(chunk_len=512), 2),
+    (dict(headdim=130), 2),
+    (dict(dstate=6), 2),
+    (dict(batch=0), 1),
+    (dict(reserved=1), 1),
+    (dict(flags=8), 1),
+])
+def test_supported_rejects(lib, kw, code):
+    assert lib.ssd_supported(ctypes.byref(_dims(**kw)), ssd.SSD_BF16) == code
+    assert lib.ssd_last_error()
+
+
+def test_supported_accepts_workloads(lib):
+    from state_space_model_mamba_gb300.inputs import WORKLOADS
+    for w in WORKLOADS.values():
+        d = _dims(**w.dims())
+        assert lib.ssd_supported(ctypes.byref(d), 0 if w.dtype == "f32" else 1) == 0
+
+
+def test_calls_reject_bad_arguments_before_launch(lib):
+    d = _dims(batch=1, seqlen=64, nheads=2, headdim=8, dstate=8, chunk_len=16)
+    fake = ctypes.c_void_p(0x10000)  # never dereferenced: validation fails first
+    args = [fake] * 10
+    # NULL x
+    rc = lib.ssd_forward(ctypes.byref(d), 0, None, *args[1:], fake, 1 << 20, None)
+    assert rc == 1 and b"x is NULL" in lib.ssd_last_error()
+    # misaligned B
+    bad = ctypes.c_void_p(0x10004)
+    rc = lib.ssd_forward(ctypes.byref(d), 0, fake, fake, fake, bad, fake, fake, None, None, fake,
+                         None, fake, 1 << 20, None)
+    assert rc == 1 and b"aligned" in lib.ssd_last_error()
+    # workspace too small
+    rc = lib.ssd_forward(ctypes.byref(d), 0, fake, fake, fake, fake, fake, fake, None, None, fake,
+                         None, fake, 16, None)
+    assert rc == 3
+    # backward: NULL dB
+    rc = lib.ssd_backward(ctypes.byref(d), 0, fake, fake, fake, fake, fake, fake, None, None, fake,
+                          None, fake, fake, fake, None, fake, fake, None, fake, 1 << 30, None)
+    assert rc == 1 and b"dB is NULL" in lib.ssd_last_error()
+    # bad dtype
+    rc = lib.ssd_forward(ctypes.byref(d), 7, *([fake] * 6), None, None, fake, None, fake, 1 << 20, None)
+    assert rc == 1
+
+
+def test_binding_fails_loudly_without_library(tmp_path):
+    with pytest.raises(RuntimeError, match="missing"):
+        ssd.load_library(str(tmp_path / "nope.so"))
