@@ -1,0 +1,472 @@
+#!/usr/bin/env python
+"""Benchmark of the SSD chunked selective scan: forward + backward tokens/s.
+
+One step = ssd_forward + ssd_backward (the backward recomputes every forward
+intermediate) over one batch of the Mamba-2 2.7B-layer shape (batch 2,
+seqlen 8192, nheads 80, headdim 64, dstate 128, ngroups 1, chunk 256; bf16
+x/B/C/dy, fp32 dt/A/D), synthetic seeded inputs resident in HBM.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line (rank 0).  Under torchrun (N > 1) every rank runs an
+independent replica of the workload (the scan has no data-path exchange) and
+`value` is the tokens all ranks processed divided by the slowest rank's time.
+`--impl reference` times the CPU oracle (plain fp64 recurrence) on the host
+cores on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import glob
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+from state_space_model_mamba_gb300.inputs import WORKLOADS, generate  # noqa: E402
+
+METRIC = "SSD fwd+bwd tokens/sec (2.7B-layer shape, 1 GB300); % of tensor/HBM roofline"
+UNIT = "tokens/s"
+DEFAULT_WORKLOAD = "mamba2_2p7b"
+L2_BYTES = 129 * 1024 * 1024
+PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+# ----------------------------------------------------------------------------- helpers
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    return int(os.environ.get("RANK", "0")), ws, int(os.environ.get("LOCAL_RANK", "0"))
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(PEAKS_FALLBACK), "fallback"
+
+
+def kernel_costs(w, tc: bool) -> dict:
+    """Algorithmic work of each kernel per launch: (flops, bytes).  Flops count
+    the causal half of the Q x Q blocks; bytes count every input read once and
+    every output written once."""
+    b, L, H, P, N, G, Q = w.batch, w.seqlen, w.nheads, w.headdim, w.dstate, w.ngroups, w.chunk_len
+    n = -(-L // Q)
+    Lp = n * Q
+    s = 2 if w.dtype == "bf16" else 4
+    st = b * n * H * P * N                       # chunk-state elements
+    tri = Q * (Q + 1) // 2                       # causal pairs per chunk
+    tok_h = b * H * L
+    x_b = s * b * L * H * P                      # one [b,L,H,P] tensor
+    bc_b = s * b * L * G * N                     # one [b,L,G,N] tensor
+    cum_b = 4 * b * H * Lp
+    stb = 4 * st + (2 * st if tc else 0)         # fp32 state (+ bf16 operand copy)
+    c = {
+        "k1_chunk_cumsum": (0.0, 4 * tok_h + cum_b + 4 * b * H * n),
+        "k2_cb": (2.0 * b * n * G * tri * N, 2 * bc_b + 4 * b * n * G * tri),
+        "k3_state": (2.0 * b * n * H * Q * P * N, x_b + bc_b + 4 * tok_h + cum_b + 4 * st),
+        "k4_state_passing": (2.0 * st, 4 * st + stb),
+        "k5_scan": (b * n * H * (2.0 * Q * P * N + 2.0 * tri * P),
+                    2 * x_b + bc_b + 4 * b * n * G * tri + (2 if tc else 4) * st + cum_b + 4 * tok_h),
+        "bwd_blue": (b * n * H * 4.0 * Q * P * N, x_b + bc_b + (2 if tc else 4) * st + 4 * st + 2 * cum_b),
+        "bwd_k4_state_passing": (4.0 * st, 8 * st + stb),
+        "bwd_main": (b * n * H * (4.0 * tri * P + 2.0 * Q * P * N),
+                     3 * x_b + bc_b + 4 * b * n * G * tri + (2 if tc else 4) * st + 6 * cum_b),
+        "bwd_group": (b * n * G * 4.0 * tri * N + b * n * H * 4.0 * Q * P * N,
+                      2 * x_b + 2 * (2 if tc else 4) * st + 4 * bc_b + 2 * cum_b),
+        "bwd_k1_chunk_cumsum": (0.0, 4 * cum_b + 8 * tok_h),
+        "bwd_finalize": (0.0, 4 * b * H * n * 2),
+    }
+    return c
+
+
+def cost_key(name: str) -> str:
+    for suffix in ("_simt", "_tc"):
+        if name.endswith(suffix):
+            return name[: -len(suffix)]
+    return name
+
+
+def source_digest() -> str:
+    h = hashlib.sha256()
+    for f in sorted(glob.glob(os.path.join(ROOT, "state_space_model_mamba_gb300", "csrc", "*"))):
+        with open(f, "rb") as fh:
+            h.update(os.path.basename(f).encode())
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(kernel: str, workload: str):
+    """Per-launch DRAM bytes of `kernel` from the committed ncu summary, if it
+    was taken on the current kernel sources."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    e = d.get(workload, {}).get(kernel)
+    if not e or e.get("source_digest") != source_digest():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled during the timed region."""
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"ssd_clocks_{os.getpid()}.csv")
+
+    def __enter__(self):
+        try:
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-i", str(self.index), "-lms", "50"], stdout=self.fh, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.1)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.fh.close()
+        return False
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) >= 10:
+                    rows.append(parts)
+        os.unlink(self.path)
+        sm = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        mx = [float(r[3]) for r in rows if r[3].replace(".", "").isdigit()]
+        pw = [float(r[4]) for r in rows if r[4].replace(".", "").isdigit()]
+        reasons = set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for r in rows:
+            for nm, v in zip(names, r[6:10]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        load = sorted(sm)[len(sm) // 4:] if len(sm) >= 4 else sm  # drop the idle ramp samples
+        return {"sm_mhz": statistics.median(load) if load else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "power_w_max": max(pw) if pw else None,
+                "samples": len(rows), "reasons": sorted(reasons)}
+
+
+# ----------------------------------------------------------------------------- CPU oracle
+def oracle_sample(inp, w, heads: int, seqlen: int):
+    """Run the oracle forward + backward on batch 0, the first `heads` heads and
+    the first `seqlen` tokens.  Returns (seconds, head_tokens, threads)."""
+    import oracle
+    G = w.ngroups
+    hpg = w.nheads // G
+    heads = max(1, min(heads, w.nheads))
+    hsel = slice(0, heads)
+    gcount = -(-heads // hpg)
+    sub = dict(
+        x=inp["x"][:1, :seqlen, hsel], dt=inp["dt"][:1, hsel, :seqlen], A=inp["A"][hsel],
+        B=inp["B"][:1, :seqlen, :gcount], C=inp["C"][:1, :seqlen, :gcount], D=inp["D"][hsel],
+        init=None if inp["init"] is None else inp["init"][:1, hsel],
+        dy=inp["dy"][:1, :seqlen, hsel],
+        d_final=None if inp["d_final"] is None else inp["d_final"][:1, hsel])
+    if heads % hpg != 0 or gcount * hpg != heads:
+        # keep whole groups: use one group per head for the sample
+        sub["B"] = np.repeat(sub["B"][:, :, :1], heads, axis=2)
+        sub["C"] = np.repeat(sub["C"][:, :, :1], heads, axis=2)
+    vl = None
+    if inp["valid_len"] is not None:
+        vl = np.minimum(inp["valid_len"][:1], seqlen).astype(np.int32)
+    t0 = time.perf_counter()
+    oracle.forward(sub["x"], sub["dt"], sub["A"], sub["B"], sub["C"], sub["D"], sub["init"], vl)
+    oracle.backward(sub["x"], sub["dt"], sub["A"], sub["B"], sub["C"], sub["D"], sub["init"], vl,
+                    sub["dy"], sub["d_final"])
+    dt = time.perf_counter() - t0
+    return dt, heads * seqlen, oracle.num_threads()
+
+
+def cpu_baseline(inp, w, target_s: float = 15.0):
+    """Time the oracle on a bounded sample of about `target_s` seconds: the
+    first heads of batch 0 over the whole sequence, repeated until the time is
+    reached (one repetition when the sample alone is that long)."""
+    import oracle
+    cores = oracle.num_threads()
+    heads = min(w.nheads, max(2 * cores, 1))
+    probe_len = min(w.seqlen, 512)
+    t, ht, thr = oracle_sample(inp, w, heads, probe_len)
+    rate = ht / max(t, 1e-9)                                   # head-tokens / s
+    seqlen = int(min(w.seqlen, max(probe_len, rate * target_s / heads)))
+    tot, reps, done = 0.0, 0, 0
+    while tot < 0.8 * target_s or reps == 0:
+        t, ht, thr = oracle_sample(inp, w, heads, seqlen)
+        tot += t
+        reps += 1
+        done += ht
+    value = done / tot / w.nheads                              # tokens/s of the full-head workload
+    return {"value": value, "unit": UNIT, "cores": thr, "kind": "oracle",
+            "sample": f"fp64 serial recurrence fwd+bwd on batch 0, heads 0..{heads - 1} of "
+                      f"{w.nheads}, first {seqlen} of {w.seqlen} tokens, {reps} repetition(s), "
+                      f"{tot:.1f} s; scaled to tokens/s of all {w.nheads} heads"}
+
+
+# ----------------------------------------------------------------------------- arms
+def run_reference(args, w, rank, world):
+    if rank != 0:
+        return None
+    inp = generate(w)
+    import oracle
+    cores = oracle.num_threads()
+    heads = min(w.nheads, cores)
+    total_steps = args.steps + args.warmup
+    budget = 120.0 / max(total_steps, 1)                       # seconds per step
+    t, ht, _ = oracle_sample(inp, w, heads, min(w.seqlen, 256))
+    rate = ht / max(t, 1e-9)
+    seqlen = int(min(w.seqlen, max(64, rate * budget / heads)))
+    for _ in range(args.warmup):
+        oracle_sample(inp, w, heads, seqlen)
+    times = []
+    for _ in range(args.steps):
+        t, ht, thr = oracle_sample(inp, w, heads, seqlen)
+        times.append(t)
+    tot = sum(times)
+    value = ht * args.steps / tot / w.nheads
+    sample = (f"each step: fp64 oracle fwd+bwd on batch 0, heads 0..{heads - 1} of {w.nheads}, "
+              f"first {seqlen} of {w.seqlen} tokens; value scaled to tokens/s of all heads")
+    return {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * tot / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, **w.dims()},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": thr, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def run_ours(args, w, rank, world, local_rank):
+    import torch
+    import torch.distributed as dist
+
+    from state_space_model_mamba_gb300 import ssd
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    inp = generate(w)
+    bf = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+
+    def up(a, dt=torch.float32):
+        return None if a is None else torch.from_numpy(np.ascontiguousarray(a)).to(dev, dt)
+
+    x, B, C, dy = up(inp["x"], bf), up(inp["B"], bf), up(inp["C"], bf), up(inp["dy"], bf)
+    dt, A, D = up(inp["dt"]), up(inp["A"]), up(inp["D"])
+    init, dfin = up(inp["init"]), up(inp["d_final"])
+    vl = None if inp["valid_len"] is None else torch.from_numpy(inp["valid_len"]).to(dev)
+    dims = ssd.dims_of(x, B, w.chunk_len)
+    code = ssd.SSD_BF16 if w.dtype == "bf16" else ssd.SSD_F32
+    ws = torch.empty(max(ssd.workspace_bytes(dims, code, True),
+                         ssd.workspace_bytes(dims, code, False)), dtype=torch.uint8, device=dev)
+    y = torch.empty_like(x)
+    fin = torch.empty(w.batch, w.nheads, w.headdim, w.dstate, device=dev)
+    g = dict(dx=torch.empty_like(x), ddt=torch.empty_like(dt), dA=torch.empty_like(A),
+             dB=torch.empty_like(B), dC=torch.empty_like(C), dD=torch.empty_like(D),
+             d_init=torch.empty_like(fin))
+
+    def step():
+        ssd.forward_into(dims, x, dt, A, B, C, D, init, vl, y, fin, ws)
+        n1 = ssd.last_launch_count()
+        ssd.backward_into(dims, x, dt, A, B, C, D, init, vl, dy, dfin, g["dx"], g["ddt"], g["dA"],
+                          g["dB"], g["dC"], g["dD"], g["d_init"], ws)
+        return n1 + ssd.last_launch_count()
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    for _ in range(args.warmup):
+        launches_per_step = step()
+    # launch sequence of one step (names of the timed kernel units)
+    probe = ssd.KernelTimer(capacity_kernels=64)
+    with probe:
+        step()
+    pattern = [nm for nm, _ in probe.durations()]
+    torch.cuda.synchronize()
+    ssd.workspace_status(ws)
+
+    # ---------------- timed region (device time, CUDA events on the launching stream)
+    stream = torch.cuda.current_stream(dev)
+    timer = ssd.KernelTimer(capacity_kernels=len(pattern) * args.steps + 8)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local_rank)
+    barrier()
+    torch.cuda.synchronize()
+    with clocks:
+        ev0.record(stream)
+        with timer:
+            for _ in range(args.steps):
+                step()
+        ev1.record(stream)
+        torch.cuda.synchronize()
+    barrier()
+    ms_total = ev0.elapsed_time(ev1)
+    if world > 1:
+        tt = torch.tensor([ms_total], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms_total = float(tt.item())
+    ms_step = ms_total / args.steps
+    value = w.tokens * world / (ms_step * 1e-3)
+    ssd.workspace_status(ws)
+
+    # per-kernel live durations
+    per = {}
+    for name, ms in timer.durations(pattern):
+        per.setdefault(name, []).append(ms)
+    tot_k = sum(sum(v) for v in per.values())
+    shares = {k: {"launches": len(v), "avg_us": 1e3 * sum(v) / len(v),
+                  "share": sum(v) / tot_k if tot_k else None} for k, v in per.items()}
+    top = max(per, key=lambda k: sum(per[k]))
+    peaks, peak_src = load_peaks()
+    costs = kernel_costs(w, tc=not top.endswith("_simt"))
+    flops, byts = costs[cost_key(top)]
+    avg_s = statistics.mean(per[top]) * 1e-3
+    ridge = peaks["bf16_tflops_sustained"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
+    if top.endswith("_simt") and flops > 0:
+        sm_mhz = peaks.get("sm_max_mhz", 2070.0)
+        alu_peak = 152 * 128 * 2 * sm_mhz * 1e6 / 1e12              # fp32 FFMA TFLOP/s
+        roof = {"bound": "alu", "achieved": flops / avg_s / 1e12, "peak": alu_peak,
+                "unit": "TFLOP/s"}
+    elif flops > 0 and flops / max(byts, 1) > ridge:
+        roof = {"bound": "tensor", "achieved": flops / avg_s / 1e12,
+                "peak": peaks["bf16_tflops_sustained"], "unit": "TFLOP/s"}
+    else:
+        roof = {"bound": "hbm", "achieved": byts / avg_s / 1e9, "peak": peaks["hbm_gbs"],
+                "unit": "GB/s"}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["kernel"] = top
+    roof["peak_source"] = f"{peak_src} (MEASURED_PEAKS.json)" if peak_src == "measured" else "fallback"
+    roof["algorithmic_flops_per_launch"] = flops
+    roof["algorithmic_bytes_per_launch"] = byts
+    roof["traffic"] = ncu_traffic(top, w.name)
+
+    # ---------------- end to end: pinned host buffers -> device -> host every step
+    host_in = {k: torch.from_numpy(np.ascontiguousarray(inp[k])).to(
+        dtype=(bf if k in ("x", "B", "C", "dy") else torch.float32)).pin_memory()
+        for k in ("x", "dt", "A", "B", "C", "D", "dy")}
+    if inp["init"] is not None:
+        host_in["init"] = torch.from_numpy(inp["init"]).pin_memory()
+    if inp["d_final"] is not None:
+        host_in["d_final"] = torch.from_numpy(inp["d_final"]).pin_memory()
+    dev_in = {"x": x, "dt": dt, "A": A, "B": B, "C": C, "D": D, "dy": dy, "init": init,
+              "d_final": dfin}
+    outs = {"y": y, "final_state": fin, **g}
+    host_out = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in outs.items()}
+    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+    d2h = sum(t.numel() * t.element_size() for t in host_out.values())
+    e2e_steps = max(3, min(args.steps, 20))
+
+    def e2e_step():
+        for k, t in host_in.items():
+            dev_in[k].copy_(t, non_blocking=True)
+        step()
+        for k, t in outs.items():
+            host_out[k].copy_(t, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    if world > 1:
+        tt = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        e2e_ms = float(tt.item())
+
+    if rank != 0:
+        return None
+    in_bytes = sum(t.numel() * t.element_size() for t in (x, dt, A, B, C, D, dy))
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+        "config": {"workload": w.name, **w.dims(),
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "l2": f"inputs larger than L2 ({in_bytes / 1e6:.0f} MB > {L2_BYTES / 1e6:.0f} MB); no flush",
+                   "step": "ssd_forward + ssd_backward (recompute), inputs resident in HBM"},
+        "roofline": roof,
+        "kernels": {k: {kk: (round(vv, 4) if isinstance(vv, float) else vv) for kk, vv in s.items()}
+                    for k, s in sorted(shares.items(), key=lambda kv: -kv[1]["share"])},
+        "e2e": {"value": w.tokens * world / (e2e_ms * 1e-3), "unit": UNIT,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": e2e_ms, "steps": e2e_steps},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clocks.summary(),
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(inp, w, args.cpu_seconds)
+    return line
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    rank, world, local_rank = dist_env()
+    w = WORKLOADS[args.workload]
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        backend = "nccl" if args.impl == "ours" else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local_rank)
+        dist.init_process_group(backend=backend)
+    if args.impl == "reference":
+        line = run_reference(args, w, rank, world)
+    else:
+        line = run_ours(args, w, rank, world, local_rank)
+    if rank == 0 and line is not None:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

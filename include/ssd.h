@@ -122,6 +122,24 @@ ssd_status ssd_backward(const ssd_dims *dims, ssd_dtype dtype,
  * call on this workspace left: SSD_OK or SSD_ERR_TIMEOUT. */
 ssd_status ssd_workspace_status(const void *workspace, size_t workspace_bytes, void *stream);
 
+/* ---- Diagnostics (no counterpart on the pages; used by the benchmark) ----
+ *
+ * ssd_last_launch_count: number of kernels the most recent ssd_forward /
+ * ssd_backward call on the calling host thread enqueued.
+ *
+ * ssd_profile_begin / ssd_profile_end: while active on the calling host
+ * thread, every kernel the library enqueues is bracketed by two
+ * cudaEventRecord calls on the call's stream, taken in order from `events`
+ * (an array of `capacity` cudaEvent_t created by the caller); recording stops
+ * silently when the array is full.  ssd_profile_end deactivates it and
+ * returns how many events were recorded (2 per kernel); ssd_profile_name(i)
+ * names the i-th recorded kernel (i < 4096).  Timing events add no device
+ * work besides the records themselves. */
+int ssd_last_launch_count(void);
+ssd_status ssd_profile_begin(void **events, int capacity);
+int ssd_profile_end(void);
+const char *ssd_profile_name(int i);
+
 /* Static description of a status code. */
 const char *ssd_status_str(ssd_status status);
 

@@ -25,6 +25,29 @@ ssd_status fail(ssd_status st, const char *fmt, ...) {
     return st;
 }
 
+// Diagnostics: kernels enqueued by the current call, and optional CUDA-event
+// pairs recorded around every launch (ssd_profile_begin / ssd_profile_end).
+thread_local int g_launches = 0;
+struct Recorder {
+    cudaEvent_t *ev = nullptr;  // 2 events per kernel: start, end
+    int cap = 0;                // capacity in events
+    int n = 0;                  // events recorded
+    const char *names[4096];
+};
+thread_local Recorder g_rec;
+
+cudaError_t mark_start(const char *name, cudaStream_t s) {
+    ++g_launches;
+    if (!g_rec.ev || g_rec.n + 2 > g_rec.cap) return cudaSuccess;
+    g_rec.names[(g_rec.n / 2) % 4096] = name;
+    return cudaEventRecord(g_rec.ev[g_rec.n++], s);
+}
+
+cudaError_t mark_end(cudaStream_t s) {
+    if (!g_rec.ev || (g_rec.n & 1) == 0) return cudaSuccess;
+    return cudaEventRecord(g_rec.ev[g_rec.n++], s);
+}
+
 constexpr size_t kAlign = 256;
 size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
 
@@ -150,17 +173,25 @@ Params base_params(const ssd_dims &d, const Layout &lo, void *ws) {
             return fail(SSD_ERR_CUDA, "%s: %s", #expr, cudaGetErrorString(e_));          \
     } while (0)
 
+#define SSD_LAUNCH(name, expr, nk)                                                        \
+    do {                                                                                  \
+        SSD_TRY(mark_start(name, s));                                                     \
+        g_launches += (nk) - 1;                                                           \
+        SSD_TRY(expr);                                                                    \
+        SSD_TRY(mark_end(s));                                                             \
+    } while (0)
+
 template <typename T>
 ssd_status run_forward_chain(const Params &p, bool tc, bool write_final, cudaStream_t s) {
-    SSD_TRY(launch_k1_cumsum(p, s));
+    SSD_LAUNCH("k1_chunk_cumsum", launch_k1_cumsum(p, s), 1);
     if (tc) {
-        SSD_TRY(launch_tc_k2(p, s));
-        SSD_TRY(launch_tc_k3(p, s));
+        SSD_LAUNCH("k2_cb_tc", launch_tc_k2(p, s), 1);
+        SSD_LAUNCH("k3_state_tc", launch_tc_k3(p, s), 1);
     } else {
-        SSD_TRY(launch_simt_k2<T>(p, s));
-        SSD_TRY(launch_simt_k3<T>(p, s));
+        SSD_LAUNCH("k2_cb_simt", launch_simt_k2<T>(p, s), 1);
+        SSD_LAUNCH("k3_state_simt", launch_simt_k3<T>(p, s), 1);
     }
-    SSD_TRY(launch_k4_state_passing(p, write_final, s));
+    SSD_LAUNCH("k4_state_passing", launch_k4_state_passing(p, write_final, s), 1);
     return SSD_OK;
 }
 
@@ -220,16 +251,17 @@ ssd_status ssd_forward(const ssd_dims *dims, ssd_dtype dtype, const void *x, con
     p.x = x; p.dt = dt; p.A = A; p.B = B; p.C = C; p.D = D; p.init = init_state;
     p.valid_len = valid_len; p.y = y; p.final_state = final_state;
     cudaStream_t s = (cudaStream_t)stream;
+    g_launches = 0;
     SSD_TRY(cudaMemsetAsync(p.status, 0, sizeof(int), s));
     if (dtype == SSD_F32) {
         st = run_forward_chain<float>(p, false, true, s);
         if (st != SSD_OK) return st;
-        SSD_TRY(launch_simt_k5<float>(p, s));
+        SSD_LAUNCH("k5_scan_simt", launch_simt_k5<float>(p, s), 1);
     } else {
         st = run_forward_chain<bf16>(p, tc, true, s);
         if (st != SSD_OK) return st;
-        if (tc) SSD_TRY(launch_tc_k5(p, s));
-        else SSD_TRY(launch_simt_k5<bf16>(p, s));
+        if (tc) SSD_LAUNCH("k5_scan_tc", launch_tc_k5(p, s), 1);
+        else SSD_LAUNCH("k5_scan_simt", launch_simt_k5<bf16>(p, s), 1);
     }
     return SSD_OK;
 }
@@ -262,32 +294,56 @@ ssd_status ssd_backward(const ssd_dims *dims, ssd_dtype dtype, const void *x, co
     p.valid_len = valid_len; p.dy = dy; p.d_final = d_final_state; p.dx = dx; p.ddt = ddt;
     p.dA = dA; p.dB = dB; p.dC = dC; p.dD = dD; p.d_init = d_init_state;
     cudaStream_t s = (cudaStream_t)stream;
+    g_launches = 0;
     SSD_TRY(cudaMemsetAsync(p.status, 0, sizeof(int), s));
     if (dtype == SSD_F32) {
         st = run_forward_chain<float>(p, false, false, s);
         if (st != SSD_OK) return st;
-        SSD_TRY(launch_simt_bwd_blue<float>(p, s));
-        SSD_TRY(launch_bwd_k4(p, s));
-        SSD_TRY(launch_simt_bwd_main<float>(p, s));
-        SSD_TRY(launch_simt_bwd_group<float>(p, s));
+        SSD_LAUNCH("bwd_blue_simt", launch_simt_bwd_blue<float>(p, s), 2);
+        SSD_LAUNCH("bwd_k4_state_passing", launch_bwd_k4(p, s), 1);
+        SSD_LAUNCH("bwd_main_simt", launch_simt_bwd_main<float>(p, s), 1);
+        SSD_LAUNCH("bwd_group_simt", launch_simt_bwd_group<float>(p, s), 2);
     } else {
         st = run_forward_chain<bf16>(p, tc, false, s);
         if (st != SSD_OK) return st;
         if (tc) {
-            SSD_TRY(launch_tc_bwd_blue(p, s));
-            SSD_TRY(launch_bwd_k4(p, s));
-            SSD_TRY(launch_tc_bwd_main(p, s));
-            SSD_TRY(launch_tc_bwd_group(p, s));
+            SSD_LAUNCH("bwd_blue_tc", launch_tc_bwd_blue(p, s), 1);
+            SSD_LAUNCH("bwd_k4_state_passing", launch_bwd_k4(p, s), 1);
+            SSD_LAUNCH("bwd_main_tc", launch_tc_bwd_main(p, s), 1);
+            SSD_LAUNCH("bwd_group_tc", launch_tc_bwd_group(p, s), 2);
         } else {
-            SSD_TRY(launch_simt_bwd_blue<bf16>(p, s));
-            SSD_TRY(launch_bwd_k4(p, s));
-            SSD_TRY(launch_simt_bwd_main<bf16>(p, s));
-            SSD_TRY(launch_simt_bwd_group<bf16>(p, s));
+            SSD_LAUNCH("bwd_blue_simt", launch_simt_bwd_blue<bf16>(p, s), 2);
+            SSD_LAUNCH("bwd_k4_state_passing", launch_bwd_k4(p, s), 1);
+            SSD_LAUNCH("bwd_main_simt", launch_simt_bwd_main<bf16>(p, s), 1);
+            SSD_LAUNCH("bwd_group_simt", launch_simt_bwd_group<bf16>(p, s), 2);
         }
     }
-    SSD_TRY(launch_bwd_k1(p, s));
-    SSD_TRY(launch_bwd_finalize(p, s));
+    SSD_LAUNCH("bwd_k1_chunk_cumsum", launch_bwd_k1(p, s), 1);
+    SSD_LAUNCH("bwd_finalize", launch_bwd_finalize(p, s), 1);
     return SSD_OK;
+}
+
+int ssd_last_launch_count(void) { return g_launches; }
+
+ssd_status ssd_profile_begin(void **events, int capacity) {
+    g_last_error[0] = 0;
+    if (!events || capacity < 2) return fail(SSD_ERR_INVALID_ARG, "need an array of >= 2 events");
+    g_rec.ev = (cudaEvent_t *)events;
+    g_rec.cap = capacity;
+    g_rec.n = 0;
+    return SSD_OK;
+}
+
+int ssd_profile_end(void) {
+    const int n = g_rec.n;
+    g_rec.ev = nullptr;
+    g_rec.cap = 0;
+    return n;
+}
+
+const char *ssd_profile_name(int i) {
+    if (i < 0 || i >= 4096) return "";
+    return g_rec.names[i];
 }
 
 ssd_status ssd_workspace_status(const void *workspace, size_t workspace_bytes, void *stream) {

@@ -24,7 +24,8 @@ SSD_FLAG_SIMT = 1
 STATUS = {0: "SSD_OK", 1: "SSD_ERR_INVALID_ARG", 2: "SSD_ERR_UNSUPPORTED",
           3: "SSD_ERR_WORKSPACE", 4: "SSD_ERR_CUDA", 5: "SSD_ERR_TIMEOUT"}
 EXPORTED = ("ssd_supported", "ssd_workspace_bytes", "ssd_forward", "ssd_backward",
-            "ssd_workspace_status", "ssd_status_str", "ssd_last_error", "ssd_version")
+            "ssd_workspace_status", "ssd_status_str", "ssd_last_error", "ssd_version",
+            "ssd_last_launch_count", "ssd_profile_begin", "ssd_profile_end", "ssd_profile_name")
 
 
 class SsdDims(ctypes.Structure):
@@ -73,6 +74,12 @@ def load_library(path: str | None = None):
         lib.ssd_status_str.restype = ctypes.c_char_p
         lib.ssd_last_error.restype = ctypes.c_char_p
         lib.ssd_version.restype = i32
+        lib.ssd_last_launch_count.restype = i32
+        lib.ssd_profile_begin.argtypes = [vp, i32]
+        lib.ssd_profile_begin.restype = i32
+        lib.ssd_profile_end.restype = i32
+        lib.ssd_profile_name.argtypes = [i32]
+        lib.ssd_profile_name.restype = ctypes.c_char_p
         if path is None:
             _lib = lib
         return lib
@@ -220,3 +227,49 @@ def workspace_status(workspace: torch.Tensor) -> None:
     """Raise if the last call on ``workspace`` recorded a device-side timeout."""
     _check(load_library().ssd_workspace_status(_ptr(workspace), workspace.numel(),
                                                _stream_ptr(workspace.device)))
+
+
+def last_launch_count() -> int:
+    """Kernels enqueued by the most recent forward/backward call on this thread."""
+    return int(load_library().ssd_last_launch_count())
+
+
+class KernelTimer:
+    """Records a CUDA-event pair around every kernel the library launches while
+    active (on the launching stream).  ``durations()`` returns a list of
+    (kernel name, milliseconds) in launch order after a synchronize."""
+
+    def __init__(self, capacity_kernels: int):
+        self.events = [torch.cuda.Event(enable_timing=True) for _ in range(2 * capacity_kernels)]
+        for e in self.events:
+            e.record()  # materialise the underlying cudaEvent_t
+        torch.cuda.synchronize()
+        self._arr = (ctypes.c_void_p * len(self.events))(*[e.cuda_event for e in self.events])
+        self.n = 0
+
+    def __enter__(self):
+        _check(load_library().ssd_profile_begin(self._arr, len(self.events)))
+        return self
+
+    def __exit__(self, *exc):
+        self.n = int(load_library().ssd_profile_end())
+        return False
+
+    def names(self, count: int) -> list:
+        lib = load_library()
+        return [lib.ssd_profile_name(i).decode() for i in range(min(count, 4096))]
+
+    def durations(self, pattern: list | None = None) -> list:
+        """(name, ms) per recorded kernel.  Names past the library's 4096-entry
+        name table are taken from ``pattern`` (the per-step launch sequence)."""
+        torch.cuda.synchronize()
+        k = self.n // 2
+        names = self.names(k)
+        out = []
+        for i in range(k):
+            if pattern:
+                nm = pattern[i % len(pattern)]
+            else:
+                nm = names[i] if i < len(names) else ""
+            out.append((nm, self.events[2 * i].elapsed_time(self.events[2 * i + 1])))
+        return out
