@@ -88,8 +88,8 @@ typedef struct {
 /* Shape support: returns SSD_OK when (dims, dtype) can run, else
  * SSD_ERR_INVALID_ARG / SSD_ERR_UNSUPPORTED.  Limits: headdim <= 128 and a
  * multiple of 4; dstate <= 256 and a multiple of 4.  The tcgen05 path of
- * SSD_BF16 needs chunk_len in {64, 128, 256}, headdim == 64 and dstate in
- * {64, 128}; other SSD_BF16 shapes run on the CUDA-core kernels. */
+ * SSD_BF16 covers chunk_len in {128, 256}, headdim == 64 and dstate == 128;
+ * other SSD_BF16 shapes run on the CUDA-core kernels. */
 ssd_status ssd_supported(const ssd_dims *dims, ssd_dtype dtype);
 
 /* Bytes of device workspace ssd_forward (backward = 0) or ssd_backward

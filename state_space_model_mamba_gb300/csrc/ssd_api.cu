@@ -55,7 +55,7 @@ struct Layout {
     size_t status, cumA, endA, CB, states, states_bf, dstates, dstates_bf;
     size_t dcum_blue, dcum_main, d_delta, ddt_main, d_endA_part, dD_part, dA_part, d_cb, dBC_part;
     size_t total;
-    int k4_nblk, dD_per, nslice;
+    int k4_nblk, dD_per, nslice, nslice_cb;
 };
 
 bool use_tensor_cores(const ssd_dims &d, ssd_dtype dt) {
@@ -73,6 +73,7 @@ Layout make_layout(const ssd_dims &d, ssd_dtype dt, bool backward) {
     lo.k4_nblk = (int)((P * N / 4 + kK4Threads - 1) / kK4Threads);
     lo.dD_per = tc ? tc_dD_per(d.chunk_len) : (int)(Q / kMainRows);
     lo.nslice = tc ? tc_group_slices(d) : 1;
+    lo.nslice_cb = tc ? tc_dcb_slices(d) : 1;
     size_t off = 0;
     auto take = [&](size_t bytes) { size_t o = off; off += align_up(bytes); return o; };
     lo.status = take(16);
@@ -91,7 +92,7 @@ Layout make_layout(const ssd_dims &d, ssd_dtype dt, bool backward) {
         lo.d_endA_part = take(4 * b * H * n * lo.k4_nblk);
         lo.dD_part = take(4 * b * n * H * lo.dD_per);
         lo.dA_part = take(4 * b * H * n);
-        lo.d_cb = tc ? 0 : take(4 * b * n * G * Q * Q);
+        lo.d_cb = take(4 * (size_t)lo.nslice_cb * b * n * G * Q * Q);
         lo.dBC_part = tc ? take(4 * (size_t)lo.nslice * 2 * b * n * G * Q * N) : 0;
     }
     lo.total = off;
@@ -157,12 +158,13 @@ Params base_params(const ssd_dims &d, const Layout &lo, void *ws) {
         p.d_endA_part = f(lo.d_endA_part);
         p.dD_part = f(lo.dD_part);
         p.dA_part = f(lo.dA_part);
-        p.d_cb = lo.d_cb ? f(lo.d_cb) : nullptr;
+        p.d_cb = f(lo.d_cb);
         p.dBC_part = lo.dBC_part ? f(lo.dBC_part) : nullptr;
     }
     p.k4_nblk = lo.k4_nblk;
     p.dD_per = lo.dD_per;
     p.nslice = lo.nslice;
+    p.nslice_cb = lo.nslice_cb;
     return p;
 }
 
@@ -310,7 +312,7 @@ ssd_status ssd_backward(const ssd_dims *dims, ssd_dtype dtype, const void *x, co
             SSD_LAUNCH("bwd_blue_tc", launch_tc_bwd_blue(p, s), 1);
             SSD_LAUNCH("bwd_k4_state_passing", launch_bwd_k4(p, s), 1);
             SSD_LAUNCH("bwd_main_tc", launch_tc_bwd_main(p, s), 1);
-            SSD_LAUNCH("bwd_group_tc", launch_tc_bwd_group(p, s), 2);
+            SSD_LAUNCH("bwd_group_tc", launch_tc_bwd_group(p, s), 3);
         } else {
             SSD_LAUNCH("bwd_blue_simt", launch_simt_bwd_blue<bf16>(p, s), 2);
             SSD_LAUNCH("bwd_k4_state_passing", launch_bwd_k4(p, s), 1);

@@ -40,7 +40,8 @@ struct Params {
     float *dD_part;      // [b, n, H, dD_per]
     int dD_per;
     float *dA_part;      // [b, H, n]
-    float *d_cb;         // [b, n, G, Q, Q]   (CUDA-core group path)
+    float *d_cb;         // [nslice_cb, b, n, G, Q, Q] d_cb (partial sums per head slice)
+    int nslice_cb;
     float *dBC_part;     // [nslice, 2, b, n, G, Q, N]  (tensor-core group path)
     int nslice;
     int *status;         // device status word (SSD_OK / SSD_ERR_TIMEOUT)

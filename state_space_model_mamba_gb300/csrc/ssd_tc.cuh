@@ -9,7 +9,9 @@ namespace ssd {
 bool tc_supported(int64_t P, int64_t N, int64_t Q);
 // dD partials per (b, chunk, head) written by the tensor-core main backward.
 int tc_dD_per(int64_t Q);
-// Head slices of the group-level backward (partial dB / dC sums).
+// Head slices of the group-level backward: d_cb partial sums (first) and the
+// dB / dC partial sums (second).
+int tc_dcb_slices(const ssd_dims &d);
 int tc_group_slices(const ssd_dims &d);
 
 cudaError_t launch_tc_k2(const Params &p, cudaStream_t s);
