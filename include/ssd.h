@@ -140,6 +140,37 @@ ssd_status ssd_profile_begin(void **events, int capacity);
 int ssd_profile_end(void);
 const char *ssd_profile_name(int i);
 
+/* ---- Forward without any device allocation (no counterpart on the pages) ----
+ *
+ * For callers that cannot call cudaMalloc themselves or have it called for
+ * them: code whose device memory is owned by an arena or pool it may not
+ * grow, plug-ins whose host framework forbids allocation on the hot path,
+ * and code running while another component captures or replays work.
+ * ssd_forward_noalloc computes exactly what ssd_forward computes, with the
+ * same arguments minus the workspace: its scratch is a fixed array of
+ * SSD_NOALLOC_SCRATCH_BYTES bytes in this library's device memory, created
+ * on every GPU that loads the library and held until the process exits.
+ *
+ *  - Size limit: shapes whose forward workspace (ssd_workspace_bytes(dims,
+ *    dtype, 0)) exceeds SSD_NOALLOC_SCRATCH_BYTES are rejected with
+ *    SSD_ERR_UNSUPPORTED and a message in ssd_last_error(); nothing is
+ *    enqueued.
+ *  - First call per device: it looks up the array's device address for the
+ *    current device (cudaGetSymbolAddress, which may load the library's code
+ *    onto that device).  Make that first call before any stream capture.
+ *  - Sharing: every call on a device uses the same array and leaves its
+ *    contents behind; the call clears what must start at zero itself.  Calls
+ *    whose GPU work overlaps (different streams, or different host threads
+ *    without ordering) race on the array and give wrong results: serialise
+ *    them on one stream.
+ *  - It calls no cudaMalloc, cudaFree or allocating library routine. */
+#define SSD_NOALLOC_SCRATCH_BYTES (64u * 1024u * 1024u)
+ssd_status ssd_forward_noalloc(const ssd_dims *dims, ssd_dtype dtype,
+                               const void *x, const float *dt, const float *A,
+                               const void *B, const void *C, const float *D,
+                               const float *init_state, const int32_t *valid_len,
+                               void *y, float *final_state, void *stream);
+
 /* Static description of a status code. */
 const char *ssd_status_str(ssd_status status);
 

@@ -198,6 +198,9 @@ ssd_status run_forward_chain(const Params &p, bool tc, bool write_final, cudaStr
 }
 
 }  // namespace
+
+void record_error(const char *msg) { snprintf(g_last_error, sizeof(g_last_error), "%s", msg); }
+
 }  // namespace ssd
 
 using namespace ssd;

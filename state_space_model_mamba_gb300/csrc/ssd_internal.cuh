@@ -103,6 +103,9 @@ __device__ __forceinline__ float block_sum(float v, float *red) {
     return s;  // valid in warp 0
 }
 
+// Sets the message ssd_last_error() returns on the calling host thread.
+void record_error(const char *msg);
+
 // ---------------------------------------------------------------- launchers
 // Shared by both execution paths (ssd_scan.cu).
 cudaError_t launch_k1_cumsum(const Params &p, cudaStream_t s);
