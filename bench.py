@@ -81,6 +81,10 @@ def kernel_costs(w, tc: bool) -> dict:
         "bwd_k4_state_passing": (4.0 * st, 8 * st + stb),
         "bwd_main": (b * n * H * (4.0 * tri * P + 2.0 * Q * P * N),
                      3 * x_b + bc_b + 4 * b * n * G * tri + (2 if tc else 4) * st + 6 * cum_b),
+        "bwd_k3": (b * n * H * 2.0 * Q * P * N,
+                   2 * x_b + bc_b + (2 if tc else 4) * st + 4 * cum_b),
+        "bwd_orange": (b * n * H * 4.0 * tri * P,
+                       4 * x_b + 2 * b * n * G * tri + 6 * cum_b),
         "bwd_group": (b * n * G * 4.0 * tri * N + b * n * H * 4.0 * Q * P * N,
                       2 * x_b + 2 * (2 if tc else 4) * st + 4 * bc_b + 2 * cum_b),
         "bwd_k1_chunk_cumsum": (0.0, 4 * cum_b + 8 * tok_h),

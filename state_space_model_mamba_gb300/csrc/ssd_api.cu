@@ -55,7 +55,7 @@ struct Layout {
     size_t status, cumA, endA, CB, states, states_bf, dstates, dstates_bf;
     size_t dcum_blue, dcum_main, d_delta, ddt_main, d_endA_part, dD_part, dA_part, d_cb, dBC_part;
     size_t total;
-    int k4_nblk, dD_per, nslice, nslice_cb;
+    int k4_nblk, dD_per, nslice, nslice_cb, nslice_k5;
 };
 
 bool use_tensor_cores(const ssd_dims &d, ssd_dtype dt) {
@@ -74,6 +74,7 @@ Layout make_layout(const ssd_dims &d, ssd_dtype dt, bool backward) {
     lo.dD_per = tc ? tc_dD_per(d.chunk_len) : (int)(Q / kMainRows);
     lo.nslice = tc ? tc_group_slices(d) : 1;
     lo.nslice_cb = tc ? tc_dcb_slices(d) : 1;
+    lo.nslice_k5 = tc ? tc_k5_slices(d) : 1;
     size_t off = 0;
     auto take = [&](size_t bytes) { size_t o = off; off += align_up(bytes); return o; };
     lo.status = take(16);
@@ -146,6 +147,8 @@ Params base_params(const ssd_dims &d, const Layout &lo, void *ws) {
     p.cumA = f(lo.cumA);
     p.endA = f(lo.endA);
     p.CB = f(lo.CB);
+    p.CBh = (bf16 *)(w + lo.CB);
+    p.CBt = p.CBh + (size_t)p.b * p.n * p.G * p.Q * p.Q;
     p.states = f(lo.states);
     p.states_bf = lo.states_bf ? (bf16 *)(w + lo.states_bf) : nullptr;
     if (lo.dstates) {
@@ -165,6 +168,7 @@ Params base_params(const ssd_dims &d, const Layout &lo, void *ws) {
     p.dD_per = lo.dD_per;
     p.nslice = lo.nslice;
     p.nslice_cb = lo.nslice_cb;
+    p.nslice_k5 = lo.nslice_k5;
     return p;
 }
 
@@ -314,7 +318,8 @@ ssd_status ssd_backward(const ssd_dims *dims, ssd_dtype dtype, const void *x, co
         if (tc) {
             SSD_LAUNCH("bwd_blue_tc", launch_tc_bwd_blue(p, s), 1);
             SSD_LAUNCH("bwd_k4_state_passing", launch_bwd_k4(p, s), 1);
-            SSD_LAUNCH("bwd_main_tc", launch_tc_bwd_main(p, s), 1);
+            SSD_LAUNCH("bwd_k3_tc", launch_tc_bwd_k3(p, s), 1);
+            SSD_LAUNCH("bwd_orange_tc", launch_tc_bwd_orange(p, s), 1);
             SSD_LAUNCH("bwd_group_tc", launch_tc_bwd_group(p, s), 3);
         } else {
             SSD_LAUNCH("bwd_blue_simt", launch_simt_bwd_blue<bf16>(p, s), 2);

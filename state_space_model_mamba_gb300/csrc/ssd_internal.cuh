@@ -33,6 +33,8 @@ struct Params {
     float *ddt, *dA, *dD, *d_init;
     // workspace
     float *cumA, *endA, *CB, *states, *dstates;
+    bf16 *CBh;           // bf16 CB  [b, n, G, Q(t), Q(s)] in the CB region (tensor-core path)
+    bf16 *CBt;           // bf16 CB^T [b, n, G, Q(s), Q(t)] right after it
     bf16 *states_bf, *dstates_bf;
     float *dcum_blue, *dcum_main, *d_delta, *ddt_main;
     float *d_endA_part;  // [b, H, n, k4_nblk]
@@ -44,6 +46,7 @@ struct Params {
     int nslice_cb;
     float *dBC_part;     // [nslice, 2, b, n, G, Q, N]  (tensor-core group path)
     int nslice;
+    int nslice_k5;       // head slices of the persistent per-group kernels (tensor-core path)
     int *status;         // device status word (SSD_OK / SSD_ERR_TIMEOUT)
 };
 

@@ -6,8 +6,12 @@
 // (cp.async.bulk.tensor, 128-byte swizzle); operands that carry a per-token
 // factor (the causal decay matrix W, the K3 / BLUE scales) are formed by the
 // CTA's threads in registers and written to shared memory in the same
-// swizzled layout.  One elected thread issues the MMAs; the epilogues read
-// TMEM with tcgen05.ld (warp w owns TMEM lanes 32w..32w+31).
+// swizzled layout, or -- for the decay matrix W of K5 and the ORANGE
+// backward -- into TMEM as packed bf16 pairs, the MMA's A operand.  One
+// elected thread issues the MMAs; the epilogues read TMEM with tcgen05.ld
+// (warp w owns TMEM lanes 32(w%4)..32(w%4)+31; with 256 threads, warps w and
+// w+4 split the columns).  K5 and the backward's ORANGE / K3 kernels loop
+// over the heads of a group with the group's operands resident.
 //
 // Formulas (burn-mamba, "combined_backward.rs"): K2 CB = C B^T; K3 intra =
 // x^T (B * dt * exp(cumA_last - cumA)); K5 y = exp(cumA) (C s_in^T) +
@@ -35,11 +39,12 @@ namespace {
 constexpr int kP = 64;     // headdim
 constexpr int kN = 128;    // dstate
 constexpr int kThreads = 128;
+constexpr int kThreadsWide = 256;
 constexpr int kTile = 16384;  // one [128 rows][64] bf16 SW128 tile
 constexpr int kStatusTimeout = 5;
 
 struct TcMaps {
-    CUtensorMap x, dy, B, C, st, dst;
+    CUtensorMap x, dy, B, C, st, dst, cb, cbt;
 };
 
 __device__ __forceinline__ uint8_t *align1024(uint8_t *p) {
@@ -106,22 +111,10 @@ __device__ __forceinline__ float dot_row64(const uint8_t *tile, int row, const f
     return acc;
 }
 
-// Unpack one swizzled bf16 row (64 values) into floats.
-__device__ __forceinline__ void load_row64(const uint8_t *tile, int row, float *out) {
-    const uint32_t base = smem_u32(tile);
+// Store 32 floats as 32 contiguous bf16 in global memory (64-byte aligned).
+__device__ __forceinline__ void store_row32_bf16(bf16 *dst, const float *v) {
 #pragma unroll
-    for (int c8 = 0; c8 < 8; ++c8) {
-        const uint4 u = ld_shared_v4(base + sw128_chunk(row, c8));
-        float *o = out + 8 * c8;
-        o[0] = bf_lo(u.x); o[1] = bf_hi(u.x); o[2] = bf_lo(u.y); o[3] = bf_hi(u.y);
-        o[4] = bf_lo(u.z); o[5] = bf_hi(u.z); o[6] = bf_lo(u.w); o[7] = bf_hi(u.w);
-    }
-}
-
-// Store 64 floats as a contiguous bf16 row in global memory.
-__device__ __forceinline__ void store_row64_bf16(bf16 *dst, const float *v) {
-#pragma unroll
-    for (int c8 = 0; c8 < 8; ++c8) {
+    for (int c8 = 0; c8 < 4; ++c8) {
         uint4 u;
         u.x = pack_bf2(v[8 * c8 + 0], v[8 * c8 + 1]);
         u.y = pack_bf2(v[8 * c8 + 2], v[8 * c8 + 3]);
@@ -133,7 +126,9 @@ __device__ __forceinline__ void store_row64_bf16(bf16 *dst, const float *v) {
 
 // ====================================================================== K2
 // CTA per (b, chunk, group).  CB[t, s] = sum_r C[t, r] B[s, r] for the causal
-// column range of each 128-row t-block (both operands K-major).
+// column range of each 128-row t-block (both operands K-major), stored in bf16
+// (it only ever feeds bf16 MMA operands); then CB^T[s, t] (t >= s's 128-row
+// block) the same way for the backward, whose ORANGE term works on rows s.
 template <int Q>
 __global__ void __launch_bounds__(kThreads) tc_k2_kernel(const Params p, const __grid_constant__ TcMaps maps) {
     constexpr int NT = Q / 128;
@@ -187,16 +182,40 @@ __global__ void __launch_bounds__(kThreads) tc_k2_kernel(const Params p, const _
     ok = wait_all(&bar_mma, 0, ok);
     tc_fence_after();
     if (ok) {
-        float *cb = p.CB + ix_cb(p, bi, c, g);
+        bf16 *cb = p.CBh + ix_cb(p, bi, c, g);
         for (int tb = 0; tb < NT; ++tb) {
             const int t = tb * 128 + 32 * warp + lane;
             const uint32_t col = tb == 0 ? 0u : 128u;
             for (int s0 = 0; s0 < 128 * (tb + 1); s0 += 32) {
                 float v[32];
                 tmem_ld32(tmem_addr(tm, 32 * warp, col + s0), v);
-                float4 *dst = reinterpret_cast<float4 *>(cb + (size_t)t * Q + s0);
-#pragma unroll
-                for (int j = 0; j < 8; ++j) dst[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+                store_row32_bf16(cb + (size_t)t * Q + s0, v);
+            }
+        }
+    }
+    // ---- CB^T (rows s, columns t >= 128 mb) for the backward's transposed ORANGE
+    tc_sync();
+    if (tid == 0 && ok) {
+        for (int mb = 0; mb < NT; ++mb) {
+            const uint32_t idesc = idesc_bf16(128, Q - 128 * mb, false, false);
+            const uint32_t col = mb == 0 ? 0u : 256u;
+            for (int ks = 0; ks < kN / 16; ++ks)
+                mma_bf16(tm + col, sdesc_kmajor(smem_u32(Bs + mb * kTile), ks, RB),
+                         sdesc_kmajor(smem_u32(Cs + mb * kTile), ks, RB), idesc, ks > 0);
+        }
+        mma_commit(&bar_mma);
+    }
+    ok = wait_all(&bar_mma, 1, ok);
+    tc_fence_after();
+    if (ok) {
+        bf16 *cbt = p.CBt + ix_cb(p, bi, c, g);
+        for (int mb = 0; mb < NT; ++mb) {
+            const int s = mb * 128 + 32 * warp + lane;
+            const uint32_t col = mb == 0 ? 0u : 256u;
+            for (int j = 0; j < Q - 128 * mb; j += 32) {
+                float v[32];
+                tmem_ld32(tmem_addr(tm, 32 * warp, col + j), v);
+                store_row32_bf16(cbt + (size_t)s * Q + 128 * mb + j, v);
             }
         }
     } else if (tid == 0) {
@@ -283,37 +302,84 @@ __global__ void __launch_bounds__(kThreads) tc_k3_kernel(const Params p, const _
 }
 
 // ====================================================================== K5
-// CTA per (b, chunk, head).  Per 128-row t-block tb:
-//   ORANGE (TMEM cols tb*64):        W[tb] (K-major, formed here) x  (x MN-major)
-//   BLUE   (TMEM cols NT*64+tb*64):  C[tb] (K-major)             s_in (K-major)
-// y = ORANGE + exp(cumA_t) * BLUE + D x;  W[t, s] = CB[t, s] exp(cumA_t - cumA_s) dt_s (s <= t).
+// CTA per (b, chunk, group, head slice), 256 threads, looping over the slice's
+// heads with one CTA barrier per head.  C (BLUE's A operand) and the bf16 CB
+// tiles stay resident in shared memory; x and s_in are refilled per head by
+// TMA as soon as the previous head's MMAs complete, and land while this
+// head's W is built and the previous head's epilogue runs.  Per-head scalars
+// are prefetched two heads ahead.  Per 128-row t-block tb:
+//   ORANGE (TMEM cols tb*64):        W[tb] (A operand in TMEM) x  (x MN-major)
+//   BLUE   (TMEM cols NT*64+tb*64):  C[tb] (K-major)            s_in (K-major)
+// y = ORANGE + exp(cumA_t) * BLUE + D x, W[t, s] = CB[t, s] exp(cumA_t - cumA_s) dt_s
+// (s <= t), stored to TMEM as packed bf16 pairs.  The decay is factored
+// through pivots (both factors <= 1): cumA[64 sb + 63] for a 64 x 64 block
+// strictly below the diagonal, cumA[16 v + 15] for a 16-wide sub-block left of
+// the row's own inside a diagonal block; only the row's own 16-wide sub-block
+// takes direct exponentials.
 template <int Q>
-__global__ void __launch_bounds__(kThreads) tc_k5_kernel(const Params p, const __grid_constant__ TcMaps maps) {
+__global__ void __launch_bounds__(kThreadsWide, 1) tc_k5_kernel(const Params p, const __grid_constant__ TcMaps maps) {
     constexpr int NT = Q / 128;
     constexpr uint32_t XB = Q * 128, RB = Q * 128, SB = 64 * 128;
-    constexpr uint32_t WB = kTile * 2 * (NT * (NT + 1) / 2);  // tb0: 2 tiles, tb1: 4 tiles
-    constexpr uint32_t NCOL = NT == 2 ? 256 : 128;
+    constexpr int NWT = NT * (NT + 1);  // CB tiles: tb0 2, tb1 4
+    constexpr uint32_t NCOL = NT == 2 ? 512 : 256;
+    constexpr uint32_t OCOL = 0, BCOL = NT * 64, WCOL = 2 * NT * 64;
+    constexpr int NSC = 4;              // scalar buffers: prefetch distance 2, plus the epilogue's
+    constexpr int FST = 4 * Q + 24;     // cum Q | dts Q | gcol Q | g16 Q | piv 8 | piv16 16
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = align1024(smem_raw);
-    uint8_t *xs = sm, *Cs = xs + XB, *Ss = Cs + 2 * RB, *Ws = Ss + 2 * SB;
-    float *cum = reinterpret_cast<float *>(Ws + WB);
-    float *dts = cum + Q;
-    __shared__ uint64_t bar_tma, bar_mma;
+    uint8_t *Cs = sm, *CBs = Cs + 2 * RB, *xs = CBs + NWT * kTile, *Ss = xs + XB;
+    float *fbuf = reinterpret_cast<float *>(Ss + 2 * SB);  // [NSC][FST]
+    __shared__ uint64_t bar_res, bar_x, bar_mma;
     __shared__ uint32_t s_tmem;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int h = blockIdx.x % p.H, c = (blockIdx.x / p.H) % p.n, bi = blockIdx.x / (p.H * p.n);
-    const int g = h / p.hpg, t0 = c * Q;
-    const int V = valid_len_of(p, bi);
-    const int vrows = min(Q, V - t0);
+    const int q4 = warp & 3, hf = warp >> 2;
+    int idx = blockIdx.x;
+    const int slice = idx % p.nslice_k5;
+    idx /= p.nslice_k5;
+    const int g = idx % p.G, c = (idx / p.G) % p.n, bi = idx / (p.G * p.n);
+    const int t0 = c * Q;
+    const int vrows = min(Q, valid_len_of(p, bi) - t0);
+    const int per = (p.hpg + p.nslice_k5 - 1) / p.nslice_k5;
+    const int h_begin = g * p.hpg + slice * per;
+    const int h_end = min(g * p.hpg + p.hpg, h_begin + per);
+    const int nh = h_end - h_begin;
     bf16 *Y = (bf16 *)p.y;
+    if (nh <= 0) return;
     if (vrows <= 0) {
         const int rows = min(Q, p.L - t0);
-        for (int i = tid; i < rows * (kP / 8); i += kThreads)
-            reinterpret_cast<uint4 *>(Y + ix_x(p, bi, t0 + i / 8, h, 0))[i % 8] = make_uint4(0, 0, 0, 0);
+        for (int hh = h_begin; hh < h_end; ++hh)
+            for (int i = tid; i < rows * (kP / 8); i += kThreadsWide)
+                reinterpret_cast<uint4 *>(Y + ix_x(p, bi, t0 + i / 8, hh, 0))[i % 8] = make_uint4(0, 0, 0, 0);
         return;
     }
+    // raw per-head scalars into buffer `b`: cumA, dt (0 past valid_len)
+    auto load_raw = [&](int h, int b) {
+        float *f = fbuf + b * FST;
+        const float *cumg = p.cumA + ix_chunk(p, bi, h, c) * Q;
+        for (int l = tid; l < Q; l += kThreadsWide) {
+            f[l] = cumg[l];
+            f[Q + l] = l < vrows ? p.dt[ix_dt(p, bi, h, t0 + l)] : 0.f;
+        }
+    };
+    // column factors dt exp(piv - cumA) and pivots, from the raw values (visible after a barrier)
+    auto derive = [&](int b) {
+        float *f = fbuf + b * FST;
+        for (int l = tid; l < Q; l += kThreadsWide) {
+            f[2 * Q + l] = f[Q + l] * __expf(f[l | 63] - f[l]);
+            f[3 * Q + l] = f[Q + l] * __expf(f[l | 15] - f[l]);
+        }
+        for (int j = tid; j < Q / 64; j += kThreadsWide) f[4 * Q + j] = f[64 * j + 63];
+        for (int j = tid; j < Q / 16; j += kThreadsWide) f[4 * Q + 8 + j] = f[16 * j + 15];
+    };
+    auto issue_head = [&](int h) {
+        const int sidx = (bi * p.n + c) * p.H + h;
+        mbar_arrive_expect_tx(&bar_x, XB + 2 * SB);
+        for (int j = 0; j < NT; ++j) tma_load_4d(xs + j * kTile, &maps.x, &bar_x, 0, h, t0 + 128 * j, bi);
+        for (int rb = 0; rb < 2; ++rb) tma_load_3d(Ss + rb * SB, &maps.st, &bar_x, 64 * rb, 0, sidx);
+    };
     if (tid == 0) {
-        mbar_init(&bar_tma, 1);
+        mbar_init(&bar_res, 1);
+        mbar_init(&bar_x, 1);
         mbar_init(&bar_mma, 1);
         mbar_fence_init();
     }
@@ -321,98 +387,173 @@ __global__ void __launch_bounds__(kThreads) tc_k5_kernel(const Params p, const _
     tc_sync();
     const uint32_t tm = s_tmem;
     if (tid == 0) {
-        mbar_arrive_expect_tx(&bar_tma, XB + 2 * RB + 2 * SB);
-        const int sidx = (bi * p.n + c) * p.H + h;
-        for (int j = 0; j < NT; ++j) {
-            tma_load_4d(xs + j * kTile, &maps.x, &bar_tma, 0, h, t0 + 128 * j, bi);
+        mbar_arrive_expect_tx(&bar_res, 2 * RB + NWT * kTile);
+        const int cbrow = ((bi * p.n + c) * p.G + g) * Q;
+        for (int j = 0; j < NT; ++j)
             for (int rb = 0; rb < 2; ++rb)
-                tma_load_4d(Cs + rb * RB + j * kTile, &maps.C, &bar_tma, 64 * rb, g, t0 + 128 * j, bi);
-        }
-        for (int rb = 0; rb < 2; ++rb) tma_load_3d(Ss + rb * SB, &maps.st, &bar_tma, 64 * rb, 0, sidx);
+                tma_load_4d(Cs + rb * RB + j * kTile, &maps.C, &bar_res, 64 * rb, g, t0 + 128 * j, bi);
+        for (int tb = 0; tb < NT; ++tb)
+            for (int sb = 0; sb < 2 * (tb + 1); ++sb)
+                tma_load_2d(CBs + (tb * (tb + 1) + sb) * kTile, &maps.cb, &bar_res, 64 * sb, cbrow + 128 * tb);
+        issue_head(h_begin);
     }
-    const float *cumg = p.cumA + ix_chunk(p, bi, h, c) * Q;
-    for (int l = tid; l < Q; l += kThreads) {
-        cum[l] = cumg[l];
-        dts[l] = l < vrows ? p.dt[ix_dt(p, bi, h, t0 + l)] : 0.f;
-    }
-    __syncthreads();
-    // ---- form W (bf16, K-major per t-block) while the TMA loads land
-    const float *cb = p.CB + ix_cb(p, bi, c, g);
-    for (int tb = 0; tb < NT; ++tb) {
-        uint8_t *Wt = Ws + kTile * 2 * (tb * (tb + 1) / 2);
-        const int nch = 16 * (tb + 1);  // 8-column chunks per row
-        for (int i = tid; i < 128 * nch; i += kThreads) {
-            const int row = i / nch, ch = i % nch;
-            const int t = tb * 128 + row, s0 = 8 * ch;
-            uint32_t u[4] = {0u, 0u, 0u, 0u};
-            if (s0 <= t && t < vrows) {
-                const float4 a = *reinterpret_cast<const float4 *>(cb + (size_t)t * Q + s0);
-                const float4 b = *reinterpret_cast<const float4 *>(cb + (size_t)t * Q + s0 + 4);
-                const float cv[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-                const float ct = cum[t];
-                float w[8];
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const int s = s0 + e;
-                    w[e] = (s <= t && s < vrows) ? cv[e] * __expf(ct - cum[s]) * dts[s] : 0.f;
-                }
-                u[0] = pack_bf2(w[0], w[1]);
-                u[1] = pack_bf2(w[2], w[3]);
-                u[2] = pack_bf2(w[4], w[5]);
-                u[3] = pack_bf2(w[6], w[7]);
-            }
-            st_shared_v4(smem_u32(Wt + (s0 / 64) * kTile) + sw128_chunk(row, (s0 % 64) / 8), u[0], u[1], u[2], u[3]);
-        }
-    }
-    bool ok = wait_all(&bar_tma, 0, true);
+    load_raw(h_begin, 0);
+    if (nh > 1) load_raw(h_begin + 1, 1);
+    int x_issued = 1, x_landed = 0;
+    bool ok = wait_all(&bar_res, 0, true);  // publishes the raw scalars of heads 0 and 1
     if (ok && vrows < Q) {
-        zero_rows_from(xs, Q, vrows);
         zero_rows_from(Cs, Q, vrows);
         zero_rows_from(Cs + RB, Q, vrows);
+        fence_async_smem();
     }
-    fence_async_smem();
-    tc_sync();
-    if (tid == 0 && ok) {
-        for (int tb = 0; tb < NT; ++tb) {
-            uint8_t *Wt = Ws + kTile * 2 * (tb * (tb + 1) / 2);
-            const uint32_t id = idesc_bf16(128, 64, false, true);
-            for (int ks = 0; ks < 8 * (tb + 1); ++ks)
-                mma_bf16(tm + tb * 64, sdesc_kmajor(smem_u32(Wt), ks, kTile), sdesc_mnmajor(smem_u32(xs), ks, XB), id,
-                         ks > 0);
-            const uint32_t ib = idesc_bf16(128, 64, false, false);
-            for (int ks = 0; ks < kN / 16; ++ks)
-                mma_bf16(tm + NT * 64 + tb * 64, sdesc_kmajor(smem_u32(Cs + tb * kTile), ks, RB),
-                         sdesc_kmajor(smem_u32(Ss), ks, SB), ib, ks > 0);
-        }
-        mma_commit(&bar_mma);
-    }
-    ok = wait_all(&bar_mma, 0, ok);
-    tc_fence_after();
-    if (ok) {
-        const float Dh = p.D[h];
-        for (int tb = 0; tb < NT; ++tb) {
-            const int t = tb * 128 + 32 * warp + lane;
-            float o[64], bl[64], xv[64];
-            tmem_ld32(tmem_addr(tm, 32 * warp, tb * 64), o);
-            tmem_ld32(tmem_addr(tm, 32 * warp, tb * 64 + 32), o + 32);
-            tmem_ld32(tmem_addr(tm, 32 * warp, NT * 64 + tb * 64), bl);
-            tmem_ld32(tmem_addr(tm, 32 * warp, NT * 64 + tb * 64 + 32), bl + 32);
-            if (t0 + t < p.L) {
-                if (t < vrows) {
-                    load_row64(xs, t, xv);
-                    const float e = __expf(cum[t]);
-#pragma unroll
-                    for (int j = 0; j < 64; ++j) o[j] = o[j] + e * bl[j] + Dh * xv[j];
-                } else {
-#pragma unroll
-                    for (int j = 0; j < 64; ++j) o[j] = 0.f;
-                }
-                store_row64_bf16(Y + ix_x(p, bi, t0 + t, h, 0), o);
+    derive(0);
+    __syncthreads();
+    uint4 xr[NT][4];  // this thread's D x slices of the head whose epilogue comes next
+    for (int k = 0; k <= nh && ok; ++k) {
+        const int h = h_begin + k, cur = k % NSC, prv = (k + NSC - 1) % NSC;
+        if (k > 0) {
+            // MMAs of head k-1 done: the TMEM W region and the x / s_in buffers are free
+            ok = mbar_wait(&bar_mma, (uint32_t)((k - 1) & 1)) && ok;
+            tc_fence_after();
+            if (k < nh) {
+                if (tid == 0 && ok) issue_head(h);
+                x_issued = k + 1;
             }
         }
-    } else if (tid == 0) {
-        flag_timeout(p);
+        if (k < nh) {
+            const float *f = fbuf + cur * FST;
+            const float *cum = f, *dts = f + Q, *gcol = f + 2 * Q, *g16 = f + 3 * Q;
+            const float *piv = f + 4 * Q, *piv16 = f + 4 * Q + 8;
+            // ---- W_k into TMEM (packed bf16 pairs, lane = t), while x_k / s_in_k land.
+            // The two warp halves take alternate 64-column groups (balanced diagonal work).
+            for (int tb = 0; tb < NT; ++tb) {
+                const int t = tb * 128 + 32 * q4 + lane;
+                const int tr = t >> 6, row = t - 128 * tb;
+                const float ct = cum[t];
+                for (int s0g = 64 * hf; s0g < 128 * (tb + 1); s0g += 128) {
+                    const int sb = s0g >> 6;
+                    float pk[32];
+                    if (sb > tr) {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) pk[j] = 0.f;
+                    } else {
+                        const uint32_t cbb = smem_u32(CBs + (tb * (tb + 1) + sb) * kTile);
+                        if (sb < tr) {
+                            const float e = __expf(ct - piv[sb]);
+#pragma unroll
+                            for (int c8 = 0; c8 < 8; ++c8) {
+                                const uint4 u = ld_shared_v4(cbb + sw128_chunk(row, c8));
+                                const float4 g0 = *reinterpret_cast<const float4 *>(gcol + s0g + 8 * c8);
+                                const float4 g1 = *reinterpret_cast<const float4 *>(gcol + s0g + 8 * c8 + 4);
+                                pk[4 * c8 + 0] = __uint_as_float(pack_bf2(bf_lo(u.x) * e * g0.x, bf_hi(u.x) * e * g0.y));
+                                pk[4 * c8 + 1] = __uint_as_float(pack_bf2(bf_lo(u.y) * e * g0.z, bf_hi(u.y) * e * g0.w));
+                                pk[4 * c8 + 2] = __uint_as_float(pack_bf2(bf_lo(u.z) * e * g1.x, bf_hi(u.z) * e * g1.y));
+                                pk[4 * c8 + 3] = __uint_as_float(pack_bf2(bf_lo(u.w) * e * g1.z, bf_hi(u.w) * e * g1.w));
+                            }
+                        } else {
+                            // diagonal 64-group: 16-wide sub-blocks, pivot cumA[16 v + 15]
+                            // left of the row's own sub-block, direct exponentials inside it
+                            const int u16 = (t & 63) >> 4;
+                            float e16 = 0.f;
+#pragma unroll
+                            for (int c8 = 0; c8 < 8; ++c8) {
+                                const int v16 = c8 >> 1;
+                                const uint4 u = ld_shared_v4(cbb + sw128_chunk(row, c8));
+                                const float cv[8] = {bf_lo(u.x), bf_hi(u.x), bf_lo(u.y), bf_hi(u.y),
+                                                     bf_lo(u.z), bf_hi(u.z), bf_lo(u.w), bf_hi(u.w)};
+                                float w[8];
+                                if (v16 < u16) {
+                                    if ((c8 & 1) == 0) e16 = __expf(ct - piv16[4 * sb + v16]);
+#pragma unroll
+                                    for (int j = 0; j < 8; ++j) w[j] = cv[j] * e16 * g16[s0g + 8 * c8 + j];
+                                } else if (v16 == u16) {
+#pragma unroll
+                                    for (int j = 0; j < 8; ++j) {
+                                        const int s = s0g + 8 * c8 + j;
+                                        w[j] = s <= t ? cv[j] * __expf(ct - cum[s]) * dts[s] : 0.f;
+                                    }
+                                } else {
+#pragma unroll
+                                    for (int j = 0; j < 8; ++j) w[j] = 0.f;
+                                }
+#pragma unroll
+                                for (int j = 0; j < 4; ++j) pk[4 * c8 + j] = __uint_as_float(pack_bf2(w[2 * j], w[2 * j + 1]));
+                            }
+                        }
+                    }
+                    tmem_st32(tmem_addr(tm, 32 * q4, WCOL + 64 * (tb * (tb + 1) / 2) + (s0g >> 1)), pk);
+                }
+            }
+            // prefetch raw scalars of head k + 2, derive those of head k + 1 (raw visible since the last barrier)
+            if (k + 2 < nh) load_raw(h + 2, (k + 2) % NSC);
+            if (k + 1 < nh) derive((k + 1) % NSC);
+        }
+        // ---- epilogue of head k - 1
+        if (k > 0) {
+            const float *cum = fbuf + prv * FST;
+            const float Dh = p.D[h - 1];
+#pragma unroll
+            for (int tb = 0; tb < NT; ++tb) {
+                const int t = tb * 128 + 32 * q4 + lane;
+                float o[32], bl[32];
+                tmem_ld32(tmem_addr(tm, 32 * q4, OCOL + tb * 64 + hf * 32), o);
+                tmem_ld32(tmem_addr(tm, 32 * q4, BCOL + tb * 64 + hf * 32), bl);
+                if (t0 + t < p.L) {
+                    if (t < vrows) {
+                        const float e = __expf(cum[t]);
+#pragma unroll
+                        for (int c8 = 0; c8 < 4; ++c8) {
+                            const uint4 u = xr[tb][c8];
+                            const float xv[8] = {bf_lo(u.x), bf_hi(u.x), bf_lo(u.y), bf_hi(u.y),
+                                                 bf_lo(u.z), bf_hi(u.z), bf_lo(u.w), bf_hi(u.w)};
+#pragma unroll
+                            for (int j = 0; j < 8; ++j) o[8 * c8 + j] += e * bl[8 * c8 + j] + Dh * xv[j];
+                        }
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) o[j] = 0.f;
+                    }
+                    store_row32_bf16(Y + ix_x(p, bi, t0 + t, h - 1, 32 * hf), o);
+                }
+            }
+        }
+        if (k == nh) break;
+        // ---- x_k landed: keep this thread's D x slices, zero padded rows
+        ok = mbar_wait(&bar_x, (uint32_t)(k & 1)) && ok;
+        if (ok) x_landed = k + 1;
+#pragma unroll
+        for (int tb = 0; tb < NT; ++tb) {
+            const int t = tb * 128 + 32 * q4 + lane;
+#pragma unroll
+            for (int c8 = 0; c8 < 4; ++c8) xr[tb][c8] = ld_shared_v4(smem_u32(xs) + sw128_chunk(t, 4 * hf + c8));
+        }
+        if (vrows < Q) {
+            __syncthreads();
+            zero_rows_from(xs, Q, vrows);
+            fence_async_smem();
+        }
+        // ---- one barrier: W_k stored, accumulators of k-1 read, x_k in place
+        tc_fence_before();
+        ok = __syncthreads_and(ok ? 1 : 0) != 0;
+        tc_fence_after();
+        if (tid == 0 && ok) {
+            const uint32_t id = idesc_bf16(128, 64, false, true);
+            const uint32_t ib = idesc_bf16(128, 64, false, false);
+            for (int tb = 0; tb < NT; ++tb) {
+                const uint32_t wc = WCOL + 64 * (tb * (tb + 1) / 2);
+                for (int ks = 0; ks < 8 * (tb + 1); ++ks)
+                    mma_bf16_tmem_a(tm + OCOL + tb * 64, tm + wc + 8 * ks, sdesc_mnmajor(smem_u32(xs), ks, XB), id,
+                                    ks > 0);
+                for (int ks = 0; ks < kN / 16; ++ks)
+                    mma_bf16(tm + BCOL + tb * 64, sdesc_kmajor(smem_u32(Cs + tb * kTile), ks, RB),
+                             sdesc_kmajor(smem_u32(Ss), ks, SB), ib, ks > 0);
+            }
+            mma_commit(&bar_mma);
+        }
     }
+    if (!ok && tid == 0) flag_timeout(p);
+    // a load issued for a head that was never waited for has to land before exit
+    if (x_issued > x_landed) mbar_wait(&bar_x, (uint32_t)((x_issued - 1) & 1));
     tc_sync();
     if (warp == 0) tmem_dealloc(tm, NCOL);
 }
@@ -510,281 +651,511 @@ __global__ void __launch_bounds__(kThreads) tc_bwd_blue_kernel(const Params p, c
     if (warp == 0) tmem_dealloc(tm, NCOL);
 }
 
-// ====================================================================== main backward
-// CTA per (b, chunk, head).  TMEM (Q = 256): dW tb0 cols [0,128), tb1 [128,384);
-// U = B d_intra^T per 128-row s-block at [384 + mb*64); dx accumulators reuse
-// [mb*64) once dW has been read.
-//   phase 1: dW = dy x^T (K-major, K = headdim), U (K-major, K = dstate)
-//   phase 2: d_bbs[s] = sum_p x U, dD partial; then W, row/column sums from dW
-//            (W written MN-major over the freed x / B tiles)
-//   phase 3: dx = W^T dy  (A = W MN-major, B = dy MN-major)
-//   phase 4: dx += bbs * U + D dy; per-token outputs.
+// ====================================================================== K3 backward
+// CTA per (b, chunk, group, head slice), 256 threads, looping over the slice's
+// heads with a two-stage TMA ring (x, d_intra); B stays resident.  Per head
+// (the K3 BACKWARD block, with the per-head d_b_scaled folded away):
+//   U[s, p]   = sum_r B[s, r] d_intra[p, r]           (TMEM, A = B K-major, B = d_intra K-major)
+//   d_bbs[s]  = sum_p x[s, p] U[s, p]
+//   dx        = bbs[s] U[s, p]                        (first writer of dx; the ORANGE kernel adds)
+//   ddt_main  = d_bbs exp(cumA_last - cumA)           (the K3 part of ddt)
+//   d_delta   = d_bbs dt exp(cumA_last - cumA)        (the K3 part of d cumA)
 template <int Q>
-__global__ void __launch_bounds__(kThreads) tc_bwd_main_kernel(const Params p, const __grid_constant__ TcMaps maps) {
+__global__ void __launch_bounds__(kThreadsWide, 1) tc_bwd_k3_kernel(const Params p, const __grid_constant__ TcMaps maps) {
     constexpr int NT = Q / 128;
     constexpr uint32_t XB = Q * 128, RB = Q * 128, SB = 64 * 128;
-    constexpr uint32_t NCOL = NT == 2 ? 512 : 256;
-    constexpr uint32_t UCOL = NT == 2 ? 384 : 128;   // U accumulators
+    constexpr uint32_t STG = XB + 2 * SB;
+    constexpr uint32_t NCOL = NT == 2 ? 256 : 128;  // U, two buffers of NT * 64 columns
+    constexpr int NSC = 3;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = align1024(smem_raw);
-    uint8_t *DYs = sm, *Xs = DYs + XB, *Bs = Xs + XB, *DIs = Bs + 2 * RB;
-    uint8_t *Ws = Xs;  // reuses x + B (3 * Q * 128 bytes >= W bytes)
-    float *cum = reinterpret_cast<float *>(DIs + 2 * SB);
-    float *dts = cum + Q;              // dt (0 past valid_len)
-    float *dec_end = dts + Q;          // exp(cumA_last - cumA)
-    float *dbbs = dec_end + Q;         // d_bbs
-    float *tgt = dbbs + Q;             // row sums of dW * W
-    float *colp = tgt + Q;             // [NT][4][2][Q] column partials (ddt_orange, src)
-    float *red = colp + NT * 4 * 2 * Q;  // [4] dD partials
-    __shared__ uint64_t bar_tma, bar_mma1, bar_mma2;
+    uint8_t *Bs = sm, *stg = Bs + 2 * RB;
+    float *fbuf = reinterpret_cast<float *>(stg + 2 * STG);  // [NSC][3Q]: dts, dec_end, (spare)
+    float *dbbp = fbuf + NSC * 3 * Q;                        // [2][Q]
+    __shared__ uint64_t bar_res, bar_x[2], bar_mma[2];
     __shared__ uint32_t s_tmem;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int h = blockIdx.x % p.H, c = (blockIdx.x / p.H) % p.n, bi = blockIdx.x / (p.H * p.n);
-    const int g = h / p.hpg, t0 = c * Q;
-    const int V = valid_len_of(p, bi);
-    const int vrows = min(Q, V - t0);
-    const size_t cbase = ix_chunk(p, bi, h, c) * Q;
+    const int q4 = warp & 3, hf = warp >> 2;
+    int idx = blockIdx.x;
+    const int slice = idx % p.nslice_k5;
+    idx /= p.nslice_k5;
+    const int g = idx % p.G, c = (idx / p.G) % p.n, bi = idx / (p.G * p.n);
+    const int t0 = c * Q;
+    const int vrows = min(Q, valid_len_of(p, bi) - t0);
+    const int per = (p.hpg + p.nslice_k5 - 1) / p.nslice_k5;
+    const int h_begin = g * p.hpg + slice * per;
+    const int h_end = min(g * p.hpg + p.hpg, h_begin + per);
+    const int nh = h_end - h_begin;
     bf16 *DX = (bf16 *)p.dx;
+    if (nh <= 0) return;
     if (vrows <= 0) {
         const int rows = min(Q, p.L - t0);
-        for (int i = tid; i < rows * (kP / 8); i += kThreads)
-            reinterpret_cast<uint4 *>(DX + ix_x(p, bi, t0 + i / 8, h, 0))[i % 8] = make_uint4(0, 0, 0, 0);
-        for (int i = tid; i < Q; i += kThreads) {
-            p.ddt_main[cbase + i] = 0.f;
-            p.d_delta[cbase + i] = 0.f;
-            p.dcum_main[cbase + i] = 0.f;
+        for (int hh = h_begin; hh < h_end; ++hh) {
+            for (int i = tid; i < rows * (kP / 8); i += kThreadsWide)
+                reinterpret_cast<uint4 *>(DX + ix_x(p, bi, t0 + i / 8, hh, 0))[i % 8] = make_uint4(0, 0, 0, 0);
+            const size_t cb = ix_chunk(p, bi, hh, c) * Q;
+            for (int i = tid; i < Q; i += kThreadsWide) {
+                p.ddt_main[cb + i] = 0.f;
+                p.d_delta[cb + i] = 0.f;
+            }
         }
-        if (tid == 0) p.dD_part[((size_t)bi * p.n + c) * p.H + h] = 0.f;
         return;
     }
+    auto load_scalars = [&](int h, int b) {
+        float *f = fbuf + b * 3 * Q;
+        const float *cumg = p.cumA + ix_chunk(p, bi, h, c) * Q;
+        const float cend = p.endA[ix_chunk(p, bi, h, c)];
+        for (int l = tid; l < Q; l += kThreadsWide) {
+            f[l] = l < vrows ? p.dt[ix_dt(p, bi, h, t0 + l)] : 0.f;
+            f[Q + l] = __expf(cend - cumg[l]);
+        }
+    };
+    auto issue = [&](int k) {
+        const int h = h_begin + k, st = k & 1;
+        uint8_t *xs = stg + st * STG, *dis = xs + XB;
+        const int sidx = (bi * p.n + c) * p.H + h;
+        mbar_arrive_expect_tx(&bar_x[st], STG);
+        for (int j = 0; j < NT; ++j) tma_load_4d(xs + j * kTile, &maps.x, &bar_x[st], 0, h, t0 + 128 * j, bi);
+        for (int rb = 0; rb < 2; ++rb) tma_load_3d(dis + rb * SB, &maps.dst, &bar_x[st], 64 * rb, 0, sidx);
+    };
     if (tid == 0) {
-        mbar_init(&bar_tma, 1);
-        mbar_init(&bar_mma1, 1);
-        mbar_init(&bar_mma2, 1);
+        mbar_init(&bar_res, 1);
+        mbar_init(&bar_x[0], 1);
+        mbar_init(&bar_x[1], 1);
+        mbar_init(&bar_mma[0], 1);
+        mbar_init(&bar_mma[1], 1);
         mbar_fence_init();
     }
     if (warp == 0) tmem_alloc(&s_tmem, NCOL);
     tc_sync();
     const uint32_t tm = s_tmem;
     if (tid == 0) {
-        mbar_arrive_expect_tx(&bar_tma, 2 * XB + 2 * RB + 2 * SB);
-        const int sidx = (bi * p.n + c) * p.H + h;
-        for (int j = 0; j < NT; ++j) {
-            tma_load_4d(DYs + j * kTile, &maps.dy, &bar_tma, 0, h, t0 + 128 * j, bi);
-            tma_load_4d(Xs + j * kTile, &maps.x, &bar_tma, 0, h, t0 + 128 * j, bi);
+        mbar_arrive_expect_tx(&bar_res, 2 * RB);
+        for (int j = 0; j < NT; ++j)
             for (int rb = 0; rb < 2; ++rb)
-                tma_load_4d(Bs + rb * RB + j * kTile, &maps.B, &bar_tma, 64 * rb, g, t0 + 128 * j, bi);
-        }
-        for (int rb = 0; rb < 2; ++rb) tma_load_3d(DIs + rb * SB, &maps.dst, &bar_tma, 64 * rb, 0, sidx);
+                tma_load_4d(Bs + rb * RB + j * kTile, &maps.B, &bar_res, 64 * rb, g, t0 + 128 * j, bi);
+        issue(0);
+        if (nh > 1) issue(1);
     }
-    {
-        const float *cumg = p.cumA + cbase;
-        const float cend = p.endA[ix_chunk(p, bi, h, c)];
-        for (int l = tid; l < Q; l += kThreads) {
-            const float cl = cumg[l];
-            cum[l] = cl;
-            dts[l] = l < vrows ? p.dt[ix_dt(p, bi, h, t0 + l)] : 0.f;
-            dec_end[l] = __expf(cend - cl);
-        }
-        for (int i = tid; i < NT * 4 * 2 * Q; i += kThreads) colp[i] = 0.f;
-    }
-    bool ok = wait_all(&bar_tma, 0, true);
+    load_scalars(h_begin, 0);
+    if (nh > 1) load_scalars(h_begin + 1, 1);
+    int issued = nh > 1 ? 2 : 1, landed = 0;
+    bool ok = wait_all(&bar_res, 0, true);
     if (ok && vrows < Q) {
-        zero_rows_from(DYs, Q, vrows);
-        zero_rows_from(Xs, Q, vrows);
         zero_rows_from(Bs, Q, vrows);
         zero_rows_from(Bs + RB, Q, vrows);
+        fence_async_smem();
     }
-    fence_async_smem();
-    tc_sync();
-    // ---- phase 1 MMAs
-    if (tid == 0 && ok) {
-        for (int tb = 0; tb < NT; ++tb) {
-            const uint32_t id = idesc_bf16(128, 128 * (tb + 1), false, false);
-            const uint32_t col = tb == 0 ? 0u : 128u;
-            for (int ks = 0; ks < kP / 16; ++ks)
-                mma_bf16(tm + col, sdesc_kmajor(smem_u32(DYs + tb * kTile), ks, XB),
-                         sdesc_kmajor(smem_u32(Xs), ks, XB), id, ks > 0);
+    for (int k = 0; k < nh && ok; ++k) {
+        const int h = h_begin + k, st = k & 1;
+        uint8_t *xs = stg + st * STG, *dis = xs + XB;
+        const float *f = fbuf + (k % NSC) * 3 * Q;
+        const float *dts = f, *dec = f + Q;
+        ok = mbar_wait(&bar_x[st], (uint32_t)((k >> 1) & 1)) && ok;
+        if (ok) landed = k + 1;
+        if (vrows < Q) {
+            __syncthreads();
+            zero_rows_from(xs, Q, vrows);
         }
-        const uint32_t iu = idesc_bf16(128, 64, false, false);
-        for (int mb = 0; mb < NT; ++mb)
-            for (int ks = 0; ks < kN / 16; ++ks)
-                mma_bf16(tm + UCOL + mb * 64, sdesc_kmajor(smem_u32(Bs + mb * kTile), ks, RB),
-                         sdesc_kmajor(smem_u32(DIs), ks, SB), iu, ks > 0);
-        mma_commit(&bar_mma1);
-    }
-    ok = wait_all(&bar_mma1, 0, ok);
-    tc_fence_after();
-    // ---- phase 2a: x-dependent reductions (before x / B are overwritten by W)
-    float dd = 0.f;
-    if (ok) {
+        fence_async_smem();
+        tc_fence_before();
+        ok = __syncthreads_and(ok ? 1 : 0) != 0;
+        tc_fence_after();
+        if (!ok) break;
+        const uint32_t ucol = (uint32_t)(st * NT * 64);
+        if (tid == 0) {
+            const uint32_t iu = idesc_bf16(128, 64, false, false);
+            for (int mb = 0; mb < NT; ++mb)
+                for (int ks = 0; ks < kN / 16; ++ks)
+                    mma_bf16(tm + ucol + mb * 64, sdesc_kmajor(smem_u32(Bs + mb * kTile), ks, RB),
+                             sdesc_kmajor(smem_u32(dis), ks, SB), iu, ks > 0);
+            mma_commit(&bar_mma[st]);
+        }
+        if (k + 2 < nh) load_scalars(h + 2, (k + 2) % NSC);
+        ok = mbar_wait(&bar_mma[st], (uint32_t)((k >> 1) & 1)) && ok;
+        tc_fence_after();
         for (int mb = 0; mb < NT; ++mb) {
-            const int s = mb * 128 + 32 * warp + lane;
-            float u[64];
-            tmem_ld32(tmem_addr(tm, 32 * warp, UCOL + mb * 64), u);
-            tmem_ld32(tmem_addr(tm, 32 * warp, UCOL + mb * 64 + 32), u + 32);
-            dbbs[s] = dot_row64(Xs, s, u);
-            float dyv[64];
-            load_row64(DYs, s, dyv);
-            dd += dot_row64(Xs, s, dyv);
+            const int s = mb * 128 + 32 * q4 + lane;
+            float u[32];
+            tmem_ld32(tmem_addr(tm, 32 * q4, ucol + mb * 64 + 32 * hf), u);
+            float part = 0.f;
+            const uint32_t xb = smem_u32(xs);
+#pragma unroll
+            for (int c8 = 0; c8 < 4; ++c8) {
+                const uint4 xv = ld_shared_v4(xb + sw128_chunk(s, 4 * hf + c8));
+                const float *uu = u + 8 * c8;
+                part += bf_lo(xv.x) * uu[0] + bf_hi(xv.x) * uu[1] + bf_lo(xv.y) * uu[2] + bf_hi(xv.y) * uu[3] +
+                        bf_lo(xv.z) * uu[4] + bf_hi(xv.z) * uu[5] + bf_lo(xv.w) * uu[6] + bf_hi(xv.w) * uu[7];
+            }
+            dbbp[hf * Q + s] = part;
+            if (t0 + s < p.L) {
+                const float bbs = s < vrows ? dts[s] * dec[s] : 0.f;
+#pragma unroll
+                for (int j = 0; j < 32; ++j) u[j] *= bbs;
+                store_row32_bf16(DX + ix_x(p, bi, t0 + s, h, 32 * hf), u);
+            }
+        }
+        tc_fence_before();
+        ok = __syncthreads_and(ok ? 1 : 0) != 0;  // d_bbs halves complete; stage st no longer read
+        tc_fence_after();
+        if (tid == 0 && k + 2 < nh) issue(k + 2);
+        if (k + 2 < nh) issued = k + 3;
+        const size_t cbase = ix_chunk(p, bi, h, c) * Q;
+        for (int s = tid; s < Q; s += kThreadsWide) {
+            const float dbb = s < vrows ? dbbp[s] + dbbp[Q + s] : 0.f;
+            p.ddt_main[cbase + s] = dbb * dec[s];
+            p.d_delta[cbase + s] = dbb * dts[s] * dec[s];
         }
     }
-    dd = warp_sum(dd);
-    if (lane == 0) red[warp] = dd;
+    if (!ok && tid == 0) flag_timeout(p);
+    // loads issued for heads that were never waited for have to land before exit
+    for (int k = landed; k < issued; ++k) mbar_wait(&bar_x[k & 1], (uint32_t)((k >> 1) & 1));
     tc_sync();
-    // ---- phase 2b: W (bf16, MN-major per 128-row s-block, rows t >= 128*mb), sums
-    if (ok) {
-        const float *cbm = p.CB + ix_cb(p, bi, c, g);
-        for (int tb = 0; tb < NT; ++tb) {
-            const int t = tb * 128 + 32 * warp + lane;
-            const bool tv = t < vrows;
-            const float ct = cum[t];
-            const uint32_t col0 = tb == 0 ? 0u : 128u;
-            float rowsum = 0.f;
-            for (int s0 = 0; s0 < 128 * (tb + 1); s0 += 32) {
-                float dw[32];
-                tmem_ld32(tmem_addr(tm, 32 * warp, col0 + s0), dw);
-                float gsum[32], dsum[32];
-                float wv[32];
-                const float *cbrow = cbm + (size_t)t * Q + s0;
+    if (warp == 0) tmem_dealloc(tm, NCOL);
+}
+
+// ====================================================================== ORANGE backward
+// CTA per (b, chunk, group, head slice), 256 threads, looping over the slice's
+// heads.  The ORANGE block of the backward in transposed form: TMEM lane = the
+// source position s, so the column sums of the page (ddt over targets, the
+// source part of d cumA) become per-thread row sums and only the target part
+// of d cumA needs a cross-lane reduction.  Per head and 128-row s-block mb:
+//   dW^T[s, t] = sum_p x[s, p] dy[t, p]          t >= 128 mb      (TMEM, A = x, B = dy, K-major)
+//   W^T[s, t]  = CB^T[s, t] exp(cumA_t - cumA_s) dt_s   (t >= s)  (packed bf16 in TMEM, in place)
+//   ddt_orange[s] = sum_t dW^T CB^T decay,  src[s] = dt_s ddt_orange[s],  tgt[t] = sum_s dW^T W^T
+//   dx[s, p]  += sum_t W^T[s, t] dy[t, p] + D dy[s, p]    (A = W^T in TMEM, B = dy MN-major)
+// CB^T stays resident; x is single-buffered (refilled once dW^T is computed),
+// dy double-buffered.  The decay is factored through 64-group pivots off the
+// diagonal groups and 16-wide sub-block pivots inside them (all factors <= 1).
+// dx, ddt_main and d_delta already hold the K3 terms (K3 backward kernel).
+template <int Q>
+__global__ void __launch_bounds__(kThreadsWide, 1) tc_bwd_orange_kernel(const Params p, const __grid_constant__ TcMaps maps) {
+    constexpr int NT = Q / 128;
+    constexpr uint32_t XB = Q * 128;
+    constexpr int NCBT = NT == 2 ? 6 : 2;            // CB^T tiles: mb0 Q/64, mb1 Q/64 - 2
+    constexpr uint32_t NCOL = NT == 2 ? 512 : 256;
+    constexpr uint32_t DXCOL = NT == 2 ? 384 : 128;  // dx accumulators (dW^T occupies [0, DXCOL))
+    // per-head scalars: cum Q | dts Q | E (pivot rows) 384 | E16 16x64 | piv 8 | piv16 16
+    constexpr int EOFF = 2 * Q, E16OFF = EOFF + 384, POFF = E16OFF + 1024, P16OFF = POFF + 8;
+    constexpr int FST = P16OFF + 16;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *sm = align1024(smem_raw);
+    uint8_t *CBt = sm, *xs = CBt + NCBT * kTile, *dys = xs + XB;  // dys: 2 buffers
+    float *fbuf = reinterpret_cast<float *>(dys + 2 * XB);       // [2][FST]
+    float *colp = fbuf + 2 * FST;                                 // [NT][4][Q]  tgt partials
+    float *rowp = colp + NT * 4 * Q;                              // [2 hf][Q] ddt_orange halves
+    float *red = rowp + 2 * Q;                                    // [8] dD partials
+    __shared__ uint64_t bar_res, bar_x, bar_dy[2], bar_m1, bar_m2;
+    __shared__ uint32_t s_tmem;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int q4 = warp & 3, hf = warp >> 2;
+    int idx = blockIdx.x;
+    const int slice = idx % p.nslice_k5;
+    idx /= p.nslice_k5;
+    const int g = idx % p.G, c = (idx / p.G) % p.n, bi = idx / (p.G * p.n);
+    const int t0 = c * Q;
+    const int vrows = min(Q, valid_len_of(p, bi) - t0);
+    const int per = (p.hpg + p.nslice_k5 - 1) / p.nslice_k5;
+    const int h_begin = g * p.hpg + slice * per;
+    const int h_end = min(g * p.hpg + p.hpg, h_begin + per);
+    const int nh = h_end - h_begin;
+    bf16 *DX = (bf16 *)p.dx;
+    if (nh <= 0) return;
+    if (vrows <= 0) {  // dx, ddt_main, d_delta were zeroed by the K3 backward kernel
+        for (int hh = h_begin; hh < h_end; ++hh) {
+            const size_t cb = ix_chunk(p, bi, hh, c) * Q;
+            for (int i = tid; i < Q; i += kThreadsWide) p.dcum_main[cb + i] = 0.f;
+            if (tid == 0) p.dD_part[((size_t)bi * p.n + c) * p.H + hh] = 0.f;
+        }
+        return;
+    }
+    auto tile_of = [&](int mb, int tj) -> uint8_t * {  // CB^T tile of s-block mb, t-tile tj (tj >= 2 mb)
+        return CBt + (mb == 0 ? tj : (Q / 64) + tj - 2) * kTile;
+    };
+    auto load_raw = [&](int h, int b) {
+        float *f = fbuf + b * FST;
+        const float *cumg = p.cumA + ix_chunk(p, bi, h, c) * Q;
+        for (int l = tid; l < Q; l += kThreadsWide) {
+            f[l] = cumg[l];
+            f[Q + l] = l < vrows ? p.dt[ix_dt(p, bi, h, t0 + l)] : 0.f;
+        }
+    };
+    // pivot tables from the raw cumA (visible after a barrier)
+    auto derive = [&](int b) {
+        float *f = fbuf + b * FST;
+        // E[sg][t] = exp(cumA_t - cumA[64 sg + 63]) for t >= 64 (sg + 1); rows packed at 0, 192, 320
+        for (int i = tid; i < 384; i += kThreadsWide) {
+            const int sg = i < 192 ? 0 : (i < 320 ? 1 : 2);
+            const int base = sg == 0 ? 0 : (sg == 1 ? 192 : 320);
+            const int t = 64 * (sg + 1) + (i - base);
+            f[EOFF + i] = (sg < Q / 64 - 1 && t < Q) ? __expf(f[t] - f[64 * sg + 63]) : 0.f;
+        }
+        // E16[v][tt] = exp(cumA_t - cumA[16 v + 15]) for t = 64 (v / 4) + tt in v's 64-group
+        for (int i = tid; i < 1024; i += kThreadsWide) {
+            const int v = i >> 6, tt = i & 63;
+            const int t = 64 * (v >> 2) + tt;
+            f[E16OFF + i] = (16 * v < Q && t < Q && t > 16 * v + 15) ? __expf(f[t] - f[16 * v + 15]) : 0.f;
+        }
+        for (int j = tid; j < Q / 64; j += kThreadsWide) f[POFF + j] = f[64 * j + 63];
+        for (int j = tid; j < Q / 16; j += kThreadsWide) f[P16OFF + j] = f[16 * j + 15];
+    };
+    auto issue_x = [&](int h) {
+        mbar_arrive_expect_tx(&bar_x, XB);
+        for (int j = 0; j < NT; ++j) tma_load_4d(xs + j * kTile, &maps.x, &bar_x, 0, h, t0 + 128 * j, bi);
+    };
+    auto issue_dy = [&](int k) {
+        const int h = h_begin + k, b = k & 1;
+        mbar_arrive_expect_tx(&bar_dy[b], XB);
+        for (int j = 0; j < NT; ++j)
+            tma_load_4d(dys + b * XB + j * kTile, &maps.dy, &bar_dy[b], 0, h, t0 + 128 * j, bi);
+    };
+    if (tid == 0) {
+        mbar_init(&bar_res, 1);
+        mbar_init(&bar_x, 1);
+        mbar_init(&bar_dy[0], 1);
+        mbar_init(&bar_dy[1], 1);
+        mbar_init(&bar_m1, 1);
+        mbar_init(&bar_m2, 1);
+        mbar_fence_init();
+    }
+    if (warp == 0) tmem_alloc(&s_tmem, NCOL);
+    tc_sync();
+    const uint32_t tm = s_tmem;
+    if (tid == 0) {
+        mbar_arrive_expect_tx(&bar_res, NCBT * kTile);
+        const int cbrow = ((bi * p.n + c) * p.G + g) * Q;
+        for (int mb = 0; mb < NT; ++mb)
+            for (int tj = 2 * mb; tj < Q / 64; ++tj)
+                tma_load_2d(tile_of(mb, tj), &maps.cbt, &bar_res, 64 * tj, cbrow + 128 * mb);
+        issue_x(h_begin);
+        issue_dy(0);
+        if (nh > 1) issue_dy(1);
+    }
+    load_raw(h_begin, 0);
+    int x_iss = 1, x_land = 0, dy_iss = nh > 1 ? 2 : 1, dy_land = 0;
+    bool ok = wait_all(&bar_res, 0, true);
+    derive(0);
+    for (int k = 0; k < nh && ok; ++k) {
+        const int h = h_begin + k, sb = k & 1;
+        const float *f = fbuf + sb * FST;
+        const float *cum = f, *dts = f + Q, *E = f + EOFF, *E16 = f + E16OFF, *piv = f + POFF, *piv16 = f + P16OFF;
+        uint8_t *dyb = dys + sb * XB;
+        // ---- x_k, dy_k landed; dD partial; padded rows zeroed
+        ok = mbar_wait(&bar_x, (uint32_t)(k & 1)) && ok;
+        ok = mbar_wait(&bar_dy[sb], (uint32_t)((k >> 1) & 1)) && ok;
+        if (ok) {
+            x_land = k + 1;
+            dy_land = k + 1;
+        }
+        if (vrows < Q) {
+            __syncthreads();
+            zero_rows_from(xs, Q, vrows);
+            zero_rows_from(dyb, Q, vrows);
+            fence_async_smem();
+        }
+        tc_fence_before();
+        ok = __syncthreads_and(ok ? 1 : 0) != 0;  // also: tables of head k derived, previous head done
+        tc_fence_after();
+        if (!ok) break;
+        if (tid == 0) {
+            for (int mb = 0; mb < NT; ++mb) {
+                const uint32_t id = idesc_bf16(128, Q - 128 * mb, false, false);
+                for (int ks = 0; ks < kP / 16; ++ks)
+                    mma_bf16(tm + (mb == 0 ? 0u : 256u), sdesc_kmajor(smem_u32(xs + mb * kTile), ks, XB),
+                             sdesc_kmajor(smem_u32(dyb + mb * kTile), ks, XB), id, ks > 0);
+            }
+            mma_commit(&bar_m1);
+        }
+        {   // dD partial while the MMA runs
+            float dd = 0.f;
+            for (int mb = 0; mb < NT; ++mb) {
+                const int s = mb * 128 + 32 * q4 + lane;
 #pragma unroll
-                for (int j4 = 0; j4 < 8; ++j4) {
-                    float4 cv = make_float4(0.f, 0.f, 0.f, 0.f);
-                    if (tv && s0 + 4 * j4 <= t) cv = *reinterpret_cast<const float4 *>(cbrow + 4 * j4);
-                    const float cvv[4] = {cv.x, cv.y, cv.z, cv.w};
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int j = 4 * j4 + e, s = s0 + j;
-                        float gg = 0.f, w = 0.f;
-                        if (tv && s <= t && s < vrows) {
-                            const float cbd = cvv[e] * __expf(ct - cum[s]);
-                            gg = dw[j] * cbd;
-                            w = cbd * dts[s];
-                        }
-                        gsum[j] = gg;
-                        dsum[j] = gg * dts[s];
-                        wv[j] = w;
-                        rowsum += gg * dts[s];
-                    }
-                }
-                // column sums over the warp's 32 rows: butterfly transpose-reduce
-#pragma unroll
-                for (int off = 16; off >= 1; off >>= 1) {
-#pragma unroll
-                    for (int j = 0; j < off; ++j) {
-                        const bool upper = (lane & off) != 0;
-                        const float send_g = upper ? gsum[j] : gsum[j + off];
-                        const float send_d = upper ? dsum[j] : dsum[j + off];
-                        const float rg = __shfl_xor_sync(0xffffffffu, send_g, off);
-                        const float rd = __shfl_xor_sync(0xffffffffu, send_d, off);
-                        if (upper) {
-                            gsum[j] = gsum[j + off] + rg;
-                            dsum[j] = dsum[j + off] + rd;
-                        } else {
-                            gsum[j] = gsum[j] + rg;
-                            dsum[j] = dsum[j] + rd;
-                        }
-                    }
-                }
-                // lane now holds column s0 + lane in gsum[0], dsum[0]
-                colp[((tb * 4 + warp) * 2 + 0) * Q + s0 + lane] = gsum[0];
-                colp[((tb * 4 + warp) * 2 + 1) * Q + s0 + lane] = dsum[0];
-                // W values into the MN-major tile of s-block mb = s0 / 128
-                const int mb = s0 / 128;
-                const uint32_t mbase = (mb == 0) ? 0u : (uint32_t)(2 * Q * 128);
-                const uint32_t blk = (uint32_t)((Q - 128 * mb) * 128);  // bytes per 64-column block
-                const int wrow = t - 128 * mb;
-                if (wrow >= 0) {
-                    const int sb = (s0 % 128) / 64;       // which 64-column block of the pair
-                    const int c8b = (s0 % 64) / 8;         // first chunk of the 32 columns
-                    const uint32_t base = smem_u32(Ws) + mbase + sb * blk;
-#pragma unroll
-                    for (int q4 = 0; q4 < 4; ++q4)
-                        st_shared_v4(base + sw128_chunk(wrow, c8b + q4), pack_bf2(wv[8 * q4], wv[8 * q4 + 1]),
-                                     pack_bf2(wv[8 * q4 + 2], wv[8 * q4 + 3]), pack_bf2(wv[8 * q4 + 4], wv[8 * q4 + 5]),
-                                     pack_bf2(wv[8 * q4 + 6], wv[8 * q4 + 7]));
+                for (int c8 = 0; c8 < 4; ++c8) {
+                    const uint4 xv = ld_shared_v4(smem_u32(xs) + sw128_chunk(s, 4 * hf + c8));
+                    const uint4 dv = ld_shared_v4(smem_u32(dyb) + sw128_chunk(s, 4 * hf + c8));
+                    dd += bf_lo(xv.x) * bf_lo(dv.x) + bf_hi(xv.x) * bf_hi(dv.x) + bf_lo(xv.y) * bf_lo(dv.y) +
+                          bf_hi(xv.y) * bf_hi(dv.y) + bf_lo(xv.z) * bf_lo(dv.z) + bf_hi(xv.z) * bf_hi(dv.z) +
+                          bf_lo(xv.w) * bf_lo(dv.w) + bf_hi(xv.w) * bf_hi(dv.w);
                 }
             }
-            tgt[t] = rowsum;
+            dd = warp_sum(dd);
+            if (lane == 0) red[warp] = dd;
         }
-    }
-    fence_async_smem();
-    tc_sync();
-    // ---- phase 3: dx = W^T dy into the freed dW columns
-    if (tid == 0 && ok) {
-        const uint32_t id = idesc_bf16(128, 64, true, true);
+        if (k + 1 < nh) load_raw(h + 1, sb ^ 1);
+        ok = mbar_wait(&bar_m1, (uint32_t)(k & 1)) && ok;
+        tc_fence_after();
+        // x is free once dW^T is computed: refill with the next head
+        if (tid == 0 && ok && k + 1 < nh) issue_x(h + 1);
+        if (k + 1 < nh) x_iss = k + 2;
+        // ---- epilogue 1: W^T in place, ddt_orange row sums, target column partials
         for (int mb = 0; mb < NT; ++mb) {
-            const uint32_t mbase = (mb == 0) ? 0u : (uint32_t)(2 * Q * 128);
-            const uint32_t blk = (uint32_t)((Q - 128 * mb) * 128);
-            const int nks = (Q - 128 * mb) / 16;
-            for (int ks = 0; ks < nks; ++ks)
-                mma_bf16(tm + mb * 64, sdesc_mnmajor(smem_u32(Ws) + mbase, ks, blk),
-                         sdesc_mnmajor(smem_u32(DYs) + (uint32_t)(128 * mb * 128), ks, XB), id, ks > 0);
+            const int sl = 32 * q4 + lane, s = 128 * mb + sl;
+            const int sg = s >> 6, u16 = (s & 63) >> 4;
+            const float cs = cum[s], ds = dts[s];
+            const float fs0 = __expf(piv[sg] - cs);           // off-diagonal row factor
+            const float f160 = __expf(piv16[s >> 4] - cs);    // in-group row factor
+            const float *Erow = E + (sg == 0 ? 0 : (sg == 1 ? 192 : 320)) - 64 * (sg + 1);  // Erow[t]
+            const float *E16row = E16 + 64 * (s >> 4) - 64 * sg;                            // E16row[t]
+            const uint32_t dwc = mb == 0 ? 0u : 256u;
+            float a_ddt = 0.f;  // sum_t dW^T CB^T decay  (ddt_orange; src = dt_s * this)
+            for (int j = hf; j < (Q - 128 * mb) / 64; j += 2) {  // 64-wide t chunks, alternate halves
+                const int tc0 = 128 * mb + 64 * j, tg = tc0 >> 6;
+                float dw[64];
+                tmem_ld32(tmem_addr(tm, 32 * q4, dwc + 64 * j), dw);
+                tmem_ld32(tmem_addr(tm, 32 * q4, dwc + 64 * j + 32), dw + 32);
+                float pk[32];
+                float col[64];
+                if (tg < sg) {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) pk[i] = 0.f;
+#pragma unroll
+                    for (int i = 0; i < 64; ++i) col[i] = 0.f;
+                } else {
+                    const uint32_t cbb = smem_u32(tile_of(mb, tg));
+#pragma unroll
+                    for (int c8 = 0; c8 < 8; ++c8) {
+                        const uint4 u = ld_shared_v4(cbb + sw128_chunk(sl, c8));
+                        const float cv[8] = {bf_lo(u.x), bf_hi(u.x), bf_lo(u.y), bf_hi(u.y),
+                                             bf_lo(u.z), bf_hi(u.z), bf_lo(u.w), bf_hi(u.w)};
+                        float w[8];
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) {
+                            const int t = tc0 + 8 * c8 + e;
+                            float cbd;  // CB^T[s, t] exp(cumA_t - cumA_s), t >= s
+                            if (tg > sg) {
+                                cbd = cv[e] * Erow[t] * fs0;
+                            } else {
+                                const int ut = (t & 63) >> 4;
+                                if (ut > u16) cbd = cv[e] * E16row[t] * f160;
+                                else if (ut == u16) cbd = t >= s ? cv[e] * __expf(cum[t] - cs) : 0.f;
+                                else cbd = 0.f;
+                            }
+                            const float gv = dw[8 * c8 + e] * cbd;
+                            a_ddt += gv;
+                            col[8 * c8 + e] = gv * ds;  // dW^T W^T
+                            w[e] = cbd * ds;            // W^T
+                        }
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) pk[4 * c8 + e] = __uint_as_float(pack_bf2(w[2 * e], w[2 * e + 1]));
+                    }
+                }
+                tmem_st32(tmem_addr(tm, 32 * q4, dwc + 64 * j), pk);  // W^T of this chunk, packed, in place
+                // target partials: transpose-reduce each 32-column half across the warp
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh) {
+                    float *cc = col + 32 * hh;
+#pragma unroll
+                    for (int off = 16; off >= 1; off >>= 1) {
+#pragma unroll
+                        for (int i = 0; i < off; ++i) {
+                            const bool upper = (lane & off) != 0;
+                            const float send = upper ? cc[i] : cc[i + off];
+                            const float r = __shfl_xor_sync(0xffffffffu, send, off);
+                            cc[i] = (upper ? cc[i + off] : cc[i]) + r;
+                        }
+                    }
+                    colp[(mb * 4 + q4) * Q + tc0 + 32 * hh + lane] = cc[0];
+                }
+            }
+            rowp[hf * Q + s] = a_ddt;
         }
-        mma_commit(&bar_mma2);
-    }
-    ok = wait_all(&bar_mma2, 0, ok);
-    tc_fence_after();
-    // ---- phase 4: dx and per-token outputs
-    if (ok) {
+        tc_fence_before();
+        ok = __syncthreads_and(ok ? 1 : 0) != 0;
+        tc_fence_after();
+        // ---- dx = W^T dy (A = W^T packed in TMEM; B = dy MN-major, rows t >= 128 mb)
+        if (tid == 0 && ok) {
+            const uint32_t id = idesc_bf16(128, 64, false, true);
+            for (int mb = 0; mb < NT; ++mb) {
+                const uint32_t dwc = mb == 0 ? 0u : 256u;
+                for (int ks = 0; ks < (Q - 128 * mb) / 16; ++ks)
+                    mma_bf16_tmem_a(tm + DXCOL + 64 * mb, tm + dwc + 64 * (ks >> 2) + 8 * (ks & 3),
+                                    sdesc_mnmajor(smem_u32(dyb) + (uint32_t)(128 * mb * 128), ks, XB), id, ks > 0);
+            }
+            mma_commit(&bar_m2);
+        }
+        // D dy slices of this head (dy_k is refilled only after these MMAs complete)
+        uint4 dyr[NT][4];
+#pragma unroll
+        for (int mb = 0; mb < NT; ++mb) {
+            const int s = 128 * mb + 32 * q4 + lane;
+#pragma unroll
+            for (int c8 = 0; c8 < 4; ++c8) dyr[mb][c8] = ld_shared_v4(smem_u32(dyb) + sw128_chunk(s, 4 * hf + c8));
+        }
+        if (k + 1 < nh) derive(sb ^ 1);  // raw scalars of head k + 1 visible since the last barrier
+        ok = mbar_wait(&bar_m2, (uint32_t)(k & 1)) && ok;
+        tc_fence_after();
+        tc_fence_before();
+        ok = __syncthreads_and(ok ? 1 : 0) != 0;  // every thread has its dy slices
+        tc_fence_after();
+        if (tid == 0 && ok && k + 2 < nh) issue_dy(k + 2);
+        if (k + 2 < nh) dy_iss = k + 3;
+        // ---- epilogue 2: dx += W^T dy + D dy (dx holds the K3 term)
         const float Dh = p.D[h];
         for (int mb = 0; mb < NT; ++mb) {
-            const int s = mb * 128 + 32 * warp + lane;
-            float acc[64], u[64], dyv[64];
-            tmem_ld32(tmem_addr(tm, 32 * warp, mb * 64), acc);
-            tmem_ld32(tmem_addr(tm, 32 * warp, mb * 64 + 32), acc + 32);
-            tmem_ld32(tmem_addr(tm, 32 * warp, UCOL + mb * 64), u);
-            tmem_ld32(tmem_addr(tm, 32 * warp, UCOL + mb * 64 + 32), u + 32);
-            if (t0 + s < p.L) {
-                if (s < vrows) {
-                    load_row64(DYs, s, dyv);
-                    const float bbs = dts[s] * dec_end[s];
+            const int s = 128 * mb + 32 * q4 + lane;
+            float acc[32];
+            tmem_ld32(tmem_addr(tm, 32 * q4, DXCOL + 64 * mb + 32 * hf), acc);
+            if (t0 + s < p.L && s < vrows) {
+                bf16 *dst = DX + ix_x(p, bi, t0 + s, h, 32 * hf);
 #pragma unroll
-                    for (int j = 0; j < 64; ++j) acc[j] = acc[j] + bbs * u[j] + Dh * dyv[j];
-                } else {
-#pragma unroll
-                    for (int j = 0; j < 64; ++j) acc[j] = 0.f;
+                for (int c8 = 0; c8 < 4; ++c8) {
+                    const uint4 prev = reinterpret_cast<const uint4 *>(dst)[c8];
+                    const uint4 dv = dyr[mb][c8];
+                    float *a = acc + 8 * c8;
+                    a[0] += Dh * bf_lo(dv.x) + bf_lo(prev.x); a[1] += Dh * bf_hi(dv.x) + bf_hi(prev.x);
+                    a[2] += Dh * bf_lo(dv.y) + bf_lo(prev.y); a[3] += Dh * bf_hi(dv.y) + bf_hi(prev.y);
+                    a[4] += Dh * bf_lo(dv.z) + bf_lo(prev.z); a[5] += Dh * bf_hi(dv.z) + bf_hi(prev.z);
+                    a[6] += Dh * bf_lo(dv.w) + bf_lo(prev.w); a[7] += Dh * bf_hi(dv.w) + bf_hi(prev.w);
                 }
-                store_row64_bf16(DX + ix_x(p, bi, t0 + s, h, 0), acc);
+                store_row32_bf16(dst, acc);
             }
         }
-        for (int s = tid; s < Q; s += kThreads) {
-            float ddo = 0.f, src = 0.f;
-            for (int tb = 0; tb < NT; ++tb)
-                for (int w = 0; w < 4; ++w) {
-                    ddo += colp[((tb * 4 + w) * 2 + 0) * Q + s];
-                    src += colp[((tb * 4 + w) * 2 + 1) * Q + s];
-                }
-            const float dbb = s < vrows ? dbbs[s] : 0.f;
-            const float ddelta = dbb * dts[s] * dec_end[s];
-            p.ddt_main[cbase + s] = ddo + dbb * dec_end[s];
-            p.d_delta[cbase + s] = ddelta;
-            p.dcum_main[cbase + s] = tgt[s] - src - ddelta;
+        // ---- per-token outputs of head k
+        const size_t cbase = ix_chunk(p, bi, h, c) * Q;
+        for (int q = tid; q < Q; q += kThreadsWide) {
+            float tgt = 0.f;
+            for (int mb = 0; mb < NT; ++mb)
+                if (q >= 128 * mb)
+                    for (int w = 0; w < 4; ++w) tgt += colp[(mb * 4 + w) * Q + q];
+            const float ddo = rowp[q] + rowp[Q + q];   // ddt_orange
+            const float src = dts[q] * ddo;            // sum_t dW^T W^T
+            p.ddt_main[cbase + q] += ddo;
+            p.dcum_main[cbase + q] = tgt - src - p.d_delta[cbase + q];
         }
-        if (tid == 0) p.dD_part[((size_t)bi * p.n + c) * p.H + h] = red[0] + red[1] + red[2] + red[3];
-    } else if (tid == 0) {
-        flag_timeout(p);
+        if (tid == 0) {
+            float d = 0.f;
+            for (int w = 0; w < 8; ++w) d += red[w];
+            p.dD_part[((size_t)bi * p.n + c) * p.H + h] = d;
+        }
     }
+    if (!ok && tid == 0) flag_timeout(p);
+    if (x_iss > x_land) mbar_wait(&bar_x, (uint32_t)((x_iss - 1) & 1));
+    for (int k = dy_land; k < dy_iss; ++k) mbar_wait(&bar_dy[k & 1], (uint32_t)((k >> 1) & 1));
     tc_sync();
     if (warp == 0) tmem_dealloc(tm, NCOL);
 }
 
 // ====================================================================== group backward
-// G1: CTA per (b, chunk, group, head slice, t-block).  Accumulates, over the
-// slice's heads, d_cb[t, s] = sum_h dt_h[s] exp(cumA_h[t] - cumA_h[s]) dW_h[t, s]
-// (s <= t) in TMEM (dW_h = dy_h x_h^T by MMA each head), then writes the fp32
-// partial to the workspace.
+// G1: CTA per (b, chunk, group, head slice, t-block), 256 threads.  Accumulates,
+// over the slice's heads, d_cb[t, s] = sum_h dt_h[s] exp(cumA_h[t] - cumA_h[s]) dW_h[t, s]
+// (s <= t) in TMEM (dW_h = dy_h x_h^T by MMA each head, two-stage TMA ring),
+// then writes the fp32 partial to the workspace.  Off-diagonal 64 x 64 blocks
+// use the pivot factorisation of the decay (one exponential per row chunk).
 template <int Q>
-__global__ void __launch_bounds__(kThreads) tc_bwd_dcb_kernel(const Params p, const __grid_constant__ TcMaps maps) {
+__global__ void __launch_bounds__(kThreadsWide, 1) tc_bwd_dcb_kernel(const Params p, const __grid_constant__ TcMaps maps) {
     constexpr int NT = Q / 128;
     constexpr uint32_t STG = kTile * (1 + NT);  // dy rows (1 tile) + x rows (up to NT tiles)
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = align1024(smem_raw);
     float *cumv = reinterpret_cast<float *>(sm + 2 * STG);  // [2][Q]
-    float *dtv = cumv + 2 * Q;                              // [2][Q]
+    float *gcv = cumv + 2 * Q;                              // [2][Q]  dt * exp(piv - cumA)
+    float *dtv = gcv + 2 * Q;                               // [2][Q]
+    float *pivv = dtv + 2 * Q;                              // [2][8]
     __shared__ uint64_t bar_tma[2], bar_mma;
     __shared__ uint32_t s_tmem;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int q4 = warp & 3, hf = warp >> 2;
     int idx = blockIdx.x;
     const int tb = idx % NT;
     idx /= NT;
@@ -799,7 +1170,7 @@ __global__ void __launch_bounds__(kThreads) tc_bwd_dcb_kernel(const Params p, co
     const int h_end = min(g * p.hpg + p.hpg, h_begin + per);
     float *out = p.d_cb + ((size_t)slice * p.b * p.n * p.G + ((size_t)bi * p.n + c) * p.G + g) * (size_t)Q * Q;
     if (vrows <= 0 || h_begin >= h_end) {
-        for (int i = tid; i < 128 * ncols; i += kThreads)
+        for (int i = tid; i < 128 * ncols; i += kThreadsWide)
             out[(size_t)(tb * 128 + i / ncols) * Q + i % ncols] = 0.f;
         return;
     }
@@ -828,19 +1199,30 @@ __global__ void __launch_bounds__(kThreads) tc_bwd_dcb_kernel(const Params p, co
         if (nh > 1) issue(1);
     }
     bool ok = true;
-    const int t = tb * 128 + 32 * warp + lane;
-    const bool tv = t < vrows;
+    const int t = tb * 128 + 32 * q4 + lane;
+    const int tr = t >> 6;
+    const int drow = vrows - 128 * tb;  // valid rows of the dy tile
     for (int k = 0; k < nh && ok; ++k) {
         const int h = h_begin + k, st = k & 1;
-        float *cv = cumv + st * Q, *dv = dtv + st * Q;
+        float *cv = cumv + st * Q, *gv = gcv + st * Q, *dv = dtv + st * Q, *pv = pivv + st * 8;
         const float *cumg = p.cumA + ix_chunk(p, bi, h, c) * Q;
-        for (int l = tid; l < Q; l += kThreads) {
+        for (int l = tid; l < Q; l += kThreadsWide) {
             cv[l] = cumg[l];
             dv[l] = l < vrows ? p.dt[ix_dt(p, bi, h, t0 + l)] : 0.f;
         }
+        __syncthreads();
+        for (int j = tid; j < Q / 64; j += kThreadsWide) pv[j] = cv[64 * j + 63];
+        __syncthreads();
+        for (int l = tid; l < Q; l += kThreadsWide) gv[l] = dv[l] * __expf(pv[l >> 6] - cv[l]);
         tc_fence_before();
         ok = wait_all(&bar_tma[st], (uint32_t)((k >> 1) & 1), ok);
-        tc_fence_after();
+        if (ok && vrows < Q) {
+            uint8_t *dys = sm + st * STG, *xs = dys + kTile;
+            zero_rows_from(dys, 128, max(drow, 0));
+            zero_rows_from(xs, 128 * (tb + 1), vrows);
+            fence_async_smem();
+        }
+        tc_sync();
         if (tid == 0 && ok) {
             uint8_t *dys = sm + st * STG, *xs = dys + kTile;
             const uint32_t id = idesc_bf16(128, ncols, false, false);
@@ -855,17 +1237,27 @@ __global__ void __launch_bounds__(kThreads) tc_bwd_dcb_kernel(const Params p, co
         if (tid == 0 && ok && k + 2 < nh) issue(k + 2);
         if (ok) {
             const float ct = cv[t];
-            for (int s0 = 0; s0 < ncols; s0 += 32) {
+            for (int j = hf; j < ncols / 32; j += 2) {
+                const int s0 = 32 * j, sb = s0 >> 6;
                 float dw[32], acc[32];
-                tmem_ld32(tmem_addr(tm, 32 * warp, DW + s0), dw);
-                if (k > 0) tmem_ld32(tmem_addr(tm, 32 * warp, ACC + s0), acc);
+                tmem_ld32(tmem_addr(tm, 32 * q4, DW + s0), dw);
+                if (k > 0) tmem_ld32(tmem_addr(tm, 32 * q4, ACC + s0), acc);
+                else {
 #pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    const int s = s0 + j;
-                    const float v = (tv && s <= t && s < vrows) ? dw[j] * dv[s] * __expf(ct - cv[s]) : 0.f;
-                    acc[j] = (k > 0 ? acc[j] : 0.f) + v;
+                    for (int i = 0; i < 32; ++i) acc[i] = 0.f;
                 }
-                tmem_st32(tmem_addr(tm, 32 * warp, ACC + s0), acc);
+                if (sb < tr) {
+                    const float e = __expf(ct - pv[sb]);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) acc[i] += dw[i] * e * gv[s0 + i];
+                } else if (sb == tr) {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        const int s = s0 + i;
+                        acc[i] += s <= t ? dw[i] * dv[s] * __expf(ct - cv[s]) : 0.f;
+                    }
+                }
+                tmem_st32(tmem_addr(tm, 32 * q4, ACC + s0), acc);
             }
         }
         tc_fence_before();
@@ -874,12 +1266,13 @@ __global__ void __launch_bounds__(kThreads) tc_bwd_dcb_kernel(const Params p, co
     }
     if (ok) {
         float *orow = out + (size_t)t * Q;
-        for (int s0 = 0; s0 < ncols; s0 += 32) {
+        for (int j = hf; j < ncols / 32; j += 2) {
+            const int s0 = 32 * j;
             float v[32];
-            tmem_ld32(tmem_addr(tm, 32 * warp, ACC + s0), v);
+            tmem_ld32(tmem_addr(tm, 32 * q4, ACC + s0), v);
             float4 *dst = reinterpret_cast<float4 *>(orow + s0);
 #pragma unroll
-            for (int j = 0; j < 8; ++j) dst[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+            for (int i = 0; i < 8; ++i) dst[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
         }
     } else if (tid == 0) {
         flag_timeout(p);
@@ -896,7 +1289,7 @@ __global__ void __launch_bounds__(kThreads) tc_bwd_dcb_kernel(const Params p, co
 //                  dB += sum_h (x_h bbs_h) d_intra_h
 // and writes the fp32 partial sums of the slice.
 template <int Q>
-__global__ void __launch_bounds__(kThreads) tc_bwd_dbc_kernel(const Params p, const __grid_constant__ TcMaps maps) {
+__global__ void __launch_bounds__(kThreadsWide, 1) tc_bwd_dbc_kernel(const Params p, const __grid_constant__ TcMaps maps) {
     constexpr int NT = Q / 128;
     constexpr uint32_t XB = Q * 128, RB = Q * 128, SB = 64 * 128;
     constexpr uint32_t STG = 2 * XB + 4 * SB;  // dy, x, s_in (2 r-blocks), d_intra (2 r-blocks)
@@ -908,6 +1301,7 @@ __global__ void __launch_bounds__(kThreads) tc_bwd_dbc_kernel(const Params p, co
     __shared__ uint64_t bar_tma[2], bar_mma[2], bar_a;
     __shared__ uint32_t s_tmem;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int q4 = warp & 3, hf = warp >> 2;
     int idx = blockIdx.x;
     const int slice = idx % p.nslice;
     idx /= p.nslice;
@@ -923,7 +1317,7 @@ __global__ void __launch_bounds__(kThreads) tc_bwd_dbc_kernel(const Params p, co
     const bool do_k2 = slice == 0;
     const int nh = max(0, h_end - h_begin);
     if (vrows <= 0 || (!do_k2 && nh == 0)) {
-        for (int i = tid; i < Q * kN; i += kThreads) {
+        for (int i = tid; i < Q * kN; i += kThreadsWide) {
             outC[i] = 0.f;
             outB[i] = 0.f;
         }
@@ -954,7 +1348,7 @@ __global__ void __launch_bounds__(kThreads) tc_bwd_dbc_kernel(const Params p, co
         }
         const size_t cstride = (size_t)p.b * p.n * p.G * Q * Q;
         const float *part = p.d_cb + (((size_t)bi * p.n + c) * p.G + g) * (size_t)Q * Q;
-        for (int i = tid; i < Q * (Q / 8); i += kThreads) {
+        for (int i = tid; i < Q * (Q / 8); i += kThreadsWide) {
             const int t = i / (Q / 8), s0 = 8 * (i % (Q / 8));
             float v[8];
 #pragma unroll
@@ -1051,7 +1445,7 @@ __global__ void __launch_bounds__(kThreads) tc_bwd_dbc_kernel(const Params p, co
         float *ec = fv + st * 2 * Q, *bb = ec + Q;
         const float *cumg = p.cumA + ix_chunk(p, bi, h, c) * Q;
         const float cend = p.endA[ix_chunk(p, bi, h, c)];
-        for (int l = tid; l < Q; l += kThreads) {
+        for (int l = tid; l < Q; l += kThreadsWide) {
             const float cl = cumg[l];
             const bool v = l < vrows;
             ec[l] = v ? __expf(cl) : 0.f;
@@ -1096,14 +1490,14 @@ __global__ void __launch_bounds__(kThreads) tc_bwd_dbc_kernel(const Params p, co
     tc_fence_after();
     if (ok) {
         for (int tb = 0; tb < NT; ++tb) {
-            const int t = tb * 128 + 32 * warp + lane;
-            for (int r0 = 0; r0 < kN; r0 += 32) {
+            const int t = tb * 128 + 32 * q4 + lane;
+            for (int r0 = 64 * hf; r0 < 64 * hf + 64; r0 += 32) {
                 float v[32];
-                tmem_ld32(tmem_addr(tm, 32 * warp, tb * 128 + r0), v);
+                tmem_ld32(tmem_addr(tm, 32 * q4, tb * 128 + r0), v);
                 float4 *dC = reinterpret_cast<float4 *>(outC + (size_t)t * kN + r0);
 #pragma unroll
                 for (int j = 0; j < 8; ++j) dC[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
-                tmem_ld32(tmem_addr(tm, 32 * warp, DBCOL + tb * 128 + r0), v);
+                tmem_ld32(tmem_addr(tm, 32 * q4, DBCOL + tb * 128 + r0), v);
                 float4 *dB = reinterpret_cast<float4 *>(outB + (size_t)t * kN + r0);
 #pragma unroll
                 for (int j = 0; j < 8; ++j) dB[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
@@ -1200,6 +1594,13 @@ cudaError_t make_maps(const Params &p, TcMaps *mp, bool backward) {
     if ((e = map_tokens(&mp->B, p.B, p.b, p.L, p.G, kN)) != cudaSuccess) return e;
     if ((e = map_tokens(&mp->C, p.C, p.b, p.L, p.G, kN)) != cudaSuccess) return e;
     if (p.states_bf && (e = map_states(&mp->st, p.states_bf, (long long)p.b * p.n * p.H)) != cudaSuccess) return e;
+    if (p.CBh) {  // CB and CB^T, bf16 [b*n*G*Q rows][Q]: boxes of 64 columns x 128 rows
+        cuuint64_t dims[2] = {(cuuint64_t)p.Q, (cuuint64_t)p.b * p.n * p.G * p.Q};
+        cuuint64_t strides[1] = {(cuuint64_t)p.Q * 2};
+        cuuint32_t box[2] = {64, 128};
+        if ((e = encode(&mp->cb, p.CBh, 2, dims, strides, box)) != cudaSuccess) return e;
+        if ((e = encode(&mp->cbt, p.CBt, 2, dims, strides, box)) != cudaSuccess) return e;
+    }
     if (backward) {
         if ((e = map_tokens(&mp->dy, p.dy, p.b, p.L, p.H, kP)) != cudaSuccess) return e;
         if (p.dstates_bf && (e = map_states(&mp->dst, p.dstates_bf, (long long)p.b * p.n * p.H)) != cudaSuccess)
@@ -1209,35 +1610,42 @@ cudaError_t make_maps(const Params &p, TcMaps *mp, bool backward) {
 }
 
 template <typename K>
-cudaError_t launch(K kernel, unsigned grid, size_t smem, cudaStream_t s, const Params &p, const TcMaps &maps) {
+cudaError_t launch(K kernel, unsigned grid, size_t smem, cudaStream_t s, const Params &p, const TcMaps &maps,
+                   int threads = kThreads) {
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    kernel<<<grid, kThreads, smem, s>>>(p, maps);
+    kernel<<<grid, threads, smem, s>>>(p, maps);
     return cudaGetLastError();
 }
 
 constexpr size_t smem_k2(int Q) { return 1024 + 4 * (size_t)Q * 128; }
 constexpr size_t smem_k3(int Q) { return 1024 + 3 * (size_t)Q * 128 + 4 * Q; }
 constexpr size_t smem_k5(int Q) {
-    return 1024 + 3 * (size_t)Q * 128 + 2 * 64 * 128 + (size_t)kTile * 2 * ((Q / 128) * (Q / 128 + 1) / 2) + 8 * Q;
+    return 1024 + 3 * (size_t)Q * 128 + 2 * 64 * 128 + (size_t)kTile * (Q / 128) * (Q / 128 + 1) +
+           4 * 4 * (4 * Q + 24);
 }
 constexpr size_t smem_blue(int Q) { return 1024 + 3 * (size_t)Q * 128 + 2 * 64 * 128 + 4 * Q; }
-constexpr size_t smem_main(int Q) {
-    return 1024 + 4 * (size_t)Q * 128 + 2 * 64 * 128 + 4 * (5 * Q + (Q / 128) * 4 * 2 * Q + 4);
+constexpr size_t smem_k3bwd(int Q) {
+    return 1024 + 2 * (size_t)Q * 128 + 2 * ((size_t)Q * 128 + 2 * 64 * 128) + 4 * (3 * 3 * Q + 2 * Q);
+}
+constexpr size_t smem_orange(int Q) {
+    return 1024 + (size_t)kTile * (Q == 256 ? 6 : 2) + 3 * (size_t)Q * 128 +
+           4 * (2 * (2 * Q + 384 + 1024 + 24) + (Q / 128) * 4 * Q + 2 * Q + 8);
 }
 // Padded above half of the SM's shared memory: a CTA holding 512 TMEM columns
 // must never share its SM with another CTA of the same kernel.
 constexpr size_t smem_dcb(int Q) {
-    return (1024 + 2 * (size_t)kTile * (1 + Q / 128) + 4 * 4 * Q) > 120 * 1024
-               ? 1024 + 2 * (size_t)kTile * (1 + Q / 128) + 4 * 4 * Q
+    return (1024 + 2 * (size_t)kTile * (1 + Q / 128) + 4 * (6 * Q + 16)) > 120 * 1024
+               ? 1024 + 2 * (size_t)kTile * (1 + Q / 128) + 4 * (6 * Q + 16)
                : 120 * 1024;
 }
 constexpr size_t smem_dbc(int Q) {
     return 1024 + 2 * (2 * (size_t)Q * 128 + 4 * 64 * 128) + 4 * 4 * Q;
 }
-static_assert(smem_main(256) <= 232448 && smem_main(256) > 116 * 1024, "main backward: one CTA per SM");
+static_assert(smem_orange(256) <= 232448 && smem_orange(256) > 116 * 1024, "ORANGE backward: one CTA per SM");
+static_assert(smem_k3bwd(256) <= 232448 && smem_k3bwd(256) > 116 * 1024, "K3 backward: one CTA per SM");
 static_assert(smem_k2(256) > 116 * 1024, "K2 (512 TMEM columns): one CTA per SM");
-static_assert(smem_k5(256) <= 232448, "K5 shared memory");
+static_assert(smem_k5(256) <= 232448 && smem_k5(256) > 116 * 1024, "K5: one CTA per SM");
 static_assert(smem_dbc(256) <= 232448, "group backward shared memory");
 static_assert(2 * (size_t)256 * 256 + 2 * 256 * 128 <= 2 * (2 * (size_t)256 * 128 + 4 * 64 * 128),
               "d_cb + B tile must fit the two long-K stages");
@@ -1253,6 +1661,17 @@ int tc_dcb_slices(const ssd_dims &d) {
     long long s = (2 * 152 + ctas - 1) / ctas;
     if (s < 1) s = 1;
     if (s > hpg) s = hpg;
+    return (int)s;
+}
+int tc_k5_slices(const ssd_dims &d) {
+    // about 8 heads per CTA (the resident C / CB loads amortise over them),
+    // but at least two CTAs per SM
+    const long long hpg = d.nheads / d.ngroups;
+    const long long n = (d.seqlen + d.chunk_len - 1) / d.chunk_len;
+    const long long groups = d.batch * n * d.ngroups;
+    long long s = (hpg + 7) / 8;
+    while (s < hpg && groups * s < 2 * 152) ++s;
+    if (s < 1) s = 1;
     return (int)s;
 }
 int tc_group_slices(const ssd_dims &d) {
@@ -1291,8 +1710,8 @@ cudaError_t launch_tc_k5(const Params &p, cudaStream_t s) {
     TcMaps m;
     cudaError_t e = make_maps(p, &m, false);
     if (e != cudaSuccess) return e;
-    const unsigned grid = (unsigned)(p.b * p.n * p.H);
-#define CALL(Q) launch(tc_k5_kernel<Q>, grid, smem_k5(Q), s, p, m)
+    const unsigned grid = (unsigned)(p.b * p.n * p.G * p.nslice_k5);
+#define CALL(Q) launch(tc_k5_kernel<Q>, grid, smem_k5(Q), s, p, m, kThreadsWide)
     return SSD_TC_DISPATCH(p.Q, CALL);
 #undef CALL
 }
@@ -1307,12 +1726,22 @@ cudaError_t launch_tc_bwd_blue(const Params &p, cudaStream_t s) {
 #undef CALL
 }
 
-cudaError_t launch_tc_bwd_main(const Params &p, cudaStream_t s) {
+cudaError_t launch_tc_bwd_k3(const Params &p, cudaStream_t s) {
     TcMaps m;
     cudaError_t e = make_maps(p, &m, true);
     if (e != cudaSuccess) return e;
-    const unsigned grid = (unsigned)(p.b * p.n * p.H);
-#define CALL(Q) launch(tc_bwd_main_kernel<Q>, grid, smem_main(Q), s, p, m)
+    const unsigned grid = (unsigned)(p.b * p.n * p.G * p.nslice_k5);
+#define CALL(Q) launch(tc_bwd_k3_kernel<Q>, grid, smem_k3bwd(Q), s, p, m, kThreadsWide)
+    return SSD_TC_DISPATCH(p.Q, CALL);
+#undef CALL
+}
+
+cudaError_t launch_tc_bwd_orange(const Params &p, cudaStream_t s) {
+    TcMaps m;
+    cudaError_t e = make_maps(p, &m, true);
+    if (e != cudaSuccess) return e;
+    const unsigned grid = (unsigned)(p.b * p.n * p.G * p.nslice_k5);
+#define CALL(Q) launch(tc_bwd_orange_kernel<Q>, grid, smem_orange(Q), s, p, m, kThreadsWide)
     return SSD_TC_DISPATCH(p.Q, CALL);
 #undef CALL
 }
@@ -1323,8 +1752,8 @@ cudaError_t launch_tc_bwd_group(const Params &p, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     const unsigned g1 = (unsigned)(p.b * p.n * p.G * p.nslice_cb * (p.Q / 128));
     const unsigned g2 = (unsigned)(p.b * p.n * p.G * p.nslice);
-#define CALL1(Q) launch(tc_bwd_dcb_kernel<Q>, g1, smem_dcb(Q), s, p, m)
-#define CALL2(Q) launch(tc_bwd_dbc_kernel<Q>, g2, smem_dbc(Q), s, p, m)
+#define CALL1(Q) launch(tc_bwd_dcb_kernel<Q>, g1, smem_dcb(Q), s, p, m, kThreadsWide)
+#define CALL2(Q) launch(tc_bwd_dbc_kernel<Q>, g2, smem_dbc(Q), s, p, m, kThreadsWide)
     if ((e = SSD_TC_DISPATCH(p.Q, CALL1)) != cudaSuccess) return e;
     if ((e = SSD_TC_DISPATCH(p.Q, CALL2)) != cudaSuccess) return e;
 #undef CALL1

@@ -12,13 +12,16 @@ int tc_dD_per(int64_t Q);
 // Head slices of the group-level backward: d_cb partial sums (first) and the
 // dB / dC partial sums (second).
 int tc_dcb_slices(const ssd_dims &d);
+// Head slices of the persistent per-group kernels (K5, K3 and ORANGE backward).
+int tc_k5_slices(const ssd_dims &d);
 int tc_group_slices(const ssd_dims &d);
 
 cudaError_t launch_tc_k2(const Params &p, cudaStream_t s);
 cudaError_t launch_tc_k3(const Params &p, cudaStream_t s);
 cudaError_t launch_tc_k5(const Params &p, cudaStream_t s);
 cudaError_t launch_tc_bwd_blue(const Params &p, cudaStream_t s);
-cudaError_t launch_tc_bwd_main(const Params &p, cudaStream_t s);
+cudaError_t launch_tc_bwd_k3(const Params &p, cudaStream_t s);
+cudaError_t launch_tc_bwd_orange(const Params &p, cudaStream_t s);
 cudaError_t launch_tc_bwd_group(const Params &p, cudaStream_t s);
 
 }  // namespace ssd
