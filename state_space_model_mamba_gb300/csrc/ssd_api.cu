@@ -318,8 +318,8 @@ ssd_status ssd_backward(const ssd_dims *dims, ssd_dtype dtype, const void *x, co
         if (tc) {
             SSD_LAUNCH("bwd_blue_tc", launch_tc_bwd_blue(p, s), 1);
             SSD_LAUNCH("bwd_k4_state_passing", launch_bwd_k4(p, s), 1);
-            SSD_LAUNCH("bwd_k3_tc", launch_tc_bwd_k3(p, s), 1);
             SSD_LAUNCH("bwd_orange_tc", launch_tc_bwd_orange(p, s), 1);
+            SSD_LAUNCH("bwd_k3_tc", launch_tc_bwd_k3(p, s), 1);
             SSD_LAUNCH("bwd_group_tc", launch_tc_bwd_group(p, s), 3);
         } else {
             SSD_LAUNCH("bwd_blue_simt", launch_simt_bwd_blue<bf16>(p, s), 2);

@@ -657,9 +657,11 @@ __global__ void __launch_bounds__(kThreads) tc_bwd_blue_kernel(const Params p, c
 // (the K3 BACKWARD block, with the per-head d_b_scaled folded away):
 //   U[s, p]   = sum_r B[s, r] d_intra[p, r]           (TMEM, A = B K-major, B = d_intra K-major)
 //   d_bbs[s]  = sum_p x[s, p] U[s, p]
-//   dx        = bbs[s] U[s, p]                        (first writer of dx; the ORANGE kernel adds)
-//   ddt_main  = d_bbs exp(cumA_last - cumA)           (the K3 part of ddt)
-//   d_delta   = d_bbs dt exp(cumA_last - cumA)        (the K3 part of d cumA)
+//   dx       += bbs[s] U[s, p]                        (dx holds the ORANGE and skip terms)
+//   ddt_main += d_bbs exp(cumA_last - cumA)           (the K3 part of ddt)
+//   d_delta   = d_bbs dt exp(cumA_last - cumA),  dcum_main -= d_delta   (the K3 part of d cumA)
+// Runs after the ORANGE kernel; its read-modify-writes are prefetched at the
+// top of each head so the global loads overlap the TMA wait and the MMA.
 template <int Q>
 __global__ void __launch_bounds__(kThreadsWide, 1) tc_bwd_k3_kernel(const Params p, const __grid_constant__ TcMaps maps) {
     constexpr int NT = Q / 128;
@@ -688,16 +690,10 @@ __global__ void __launch_bounds__(kThreadsWide, 1) tc_bwd_k3_kernel(const Params
     const int nh = h_end - h_begin;
     bf16 *DX = (bf16 *)p.dx;
     if (nh <= 0) return;
-    if (vrows <= 0) {
-        const int rows = min(Q, p.L - t0);
+    if (vrows <= 0) {  // dx, ddt_main, dcum_main already zero (ORANGE kernel)
         for (int hh = h_begin; hh < h_end; ++hh) {
-            for (int i = tid; i < rows * (kP / 8); i += kThreadsWide)
-                reinterpret_cast<uint4 *>(DX + ix_x(p, bi, t0 + i / 8, hh, 0))[i % 8] = make_uint4(0, 0, 0, 0);
             const size_t cb = ix_chunk(p, bi, hh, c) * Q;
-            for (int i = tid; i < Q; i += kThreadsWide) {
-                p.ddt_main[cb + i] = 0.f;
-                p.d_delta[cb + i] = 0.f;
-            }
+            for (int i = tid; i < Q; i += kThreadsWide) p.d_delta[cb + i] = 0.f;
         }
         return;
     }
@@ -751,6 +747,27 @@ __global__ void __launch_bounds__(kThreadsWide, 1) tc_bwd_k3_kernel(const Params
         uint8_t *xs = stg + st * STG, *dis = xs + XB;
         const float *f = fbuf + (k % NSC) * 3 * Q;
         const float *dts = f, *dec = f + Q;
+        const size_t cbase = ix_chunk(p, bi, h, c) * Q;
+        // prefetch this head's read-modify-write operands (dx rows, per-token sums)
+        uint4 dxr[NT][4];
+#pragma unroll
+        for (int mb = 0; mb < NT; ++mb) {
+            const int s = mb * 128 + 32 * q4 + lane;
+            if (t0 + s < p.L && s < vrows) {
+                const uint4 *src = reinterpret_cast<const uint4 *>(DX + ix_x(p, bi, t0 + s, h, 32 * hf));
+#pragma unroll
+                for (int c8 = 0; c8 < 4; ++c8) dxr[mb][c8] = src[c8];
+            }
+        }
+        float ddt_pre[(Q + kThreadsWide - 1) / kThreadsWide], dcum_pre[(Q + kThreadsWide - 1) / kThreadsWide];
+#pragma unroll
+        for (int i = 0; i < (Q + kThreadsWide - 1) / kThreadsWide; ++i) {
+            const int s = tid + i * kThreadsWide;
+            if (s < Q) {
+                ddt_pre[i] = p.ddt_main[cbase + s];
+                dcum_pre[i] = p.dcum_main[cbase + s];
+            }
+        }
         ok = mbar_wait(&bar_x[st], (uint32_t)((k >> 1) & 1)) && ok;
         if (ok) landed = k + 1;
         if (vrows < Q) {
@@ -788,10 +805,17 @@ __global__ void __launch_bounds__(kThreadsWide, 1) tc_bwd_k3_kernel(const Params
                         bf_lo(xv.z) * uu[4] + bf_hi(xv.z) * uu[5] + bf_lo(xv.w) * uu[6] + bf_hi(xv.w) * uu[7];
             }
             dbbp[hf * Q + s] = part;
-            if (t0 + s < p.L) {
-                const float bbs = s < vrows ? dts[s] * dec[s] : 0.f;
+            if (t0 + s < p.L && s < vrows) {
+                const float bbs = dts[s] * dec[s];
 #pragma unroll
-                for (int j = 0; j < 32; ++j) u[j] *= bbs;
+                for (int c8 = 0; c8 < 4; ++c8) {
+                    const uint4 pv = dxr[mb][c8];
+                    float *a = u + 8 * c8;
+                    a[0] = a[0] * bbs + bf_lo(pv.x); a[1] = a[1] * bbs + bf_hi(pv.x);
+                    a[2] = a[2] * bbs + bf_lo(pv.y); a[3] = a[3] * bbs + bf_hi(pv.y);
+                    a[4] = a[4] * bbs + bf_lo(pv.z); a[5] = a[5] * bbs + bf_hi(pv.z);
+                    a[6] = a[6] * bbs + bf_lo(pv.w); a[7] = a[7] * bbs + bf_hi(pv.w);
+                }
                 store_row32_bf16(DX + ix_x(p, bi, t0 + s, h, 32 * hf), u);
             }
         }
@@ -800,11 +824,16 @@ __global__ void __launch_bounds__(kThreadsWide, 1) tc_bwd_k3_kernel(const Params
         tc_fence_after();
         if (tid == 0 && k + 2 < nh) issue(k + 2);
         if (k + 2 < nh) issued = k + 3;
-        const size_t cbase = ix_chunk(p, bi, h, c) * Q;
-        for (int s = tid; s < Q; s += kThreadsWide) {
-            const float dbb = s < vrows ? dbbp[s] + dbbp[Q + s] : 0.f;
-            p.ddt_main[cbase + s] = dbb * dec[s];
-            p.d_delta[cbase + s] = dbb * dts[s] * dec[s];
+#pragma unroll
+        for (int i = 0; i < (Q + kThreadsWide - 1) / kThreadsWide; ++i) {
+            const int s = tid + i * kThreadsWide;
+            if (s < Q) {
+                const float dbb = s < vrows ? dbbp[s] + dbbp[Q + s] : 0.f;
+                const float ddelta = dbb * dts[s] * dec[s];
+                p.ddt_main[cbase + s] = ddt_pre[i] + dbb * dec[s];
+                p.d_delta[cbase + s] = ddelta;
+                p.dcum_main[cbase + s] = dcum_pre[i] - ddelta;
+            }
         }
     }
     if (!ok && tid == 0) flag_timeout(p);
@@ -827,7 +856,8 @@ __global__ void __launch_bounds__(kThreadsWide, 1) tc_bwd_k3_kernel(const Params
 // CB^T stays resident; x is single-buffered (refilled once dW^T is computed),
 // dy double-buffered.  The decay is factored through 64-group pivots off the
 // diagonal groups and 16-wide sub-block pivots inside them (all factors <= 1).
-// dx, ddt_main and d_delta already hold the K3 terms (K3 backward kernel).
+// This kernel writes dx, ddt_main and dcum_main first; the K3 backward kernel
+// runs after it and adds the K3 terms.
 template <int Q>
 __global__ void __launch_bounds__(kThreadsWide, 1) tc_bwd_orange_kernel(const Params p, const __grid_constant__ TcMaps maps) {
     constexpr int NT = Q / 128;
@@ -861,10 +891,16 @@ __global__ void __launch_bounds__(kThreadsWide, 1) tc_bwd_orange_kernel(const Pa
     const int nh = h_end - h_begin;
     bf16 *DX = (bf16 *)p.dx;
     if (nh <= 0) return;
-    if (vrows <= 0) {  // dx, ddt_main, d_delta were zeroed by the K3 backward kernel
+    if (vrows <= 0) {  // a chunk wholly past valid_len contributes nothing
+        const int rows = min(Q, p.L - t0);
         for (int hh = h_begin; hh < h_end; ++hh) {
+            for (int i = tid; i < rows * (kP / 8); i += kThreadsWide)
+                reinterpret_cast<uint4 *>(DX + ix_x(p, bi, t0 + i / 8, hh, 0))[i % 8] = make_uint4(0, 0, 0, 0);
             const size_t cb = ix_chunk(p, bi, hh, c) * Q;
-            for (int i = tid; i < Q; i += kThreadsWide) p.dcum_main[cb + i] = 0.f;
+            for (int i = tid; i < Q; i += kThreadsWide) {
+                p.dcum_main[cb + i] = 0.f;
+                p.ddt_main[cb + i] = 0.f;
+            }
             if (tid == 0) p.dD_part[((size_t)bi * p.n + c) * p.H + hh] = 0.f;
         }
         return;
@@ -1018,19 +1054,37 @@ __global__ void __launch_bounds__(kThreadsWide, 1) tc_bwd_orange_kernel(const Pa
                         const uint4 u = ld_shared_v4(cbb + sw128_chunk(sl, c8));
                         const float cv[8] = {bf_lo(u.x), bf_hi(u.x), bf_lo(u.y), bf_hi(u.y),
                                              bf_lo(u.z), bf_hi(u.z), bf_lo(u.w), bf_hi(u.w)};
-                        float w[8];
+                        float w[8], cbdv[8];
+                        const int tb8 = tc0 + 8 * c8;
+                        if (tg > sg) {  // off the diagonal group: row factor x column table
+                            const float4 e0 = *reinterpret_cast<const float4 *>(Erow + tb8);
+                            const float4 e1 = *reinterpret_cast<const float4 *>(Erow + tb8 + 4);
+                            const float ev[8] = {e0.x, e0.y, e0.z, e0.w, e1.x, e1.y, e1.z, e1.w};
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) cbdv[e] = cv[e] * ev[e] * fs0;
+                        } else {
+                            const int ut = (tb8 & 63) >> 4;  // the same for the whole 8-chunk
+                            if (ut > u16) {
+                                const float4 e0 = *reinterpret_cast<const float4 *>(E16row + tb8);
+                                const float4 e1 = *reinterpret_cast<const float4 *>(E16row + tb8 + 4);
+                                const float ev[8] = {e0.x, e0.y, e0.z, e0.w, e1.x, e1.y, e1.z, e1.w};
+#pragma unroll
+                                for (int e = 0; e < 8; ++e) cbdv[e] = cv[e] * ev[e] * f160;
+                            } else if (ut == u16) {
+                                const float4 c0 = *reinterpret_cast<const float4 *>(cum + tb8);
+                                const float4 c1 = *reinterpret_cast<const float4 *>(cum + tb8 + 4);
+                                const float ct8[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+#pragma unroll
+                                for (int e = 0; e < 8; ++e)
+                                    cbdv[e] = tb8 + e >= s ? cv[e] * __expf(ct8[e] - cs) : 0.f;
+                            } else {
+#pragma unroll
+                                for (int e = 0; e < 8; ++e) cbdv[e] = 0.f;
+                            }
+                        }
 #pragma unroll
                         for (int e = 0; e < 8; ++e) {
-                            const int t = tc0 + 8 * c8 + e;
-                            float cbd;  // CB^T[s, t] exp(cumA_t - cumA_s), t >= s
-                            if (tg > sg) {
-                                cbd = cv[e] * Erow[t] * fs0;
-                            } else {
-                                const int ut = (t & 63) >> 4;
-                                if (ut > u16) cbd = cv[e] * E16row[t] * f160;
-                                else if (ut == u16) cbd = t >= s ? cv[e] * __expf(cum[t] - cs) : 0.f;
-                                else cbd = 0.f;
-                            }
+                            const float cbd = cbdv[e];  // CB^T[s, t] exp(cumA_t - cumA_s), t >= s
                             const float gv = dw[8 * c8 + e] * cbd;
                             a_ddt += gv;
                             col[8 * c8 + e] = gv * ds;  // dW^T W^T
@@ -1090,25 +1144,28 @@ __global__ void __launch_bounds__(kThreadsWide, 1) tc_bwd_orange_kernel(const Pa
         tc_fence_after();
         if (tid == 0 && ok && k + 2 < nh) issue_dy(k + 2);
         if (k + 2 < nh) dy_iss = k + 3;
-        // ---- epilogue 2: dx += W^T dy + D dy (dx holds the K3 term)
+        // ---- epilogue 2: dx = W^T dy + D dy (the K3 backward adds its term afterwards)
         const float Dh = p.D[h];
         for (int mb = 0; mb < NT; ++mb) {
             const int s = 128 * mb + 32 * q4 + lane;
             float acc[32];
             tmem_ld32(tmem_addr(tm, 32 * q4, DXCOL + 64 * mb + 32 * hf), acc);
-            if (t0 + s < p.L && s < vrows) {
-                bf16 *dst = DX + ix_x(p, bi, t0 + s, h, 32 * hf);
+            if (t0 + s < p.L) {
+                if (s < vrows) {
 #pragma unroll
-                for (int c8 = 0; c8 < 4; ++c8) {
-                    const uint4 prev = reinterpret_cast<const uint4 *>(dst)[c8];
-                    const uint4 dv = dyr[mb][c8];
-                    float *a = acc + 8 * c8;
-                    a[0] += Dh * bf_lo(dv.x) + bf_lo(prev.x); a[1] += Dh * bf_hi(dv.x) + bf_hi(prev.x);
-                    a[2] += Dh * bf_lo(dv.y) + bf_lo(prev.y); a[3] += Dh * bf_hi(dv.y) + bf_hi(prev.y);
-                    a[4] += Dh * bf_lo(dv.z) + bf_lo(prev.z); a[5] += Dh * bf_hi(dv.z) + bf_hi(prev.z);
-                    a[6] += Dh * bf_lo(dv.w) + bf_lo(prev.w); a[7] += Dh * bf_hi(dv.w) + bf_hi(prev.w);
+                    for (int c8 = 0; c8 < 4; ++c8) {
+                        const uint4 dv = dyr[mb][c8];
+                        float *a = acc + 8 * c8;
+                        a[0] += Dh * bf_lo(dv.x); a[1] += Dh * bf_hi(dv.x);
+                        a[2] += Dh * bf_lo(dv.y); a[3] += Dh * bf_hi(dv.y);
+                        a[4] += Dh * bf_lo(dv.z); a[5] += Dh * bf_hi(dv.z);
+                        a[6] += Dh * bf_lo(dv.w); a[7] += Dh * bf_hi(dv.w);
+                    }
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) acc[j] = 0.f;
                 }
-                store_row32_bf16(dst, acc);
+                store_row32_bf16(DX + ix_x(p, bi, t0 + s, h, 32 * hf), acc);
             }
         }
         // ---- per-token outputs of head k
@@ -1120,8 +1177,8 @@ __global__ void __launch_bounds__(kThreadsWide, 1) tc_bwd_orange_kernel(const Pa
                     for (int w = 0; w < 4; ++w) tgt += colp[(mb * 4 + w) * Q + q];
             const float ddo = rowp[q] + rowp[Q + q];   // ddt_orange
             const float src = dts[q] * ddo;            // sum_t dW^T W^T
-            p.ddt_main[cbase + q] += ddo;
-            p.dcum_main[cbase + q] = tgt - src - p.d_delta[cbase + q];
+            p.ddt_main[cbase + q] = ddo;          // the K3 backward adds its terms to both
+            p.dcum_main[cbase + q] = tgt - src;
         }
         if (tid == 0) {
             float d = 0.f;
