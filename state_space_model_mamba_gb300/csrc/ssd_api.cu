@@ -70,7 +70,8 @@ Layout make_layout(const ssd_dims &d, ssd_dtype dt, bool backward) {
     const size_t n = (d.seqlen + d.chunk_len - 1) / d.chunk_len;
     const bool tc = use_tensor_cores(d, dt);
     const size_t tok = b * H * n * Q, nst = b * n * H * P * N;
-    lo.k4_nblk = (int)((P * N / 4 + kK4Threads - 1) / kK4Threads);
+    // one d_endA partial per warp of the K4 backward
+    lo.k4_nblk = (int)((P * N / kK4Vec + kK4Threads - 1) / kK4Threads) * (kK4Threads / 32);
     lo.dD_per = tc ? tc_dD_per(d.chunk_len) : (int)(Q / kMainRows);
     lo.nslice = tc ? tc_group_slices(d) : 1;
     lo.nslice_cb = tc ? tc_dcb_slices(d) : 1;
@@ -81,10 +82,11 @@ Layout make_layout(const ssd_dims &d, ssd_dtype dt, bool backward) {
     lo.cumA = take(4 * tok);
     lo.endA = take(4 * b * H * n);
     lo.CB = take(4 * b * n * G * Q * Q);
-    lo.states = take(4 * nst);
+    // chunk states: fp32 on the CUDA-core path, bf16 only on the tensor-core path
+    lo.states = tc ? 0 : take(4 * nst);
     lo.states_bf = tc ? take(2 * nst) : 0;
     if (backward) {
-        lo.dstates = take(4 * nst);
+        lo.dstates = tc ? 0 : take(4 * nst);
         lo.dstates_bf = tc ? take(2 * nst) : 0;
         lo.dcum_blue = take(4 * tok);
         lo.dcum_main = take(4 * tok);
@@ -149,10 +151,10 @@ Params base_params(const ssd_dims &d, const Layout &lo, void *ws) {
     p.CB = f(lo.CB);
     p.CBh = (bf16 *)(w + lo.CB);
     p.CBt = p.CBh + (size_t)p.b * p.n * p.G * p.Q * p.Q;
-    p.states = f(lo.states);
+    p.states = lo.states ? f(lo.states) : nullptr;
     p.states_bf = lo.states_bf ? (bf16 *)(w + lo.states_bf) : nullptr;
-    if (lo.dstates) {
-        p.dstates = f(lo.dstates);
+    if (lo.dcum_blue) {  // backward layout
+        p.dstates = lo.dstates ? f(lo.dstates) : nullptr;
         p.dstates_bf = lo.dstates_bf ? (bf16 *)(w + lo.dstates_bf) : nullptr;
         p.dcum_blue = f(lo.dcum_blue);
         p.dcum_main = f(lo.dcum_main);

@@ -48,119 +48,193 @@ cudaError_t launch_k1_cumsum(const Params &p, cudaStream_t s) {
 }
 
 // ------------------------------------------------------------------ K4 forward
-// One thread per 4 consecutive (p, r) entries of one (b, h) state.  The chunk
-// loop is serial; the chunk-state reads do not depend on the carry, so they
-// are issued kUnroll chunks ahead.  The slot holding intra_c is overwritten
-// with the chunk-input state s_c (and a bf16 copy when requested).
-constexpr int kUnroll = 8;
+// One thread per 16 consecutive (p, r) entries of one (b, h) state, 128-thread
+// blocks, sized so that the whole grid is resident at once: the chain over
+// chunks is serial, so a second wave would double the kernel's time.  The
+// chunk-state reads do not depend on the carry; they are issued kAhead chunks
+// ahead and held packed (8 registers per 16 bf16) until used.  The slot
+// holding intra_c is overwritten with the chunk-input state s_c.  The carry is
+// fp32; the stored states are S (fp32 on the CUDA-core path, bf16 on the
+// tensor-core path, whose every consumer reads bf16 operands).
+constexpr int kVec = kK4Vec;
 
-__device__ __forceinline__ float4 fma4(float a, float4 s, float4 b) {
-    return make_float4(fmaf(a, s.x, b.x), fmaf(a, s.y, b.y), fmaf(a, s.z, b.z), fmaf(a, s.w, b.w));
+template <typename S>
+struct Packed;
+template <>
+struct Packed<bf16> {
+    uint4 u[2];
+};
+template <>
+struct Packed<float> {
+    float4 u[4];
+};
+
+__device__ __forceinline__ Packed<bf16> load16(const bf16 *src) {
+    const uint4 *q = reinterpret_cast<const uint4 *>(src);
+    return Packed<bf16>{{q[0], q[1]}};
+}
+__device__ __forceinline__ Packed<float> load16(const float *src) {
+    const float4 *q = reinterpret_cast<const float4 *>(src);
+    return Packed<float>{{q[0], q[1], q[2], q[3]}};
+}
+__device__ __forceinline__ void unpack16(const Packed<bf16> &x, float *v) {
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+        const uint32_t w[4] = {x.u[j].x, x.u[j].y, x.u[j].z, x.u[j].w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            v[8 * j + 2 * i] = __uint_as_float(w[i] << 16);
+            v[8 * j + 2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+        }
+    }
+}
+__device__ __forceinline__ void unpack16(const Packed<float> &x, float *v) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        v[4 * j] = x.u[j].x;
+        v[4 * j + 1] = x.u[j].y;
+        v[4 * j + 2] = x.u[j].z;
+        v[4 * j + 3] = x.u[j].w;
+    }
+}
+__device__ __forceinline__ void store16(float *dst, const float *v) {
+    float4 *q = reinterpret_cast<float4 *>(dst);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) q[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+}
+__device__ __forceinline__ void store16(bf16 *dst, const float *v) {
+    uint32_t w[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        __nv_bfloat162 t = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
+        w[i] = *reinterpret_cast<uint32_t *>(&t);
+    }
+    uint4 *q = reinterpret_cast<uint4 *>(dst);
+    q[0] = make_uint4(w[0], w[1], w[2], w[3]);
+    q[1] = make_uint4(w[4], w[5], w[6], w[7]);
 }
 
-__device__ __forceinline__ void store_bf4(bf16 *dst, float4 v) {
-    __nv_bfloat162 lo = __floats2bfloat162_rn(v.x, v.y), hi = __floats2bfloat162_rn(v.z, v.w);
-    uint2 u;
-    u.x = *reinterpret_cast<uint32_t *>(&lo);
-    u.y = *reinterpret_cast<uint32_t *>(&hi);
-    *reinterpret_cast<uint2 *>(dst) = u;
-}
+// chunks read ahead: bounded by registers (the grid must stay one wave)
+template <typename S>
+__host__ __device__ constexpr int k4_ahead_fwd() { return sizeof(S) == 2 ? 6 : 3; }
+template <typename S>
+__host__ __device__ constexpr int k4_ahead_bwd() { return sizeof(S) == 2 ? 4 : 2; }
 
-__global__ void k4_state_passing(Params p, int write_final) {
-    const size_t PN = (size_t)p.P * p.N, nvec = PN / 4;
+template <typename S>
+__global__ void __launch_bounds__(kK4Threads, 5) k4_state_passing(Params p, S *st, int write_final) {
+    constexpr int U = k4_ahead_fwd<S>();
+    const size_t PN = (size_t)p.P * p.N, nvec = PN / kVec;
     const size_t gid = blockIdx.x * (size_t)blockDim.x + threadIdx.x;
     if (gid >= (size_t)p.b * p.H * nvec) return;
     const size_t e = gid % nvec, bh = gid / nvec;
     const int h = (int)(bh % p.H), bi = (int)(bh / p.H);
-    float4 s = p.init ? reinterpret_cast<const float4 *>(p.init)[bh * nvec + e]
-                      : make_float4(0.f, 0.f, 0.f, 0.f);
+    float s[kVec];
+    if (p.init) unpack16(load16(p.init + bh * PN + kVec * e), s);
+    else {
+#pragma unroll
+        for (int i = 0; i < kVec; ++i) s[i] = 0.f;
+    }
     const float *endA = p.endA + ix_chunk(p, bi, h, 0);
-    for (int c0 = 0; c0 < p.n; c0 += kUnroll) {
-        float4 in[kUnroll];
+    for (int c0 = 0; c0 < p.n; c0 += U) {
+        Packed<S> in[U];
 #pragma unroll
-        for (int u = 0; u < kUnroll; ++u)
-            if (c0 + u < p.n)
-                in[u] = reinterpret_cast<const float4 *>(p.states + ix_state(p, bi, c0 + u, h))[e];
+        for (int u = 0; u < U; ++u)
+            if (c0 + u < p.n) in[u] = load16(st + ix_state(p, bi, c0 + u, h) + kVec * e);
 #pragma unroll
-        for (int u = 0; u < kUnroll; ++u) {
+        for (int u = 0; u < U; ++u) {
             const int c = c0 + u;
             if (c < p.n) {
-                const size_t off = ix_state(p, bi, c, h) + 4 * e;
-                *reinterpret_cast<float4 *>(p.states + off) = s;
-                if (p.states_bf) store_bf4(p.states_bf + off, s);
-                s = fma4(__expf(endA[c]), s, in[u]);
+                store16(st + ix_state(p, bi, c, h) + kVec * e, s);
+                const float a = __expf(endA[c]);
+                float v[kVec];
+                unpack16(in[u], v);
+#pragma unroll
+                for (int i = 0; i < kVec; ++i) s[i] = fmaf(a, s[i], v[i]);
             }
         }
     }
-    if (write_final && p.final_state) reinterpret_cast<float4 *>(p.final_state)[bh * nvec + e] = s;
+    if (write_final && p.final_state) store16(p.final_state + bh * PN + kVec * e, s);
 }
 
 cudaError_t launch_k4_state_passing(const Params &p, bool write_final, cudaStream_t s) {
-    const long long nthr = (long long)p.b * p.H * ((long long)p.P * p.N / 4);
+    const long long nthr = (long long)p.b * p.H * ((long long)p.P * p.N / kVec);
     const long long blocks = (nthr + kK4Threads - 1) / kK4Threads;
-    k4_state_passing<<<(unsigned)blocks, kK4Threads, 0, s>>>(p, write_final ? 1 : 0);
+    if (p.states)
+        k4_state_passing<float><<<(unsigned)blocks, kK4Threads, 0, s>>>(p, p.states, write_final ? 1 : 0);
+    else
+        k4_state_passing<bf16><<<(unsigned)blocks, kK4Threads, 0, s>>>(p, p.states_bf, write_final ? 1 : 0);
     return cudaGetLastError();
 }
 
 // ------------------------------------------------------------------ K4 backward
 // Reverse chunk loop over the carried state gradient d (seeded with
 // d_final_state):  d_intra_c = d;  d_endA_c = exp(endA_c) * <d, s_c>;
-// d <- exp(endA_c) d + d_s_in_c.  Block = kK4Threads threads x 4 entries of one
-// (b, h); the per-chunk dot product is reduced in a fixed order inside the
-// block and written as one partial per block (summed later by the K1 backward).
-__global__ void bwd_k4_state_passing(Params p) {
-    __shared__ float red[2][32];
-    const size_t PN = (size_t)p.P * p.N, nvec = PN / 4;
-    const int nblk = p.k4_nblk;
+// d <- exp(endA_c) d + d_s_in_c.  One thread per 16 entries of one (b, h),
+// laid out as in the forward; the per-chunk dot product is reduced inside
+// each warp and written as one partial per warp (k4_nblk partials per
+// (b, h, chunk), summed in a fixed order by the K1 backward), so the chunk
+// loop has no block barrier.  `dst` holds d_s_in on entry and d_intra on
+// exit; `st` holds s_in.
+template <typename S>
+__global__ void __launch_bounds__(kK4Threads, 5) bwd_k4_state_passing(Params p, S *dst, const S *st) {
+    constexpr int U = k4_ahead_bwd<S>();
+    const size_t PN = (size_t)p.P * p.N, nvec = PN / kVec;
+    const int nblk = (int)((nvec + kK4Threads - 1) / kK4Threads);
     const int bh = blockIdx.x / nblk, slab = blockIdx.x % nblk;
     const int h = bh % p.H, bi = bh / p.H;
     const size_t e = (size_t)slab * blockDim.x + threadIdx.x;
     const bool active = e < nvec;
-    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
-    float4 d = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (active && p.d_final) d = reinterpret_cast<const float4 *>(p.d_final)[(size_t)bh * nvec + e];
-    const float *endA = p.endA + ix_chunk(p, bi, h, 0);
-    for (int c0 = p.n - 1; c0 >= 0; c0 -= kUnroll) {
-        float4 dsin[kUnroll], sin_[kUnroll];
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    const int part_idx = slab * (kK4Threads / 32) + wid;  // < k4_nblk
+    float d[kVec];
+    if (active && p.d_final) unpack16(load16(p.d_final + (size_t)bh * PN + kVec * e), d);
+    else {
 #pragma unroll
-        for (int u = 0; u < kUnroll; ++u) {
+        for (int i = 0; i < kVec; ++i) d[i] = 0.f;
+    }
+    const float *endA = p.endA + ix_chunk(p, bi, h, 0);
+    for (int c0 = p.n - 1; c0 >= 0; c0 -= U) {
+        Packed<S> dsin[U], sin_[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
             const int c = c0 - u;
             if (c >= 0 && active) {
-                const size_t off = ix_state(p, bi, c, h) + 4 * e;
-                dsin[u] = *reinterpret_cast<const float4 *>(p.dstates + off);
-                sin_[u] = *reinterpret_cast<const float4 *>(p.states + off);
+                const size_t off = ix_state(p, bi, c, h) + kVec * e;
+                dsin[u] = load16(dst + off);
+                sin_[u] = load16(st + off);
             }
         }
 #pragma unroll
-        for (int u = 0; u < kUnroll; ++u) {
+        for (int u = 0; u < U; ++u) {
             const int c = c0 - u;
             if (c < 0) break;
             const float a = __expf(endA[c]);
             float part = 0.f;
             if (active) {
-                const size_t off = ix_state(p, bi, c, h) + 4 * e;
-                *reinterpret_cast<float4 *>(p.dstates + off) = d;
-                if (p.dstates_bf) store_bf4(p.dstates_bf + off, d);
-                part = d.x * sin_[u].x + d.y * sin_[u].y + d.z * sin_[u].z + d.w * sin_[u].w;
-                d = fma4(a, d, dsin[u]);
+                store16(dst + ix_state(p, bi, c, h) + kVec * e, d);
+                float sv[kVec], dv[kVec];
+                unpack16(sin_[u], sv);
+                unpack16(dsin[u], dv);
+#pragma unroll
+                for (int i = 0; i < kVec; ++i) {
+                    part = fmaf(d[i], sv[i], part);
+                    d[i] = fmaf(a, d[i], dv[i]);
+                }
             }
             part = warp_sum(part);
-            float *r = red[c & 1];
-            if (lane == 0) r[wid] = part;
-            __syncthreads();
-            if (wid == 0) {
-                float v = lane < nw ? r[lane] : 0.f;
-                v = warp_sum(v);
-                if (lane == 0) p.d_endA_part[ix_chunk(p, bi, h, c) * nblk + slab] = v * a;
-            }
+            if (lane == 0) p.d_endA_part[ix_chunk(p, bi, h, c) * p.k4_nblk + part_idx] = part * a;
         }
     }
-    if (active && p.d_init) reinterpret_cast<float4 *>(p.d_init)[(size_t)bh * nvec + e] = d;
+    if (active && p.d_init) store16(p.d_init + (size_t)bh * PN + kVec * e, d);
 }
 
 cudaError_t launch_bwd_k4(const Params &p, cudaStream_t s) {
-    const long long blocks = (long long)p.b * p.H * p.k4_nblk;
-    bwd_k4_state_passing<<<(unsigned)blocks, kK4Threads, 0, s>>>(p);
+    const long long nvec = (long long)p.P * p.N / kVec;
+    const long long blocks = (long long)p.b * p.H * ((nvec + kK4Threads - 1) / kK4Threads);
+    if (p.dstates)
+        bwd_k4_state_passing<float><<<(unsigned)blocks, kK4Threads, 0, s>>>(p, p.dstates, p.states);
+    else
+        bwd_k4_state_passing<bf16><<<(unsigned)blocks, kK4Threads, 0, s>>>(p, p.dstates_bf, p.states_bf);
     return cudaGetLastError();
 }
 

@@ -245,9 +245,9 @@ __global__ void __launch_bounds__(kThreads) tc_k3_kernel(const Params p, const _
     const int g = h / p.hpg, t0 = c * Q;
     const int V = valid_len_of(p, bi);
     const int vrows = min(Q, V - t0);
-    float *out = p.states + ix_state(p, bi, c, h);
+    bf16 *out = p.states_bf + ix_state(p, bi, c, h);
     if (vrows <= 0) {
-        for (int i = tid; i < kP * kN; i += kThreads) out[i] = 0.f;
+        for (int i = tid; i < kP * kN; i += kThreads) out[i] = __float2bfloat16_rn(0.f);
         return;
     }
     if (tid == 0) {
@@ -292,7 +292,7 @@ __global__ void __launch_bounds__(kThreads) tc_k3_kernel(const Params p, const _
             float v[32];
             tmem_ld32(tmem_addr(tm, 32 * warp, cc), v);
 #pragma unroll
-            for (int j = 0; j < 32; ++j) out[(size_t)(cc + j) * kN + r] = v[j];
+            for (int j = 0; j < 32; ++j) out[(size_t)(cc + j) * kN + r] = __float2bfloat16_rn(v[j]);
         }
     } else if (tid == 0) {
         flag_timeout(p);
@@ -579,10 +579,10 @@ __global__ void __launch_bounds__(kThreads) tc_bwd_blue_kernel(const Params p, c
     const int g = h / p.hpg, t0 = c * Q;
     const int V = valid_len_of(p, bi);
     const int vrows = min(Q, V - t0);
-    float *dsin = p.dstates + ix_state(p, bi, c, h);
+    bf16 *dsin = p.dstates_bf + ix_state(p, bi, c, h);
     float *dcb = p.dcum_blue + ix_chunk(p, bi, h, c) * Q;
     if (vrows <= 0) {
-        for (int i = tid; i < kP * kN; i += kThreads) dsin[i] = 0.f;
+        for (int i = tid; i < kP * kN; i += kThreads) dsin[i] = __float2bfloat16_rn(0.f);
         for (int i = tid; i < Q; i += kThreads) dcb[i] = 0.f;
         return;
     }
@@ -635,7 +635,7 @@ __global__ void __launch_bounds__(kThreads) tc_bwd_blue_kernel(const Params p, c
             float v[32];
             tmem_ld32(tmem_addr(tm, 32 * warp, cc), v);
 #pragma unroll
-            for (int j = 0; j < 32; ++j) dsin[(size_t)(cc + j) * kN + r] = v[j];
+            for (int j = 0; j < 32; ++j) dsin[(size_t)(cc + j) * kN + r] = __float2bfloat16_rn(v[j]);
         }
         for (int tb = 0; tb < NT; ++tb) {
             const int l = tb * 128 + 32 * warp + lane;
@@ -1194,148 +1194,229 @@ __global__ void __launch_bounds__(kThreadsWide, 1) tc_bwd_orange_kernel(const Pa
 }
 
 // ====================================================================== group backward
-// G1: CTA per (b, chunk, group, head slice, t-block), 256 threads.  Accumulates,
-// over the slice's heads, d_cb[t, s] = sum_h dt_h[s] exp(cumA_h[t] - cumA_h[s]) dW_h[t, s]
-// (s <= t) in TMEM (dW_h = dy_h x_h^T by MMA each head, two-stage TMA ring),
-// then writes the fp32 partial to the workspace.  Off-diagonal 64 x 64 blocks
-// use the pivot factorisation of the decay (one exponential per row chunk).
+// G1: CTA per (b, chunk, group, head slice, 128 x 128 block of d_cb on or below
+// the diagonal), 256 threads: thread = one row t of the block (its TMEM lane)
+// and 64 of its columns.  Accumulates, over the slice's heads and in registers,
+//   d_cb[t, s] = sum_h dt_h[s] exp(cumA_h[t] - cumA_h[s]) dW_h[t, s]     (s <= t)
+// where dW_h = dy_h x_h^T is one MMA per head into one of two TMEM buffers, so
+// the MMA of head k + 1 runs during the epilogue of head k.  dy / x tiles come
+// through a two-stage TMA ring; per-head scalars are fetched into registers
+// three heads ahead and staged in shared memory.  Writes the fp32 partial of
+// the slice.  The decay is factored through pivots, both factors <= 1:
+// cumA at the last row of the column block for the block below the diagonal;
+// inside a diagonal block cumA[64 j + 63] for 64-wide column blocks left of
+// the row's own, cumA[16 v + 15] for 16-wide sub-blocks left of the row's own;
+// only the row's own 16-wide sub-block takes one exponential per element.
 template <int Q>
-__global__ void __launch_bounds__(kThreadsWide, 1) tc_bwd_dcb_kernel(const Params p, const __grid_constant__ TcMaps maps) {
+__global__ void __launch_bounds__(kThreadsWide, 2) tc_bwd_dcb_kernel(const Params p, const __grid_constant__ TcMaps maps) {
     constexpr int NT = Q / 128;
-    constexpr uint32_t STG = kTile * (1 + NT);  // dy rows (1 tile) + x rows (up to NT tiles)
+    constexpr int NBLK = NT * (NT + 1) / 2;
+    constexpr uint32_t STG = 2 * kTile;  // dy rows of the t-block, x rows of the s-block
+    constexpr int NSC = 3;               // scalar buffers
+    constexpr int FST = (5 * Q + Q / 64 + Q / 16 + 3) & ~3;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = align1024(smem_raw);
-    float *cumv = reinterpret_cast<float *>(sm + 2 * STG);  // [2][Q]
-    float *gcv = cumv + 2 * Q;                              // [2][Q]  dt * exp(piv - cumA)
-    float *dtv = gcv + 2 * Q;                               // [2][Q]
-    float *pivv = dtv + 2 * Q;                              // [2][8]
-    __shared__ uint64_t bar_tma[2], bar_mma;
+    float *fbuf = reinterpret_cast<float *>(sm + 2 * STG);  // [NSC][cum | dt | g | g64 | g16 | piv64 | piv16]
+    __shared__ uint64_t bar_tma[2], bar_mma[2];
     __shared__ uint32_t s_tmem;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int q4 = warp & 3, hf = warp >> 2;
     int idx = blockIdx.x;
-    const int tb = idx % NT;
-    idx /= NT;
+    const int blk = idx % NBLK;
+    idx /= NBLK;
+    const int tb = blk == 0 ? 0 : 1, sk = blk == 2 ? 1 : 0;
     const int slice = idx % p.nslice_cb;
     idx /= p.nslice_cb;
     const int g = idx % p.G, c = (idx / p.G) % p.n, bi = idx / (p.G * p.n);
     const int t0 = c * Q;
     const int vrows = min(Q, valid_len_of(p, bi) - t0);
-    const int ncols = 128 * (tb + 1);
     const int per = (p.hpg + p.nslice_cb - 1) / p.nslice_cb;
     const int h_begin = g * p.hpg + slice * per;
-    const int h_end = min(g * p.hpg + p.hpg, h_begin + per);
-    float *out = p.d_cb + ((size_t)slice * p.b * p.n * p.G + ((size_t)bi * p.n + c) * p.G + g) * (size_t)Q * Q;
-    if (vrows <= 0 || h_begin >= h_end) {
-        for (int i = tid; i < 128 * ncols; i += kThreadsWide)
-            out[(size_t)(tb * 128 + i / ncols) * Q + i % ncols] = 0.f;
+    const int nh = max(0, min(g * p.hpg + p.hpg, h_begin + per) - h_begin);
+    const int tl = 32 * q4 + lane, t = 128 * tb + tl;  // this thread's row
+    const int cb0 = 128 * sk + 64 * hf;                // and its first column
+    float *orow = p.d_cb + ((size_t)slice * p.b * p.n * p.G + ((size_t)bi * p.n + c) * p.G + g) * (size_t)Q * Q +
+                  (size_t)t * Q + cb0;
+    float acc[64];
+#pragma unroll
+    for (int i = 0; i < 64; ++i) acc[i] = 0.f;
+    auto write_out = [&]() {
+        float4 *dst = reinterpret_cast<float4 *>(orow);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) dst[i] = make_float4(acc[4 * i], acc[4 * i + 1], acc[4 * i + 2], acc[4 * i + 3]);
+    };
+    if (vrows <= 128 * tb || nh == 0) {  // the whole block lies past valid_len
+        write_out();
         return;
     }
-    const uint32_t NCOL = tb == 0 ? 256u : 512u;
-    const uint32_t ACC = 0, DW = (uint32_t)ncols;
-    if (tid == 0) {
-        mbar_init(&bar_tma[0], 1);
-        mbar_init(&bar_tma[1], 1);
-        mbar_init(&bar_mma, 1);
-        mbar_fence_init();
-    }
-    if (warp == 0) tmem_alloc(&s_tmem, NCOL);
-    tc_sync();
-    const uint32_t tm = s_tmem;
-    const uint32_t stage_bytes = (uint32_t)(kTile * (1 + (tb + 1)));
+    const bool diag = tb == sk;
+    // --- per-head scalars: registers -> shared buffer k % NSC -> derived tables
+    float r_cum = 0.f, r_dt = 0.f;
+    auto fetch = [&](int k) {
+        if (tid < Q) {
+            const int h = h_begin + k;
+            r_cum = p.cumA[ix_chunk(p, bi, h, c) * Q + tid];
+            r_dt = tid < vrows ? p.dt[ix_dt(p, bi, h, t0 + tid)] : 0.f;
+        }
+    };
+    auto stash = [&](int k) {
+        float *f = fbuf + (k % NSC) * FST;
+        if (tid < Q) {
+            f[tid] = r_cum;
+            f[Q + tid] = r_dt;
+        }
+    };
+    auto derive = [&](int k) {
+        float *f = fbuf + (k % NSC) * FST;
+        const int l = 128 * sk + (tid & 127);  // a column of this block
+        if (tid < 128) {
+            const float cl = f[l], d = f[Q + l];
+            if (diag) {
+                f[3 * Q + l] = d * __expf(f[l | 63] - cl);
+                f[4 * Q + l] = d * __expf(f[l | 15] - cl);
+                if ((l & 63) == 63) f[5 * Q + (l >> 6)] = cl;
+                if ((l & 15) == 15) f[5 * Q + Q / 64 + (l >> 4)] = cl;
+            } else {
+                f[2 * Q + l] = d * __expf(f[128 * sk + 127] - cl);
+            }
+        }
+    };
+    const int xrow = vrows - 128 * sk;  // valid rows of the x tile (> 0)
     auto issue = [&](int k) {
         const int h = h_begin + k, st = k & 1;
         uint8_t *dys = sm + st * STG, *xs = dys + kTile;
-        mbar_arrive_expect_tx(&bar_tma[st], stage_bytes);
+        mbar_arrive_expect_tx(&bar_tma[st], STG);
         tma_load_4d(dys, &maps.dy, &bar_tma[st], 0, h, t0 + 128 * tb, bi);
-        for (int j = 0; j <= tb; ++j) tma_load_4d(xs + j * kTile, &maps.x, &bar_tma[st], 0, h, t0 + 128 * j, bi);
+        tma_load_4d(xs, &maps.x, &bar_tma[st], 0, h, t0 + 128 * sk, bi);
     };
-    const int nh = h_end - h_begin;
+    if (tid == 0) {
+        mbar_init(&bar_tma[0], 1);
+        mbar_init(&bar_tma[1], 1);
+        mbar_init(&bar_mma[0], 1);
+        mbar_init(&bar_mma[1], 1);
+        mbar_fence_init();
+    }
+    if (warp == 0) tmem_alloc(&s_tmem, 256);
+    tc_sync();
+    const uint32_t tm = s_tmem;
+    int issued = 0, landed = 0;  // TMA bookkeeping of thread 0
     if (tid == 0) {
         issue(0);
-        if (nh > 1) issue(1);
+        issued = 1;
+        if (nh > 1) {
+            issue(1);
+            issued = 2;
+        }
     }
-    bool ok = true;
-    const int t = tb * 128 + 32 * q4 + lane;
-    const int tr = t >> 6;
-    const int drow = vrows - 128 * tb;  // valid rows of the dy tile
-    for (int k = 0; k < nh && ok; ++k) {
-        const int h = h_begin + k, st = k & 1;
-        float *cv = cumv + st * Q, *gv = gcv + st * Q, *dv = dtv + st * Q, *pv = pivv + st * 8;
-        const float *cumg = p.cumA + ix_chunk(p, bi, h, c) * Q;
-        for (int l = tid; l < Q; l += kThreadsWide) {
-            cv[l] = cumg[l];
-            dv[l] = l < vrows ? p.dt[ix_dt(p, bi, h, t0 + l)] : 0.f;
-        }
-        __syncthreads();
-        for (int j = tid; j < Q / 64; j += kThreadsWide) pv[j] = cv[64 * j + 63];
-        __syncthreads();
-        for (int l = tid; l < Q; l += kThreadsWide) gv[l] = dv[l] * __expf(pv[l >> 6] - cv[l]);
-        tc_fence_before();
-        ok = wait_all(&bar_tma[st], (uint32_t)((k >> 1) & 1), ok);
-        if (ok && vrows < Q) {
-            uint8_t *dys = sm + st * STG, *xs = dys + kTile;
-            zero_rows_from(dys, 128, max(drow, 0));
-            zero_rows_from(xs, 128 * (tb + 1), vrows);
+    fetch(0);
+    stash(0);
+    if (nh > 1) {
+        fetch(1);
+        stash(1);
+    }
+    if (nh > 2) fetch(2);
+    __syncthreads();
+    derive(0);
+    // Wait for head k's tiles, zero x rows past valid_len, and (thread 0) issue
+    // dW_k into TMEM buffer k & 1.  Returns a CTA-uniform status.
+    auto land_and_mma = [&](int k, bool ok_in) -> bool {
+        const int st = k & 1;
+        bool ok = ok_in && mbar_wait(&bar_tma[st], (uint32_t)((k >> 1) & 1));
+        if (tid == 0 && ok) landed = k + 1;
+        if (ok && xrow < 128) {
+            zero_rows_from(sm + st * STG + kTile, 128, xrow);
             fence_async_smem();
-        }
-        tc_sync();
-        if (tid == 0 && ok) {
-            uint8_t *dys = sm + st * STG, *xs = dys + kTile;
-            const uint32_t id = idesc_bf16(128, ncols, false, false);
-            for (int ks = 0; ks < kP / 16; ++ks)
-                mma_bf16(tm + DW, sdesc_kmajor(smem_u32(dys), ks, kTile), sdesc_kmajor(smem_u32(xs), ks, kTile), id,
-                         ks > 0);
-            mma_commit(&bar_mma);
-        }
-        ok = wait_all(&bar_mma, (uint32_t)(k & 1), ok);
-        tc_fence_after();
-        // the stage just consumed can be refilled with head k + 2
-        if (tid == 0 && ok && k + 2 < nh) issue(k + 2);
-        if (ok) {
-            const float ct = cv[t];
-            for (int j = hf; j < ncols / 32; j += 2) {
-                const int s0 = 32 * j, sb = s0 >> 6;
-                float dw[32], acc[32];
-                tmem_ld32(tmem_addr(tm, 32 * q4, DW + s0), dw);
-                if (k > 0) tmem_ld32(tmem_addr(tm, 32 * q4, ACC + s0), acc);
-                else {
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) acc[i] = 0.f;
-                }
-                if (sb < tr) {
-                    const float e = __expf(ct - pv[sb]);
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) acc[i] += dw[i] * e * gv[s0 + i];
-                } else if (sb == tr) {
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        const int s = s0 + i;
-                        acc[i] += s <= t ? dw[i] * dv[s] * __expf(ct - cv[s]) : 0.f;
-                    }
-                }
-                tmem_st32(tmem_addr(tm, 32 * q4, ACC + s0), acc);
-            }
         }
         tc_fence_before();
         ok = __syncthreads_and(ok ? 1 : 0) != 0;
         tc_fence_after();
-    }
-    if (ok) {
-        float *orow = out + (size_t)t * Q;
-        for (int j = hf; j < ncols / 32; j += 2) {
-            const int s0 = 32 * j;
-            float v[32];
-            tmem_ld32(tmem_addr(tm, 32 * q4, ACC + s0), v);
-            float4 *dst = reinterpret_cast<float4 *>(orow + s0);
+        if (tid == 0 && ok) {
+            const uint32_t dys = smem_u32(sm + st * STG), xs = dys + kTile;
+            const uint32_t id = idesc_bf16(128, 128, false, false);
 #pragma unroll
-            for (int i = 0; i < 8; ++i) dst[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+            for (int ks = 0; ks < kP / 16; ++ks)
+                mma_bf16(tm + 128 * st, sdesc_kmajor(dys, ks, kTile), sdesc_kmajor(xs, ks, kTile), id, ks > 0);
+            mma_commit(&bar_mma[st]);
         }
-    } else if (tid == 0) {
-        flag_timeout(p);
+        return ok;
+    };
+    bool ok = land_and_mma(0, true), okt = true;
+    const bool row_ok = t < vrows;
+    const int tr = tl >> 6, u16 = (tl & 63) >> 4;  // 64-row block and 16-row sub-block (diagonal blocks)
+    for (int k = 0; k < nh && ok; ++k) {
+        const int st = k & 1;
+        if (k + 1 < nh) {
+            ok = land_and_mma(k + 1, okt);  // the epilogue of head k - 1 has left buffer (k + 1) & 1
+        } else {
+            ok = __syncthreads_and(okt ? 1 : 0) != 0;
+        }
+        if (k + 2 < nh) stash(k + 2);
+        if (k + 3 < nh) fetch(k + 3);
+        if (k + 1 < nh) derive(k + 1);
+        okt = ok && mbar_wait(&bar_mma[st], (uint32_t)((k >> 1) & 1));
+        tc_fence_after();
+        if (tid == 0 && okt && k + 2 < nh) {
+            issue(k + 2);  // stage st is free: MMA k has read it
+            issued = k + 3;
+        }
+        const float *f = fbuf + (k % NSC) * FST;
+        const float ct = f[t];
+        // ---- epilogue of head k: acc += dt_s exp(cumA_t - cumA_s) dW[t, s]
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+            float dw[32];
+            tmem_ld32(tmem_addr(tm, 32 * q4, 128 * st + 64 * hf + 32 * half), dw);
+            const int s0 = cb0 + 32 * half;
+            float *a = acc + 32 * half;
+            if (row_ok && (!diag || hf < tr)) {
+                // one pivot for all 32 columns
+                const float e = __expf(ct - (diag ? f[5 * Q + (s0 >> 6)] : f[128 * sk + 127]));
+                const float4 *gv = reinterpret_cast<const float4 *>(f + (diag ? 3 : 2) * Q + s0);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const float4 gq = gv[i];
+                    a[4 * i + 0] = fmaf(dw[4 * i + 0] * gq.x, e, a[4 * i + 0]);
+                    a[4 * i + 1] = fmaf(dw[4 * i + 1] * gq.y, e, a[4 * i + 1]);
+                    a[4 * i + 2] = fmaf(dw[4 * i + 2] * gq.z, e, a[4 * i + 2]);
+                    a[4 * i + 3] = fmaf(dw[4 * i + 3] * gq.w, e, a[4 * i + 3]);
+                }
+            } else if (row_ok && hf == tr) {
+#pragma unroll
+                for (int v2 = 0; v2 < 2; ++v2) {
+                    const int sv = s0 + 16 * v2, v16 = 2 * half + v2;
+                    float *av = a + 16 * v2;
+                    const float *dv = dw + 16 * v2;
+                    if (v16 < u16) {
+                        const float e = __expf(ct - f[5 * Q + Q / 64 + (sv >> 4)]);
+                        const float4 *gv = reinterpret_cast<const float4 *>(f + 4 * Q + sv);
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            const float4 gq = gv[i];
+                            av[4 * i + 0] = fmaf(dv[4 * i + 0] * gq.x, e, av[4 * i + 0]);
+                            av[4 * i + 1] = fmaf(dv[4 * i + 1] * gq.y, e, av[4 * i + 1]);
+                            av[4 * i + 2] = fmaf(dv[4 * i + 2] * gq.z, e, av[4 * i + 2]);
+                            av[4 * i + 3] = fmaf(dv[4 * i + 3] * gq.w, e, av[4 * i + 3]);
+                        }
+                    } else if (v16 == u16) {
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) {
+                            const int s = sv + i;
+                            if (s <= t) av[i] = fmaf(dv[i] * f[Q + s], __expf(ct - f[s]), av[i]);
+                        }
+                    }
+                }
+            }
+        }
     }
+    tc_fence_before();
+    ok = __syncthreads_and(ok && okt ? 1 : 0) != 0;
+    tc_fence_after();
+    if (ok) write_out();
+    else if (tid == 0) flag_timeout(p);
+    if (tid == 0)
+        for (int k = landed; k < issued; ++k) mbar_wait(&bar_tma[k & 1], (uint32_t)((k >> 1) & 1));
     tc_sync();
-    if (warp == 0) tmem_dealloc(tm, NCOL);
+    if (warp == 0) tmem_dealloc(tm, 256);
 }
 
 // G2: CTA per (b, chunk, group, head slice).  TMEM: dC accumulators at
@@ -1689,12 +1770,12 @@ constexpr size_t smem_orange(int Q) {
     return 1024 + (size_t)kTile * (Q == 256 ? 6 : 2) + 3 * (size_t)Q * 128 +
            4 * (2 * (2 * Q + 384 + 1024 + 24) + (Q / 128) * 4 * Q + 2 * Q + 8);
 }
-// Padded above half of the SM's shared memory: a CTA holding 512 TMEM columns
-// must never share its SM with another CTA of the same kernel.
+// Padded above a third of the SM's shared memory: two CTAs of 256 TMEM columns
+// each may share an SM, a third must not.
 constexpr size_t smem_dcb(int Q) {
-    return (1024 + 2 * (size_t)kTile * (1 + Q / 128) + 4 * (6 * Q + 16)) > 120 * 1024
-               ? 1024 + 2 * (size_t)kTile * (1 + Q / 128) + 4 * (6 * Q + 16)
-               : 120 * 1024;
+    return 1024 + 4 * (size_t)kTile + 4 * 3 * (size_t)((5 * Q + Q / 64 + Q / 16 + 3) & ~3) > 80 * 1024
+               ? 1024 + 4 * (size_t)kTile + 4 * 3 * (size_t)((5 * Q + Q / 64 + Q / 16 + 3) & ~3)
+               : 80 * 1024;
 }
 constexpr size_t smem_dbc(int Q) {
     return 1024 + 2 * (2 * (size_t)Q * 128 + 4 * 64 * 128) + 4 * 4 * Q;
@@ -1704,6 +1785,8 @@ static_assert(smem_k3bwd(256) <= 232448 && smem_k3bwd(256) > 116 * 1024, "K3 bac
 static_assert(smem_k2(256) > 116 * 1024, "K2 (512 TMEM columns): one CTA per SM");
 static_assert(smem_k5(256) <= 232448 && smem_k5(256) > 116 * 1024, "K5: one CTA per SM");
 static_assert(smem_dbc(256) <= 232448, "group backward shared memory");
+static_assert(3 * (smem_dcb(128) + 1024) > 233472 && 2 * (smem_dcb(256) + 1024) <= 233472,
+              "G1: two CTAs per SM, never three");
 static_assert(2 * (size_t)256 * 256 + 2 * 256 * 128 <= 2 * (2 * (size_t)256 * 128 + 4 * 64 * 128),
               "d_cb + B tile must fit the two long-K stages");
 
@@ -1712,13 +1795,23 @@ static_assert(2 * (size_t)256 * 256 + 2 * 256 * 128 <= 2 * (2 * (size_t)256 * 12
 bool tc_supported(int64_t P, int64_t N, int64_t Q) { return P == kP && N == kN && (Q == 128 || Q == 256); }
 int tc_dD_per(int64_t) { return 1; }
 int tc_dcb_slices(const ssd_dims &d) {
+    // CTAs: one per 128 x 128 block on or below the diagonal and head slice;
+    // two fit an SM.  Minimise (waves x heads per CTA), fewest slices on ties
+    // (each slice adds a partial d_cb to write and read back).
     const long long hpg = d.nheads / d.ngroups;
     const long long n = (d.seqlen + d.chunk_len - 1) / d.chunk_len;
-    const long long ctas = d.batch * n * d.ngroups * (d.chunk_len / 128);
-    long long s = (2 * 152 + ctas - 1) / ctas;
-    if (s < 1) s = 1;
-    if (s > hpg) s = hpg;
-    return (int)s;
+    const long long nt = d.chunk_len / 128;
+    const long long ctas = d.batch * n * d.ngroups * (nt * (nt + 1) / 2);
+    const long long slots = 2 * 152;
+    long long best = 1, best_cost = -1;
+    for (long long s = 1; s <= hpg && s <= 16; ++s) {
+        const long long cost = ((ctas * s + slots - 1) / slots) * ((hpg + s - 1) / s);
+        if (best_cost < 0 || cost < best_cost) {
+            best = s;
+            best_cost = cost;
+        }
+    }
+    return (int)best;
 }
 int tc_k5_slices(const ssd_dims &d) {
     // about 8 heads per CTA (the resident C / CB loads amortise over them),
@@ -1807,7 +1900,7 @@ cudaError_t launch_tc_bwd_group(const Params &p, cudaStream_t s) {
     TcMaps m;
     cudaError_t e = make_maps(p, &m, true);
     if (e != cudaSuccess) return e;
-    const unsigned g1 = (unsigned)(p.b * p.n * p.G * p.nslice_cb * (p.Q / 128));
+    const unsigned g1 = (unsigned)(p.b * p.n * p.G * p.nslice_cb * (p.Q == 256 ? 3 : 1));
     const unsigned g2 = (unsigned)(p.b * p.n * p.G * p.nslice);
 #define CALL1(Q) launch(tc_bwd_dcb_kernel<Q>, g1, smem_dcb(Q), s, p, m, kThreadsWide)
 #define CALL2(Q) launch(tc_bwd_dbc_kernel<Q>, g2, smem_dbc(Q), s, p, m, kThreadsWide)

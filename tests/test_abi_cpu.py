@@ -56,8 +56,10 @@ def test_workspace_sizes(lib):
     d = _dims()
     f = lib.ssd_workspace_bytes(ctypes.byref(d), ssd.SSD_BF16, 0)
     b = lib.ssd_workspace_bytes(ctypes.byref(d), ssd.SSD_BF16, 1)
-    states = 2 * 32 * 80 * 64 * 128 * 4
-    assert f >= states and b >= 2 * states and b > f
+    states_bf16 = 2 * 32 * 80 * 64 * 128 * 2       # tensor-core path stores chunk states in bf16
+    assert f >= states_bf16 and b >= 2 * states_bf16 and b > f
+    simt = _dims(flags=ssd.SSD_FLAG_SIMT)          # CUDA-core path keeps them in fp32
+    assert lib.ssd_workspace_bytes(ctypes.byref(simt), ssd.SSD_BF16, 1) >= 4 * states_bf16
     assert lib.ssd_workspace_bytes(ctypes.byref(_dims(ngroups=3)), ssd.SSD_BF16, 0) == 0
     # ragged sequence length rounds the chunk count up
     r = lib.ssd_workspace_bytes(ctypes.byref(_dims(seqlen=8193)), ssd.SSD_BF16, 0)
