@@ -54,6 +54,8 @@ size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
 struct Layout {
     size_t status, cumA, endA, CB, states, states_bf, dstates, dstates_bf;
     size_t dcum_blue, dcum_main, d_delta, ddt_main, d_endA_part, dD_part, dA_part, d_cb, dBC_part;
+    size_t d_cb_bf, cb_count;
+    int n_count;
     size_t total;
     int k4_nblk, dD_per, nslice, nslice_cb, nslice_k5;
 };
@@ -97,6 +99,10 @@ Layout make_layout(const ssd_dims &d, ssd_dtype dt, bool backward) {
         lo.dA_part = take(4 * b * H * n);
         lo.d_cb = take(4 * (size_t)lo.nslice_cb * b * n * G * Q * Q);
         lo.dBC_part = tc ? take(4 * (size_t)lo.nslice * 2 * b * n * G * Q * N) : 0;
+        // summed d_cb in bf16 and one arrival counter per 128 x 128 block on or below the diagonal
+        lo.d_cb_bf = tc ? take(2 * b * n * G * Q * Q) : 0;
+        lo.n_count = tc ? (int)(b * n * G * ((Q / 128) * (Q / 128 + 1) / 2)) : 0;
+        lo.cb_count = tc ? take(4 * (size_t)lo.n_count) : 0;
     }
     lo.total = off;
     return lo;
@@ -165,6 +171,9 @@ Params base_params(const ssd_dims &d, const Layout &lo, void *ws) {
         p.dA_part = f(lo.dA_part);
         p.d_cb = f(lo.d_cb);
         p.dBC_part = lo.dBC_part ? f(lo.dBC_part) : nullptr;
+        p.d_cb_bf = lo.d_cb_bf ? (bf16 *)(w + lo.d_cb_bf) : nullptr;
+        p.cb_count = lo.cb_count ? (int *)(w + lo.cb_count) : nullptr;
+        p.n_count = lo.n_count;
     }
     p.k4_nblk = lo.k4_nblk;
     p.dD_per = lo.dD_per;

@@ -44,6 +44,9 @@ struct Params {
     float *dA_part;      // [b, H, n]
     float *d_cb;         // [nslice_cb, b, n, G, Q, Q] d_cb (partial sums per head slice)
     int nslice_cb;
+    bf16 *d_cb_bf;       // [b, n, G, Q, Q] summed d_cb in bf16 (tensor-core group path)
+    int *cb_count;       // [n_count] arrival counters of the d_cb partial blocks
+    int n_count;
     float *dBC_part;     // [nslice, 2, b, n, G, Q, N]  (tensor-core group path)
     int nslice;
     int nslice_k5;       // head slices of the persistent per-group kernels (tensor-core path)

@@ -13,9 +13,13 @@ namespace ssd {
 // ------------------------------------------------------------------ K1 forward
 // One warp per (b, h, chunk): inclusive warp-shuffle scan of dt*A over the
 // chunk's Q tokens, 32 at a time with a running carry.  Tokens at or past the
-// sample's valid length contribute dt = 0.
+// sample's valid length contribute dt = 0.  (The grid has b*H*n*32 >= n_count
+// threads, so the counter clear needs no extra launch.)
 __global__ void k1_chunk_cumsum(Params p) {
-    const int warp = (int)((blockIdx.x * (size_t)blockDim.x + threadIdx.x) >> 5);
+    const size_t gid = blockIdx.x * (size_t)blockDim.x + threadIdx.x;
+    // the backward's first kernel also clears the d_cb arrival counters
+    if (p.cb_count && gid < (size_t)p.n_count) p.cb_count[gid] = 0;
+    const int warp = (int)(gid >> 5);
     const int lane = threadIdx.x & 31;
     if (warp >= p.b * p.H * p.n) return;
     const int c = warp % p.n, bh = warp / p.n, h = bh % p.H, bi = bh / p.H;

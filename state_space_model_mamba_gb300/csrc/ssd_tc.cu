@@ -44,7 +44,7 @@ constexpr int kTile = 16384;  // one [128 rows][64] bf16 SW128 tile
 constexpr int kStatusTimeout = 5;
 
 struct TcMaps {
-    CUtensorMap x, dy, B, C, st, dst, cb, cbt;
+    CUtensorMap x, dy, B, C, st, dst, cb, cbt, dcb;
 };
 
 __device__ __forceinline__ uint8_t *align1024(uint8_t *p) {
@@ -59,6 +59,20 @@ __device__ __forceinline__ void flag_timeout(const Params &p) { atomicExch(p.sta
 __device__ __forceinline__ bool wait_all(uint64_t *bar, uint32_t parity, bool ok) {
     const bool r = ok ? mbar_wait(bar, parity) : false;
     return __syncthreads_and(r ? 1 : 0) != 0;
+}
+
+// AND of `v` over the `nthreads` threads (whole warps) that use named barrier `id`.
+__device__ __forceinline__ bool bar_and(int id, int nthreads, bool v) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred pv, pr;\n\t"
+        "setp.ne.u32 pv, %1, 0;\n\t"
+        "bar.red.and.pred pr, %2, %3, pv;\n\t"
+        "selp.u32 %0, 1, 0, pr;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)v), "r"(id), "r"(nthreads)
+        : "memory");
+    return r != 0;
 }
 
 // Synchronise the CTA around tcgen05 work (orders TMEM accesses with the barrier).
@@ -1201,8 +1215,9 @@ __global__ void __launch_bounds__(kThreadsWide, 1) tc_bwd_orange_kernel(const Pa
 // where dW_h = dy_h x_h^T is one MMA per head into one of two TMEM buffers, so
 // the MMA of head k + 1 runs during the epilogue of head k.  dy / x tiles come
 // through a two-stage TMA ring; per-head scalars are fetched into registers
-// three heads ahead and staged in shared memory.  Writes the fp32 partial of
-// the slice.  The decay is factored through pivots, both factors <= 1:
+// three heads ahead and staged in shared memory.  The slices' fp32 partials
+// are summed, in slice order, by the last CTA of the block to finish, which
+// writes d_cb in bf16 (the operand type of the next kernel).  The decay is factored through pivots, both factors <= 1:
 // cumA at the last row of the column block for the block below the diagonal;
 // inside a diagonal block cumA[64 j + 63] for 64-wide column blocks left of
 // the row's own, cumA[16 v + 15] for 16-wide sub-blocks left of the row's own;
@@ -1219,6 +1234,7 @@ __global__ void __launch_bounds__(kThreadsWide, 2) tc_bwd_dcb_kernel(const Param
     float *fbuf = reinterpret_cast<float *>(sm + 2 * STG);  // [NSC][cum | dt | g | g64 | g16 | piv64 | piv16]
     __shared__ uint64_t bar_tma[2], bar_mma[2];
     __shared__ uint32_t s_tmem;
+    __shared__ int s_last;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int q4 = warp & 3, hf = warp >> 2;
     int idx = blockIdx.x;
@@ -1235,18 +1251,19 @@ __global__ void __launch_bounds__(kThreadsWide, 2) tc_bwd_dcb_kernel(const Param
     const int nh = max(0, min(g * p.hpg + p.hpg, h_begin + per) - h_begin);
     const int tl = 32 * q4 + lane, t = 128 * tb + tl;  // this thread's row
     const int cb0 = 128 * sk + 64 * hf;                // and its first column
-    float *orow = p.d_cb + ((size_t)slice * p.b * p.n * p.G + ((size_t)bi * p.n + c) * p.G + g) * (size_t)Q * Q +
-                  (size_t)t * Q + cb0;
+    const size_t cbase = ((size_t)bi * p.n + c) * p.G + g;  // (b, chunk, group)
+    const size_t pstride = (size_t)p.b * p.n * p.G * Q * Q;   // between slices' partials
+    const size_t roff = cbase * Q * Q + (size_t)t * Q + cb0;  // this thread's 64 columns
+    bf16 *brow = p.d_cb_bf + roff;
     float acc[64];
 #pragma unroll
     for (int i = 0; i < 64; ++i) acc[i] = 0.f;
-    auto write_out = [&]() {
-        float4 *dst = reinterpret_cast<float4 *>(orow);
+    auto write_bf16 = [&](const float *v) {
 #pragma unroll
-        for (int i = 0; i < 16; ++i) dst[i] = make_float4(acc[4 * i], acc[4 * i + 1], acc[4 * i + 2], acc[4 * i + 3]);
+        for (int i = 0; i < 2; ++i) store_row32_bf16(brow + 32 * i, v + 32 * i);
     };
-    if (vrows <= 128 * tb || nh == 0) {  // the whole block lies past valid_len
-        write_out();
+    if (vrows <= 128 * tb) {  // the whole block lies past valid_len: zeros, written once
+        if (slice == 0) write_bf16(acc);
         return;
     }
     const bool diag = tb == sk;
@@ -1300,7 +1317,7 @@ __global__ void __launch_bounds__(kThreadsWide, 2) tc_bwd_dcb_kernel(const Param
     tc_sync();
     const uint32_t tm = s_tmem;
     int issued = 0, landed = 0;  // TMA bookkeeping of thread 0
-    if (tid == 0) {
+    if (tid == 0 && nh > 0) {
         issue(0);
         issued = 1;
         if (nh > 1) {
@@ -1308,15 +1325,17 @@ __global__ void __launch_bounds__(kThreadsWide, 2) tc_bwd_dcb_kernel(const Param
             issued = 2;
         }
     }
-    fetch(0);
-    stash(0);
+    if (nh > 0) {
+        fetch(0);
+        stash(0);
+    }
     if (nh > 1) {
         fetch(1);
         stash(1);
     }
     if (nh > 2) fetch(2);
     __syncthreads();
-    derive(0);
+    if (nh > 0) derive(0);
     // Wait for head k's tiles, zero x rows past valid_len, and (thread 0) issue
     // dW_k into TMEM buffer k & 1.  Returns a CTA-uniform status.
     auto land_and_mma = [&](int k, bool ok_in) -> bool {
@@ -1340,7 +1359,7 @@ __global__ void __launch_bounds__(kThreadsWide, 2) tc_bwd_dcb_kernel(const Param
         }
         return ok;
     };
-    bool ok = land_and_mma(0, true), okt = true;
+    bool ok = nh > 0 ? land_and_mma(0, true) : true, okt = true;
     const bool row_ok = t < vrows;
     const int tr = tl >> 6, u16 = (tl & 63) >> 4;  // 64-row block and 16-row sub-block (diagonal blocks)
     for (int k = 0; k < nh && ok; ++k) {
@@ -1411,35 +1430,77 @@ __global__ void __launch_bounds__(kThreadsWide, 2) tc_bwd_dcb_kernel(const Param
     tc_fence_before();
     ok = __syncthreads_and(ok && okt ? 1 : 0) != 0;
     tc_fence_after();
-    if (ok) write_out();
-    else if (tid == 0) flag_timeout(p);
+    if (!ok && tid == 0) flag_timeout(p);
     if (tid == 0)
         for (int k = landed; k < issued; ++k) mbar_wait(&bar_tma[k & 1], (uint32_t)((k >> 1) & 1));
     tc_sync();
     if (warp == 0) tmem_dealloc(tm, 256);
+    if (!ok) return;
+    // ---- sum over head slices: every slice writes its fp32 partial; the last
+    // to arrive adds them in slice order (the same sum whichever CTA is last)
+    // and writes the block in bf16
+    const int ns = p.nslice_cb;
+    if (ns > 1) {
+        float4 *dst = reinterpret_cast<float4 *>(p.d_cb + slice * pstride + roff);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) dst[i] = make_float4(acc[4 * i], acc[4 * i + 1], acc[4 * i + 2], acc[4 * i + 3]);
+        __threadfence();
+        __syncthreads();
+        if (tid == 0) s_last = atomicAdd(p.cb_count + cbase * NBLK + blk, 1) == ns - 1;
+        __syncthreads();
+        if (!s_last) return;
+        __threadfence();
+        // in place, four columns at a time: acc <- sum over slices in slice order
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int sl = 0; sl < ns; ++sl) {
+                const float4 u = sl == slice ? make_float4(acc[4 * i], acc[4 * i + 1], acc[4 * i + 2], acc[4 * i + 3])
+                                             : __ldcg(reinterpret_cast<const float4 *>(p.d_cb + sl * pstride + roff) + i);
+                v.x += u.x;
+                v.y += u.y;
+                v.z += u.z;
+                v.w += u.w;
+            }
+            acc[4 * i] = v.x;
+            acc[4 * i + 1] = v.y;
+            acc[4 * i + 2] = v.z;
+            acc[4 * i + 3] = v.w;
+        }
+        write_bf16(acc);
+        if (tid == 0) p.cb_count[cbase * NBLK + blk] = 0;  // ready for the next call
+    } else {
+        write_bf16(acc);
+    }
 }
 
-// G2: CTA per (b, chunk, group, head slice).  TMEM: dC accumulators at
-// [tb*128), dB accumulators at [NT*128 + mb*128).
+// G2: CTA per (b, chunk, group, head slice): 8 consumer warps and one TMA
+// producer warp.  TMEM: dC accumulators at [tb*128), dB accumulators at
+// [NT*128 + mb*128).
 //   slice 0 only:  dC += d_cb B        (A = d_cb K-major, B = B MN-major)
 //                  dB += d_cb^T C      (A = d_cb MN-major view, B = C MN-major)
 //   every slice:   dC += sum_h (dy_h exp(cumA_h)) s_in_h      (long-K over heads)
 //                  dB += sum_h (x_h bbs_h) d_intra_h
-// and writes the fp32 partial sums of the slice.
+// The producer refills a stage as soon as the MMAs of the head that used it
+// complete; consumer thread t scales row t of the landed dy / x tiles (its
+// scalars fetched into registers two heads ahead) and one thread issues the
+// MMAs, so the loop runs at the rate the tiles arrive.  Writes the fp32
+// partial sums of the slice.
 template <int Q>
-__global__ void __launch_bounds__(kThreadsWide, 1) tc_bwd_dbc_kernel(const Params p, const __grid_constant__ TcMaps maps) {
+__global__ void __launch_bounds__(kThreadsWide + 32, 1) tc_bwd_dbc_kernel(const Params p, const __grid_constant__ TcMaps maps) {
     constexpr int NT = Q / 128;
     constexpr uint32_t XB = Q * 128, RB = Q * 128, SB = 64 * 128;
     constexpr uint32_t STG = 2 * XB + 4 * SB;  // dy, x, s_in (2 r-blocks), d_intra (2 r-blocks)
     constexpr uint32_t NCOL = NT == 2 ? 512 : 256;
     constexpr uint32_t DBCOL = NT * 128;
+    constexpr int NCONS = kThreadsWide;         // consumer threads; the producer warp follows
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = align1024(smem_raw);
-    float *fv = reinterpret_cast<float *>(sm + 2 * STG);  // [2][2][Q]: exp(cumA), bbs per stage
     __shared__ uint64_t bar_tma[2], bar_mma[2], bar_a;
     __shared__ uint32_t s_tmem;
+    __shared__ int s_issued, s_landed, s_perr;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int q4 = warp & 3, hf = warp >> 2;
+    const int q4 = warp & 3, hf = (warp >> 2) & 1;
     int idx = blockIdx.x;
     const int slice = idx % p.nslice;
     idx /= p.nslice;
@@ -1455,7 +1516,7 @@ __global__ void __launch_bounds__(kThreadsWide, 1) tc_bwd_dbc_kernel(const Param
     const bool do_k2 = slice == 0;
     const int nh = max(0, h_end - h_begin);
     if (vrows <= 0 || (!do_k2 && nh == 0)) {
-        for (int i = tid; i < Q * kN; i += kThreadsWide) {
+        for (int i = tid; i < Q * kN; i += blockDim.x) {
             outC[i] = 0.f;
             outB[i] = 0.f;
         }
@@ -1468,6 +1529,9 @@ __global__ void __launch_bounds__(kThreadsWide, 1) tc_bwd_dbc_kernel(const Param
         mbar_init(&bar_mma[1], 1);
         mbar_init(&bar_a, 1);
         mbar_fence_init();
+        s_issued = 0;
+        s_landed = 0;
+        s_perr = 0;
     }
     if (warp == 0) tmem_alloc(&s_tmem, NCOL);
     tc_sync();
@@ -1476,34 +1540,18 @@ __global__ void __launch_bounds__(kThreadsWide, 1) tc_bwd_dbc_kernel(const Param
     uint32_t pa = 0;  // bar_a phase
     bool have_acc = false;
     if (do_k2) {
-        // d_cb (bf16, K-major [t][s] in 64-column blocks of Q rows) from the G1 partials
+        // d_cb (bf16 [t][s], 64-column blocks of Q rows; only blocks on or
+        // below the diagonal are loaded or read) and B, then C, in one buffer
         uint8_t *dcb = sm, *BCs = sm + (uint32_t)Q * Q * 2;
         if (tid == 0) {
-            mbar_arrive_expect_tx(&bar_a, 2 * RB);
+            mbar_arrive_expect_tx(&bar_a, NT * (NT + 1) * kTile + 2 * RB);
+            const int row0 = ((bi * p.n + c) * p.G + g) * Q;
+            for (int tb = 0; tb < NT; ++tb)
+                for (int j = 0; j < 2 * (tb + 1); ++j)
+                    tma_load_2d(dcb + j * RB + tb * kTile, &maps.dcb, &bar_a, 64 * j, row0 + 128 * tb);
             for (int rb = 0; rb < 2; ++rb)
                 for (int j = 0; j < NT; ++j)
                     tma_load_4d(BCs + rb * RB + j * kTile, &maps.B, &bar_a, 64 * rb, g, t0 + 128 * j, bi);
-        }
-        const size_t cstride = (size_t)p.b * p.n * p.G * Q * Q;
-        const float *part = p.d_cb + (((size_t)bi * p.n + c) * p.G + g) * (size_t)Q * Q;
-        for (int i = tid; i < Q * (Q / 8); i += kThreadsWide) {
-            const int t = i / (Q / 8), s0 = 8 * (i % (Q / 8));
-            float v[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) v[e] = 0.f;
-            if (s0 <= t) {
-                for (int sl = 0; sl < p.nslice_cb; ++sl) {
-                    const float4 a = *reinterpret_cast<const float4 *>(part + sl * cstride + (size_t)t * Q + s0);
-                    const float4 b = *reinterpret_cast<const float4 *>(part + sl * cstride + (size_t)t * Q + s0 + 4);
-                    v[0] += a.x; v[1] += a.y; v[2] += a.z; v[3] += a.w;
-                    v[4] += b.x; v[5] += b.y; v[6] += b.z; v[7] += b.w;
-                }
-#pragma unroll
-                for (int e = 0; e < 8; ++e)
-                    if (s0 + e > t) v[e] = 0.f;
-            }
-            st_shared_v4(smem_u32(dcb + (s0 / 64) * RB) + sw128_chunk(t, (s0 % 64) / 8), pack_bf2(v[0], v[1]),
-                         pack_bf2(v[2], v[3]), pack_bf2(v[4], v[5]), pack_bf2(v[6], v[7]));
         }
         ok = wait_all(&bar_a, pa, ok);
         pa ^= 1;
@@ -1524,7 +1572,6 @@ __global__ void __launch_bounds__(kThreadsWide, 1) tc_bwd_dbc_kernel(const Param
         ok = wait_all(&bar_a, pa, ok);
         pa ^= 1;
         tc_sync();
-        // C into the same buffer, then dB += d_cb^T C
         if (tid == 0 && ok) {
             mbar_arrive_expect_tx(&bar_a, 2 * RB);
             for (int rb = 0; rb < 2; ++rb)
@@ -1552,98 +1599,130 @@ __global__ void __launch_bounds__(kThreadsWide, 1) tc_bwd_dbc_kernel(const Param
         }
         ok = wait_all(&bar_a, pa, ok);
         pa ^= 1;
-        tc_sync();
+        tc_sync();  // the stage area is free again
         have_acc = true;
     }
-    // ---- long-K part over the slice's heads (2-stage TMA pipeline)
-    auto issue = [&](int k) {
-        const int h = h_begin + k, st = k & 1;
-        uint8_t *base = sm + st * STG;
-        uint8_t *dys = base, *xs = base + XB, *sis = base + 2 * XB, *dis = sis + 2 * SB;
-        const int sidx = (bi * p.n + c) * p.H + h;
-        mbar_arrive_expect_tx(&bar_tma[st], STG);
-        for (int j = 0; j < NT; ++j) {
-            tma_load_4d(dys + j * kTile, &maps.dy, &bar_tma[st], 0, h, t0 + 128 * j, bi);
-            tma_load_4d(xs + j * kTile, &maps.x, &bar_tma[st], 0, h, t0 + 128 * j, bi);
-        }
-        for (int rb = 0; rb < 2; ++rb) {
-            tma_load_3d(sis + rb * SB, &maps.st, &bar_tma[st], 64 * rb, 0, sidx);
-            tma_load_3d(dis + rb * SB, &maps.dst, &bar_tma[st], 64 * rb, 0, sidx);
-        }
-    };
-    ok = __syncthreads_and(ok ? 1 : 0) != 0;
-    if (tid == 0 && ok && nh > 0) {
-        issue(0);
-        if (nh > 1) issue(1);
-    }
-    for (int k = 0; k < nh && ok; ++k) {
-        const int h = h_begin + k, st = k & 1;
-        uint8_t *base = sm + st * STG;
-        uint8_t *dys = base, *xs = base + XB, *sis = base + 2 * XB, *dis = sis + 2 * SB;
-        float *ec = fv + st * 2 * Q, *bb = ec + Q;
-        const float *cumg = p.cumA + ix_chunk(p, bi, h, c) * Q;
-        const float cend = p.endA[ix_chunk(p, bi, h, c)];
-        for (int l = tid; l < Q; l += kThreadsWide) {
-            const float cl = cumg[l];
-            const bool v = l < vrows;
-            ec[l] = v ? __expf(cl) : 0.f;
-            bb[l] = v ? p.dt[ix_dt(p, bi, h, t0 + l)] * __expf(cend - cl) : 0.f;
-        }
-        ok = wait_all(&bar_tma[st], (uint32_t)((k >> 1) & 1), ok);
-        if (ok) {
-            scale_rows(dys, Q, ec, vrows);
-            scale_rows(xs, Q, bb, vrows);
-        }
-        fence_async_smem();
-        tc_sync();
-        if (tid == 0 && ok) {
-            const uint32_t id = idesc_bf16(128, kN, false, true);
-            for (int tb = 0; tb < NT; ++tb)
-                for (int ks = 0; ks < kP / 16; ++ks) {
-                    const bool acc = have_acc || k > 0 || ks > 0;
-                    mma_bf16(tm + tb * 128, sdesc_kmajor(smem_u32(dys + tb * kTile), ks, XB),
-                             sdesc_mnmajor(smem_u32(sis), ks, SB), id, acc);
-                    mma_bf16(tm + DBCOL + tb * 128, sdesc_kmajor(smem_u32(xs + tb * kTile), ks, XB),
-                             sdesc_mnmajor(smem_u32(dis), ks, SB), id, acc);
+    if (warp == NCONS / 32) {
+        // ---- producer: stage k & 1 takes head k once head k - 2's MMAs are done
+        if (lane == 0 && ok) {
+            for (int k = 0; k < nh; ++k) {
+                const int h = h_begin + k, st = k & 1;
+                if (k >= 2 && !mbar_wait(&bar_mma[st], (uint32_t)(((k - 2) >> 1) & 1))) {
+                    s_perr = 1;
+                    break;
                 }
-            mma_commit(&bar_mma[st]);
-            // refill this stage with head k + 2 once its MMAs are done
-            if (k + 2 < nh) {
-                if (mbar_wait(&bar_mma[st], (uint32_t)((k >> 1) & 1))) issue(k + 2);
-                else ok = false;
+                uint8_t *base = sm + st * STG;
+                uint8_t *dys = base, *xs = base + XB, *sis = base + 2 * XB, *dis = sis + 2 * SB;
+                const int sidx = (bi * p.n + c) * p.H + h;
+                mbar_arrive_expect_tx(&bar_tma[st], STG);
+                for (int j = 0; j < NT; ++j) {
+                    tma_load_4d(dys + j * kTile, &maps.dy, &bar_tma[st], 0, h, t0 + 128 * j, bi);
+                    tma_load_4d(xs + j * kTile, &maps.x, &bar_tma[st], 0, h, t0 + 128 * j, bi);
+                }
+                for (int rb = 0; rb < 2; ++rb) {
+                    tma_load_3d(sis + rb * SB, &maps.st, &bar_tma[st], 64 * rb, 0, sidx);
+                    tma_load_3d(dis + rb * SB, &maps.dst, &bar_tma[st], 64 * rb, 0, sidx);
+                }
+                s_issued = k + 1;
             }
         }
-        ok = __syncthreads_and(ok ? 1 : 0) != 0;
-    }
-    // wait for the last MMAs
-    if (nh > 0) {
-        const int k = nh - 1, st = k & 1;
-        ok = wait_all(&bar_mma[st], (uint32_t)((k >> 1) & 1), ok);
-        if (nh > 1) {
-            // head nh-2's MMAs were waited for only when a refill followed them
-            const int k2 = nh - 2, st2 = k2 & 1;
-            ok = wait_all(&bar_mma[st2], (uint32_t)((k2 >> 1) & 1), ok);
+    } else if (ok) {
+        // ---- consumers: thread t owns token row t of the chunk
+        const int t = tid;
+        const bool valid = t < vrows;
+        float c_cur = 0.f, d_cur = 0.f, e_cur = 0.f, c_nx = 0.f, d_nx = 0.f, e_nx = 0.f;
+        auto fetch = [&](int k, float &cc, float &dd, float &ce) {
+            const size_t ck = ix_chunk(p, bi, h_begin + k, c);
+            ce = p.endA[ck];
+            cc = t < Q ? p.cumA[ck * Q + t] : 0.f;
+            dd = valid ? p.dt[ix_dt(p, bi, h_begin + k, t0 + t)] : 0.f;
+        };
+        if (nh > 0) fetch(0, c_cur, d_cur, e_cur);
+        if (nh > 1) fetch(1, c_nx, d_nx, e_nx);
+        // scale the 64 bf16 of row t in place (zero past valid_len: a select)
+        auto scale_row = [&](uint8_t *tile, float f) {
+            const uint32_t base = smem_u32(tile);
+#pragma unroll
+            for (int c8 = 0; c8 < 8; ++c8) {
+                const uint32_t a = base + sw128_chunk(t, c8);
+                if (!valid) {
+                    st_shared_v4(a, 0u, 0u, 0u, 0u);
+                    continue;
+                }
+                uint4 v = ld_shared_v4(a);
+                v.x = pack_bf2(bf_lo(v.x) * f, bf_hi(v.x) * f);
+                v.y = pack_bf2(bf_lo(v.y) * f, bf_hi(v.y) * f);
+                v.z = pack_bf2(bf_lo(v.z) * f, bf_hi(v.z) * f);
+                v.w = pack_bf2(bf_lo(v.w) * f, bf_hi(v.w) * f);
+                st_shared_v4(a, v.x, v.y, v.z, v.w);
+            }
+        };
+        for (int k = 0; k < nh; ++k) {
+            const int st = k & 1;
+            uint8_t *base = sm + st * STG;
+            uint8_t *dys = base, *xs = base + XB, *sis = base + 2 * XB, *dis = sis + 2 * SB;
+            const float e_row = __expf(c_cur);                // dy row factor exp(cumA_t)
+            const float b_row = d_cur * __expf(e_cur - c_cur);  // x row factor bbs_t
+            c_cur = c_nx;
+            d_cur = d_nx;
+            e_cur = e_nx;
+            if (k + 2 < nh) fetch(k + 2, c_nx, d_nx, e_nx);
+            bool okk = mbar_wait(&bar_tma[st], (uint32_t)((k >> 1) & 1));
+            if (okk && t < Q) {
+                scale_row(dys, e_row);
+                scale_row(xs, b_row);
+            }
+            fence_async_smem();
+            tc_fence_before();
+            okk = bar_and(1, NCONS, okk);
+            tc_fence_after();
+            if (!okk) {
+                ok = false;
+                break;
+            }
+            if (tid == 0) {
+                s_landed = k + 1;
+                const uint32_t id = idesc_bf16(128, kN, false, true);
+                for (int tb = 0; tb < NT; ++tb)
+                    for (int ks = 0; ks < kP / 16; ++ks) {
+                        const bool acc = have_acc || k > 0 || ks > 0;
+                        mma_bf16(tm + tb * 128, sdesc_kmajor(smem_u32(dys + tb * kTile), ks, XB),
+                                 sdesc_mnmajor(smem_u32(sis), ks, SB), id, acc);
+                        mma_bf16(tm + DBCOL + tb * 128, sdesc_kmajor(smem_u32(xs + tb * kTile), ks, XB),
+                                 sdesc_mnmajor(smem_u32(dis), ks, SB), id, acc);
+                    }
+                mma_commit(&bar_mma[st]);
+            }
         }
+        // the last head's MMAs complete after all earlier ones
+        if (ok && nh > 0) ok = mbar_wait(&bar_mma[(nh - 1) & 1], (uint32_t)(((nh - 1) >> 1) & 1));
     }
+    tc_fence_before();
+    ok = __syncthreads_and(ok && s_perr == 0 ? 1 : 0) != 0;
     tc_fence_after();
-    if (ok) {
-        for (int tb = 0; tb < NT; ++tb) {
-            const int t = tb * 128 + 32 * q4 + lane;
-            for (int r0 = 64 * hf; r0 < 64 * hf + 64; r0 += 32) {
-                float v[32];
-                tmem_ld32(tmem_addr(tm, 32 * q4, tb * 128 + r0), v);
-                float4 *dC = reinterpret_cast<float4 *>(outC + (size_t)t * kN + r0);
+    if (tid < NCONS) {
+        if (ok) {
+            for (int tb = 0; tb < NT; ++tb) {
+                const int t = tb * 128 + 32 * q4 + lane;
+                for (int r0 = 64 * hf; r0 < 64 * hf + 64; r0 += 32) {
+                    float v[32];
+                    tmem_ld32(tmem_addr(tm, 32 * q4, tb * 128 + r0), v);
+                    float4 *dC = reinterpret_cast<float4 *>(outC + (size_t)t * kN + r0);
 #pragma unroll
-                for (int j = 0; j < 8; ++j) dC[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
-                tmem_ld32(tmem_addr(tm, 32 * q4, DBCOL + tb * 128 + r0), v);
-                float4 *dB = reinterpret_cast<float4 *>(outB + (size_t)t * kN + r0);
+                    for (int j = 0; j < 8; ++j) dC[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+                    tmem_ld32(tmem_addr(tm, 32 * q4, DBCOL + tb * 128 + r0), v);
+                    float4 *dB = reinterpret_cast<float4 *>(outB + (size_t)t * kN + r0);
 #pragma unroll
-                for (int j = 0; j < 8; ++j) dB[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+                    for (int j = 0; j < 8; ++j) dB[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+                }
             }
+        } else if (tid == 0) {
+            flag_timeout(p);
         }
-    } else if (tid == 0) {
-        flag_timeout(p);
     }
+    // loads issued for heads that were never consumed have to land before exit
+    if (tid == 0)
+        for (int k = s_landed; k < s_issued; ++k) mbar_wait(&bar_tma[k & 1], (uint32_t)((k >> 1) & 1));
     tc_sync();
     if (warp == 0) tmem_dealloc(tm, NCOL);
 }
@@ -1740,6 +1819,12 @@ cudaError_t make_maps(const Params &p, TcMaps *mp, bool backward) {
         if ((e = encode(&mp->cbt, p.CBt, 2, dims, strides, box)) != cudaSuccess) return e;
     }
     if (backward) {
+        if (p.d_cb_bf) {  // summed d_cb, bf16 [b*n*G*Q rows][Q]: boxes of 64 columns x 128 rows
+            cuuint64_t dims[2] = {(cuuint64_t)p.Q, (cuuint64_t)p.b * p.n * p.G * p.Q};
+            cuuint64_t strides[1] = {(cuuint64_t)p.Q * 2};
+            cuuint32_t box[2] = {64, 128};
+            if ((e = encode(&mp->dcb, p.d_cb_bf, 2, dims, strides, box)) != cudaSuccess) return e;
+        }
         if ((e = map_tokens(&mp->dy, p.dy, p.b, p.L, p.H, kP)) != cudaSuccess) return e;
         if (p.dstates_bf && (e = map_states(&mp->dst, p.dstates_bf, (long long)p.b * p.n * p.H)) != cudaSuccess)
             return e;
@@ -1903,7 +1988,7 @@ cudaError_t launch_tc_bwd_group(const Params &p, cudaStream_t s) {
     const unsigned g1 = (unsigned)(p.b * p.n * p.G * p.nslice_cb * (p.Q == 256 ? 3 : 1));
     const unsigned g2 = (unsigned)(p.b * p.n * p.G * p.nslice);
 #define CALL1(Q) launch(tc_bwd_dcb_kernel<Q>, g1, smem_dcb(Q), s, p, m, kThreadsWide)
-#define CALL2(Q) launch(tc_bwd_dbc_kernel<Q>, g2, smem_dbc(Q), s, p, m, kThreadsWide)
+#define CALL2(Q) launch(tc_bwd_dbc_kernel<Q>, g2, smem_dbc(Q), s, p, m, kThreadsWide + 32)
     if ((e = SSD_TC_DISPATCH(p.Q, CALL1)) != cudaSuccess) return e;
     if ((e = SSD_TC_DISPATCH(p.Q, CALL2)) != cudaSuccess) return e;
 #undef CALL1
