@@ -57,7 +57,7 @@ struct Layout {
     size_t d_cb_bf, cb_count;
     int n_count;
     size_t total;
-    int k4_nblk, dD_per, nslice, nslice_cb, nslice_k5;
+    int k4_nblk, dD_per, nslice, nslice_cb, nslice_k5, nslice_k3;
 };
 
 bool use_tensor_cores(const ssd_dims &d, ssd_dtype dt) {
@@ -78,6 +78,7 @@ Layout make_layout(const ssd_dims &d, ssd_dtype dt, bool backward) {
     lo.nslice = tc ? tc_group_slices(d) : 1;
     lo.nslice_cb = tc ? tc_dcb_slices(d) : 1;
     lo.nslice_k5 = tc ? tc_k5_slices(d) : 1;
+    lo.nslice_k3 = tc ? tc_k3_slices(d) : 1;
     size_t off = 0;
     auto take = [&](size_t bytes) { size_t o = off; off += align_up(bytes); return o; };
     lo.status = take(16);
@@ -180,6 +181,7 @@ Params base_params(const ssd_dims &d, const Layout &lo, void *ws) {
     p.nslice = lo.nslice;
     p.nslice_cb = lo.nslice_cb;
     p.nslice_k5 = lo.nslice_k5;
+    p.nslice_k3 = lo.nslice_k3;
     return p;
 }
 

@@ -50,6 +50,7 @@ struct Params {
     float *dBC_part;     // [nslice, 2, b, n, G, Q, N]  (tensor-core group path)
     int nslice;
     int nslice_k5;       // head slices of the persistent per-group kernels (tensor-core path)
+    int nslice_k3;       // head slices of the streaming K3 / BLUE kernels (tensor-core path)
     int *status;         // device status word (SSD_OK / SSD_ERR_TIMEOUT)
 };
 

@@ -111,6 +111,34 @@ __device__ __forceinline__ void zero_rows_from(uint8_t *tile, int rows, int from
         st_shared_v4(base + (uint32_t)i * 16u, 0u, 0u, 0u, 0u);
 }
 
+// Zero rows [from, rows) of a tile of 128-byte rows, using the first `nthreads` threads.
+__device__ __forceinline__ void zero_rows_from_n(uint8_t *tile, int rows, int from, int nthreads) {
+    if (from >= rows) return;
+    const uint32_t base = smem_u32(tile);
+    for (int i = threadIdx.x + from * 8; i < rows * 8; i += nthreads)
+        st_shared_v4(base + (uint32_t)i * 16u, 0u, 0u, 0u, 0u);
+}
+
+// Scale the 64 bf16 of row `row` (SW128 tile) in place by f; zero it when
+// !valid (a select, so non-finite padding cannot leak).
+__device__ __forceinline__ void scale_row_bf16(uint8_t *tile, int row, float f, bool valid) {
+    const uint32_t base = smem_u32(tile);
+#pragma unroll
+    for (int c8 = 0; c8 < 8; ++c8) {
+        const uint32_t a = base + sw128_chunk(row, c8);
+        if (!valid) {
+            st_shared_v4(a, 0u, 0u, 0u, 0u);
+            continue;
+        }
+        uint4 v = ld_shared_v4(a);
+        v.x = pack_bf2(bf_lo(v.x) * f, bf_hi(v.x) * f);
+        v.y = pack_bf2(bf_lo(v.y) * f, bf_hi(v.y) * f);
+        v.z = pack_bf2(bf_lo(v.z) * f, bf_hi(v.z) * f);
+        v.w = pack_bf2(bf_lo(v.w) * f, bf_hi(v.w) * f);
+        st_shared_v4(a, v.x, v.y, v.z, v.w);
+    }
+}
+
 // Dot product of a swizzled bf16 row (64 values) with 64 floats.
 __device__ __forceinline__ float dot_row64(const uint8_t *tile, int row, const float *v) {
     const uint32_t base = smem_u32(tile);
@@ -240,79 +268,152 @@ __global__ void __launch_bounds__(kThreads) tc_k2_kernel(const Params p, const _
 }
 
 // ====================================================================== K3
-// CTA per (b, chunk, head).  intra[p, r] = sum_l x[l, p] * B[l, r] * bbs[l],
-// bbs = dt * exp(cumA_last - cumA), computed as D[r, p] with M = dstate (A =
-// scaled B, MN-major) and N = headdim (B operand = x, MN-major).
+// CTA per (b, chunk, group, head slice): 8 consumer warps and one TMA producer
+// warp; B stays resident, x streams through a ring of NST stages.  Per head
+//   intra[p, r] = sum_l B[l, r] (bbs[l] x[l, p]),   bbs = dt exp(cumA_last - cumA)
+// as D[r, p] (M = dstate; A = B, MN-major; B operand = scaled x, MN-major)
+// into one of two TMEM buffers, so the MMA of head k overlaps the epilogue of
+// head k - 1.  Consumer thread t scales row t of x (scalars fetched into
+// registers two heads ahead); the producer refills a stage once the MMA that
+// read it completes.  The scale sits on x, not B, so B is shared by all heads.
 template <int Q>
-__global__ void __launch_bounds__(kThreads) tc_k3_kernel(const Params p, const __grid_constant__ TcMaps maps) {
+__global__ void __launch_bounds__(kThreadsWide + 32, 1) tc_k3_kernel(const Params p, const __grid_constant__ TcMaps maps) {
     constexpr int NT = Q / 128;
-    constexpr uint32_t XB = Q * 128;  // [Q][64] bf16
-    constexpr uint32_t RB = Q * 128;
+    constexpr uint32_t XB = Q * 128, RB = Q * 128;
+    constexpr int NST = 4;
+    constexpr int NCONS = kThreadsWide;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = align1024(smem_raw);
-    uint8_t *xs = sm, *bs = sm + XB;
-    float *bbs = reinterpret_cast<float *>(bs + 2 * RB);
-    __shared__ uint64_t bar_tma, bar_mma;
+    uint8_t *Bs = sm, *xst = sm + 2 * RB;  // B: 2 r-blocks of Q rows; x: NST stages
+    __shared__ uint64_t bar_res, bar_x[NST], bar_free[NST], bar_mma[2];
     __shared__ uint32_t s_tmem;
+    __shared__ int s_issued, s_landed, s_perr;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int h = blockIdx.x % p.H, c = (blockIdx.x / p.H) % p.n, bi = blockIdx.x / (p.H * p.n);
-    const int g = h / p.hpg, t0 = c * Q;
-    const int V = valid_len_of(p, bi);
-    const int vrows = min(Q, V - t0);
-    bf16 *out = p.states_bf + ix_state(p, bi, c, h);
-    if (vrows <= 0) {
-        for (int i = tid; i < kP * kN; i += kThreads) out[i] = __float2bfloat16_rn(0.f);
+    int idx = blockIdx.x;
+    const int slice = idx % p.nslice_k3;
+    idx /= p.nslice_k3;
+    const int g = idx % p.G, c = (idx / p.G) % p.n, bi = idx / (p.G * p.n);
+    const int t0 = c * Q;
+    const int vrows = min(Q, valid_len_of(p, bi) - t0);
+    const int per = (p.hpg + p.nslice_k3 - 1) / p.nslice_k3;
+    const int h_begin = g * p.hpg + slice * per;
+    const int nh = max(0, min(g * p.hpg + p.hpg, h_begin + per) - h_begin);
+    if (nh == 0) return;
+    if (vrows <= 0) {  // a chunk wholly past valid_len: zero intra-chunk states
+        for (int k = 0; k < nh; ++k) {
+            bf16 *out = p.states_bf + ix_state(p, bi, c, h_begin + k);
+            for (int i = tid; i < kP * kN / 8; i += blockDim.x) reinterpret_cast<uint4 *>(out)[i] = make_uint4(0, 0, 0, 0);
+        }
         return;
     }
     if (tid == 0) {
-        mbar_init(&bar_tma, 1);
-        mbar_init(&bar_mma, 1);
+        mbar_init(&bar_res, 1);
+        for (int i = 0; i < NST; ++i) {
+            mbar_init(&bar_x[i], 1);
+            mbar_init(&bar_free[i], 1);
+        }
+        mbar_init(&bar_mma[0], 1);
+        mbar_init(&bar_mma[1], 1);
         mbar_fence_init();
+        s_issued = 0;
+        s_landed = 0;
+        s_perr = 0;
     }
-    if (warp == 0) tmem_alloc(&s_tmem, 64);
+    if (warp == 0) tmem_alloc(&s_tmem, 128);
     tc_sync();
     const uint32_t tm = s_tmem;
-    if (tid == 0) {
-        mbar_arrive_expect_tx(&bar_tma, XB + 2 * RB);
-        for (int j = 0; j < NT; ++j) {
-            tma_load_4d(xs + j * kTile, &maps.x, &bar_tma, 0, h, t0 + 128 * j, bi);
+    bool ok = true;
+    if (warp == NCONS / 32) {
+        // ---- producer: B once, then x_k into stage k % NST once head k - NST's MMA is done
+        if (lane == 0) {
+            mbar_arrive_expect_tx(&bar_res, 2 * RB);
             for (int rb = 0; rb < 2; ++rb)
-                tma_load_4d(bs + rb * RB + j * kTile, &maps.B, &bar_tma, 64 * rb, g, t0 + 128 * j, bi);
+                for (int j = 0; j < NT; ++j)
+                    tma_load_4d(Bs + rb * RB + j * kTile, &maps.B, &bar_res, 64 * rb, g, t0 + 128 * j, bi);
+            for (int k = 0; k < nh; ++k) {
+                const int st = k % NST;
+                if (k >= NST && !mbar_wait(&bar_free[st], (uint32_t)(((k - NST) / NST) & 1))) {
+                    s_perr = 1;
+                    break;
+                }
+                mbar_arrive_expect_tx(&bar_x[st], XB);
+                for (int j = 0; j < NT; ++j)
+                    tma_load_4d(xst + st * XB + j * kTile, &maps.x, &bar_x[st], 0, h_begin + k, t0 + 128 * j, bi);
+                s_issued = k + 1;
+            }
         }
-    }
-    const float *cum = p.cumA + ix_chunk(p, bi, h, c) * Q;
-    const float cend = p.endA[ix_chunk(p, bi, h, c)];
-    for (int l = tid; l < Q; l += kThreads)
-        bbs[l] = l < vrows ? p.dt[ix_dt(p, bi, h, t0 + l)] * __expf(cend - cum[l]) : 0.f;
-    bool ok = wait_all(&bar_tma, 0, true);
-    if (ok) {
-        scale_rows(bs, Q, bbs, vrows);
-        scale_rows(bs + RB, Q, bbs, vrows);
-        zero_rows_from(xs, Q, vrows);
-    }
-    fence_async_smem();
-    tc_sync();
-    if (tid == 0 && ok) {
-        const uint32_t idesc = idesc_bf16(128, 64, true, true);
-        for (int ks = 0; ks < Q / 16; ++ks)
-            mma_bf16(tm, sdesc_mnmajor(smem_u32(bs), ks, RB), sdesc_mnmajor(smem_u32(xs), ks, XB), idesc, ks > 0);
-        mma_commit(&bar_mma);
-    }
-    ok = wait_all(&bar_mma, 0, ok);
-    tc_fence_after();
-    if (ok) {
-        const int r = 32 * warp + lane;
-        for (int cc = 0; cc < kP; cc += 32) {
-            float v[32];
-            tmem_ld32(tmem_addr(tm, 32 * warp, cc), v);
+    } else {
+        // ---- consumers
+        const int t = tid;
+        const bool valid = t < vrows;
+        float c_cur = 0.f, d_cur = 0.f, e_cur = 0.f, c_nx = 0.f, d_nx = 0.f, e_nx = 0.f;
+        auto fetch = [&](int k, float &cc, float &dd, float &ce) {
+            const size_t ck = ix_chunk(p, bi, h_begin + k, c);
+            ce = p.endA[ck];
+            cc = t < Q ? p.cumA[ck * Q + t] : 0.f;
+            dd = valid ? p.dt[ix_dt(p, bi, h_begin + k, t0 + t)] : 0.f;
+        };
+        fetch(0, c_cur, d_cur, e_cur);
+        if (nh > 1) fetch(1, c_nx, d_nx, e_nx);
+        ok = mbar_wait(&bar_res, 0);
+        if (ok && vrows < Q) {
+            zero_rows_from_n(Bs, Q, vrows, NCONS);
+            zero_rows_from_n(Bs + RB, Q, vrows, NCONS);
+        }
+        // epilogue mapping: TMEM lane = dstate r, columns = headdim p
+        const int q4 = warp & 3, hf = warp >> 2;
+        const int r = 32 * q4 + lane;
+        for (int k = 0; k <= nh; ++k) {
+            if (k < nh) {
+                const int st = k % NST;
+                uint8_t *xs = xst + st * XB;
+                const float b_row = d_cur * __expf(e_cur - c_cur);
+                c_cur = c_nx;
+                d_cur = d_nx;
+                e_cur = e_nx;
+                if (k + 2 < nh) fetch(k + 2, c_nx, d_nx, e_nx);
+                bool okk = ok && mbar_wait(&bar_x[st], (uint32_t)((k / NST) & 1));
+                if (okk && t < Q) scale_row_bf16(xs, t, b_row, valid);
+                fence_async_smem();
+                tc_fence_before();
+                okk = bar_and(1, NCONS, okk);  // also: epilogue k - 2 has left TMEM buffer k & 1
+                tc_fence_after();
+                if (!okk) {
+                    ok = false;
+                    break;
+                }
+                if (tid == 0) {
+                    s_landed = k + 1;
+                    const uint32_t idesc = idesc_bf16(128, 64, true, true);
+                    for (int ks = 0; ks < Q / 16; ++ks)
+                        mma_bf16(tm + 64 * (k & 1), sdesc_mnmajor(smem_u32(Bs), ks, RB), sdesc_mnmajor(smem_u32(xs), ks, XB),
+                                 idesc, ks > 0);
+                    mma_commit(&bar_mma[k & 1]);
+                    mma_commit(&bar_free[st]);
+                }
+            }
+            if (k > 0) {
+                // ---- epilogue of head k - 1
+                const int kk = k - 1;
+                ok = mbar_wait(&bar_mma[kk & 1], (uint32_t)((kk >> 1) & 1)) && ok;
+                tc_fence_after();
+                float v[32];
+                tmem_ld32(tmem_addr(tm, 32 * q4, 64 * (kk & 1) + 32 * hf), v);
+                bf16 *out = p.states_bf + ix_state(p, bi, c, h_begin + kk);
 #pragma unroll
-            for (int j = 0; j < 32; ++j) out[(size_t)(cc + j) * kN + r] = __float2bfloat16_rn(v[j]);
+                for (int j = 0; j < 32; ++j) out[(size_t)(32 * hf + j) * kN + r] = __float2bfloat16_rn(v[j]);
+            }
         }
-    } else if (tid == 0) {
-        flag_timeout(p);
     }
+    tc_fence_before();
+    ok = __syncthreads_and(ok && s_perr == 0 ? 1 : 0) != 0;
+    tc_fence_after();
+    if (!ok && tid == 0) flag_timeout(p);
+    // loads issued for heads that were never consumed have to land before exit
+    if (tid == 0)
+        for (int k = s_landed; k < s_issued; ++k) mbar_wait(&bar_x[k % NST], (uint32_t)((k / NST) & 1));
     tc_sync();
-    if (warp == 0) tmem_dealloc(tm, 64);
+    if (warp == 0) tmem_dealloc(tm, 128);
 }
 
 // ====================================================================== K5
@@ -366,13 +467,22 @@ __global__ void __launch_bounds__(kThreadsWide, 1) tc_k5_kernel(const Params p, 
                 reinterpret_cast<uint4 *>(Y + ix_x(p, bi, t0 + i / 8, hh, 0))[i % 8] = make_uint4(0, 0, 0, 0);
         return;
     }
-    // raw per-head scalars into buffer `b`: cumA, dt (0 past valid_len)
-    auto load_raw = [&](int h, int b) {
+    // raw per-head scalars cumA, dt (0 past valid_len): fetched into registers
+    // (thread l holds token l) one head before they are staged in buffer `b`,
+    // so the global load latency is hidden behind a whole head's work
+    float r_cum = 0.f, r_dt = 0.f;
+    auto fetch = [&](int k) {
+        const int h = h_begin + k;
+        if (tid < Q) {
+            r_cum = p.cumA[ix_chunk(p, bi, h, c) * Q + tid];
+            r_dt = tid < vrows ? p.dt[ix_dt(p, bi, h, t0 + tid)] : 0.f;
+        }
+    };
+    auto stash = [&](int b) {
         float *f = fbuf + b * FST;
-        const float *cumg = p.cumA + ix_chunk(p, bi, h, c) * Q;
-        for (int l = tid; l < Q; l += kThreadsWide) {
-            f[l] = cumg[l];
-            f[Q + l] = l < vrows ? p.dt[ix_dt(p, bi, h, t0 + l)] : 0.f;
+        if (tid < Q) {
+            f[tid] = r_cum;
+            f[Q + tid] = r_dt;
         }
     };
     // column factors dt exp(piv - cumA) and pivots, from the raw values (visible after a barrier)
@@ -411,8 +521,13 @@ __global__ void __launch_bounds__(kThreadsWide, 1) tc_k5_kernel(const Params p, 
                 tma_load_2d(CBs + (tb * (tb + 1) + sb) * kTile, &maps.cb, &bar_res, 64 * sb, cbrow + 128 * tb);
         issue_head(h_begin);
     }
-    load_raw(h_begin, 0);
-    if (nh > 1) load_raw(h_begin + 1, 1);
+    fetch(0);
+    stash(0);
+    if (nh > 1) {
+        fetch(1);
+        stash(1);
+    }
+    if (nh > 2) fetch(2);
     int x_issued = 1, x_landed = 0;
     bool ok = wait_all(&bar_res, 0, true);  // publishes the raw scalars of heads 0 and 1
     if (ok && vrows < Q) {
@@ -423,8 +538,10 @@ __global__ void __launch_bounds__(kThreadsWide, 1) tc_k5_kernel(const Params p, 
     derive(0);
     __syncthreads();
     uint4 xr[NT][4];  // this thread's D x slices of the head whose epilogue comes next
+    float D_ep = 0.f;  // D of the head whose epilogue comes next
     for (int k = 0; k <= nh && ok; ++k) {
         const int h = h_begin + k, cur = k % NSC, prv = (k + NSC - 1) % NSC;
+        const float D_k = k < nh ? p.D[h] : 0.f;  // used one iteration later
         if (k > 0) {
             // MMAs of head k-1 done: the TMEM W region and the x / s_in buffers are free
             ok = mbar_wait(&bar_mma, (uint32_t)((k - 1) & 1)) && ok;
@@ -499,13 +616,16 @@ __global__ void __launch_bounds__(kThreadsWide, 1) tc_k5_kernel(const Params p, 
                 }
             }
             // prefetch raw scalars of head k + 2, derive those of head k + 1 (raw visible since the last barrier)
-            if (k + 2 < nh) load_raw(h + 2, (k + 2) % NSC);
+            if (k + 2 < nh) {
+                stash((k + 2) % NSC);
+                if (k + 3 < nh) fetch(k + 3);
+            }
             if (k + 1 < nh) derive((k + 1) % NSC);
         }
         // ---- epilogue of head k - 1
         if (k > 0) {
             const float *cum = fbuf + prv * FST;
-            const float Dh = p.D[h - 1];
+            const float Dh = D_ep;
 #pragma unroll
             for (int tb = 0; tb < NT; ++tb) {
                 const int t = tb * 128 + 32 * q4 + lane;
@@ -532,6 +652,7 @@ __global__ void __launch_bounds__(kThreadsWide, 1) tc_k5_kernel(const Params p, 
             }
         }
         if (k == nh) break;
+        D_ep = D_k;
         // ---- x_k landed: keep this thread's D x slices, zero padded rows
         ok = mbar_wait(&bar_x, (uint32_t)(k & 1)) && ok;
         if (ok) x_landed = k + 1;
@@ -573,96 +694,193 @@ __global__ void __launch_bounds__(kThreadsWide, 1) tc_k5_kernel(const Params p, 
 }
 
 // ====================================================================== BLUE backward
-// CTA per (b, chunk, head).  d_ch = dy * exp(cumA) (formed in place over dy).
-//   d_s_in[r, p] = sum_l C[l, r] d_ch[l, p]        (TMEM cols 0..63; A = C MN-major, B = d_ch MN-major)
-//   u[l, p]      = sum_r C[l, r] s_in[p, r]        (TMEM cols 64 + tb*64; both K-major)
+// CTA per (b, chunk, group, head slice): 8 consumer warps and one TMA producer
+// warp; C stays resident, (dy, s_in) stream through a ring of NST stages.  Per head
+//   d_ch[l, p]     = dy[l, p] exp(cumA_l)   (row l scaled in place by consumer thread l,
+//                                            which keeps it in registers for the dot below)
+//   d_s_in[r, p]   = sum_l C[l, r] d_ch[l, p]   (A = C MN-major, B = d_ch MN-major)
+//   u[l, p]        = sum_r C[l, r] s_in[p, r]   (A = C K-major,  B = s_in K-major)
 //   d_cumA_blue[l] = sum_p d_ch[l, p] u[l, p]
+// into one of two TMEM buffers, so the MMAs of head k overlap the epilogue of
+// head k - 1.
 template <int Q>
-__global__ void __launch_bounds__(kThreads) tc_bwd_blue_kernel(const Params p, const __grid_constant__ TcMaps maps) {
+__global__ void __launch_bounds__(kThreadsWide + 32, 1) tc_bwd_blue_kernel(const Params p, const __grid_constant__ TcMaps maps) {
     constexpr int NT = Q / 128;
     constexpr uint32_t XB = Q * 128, RB = Q * 128, SB = 64 * 128;
-    constexpr uint32_t NCOL = NT == 2 ? 256 : 128;
+    constexpr uint32_t STG = XB + 2 * SB;
+    constexpr int NST = 3;
+    constexpr uint32_t BUF = 256;  // TMEM columns per buffer: d_s_in 64 | u NT * 64
+    constexpr int NCONS = kThreadsWide;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = align1024(smem_raw);
-    uint8_t *Cs = sm, *Ds = Cs + 2 * RB, *Ss = Ds + XB;
-    float *ecum = reinterpret_cast<float *>(Ss + 2 * SB);
-    __shared__ uint64_t bar_tma, bar_mma;
+    uint8_t *Cs = sm, *stg = sm + 2 * RB;
+    __shared__ uint64_t bar_res, bar_x[NST], bar_free[NST], bar_mma[2];
     __shared__ uint32_t s_tmem;
+    __shared__ int s_issued, s_landed, s_perr;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int h = blockIdx.x % p.H, c = (blockIdx.x / p.H) % p.n, bi = blockIdx.x / (p.H * p.n);
-    const int g = h / p.hpg, t0 = c * Q;
-    const int V = valid_len_of(p, bi);
-    const int vrows = min(Q, V - t0);
-    bf16 *dsin = p.dstates_bf + ix_state(p, bi, c, h);
-    float *dcb = p.dcum_blue + ix_chunk(p, bi, h, c) * Q;
+    int idx = blockIdx.x;
+    const int slice = idx % p.nslice_k3;
+    idx /= p.nslice_k3;
+    const int g = idx % p.G, c = (idx / p.G) % p.n, bi = idx / (p.G * p.n);
+    const int t0 = c * Q;
+    const int vrows = min(Q, valid_len_of(p, bi) - t0);
+    const int per = (p.hpg + p.nslice_k3 - 1) / p.nslice_k3;
+    const int h_begin = g * p.hpg + slice * per;
+    const int nh = max(0, min(g * p.hpg + p.hpg, h_begin + per) - h_begin);
+    if (nh == 0) return;
     if (vrows <= 0) {
-        for (int i = tid; i < kP * kN; i += kThreads) dsin[i] = __float2bfloat16_rn(0.f);
-        for (int i = tid; i < Q; i += kThreads) dcb[i] = 0.f;
+        for (int k = 0; k < nh; ++k) {
+            bf16 *dsin = p.dstates_bf + ix_state(p, bi, c, h_begin + k);
+            for (int i = tid; i < kP * kN / 8; i += blockDim.x) reinterpret_cast<uint4 *>(dsin)[i] = make_uint4(0, 0, 0, 0);
+            float *dcb = p.dcum_blue + ix_chunk(p, bi, h_begin + k, c) * Q;
+            for (int i = tid; i < Q; i += blockDim.x) dcb[i] = 0.f;
+        }
         return;
     }
     if (tid == 0) {
-        mbar_init(&bar_tma, 1);
-        mbar_init(&bar_mma, 1);
+        mbar_init(&bar_res, 1);
+        for (int i = 0; i < NST; ++i) {
+            mbar_init(&bar_x[i], 1);
+            mbar_init(&bar_free[i], 1);
+        }
+        mbar_init(&bar_mma[0], 1);
+        mbar_init(&bar_mma[1], 1);
         mbar_fence_init();
+        s_issued = 0;
+        s_landed = 0;
+        s_perr = 0;
     }
-    if (warp == 0) tmem_alloc(&s_tmem, NCOL);
+    if (warp == 0) tmem_alloc(&s_tmem, 512);
     tc_sync();
     const uint32_t tm = s_tmem;
-    if (tid == 0) {
-        mbar_arrive_expect_tx(&bar_tma, XB + 2 * RB + 2 * SB);
-        const int sidx = (bi * p.n + c) * p.H + h;
-        for (int j = 0; j < NT; ++j) {
-            tma_load_4d(Ds + j * kTile, &maps.dy, &bar_tma, 0, h, t0 + 128 * j, bi);
+    bool ok = true;
+    if (warp == NCONS / 32) {
+        // ---- producer: C once, then (dy_k, s_in_k) into stage k % NST once head k - NST's MMAs are done
+        if (lane == 0) {
+            mbar_arrive_expect_tx(&bar_res, 2 * RB);
             for (int rb = 0; rb < 2; ++rb)
-                tma_load_4d(Cs + rb * RB + j * kTile, &maps.C, &bar_tma, 64 * rb, g, t0 + 128 * j, bi);
+                for (int j = 0; j < NT; ++j)
+                    tma_load_4d(Cs + rb * RB + j * kTile, &maps.C, &bar_res, 64 * rb, g, t0 + 128 * j, bi);
+            for (int k = 0; k < nh; ++k) {
+                const int st = k % NST, h = h_begin + k;
+                if (k >= NST && !mbar_wait(&bar_free[st], (uint32_t)(((k - NST) / NST) & 1))) {
+                    s_perr = 1;
+                    break;
+                }
+                uint8_t *dys = stg + st * STG, *sis = dys + XB;
+                const int sidx = (bi * p.n + c) * p.H + h;
+                mbar_arrive_expect_tx(&bar_x[st], STG);
+                for (int j = 0; j < NT; ++j) tma_load_4d(dys + j * kTile, &maps.dy, &bar_x[st], 0, h, t0 + 128 * j, bi);
+                for (int rb = 0; rb < 2; ++rb) tma_load_3d(sis + rb * SB, &maps.st, &bar_x[st], 64 * rb, 0, sidx);
+                s_issued = k + 1;
+            }
         }
-        for (int rb = 0; rb < 2; ++rb) tma_load_3d(Ss + rb * SB, &maps.st, &bar_tma, 64 * rb, 0, sidx);
-    }
-    const float *cum = p.cumA + ix_chunk(p, bi, h, c) * Q;
-    for (int l = tid; l < Q; l += kThreads) ecum[l] = l < vrows ? __expf(cum[l]) : 0.f;
-    bool ok = wait_all(&bar_tma, 0, true);
-    if (ok) {
-        scale_rows(Ds, Q, ecum, vrows);
-        if (vrows < Q) {
-            zero_rows_from(Cs, Q, vrows);
-            zero_rows_from(Cs + RB, Q, vrows);
+    } else {
+        // ---- consumers: thread t owns token row t; for the d_s_in epilogue,
+        // TMEM lane r = 32 (warp % 4) + lane and headdim half warp / 4
+        const int t = tid;
+        const bool valid = t < vrows;
+        const int q4 = warp & 3, hf = warp >> 2;
+        const int r = 32 * q4 + lane;
+        float c_cur = 0.f, c_nx = 0.f;
+        auto fetch = [&](int k) { return t < Q ? p.cumA[ix_chunk(p, bi, h_begin + k, c) * Q + t] : 0.f; };
+        c_cur = fetch(0);
+        if (nh > 1) c_nx = fetch(1);
+        ok = mbar_wait(&bar_res, 0);
+        if (ok && vrows < Q) {
+            zero_rows_from_n(Cs, Q, vrows, NCONS);
+            zero_rows_from_n(Cs + RB, Q, vrows, NCONS);
         }
-    }
-    fence_async_smem();
-    tc_sync();
-    if (tid == 0 && ok) {
-        const uint32_t i1 = idesc_bf16(128, 64, true, true);
-        for (int ks = 0; ks < Q / 16; ++ks)
-            mma_bf16(tm, sdesc_mnmajor(smem_u32(Cs), ks, RB), sdesc_mnmajor(smem_u32(Ds), ks, XB), i1, ks > 0);
-        const uint32_t i2 = idesc_bf16(128, 64, false, false);
-        for (int tb = 0; tb < NT; ++tb)
-            for (int ks = 0; ks < kN / 16; ++ks)
-                mma_bf16(tm + 64 + tb * 64, sdesc_kmajor(smem_u32(Cs + tb * kTile), ks, RB),
-                         sdesc_kmajor(smem_u32(Ss), ks, SB), i2, ks > 0);
-        mma_commit(&bar_mma);
-    }
-    ok = wait_all(&bar_mma, 0, ok);
-    tc_fence_after();
-    if (ok) {
-        const int r = 32 * warp + lane;
-        for (int cc = 0; cc < kP; cc += 32) {
-            float v[32];
-            tmem_ld32(tmem_addr(tm, 32 * warp, cc), v);
+        uint4 dch[8], dch_prev[8];  // scaled dy row t of the current / previous head
 #pragma unroll
-            for (int j = 0; j < 32; ++j) dsin[(size_t)(cc + j) * kN + r] = __float2bfloat16_rn(v[j]);
+        for (int i = 0; i < 8; ++i) dch_prev[i] = dch[i] = make_uint4(0, 0, 0, 0);
+        for (int k = 0; k <= nh; ++k) {
+            if (k < nh) {
+                const int st = k % NST;
+                uint8_t *dys = stg + st * STG, *sis = dys + XB;
+                const float e_row = __expf(c_cur);
+                c_cur = c_nx;
+                if (k + 2 < nh) c_nx = fetch(k + 2);
+                bool okk = ok && mbar_wait(&bar_x[st], (uint32_t)((k / NST) & 1));
+                if (okk && t < Q) {
+                    const uint32_t base = smem_u32(dys);
+#pragma unroll
+                    for (int c8 = 0; c8 < 8; ++c8) {
+                        const uint32_t a = base + sw128_chunk(t, c8);
+                        uint4 v = make_uint4(0, 0, 0, 0);
+                        if (valid) {
+                            v = ld_shared_v4(a);
+                            v.x = pack_bf2(bf_lo(v.x) * e_row, bf_hi(v.x) * e_row);
+                            v.y = pack_bf2(bf_lo(v.y) * e_row, bf_hi(v.y) * e_row);
+                            v.z = pack_bf2(bf_lo(v.z) * e_row, bf_hi(v.z) * e_row);
+                            v.w = pack_bf2(bf_lo(v.w) * e_row, bf_hi(v.w) * e_row);
+                        }
+                        st_shared_v4(a, v.x, v.y, v.z, v.w);
+                        dch[c8] = v;
+                    }
+                }
+                fence_async_smem();
+                tc_fence_before();
+                okk = bar_and(1, NCONS, okk);  // also: epilogue k - 2 has left TMEM buffer k & 1
+                tc_fence_after();
+                if (!okk) {
+                    ok = false;
+                    break;
+                }
+                if (tid == 0) {
+                    s_landed = k + 1;
+                    const uint32_t buf = BUF * (k & 1);
+                    const uint32_t i1 = idesc_bf16(128, 64, true, true);
+                    for (int ks = 0; ks < Q / 16; ++ks)
+                        mma_bf16(tm + buf, sdesc_mnmajor(smem_u32(Cs), ks, RB), sdesc_mnmajor(smem_u32(dys), ks, XB), i1,
+                                 ks > 0);
+                    const uint32_t i2 = idesc_bf16(128, 64, false, false);
+                    for (int tb = 0; tb < NT; ++tb)
+                        for (int ks = 0; ks < kN / 16; ++ks)
+                            mma_bf16(tm + buf + 64 + tb * 64, sdesc_kmajor(smem_u32(Cs + tb * kTile), ks, RB),
+                                     sdesc_kmajor(smem_u32(sis), ks, SB), i2, ks > 0);
+                    mma_commit(&bar_mma[k & 1]);
+                    mma_commit(&bar_free[st]);
+                }
+            }
+            if (k > 0) {
+                // ---- epilogue of head k - 1
+                const int kk = k - 1, h = h_begin + kk;
+                const uint32_t buf = BUF * (kk & 1);
+                ok = mbar_wait(&bar_mma[kk & 1], (uint32_t)((kk >> 1) & 1)) && ok;
+                tc_fence_after();
+                float v[32];
+                tmem_ld32(tmem_addr(tm, 32 * q4, buf + 32 * hf), v);
+                bf16 *dsin = p.dstates_bf + ix_state(p, bi, c, h);
+#pragma unroll
+                for (int j = 0; j < 32; ++j) dsin[(size_t)(32 * hf + j) * kN + r] = __float2bfloat16_rn(v[j]);
+                if (t < Q) {  // warp w holds rows 128 (w / 4) + 32 (w % 4) + lane of u: its own t
+                    float u[64];
+                    tmem_ld32(tmem_addr(tm, 32 * q4, buf + 64 + 64 * hf), u);
+                    tmem_ld32(tmem_addr(tm, 32 * q4, buf + 64 + 64 * hf + 32), u + 32);
+                    float acc = 0.f;
+#pragma unroll
+                    for (int c8 = 0; c8 < 8; ++c8) {
+                        const uint4 d = dch_prev[c8];
+                        const float *uu = u + 8 * c8;
+                        acc += bf_lo(d.x) * uu[0] + bf_hi(d.x) * uu[1] + bf_lo(d.y) * uu[2] + bf_hi(d.y) * uu[3] +
+                               bf_lo(d.z) * uu[4] + bf_hi(d.z) * uu[5] + bf_lo(d.w) * uu[6] + bf_hi(d.w) * uu[7];
+                    }
+                    p.dcum_blue[ix_chunk(p, bi, h, c) * Q + t] = valid ? acc : 0.f;
+                }
+            }
+#pragma unroll
+            for (int i = 0; i < 8; ++i) dch_prev[i] = dch[i];
         }
-        for (int tb = 0; tb < NT; ++tb) {
-            const int l = tb * 128 + 32 * warp + lane;
-            float u[64];
-            tmem_ld32(tmem_addr(tm, 32 * warp, 64 + tb * 64), u);
-            tmem_ld32(tmem_addr(tm, 32 * warp, 64 + tb * 64 + 32), u + 32);
-            dcb[l] = l < vrows ? dot_row64(Ds, l, u) : 0.f;
-        }
-    } else if (tid == 0) {
-        flag_timeout(p);
     }
+    tc_fence_before();
+    ok = __syncthreads_and(ok && s_perr == 0 ? 1 : 0) != 0;
+    tc_fence_after();
+    if (!ok && tid == 0) flag_timeout(p);
+    if (tid == 0)
+        for (int k = s_landed; k < s_issued; ++k) mbar_wait(&bar_x[k % NST], (uint32_t)((k / NST) & 1));
     tc_sync();
-    if (warp == 0) tmem_dealloc(tm, NCOL);
+    if (warp == 0) tmem_dealloc(tm, 512);
 }
 
 // ====================================================================== K3 backward
@@ -711,13 +929,22 @@ __global__ void __launch_bounds__(kThreadsWide, 1) tc_bwd_k3_kernel(const Params
         }
         return;
     }
-    auto load_scalars = [&](int h, int b) {
+    // per-head scalars fetched into registers (thread l holds token l) a head
+    // before they are staged: dt, and the decay to the chunk end
+    float r_dt = 0.f, r_cum = 0.f, r_end = 0.f;
+    auto fetch = [&](int k) {
+        const int h = h_begin + k;
+        if (tid < Q) {
+            r_cum = p.cumA[ix_chunk(p, bi, h, c) * Q + tid];
+            r_end = p.endA[ix_chunk(p, bi, h, c)];
+            r_dt = tid < vrows ? p.dt[ix_dt(p, bi, h, t0 + tid)] : 0.f;
+        }
+    };
+    auto stash = [&](int b) {
         float *f = fbuf + b * 3 * Q;
-        const float *cumg = p.cumA + ix_chunk(p, bi, h, c) * Q;
-        const float cend = p.endA[ix_chunk(p, bi, h, c)];
-        for (int l = tid; l < Q; l += kThreadsWide) {
-            f[l] = l < vrows ? p.dt[ix_dt(p, bi, h, t0 + l)] : 0.f;
-            f[Q + l] = __expf(cend - cumg[l]);
+        if (tid < Q) {
+            f[tid] = r_dt;
+            f[Q + tid] = __expf(r_end - r_cum);
         }
     };
     auto issue = [&](int k) {
@@ -747,8 +974,13 @@ __global__ void __launch_bounds__(kThreadsWide, 1) tc_bwd_k3_kernel(const Params
         issue(0);
         if (nh > 1) issue(1);
     }
-    load_scalars(h_begin, 0);
-    if (nh > 1) load_scalars(h_begin + 1, 1);
+    fetch(0);
+    stash(0);
+    if (nh > 1) {
+        fetch(1);
+        stash(1);
+    }
+    if (nh > 2) fetch(2);
     int issued = nh > 1 ? 2 : 1, landed = 0;
     bool ok = wait_all(&bar_res, 0, true);
     if (ok && vrows < Q) {
@@ -802,7 +1034,10 @@ __global__ void __launch_bounds__(kThreadsWide, 1) tc_bwd_k3_kernel(const Params
                              sdesc_kmajor(smem_u32(dis), ks, SB), iu, ks > 0);
             mma_commit(&bar_mma[st]);
         }
-        if (k + 2 < nh) load_scalars(h + 2, (k + 2) % NSC);
+        if (k + 2 < nh) {  // buffer (k + 2) % NSC was last read by head k - 1
+            stash((k + 2) % NSC);
+            if (k + 3 < nh) fetch(k + 3);
+        }
         ok = mbar_wait(&bar_mma[st], (uint32_t)((k >> 1) & 1)) && ok;
         tc_fence_after();
         for (int mb = 0; mb < NT; ++mb) {
@@ -881,7 +1116,8 @@ __global__ void __launch_bounds__(kThreadsWide, 1) tc_bwd_orange_kernel(const Pa
     constexpr uint32_t DXCOL = NT == 2 ? 384 : 128;  // dx accumulators (dW^T occupies [0, DXCOL))
     // per-head scalars: cum Q | dts Q | E (pivot rows) 384 | E16 16x64 | piv 8 | piv16 16
     constexpr int EOFF = 2 * Q, E16OFF = EOFF + 384, POFF = E16OFF + 1024, P16OFF = POFF + 8;
-    constexpr int FST = P16OFF + 16;
+    constexpr int DOFF = P16OFF + 16;  // D of the head
+    constexpr int FST = DOFF + 4;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = align1024(smem_raw);
     uint8_t *CBt = sm, *xs = CBt + NCBT * kTile, *dys = xs + XB;  // dys: 2 buffers
@@ -922,13 +1158,24 @@ __global__ void __launch_bounds__(kThreadsWide, 1) tc_bwd_orange_kernel(const Pa
     auto tile_of = [&](int mb, int tj) -> uint8_t * {  // CB^T tile of s-block mb, t-tile tj (tj >= 2 mb)
         return CBt + (mb == 0 ? tj : (Q / 64) + tj - 2) * kTile;
     };
-    auto load_raw = [&](int h, int b) {
-        float *f = fbuf + b * FST;
-        const float *cumg = p.cumA + ix_chunk(p, bi, h, c) * Q;
-        for (int l = tid; l < Q; l += kThreadsWide) {
-            f[l] = cumg[l];
-            f[Q + l] = l < vrows ? p.dt[ix_dt(p, bi, h, t0 + l)] : 0.f;
+    // raw per-head scalars (cumA, dt, D): fetched into registers (thread l holds
+    // token l) a head before they are staged in buffer `b`
+    float r_cum = 0.f, r_dt = 0.f, r_D = 0.f;
+    auto fetch = [&](int k) {
+        const int h = h_begin + k;
+        if (tid < Q) {
+            r_cum = p.cumA[ix_chunk(p, bi, h, c) * Q + tid];
+            r_dt = tid < vrows ? p.dt[ix_dt(p, bi, h, t0 + tid)] : 0.f;
         }
+        if (tid == 0) r_D = p.D[h];
+    };
+    auto stash = [&](int b) {
+        float *f = fbuf + b * FST;
+        if (tid < Q) {
+            f[tid] = r_cum;
+            f[Q + tid] = r_dt;
+        }
+        if (tid == 0) f[DOFF] = r_D;
     };
     // pivot tables from the raw cumA (visible after a barrier)
     auto derive = [&](int b) {
@@ -981,7 +1228,9 @@ __global__ void __launch_bounds__(kThreadsWide, 1) tc_bwd_orange_kernel(const Pa
         issue_dy(0);
         if (nh > 1) issue_dy(1);
     }
-    load_raw(h_begin, 0);
+    fetch(0);
+    stash(0);
+    if (nh > 1) fetch(1);
     int x_iss = 1, x_land = 0, dy_iss = nh > 1 ? 2 : 1, dy_land = 0;
     bool ok = wait_all(&bar_res, 0, true);
     derive(0);
@@ -1032,7 +1281,10 @@ __global__ void __launch_bounds__(kThreadsWide, 1) tc_bwd_orange_kernel(const Pa
             dd = warp_sum(dd);
             if (lane == 0) red[warp] = dd;
         }
-        if (k + 1 < nh) load_raw(h + 1, sb ^ 1);
+        if (k + 1 < nh) {  // buffer sb ^ 1 was last read before this head's first barrier
+            stash(sb ^ 1);
+            if (k + 2 < nh) fetch(k + 2);
+        }
         ok = mbar_wait(&bar_m1, (uint32_t)(k & 1)) && ok;
         tc_fence_after();
         // x is free once dW^T is computed: refill with the next head
@@ -1159,7 +1411,7 @@ __global__ void __launch_bounds__(kThreadsWide, 1) tc_bwd_orange_kernel(const Pa
         if (tid == 0 && ok && k + 2 < nh) issue_dy(k + 2);
         if (k + 2 < nh) dy_iss = k + 3;
         // ---- epilogue 2: dx = W^T dy + D dy (the K3 backward adds its term afterwards)
-        const float Dh = p.D[h];
+        const float Dh = f[DOFF];
         for (int mb = 0; mb < NT; ++mb) {
             const int s = 128 * mb + 32 * q4 + lane;
             float acc[32];
@@ -1639,24 +1891,6 @@ __global__ void __launch_bounds__(kThreadsWide + 32, 1) tc_bwd_dbc_kernel(const 
         };
         if (nh > 0) fetch(0, c_cur, d_cur, e_cur);
         if (nh > 1) fetch(1, c_nx, d_nx, e_nx);
-        // scale the 64 bf16 of row t in place (zero past valid_len: a select)
-        auto scale_row = [&](uint8_t *tile, float f) {
-            const uint32_t base = smem_u32(tile);
-#pragma unroll
-            for (int c8 = 0; c8 < 8; ++c8) {
-                const uint32_t a = base + sw128_chunk(t, c8);
-                if (!valid) {
-                    st_shared_v4(a, 0u, 0u, 0u, 0u);
-                    continue;
-                }
-                uint4 v = ld_shared_v4(a);
-                v.x = pack_bf2(bf_lo(v.x) * f, bf_hi(v.x) * f);
-                v.y = pack_bf2(bf_lo(v.y) * f, bf_hi(v.y) * f);
-                v.z = pack_bf2(bf_lo(v.z) * f, bf_hi(v.z) * f);
-                v.w = pack_bf2(bf_lo(v.w) * f, bf_hi(v.w) * f);
-                st_shared_v4(a, v.x, v.y, v.z, v.w);
-            }
-        };
         for (int k = 0; k < nh; ++k) {
             const int st = k & 1;
             uint8_t *base = sm + st * STG;
@@ -1669,8 +1903,8 @@ __global__ void __launch_bounds__(kThreadsWide + 32, 1) tc_bwd_dbc_kernel(const 
             if (k + 2 < nh) fetch(k + 2, c_nx, d_nx, e_nx);
             bool okk = mbar_wait(&bar_tma[st], (uint32_t)((k >> 1) & 1));
             if (okk && t < Q) {
-                scale_row(dys, e_row);
-                scale_row(xs, b_row);
+                scale_row_bf16(dys, t, e_row, valid);
+                scale_row_bf16(xs, t, b_row, valid);
             }
             fence_async_smem();
             tc_fence_before();
@@ -1842,18 +2076,18 @@ cudaError_t launch(K kernel, unsigned grid, size_t smem, cudaStream_t s, const P
 }
 
 constexpr size_t smem_k2(int Q) { return 1024 + 4 * (size_t)Q * 128; }
-constexpr size_t smem_k3(int Q) { return 1024 + 3 * (size_t)Q * 128 + 4 * Q; }
+constexpr size_t smem_k3(int Q) { return 1024 + 2 * (size_t)Q * 128 + 4 * (size_t)Q * 128; }
 constexpr size_t smem_k5(int Q) {
     return 1024 + 3 * (size_t)Q * 128 + 2 * 64 * 128 + (size_t)kTile * (Q / 128) * (Q / 128 + 1) +
            4 * 4 * (4 * Q + 24);
 }
-constexpr size_t smem_blue(int Q) { return 1024 + 3 * (size_t)Q * 128 + 2 * 64 * 128 + 4 * Q; }
+constexpr size_t smem_blue(int Q) { return 1024 + 2 * (size_t)Q * 128 + 3 * ((size_t)Q * 128 + 2 * 64 * 128); }
 constexpr size_t smem_k3bwd(int Q) {
     return 1024 + 2 * (size_t)Q * 128 + 2 * ((size_t)Q * 128 + 2 * 64 * 128) + 4 * (3 * 3 * Q + 2 * Q);
 }
 constexpr size_t smem_orange(int Q) {
     return 1024 + (size_t)kTile * (Q == 256 ? 6 : 2) + 3 * (size_t)Q * 128 +
-           4 * (2 * (2 * Q + 384 + 1024 + 24) + (Q / 128) * 4 * Q + 2 * Q + 8);
+           4 * (2 * (2 * Q + 384 + 1024 + 28) + (Q / 128) * 4 * Q + 2 * Q + 8);
 }
 // Padded above a third of the SM's shared memory: two CTAs of 256 TMEM columns
 // each may share an SM, a third must not.
@@ -1869,6 +2103,8 @@ static_assert(smem_orange(256) <= 232448 && smem_orange(256) > 116 * 1024, "ORAN
 static_assert(smem_k3bwd(256) <= 232448 && smem_k3bwd(256) > 116 * 1024, "K3 backward: one CTA per SM");
 static_assert(smem_k2(256) > 116 * 1024, "K2 (512 TMEM columns): one CTA per SM");
 static_assert(smem_k5(256) <= 232448 && smem_k5(256) > 116 * 1024, "K5: one CTA per SM");
+static_assert(smem_k3(256) <= 232448 && smem_blue(256) <= 232448, "K3 / BLUE shared memory");
+static_assert(smem_blue(128) > 116 * 1024, "BLUE (512 TMEM columns): one CTA per SM");
 static_assert(smem_dbc(256) <= 232448, "group backward shared memory");
 static_assert(3 * (smem_dcb(128) + 1024) > 233472 && 2 * (smem_dcb(256) + 1024) <= 233472,
               "G1: two CTAs per SM, never three");
@@ -1881,15 +2117,17 @@ bool tc_supported(int64_t P, int64_t N, int64_t Q) { return P == kP && N == kN &
 int tc_dD_per(int64_t) { return 1; }
 int tc_dcb_slices(const ssd_dims &d) {
     // CTAs: one per 128 x 128 block on or below the diagonal and head slice;
-    // two fit an SM.  Minimise (waves x heads per CTA), fewest slices on ties
-    // (each slice adds a partial d_cb to write and read back).
+    // two fit an SM.  Head slices only when the blocks alone leave SMs idle
+    // (each slice adds a partial d_cb to write and read back): then minimise
+    // (waves x heads per CTA) over up to two waves, fewest slices on ties.
     const long long hpg = d.nheads / d.ngroups;
     const long long n = (d.seqlen + d.chunk_len - 1) / d.chunk_len;
     const long long nt = d.chunk_len / 128;
     const long long ctas = d.batch * n * d.ngroups * (nt * (nt + 1) / 2);
     const long long slots = 2 * 152;
+    if (ctas >= slots) return 1;
     long long best = 1, best_cost = -1;
-    for (long long s = 1; s <= hpg && s <= 16; ++s) {
+    for (long long s = 1; s <= hpg && ctas * s <= 2 * slots + ctas; ++s) {
         const long long cost = ((ctas * s + slots - 1) / slots) * ((hpg + s - 1) / s);
         if (best_cost < 0 || cost < best_cost) {
             best = s;
@@ -1908,6 +2146,21 @@ int tc_k5_slices(const ssd_dims &d) {
     while (s < hpg && groups * s < 2 * 152) ++s;
     if (s < 1) s = 1;
     return (int)s;
+}
+int tc_k3_slices(const ssd_dims &d) {
+    // one CTA per SM: minimise (waves x heads per CTA), fewest slices on ties
+    const long long hpg = d.nheads / d.ngroups;
+    const long long n = (d.seqlen + d.chunk_len - 1) / d.chunk_len;
+    const long long groups = d.batch * n * d.ngroups;
+    long long best = 1, best_cost = -1;
+    for (long long s = 1; s <= hpg; ++s) {
+        const long long cost = ((groups * s + 151) / 152) * ((hpg + s - 1) / s);
+        if (best_cost < 0 || cost < best_cost) {
+            best = s;
+            best_cost = cost;
+        }
+    }
+    return (int)best;
 }
 int tc_group_slices(const ssd_dims &d) {
     const long long hpg = d.nheads / d.ngroups;
@@ -1935,8 +2188,8 @@ cudaError_t launch_tc_k3(const Params &p, cudaStream_t s) {
     TcMaps m;
     cudaError_t e = make_maps(p, &m, false);
     if (e != cudaSuccess) return e;
-    const unsigned grid = (unsigned)(p.b * p.n * p.H);
-#define CALL(Q) launch(tc_k3_kernel<Q>, grid, smem_k3(Q), s, p, m)
+    const unsigned grid = (unsigned)(p.b * p.n * p.G * p.nslice_k3);
+#define CALL(Q) launch(tc_k3_kernel<Q>, grid, smem_k3(Q), s, p, m, kThreadsWide + 32)
     return SSD_TC_DISPATCH(p.Q, CALL);
 #undef CALL
 }
@@ -1955,8 +2208,8 @@ cudaError_t launch_tc_bwd_blue(const Params &p, cudaStream_t s) {
     TcMaps m;
     cudaError_t e = make_maps(p, &m, true);
     if (e != cudaSuccess) return e;
-    const unsigned grid = (unsigned)(p.b * p.n * p.H);
-#define CALL(Q) launch(tc_bwd_blue_kernel<Q>, grid, smem_blue(Q), s, p, m)
+    const unsigned grid = (unsigned)(p.b * p.n * p.G * p.nslice_k3);
+#define CALL(Q) launch(tc_bwd_blue_kernel<Q>, grid, smem_blue(Q), s, p, m, kThreadsWide + 32)
     return SSD_TC_DISPATCH(p.Q, CALL);
 #undef CALL
 }

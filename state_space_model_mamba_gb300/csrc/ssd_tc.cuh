@@ -14,6 +14,8 @@ int tc_dD_per(int64_t Q);
 int tc_dcb_slices(const ssd_dims &d);
 // Head slices of the persistent per-group kernels (K5, K3 and ORANGE backward).
 int tc_k5_slices(const ssd_dims &d);
+// Head slices of the streaming per-group kernels (K3 forward, BLUE backward).
+int tc_k3_slices(const ssd_dims &d);
 int tc_group_slices(const ssd_dims &d);
 
 cudaError_t launch_tc_k2(const Params &p, cudaStream_t s);
