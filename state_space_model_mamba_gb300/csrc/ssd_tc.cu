@@ -75,6 +75,11 @@ __device__ __forceinline__ bool bar_and(int id, int nthreads, bool v) {
     return r != 0;
 }
 
+// Barrier among the `nthreads` threads (whole warps) that use named barrier `id`.
+__device__ __forceinline__ void bar_sync_n(int id, int nthreads) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
 // Synchronise the CTA around tcgen05 work (orders TMEM accesses with the barrier).
 __device__ __forceinline__ void tc_sync() {
     tc_fence_before();
@@ -1094,41 +1099,47 @@ __global__ void __launch_bounds__(kThreadsWide, 1) tc_bwd_k3_kernel(const Params
 
 // ====================================================================== ORANGE backward
 // CTA per (b, chunk, group, head slice), 256 threads, looping over the slice's
-// heads.  The ORANGE block of the backward in transposed form: TMEM lane = the
-// source position s, so the column sums of the page (ddt over targets, the
-// source part of d cumA) become per-thread row sums and only the target part
-// of d cumA needs a cross-lane reduction.  Per head and 128-row s-block mb:
-//   dW^T[s, t] = sum_p x[s, p] dy[t, p]          t >= 128 mb      (TMEM, A = x, B = dy, K-major)
-//   W^T[s, t]  = CB^T[s, t] exp(cumA_t - cumA_s) dt_s   (t >= s)  (packed bf16 in TMEM, in place)
-//   ddt_orange[s] = sum_t dW^T CB^T decay,  src[s] = dt_s ddt_orange[s],  tgt[t] = sum_s dW^T W^T
-//   dx[s, p]  += sum_t W^T[s, t] dy[t, p] + D dy[s, p]    (A = W^T in TMEM, B = dy MN-major)
-// CB^T stays resident; x is single-buffered (refilled once dW^T is computed),
-// dy double-buffered.  The decay is factored through 64-group pivots off the
-// diagonal groups and 16-wide sub-block pivots inside them (all factors <= 1).
-// This kernel writes dx, ddt_main and dcum_main first; the K3 backward kernel
-// runs after it and adds the K3 terms.
+// heads; thread 0 refills the CB^T copy and x as soon as the previous head's
+// MMAs complete (every thread waits for them anyway), dy two heads ahead.  The ORANGE block of the backward is
+// restated so that every reduction becomes a per-row dot product of two MMA
+// outputs (thread = row of the chunk):
+//   M^T[s, t]   = CB^T[s, t] exp(cumA_t - cumA_s)   (t >= s, 0 above): built per
+//                 head in shared memory from a copy of CB^T kept in TMEM
+//   dx'[s, p]   = sum_t M^T[s, t] dy[t, p]           (A = M^T K-major,  B = dy MN-major)
+//   yo[t, p]    = sum_s M^T[s, t] dt_s x[s, p]       (A = M^T MN-major, B = dt*x MN-major)
+//   ddt_orange[s] = sum_p x[s, p] dx'[s, p]          (= sum_t dW[t, s] CB[t, s] decay[t, s])
+//   dx[s, p]    = dt_s dx'[s, p] + D dy[s, p]        (= sum_t W[t, s] dy[t, p] + D dy[s, p])
+//   tgt[t]      = sum_p dy[t, p] yo[t, p]            (= sum_s dW[t, s] W[t, s])
+//   src[s]      = sum_p (dt x)[s, p] dx'[s, p]       (= sum_t dW[t, s] W[t, s])
+// with dW = dy x^T and W = M diag(dt); the page's column sums over targets and
+// the row sums over sources reduce to these because dW is a product.  tgt and
+// src use the same bf16 operands (M^T and dt x as the MMAs saw them), so their
+// sums over the chunk cancel to fp32 rounding as the page's do.  M^T is
+// built in two halves (s-block 1, then s-block 0) so the first half's MMAs run
+// while the second half is built.  The decay is factored through 64-group
+// pivots off the diagonal groups and 16-wide sub-block pivots inside them (all
+// factors <= 1).  This kernel writes dx, ddt_main, dcum_main and the dD
+// partials first; the K3 backward kernel runs after it and adds its terms.
 template <int Q>
 __global__ void __launch_bounds__(kThreadsWide, 1) tc_bwd_orange_kernel(const Params p, const __grid_constant__ TcMaps maps) {
     constexpr int NT = Q / 128;
     constexpr uint32_t XB = Q * 128;
-    constexpr int NCBT = NT == 2 ? 6 : 2;            // CB^T tiles: mb0 Q/64, mb1 Q/64 - 2
-    constexpr uint32_t NCOL = NT == 2 ? 512 : 256;
-    constexpr uint32_t DXCOL = NT == 2 ? 384 : 128;  // dx accumulators (dW^T occupies [0, DXCOL))
-    // per-head scalars: cum Q | dts Q | E (pivot rows) 384 | E16 16x64 | piv 8 | piv16 16
-    constexpr int EOFF = 2 * Q, E16OFF = EOFF + 384, POFF = E16OFF + 1024, P16OFF = POFF + 8;
-    constexpr int DOFF = P16OFF + 16;  // D of the head
+    constexpr int NCBT = NT == 2 ? 6 : 2;  // M^T tiles: s-block 0 Q/64, s-block 1 Q/64 - 2
+    constexpr int NCONS = kThreadsWide;
+    constexpr int NSC = 3;                 // scalar buffers: staged two heads ahead
+    // per-head tables (32-bit words): cum Q | dt Q | E pairs 192 | E16 pairs 16 x 32 | piv 8 | piv16 16 | D 4
+    constexpr int E2OFF = 2 * Q, E16OFF = E2OFF + 192, POFF = E16OFF + 512, P16OFF = POFF + 8;
+    constexpr int DOFF = P16OFF + 16;
     constexpr int FST = DOFF + 4;
+    constexpr uint32_t CBCOL0 = 256, CBCOL1 = 384;  // CB^T resident in TMEM (packed bf16 pairs)
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = align1024(smem_raw);
-    uint8_t *CBt = sm, *xs = CBt + NCBT * kTile, *dys = xs + XB;  // dys: 2 buffers
-    float *fbuf = reinterpret_cast<float *>(dys + 2 * XB);       // [2][FST]
-    float *colp = fbuf + 2 * FST;                                 // [NT][4][Q]  tgt partials
-    float *rowp = colp + NT * 4 * Q;                              // [2 hf][Q] ddt_orange halves
-    float *red = rowp + 2 * Q;                                    // [8] dD partials
-    __shared__ uint64_t bar_res, bar_x, bar_dy[2], bar_m1, bar_m2;
+    uint8_t *Mt = sm, *xs = Mt + NCBT * kTile, *dys = xs + XB;  // dys: 2 buffers
+    float *fbuf = reinterpret_cast<float *>(dys + 2 * XB);       // [NSC][FST]
+    __shared__ uint64_t bar_cb, bar_x, bar_dy[2], bar_mma;
     __shared__ uint32_t s_tmem;
+    __shared__ int s_x_issued, s_dy_issued, s_landed;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int q4 = warp & 3, hf = warp >> 2;
     int idx = blockIdx.x;
     const int slice = idx % p.nslice_k5;
     idx /= p.nslice_k5;
@@ -1137,326 +1148,347 @@ __global__ void __launch_bounds__(kThreadsWide, 1) tc_bwd_orange_kernel(const Pa
     const int vrows = min(Q, valid_len_of(p, bi) - t0);
     const int per = (p.hpg + p.nslice_k5 - 1) / p.nslice_k5;
     const int h_begin = g * p.hpg + slice * per;
-    const int h_end = min(g * p.hpg + p.hpg, h_begin + per);
-    const int nh = h_end - h_begin;
+    const int nh = max(0, min(g * p.hpg + p.hpg, h_begin + per) - h_begin);
     bf16 *DX = (bf16 *)p.dx;
-    if (nh <= 0) return;
+    if (nh == 0) return;
     if (vrows <= 0) {  // a chunk wholly past valid_len contributes nothing
         const int rows = min(Q, p.L - t0);
-        for (int hh = h_begin; hh < h_end; ++hh) {
-            for (int i = tid; i < rows * (kP / 8); i += kThreadsWide)
+        for (int hh = h_begin; hh < h_begin + nh; ++hh) {
+            for (int i = tid; i < rows * (kP / 8); i += blockDim.x)
                 reinterpret_cast<uint4 *>(DX + ix_x(p, bi, t0 + i / 8, hh, 0))[i % 8] = make_uint4(0, 0, 0, 0);
             const size_t cb = ix_chunk(p, bi, hh, c) * Q;
-            for (int i = tid; i < Q; i += kThreadsWide) {
+            for (int i = tid; i < Q; i += blockDim.x) {
                 p.dcum_main[cb + i] = 0.f;
                 p.ddt_main[cb + i] = 0.f;
             }
-            if (tid == 0) p.dD_part[((size_t)bi * p.n + c) * p.H + hh] = 0.f;
+            for (int i = tid; i < p.dD_per; i += blockDim.x)
+                p.dD_part[(((size_t)bi * p.n + c) * p.H + hh) * p.dD_per + i] = 0.f;
         }
         return;
     }
-    auto tile_of = [&](int mb, int tj) -> uint8_t * {  // CB^T tile of s-block mb, t-tile tj (tj >= 2 mb)
-        return CBt + (mb == 0 ? tj : (Q / 64) + tj - 2) * kTile;
-    };
-    // raw per-head scalars (cumA, dt, D): fetched into registers (thread l holds
-    // token l) a head before they are staged in buffer `b`
-    float r_cum = 0.f, r_dt = 0.f, r_D = 0.f;
-    auto fetch = [&](int k) {
-        const int h = h_begin + k;
-        if (tid < Q) {
-            r_cum = p.cumA[ix_chunk(p, bi, h, c) * Q + tid];
-            r_dt = tid < vrows ? p.dt[ix_dt(p, bi, h, t0 + tid)] : 0.f;
-        }
-        if (tid == 0) r_D = p.D[h];
-    };
-    auto stash = [&](int b) {
-        float *f = fbuf + b * FST;
-        if (tid < Q) {
-            f[tid] = r_cum;
-            f[Q + tid] = r_dt;
-        }
-        if (tid == 0) f[DOFF] = r_D;
-    };
-    // pivot tables from the raw cumA (visible after a barrier)
-    auto derive = [&](int b) {
-        float *f = fbuf + b * FST;
-        // E[sg][t] = exp(cumA_t - cumA[64 sg + 63]) for t >= 64 (sg + 1); rows packed at 0, 192, 320
-        for (int i = tid; i < 384; i += kThreadsWide) {
-            const int sg = i < 192 ? 0 : (i < 320 ? 1 : 2);
-            const int base = sg == 0 ? 0 : (sg == 1 ? 192 : 320);
-            const int t = 64 * (sg + 1) + (i - base);
-            f[EOFF + i] = (sg < Q / 64 - 1 && t < Q) ? __expf(f[t] - f[64 * sg + 63]) : 0.f;
-        }
-        // E16[v][tt] = exp(cumA_t - cumA[16 v + 15]) for t = 64 (v / 4) + tt in v's 64-group
-        for (int i = tid; i < 1024; i += kThreadsWide) {
-            const int v = i >> 6, tt = i & 63;
-            const int t = 64 * (v >> 2) + tt;
-            f[E16OFF + i] = (16 * v < Q && t < Q && t > 16 * v + 15) ? __expf(f[t] - f[16 * v + 15]) : 0.f;
-        }
-        for (int j = tid; j < Q / 64; j += kThreadsWide) f[POFF + j] = f[64 * j + 63];
-        for (int j = tid; j < Q / 16; j += kThreadsWide) f[P16OFF + j] = f[16 * j + 15];
-    };
-    auto issue_x = [&](int h) {
-        mbar_arrive_expect_tx(&bar_x, XB);
-        for (int j = 0; j < NT; ++j) tma_load_4d(xs + j * kTile, &maps.x, &bar_x, 0, h, t0 + 128 * j, bi);
-    };
-    auto issue_dy = [&](int k) {
-        const int h = h_begin + k, b = k & 1;
-        mbar_arrive_expect_tx(&bar_dy[b], XB);
-        for (int j = 0; j < NT; ++j)
-            tma_load_4d(dys + b * XB + j * kTile, &maps.dy, &bar_dy[b], 0, h, t0 + 128 * j, bi);
+    auto tile_of = [&](int mb, int tj) -> uint8_t * {  // M^T tile of s-block mb, t-tile tj (tj >= 2 mb)
+        return Mt + (mb == 0 ? tj : (Q / 64) + tj - 2) * kTile;
     };
     if (tid == 0) {
-        mbar_init(&bar_res, 1);
+        mbar_init(&bar_cb, 1);
         mbar_init(&bar_x, 1);
         mbar_init(&bar_dy[0], 1);
         mbar_init(&bar_dy[1], 1);
-        mbar_init(&bar_m1, 1);
-        mbar_init(&bar_m2, 1);
+        mbar_init(&bar_mma, 1);
         mbar_fence_init();
+        s_x_issued = 0;
+        s_dy_issued = 0;
+        s_landed = 0;
     }
-    if (warp == 0) tmem_alloc(&s_tmem, NCOL);
+    if (warp == 0) tmem_alloc(&s_tmem, 512);
     tc_sync();
-    const uint32_t tm = s_tmem;
-    if (tid == 0) {
-        mbar_arrive_expect_tx(&bar_res, NCBT * kTile);
-        const int cbrow = ((bi * p.n + c) * p.G + g) * Q;
+    const uint32_t tm = s_tmem;  // dx'[mb] at 64 mb, yo[tb] at 128 + 64 tb, CB^T at 256
+    bool ok = true;
+    const int cbrow = ((bi * p.n + c) * p.G + g) * Q;
+    auto issue_x = [&](int k) {  // thread 0: x of head k
+        mbar_arrive_expect_tx(&bar_x, XB);
+        for (int j = 0; j < NT; ++j) tma_load_4d(xs + j * kTile, &maps.x, &bar_x, 0, h_begin + k, t0 + 128 * j, bi);
+        s_x_issued = k + 1;
+    };
+    auto issue_dy = [&](int k) {  // thread 0: dy of head k into buffer k & 1
+        const int b = k & 1;
+        mbar_arrive_expect_tx(&bar_dy[b], XB);
+        for (int j = 0; j < NT; ++j)
+            tma_load_4d(dys + b * XB + j * kTile, &maps.dy, &bar_dy[b], 0, h_begin + k, t0 + 128 * j, bi);
+        s_dy_issued = k + 1;
+    };
+    if (tid == 0) {  // CB^T once (staged through the M^T buffer into TMEM), then the head ring
+        mbar_arrive_expect_tx(&bar_cb, NCBT * kTile);
         for (int mb = 0; mb < NT; ++mb)
             for (int tj = 2 * mb; tj < Q / 64; ++tj)
-                tma_load_2d(tile_of(mb, tj), &maps.cbt, &bar_res, 64 * tj, cbrow + 128 * mb);
-        issue_x(h_begin);
+                tma_load_2d(tile_of(mb, tj), &maps.cbt, &bar_cb, 64 * tj, cbrow + 128 * mb);
+        issue_x(0);
         issue_dy(0);
-        if (nh > 1) issue_dy(1);
     }
-    fetch(0);
-    stash(0);
-    if (nh > 1) fetch(1);
-    int x_iss = 1, x_land = 0, dy_iss = nh > 1 ? 2 : 1, dy_land = 0;
-    bool ok = wait_all(&bar_res, 0, true);
-    derive(0);
-    for (int k = 0; k < nh && ok; ++k) {
-        const int h = h_begin + k, sb = k & 1;
-        const float *f = fbuf + sb * FST;
-        const float *cum = f, *dts = f + Q, *E = f + EOFF, *E16 = f + E16OFF, *piv = f + POFF, *piv16 = f + P16OFF;
-        uint8_t *dyb = dys + sb * XB;
-        // ---- x_k, dy_k landed; dD partial; padded rows zeroed
-        ok = mbar_wait(&bar_x, (uint32_t)(k & 1)) && ok;
-        ok = mbar_wait(&bar_dy[sb], (uint32_t)((k >> 1) & 1)) && ok;
-        if (ok) {
-            x_land = k + 1;
-            dy_land = k + 1;
-        }
-        if (vrows < Q) {
-            __syncthreads();
-            zero_rows_from(xs, Q, vrows);
-            zero_rows_from(dyb, Q, vrows);
-            fence_async_smem();
-        }
+    {
+        const int i = tid;  // chunk row of this thread (token for the row outputs)
+        const bool valid = i < vrows;
+        float r_cum = 0.f, r_dt = 0.f, r_D = 0.f;
+        auto fetch = [&](int k) {
+            const int h = h_begin + k;
+            if (i < Q) {
+                r_cum = p.cumA[ix_chunk(p, bi, h, c) * Q + i];
+                r_dt = valid ? p.dt[ix_dt(p, bi, h, t0 + i)] : 0.f;
+            }
+            if (i == 0) r_D = p.D[h];
+        };
+        auto stash = [&](int k) {
+            float *f = fbuf + (k % NSC) * FST;
+            if (i < Q) {
+                f[i] = r_cum;
+                f[Q + i] = r_dt;
+            }
+            if (i == 0) f[DOFF] = r_D;
+        };
+        // pivot tables from the raw cumA (visible after a barrier), as bf16 pairs
+        auto derive = [&](int k) {
+            float *f = fbuf + (k % NSC) * FST;
+            uint32_t *f2 = reinterpret_cast<uint32_t *>(f);
+            // E[sg][t] = exp(cumA_t - cumA[64 sg + 63]) for t >= 64 (sg + 1); pair rows at 0, 96, 160
+            for (int e = i; e < 192; e += NCONS) {
+                const int sg = e < 96 ? 0 : (e < 160 ? 1 : 2);
+                const int t = 64 * (sg + 1) + 2 * (e - (sg == 0 ? 0 : (sg == 1 ? 96 : 160)));
+                const float pv = f[64 * sg + 63];
+                f2[E2OFF + e] = (sg < Q / 64 - 1 && t < Q) ? pack_bf2(__expf(f[t] - pv), __expf(f[t + 1] - pv)) : 0u;
+            }
+            // E16[v][tt] = exp(cumA_t - cumA[16 v + 15]) for t = 64 (v / 4) + tt past v's sub-block
+            for (int e = i; e < 512; e += NCONS) {
+                const int v = e >> 5, t = 64 * (v >> 2) + 2 * (e & 31);
+                float lo = 0.f, hi = 0.f;
+                if (16 * v < Q && t < Q) {
+                    const float pv = f[16 * v + 15];
+                    if (t > 16 * v + 15) lo = __expf(f[t] - pv);
+                    if (t + 1 > 16 * v + 15) hi = __expf(f[t + 1] - pv);
+                }
+                f2[E16OFF + e] = pack_bf2(lo, hi);
+            }
+            if (i < Q / 64) f[POFF + i] = f[64 * i + 63];
+            if (i < Q / 16) f[P16OFF + i] = f[16 * i + 15];
+        };
+        // M^T[s, t] for row s of t-tile tj: CB^T from TMEM, scaled as packed bf16 pairs
+        // (off the row's own 16-wide sub-block), written to the shared-memory tile
+        const int q4 = warp & 3;  // this warp's TMEM lane quarter (= row s % 128 / 32)
+        auto cb_col = [&](int mb, int tj) -> uint32_t { return (mb == 0 ? CBCOL0 : CBCOL1) + 32 * (tj - 2 * mb); };
+        // Each thread owns exactly one row-tile on the diagonal 64-group (see the unit
+        // mapping below); the CB^T values of that row's own 16-wide sub-block are kept
+        // in registers, so the sub-block's direct exponentials need no lane-dependent
+        // TMEM column.
+        uint32_t cbown[8];
+        auto transform = [&](const float *f, int s, int tj) {
+            const int sg = s >> 6, row = s & 127, mb = s >> 7;
+            const uint32_t base = smem_u32(tile_of(mb, tj));
+            uint32_t cb[32];
+            tmem_ld32u(tmem_addr(tm, 32 * q4, cb_col(mb, tj)), cb);
+            if (tj < sg) {  // wholly above the diagonal (never read by an MMA; kept finite)
+#pragma unroll
+                for (int c8 = 0; c8 < 8; ++c8) st_shared_v4(base + sw128_chunk(row, c8), 0u, 0u, 0u, 0u);
+                return;
+            }
+            const uint32_t *f2 = reinterpret_cast<const uint32_t *>(f);
+            const float cs = f[s];
+            // off the diagonal group: column table of the 64-group pivot; on it: column table
+            // of the row's 16-wide sub-block pivot (0 up to and including that sub-block)
+            const bool diag = tj == sg;
+            const float fr = __expf((diag ? f[P16OFF + (s >> 4)] : f[POFF + sg]) - cs);
+            const uint32_t fr2 = pack_bf2(fr, fr);
+            const uint32_t *Erow = diag ? f2 + E16OFF + 32 * (s >> 4) - 32 * sg
+                                        : f2 + E2OFF + (sg == 0 ? 0 : (sg == 1 ? 96 : 160)) - 32 * (sg + 1);
+#pragma unroll
+            for (int c8 = 0; c8 < 8; ++c8) {
+                const uint4 e = *reinterpret_cast<const uint4 *>(Erow + 32 * tj + 4 * c8);
+                st_shared_v4(base + sw128_chunk(row, c8), bmul2(bmul2(cb[4 * c8], e.x), fr2),
+                             bmul2(bmul2(cb[4 * c8 + 1], e.y), fr2), bmul2(bmul2(cb[4 * c8 + 2], e.z), fr2),
+                             bmul2(bmul2(cb[4 * c8 + 3], e.w), fr2));
+            }
+            if (diag) {  // the row's own 16-wide sub-block: direct exponentials, 0 for t < s
+                const int t16 = s & ~15, us = (s & 63) >> 4;
+                float w[16];
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    const uint32_t pr = cbown[j >> 1];
+                    const float cv = (j & 1) ? bf_hi(pr) : bf_lo(pr);
+                    w[j] = t16 + j >= s ? cv * __expf(f[t16 + j] - cs) : 0.f;
+                }
+                st_shared_v4(base + sw128_chunk(row, 2 * us), pack_bf2(w[0], w[1]), pack_bf2(w[2], w[3]),
+                             pack_bf2(w[4], w[5]), pack_bf2(w[6], w[7]));
+                st_shared_v4(base + sw128_chunk(row, 2 * us + 1), pack_bf2(w[8], w[9]), pack_bf2(w[10], w[11]),
+                             pack_bf2(w[12], w[13]), pack_bf2(w[14], w[15]));
+            }
+        };
+        // CB^T: shared-memory tiles (TMA) -> TMEM, by the threads that later transform each row
+        auto cb_to_tmem = [&](int s, int tj) {
+            const int row = s & 127, mb = s >> 7;
+            const uint32_t base = smem_u32(tile_of(mb, tj));
+            uint32_t v[32];
+#pragma unroll
+            for (int c8 = 0; c8 < 8; ++c8) {
+                const uint4 u = ld_shared_v4(base + sw128_chunk(row, c8));
+                v[4 * c8] = u.x;
+                v[4 * c8 + 1] = u.y;
+                v[4 * c8 + 2] = u.z;
+                v[4 * c8 + 3] = u.w;
+            }
+            tmem_st32u(tmem_addr(tm, 32 * q4, cb_col(mb, tj)), v);
+            if (tj == (s >> 6)) {  // this thread's diagonal row-tile: keep its own sub-block
+                const int us = (s & 63) >> 4;
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    cbown[j] = us == 0 ? v[j] : (us == 1 ? v[8 + j] : (us == 2 ? v[16 + j] : v[24 + j]));
+            }
+        };
+        // row-tile units: s-block 1 (phase A) row 128 + r, t-tile 2 + (i / 128); s-block 0
+        // (phase B) row r, t-tiles 1 - (i / 128) and 3 - (i / 128).  Every thread gets
+        // exactly one unit on the diagonal 64-group and TMEM lane quarter r / 32.
+        const int r = i & 127, hi = i >> 7;
+        ok = mbar_wait(&bar_cb, 0);
+        if (NT == 2) cb_to_tmem(128 + r, 2 + hi);
+        cb_to_tmem(r, 1 - hi);
+        if (NT == 2) cb_to_tmem(r, 3 - hi);
         tc_fence_before();
-        ok = __syncthreads_and(ok ? 1 : 0) != 0;  // also: tables of head k derived, previous head done
+        ok = bar_and(1, NCONS, ok);
         tc_fence_after();
-        if (!ok) break;
-        if (tid == 0) {
-            for (int mb = 0; mb < NT; ++mb) {
-                const uint32_t id = idesc_bf16(128, Q - 128 * mb, false, false);
-                for (int ks = 0; ks < kP / 16; ++ks)
-                    mma_bf16(tm + (mb == 0 ? 0u : 256u), sdesc_kmajor(smem_u32(xs + mb * kTile), ks, XB),
-                             sdesc_kmajor(smem_u32(dyb + mb * kTile), ks, XB), id, ks > 0);
-            }
-            mma_commit(&bar_m1);
+        fetch(0);
+        stash(0);
+        if (nh > 1) {
+            fetch(1);
+            stash(1);
         }
-        {   // dD partial while the MMA runs
-            float dd = 0.f;
-            for (int mb = 0; mb < NT; ++mb) {
-                const int s = mb * 128 + 32 * q4 + lane;
+        if (nh > 2) fetch(2);
+        bar_sync_n(1, NCONS);
+        derive(0);
+        bar_sync_n(1, NCONS);
+        // epilogue mapping: warp w holds TMEM lanes 32 (w % 4) .. of block w / 4 = row i's block
+        const int blk = warp >> 2;
+        for (int k = 0; k < nh; ++k) {
+            const int h = h_begin + k, db = k & 1;
+            const float *f = fbuf + (k % NSC) * FST;
+            uint8_t *dyb = dys + db * XB;
+            // ---- head k's tiles landed: keep row i of x and dy, stage dt * x, zero padding
+            bool okk = ok && mbar_wait(&bar_x, (uint32_t)(k & 1));
+            okk = okk && mbar_wait(&bar_dy[db], (uint32_t)((k >> 1) & 1));
+            uint4 xr[8];  // row i of x; dy row i stays in shared memory until the epilogue
+            if (i < Q) {
+                const float dti = f[Q + i];
+                const uint32_t xb = smem_u32(xs), yb = smem_u32(dyb);
 #pragma unroll
-                for (int c8 = 0; c8 < 4; ++c8) {
-                    const uint4 xv = ld_shared_v4(smem_u32(xs) + sw128_chunk(s, 4 * hf + c8));
-                    const uint4 dv = ld_shared_v4(smem_u32(dyb) + sw128_chunk(s, 4 * hf + c8));
-                    dd += bf_lo(xv.x) * bf_lo(dv.x) + bf_hi(xv.x) * bf_hi(dv.x) + bf_lo(xv.y) * bf_lo(dv.y) +
-                          bf_hi(xv.y) * bf_hi(dv.y) + bf_lo(xv.z) * bf_lo(dv.z) + bf_hi(xv.z) * bf_hi(dv.z) +
-                          bf_lo(xv.w) * bf_lo(dv.w) + bf_hi(xv.w) * bf_hi(dv.w);
+                for (int c8 = 0; c8 < 8; ++c8) {
+                    const uint32_t ax = xb + sw128_chunk(i, c8), ay = yb + sw128_chunk(i, c8);
+                    uint4 xv = make_uint4(0, 0, 0, 0);
+                    if (valid && okk) xv = ld_shared_v4(ax);
+                    xr[c8] = xv;
+                    st_shared_v4(ax, pack_bf2(bf_lo(xv.x) * dti, bf_hi(xv.x) * dti), pack_bf2(bf_lo(xv.y) * dti, bf_hi(xv.y) * dti),
+                                 pack_bf2(bf_lo(xv.z) * dti, bf_hi(xv.z) * dti), pack_bf2(bf_lo(xv.w) * dti, bf_hi(xv.w) * dti));
+                    if (!valid) st_shared_v4(ay, 0u, 0u, 0u, 0u);
                 }
             }
-            dd = warp_sum(dd);
-            if (lane == 0) red[warp] = dd;
-        }
-        if (k + 1 < nh) {  // buffer sb ^ 1 was last read before this head's first barrier
-            stash(sb ^ 1);
-            if (k + 2 < nh) fetch(k + 2);
-        }
-        ok = mbar_wait(&bar_m1, (uint32_t)(k & 1)) && ok;
-        tc_fence_after();
-        // x is free once dW^T is computed: refill with the next head
-        if (tid == 0 && ok && k + 1 < nh) issue_x(h + 1);
-        if (k + 1 < nh) x_iss = k + 2;
-        // ---- epilogue 1: W^T in place, ddt_orange row sums, target column partials
-        for (int mb = 0; mb < NT; ++mb) {
-            const int sl = 32 * q4 + lane, s = 128 * mb + sl;
-            const int sg = s >> 6, u16 = (s & 63) >> 4;
-            const float cs = cum[s], ds = dts[s];
-            const float fs0 = __expf(piv[sg] - cs);           // off-diagonal row factor
-            const float f160 = __expf(piv16[s >> 4] - cs);    // in-group row factor
-            const float *Erow = E + (sg == 0 ? 0 : (sg == 1 ? 192 : 320)) - 64 * (sg + 1);  // Erow[t]
-            const float *E16row = E16 + 64 * (s >> 4) - 64 * sg;                            // E16row[t]
-            const uint32_t dwc = mb == 0 ? 0u : 256u;
-            float a_ddt = 0.f;  // sum_t dW^T CB^T decay  (ddt_orange; src = dt_s * this)
-            for (int j = hf; j < (Q - 128 * mb) / 64; j += 2) {  // 64-wide t chunks, alternate halves
-                const int tc0 = 128 * mb + 64 * j, tg = tc0 >> 6;
-                float dw[64];
-                tmem_ld32(tmem_addr(tm, 32 * q4, dwc + 64 * j), dw);
-                tmem_ld32(tmem_addr(tm, 32 * q4, dwc + 64 * j + 32), dw + 32);
-                float pk[32];
-                float col[64];
-                if (tg < sg) {
+            // ---- M^T, s-block 1 first (its MMAs run while s-block 0 is built)
+            if (NT == 2 && okk) transform(f, 128 + r, 2 + hi);
+            fence_async_smem();
+            tc_fence_before();
+            okk = bar_and(1, NCONS, okk);
+            tc_fence_after();
+            if (!okk) {
+                ok = false;
+                break;
+            }
+            if (tid == 0) {
+                s_landed = k + 1;
+                if (k + 1 < nh) issue_dy(k + 1);  // its buffer was last read by head k - 1's epilogue
+            }
+            if (NT == 2 && tid == 192) {  // warp 6's phase-B units are the lightest
+                // dx'[1] = M^T[s-block 1] dy[t >= 128];  yo[1] = (s-block 1 part)
+                const uint32_t ia = idesc_bf16(128, 64, false, true), ib = idesc_bf16(128, 64, true, true);
+                for (int ks = 0; ks < 8; ++ks)
+                    mma_bf16(tm + 64, sdesc_kmajor(smem_u32(tile_of(1, 2)), ks, kTile),
+                             sdesc_mnmajor(smem_u32(dyb) + 128 * 128, ks, XB), ia, ks > 0);
+                for (int ks = 0; ks < 8; ++ks)
+                    mma_bf16(tm + 128 + 64, sdesc_mnmajor(smem_u32(tile_of(1, 2)), ks, kTile),
+                             sdesc_mnmajor(smem_u32(xs) + 128 * 128, ks, XB), ib, ks > 0);
+            }
+            if (k + 2 < nh) {  // buffer (k + 2) % NSC was last read by head k - 1
+                stash(k + 2);
+                if (k + 3 < nh) fetch(k + 3);
+            }
+            // ---- M^T, s-block 0
+            transform(f, r, 1 - hi);
+            if (NT == 2) transform(f, r, 3 - hi);
+            if (k + 1 < nh) derive(k + 1);  // raw scalars of head k + 1 visible since the last barrier
+            fence_async_smem();
+            tc_fence_before();
+            okk = bar_and(1, NCONS, true);
+            tc_fence_after();
+            if (tid == 0) {
+                // dx'[0] = M^T[s-block 0] dy;  yo[0] = M[t-block 0, s-block 0] (dt x);  yo[1] += s-block 0 part
+                const uint32_t ia = idesc_bf16(128, 64, false, true), ib = idesc_bf16(128, 64, true, true);
+                for (int ks = 0; ks < Q / 16; ++ks)
+                    mma_bf16(tm, sdesc_kmajor(smem_u32(tile_of(0, 0)), ks, kTile), sdesc_mnmajor(smem_u32(dyb), ks, XB),
+                             ia, ks > 0);
+                for (int tb = 0; tb < NT; ++tb)
+                    for (int ks = 0; ks < 8; ++ks)
+                        mma_bf16(tm + 128 + 64 * tb, sdesc_mnmajor(smem_u32(tile_of(0, 2 * tb)), ks, kTile),
+                                 sdesc_mnmajor(smem_u32(xs), ks, XB), ib, tb == 1 || ks > 0);
+                mma_commit(&bar_mma);
+            }
+            // ---- epilogue of head k (row i)
+            okk = mbar_wait(&bar_mma, (uint32_t)(k & 1));
+            tc_fence_after();
+            if (!okk) ok = false;
+            if (tid == 0 && okk && k + 1 < nh) issue_x(k + 1);  // x is free once the MMAs are done
+            const float dti = i < Q ? f[Q + i] : 0.f, Dh = f[DOFF];
+            float ddo = 0.f, src = 0.f, tgt = 0.f, dd = 0.f;
+            if (i < Q) {
+                // dx'[i]: TMEM block blk (= i / 128), lanes 32 q4 + lane
+                const uint32_t yb = smem_u32(dyb);
+                uint4 dyr[8];
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) pk[i] = 0.f;
-#pragma unroll
-                    for (int i = 0; i < 64; ++i) col[i] = 0.f;
-                } else {
-                    const uint32_t cbb = smem_u32(tile_of(mb, tg));
-#pragma unroll
-                    for (int c8 = 0; c8 < 8; ++c8) {
-                        const uint4 u = ld_shared_v4(cbb + sw128_chunk(sl, c8));
-                        const float cv[8] = {bf_lo(u.x), bf_hi(u.x), bf_lo(u.y), bf_hi(u.y),
-                                             bf_lo(u.z), bf_hi(u.z), bf_lo(u.w), bf_hi(u.w)};
-                        float w[8], cbdv[8];
-                        const int tb8 = tc0 + 8 * c8;
-                        if (tg > sg) {  // off the diagonal group: row factor x column table
-                            const float4 e0 = *reinterpret_cast<const float4 *>(Erow + tb8);
-                            const float4 e1 = *reinterpret_cast<const float4 *>(Erow + tb8 + 4);
-                            const float ev[8] = {e0.x, e0.y, e0.z, e0.w, e1.x, e1.y, e1.z, e1.w};
-#pragma unroll
-                            for (int e = 0; e < 8; ++e) cbdv[e] = cv[e] * ev[e] * fs0;
-                        } else {
-                            const int ut = (tb8 & 63) >> 4;  // the same for the whole 8-chunk
-                            if (ut > u16) {
-                                const float4 e0 = *reinterpret_cast<const float4 *>(E16row + tb8);
-                                const float4 e1 = *reinterpret_cast<const float4 *>(E16row + tb8 + 4);
-                                const float ev[8] = {e0.x, e0.y, e0.z, e0.w, e1.x, e1.y, e1.z, e1.w};
-#pragma unroll
-                                for (int e = 0; e < 8; ++e) cbdv[e] = cv[e] * ev[e] * f160;
-                            } else if (ut == u16) {
-                                const float4 c0 = *reinterpret_cast<const float4 *>(cum + tb8);
-                                const float4 c1 = *reinterpret_cast<const float4 *>(cum + tb8 + 4);
-                                const float ct8[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
-#pragma unroll
-                                for (int e = 0; e < 8; ++e)
-                                    cbdv[e] = tb8 + e >= s ? cv[e] * __expf(ct8[e] - cs) : 0.f;
-                            } else {
-#pragma unroll
-                                for (int e = 0; e < 8; ++e) cbdv[e] = 0.f;
-                            }
-                        }
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) {
-                            const float cbd = cbdv[e];  // CB^T[s, t] exp(cumA_t - cumA_s), t >= s
-                            const float gv = dw[8 * c8 + e] * cbd;
-                            a_ddt += gv;
-                            col[8 * c8 + e] = gv * ds;  // dW^T W^T
-                            w[e] = cbd * ds;            // W^T
-                        }
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) pk[4 * c8 + e] = __uint_as_float(pack_bf2(w[2 * e], w[2 * e + 1]));
-                    }
-                }
-                tmem_st32(tmem_addr(tm, 32 * q4, dwc + 64 * j), pk);  // W^T of this chunk, packed, in place
-                // target partials: transpose-reduce each 32-column half across the warp
+                for (int c8 = 0; c8 < 8; ++c8) dyr[c8] = ld_shared_v4(yb + sw128_chunk(i, c8));
 #pragma unroll
                 for (int hh = 0; hh < 2; ++hh) {
-                    float *cc = col + 32 * hh;
-#pragma unroll
-                    for (int off = 16; off >= 1; off >>= 1) {
-#pragma unroll
-                        for (int i = 0; i < off; ++i) {
-                            const bool upper = (lane & off) != 0;
-                            const float send = upper ? cc[i] : cc[i + off];
-                            const float r = __shfl_xor_sync(0xffffffffu, send, off);
-                            cc[i] = (upper ? cc[i + off] : cc[i]) + r;
-                        }
-                    }
-                    colp[(mb * 4 + q4) * Q + tc0 + 32 * hh + lane] = cc[0];
-                }
-            }
-            rowp[hf * Q + s] = a_ddt;
-        }
-        tc_fence_before();
-        ok = __syncthreads_and(ok ? 1 : 0) != 0;
-        tc_fence_after();
-        // ---- dx = W^T dy (A = W^T packed in TMEM; B = dy MN-major, rows t >= 128 mb)
-        if (tid == 0 && ok) {
-            const uint32_t id = idesc_bf16(128, 64, false, true);
-            for (int mb = 0; mb < NT; ++mb) {
-                const uint32_t dwc = mb == 0 ? 0u : 256u;
-                for (int ks = 0; ks < (Q - 128 * mb) / 16; ++ks)
-                    mma_bf16_tmem_a(tm + DXCOL + 64 * mb, tm + dwc + 64 * (ks >> 2) + 8 * (ks & 3),
-                                    sdesc_mnmajor(smem_u32(dyb) + (uint32_t)(128 * mb * 128), ks, XB), id, ks > 0);
-            }
-            mma_commit(&bar_m2);
-        }
-        // D dy slices of this head (dy_k is refilled only after these MMAs complete)
-        uint4 dyr[NT][4];
-#pragma unroll
-        for (int mb = 0; mb < NT; ++mb) {
-            const int s = 128 * mb + 32 * q4 + lane;
-#pragma unroll
-            for (int c8 = 0; c8 < 4; ++c8) dyr[mb][c8] = ld_shared_v4(smem_u32(dyb) + sw128_chunk(s, 4 * hf + c8));
-        }
-        if (k + 1 < nh) derive(sb ^ 1);  // raw scalars of head k + 1 visible since the last barrier
-        ok = mbar_wait(&bar_m2, (uint32_t)(k & 1)) && ok;
-        tc_fence_after();
-        tc_fence_before();
-        ok = __syncthreads_and(ok ? 1 : 0) != 0;  // every thread has its dy slices
-        tc_fence_after();
-        if (tid == 0 && ok && k + 2 < nh) issue_dy(k + 2);
-        if (k + 2 < nh) dy_iss = k + 3;
-        // ---- epilogue 2: dx = W^T dy + D dy (the K3 backward adds its term afterwards)
-        const float Dh = f[DOFF];
-        for (int mb = 0; mb < NT; ++mb) {
-            const int s = 128 * mb + 32 * q4 + lane;
-            float acc[32];
-            tmem_ld32(tmem_addr(tm, 32 * q4, DXCOL + 64 * mb + 32 * hf), acc);
-            if (t0 + s < p.L) {
-                if (s < vrows) {
+                    float z[32];
+                    tmem_ld32(tmem_addr(tm, 32 * q4, 64 * blk + 32 * hh), z);
+                    float o[32];
 #pragma unroll
                     for (int c8 = 0; c8 < 4; ++c8) {
-                        const uint4 dv = dyr[mb][c8];
-                        float *a = acc + 8 * c8;
-                        a[0] += Dh * bf_lo(dv.x); a[1] += Dh * bf_hi(dv.x);
-                        a[2] += Dh * bf_lo(dv.y); a[3] += Dh * bf_hi(dv.y);
-                        a[4] += Dh * bf_lo(dv.z); a[5] += Dh * bf_hi(dv.z);
-                        a[6] += Dh * bf_lo(dv.w); a[7] += Dh * bf_hi(dv.w);
-                    }
-                } else {
+                        const uint4 xv = xr[4 * hh + c8], yv = dyr[4 * hh + c8];
+                        const float xa[8] = {bf_lo(xv.x), bf_hi(xv.x), bf_lo(xv.y), bf_hi(xv.y),
+                                             bf_lo(xv.z), bf_hi(xv.z), bf_lo(xv.w), bf_hi(xv.w)};
+                        const float ya[8] = {bf_lo(yv.x), bf_hi(yv.x), bf_lo(yv.y), bf_hi(yv.y),
+                                             bf_lo(yv.z), bf_hi(yv.z), bf_lo(yv.w), bf_hi(yv.w)};
+                        // dt * x exactly as the yo MMA saw it (bf16), so that sum_t tgt and
+                        // sum_s src are sums of the same products and cancel to fp32 rounding
+                        const uint32_t q0 = pack_bf2(xa[0] * dti, xa[1] * dti), q1 = pack_bf2(xa[2] * dti, xa[3] * dti);
+                        const uint32_t q2 = pack_bf2(xa[4] * dti, xa[5] * dti), q3 = pack_bf2(xa[6] * dti, xa[7] * dti);
+                        const float xd[8] = {bf_lo(q0), bf_hi(q0), bf_lo(q1), bf_hi(q1),
+                                             bf_lo(q2), bf_hi(q2), bf_lo(q3), bf_hi(q3)};
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) acc[j] = 0.f;
+                        for (int e = 0; e < 8; ++e) {
+                            const float zz = z[8 * c8 + e];
+                            ddo = fmaf(xa[e], zz, ddo);
+                            src = fmaf(xd[e], zz, src);
+                            dd = fmaf(xa[e], ya[e], dd);
+                            o[8 * c8 + e] = valid ? fmaf(dti, zz, Dh * ya[e]) : 0.f;
+                        }
+                    }
+                    if (t0 + i < p.L) store_row32_bf16(DX + ix_x(p, bi, t0 + i, h, 32 * hh), o);
                 }
-                store_row32_bf16(DX + ix_x(p, bi, t0 + s, h, 32 * hf), acc);
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh) {
+                    float y[32];
+                    tmem_ld32(tmem_addr(tm, 32 * q4, 128 + 64 * blk + 32 * hh), y);
+#pragma unroll
+                    for (int c8 = 0; c8 < 4; ++c8) {
+                        const uint4 yv = dyr[4 * hh + c8];
+                        const float ya[8] = {bf_lo(yv.x), bf_hi(yv.x), bf_lo(yv.y), bf_hi(yv.y),
+                                             bf_lo(yv.z), bf_hi(yv.z), bf_lo(yv.w), bf_hi(yv.w)};
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) tgt = fmaf(ya[e], y[8 * c8 + e], tgt);
+                    }
+                }
+                const size_t cbase = ix_chunk(p, bi, h, c) * Q;
+                p.ddt_main[cbase + i] = valid ? ddo : 0.f;             // the K3 backward adds its terms
+                p.dcum_main[cbase + i] = valid ? tgt - src : 0.f;
             }
-        }
-        // ---- per-token outputs of head k
-        const size_t cbase = ix_chunk(p, bi, h, c) * Q;
-        for (int q = tid; q < Q; q += kThreadsWide) {
-            float tgt = 0.f;
-            for (int mb = 0; mb < NT; ++mb)
-                if (q >= 128 * mb)
-                    for (int w = 0; w < 4; ++w) tgt += colp[(mb * 4 + w) * Q + q];
-            const float ddo = rowp[q] + rowp[Q + q];   // ddt_orange
-            const float src = dts[q] * ddo;            // sum_t dW^T W^T
-            p.ddt_main[cbase + q] = ddo;          // the K3 backward adds its terms to both
-            p.dcum_main[cbase + q] = tgt - src;
-        }
-        if (tid == 0) {
-            float d = 0.f;
-            for (int w = 0; w < 8; ++w) d += red[w];
-            p.dD_part[((size_t)bi * p.n + c) * p.H + h] = d;
+            dd = warp_sum(dd);
+            if (lane == 0) p.dD_part[(((size_t)bi * p.n + c) * p.H + h) * p.dD_per + warp] = dd;
         }
     }
+    tc_fence_before();
+    ok = __syncthreads_and(ok ? 1 : 0) != 0;
+    tc_fence_after();
     if (!ok && tid == 0) flag_timeout(p);
-    if (x_iss > x_land) mbar_wait(&bar_x, (uint32_t)((x_iss - 1) & 1));
-    for (int k = dy_land; k < dy_iss; ++k) mbar_wait(&bar_dy[k & 1], (uint32_t)((k >> 1) & 1));
+    // loads issued for heads that were never consumed have to land before exit
+    if (tid == 0) {
+        mbar_wait(&bar_cb, 0);  // landed long ago unless the kernel gave up early
+        if (s_x_issued > s_landed) mbar_wait(&bar_x, (uint32_t)((s_x_issued - 1) & 1));
+        for (int k = s_landed; k < s_dy_issued; ++k) mbar_wait(&bar_dy[k & 1], (uint32_t)((k >> 1) & 1));
+    }
     tc_sync();
-    if (warp == 0) tmem_dealloc(tm, NCOL);
+    if (warp == 0) tmem_dealloc(tm, 512);
 }
 
 // ====================================================================== group backward
@@ -2085,9 +2117,12 @@ constexpr size_t smem_blue(int Q) { return 1024 + 2 * (size_t)Q * 128 + 3 * ((si
 constexpr size_t smem_k3bwd(int Q) {
     return 1024 + 2 * (size_t)Q * 128 + 2 * ((size_t)Q * 128 + 2 * 64 * 128) + 4 * (3 * 3 * Q + 2 * Q);
 }
+// Padded above half of the SM's shared memory: a CTA holding 512 TMEM columns
+// must never share its SM with another CTA of the same kernel.
 constexpr size_t smem_orange(int Q) {
-    return 1024 + (size_t)kTile * (Q == 256 ? 6 : 2) + 3 * (size_t)Q * 128 +
-           4 * (2 * (2 * Q + 384 + 1024 + 28) + (Q / 128) * 4 * Q + 2 * Q + 8);
+    return 1024 + (size_t)kTile * (Q == 256 ? 6 : 2) + 3 * (size_t)Q * 128 + 4 * 3 * (2 * Q + 732) > 120 * 1024
+               ? 1024 + (size_t)kTile * (Q == 256 ? 6 : 2) + 3 * (size_t)Q * 128 + 4 * 3 * (2 * Q + 732)
+               : 120 * 1024;
 }
 // Padded above a third of the SM's shared memory: two CTAs of 256 TMEM columns
 // each may share an SM, a third must not.
@@ -2099,7 +2134,7 @@ constexpr size_t smem_dcb(int Q) {
 constexpr size_t smem_dbc(int Q) {
     return 1024 + 2 * (2 * (size_t)Q * 128 + 4 * 64 * 128) + 4 * 4 * Q;
 }
-static_assert(smem_orange(256) <= 232448 && smem_orange(256) > 116 * 1024, "ORANGE backward: one CTA per SM");
+static_assert(smem_orange(256) <= 232448 && smem_orange(128) > 116 * 1024, "ORANGE backward: one CTA per SM");
 static_assert(smem_k3bwd(256) <= 232448 && smem_k3bwd(256) > 116 * 1024, "K3 backward: one CTA per SM");
 static_assert(smem_k2(256) > 116 * 1024, "K2 (512 TMEM columns): one CTA per SM");
 static_assert(smem_k5(256) <= 232448 && smem_k5(256) > 116 * 1024, "K5: one CTA per SM");
@@ -2114,7 +2149,7 @@ static_assert(2 * (size_t)256 * 256 + 2 * 256 * 128 <= 2 * (2 * (size_t)256 * 12
 }  // namespace
 
 bool tc_supported(int64_t P, int64_t N, int64_t Q) { return P == kP && N == kN && (Q == 128 || Q == 256); }
-int tc_dD_per(int64_t) { return 1; }
+int tc_dD_per(int64_t) { return kThreadsWide / 32; }  // one dD partial per ORANGE consumer warp
 int tc_dcb_slices(const ssd_dims &d) {
     // CTAs: one per 128 x 128 block on or below the diagonal and head slice;
     // two fit an SM.  Head slices only when the blocks alone leave SMs idle
@@ -2148,13 +2183,14 @@ int tc_k5_slices(const ssd_dims &d) {
     return (int)s;
 }
 int tc_k3_slices(const ssd_dims &d) {
-    // one CTA per SM: minimise (waves x heads per CTA), fewest slices on ties
+    // one CTA per SM: minimise waves x (heads per CTA + the resident operand's
+    // load, about two heads' worth), fewest slices on ties
     const long long hpg = d.nheads / d.ngroups;
     const long long n = (d.seqlen + d.chunk_len - 1) / d.chunk_len;
     const long long groups = d.batch * n * d.ngroups;
     long long best = 1, best_cost = -1;
     for (long long s = 1; s <= hpg; ++s) {
-        const long long cost = ((groups * s + 151) / 152) * ((hpg + s - 1) / s);
+        const long long cost = ((groups * s + 151) / 152) * ((hpg + s - 1) / s + 2);
         if (best_cost < 0 || cost < best_cost) {
             best = s;
             best_cost = cost;
