@@ -443,8 +443,10 @@ __global__ void __launch_bounds__(kThreadsWide, 1) tc_k5_kernel(const Params p, 
     constexpr int NWT = NT * (NT + 1);  // CB tiles: tb0 2, tb1 4
     constexpr uint32_t NCOL = NT == 2 ? 512 : 256;
     constexpr uint32_t OCOL = 0, BCOL = NT * 64, WCOL = 2 * NT * 64;
-    constexpr int NSC = 4;              // scalar buffers: prefetch distance 2, plus the epilogue's
-    constexpr int FST = 4 * Q + 24;     // cum Q | dts Q | gcol Q | g16 Q | piv 8 | piv16 16
+    constexpr int NSC = 3;              // scalar buffers: staged two heads ahead
+    // per-head tables (32-bit words): cum Q | dt Q | gcol pairs Q/2 | T16 pairs (Q/64) x 4 x 32 | piv 8
+    constexpr int GOFF = 2 * Q, TOFF = GOFF + Q / 2, POFF = TOFF + (Q / 64) * 128;
+    constexpr int FST = POFF + 8;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = align1024(smem_raw);
     uint8_t *Cs = sm, *CBs = Cs + 2 * RB, *xs = CBs + NWT * kTile, *Ss = xs + XB;
@@ -490,15 +492,29 @@ __global__ void __launch_bounds__(kThreadsWide, 1) tc_k5_kernel(const Params p, 
             f[Q + tid] = r_dt;
         }
     };
-    // column factors dt exp(piv - cumA) and pivots, from the raw values (visible after a barrier)
+    // column tables from the raw values (visible after a barrier), as bf16 pairs:
+    //   gcol[s]       = dt_s exp(piv_g - cumA_s), piv_g = cumA[64 g + 63] of s's 64-group g
+    //   T16[g][u][s'] = dt_s exp(P_u - cumA_s) for s' = s - 64 g < 16 u, else 0, where
+    //                   P_u = cumA[64 g + 16 u - 1] ends the 16-wide sub-blocks left of u
     auto derive = [&](int b) {
         float *f = fbuf + b * FST;
-        for (int l = tid; l < Q; l += kThreadsWide) {
-            f[2 * Q + l] = f[Q + l] * __expf(f[l | 63] - f[l]);
-            f[3 * Q + l] = f[Q + l] * __expf(f[l | 15] - f[l]);
+        uint32_t *f2 = reinterpret_cast<uint32_t *>(f);
+        for (int e = tid; e < Q / 2; e += kThreadsWide) {
+            const int s = 2 * e;
+            const float pv = f[s | 63];
+            f2[GOFF + e] = pack_bf2(f[Q + s] * __expf(pv - f[s]), f[Q + s + 1] * __expf(pv - f[s + 1]));
         }
-        for (int j = tid; j < Q / 64; j += kThreadsWide) f[4 * Q + j] = f[64 * j + 63];
-        for (int j = tid; j < Q / 16; j += kThreadsWide) f[4 * Q + 8 + j] = f[16 * j + 15];
+        for (int e = tid; e < (Q / 64) * 128; e += kThreadsWide) {
+            const int gb = e >> 7, u = (e >> 5) & 3, s = 64 * gb + 2 * (e & 31);
+            float lo = 0.f, hi = 0.f;
+            if (2 * (e & 31) < 16 * u) {
+                const float pv = f[64 * gb + 16 * u - 1];
+                lo = f[Q + s] * __expf(pv - f[s]);
+                hi = f[Q + s + 1] * __expf(pv - f[s + 1]);
+            }
+            f2[TOFF + e] = pack_bf2(lo, hi);
+        }
+        for (int j = tid; j < Q / 64; j += kThreadsWide) f[POFF + j] = f[64 * j + 63];
     };
     auto issue_head = [&](int h) {
         const int sidx = (bi * p.n + c) * p.H + h;
@@ -544,8 +560,11 @@ __global__ void __launch_bounds__(kThreadsWide, 1) tc_k5_kernel(const Params p, 
     __syncthreads();
     uint4 xr[NT][4];  // this thread's D x slices of the head whose epilogue comes next
     float D_ep = 0.f;  // D of the head whose epilogue comes next
+    float ep_ep[NT], ep_k[NT];  // exp(cumA_t) of this thread's epilogue rows: next epilogue's, this head's
+#pragma unroll
+    for (int tb = 0; tb < NT; ++tb) ep_ep[tb] = ep_k[tb] = 0.f;
     for (int k = 0; k <= nh && ok; ++k) {
-        const int h = h_begin + k, cur = k % NSC, prv = (k + NSC - 1) % NSC;
+        const int h = h_begin + k, cur = k % NSC;
         const float D_k = k < nh ? p.D[h] : 0.f;  // used one iteration later
         if (k > 0) {
             // MMAs of head k-1 done: the TMEM W region and the x / s_in buffers are free
@@ -558,66 +577,68 @@ __global__ void __launch_bounds__(kThreadsWide, 1) tc_k5_kernel(const Params p, 
         }
         if (k < nh) {
             const float *f = fbuf + cur * FST;
-            const float *cum = f, *dts = f + Q, *gcol = f + 2 * Q, *g16 = f + 3 * Q;
-            const float *piv = f + 4 * Q, *piv16 = f + 4 * Q + 8;
+            const float *cum = f, *dts = f + Q, *piv = f + POFF;
+#pragma unroll
+            for (int tb = 0; tb < NT; ++tb) ep_k[tb] = __expf(cum[tb * 128 + 32 * q4 + lane]);
             // ---- W_k into TMEM (packed bf16 pairs, lane = t), while x_k / s_in_k land.
-            // The two warp halves take alternate 64-column groups (balanced diagonal work).
-            for (int tb = 0; tb < NT; ++tb) {
-                const int t = tb * 128 + 32 * q4 + lane;
-                const int tr = t >> 6, row = t - 128 * tb;
-                const float ct = cum[t];
-                for (int s0g = 64 * hf; s0g < 128 * (tb + 1); s0g += 128) {
-                    const int sb = s0g >> 6;
-                    float pk[32];
-                    if (sb > tr) {
+            // Units (t-block tb, 64-column group sb) of rows t = 128 tb + 32 q4 + lane:
+            // every thread gets three, exactly one of them on the diagonal 64-group.
+            const uint32_t *f2 = reinterpret_cast<const uint32_t *>(f);
+            auto build = [&](int tb, int sb) {
+                const int t = tb * 128 + 32 * q4 + lane, tr = t >> 6, row = t - 128 * tb;
+                uint32_t pk[32];
+                if (sb > tr) {
 #pragma unroll
-                        for (int j = 0; j < 32; ++j) pk[j] = 0.f;
-                    } else {
-                        const uint32_t cbb = smem_u32(CBs + (tb * (tb + 1) + sb) * kTile);
-                        if (sb < tr) {
-                            const float e = __expf(ct - piv[sb]);
+                    for (int j = 0; j < 32; ++j) pk[j] = 0u;
+                } else {
+                    const uint32_t cbb = smem_u32(CBs + (tb * (tb + 1) + sb) * kTile);
+                    const bool diag = sb == tr;
+                    const int u = (t & 63) >> 4, t16 = t & ~15;
+                    const float ct = cum[t];
+                    // row factor: exp(cumA_t - pivot); on the diagonal group the pivot ends the
+                    // sub-blocks left of the row's own (none when u = 0: the table is all 0)
+                    const float er = diag ? (u > 0 ? __expf(ct - cum[t16 - 1]) : 0.f) : __expf(ct - piv[sb]);
+                    const uint32_t er2 = pack_bf2(er, er);
+                    const uint32_t *tab = diag ? f2 + TOFF + 128 * sb + 32 * u : f2 + GOFF + 32 * sb;
 #pragma unroll
-                            for (int c8 = 0; c8 < 8; ++c8) {
-                                const uint4 u = ld_shared_v4(cbb + sw128_chunk(row, c8));
-                                const float4 g0 = *reinterpret_cast<const float4 *>(gcol + s0g + 8 * c8);
-                                const float4 g1 = *reinterpret_cast<const float4 *>(gcol + s0g + 8 * c8 + 4);
-                                pk[4 * c8 + 0] = __uint_as_float(pack_bf2(bf_lo(u.x) * e * g0.x, bf_hi(u.x) * e * g0.y));
-                                pk[4 * c8 + 1] = __uint_as_float(pack_bf2(bf_lo(u.y) * e * g0.z, bf_hi(u.y) * e * g0.w));
-                                pk[4 * c8 + 2] = __uint_as_float(pack_bf2(bf_lo(u.z) * e * g1.x, bf_hi(u.z) * e * g1.y));
-                                pk[4 * c8 + 3] = __uint_as_float(pack_bf2(bf_lo(u.w) * e * g1.z, bf_hi(u.w) * e * g1.w));
-                            }
-                        } else {
-                            // diagonal 64-group: 16-wide sub-blocks, pivot cumA[16 v + 15]
-                            // left of the row's own sub-block, direct exponentials inside it
-                            const int u16 = (t & 63) >> 4;
-                            float e16 = 0.f;
-#pragma unroll
-                            for (int c8 = 0; c8 < 8; ++c8) {
-                                const int v16 = c8 >> 1;
-                                const uint4 u = ld_shared_v4(cbb + sw128_chunk(row, c8));
-                                const float cv[8] = {bf_lo(u.x), bf_hi(u.x), bf_lo(u.y), bf_hi(u.y),
-                                                     bf_lo(u.z), bf_hi(u.z), bf_lo(u.w), bf_hi(u.w)};
-                                float w[8];
-                                if (v16 < u16) {
-                                    if ((c8 & 1) == 0) e16 = __expf(ct - piv16[4 * sb + v16]);
-#pragma unroll
-                                    for (int j = 0; j < 8; ++j) w[j] = cv[j] * e16 * g16[s0g + 8 * c8 + j];
-                                } else if (v16 == u16) {
-#pragma unroll
-                                    for (int j = 0; j < 8; ++j) {
-                                        const int s = s0g + 8 * c8 + j;
-                                        w[j] = s <= t ? cv[j] * __expf(ct - cum[s]) * dts[s] : 0.f;
-                                    }
-                                } else {
-#pragma unroll
-                                    for (int j = 0; j < 8; ++j) w[j] = 0.f;
-                                }
-#pragma unroll
-                                for (int j = 0; j < 4; ++j) pk[4 * c8 + j] = __uint_as_float(pack_bf2(w[2 * j], w[2 * j + 1]));
-                            }
-                        }
+                    for (int c8 = 0; c8 < 8; ++c8) {
+                        const uint4 cv = ld_shared_v4(cbb + sw128_chunk(row, c8));
+                        const uint4 gv = *reinterpret_cast<const uint4 *>(tab + 4 * c8);
+                        pk[4 * c8] = bmul2(bmul2(cv.x, gv.x), er2);
+                        pk[4 * c8 + 1] = bmul2(bmul2(cv.y, gv.y), er2);
+                        pk[4 * c8 + 2] = bmul2(bmul2(cv.z, gv.z), er2);
+                        pk[4 * c8 + 3] = bmul2(bmul2(cv.w, gv.w), er2);
                     }
-                    tmem_st32(tmem_addr(tm, 32 * q4, WCOL + 64 * (tb * (tb + 1) / 2) + (s0g >> 1)), pk);
+                    if (diag) {  // the row's own 16-wide sub-block: direct exponentials, 0 for s > t
+                        const uint4 c0 = ld_shared_v4(cbb + sw128_chunk(row, 2 * u));
+                        const uint4 c1 = ld_shared_v4(cbb + sw128_chunk(row, 2 * u + 1));
+                        const uint32_t cw[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+                        uint32_t own[8];
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) {
+                            const int s0 = t16 + 2 * j;
+                            const float w0 = s0 <= t ? bf_lo(cw[j]) * __expf(ct - cum[s0]) * dts[s0] : 0.f;
+                            const float w1 = s0 + 1 <= t ? bf_hi(cw[j]) * __expf(ct - cum[s0 + 1]) * dts[s0 + 1] : 0.f;
+                            own[j] = pack_bf2(w0, w1);
+                        }
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) pk[j] = (j >> 3) == u ? own[j & 7] : pk[j];
+                    }
+                }
+                tmem_st32u(tmem_addr(tm, 32 * q4, WCOL + 64 * (tb * (tb + 1) / 2) + 32 * sb), pk);
+            };
+            const int dq = q4 >> 1;  // the rows' 64-group inside their t-block
+            if (hf == 0) {
+                build(0, dq);
+                if (NT == 2) {
+                    build(1, 0);
+                    build(1, 1);
+                }
+            } else {
+                build(0, 1 - dq);
+                if (NT == 2) {
+                    build(1, dq == 0 ? 3 : 2);
+                    build(1, 2 + dq);
                 }
             }
             // prefetch raw scalars of head k + 2, derive those of head k + 1 (raw visible since the last barrier)
@@ -629,7 +650,6 @@ __global__ void __launch_bounds__(kThreadsWide, 1) tc_k5_kernel(const Params p, 
         }
         // ---- epilogue of head k - 1
         if (k > 0) {
-            const float *cum = fbuf + prv * FST;
             const float Dh = D_ep;
 #pragma unroll
             for (int tb = 0; tb < NT; ++tb) {
@@ -639,7 +659,7 @@ __global__ void __launch_bounds__(kThreadsWide, 1) tc_k5_kernel(const Params p, 
                 tmem_ld32(tmem_addr(tm, 32 * q4, BCOL + tb * 64 + hf * 32), bl);
                 if (t0 + t < p.L) {
                     if (t < vrows) {
-                        const float e = __expf(cum[t]);
+                        const float e = ep_ep[tb];
 #pragma unroll
                         for (int c8 = 0; c8 < 4; ++c8) {
                             const uint4 u = xr[tb][c8];
@@ -658,6 +678,8 @@ __global__ void __launch_bounds__(kThreadsWide, 1) tc_k5_kernel(const Params p, 
         }
         if (k == nh) break;
         D_ep = D_k;
+#pragma unroll
+        for (int tb = 0; tb < NT; ++tb) ep_ep[tb] = ep_k[tb];
         // ---- x_k landed: keep this thread's D x slices, zero padded rows
         ok = mbar_wait(&bar_x, (uint32_t)(k & 1)) && ok;
         if (ok) x_landed = k + 1;
@@ -2111,7 +2133,7 @@ constexpr size_t smem_k2(int Q) { return 1024 + 4 * (size_t)Q * 128; }
 constexpr size_t smem_k3(int Q) { return 1024 + 2 * (size_t)Q * 128 + 4 * (size_t)Q * 128; }
 constexpr size_t smem_k5(int Q) {
     return 1024 + 3 * (size_t)Q * 128 + 2 * 64 * 128 + (size_t)kTile * (Q / 128) * (Q / 128 + 1) +
-           4 * 4 * (4 * Q + 24);
+           4 * 3 * (2 * Q + Q / 2 + (Q / 64) * 128 + 8);
 }
 constexpr size_t smem_blue(int Q) { return 1024 + 2 * (size_t)Q * 128 + 3 * ((size_t)Q * 128 + 2 * 64 * 128); }
 constexpr size_t smem_k3bwd(int Q) {
