@@ -144,6 +144,23 @@ __device__ __forceinline__ void scale_row_bf16(uint8_t *tile, int row, float f, 
     }
 }
 
+// Same in packed bf16 pairs (the factor rounded to bf16 first): half the
+// instructions, for operands whose bf16 rounding dominates anyway.
+__device__ __forceinline__ void scale_row_bf16x2(uint8_t *tile, int row, float f, bool valid) {
+    const uint32_t base = smem_u32(tile);
+    const uint32_t f2 = pack_bf2(f, f);
+#pragma unroll
+    for (int c8 = 0; c8 < 8; ++c8) {
+        const uint32_t a = base + sw128_chunk(row, c8);
+        if (!valid) {
+            st_shared_v4(a, 0u, 0u, 0u, 0u);
+            continue;
+        }
+        const uint4 v = ld_shared_v4(a);
+        st_shared_v4(a, bmul2(v.x, f2), bmul2(v.y, f2), bmul2(v.z, f2), bmul2(v.w, f2));
+    }
+}
+
 // Dot product of a swizzled bf16 row (64 values) with 64 floats.
 __device__ __forceinline__ float dot_row64(const uint8_t *tile, int row, const float *v) {
     const uint32_t base = smem_u32(tile);
@@ -1802,7 +1819,7 @@ __global__ void __launch_bounds__(kThreadsWide + 32, 1) tc_bwd_dbc_kernel(const 
     constexpr int NCONS = kThreadsWide;         // consumer threads; the producer warp follows
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = align1024(smem_raw);
-    __shared__ uint64_t bar_tma[2], bar_mma[2], bar_a;
+    __shared__ uint64_t bar_tma[2], bar_mma[2], bar_scaled[2], bar_a;
     __shared__ uint32_t s_tmem;
     __shared__ int s_issued, s_landed, s_perr;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -1813,14 +1830,15 @@ __global__ void __launch_bounds__(kThreadsWide + 32, 1) tc_bwd_dbc_kernel(const 
     const int g = idx % p.G, c = (idx / p.G) % p.n, bi = idx / (p.G * p.n);
     const int t0 = c * Q;
     const int vrows = min(Q, valid_len_of(p, bi) - t0);
-    const int per = (p.hpg + p.nslice - 1) / p.nslice;
-    const int h_begin = g * p.hpg + slice * per;
-    const int h_end = min(g * p.hpg + p.hpg, h_begin + per);
+    // slice j takes heads j, j + nslice, ... of the group: CTAs running side by
+    // side read neighbouring heads, i.e. neighbouring 128-byte pieces of each token row
+    const int h_begin = g * p.hpg + slice;
+    auto head = [&](int k) { return h_begin + k * p.nslice; };
     const size_t pstride = (size_t)p.b * p.n * p.G * Q * kN;
     float *outC = p.dBC_part + ((size_t)slice * 2 + 0) * pstride + (((size_t)bi * p.n + c) * p.G + g) * (size_t)Q * kN;
     float *outB = p.dBC_part + ((size_t)slice * 2 + 1) * pstride + (((size_t)bi * p.n + c) * p.G + g) * (size_t)Q * kN;
     const bool do_k2 = slice == 0;
-    const int nh = max(0, h_end - h_begin);
+    const int nh = max(0, (p.hpg - slice + p.nslice - 1) / p.nslice);
     if (vrows <= 0 || (!do_k2 && nh == 0)) {
         for (int i = tid; i < Q * kN; i += blockDim.x) {
             outC[i] = 0.f;
@@ -1833,6 +1851,8 @@ __global__ void __launch_bounds__(kThreadsWide + 32, 1) tc_bwd_dbc_kernel(const 
         mbar_init(&bar_tma[1], 1);
         mbar_init(&bar_mma[0], 1);
         mbar_init(&bar_mma[1], 1);
+        mbar_init(&bar_scaled[0], NCONS / 32);
+        mbar_init(&bar_scaled[1], NCONS / 32);
         mbar_init(&bar_a, 1);
         mbar_fence_init();
         s_issued = 0;
@@ -1909,14 +1929,11 @@ __global__ void __launch_bounds__(kThreadsWide + 32, 1) tc_bwd_dbc_kernel(const 
         have_acc = true;
     }
     if (warp == NCONS / 32) {
-        // ---- producer: stage k & 1 takes head k once head k - 2's MMAs are done
+        // ---- producer: TMA for head k + 1 once head k - 1's MMAs are done (its
+        // stage is free), and the MMAs of head k once the consumers have scaled it
         if (lane == 0 && ok) {
-            for (int k = 0; k < nh; ++k) {
-                const int h = h_begin + k, st = k & 1;
-                if (k >= 2 && !mbar_wait(&bar_mma[st], (uint32_t)(((k - 2) >> 1) & 1))) {
-                    s_perr = 1;
-                    break;
-                }
+            auto issue = [&](int k) {
+                const int h = head(k), st = k & 1;
                 uint8_t *base = sm + st * STG;
                 uint8_t *dys = base, *xs = base + XB, *sis = base + 2 * XB, *dis = sis + 2 * SB;
                 const int sidx = (bi * p.n + c) * p.H + h;
@@ -1930,46 +1947,19 @@ __global__ void __launch_bounds__(kThreadsWide + 32, 1) tc_bwd_dbc_kernel(const 
                     tma_load_3d(dis + rb * SB, &maps.dst, &bar_tma[st], 64 * rb, 0, sidx);
                 }
                 s_issued = k + 1;
-            }
-        }
-    } else if (ok) {
-        // ---- consumers: thread t owns token row t of the chunk
-        const int t = tid;
-        const bool valid = t < vrows;
-        float c_cur = 0.f, d_cur = 0.f, e_cur = 0.f, c_nx = 0.f, d_nx = 0.f, e_nx = 0.f;
-        auto fetch = [&](int k, float &cc, float &dd, float &ce) {
-            const size_t ck = ix_chunk(p, bi, h_begin + k, c);
-            ce = p.endA[ck];
-            cc = t < Q ? p.cumA[ck * Q + t] : 0.f;
-            dd = valid ? p.dt[ix_dt(p, bi, h_begin + k, t0 + t)] : 0.f;
-        };
-        if (nh > 0) fetch(0, c_cur, d_cur, e_cur);
-        if (nh > 1) fetch(1, c_nx, d_nx, e_nx);
-        for (int k = 0; k < nh; ++k) {
-            const int st = k & 1;
-            uint8_t *base = sm + st * STG;
-            uint8_t *dys = base, *xs = base + XB, *sis = base + 2 * XB, *dis = sis + 2 * SB;
-            const float e_row = __expf(c_cur);                // dy row factor exp(cumA_t)
-            const float b_row = d_cur * __expf(e_cur - c_cur);  // x row factor bbs_t
-            c_cur = c_nx;
-            d_cur = d_nx;
-            e_cur = e_nx;
-            if (k + 2 < nh) fetch(k + 2, c_nx, d_nx, e_nx);
-            bool okk = mbar_wait(&bar_tma[st], (uint32_t)((k >> 1) & 1));
-            if (okk && t < Q) {
-                scale_row_bf16(dys, t, e_row, valid);
-                scale_row_bf16(xs, t, b_row, valid);
-            }
-            fence_async_smem();
-            tc_fence_before();
-            okk = bar_and(1, NCONS, okk);
-            tc_fence_after();
-            if (!okk) {
-                ok = false;
-                break;
-            }
-            if (tid == 0) {
+            };
+            if (nh > 0) issue(0);
+            if (nh > 1) issue(1);
+            for (int k = 0; k < nh; ++k) {
+                const int st = k & 1;
+                if (!mbar_wait(&bar_scaled[st], (uint32_t)((k >> 1) & 1)) || s_perr) {
+                    s_perr = 1;
+                    break;
+                }
                 s_landed = k + 1;
+                tc_fence_after();
+                uint8_t *base = sm + st * STG;
+                uint8_t *dys = base, *xs = base + XB, *sis = base + 2 * XB, *dis = sis + 2 * SB;
                 const uint32_t id = idesc_bf16(128, kN, false, true);
                 for (int tb = 0; tb < NT; ++tb)
                     for (int ks = 0; ks < kP / 16; ++ks) {
@@ -1980,10 +1970,50 @@ __global__ void __launch_bounds__(kThreadsWide + 32, 1) tc_bwd_dbc_kernel(const 
                                  sdesc_mnmajor(smem_u32(dis), ks, SB), id, acc);
                     }
                 mma_commit(&bar_mma[st]);
+                if (k >= 1 && k + 1 < nh) {  // stage (k + 1) & 1 was read by head k - 1's MMAs
+                    if (!mbar_wait(&bar_mma[(k - 1) & 1], (uint32_t)(((k - 1) >> 1) & 1))) {
+                        s_perr = 1;
+                        break;
+                    }
+                    issue(k + 1);
+                }
             }
         }
+    } else if (ok) {
+        // ---- consumers: thread t owns token row t of the chunk
+        const int t = tid;
+        const bool valid = t < vrows;
+        float c_cur = 0.f, d_cur = 0.f, e_cur = 0.f, c_nx = 0.f, d_nx = 0.f, e_nx = 0.f;
+        auto fetch = [&](int k, float &cc, float &dd, float &ce) {
+            const size_t ck = ix_chunk(p, bi, head(k), c);
+            ce = p.endA[ck];
+            cc = t < Q ? p.cumA[ck * Q + t] : 0.f;
+            dd = valid ? p.dt[ix_dt(p, bi, head(k), t0 + t)] : 0.f;
+        };
+        if (nh > 0) fetch(0, c_cur, d_cur, e_cur);
+        if (nh > 1) fetch(1, c_nx, d_nx, e_nx);
+        for (int k = 0; k < nh; ++k) {
+            const int st = k & 1;
+            uint8_t *base = sm + st * STG;
+            uint8_t *dys = base, *xs = base + XB;
+            const float e_row = __expf(c_cur);                // dy row factor exp(cumA_t)
+            const float b_row = d_cur * __expf(e_cur - c_cur);  // x row factor bbs_t
+            c_cur = c_nx;
+            d_cur = d_nx;
+            e_cur = e_nx;
+            if (k + 2 < nh) fetch(k + 2, c_nx, d_nx, e_nx);
+            const bool okk = mbar_wait(&bar_tma[st], (uint32_t)((k >> 1) & 1));
+            if (okk && t < Q) {
+                scale_row_bf16x2(dys, t, e_row, valid);
+                scale_row_bf16x2(xs, t, b_row, valid);
+            }
+            if (!okk) s_perr = 1;
+            fence_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bar_scaled[st]);  // the producer issues head k's MMAs
+        }
         // the last head's MMAs complete after all earlier ones
-        if (ok && nh > 0) ok = mbar_wait(&bar_mma[(nh - 1) & 1], (uint32_t)(((nh - 1) >> 1) & 1));
+        if (nh > 0) ok = mbar_wait(&bar_mma[(nh - 1) & 1], (uint32_t)(((nh - 1) >> 1) & 1)) && ok;
     }
     tc_fence_before();
     ok = __syncthreads_and(ok && s_perr == 0 ? 1 : 0) != 0;
@@ -2221,13 +2251,21 @@ int tc_k3_slices(const ssd_dims &d) {
     return (int)best;
 }
 int tc_group_slices(const ssd_dims &d) {
+    // one CTA per SM; heads per CTA chosen to minimise waves x (heads per CTA + 1),
+    // the +1 standing for the CTA's fixed cost (prologue, partial write-out)
     const long long hpg = d.nheads / d.ngroups;
     const long long n = (d.seqlen + d.chunk_len - 1) / d.chunk_len;
-    const long long ctas = d.batch * n * d.ngroups;
-    long long s = (2 * 152 + ctas - 1) / ctas;
-    if (s < 1) s = 1;
-    if (s > hpg) s = hpg;
-    return (int)s;
+    const long long groups = d.batch * n * d.ngroups;
+    long long best = 1, best_cost = -1;
+    for (long long per = hpg; per >= 1; --per) {
+        const long long ns = (hpg + per - 1) / per;
+        const long long cost = ((groups * ns + 151) / 152) * (per + 1);
+        if (best_cost < 0 || cost < best_cost) {
+            best = ns;
+            best_cost = cost;
+        }
+    }
+    return (int)best;
 }
 
 #define SSD_TC_DISPATCH(Q_, call) ((Q_) == 256 ? call(256) : call(128))
