@@ -1436,7 +1436,6 @@ __global__ void __launch_bounds__(kThreadsWide, 1) tc_bwd_orange_kernel(const Pa
             // ---- M^T, s-block 0
             transform(f, r, 1 - hi);
             if (NT == 2) transform(f, r, 3 - hi);
-            if (k + 1 < nh) derive(k + 1);  // raw scalars of head k + 1 visible since the last barrier
             fence_async_smem();
             tc_fence_before();
             okk = bar_and(1, NCONS, true);
@@ -1453,13 +1452,15 @@ __global__ void __launch_bounds__(kThreadsWide, 1) tc_bwd_orange_kernel(const Pa
                                  sdesc_mnmajor(smem_u32(xs), ks, XB), ib, tb == 1 || ks > 0);
                 mma_commit(&bar_mma);
             }
+            if (k + 1 < nh) derive(k + 1);  // while the MMAs run (raw scalars visible since barrier 1)
             // ---- epilogue of head k (row i)
             okk = mbar_wait(&bar_mma, (uint32_t)(k & 1));
             tc_fence_after();
             if (!okk) ok = false;
             if (tid == 0 && okk && k + 1 < nh) issue_x(k + 1);  // x is free once the MMAs are done
             const float dti = i < Q ? f[Q + i] : 0.f, Dh = f[DOFF];
-            float ddo = 0.f, src = 0.f, tgt = 0.f, dd = 0.f;
+            const float2 dti2 = make_float2(dti, dti), Dh2 = make_float2(Dh, Dh);
+            float2 ddo2 = make_float2(0.f, 0.f), src2 = ddo2, dd2 = ddo2, tgt2 = ddo2;
             if (i < Q) {
                 // dx'[i]: TMEM block blk (= i / 128), lanes 32 q4 + lane
                 const uint32_t yb = smem_u32(dyb);
@@ -1470,30 +1471,31 @@ __global__ void __launch_bounds__(kThreadsWide, 1) tc_bwd_orange_kernel(const Pa
                 for (int hh = 0; hh < 2; ++hh) {
                     float z[32];
                     tmem_ld32(tmem_addr(tm, 32 * q4, 64 * blk + 32 * hh), z);
-                    float o[32];
+                    uint32_t o[16];
 #pragma unroll
                     for (int c8 = 0; c8 < 4; ++c8) {
                         const uint4 xv = xr[4 * hh + c8], yv = dyr[4 * hh + c8];
-                        const float xa[8] = {bf_lo(xv.x), bf_hi(xv.x), bf_lo(xv.y), bf_hi(xv.y),
-                                             bf_lo(xv.z), bf_hi(xv.z), bf_lo(xv.w), bf_hi(xv.w)};
-                        const float ya[8] = {bf_lo(yv.x), bf_hi(yv.x), bf_lo(yv.y), bf_hi(yv.y),
-                                             bf_lo(yv.z), bf_hi(yv.z), bf_lo(yv.w), bf_hi(yv.w)};
-                        // dt * x exactly as the yo MMA saw it (bf16), so that sum_t tgt and
-                        // sum_s src are sums of the same products and cancel to fp32 rounding
-                        const uint32_t q0 = pack_bf2(xa[0] * dti, xa[1] * dti), q1 = pack_bf2(xa[2] * dti, xa[3] * dti);
-                        const uint32_t q2 = pack_bf2(xa[4] * dti, xa[5] * dti), q3 = pack_bf2(xa[6] * dti, xa[7] * dti);
-                        const float xd[8] = {bf_lo(q0), bf_hi(q0), bf_lo(q1), bf_hi(q1),
-                                             bf_lo(q2), bf_hi(q2), bf_lo(q3), bf_hi(q3)};
+                        const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w}, yw[4] = {yv.x, yv.y, yv.z, yv.w};
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) {
-                            const float zz = z[8 * c8 + e];
-                            ddo = fmaf(xa[e], zz, ddo);
-                            src = fmaf(xd[e], zz, src);
-                            dd = fmaf(xa[e], ya[e], dd);
-                            o[8 * c8 + e] = valid ? fmaf(dti, zz, Dh * ya[e]) : 0.f;
+                        for (int j = 0; j < 4; ++j) {
+                            const float2 x2 = bf2_to_f2(xw[j]), y2 = bf2_to_f2(yw[j]);
+                            const float2 z2 = make_float2(z[8 * c8 + 2 * j], z[8 * c8 + 2 * j + 1]);
+                            // dt * x exactly as the yo MMA saw it (bf16), so that sum_t tgt and
+                            // sum_s src are sums of the same products and cancel to fp32 rounding
+                            const float2 xp = fmul2(x2, dti2);
+                            const float2 xd2 = bf2_to_f2(pack_bf2(xp.x, xp.y));
+                            ddo2 = ffma2(x2, z2, ddo2);
+                            src2 = ffma2(xd2, z2, src2);
+                            dd2 = ffma2(x2, y2, dd2);
+                            const float2 o2 = ffma2(dti2, z2, fmul2(Dh2, y2));
+                            o[4 * c8 + j] = valid ? pack_bf2(o2.x, o2.y) : 0u;
                         }
                     }
-                    if (t0 + i < p.L) store_row32_bf16(DX + ix_x(p, bi, t0 + i, h, 32 * hh), o);
+                    if (t0 + i < p.L) {
+                        uint4 *dst = reinterpret_cast<uint4 *>(DX + ix_x(p, bi, t0 + i, h, 32 * hh));
+#pragma unroll
+                        for (int c = 0; c < 4; ++c) dst[c] = make_uint4(o[4 * c], o[4 * c + 1], o[4 * c + 2], o[4 * c + 3]);
+                    }
                 }
 #pragma unroll
                 for (int hh = 0; hh < 2; ++hh) {
@@ -1502,16 +1504,17 @@ __global__ void __launch_bounds__(kThreadsWide, 1) tc_bwd_orange_kernel(const Pa
 #pragma unroll
                     for (int c8 = 0; c8 < 4; ++c8) {
                         const uint4 yv = dyr[4 * hh + c8];
-                        const float ya[8] = {bf_lo(yv.x), bf_hi(yv.x), bf_lo(yv.y), bf_hi(yv.y),
-                                             bf_lo(yv.z), bf_hi(yv.z), bf_lo(yv.w), bf_hi(yv.w)};
+                        const uint32_t yw[4] = {yv.x, yv.y, yv.z, yv.w};
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) tgt = fmaf(ya[e], y[8 * c8 + e], tgt);
+                        for (int j = 0; j < 4; ++j)
+                            tgt2 = ffma2(bf2_to_f2(yw[j]), make_float2(y[8 * c8 + 2 * j], y[8 * c8 + 2 * j + 1]), tgt2);
                     }
                 }
                 const size_t cbase = ix_chunk(p, bi, h, c) * Q;
-                p.ddt_main[cbase + i] = valid ? ddo : 0.f;             // the K3 backward adds its terms
-                p.dcum_main[cbase + i] = valid ? tgt - src : 0.f;
+                p.ddt_main[cbase + i] = valid ? ddo2.x + ddo2.y : 0.f;  // the K3 backward adds its terms
+                p.dcum_main[cbase + i] = valid ? (tgt2.x + tgt2.y) - (src2.x + src2.y) : 0.f;
             }
+            float dd = dd2.x + dd2.y;
             dd = warp_sum(dd);
             if (lane == 0) p.dD_part[(((size_t)bi * p.n + c) * p.H + h) * p.dD_per + warp] = dd;
         }
