@@ -55,8 +55,9 @@ cudaError_t launch_k1_cumsum(const Params &p, cudaStream_t s) {
 // One thread per 16 consecutive (p, r) entries of one (b, h) state, 128-thread
 // blocks, sized so that the whole grid is resident at once: the chain over
 // chunks is serial, so a second wave would double the kernel's time.  The
-// chunk-state reads do not depend on the carry; they are issued kAhead chunks
-// ahead and held packed (8 registers per 16 bf16) until used.  The slot
+// chunk-state reads do not depend on the carry; they are issued a fixed number
+// of chunks ahead (the forward refills a slot as soon as it is consumed) and
+// held packed (8 registers per 16 bf16) until used.  The slot
 // holding intra_c is overwritten with the chunk-input state s_c.  The carry is
 // fp32; the stored states are S (fp32 on the CUDA-core path, bf16 on the
 // tensor-core path, whose every consumer reads bf16 operands).
@@ -120,7 +121,7 @@ __device__ __forceinline__ void store16(bf16 *dst, const float *v) {
 
 // chunks read ahead: bounded by registers (the grid must stay one wave)
 template <typename S>
-__host__ __device__ constexpr int k4_ahead_fwd() { return sizeof(S) == 2 ? 6 : 3; }
+__host__ __device__ constexpr int k4_ahead_fwd() { return sizeof(S) == 2 ? 4 : 2; }
 template <typename S>
 __host__ __device__ constexpr int k4_ahead_bwd() { return sizeof(S) == 2 ? 4 : 2; }
 
@@ -139,19 +140,30 @@ __global__ void __launch_bounds__(kK4Threads, 5) k4_state_passing(Params p, S *s
         for (int i = 0; i < kVec; ++i) s[i] = 0.f;
     }
     const float *endA = p.endA + ix_chunk(p, bi, h, 0);
-    for (int c0 = 0; c0 < p.n; c0 += U) {
-        Packed<S> in[U];
+    // rolling read-ahead: slot u holds chunk c (c % U == u) and is refilled with
+    // chunk c + U as soon as it is consumed, so U chunk loads stay in flight
+    Packed<S> in[U];
+    float ea[U];
 #pragma unroll
-        for (int u = 0; u < U; ++u)
-            if (c0 + u < p.n) in[u] = load16(st + ix_state(p, bi, c0 + u, h) + kVec * e);
+    for (int u = 0; u < U; ++u)
+        if (u < p.n) {
+            in[u] = load16(st + ix_state(p, bi, u, h) + kVec * e);
+            ea[u] = endA[u];
+        }
+    for (int c0 = 0; c0 < p.n; c0 += U) {
 #pragma unroll
         for (int u = 0; u < U; ++u) {
             const int c = c0 + u;
             if (c < p.n) {
+                const Packed<S> cur = in[u];
+                const float a = __expf(ea[u]);
+                if (c + U < p.n) {
+                    in[u] = load16(st + ix_state(p, bi, c + U, h) + kVec * e);
+                    ea[u] = endA[c + U];
+                }
                 store16(st + ix_state(p, bi, c, h) + kVec * e, s);
-                const float a = __expf(endA[c]);
                 float v[kVec];
-                unpack16(in[u], v);
+                unpack16(cur, v);
 #pragma unroll
                 for (int i = 0; i < kVec; ++i) s[i] = fmaf(a, s[i], v[i]);
             }
