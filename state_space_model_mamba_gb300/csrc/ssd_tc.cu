@@ -1651,102 +1651,159 @@ __global__ void __launch_bounds__(kThreadsWide, 2) tc_bwd_dcb_kernel(const Param
             issued = 2;
         }
     }
-    if (nh > 0) {
-        fetch(0);
-        stash(0);
-    }
-    if (nh > 1) {
-        fetch(1);
-        stash(1);
-    }
-    if (nh > 2) fetch(2);
-    __syncthreads();
-    if (nh > 0) derive(0);
-    // Wait for head k's tiles, zero x rows past valid_len, and (thread 0) issue
-    // dW_k into TMEM buffer k & 1.  Returns a CTA-uniform status.
-    auto land_and_mma = [&](int k, bool ok_in) -> bool {
-        const int st = k & 1;
-        bool ok = ok_in && mbar_wait(&bar_tma[st], (uint32_t)((k >> 1) & 1));
-        if (tid == 0 && ok) landed = k + 1;
-        if (ok && xrow < 128) {
-            zero_rows_from(sm + st * STG + kTile, 128, xrow);
+    bool ok = true, okt = true;
+    if (!diag) {
+        // ---- the block below the diagonal: its pivot P = cumA[128 sk + 127] (the last
+        // column) lies between every s and t of the block, so the decay factors into a
+        // dy row scale and an x row scale (both <= 1), and the sum over heads is one
+        // long-K accumulation in TMEM with no per-head epilogue:
+        //   d_cb[t, s] = sum_h sum_p (dy_h[t, p] exp(cumA_t - P)) (x_h[s, p] dt_s exp(P - cumA_s))
+        // Thread r < 128 scales dy row 128 tb + r, thread 128 + r scales x row 128 sk + r.
+        const int r = tid & 127;
+        const bool on_dy = tid < 128;
+        const int row = on_dy ? 128 * tb + r : 128 * sk + r;  // chunk row
+        const bool rv = row < vrows;
+        float cr = 0.f, dr = 0.f, pr = 0.f, cn = 0.f, dn = 0.f, pn = 0.f;
+        auto fetch_o = [&](int k, float &cc, float &dd, float &pp) {
+            const size_t ck = ix_chunk(p, bi, h_begin + k, c) * Q;
+            pp = p.cumA[ck + 128 * sk + 127];
+            cc = p.cumA[ck + row];
+            dd = (!on_dy && rv) ? p.dt[ix_dt(p, bi, h_begin + k, t0 + row)] : 0.f;
+        };
+        if (nh > 0) fetch_o(0, cr, dr, pr);
+        if (nh > 1) fetch_o(1, cn, dn, pn);
+        for (int k = 0; k < nh && ok; ++k) {
+            const int st = k & 1;
+            const float fct = on_dy ? __expf(cr - pr) : dr * __expf(pr - cr);
+            cr = cn;
+            dr = dn;
+            pr = pn;
+            if (k + 2 < nh) fetch_o(k + 2, cn, dn, pn);
+            const bool okk = mbar_wait(&bar_tma[st], (uint32_t)((k >> 1) & 1));
+            if (tid == 0 && okk) landed = k + 1;
+            if (okk) scale_row_bf16x2(sm + st * STG + (on_dy ? 0 : kTile), r, fct, rv);
             fence_async_smem();
-        }
-        tc_fence_before();
-        ok = __syncthreads_and(ok ? 1 : 0) != 0;
-        tc_fence_after();
-        if (tid == 0 && ok) {
-            const uint32_t dys = smem_u32(sm + st * STG), xs = dys + kTile;
-            const uint32_t id = idesc_bf16(128, 128, false, false);
+            tc_fence_before();
+            ok = __syncthreads_and(okk ? 1 : 0) != 0;
+            tc_fence_after();
+            if (ok && tid == 0) {
+                const uint32_t dys = smem_u32(sm + st * STG), xs = dys + kTile;
+                const uint32_t id = idesc_bf16(128, 128, false, false);
 #pragma unroll
-            for (int ks = 0; ks < kP / 16; ++ks)
-                mma_bf16(tm + 128 * st, sdesc_kmajor(dys, ks, kTile), sdesc_kmajor(xs, ks, kTile), id, ks > 0);
-            mma_commit(&bar_mma[st]);
-        }
-        return ok;
-    };
-    bool ok = nh > 0 ? land_and_mma(0, true) : true, okt = true;
-    const bool row_ok = t < vrows;
-    const int tr = tl >> 6, u16 = (tl & 63) >> 4;  // 64-row block and 16-row sub-block (diagonal blocks)
-    for (int k = 0; k < nh && ok; ++k) {
-        const int st = k & 1;
-        if (k + 1 < nh) {
-            ok = land_and_mma(k + 1, okt);  // the epilogue of head k - 1 has left buffer (k + 1) & 1
-        } else {
-            ok = __syncthreads_and(okt ? 1 : 0) != 0;
-        }
-        if (k + 2 < nh) stash(k + 2);
-        if (k + 3 < nh) fetch(k + 3);
-        if (k + 1 < nh) derive(k + 1);
-        okt = ok && mbar_wait(&bar_mma[st], (uint32_t)((k >> 1) & 1));
-        tc_fence_after();
-        if (tid == 0 && okt && k + 2 < nh) {
-            issue(k + 2);  // stage st is free: MMA k has read it
-            issued = k + 3;
-        }
-        const float *f = fbuf + (k % NSC) * FST;
-        const float ct = f[t];
-        // ---- epilogue of head k: acc += dt_s exp(cumA_t - cumA_s) dW[t, s]
-#pragma unroll
-        for (int half = 0; half < 2; ++half) {
-            float dw[32];
-            tmem_ld32(tmem_addr(tm, 32 * q4, 128 * st + 64 * hf + 32 * half), dw);
-            const int s0 = cb0 + 32 * half;
-            float *a = acc + 32 * half;
-            if (row_ok && (!diag || hf < tr)) {
-                // one pivot for all 32 columns
-                const float e = __expf(ct - (diag ? f[5 * Q + (s0 >> 6)] : f[128 * sk + 127]));
-                const float4 *gv = reinterpret_cast<const float4 *>(f + (diag ? 3 : 2) * Q + s0);
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const float4 gq = gv[i];
-                    a[4 * i + 0] = fmaf(dw[4 * i + 0] * gq.x, e, a[4 * i + 0]);
-                    a[4 * i + 1] = fmaf(dw[4 * i + 1] * gq.y, e, a[4 * i + 1]);
-                    a[4 * i + 2] = fmaf(dw[4 * i + 2] * gq.z, e, a[4 * i + 2]);
-                    a[4 * i + 3] = fmaf(dw[4 * i + 3] * gq.w, e, a[4 * i + 3]);
+                for (int ks = 0; ks < kP / 16; ++ks)
+                    mma_bf16(tm, sdesc_kmajor(dys, ks, kTile), sdesc_kmajor(xs, ks, kTile), id, k > 0 || ks > 0);
+                mma_commit(&bar_mma[st]);
+                if (k + 2 < nh) {  // stage st takes head k + 2 once MMA k has read it
+                    if (mbar_wait(&bar_mma[st], (uint32_t)((k >> 1) & 1))) {
+                        issue(k + 2);
+                        issued = k + 3;
+                    } else {
+                        okt = false;
+                    }
                 }
-            } else if (row_ok && hf == tr) {
+            }
+        }
+        if (ok && nh > 0) okt = mbar_wait(&bar_mma[(nh - 1) & 1], (uint32_t)(((nh - 1) >> 1) & 1)) && okt;
+        tc_fence_after();
+        if (ok && nh > 0) tmem_ld64(tmem_addr(tm, 32 * q4, 64 * hf), acc);
+    } else {
+        if (nh > 0) {
+            fetch(0);
+            stash(0);
+        }
+        if (nh > 1) {
+            fetch(1);
+            stash(1);
+        }
+        if (nh > 2) fetch(2);
+        __syncthreads();
+        if (nh > 0) derive(0);
+        // Wait for head k's tiles, zero x rows past valid_len, and (thread 0) issue
+        // dW_k into TMEM buffer k & 1.  Returns a CTA-uniform status.
+        auto land_and_mma = [&](int k, bool ok_in) -> bool {
+            const int st = k & 1;
+            bool ok = ok_in && mbar_wait(&bar_tma[st], (uint32_t)((k >> 1) & 1));
+            if (tid == 0 && ok) landed = k + 1;
+            if (ok && xrow < 128) {
+                zero_rows_from(sm + st * STG + kTile, 128, xrow);
+                fence_async_smem();
+            }
+            tc_fence_before();
+            ok = __syncthreads_and(ok ? 1 : 0) != 0;
+            tc_fence_after();
+            if (tid == 0 && ok) {
+                const uint32_t dys = smem_u32(sm + st * STG), xs = dys + kTile;
+                const uint32_t id = idesc_bf16(128, 128, false, false);
 #pragma unroll
-                for (int v2 = 0; v2 < 2; ++v2) {
-                    const int sv = s0 + 16 * v2, v16 = 2 * half + v2;
-                    float *av = a + 16 * v2;
-                    const float *dv = dw + 16 * v2;
-                    if (v16 < u16) {
-                        const float e = __expf(ct - f[5 * Q + Q / 64 + (sv >> 4)]);
-                        const float4 *gv = reinterpret_cast<const float4 *>(f + 4 * Q + sv);
+                for (int ks = 0; ks < kP / 16; ++ks)
+                    mma_bf16(tm + 128 * st, sdesc_kmajor(dys, ks, kTile), sdesc_kmajor(xs, ks, kTile), id, ks > 0);
+                mma_commit(&bar_mma[st]);
+            }
+            return ok;
+        };
+        ok = nh > 0 ? land_and_mma(0, true) : true;
+        const bool row_ok = t < vrows;
+        const int tr = tl >> 6, u16 = (tl & 63) >> 4;  // 64-row block and 16-row sub-block (diagonal blocks)
+        for (int k = 0; k < nh && ok; ++k) {
+            const int st = k & 1;
+            if (k + 1 < nh) {
+                ok = land_and_mma(k + 1, okt);  // the epilogue of head k - 1 has left buffer (k + 1) & 1
+            } else {
+                ok = __syncthreads_and(okt ? 1 : 0) != 0;
+            }
+            if (k + 2 < nh) stash(k + 2);
+            if (k + 3 < nh) fetch(k + 3);
+            if (k + 1 < nh) derive(k + 1);
+            okt = ok && mbar_wait(&bar_mma[st], (uint32_t)((k >> 1) & 1));
+            tc_fence_after();
+            if (tid == 0 && okt && k + 2 < nh) {
+                issue(k + 2);  // stage st is free: MMA k has read it
+                issued = k + 3;
+            }
+            const float *f = fbuf + (k % NSC) * FST;
+            const float ct = f[t];
+            // ---- epilogue of head k: acc += dt_s exp(cumA_t - cumA_s) dW[t, s]
 #pragma unroll
-                        for (int i = 0; i < 4; ++i) {
-                            const float4 gq = gv[i];
-                            av[4 * i + 0] = fmaf(dv[4 * i + 0] * gq.x, e, av[4 * i + 0]);
-                            av[4 * i + 1] = fmaf(dv[4 * i + 1] * gq.y, e, av[4 * i + 1]);
-                            av[4 * i + 2] = fmaf(dv[4 * i + 2] * gq.z, e, av[4 * i + 2]);
-                            av[4 * i + 3] = fmaf(dv[4 * i + 3] * gq.w, e, av[4 * i + 3]);
-                        }
-                    } else if (v16 == u16) {
+            for (int half = 0; half < 2; ++half) {
+                float dw[32];
+                tmem_ld32(tmem_addr(tm, 32 * q4, 128 * st + 64 * hf + 32 * half), dw);
+                const int s0 = cb0 + 32 * half;
+                float *a = acc + 32 * half;
+                if (row_ok && (!diag || hf < tr)) {
+                    // one pivot for all 32 columns
+                    const float e = __expf(ct - (diag ? f[5 * Q + (s0 >> 6)] : f[128 * sk + 127]));
+                    const float4 *gv = reinterpret_cast<const float4 *>(f + (diag ? 3 : 2) * Q + s0);
 #pragma unroll
-                        for (int i = 0; i < 16; ++i) {
-                            const int s = sv + i;
-                            if (s <= t) av[i] = fmaf(dv[i] * f[Q + s], __expf(ct - f[s]), av[i]);
+                    for (int i = 0; i < 8; ++i) {
+                        const float4 gq = gv[i];
+                        a[4 * i + 0] = fmaf(dw[4 * i + 0] * gq.x, e, a[4 * i + 0]);
+                        a[4 * i + 1] = fmaf(dw[4 * i + 1] * gq.y, e, a[4 * i + 1]);
+                        a[4 * i + 2] = fmaf(dw[4 * i + 2] * gq.z, e, a[4 * i + 2]);
+                        a[4 * i + 3] = fmaf(dw[4 * i + 3] * gq.w, e, a[4 * i + 3]);
+                    }
+                } else if (row_ok && hf == tr) {
+#pragma unroll
+                    for (int v2 = 0; v2 < 2; ++v2) {
+                        const int sv = s0 + 16 * v2, v16 = 2 * half + v2;
+                        float *av = a + 16 * v2;
+                        const float *dv = dw + 16 * v2;
+                        if (v16 < u16) {
+                            const float e = __expf(ct - f[5 * Q + Q / 64 + (sv >> 4)]);
+                            const float4 *gv = reinterpret_cast<const float4 *>(f + 4 * Q + sv);
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) {
+                                const float4 gq = gv[i];
+                                av[4 * i + 0] = fmaf(dv[4 * i + 0] * gq.x, e, av[4 * i + 0]);
+                                av[4 * i + 1] = fmaf(dv[4 * i + 1] * gq.y, e, av[4 * i + 1]);
+                                av[4 * i + 2] = fmaf(dv[4 * i + 2] * gq.z, e, av[4 * i + 2]);
+                                av[4 * i + 3] = fmaf(dv[4 * i + 3] * gq.w, e, av[4 * i + 3]);
+                            }
+                        } else if (v16 == u16) {
+#pragma unroll
+                            for (int i = 0; i < 16; ++i) {
+                                const int s = sv + i;
+                                if (s <= t) av[i] = fmaf(dv[i] * f[Q + s], __expf(ct - f[s]), av[i]);
+                            }
                         }
                     }
                 }
