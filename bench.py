@@ -57,8 +57,10 @@ def load_peaks():
 
 def kernel_costs(w, tc: bool) -> dict:
     """Algorithmic work of each kernel per launch: (flops, bytes).  Flops count
-    the causal half of the Q x Q blocks; bytes count every input read once and
-    every output written once."""
+    the causal half of the Q x Q blocks (and K2 / its backward per group, not per
+    head); bytes count every input of the kernel read once and every output
+    written once, intermediates at the precision the path stores them (chunk
+    states and CB in bf16 on the tensor-core path, fp32 on the CUDA-core path)."""
     b, L, H, P, N, G, Q = w.batch, w.seqlen, w.nheads, w.headdim, w.dstate, w.ngroups, w.chunk_len
     n = -(-L // Q)
     Lp = n * Q
@@ -68,25 +70,33 @@ def kernel_costs(w, tc: bool) -> dict:
     tok_h = b * H * L
     x_b = s * b * L * H * P                      # one [b,L,H,P] tensor
     bc_b = s * b * L * G * N                     # one [b,L,G,N] tensor
-    cum_b = 4 * b * H * Lp
-    stb = 4 * st + (2 * st if tc else 0)         # fp32 state (+ bf16 operand copy)
+    cum_b = 4 * b * H * Lp                       # one per-token fp32 [b,H,n,Q] array
+    sts = 2 if tc else 4                         # bytes per stored chunk-state element
+    cbs = 2 if tc else 4                         # bytes per stored CB element
+    cb_b = cbs * b * n * G * tri                 # causal CB of every (chunk, group)
     c = {
         "k1_chunk_cumsum": (0.0, 4 * tok_h + cum_b + 4 * b * H * n),
-        "k2_cb": (2.0 * b * n * G * tri * N, 2 * bc_b + 4 * b * n * G * tri),
-        "k3_state": (2.0 * b * n * H * Q * P * N, x_b + bc_b + 4 * tok_h + cum_b + 4 * st),
-        "k4_state_passing": (2.0 * st, 4 * st + stb),
+        "k2_cb": (2.0 * b * n * G * tri * N, 2 * bc_b + cb_b * (2 if tc else 1)),   # CB and CB^T on tc
+        "k3_state": (2.0 * b * n * H * Q * P * N, x_b + bc_b + 4 * tok_h + cum_b + sts * st),
+        "k4_state_passing": (2.0 * st, 2 * sts * st + 4 * b * H * n),
         "k5_scan": (b * n * H * (2.0 * Q * P * N + 2.0 * tri * P),
-                    2 * x_b + bc_b + 4 * b * n * G * tri + (2 if tc else 4) * st + cum_b + 4 * tok_h),
-        "bwd_blue": (b * n * H * 4.0 * Q * P * N, x_b + bc_b + (2 if tc else 4) * st + 4 * st + 2 * cum_b),
-        "bwd_k4_state_passing": (4.0 * st, 8 * st + stb),
+                    2 * x_b + bc_b + cb_b + sts * st + cum_b + 4 * tok_h),
+        "bwd_blue": (b * n * H * 4.0 * Q * P * N, x_b + bc_b + 2 * sts * st + 2 * cum_b),
+        "bwd_k4_state_passing": (4.0 * st, 3 * sts * st + 4 * b * H * n),
         "bwd_main": (b * n * H * (4.0 * tri * P + 2.0 * Q * P * N),
-                     3 * x_b + bc_b + 4 * b * n * G * tri + (2 if tc else 4) * st + 6 * cum_b),
-        "bwd_k3": (b * n * H * 2.0 * Q * P * N,
-                   2 * x_b + bc_b + (2 if tc else 4) * st + 4 * cum_b),
-        "bwd_orange": (b * n * H * 4.0 * tri * P,
-                       4 * x_b + 2 * b * n * G * tri + 6 * cum_b),
+                     3 * x_b + bc_b + cb_b + sts * st + 6 * cum_b),
+        # ORANGE backward: dx' = M^T dy and yo = M (dt x) per head; writes dx and two per-token arrays
+        "bwd_orange": (b * n * H * 4.0 * tri * P, 3 * x_b + cb_b + 2 * cum_b + 2 * cum_b),
+        # K3 backward: U = B d_intra^T per head; adds into dx, ddt_main, d cumA (read + write)
+        "bwd_k3": (b * n * H * 2.0 * Q * P * N, 3 * x_b + bc_b + sts * st + 2 * cum_b + 5 * cum_b),
+        # G1: d_cb = sum over the group's heads of dW o decay o dt (dW causal per head)
+        "bwd_dcb": (b * n * H * 2.0 * tri * P, 2 * x_b + 2 * cum_b + cbs * b * n * G * Q * Q),
+        # G2: dC = d_cb B + sum_h (dy exp cumA) s_in, dB = d_cb^T C + sum_h (x bbs) d_intra
+        "bwd_dbc": (b * n * G * 4.0 * tri * N + b * n * H * 4.0 * Q * P * N,
+                    2 * x_b + 2 * sts * st + 2 * bc_b + cbs * b * n * G * Q * Q + 2 * cum_b + 2 * 4 * b * L * G * N),
+        "bwd_dbc_reduce": (0.0, 2 * 4 * b * L * G * N + 2 * bc_b),
         "bwd_group": (b * n * G * 4.0 * tri * N + b * n * H * 4.0 * Q * P * N,
-                      2 * x_b + 2 * (2 if tc else 4) * st + 4 * bc_b + 2 * cum_b),
+                      2 * x_b + 2 * sts * st + 4 * bc_b + 2 * cum_b),
         "bwd_k1_chunk_cumsum": (0.0, 4 * cum_b + 8 * tok_h),
         "bwd_finalize": (0.0, 4 * b * H * n * 2),
     }
@@ -376,7 +386,10 @@ def run_ours(args, w, rank, world, local_rank):
     roof["algorithmic_bytes_per_launch"] = byts
     roof["traffic"] = ncu_traffic(top, w.name)
 
-    # ---------------- end to end: pinned host buffers -> device -> host every step
+    # ---------------- end to end: pinned host buffers -> device -> host every step.
+    # Every step's inputs cross to the device and its results cross back inside the
+    # timed region; the copies of step i + 1's inputs (one copy stream) and of step
+    # i - 1's results (another) run while step i computes, on two device buffer sets.
     host_in = {k: torch.from_numpy(np.ascontiguousarray(inp[k])).to(
         dtype=(bf if k in ("x", "B", "C", "dy") else torch.float32)).pin_memory()
         for k in ("x", "dt", "A", "B", "C", "D", "dy")}
@@ -391,21 +404,60 @@ def run_ours(args, w, rank, world, local_rank):
     h2d = sum(t.numel() * t.element_size() for t in host_in.values())
     d2h = sum(t.numel() * t.element_size() for t in host_out.values())
     e2e_steps = max(3, min(args.steps, 20))
+    sets = []
+    for _ in range(2):
+        din = {k: (None if v is None else torch.empty_like(v)) for k, v in dev_in.items()}
+        din["valid_len"] = vl
+        sets.append((din, {k: torch.empty_like(v) for k, v in outs.items()}))
+    s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    ev_in = [torch.cuda.Event() for _ in range(2)]    # set j's inputs are on the device
+    ev_done = [torch.cuda.Event() for _ in range(2)]  # set j's step has finished
+    ev_out = [torch.cuda.Event() for _ in range(2)]   # set j's results are on the host
+    for j in range(2):
+        ev_done[j].record(stream)
+        ev_out[j].record(stream)
 
-    def e2e_step():
-        for k, t in host_in.items():
-            dev_in[k].copy_(t, non_blocking=True)
-        step()
-        for k, t in outs.items():
-            host_out[k].copy_(t, non_blocking=True)
+    def e2e_h2d(j):
+        with torch.cuda.stream(s_in):
+            s_in.wait_event(ev_done[j])  # the previous step on set j no longer reads its inputs
+            for k, t in host_in.items():
+                sets[j][0][k].copy_(t, non_blocking=True)
+            ev_in[j].record(s_in)
 
-    e2e_step()
+    def e2e_compute(j):
+        d, o = sets[j]
+        stream.wait_event(ev_in[j])
+        stream.wait_event(ev_out[j])  # set j's previous results have left the device
+        ssd.forward_into(dims, d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"], d["init"],
+                         d["valid_len"], o["y"], o["final_state"], ws)
+        ssd.backward_into(dims, d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"], d["init"],
+                          d["valid_len"], d["dy"], d["d_final"], o["dx"], o["ddt"], o["dA"], o["dB"],
+                          o["dC"], o["dD"], o["d_init"], ws)
+        ev_done[j].record(stream)
+
+    def e2e_d2h(j):
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(ev_done[j])
+            for k in outs:
+                host_out[k].copy_(sets[j][1][k], non_blocking=True)
+            ev_out[j].record(s_out)
+
+    def e2e_run(nsteps):
+        e2e_h2d(0)
+        for i in range(nsteps):
+            if i + 1 < nsteps:
+                e2e_h2d((i + 1) % 2)
+            e2e_compute(i % 2)
+            e2e_d2h(i % 2)
+        for j in range(2):
+            stream.wait_event(ev_out[j])
+
+    e2e_run(2)
     torch.cuda.synchronize()
     barrier()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    for _ in range(e2e_steps):
-        e2e_step()
+    e2e_run(e2e_steps)
     e1.record(stream)
     torch.cuda.synchronize()
     barrier()
@@ -431,7 +483,8 @@ def run_ours(args, w, rank, world, local_rank):
                     for k, s in sorted(shares.items(), key=lambda kv: -kv[1]["share"])},
         "e2e": {"value": w.tokens * world / (e2e_ms * 1e-3), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "ms_per_step": e2e_ms, "steps": e2e_steps},
+                "ms_per_step": e2e_ms, "steps": e2e_steps,
+                "overlap": "step i+1 inputs up and step i-1 results down on two copy streams during step i"},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks.summary(),
     }
