@@ -333,7 +333,9 @@ ssd_status ssd_backward(const ssd_dims *dims, ssd_dtype dtype, const void *x, co
             SSD_LAUNCH("bwd_k4_state_passing", launch_bwd_k4(p, s), 1);
             SSD_LAUNCH("bwd_orange_tc", launch_tc_bwd_orange(p, s), 1);
             SSD_LAUNCH("bwd_k3_tc", launch_tc_bwd_k3(p, s), 1);
-            SSD_LAUNCH("bwd_group_tc", launch_tc_bwd_group(p, s), 3);
+            SSD_LAUNCH("bwd_dcb_tc", launch_tc_bwd_dcb(p, s), 1);
+            SSD_LAUNCH("bwd_dbc_tc", launch_tc_bwd_dbc(p, s), 1);
+            SSD_LAUNCH("bwd_dbc_reduce_tc", launch_tc_bwd_dbc_reduce(p, s), 1);
         } else {
             SSD_LAUNCH("bwd_blue_simt", launch_simt_bwd_blue<bf16>(p, s), 2);
             SSD_LAUNCH("bwd_k4_state_passing", launch_bwd_k4(p, s), 1);

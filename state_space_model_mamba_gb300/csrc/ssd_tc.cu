@@ -2284,15 +2284,21 @@ int tc_dcb_slices(const ssd_dims &d) {
     return (int)best;
 }
 int tc_k5_slices(const ssd_dims &d) {
-    // about 8 heads per CTA (the resident C / CB loads amortise over them),
-    // but at least two CTAs per SM
+    // one CTA per SM: heads per CTA chosen to minimise waves x (heads per CTA + 1),
+    // the +1 standing for the CTA's fixed cost (resident operands, TMEM, tables)
     const long long hpg = d.nheads / d.ngroups;
     const long long n = (d.seqlen + d.chunk_len - 1) / d.chunk_len;
     const long long groups = d.batch * n * d.ngroups;
-    long long s = (hpg + 7) / 8;
-    while (s < hpg && groups * s < 2 * 152) ++s;
-    if (s < 1) s = 1;
-    return (int)s;
+    long long best = 1, best_cost = -1;
+    for (long long per = hpg; per >= 1; --per) {
+        const long long ns = (hpg + per - 1) / per;
+        const long long cost = ((groups * ns + 151) / 152) * (per + 1);
+        if (best_cost < 0 || cost < best_cost) {
+            best = ns;
+            best_cost = cost;
+        }
+    }
+    return (int)best;
 }
 int tc_k3_slices(const ssd_dims &d) {
     // one CTA per SM: minimise waves x (heads per CTA + the resident operand's
@@ -2390,22 +2396,31 @@ cudaError_t launch_tc_bwd_orange(const Params &p, cudaStream_t s) {
 #undef CALL
 }
 
-cudaError_t launch_tc_bwd_group(const Params &p, cudaStream_t s) {
+cudaError_t launch_tc_bwd_dcb(const Params &p, cudaStream_t s) {
     TcMaps m;
     cudaError_t e = make_maps(p, &m, true);
     if (e != cudaSuccess) return e;
-    const unsigned g1 = (unsigned)(p.b * p.n * p.G * p.nslice_cb * (p.Q == 256 ? 3 : 1));
-    const unsigned g2 = (unsigned)(p.b * p.n * p.G * p.nslice);
-#define CALL1(Q) launch(tc_bwd_dcb_kernel<Q>, g1, smem_dcb(Q), s, p, m, kThreadsWide)
-#define CALL2(Q) launch(tc_bwd_dbc_kernel<Q>, g2, smem_dbc(Q), s, p, m, kThreadsWide + 32)
-    if ((e = SSD_TC_DISPATCH(p.Q, CALL1)) != cudaSuccess) return e;
-    if ((e = SSD_TC_DISPATCH(p.Q, CALL2)) != cudaSuccess) return e;
-#undef CALL1
-#undef CALL2
+    const unsigned grid = (unsigned)(p.b * p.n * p.G * p.nslice_cb * (p.Q == 256 ? 3 : 1));
+#define CALL(Q) launch(tc_bwd_dcb_kernel<Q>, grid, smem_dcb(Q), s, p, m, kThreadsWide)
+    return SSD_TC_DISPATCH(p.Q, CALL);
+#undef CALL
+}
+
+cudaError_t launch_tc_bwd_dbc(const Params &p, cudaStream_t s) {
+    TcMaps m;
+    cudaError_t e = make_maps(p, &m, true);
+    if (e != cudaSuccess) return e;
+    const unsigned grid = (unsigned)(p.b * p.n * p.G * p.nslice);
+#define CALL(Q) launch(tc_bwd_dbc_kernel<Q>, grid, smem_dbc(Q), s, p, m, kThreadsWide + 32)
+    return SSD_TC_DISPATCH(p.Q, CALL);
+#undef CALL
+}
+
+cudaError_t launch_tc_bwd_dbc_reduce(const Params &p, cudaStream_t s) {
     const size_t nvec = (size_t)p.b * p.L * p.G * (kN / 4);
-    const unsigned g3 = (unsigned)((nvec + 255) / 256);
-    if (p.Q == 256) tc_bwd_dbc_reduce<256><<<g3, 256, 0, s>>>(p);
-    else tc_bwd_dbc_reduce<128><<<g3, 256, 0, s>>>(p);
+    const unsigned grid = (unsigned)((nvec + 255) / 256);
+    if (p.Q == 256) tc_bwd_dbc_reduce<256><<<grid, 256, 0, s>>>(p);
+    else tc_bwd_dbc_reduce<128><<<grid, 256, 0, s>>>(p);
     return cudaGetLastError();
 }
 

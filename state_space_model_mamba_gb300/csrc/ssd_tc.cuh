@@ -24,6 +24,8 @@ cudaError_t launch_tc_k5(const Params &p, cudaStream_t s);
 cudaError_t launch_tc_bwd_blue(const Params &p, cudaStream_t s);
 cudaError_t launch_tc_bwd_k3(const Params &p, cudaStream_t s);
 cudaError_t launch_tc_bwd_orange(const Params &p, cudaStream_t s);
-cudaError_t launch_tc_bwd_group(const Params &p, cudaStream_t s);
+cudaError_t launch_tc_bwd_dcb(const Params &p, cudaStream_t s);         // G1: d_cb over the group's heads
+cudaError_t launch_tc_bwd_dbc(const Params &p, cudaStream_t s);         // G2: dB, dC partial sums
+cudaError_t launch_tc_bwd_dbc_reduce(const Params &p, cudaStream_t s);  // G3: sum of the partials
 
 }  // namespace ssd
