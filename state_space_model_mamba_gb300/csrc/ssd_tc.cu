@@ -1576,17 +1576,18 @@ __global__ void __launch_bounds__(kThreadsWide, 2) tc_bwd_dcb_kernel(const Param
     const int h_begin = g * p.hpg + slice * per;
     const int nh = max(0, min(g * p.hpg + p.hpg, h_begin + per) - h_begin);
     const int tl = 32 * q4 + lane, t = 128 * tb + tl;  // this thread's row
-    const int cb0 = 128 * sk + 64 * hf;                // and its first column
+    // and its columns: two 32-wide pieces, 32 hf + 64 j (j = 0, 1) inside the block,
+    // so that on a diagonal block every warp has at most one piece on the diagonal
+    auto colp = [&](int j) { return 32 * hf + 64 * j; };
     const size_t cbase = ((size_t)bi * p.n + c) * p.G + g;  // (b, chunk, group)
     const size_t pstride = (size_t)p.b * p.n * p.G * Q * Q;   // between slices' partials
-    const size_t roff = cbase * Q * Q + (size_t)t * Q + cb0;  // this thread's 64 columns
-    bf16 *brow = p.d_cb_bf + roff;
+    const size_t rbase = cbase * Q * Q + (size_t)t * Q + 128 * sk;  // this thread's row of the block
     float acc[64];
 #pragma unroll
     for (int i = 0; i < 64; ++i) acc[i] = 0.f;
     auto write_bf16 = [&](const float *v) {
 #pragma unroll
-        for (int i = 0; i < 2; ++i) store_row32_bf16(brow + 32 * i, v + 32 * i);
+        for (int j = 0; j < 2; ++j) store_row32_bf16(p.d_cb_bf + rbase + colp(j), v + 32 * j);
     };
     if (vrows <= 128 * tb) {  // the whole block lies past valid_len: zeros, written once
         if (slice == 0) write_bf16(acc);
@@ -1705,7 +1706,10 @@ __global__ void __launch_bounds__(kThreadsWide, 2) tc_bwd_dcb_kernel(const Param
         }
         if (ok && nh > 0) okt = mbar_wait(&bar_mma[(nh - 1) & 1], (uint32_t)(((nh - 1) >> 1) & 1)) && okt;
         tc_fence_after();
-        if (ok && nh > 0) tmem_ld64(tmem_addr(tm, 32 * q4, 64 * hf), acc);
+        if (ok && nh > 0) {
+            tmem_ld32(tmem_addr(tm, 32 * q4, colp(0)), acc);
+            tmem_ld32(tmem_addr(tm, 32 * q4, colp(1)), acc + 32);
+        }
     } else {
         if (nh > 0) {
             fetch(0);
@@ -1766,10 +1770,10 @@ __global__ void __launch_bounds__(kThreadsWide, 2) tc_bwd_dcb_kernel(const Param
 #pragma unroll
             for (int half = 0; half < 2; ++half) {
                 float dw[32];
-                tmem_ld32(tmem_addr(tm, 32 * q4, 128 * st + 64 * hf + 32 * half), dw);
-                const int s0 = cb0 + 32 * half;
+                tmem_ld32(tmem_addr(tm, 32 * q4, 128 * st + colp(half)), dw);
+                const int s0 = 128 * sk + colp(half);  // the piece's 64-column block is `half`
                 float *a = acc + 32 * half;
-                if (row_ok && (!diag || hf < tr)) {
+                if (row_ok && (!diag || half < tr)) {
                     // one pivot for all 32 columns
                     const float e = __expf(ct - (diag ? f[5 * Q + (s0 >> 6)] : f[128 * sk + 127]));
                     const float4 *gv = reinterpret_cast<const float4 *>(f + (diag ? 3 : 2) * Q + s0);
@@ -1781,10 +1785,10 @@ __global__ void __launch_bounds__(kThreadsWide, 2) tc_bwd_dcb_kernel(const Param
                         a[4 * i + 2] = fmaf(dw[4 * i + 2] * gq.z, e, a[4 * i + 2]);
                         a[4 * i + 3] = fmaf(dw[4 * i + 3] * gq.w, e, a[4 * i + 3]);
                     }
-                } else if (row_ok && hf == tr) {
+                } else if (row_ok && half == tr) {
 #pragma unroll
                     for (int v2 = 0; v2 < 2; ++v2) {
-                        const int sv = s0 + 16 * v2, v16 = 2 * half + v2;
+                        const int sv = s0 + 16 * v2, v16 = 2 * hf + v2;
                         float *av = a + 16 * v2;
                         const float *dv = dw + 16 * v2;
                         if (v16 < u16) {
@@ -1824,9 +1828,10 @@ __global__ void __launch_bounds__(kThreadsWide, 2) tc_bwd_dcb_kernel(const Param
     // and writes the block in bf16
     const int ns = p.nslice_cb;
     if (ns > 1) {
-        float4 *dst = reinterpret_cast<float4 *>(p.d_cb + slice * pstride + roff);
 #pragma unroll
-        for (int i = 0; i < 16; ++i) dst[i] = make_float4(acc[4 * i], acc[4 * i + 1], acc[4 * i + 2], acc[4 * i + 3]);
+        for (int i = 0; i < 16; ++i)
+            reinterpret_cast<float4 *>(p.d_cb + slice * pstride + rbase + colp(i >> 3))[i & 7] =
+                make_float4(acc[4 * i], acc[4 * i + 1], acc[4 * i + 2], acc[4 * i + 3]);
         __threadfence();
         __syncthreads();
         if (tid == 0) s_last = atomicAdd(p.cb_count + cbase * NBLK + blk, 1) == ns - 1;
@@ -1839,7 +1844,7 @@ __global__ void __launch_bounds__(kThreadsWide, 2) tc_bwd_dcb_kernel(const Param
             float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
             for (int sl = 0; sl < ns; ++sl) {
                 const float4 u = sl == slice ? make_float4(acc[4 * i], acc[4 * i + 1], acc[4 * i + 2], acc[4 * i + 3])
-                                             : __ldcg(reinterpret_cast<const float4 *>(p.d_cb + sl * pstride + roff) + i);
+                                             : __ldcg(reinterpret_cast<const float4 *>(p.d_cb + sl * pstride + rbase + colp(i >> 3)) + (i & 7));
                 v.x += u.x;
                 v.y += u.y;
                 v.z += u.z;

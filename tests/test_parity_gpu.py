@@ -42,6 +42,15 @@ def test_bf16_small_ragged_grouped(Q, simt):
     padded_grads_zero(gpu, inp["valid_len"])
 
 
+def test_bf16_q128_several_heads_per_cta():
+    # chunk 128 with enough chunks that every per-group kernel gives a CTA several
+    # heads (the small cases above give each CTA one head), ragged and grouped
+    inp = small(2, 8192, 8, 64, 128, 2, seed=58, valid_len=[8192, 5000], bf16=True)
+    gpu = run_gpu(inp, "bf16", 128)
+    compare(gpu, run_oracle(inp), TOL["bf16"], "bf16 Q=128 multi-head")
+    padded_grads_zero(gpu, inp["valid_len"])
+
+
 @pytest.mark.parametrize("N", [64, 128])
 def test_bf16_dstate(N):
     inp = small(1, 512, 2, 64, N, 1, seed=60 + N, bf16=True)
