@@ -7,6 +7,8 @@
 #include <stdio.h>
 #include <string.h>
 
+#include <mutex>
+
 #include "ssd.h"
 #include "ssd_internal.cuh"
 #include "ssd_tc.cuh"
@@ -46,6 +48,33 @@ cudaError_t mark_start(const char *name, cudaStream_t s) {
 cudaError_t mark_end(cudaStream_t s) {
     if (!g_rec.ev || (g_rec.n & 1) == 0) return cudaSuccess;
     return cudaEventRecord(g_rec.ev[g_rec.n++], s);
+}
+
+// A second stream per device, so that K2 (CB, which only K5 and the ORANGE
+// backward read) runs beside K1 instead of after it.  The caller's stream
+// forks to it and joins back through two events; the lock covers the
+// record / wait pairs, so concurrent callers never wait on each other's record.
+struct SideStream {
+    cudaStream_t st = nullptr;
+    cudaEvent_t fork = nullptr, join = nullptr;
+};
+constexpr int kMaxDevices = 64;
+SideStream g_side[kMaxDevices];
+std::mutex g_side_mu;
+
+cudaError_t side_stream(SideStream **out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    SideStream &sd = g_side[dev];
+    if (!sd.st) {
+        if ((e = cudaStreamCreateWithFlags(&sd.st, cudaStreamNonBlocking)) != cudaSuccess) return e;
+        if ((e = cudaEventCreateWithFlags(&sd.fork, cudaEventDisableTiming)) != cudaSuccess) return e;
+        if ((e = cudaEventCreateWithFlags(&sd.join, cudaEventDisableTiming)) != cudaSuccess) return e;
+    }
+    *out = &sd;
+    return cudaSuccess;
 }
 
 constexpr size_t kAlign = 256;
@@ -202,9 +231,24 @@ Params base_params(const ssd_dims &d, const Layout &lo, void *ws) {
 
 template <typename T>
 ssd_status run_forward_chain(const Params &p, bool tc, bool write_final, cudaStream_t s) {
-    SSD_LAUNCH("k1_chunk_cumsum", launch_k1_cumsum(p, s), 1);
     if (tc) {
-        SSD_LAUNCH("k2_cb_tc", launch_tc_k2(p, s), 1);
+        // K2 on the side stream beside K1; K3 starts once both are done
+        std::lock_guard<std::mutex> lock(g_side_mu);
+        SideStream *sd = nullptr;
+        SSD_TRY(side_stream(&sd));
+        SSD_TRY(cudaEventRecord(sd->fork, s));
+        SSD_TRY(cudaStreamWaitEvent(sd->st, sd->fork, 0));
+        {
+            cudaStream_t s = sd->st;
+            SSD_LAUNCH("k2_cb_tc", launch_tc_k2(p, s), 1);
+        }
+        SSD_TRY(cudaEventRecord(sd->join, sd->st));
+        SSD_LAUNCH("k1_chunk_cumsum", launch_k1_cumsum(p, s), 1);
+        SSD_TRY(cudaStreamWaitEvent(s, sd->join, 0));
+    } else {
+        SSD_LAUNCH("k1_chunk_cumsum", launch_k1_cumsum(p, s), 1);
+    }
+    if (tc) {
         SSD_LAUNCH("k3_state_tc", launch_tc_k3(p, s), 1);
     } else {
         SSD_LAUNCH("k2_cb_simt", launch_simt_k2<T>(p, s), 1);

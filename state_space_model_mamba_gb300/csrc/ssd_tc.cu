@@ -189,25 +189,34 @@ __device__ __forceinline__ void store_row32_bf16(bf16 *dst, const float *v) {
 }
 
 // ====================================================================== K2
-// CTA per (b, chunk, group).  CB[t, s] = sum_r C[t, r] B[s, r] for the causal
-// column range of each 128-row t-block (both operands K-major), stored in bf16
-// (it only ever feeds bf16 MMA operands); then CB^T[s, t] (t >= s's 128-row
-// block) the same way for the backward, whose ORANGE term works on rows s.
+// CTA per (b, chunk, group, 128-row block tb), 256 threads.  Both products of
+// the block are issued together and committed once, both operands K-major:
+//   CB[t, s]   = sum_r C[t, r] B[s, r],  t in block tb, s < 128 (tb + 1)   (TMEM cols [0, N1))
+//   CB^T[s, t] = sum_r B[s, r] C[t, r],  s in block tb, t >= 128 tb         (TMEM cols [N1, N1 + N2))
+// stored in bf16 (they only ever feed bf16 MMA operands); CB^T serves the
+// backward, whose ORANGE term works on rows s.  The block needs C blocks
+// tb .. and B blocks .. tb, nothing else.  Epilogue: the two warps of a TMEM
+// lane quadrant take alternate 64-column pieces.
 template <int Q>
-__global__ void __launch_bounds__(kThreads) tc_k2_kernel(const Params p, const __grid_constant__ TcMaps maps) {
+__global__ void __launch_bounds__(kThreadsWide) tc_k2_kernel(const Params p, const __grid_constant__ TcMaps maps) {
     constexpr int NT = Q / 128;
     constexpr uint32_t RB = Q * 128;  // one r-block ([Q rows][64])
+    constexpr uint32_t NCOL = NT == 2 ? 512 : 256;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = align1024(smem_raw);
     uint8_t *Cs = sm, *Bs = sm + 2 * RB;
     __shared__ uint64_t bar_tma, bar_mma;
     __shared__ uint32_t s_tmem;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int g = blockIdx.x % p.G, c = (blockIdx.x / p.G) % p.n, bi = blockIdx.x / (p.G * p.n);
+    const int q4 = warp & 3, hf = warp >> 2;
+    int idx = blockIdx.x;
+    const int tb = idx % NT;
+    idx /= NT;
+    const int g = idx % p.G, c = (idx / p.G) % p.n, bi = idx / (p.G * p.n);
     const int t0 = c * Q;
     const int vrows = min(Q, valid_len_of(p, bi) - t0);
     if (vrows <= 0) return;  // consumers never read CB of chunks past valid_len
-    constexpr uint32_t NCOL = NT == 2 ? 512 : 128;
+    const int N1 = 128 * (tb + 1), N2 = Q - 128 * tb;
     if (tid == 0) {
         mbar_init(&bar_tma, 1);
         mbar_init(&bar_mma, 1);
@@ -217,12 +226,13 @@ __global__ void __launch_bounds__(kThreads) tc_k2_kernel(const Params p, const _
     tc_sync();
     const uint32_t tm = s_tmem;
     if (tid == 0) {
-        mbar_arrive_expect_tx(&bar_tma, 4 * RB);
-        for (int rb = 0; rb < 2; ++rb)
-            for (int j = 0; j < NT; ++j) {
+        mbar_arrive_expect_tx(&bar_tma, 2u * (uint32_t)(NT - tb) * kTile + 2u * (uint32_t)(tb + 1) * kTile);
+        for (int rb = 0; rb < 2; ++rb) {
+            for (int j = tb; j < NT; ++j)
                 tma_load_4d(Cs + rb * RB + j * kTile, &maps.C, &bar_tma, 64 * rb, g, t0 + 128 * j, bi);
+            for (int j = 0; j <= tb; ++j)
                 tma_load_4d(Bs + rb * RB + j * kTile, &maps.B, &bar_tma, 64 * rb, g, t0 + 128 * j, bi);
-            }
+        }
     }
     bool ok = wait_all(&bar_tma, 0, true);
     if (ok && vrows < Q) {
@@ -234,53 +244,29 @@ __global__ void __launch_bounds__(kThreads) tc_k2_kernel(const Params p, const _
     fence_async_smem();
     tc_sync();
     if (tid == 0 && ok) {
-        for (int tb = 0; tb < NT; ++tb) {
-            const uint32_t idesc = idesc_bf16(128, 128 * (tb + 1), false, false);
-            const uint32_t col = tb == 0 ? 0u : 128u;
-            for (int ks = 0; ks < kN / 16; ++ks)
-                mma_bf16(tm + col, sdesc_kmajor(smem_u32(Cs + tb * kTile), ks, RB),
-                         sdesc_kmajor(smem_u32(Bs), ks, RB), idesc, ks > 0);
-        }
+        const uint32_t i1 = idesc_bf16(128, N1, false, false), i2 = idesc_bf16(128, N2, false, false);
+        for (int ks = 0; ks < kN / 16; ++ks)
+            mma_bf16(tm, sdesc_kmajor(smem_u32(Cs + tb * kTile), ks, RB), sdesc_kmajor(smem_u32(Bs), ks, RB), i1,
+                     ks > 0);
+        for (int ks = 0; ks < kN / 16; ++ks)
+            mma_bf16(tm + (uint32_t)N1, sdesc_kmajor(smem_u32(Bs + tb * kTile), ks, RB),
+                     sdesc_kmajor(smem_u32(Cs + tb * kTile), ks, RB), i2, ks > 0);
         mma_commit(&bar_mma);
     }
     ok = wait_all(&bar_mma, 0, ok);
     tc_fence_after();
     if (ok) {
-        bf16 *cb = p.CBh + ix_cb(p, bi, c, g);
-        for (int tb = 0; tb < NT; ++tb) {
-            const int t = tb * 128 + 32 * warp + lane;
-            const uint32_t col = tb == 0 ? 0u : 128u;
-            for (int s0 = 0; s0 < 128 * (tb + 1); s0 += 32) {
-                float v[32];
-                tmem_ld32(tmem_addr(tm, 32 * warp, col + s0), v);
-                store_row32_bf16(cb + (size_t)t * Q + s0, v);
-            }
-        }
-    }
-    // ---- CB^T (rows s, columns t >= 128 mb) for the backward's transposed ORANGE
-    tc_sync();
-    if (tid == 0 && ok) {
-        for (int mb = 0; mb < NT; ++mb) {
-            const uint32_t idesc = idesc_bf16(128, Q - 128 * mb, false, false);
-            const uint32_t col = mb == 0 ? 0u : 256u;
-            for (int ks = 0; ks < kN / 16; ++ks)
-                mma_bf16(tm + col, sdesc_kmajor(smem_u32(Bs + mb * kTile), ks, RB),
-                         sdesc_kmajor(smem_u32(Cs + mb * kTile), ks, RB), idesc, ks > 0);
-        }
-        mma_commit(&bar_mma);
-    }
-    ok = wait_all(&bar_mma, 1, ok);
-    tc_fence_after();
-    if (ok) {
-        bf16 *cbt = p.CBt + ix_cb(p, bi, c, g);
-        for (int mb = 0; mb < NT; ++mb) {
-            const int s = mb * 128 + 32 * warp + lane;
-            const uint32_t col = mb == 0 ? 0u : 256u;
-            for (int j = 0; j < Q - 128 * mb; j += 32) {
-                float v[32];
-                tmem_ld32(tmem_addr(tm, 32 * warp, col + j), v);
-                store_row32_bf16(cbt + (size_t)s * Q + 128 * mb + j, v);
-            }
+        const int r = 128 * tb + 32 * q4 + lane;  // CB row t, or CB^T row s
+        bf16 *cb = p.CBh + ix_cb(p, bi, c, g) + (size_t)r * Q;
+        bf16 *cbt = p.CBt + ix_cb(p, bi, c, g) + (size_t)r * Q + 128 * tb;
+        const int npc = (N1 + N2) / 64;
+#pragma unroll 1
+        for (int j = hf; j < npc; j += 2) {
+            float v[64];
+            tmem_ld64(tmem_addr(tm, 32 * q4, 64 * j), v);
+            bf16 *dst = 64 * j < N1 ? cb + 64 * j : cbt + (64 * j - N1);
+            store_row32_bf16(dst, v);
+            store_row32_bf16(dst + 32, v + 32);
         }
     } else if (tid == 0) {
         flag_timeout(p);
@@ -2224,7 +2210,8 @@ cudaError_t launch(K kernel, unsigned grid, size_t smem, cudaStream_t s, const P
     return cudaGetLastError();
 }
 
-constexpr size_t smem_k2(int Q) { return 1024 + 4 * (size_t)Q * 128; }
+// Q = 128 holds 256 TMEM columns per CTA: padded so that at most two CTAs share an SM.
+constexpr size_t smem_k2(int Q) { return Q == 128 ? 80 * 1024 : 1024 + 4 * (size_t)Q * 128; }
 constexpr size_t smem_k3(int Q) { return 1024 + 2 * (size_t)Q * 128 + 4 * (size_t)Q * 128; }
 constexpr size_t smem_k5(int Q) {
     return 1024 + 3 * (size_t)Q * 128 + 2 * 64 * 128 + (size_t)kTile * (Q / 128) * (Q / 128 + 1) +
@@ -2254,6 +2241,8 @@ constexpr size_t smem_dbc(int Q) {
 static_assert(smem_orange(256) <= 232448 && smem_orange(128) > 116 * 1024, "ORANGE backward: one CTA per SM");
 static_assert(smem_k3bwd(256) <= 232448 && smem_k3bwd(256) > 116 * 1024, "K3 backward: one CTA per SM");
 static_assert(smem_k2(256) > 116 * 1024, "K2 (512 TMEM columns): one CTA per SM");
+static_assert(smem_k2(128) >= 1024 + 4 * 128 * 128 && 3 * (smem_k2(128) + 1024) > 233472,
+              "K2 at Q = 128 (256 TMEM columns): at most two CTAs per SM");
 static_assert(smem_k5(256) <= 232448 && smem_k5(256) > 116 * 1024, "K5: one CTA per SM");
 static_assert(smem_k3(256) <= 232448 && smem_blue(256) <= 232448, "K3 / BLUE shared memory");
 static_assert(smem_blue(128) > 116 * 1024, "BLUE (512 TMEM columns): one CTA per SM");
@@ -2345,8 +2334,8 @@ cudaError_t launch_tc_k2(const Params &p, cudaStream_t s) {
     TcMaps m;
     cudaError_t e = make_maps(p, &m, false);
     if (e != cudaSuccess) return e;
-    const unsigned grid = (unsigned)(p.b * p.n * p.G);
-#define CALL(Q) launch(tc_k2_kernel<Q>, grid, smem_k2(Q), s, p, m)
+    const unsigned grid = (unsigned)(p.b * p.n * p.G * (p.Q / 128));
+#define CALL(Q) launch(tc_k2_kernel<Q>, grid, smem_k2(Q), s, p, m, kThreadsWide)
     return SSD_TC_DISPATCH(p.Q, CALL);
 #undef CALL
 }
