@@ -427,10 +427,13 @@ __global__ void __launch_bounds__(kThreadsWide + 32, 1) tc_k3_kernel(const Param
 // ====================================================================== K5
 // CTA per (b, chunk, group, head slice), 256 threads, looping over the slice's
 // heads with one CTA barrier per head.  C (BLUE's A operand) and the bf16 CB
-// tiles stay resident in shared memory; x and s_in are refilled per head by
-// TMA as soon as the previous head's MMAs complete, and land while this
-// head's W is built and the previous head's epilogue runs.  Per-head scalars
-// are prefetched two heads ahead.  Per 128-row t-block tb:
+// tiles stay resident in shared memory.  One thread issues the ORANGE MMAs and
+// another the BLUE MMAs of a head, each committing to its own mbarrier.  W of
+// t-block 0 has two TMEM buffers, so the next head's t-block-0 units (and its
+// scalar tables) are built while this head's ORANGE MMAs run; its t-block-1
+// units follow once they complete, while the BLUE MMAs may still run.  x is
+// refilled by TMA as soon as the ORANGE MMAs complete, s_in once the BLUE ones
+// do.  Per-head scalars are prefetched two heads ahead.  Per 128-row t-block tb:
 //   ORANGE (TMEM cols tb*64):        W[tb] (A operand in TMEM) x  (x MN-major)
 //   BLUE   (TMEM cols NT*64+tb*64):  C[tb] (K-major)            s_in (K-major)
 // y = ORANGE + exp(cumA_t) * BLUE + D x, W[t, s] = CB[t, s] exp(cumA_t - cumA_s) dt_s
@@ -445,7 +448,11 @@ __global__ void __launch_bounds__(kThreadsWide, 1) tc_k5_kernel(const Params p, 
     constexpr uint32_t XB = Q * 128, RB = Q * 128, SB = 64 * 128;
     constexpr int NWT = NT * (NT + 1);  // CB tiles: tb0 2, tb1 4
     constexpr uint32_t NCOL = NT == 2 ? 512 : 256;
-    constexpr uint32_t OCOL = 0, BCOL = NT * 64, WCOL = 2 * NT * 64;
+    // TMEM: ORANGE | BLUE accumulators, W of t-block 1 (4 units), two buffers of
+    // W of t-block 0 (2 units each; head k builds into one while the MMAs of
+    // head k - 1 read the other)
+    constexpr uint32_t OCOL = 0, BCOL = NT * 64, W1COL = 2 * NT * 64, W0COL = W1COL + (NT - 1) * 128;
+    static_assert(W0COL + 128 == NCOL, "K5 TMEM columns");
     constexpr int NSC = 3;              // scalar buffers: staged two heads ahead
     // per-head tables (32-bit words): cum Q | dt Q | gcol pairs Q/2 | T16 pairs (Q/64) x 4 x 32 | piv 8
     constexpr int GOFF = 2 * Q, TOFF = GOFF + Q / 2, POFF = TOFF + (Q / 64) * 128;
@@ -454,7 +461,7 @@ __global__ void __launch_bounds__(kThreadsWide, 1) tc_k5_kernel(const Params p, 
     uint8_t *sm = align1024(smem_raw);
     uint8_t *Cs = sm, *CBs = Cs + 2 * RB, *xs = CBs + NWT * kTile, *Ss = xs + XB;
     float *fbuf = reinterpret_cast<float *>(Ss + 2 * SB);  // [NSC][FST]
-    __shared__ uint64_t bar_res, bar_x, bar_mma;
+    __shared__ uint64_t bar_res, bar_x, bar_s, bar_o, bar_b;
     __shared__ uint32_t s_tmem;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int q4 = warp & 3, hf = warp >> 2;
@@ -519,16 +526,21 @@ __global__ void __launch_bounds__(kThreadsWide, 1) tc_k5_kernel(const Params p, 
         }
         for (int j = tid; j < Q / 64; j += kThreadsWide) f[POFF + j] = f[64 * j + 63];
     };
-    auto issue_head = [&](int h) {
-        const int sidx = (bi * p.n + c) * p.H + h;
-        mbar_arrive_expect_tx(&bar_x, XB + 2 * SB);
+    auto issue_x = [&](int h) {
+        mbar_arrive_expect_tx(&bar_x, XB);
         for (int j = 0; j < NT; ++j) tma_load_4d(xs + j * kTile, &maps.x, &bar_x, 0, h, t0 + 128 * j, bi);
-        for (int rb = 0; rb < 2; ++rb) tma_load_3d(Ss + rb * SB, &maps.st, &bar_x, 64 * rb, 0, sidx);
+    };
+    auto issue_s = [&](int h) {
+        const int sidx = (bi * p.n + c) * p.H + h;
+        mbar_arrive_expect_tx(&bar_s, 2 * SB);
+        for (int rb = 0; rb < 2; ++rb) tma_load_3d(Ss + rb * SB, &maps.st, &bar_s, 64 * rb, 0, sidx);
     };
     if (tid == 0) {
         mbar_init(&bar_res, 1);
         mbar_init(&bar_x, 1);
-        mbar_init(&bar_mma, 1);
+        mbar_init(&bar_s, 1);
+        mbar_init(&bar_o, 1);
+        mbar_init(&bar_b, 1);
         mbar_fence_init();
     }
     if (warp == 0) tmem_alloc(&s_tmem, NCOL);
@@ -543,7 +555,8 @@ __global__ void __launch_bounds__(kThreadsWide, 1) tc_k5_kernel(const Params p, 
         for (int tb = 0; tb < NT; ++tb)
             for (int sb = 0; sb < 2 * (tb + 1); ++sb)
                 tma_load_2d(CBs + (tb * (tb + 1) + sb) * kTile, &maps.cb, &bar_res, 64 * sb, cbrow + 128 * tb);
-        issue_head(h_begin);
+        issue_x(h_begin);
+        issue_s(h_begin);
     }
     fetch(0);
     stash(0);
@@ -552,7 +565,7 @@ __global__ void __launch_bounds__(kThreadsWide, 1) tc_k5_kernel(const Params p, 
         stash(1);
     }
     if (nh > 2) fetch(2);
-    int x_issued = 1, x_landed = 0;
+    int x_issued = 1, x_landed = 0, s_issued = 1, s_landed = 0;
     bool ok = wait_all(&bar_res, 0, true);  // publishes the raw scalars of heads 0 and 1
     if (ok && vrows < Q) {
         zero_rows_from(Cs, Q, vrows);
@@ -569,81 +582,61 @@ __global__ void __launch_bounds__(kThreadsWide, 1) tc_k5_kernel(const Params p, 
     for (int k = 0; k <= nh && ok; ++k) {
         const int h = h_begin + k, cur = k % NSC;
         const float D_k = k < nh ? p.D[h] : 0.f;  // used one iteration later
-        if (k > 0) {
-            // MMAs of head k-1 done: the TMEM W region and the x / s_in buffers are free
-            ok = mbar_wait(&bar_mma, (uint32_t)((k - 1) & 1)) && ok;
-            tc_fence_after();
-            if (k < nh) {
-                if (tid == 0 && ok) issue_head(h);
-                x_issued = k + 1;
+        const float *f = fbuf + cur * FST;
+        const float *cum = f, *dts = f + Q, *piv = f + POFF;
+        const uint32_t *f2 = reinterpret_cast<const uint32_t *>(f);
+        // ---- W_k into TMEM (packed bf16 pairs, lane = t).  Units (t-block tb,
+        // 64-column group sb) of rows t = 128 tb + 32 q4 + lane: every thread gets
+        // one per t-block, exactly one of its three on the diagonal 64-group.
+        auto build = [&](int tb, int sb, uint32_t col) {
+            const int t = tb * 128 + 32 * q4 + lane, tr = t >> 6, row = t - 128 * tb;
+            uint32_t pk[32];
+            if (sb > tr) {
+#pragma unroll
+                for (int j = 0; j < 32; ++j) pk[j] = 0u;
+            } else {
+                const uint32_t cbb = smem_u32(CBs + (tb * (tb + 1) + sb) * kTile);
+                const bool diag = sb == tr;
+                const int u = (t & 63) >> 4, t16 = t & ~15;
+                const float ct = cum[t];
+                // row factor: exp(cumA_t - pivot); on the diagonal group the pivot ends the
+                // sub-blocks left of the row's own (none when u = 0: the table is all 0)
+                const float er = diag ? (u > 0 ? __expf(ct - cum[t16 - 1]) : 0.f) : __expf(ct - piv[sb]);
+                const uint32_t er2 = pack_bf2(er, er);
+                const uint32_t *tab = diag ? f2 + TOFF + 128 * sb + 32 * u : f2 + GOFF + 32 * sb;
+#pragma unroll
+                for (int c8 = 0; c8 < 8; ++c8) {
+                    const uint4 cv = ld_shared_v4(cbb + sw128_chunk(row, c8));
+                    const uint4 gv = *reinterpret_cast<const uint4 *>(tab + 4 * c8);
+                    pk[4 * c8] = bmul2(bmul2(cv.x, gv.x), er2);
+                    pk[4 * c8 + 1] = bmul2(bmul2(cv.y, gv.y), er2);
+                    pk[4 * c8 + 2] = bmul2(bmul2(cv.z, gv.z), er2);
+                    pk[4 * c8 + 3] = bmul2(bmul2(cv.w, gv.w), er2);
+                }
+                if (diag) {  // the row's own 16-wide sub-block: direct exponentials, 0 for s > t
+                    const uint4 c0 = ld_shared_v4(cbb + sw128_chunk(row, 2 * u));
+                    const uint4 c1 = ld_shared_v4(cbb + sw128_chunk(row, 2 * u + 1));
+                    const uint32_t cw[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+                    uint32_t own[8];
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        const int s0 = t16 + 2 * j;
+                        const float w0 = s0 <= t ? bf_lo(cw[j]) * __expf(ct - cum[s0]) * dts[s0] : 0.f;
+                        const float w1 = s0 + 1 <= t ? bf_hi(cw[j]) * __expf(ct - cum[s0 + 1]) * dts[s0 + 1] : 0.f;
+                        own[j] = pack_bf2(w0, w1);
+                    }
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) pk[j] = (j >> 3) == u ? own[j & 7] : pk[j];
+                }
             }
-        }
+            tmem_st32u(tmem_addr(tm, 32 * q4, col + 32 * sb), pk);
+        };
+        const int dq = q4 >> 1;  // the rows' 64-group inside their t-block
         if (k < nh) {
-            const float *f = fbuf + cur * FST;
-            const float *cum = f, *dts = f + Q, *piv = f + POFF;
 #pragma unroll
             for (int tb = 0; tb < NT; ++tb) ep_k[tb] = __expf(cum[tb * 128 + 32 * q4 + lane]);
-            // ---- W_k into TMEM (packed bf16 pairs, lane = t), while x_k / s_in_k land.
-            // Units (t-block tb, 64-column group sb) of rows t = 128 tb + 32 q4 + lane:
-            // every thread gets three, exactly one of them on the diagonal 64-group.
-            const uint32_t *f2 = reinterpret_cast<const uint32_t *>(f);
-            auto build = [&](int tb, int sb) {
-                const int t = tb * 128 + 32 * q4 + lane, tr = t >> 6, row = t - 128 * tb;
-                uint32_t pk[32];
-                if (sb > tr) {
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) pk[j] = 0u;
-                } else {
-                    const uint32_t cbb = smem_u32(CBs + (tb * (tb + 1) + sb) * kTile);
-                    const bool diag = sb == tr;
-                    const int u = (t & 63) >> 4, t16 = t & ~15;
-                    const float ct = cum[t];
-                    // row factor: exp(cumA_t - pivot); on the diagonal group the pivot ends the
-                    // sub-blocks left of the row's own (none when u = 0: the table is all 0)
-                    const float er = diag ? (u > 0 ? __expf(ct - cum[t16 - 1]) : 0.f) : __expf(ct - piv[sb]);
-                    const uint32_t er2 = pack_bf2(er, er);
-                    const uint32_t *tab = diag ? f2 + TOFF + 128 * sb + 32 * u : f2 + GOFF + 32 * sb;
-#pragma unroll
-                    for (int c8 = 0; c8 < 8; ++c8) {
-                        const uint4 cv = ld_shared_v4(cbb + sw128_chunk(row, c8));
-                        const uint4 gv = *reinterpret_cast<const uint4 *>(tab + 4 * c8);
-                        pk[4 * c8] = bmul2(bmul2(cv.x, gv.x), er2);
-                        pk[4 * c8 + 1] = bmul2(bmul2(cv.y, gv.y), er2);
-                        pk[4 * c8 + 2] = bmul2(bmul2(cv.z, gv.z), er2);
-                        pk[4 * c8 + 3] = bmul2(bmul2(cv.w, gv.w), er2);
-                    }
-                    if (diag) {  // the row's own 16-wide sub-block: direct exponentials, 0 for s > t
-                        const uint4 c0 = ld_shared_v4(cbb + sw128_chunk(row, 2 * u));
-                        const uint4 c1 = ld_shared_v4(cbb + sw128_chunk(row, 2 * u + 1));
-                        const uint32_t cw[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
-                        uint32_t own[8];
-#pragma unroll
-                        for (int j = 0; j < 8; ++j) {
-                            const int s0 = t16 + 2 * j;
-                            const float w0 = s0 <= t ? bf_lo(cw[j]) * __expf(ct - cum[s0]) * dts[s0] : 0.f;
-                            const float w1 = s0 + 1 <= t ? bf_hi(cw[j]) * __expf(ct - cum[s0 + 1]) * dts[s0 + 1] : 0.f;
-                            own[j] = pack_bf2(w0, w1);
-                        }
-#pragma unroll
-                        for (int j = 0; j < 32; ++j) pk[j] = (j >> 3) == u ? own[j & 7] : pk[j];
-                    }
-                }
-                tmem_st32u(tmem_addr(tm, 32 * q4, WCOL + 64 * (tb * (tb + 1) / 2) + 32 * sb), pk);
-            };
-            const int dq = q4 >> 1;  // the rows' 64-group inside their t-block
-            if (hf == 0) {
-                build(0, dq);
-                if (NT == 2) {
-                    build(1, 0);
-                    build(1, 1);
-                }
-            } else {
-                build(0, 1 - dq);
-                if (NT == 2) {
-                    build(1, dq == 0 ? 3 : 2);
-                    build(1, 2 + dq);
-                }
-            }
+            // t-block 0 into its spare buffer: the ORANGE MMAs of head k - 2 read it last
+            build(0, hf == 0 ? dq : 1 - dq, W0COL + 64 * (k & 1));
             // prefetch raw scalars of head k + 2, derive those of head k + 1 (raw visible since the last barrier)
             if (k + 2 < nh) {
                 stash((k + 2) % NSC);
@@ -651,8 +644,33 @@ __global__ void __launch_bounds__(kThreadsWide, 1) tc_k5_kernel(const Params p, 
             }
             if (k + 1 < nh) derive((k + 1) % NSC);
         }
+        if (k > 0) {
+            // ORANGE MMAs of head k-1 done: the t-block 1 W region and the x buffer are free
+            ok = mbar_wait(&bar_o, (uint32_t)((k - 1) & 1)) && ok;
+            tc_fence_after();
+            if (k < nh) {
+                if (tid == 0 && ok) issue_x(h);
+                if (ok) x_issued = k + 1;
+            }
+        }
+        if (NT == 2 && k < nh) {
+            if (hf == 0) {
+                build(1, 0, W1COL);
+                build(1, 1, W1COL);
+            } else {
+                build(1, dq == 0 ? 3 : 2, W1COL);
+                build(1, 2 + dq, W1COL);
+            }
+        }
         // ---- epilogue of head k - 1
         if (k > 0) {
+            // BLUE MMAs of head k-1 done: the accumulators are final, the s_in buffer is free
+            ok = mbar_wait(&bar_b, (uint32_t)((k - 1) & 1)) && ok;
+            tc_fence_after();
+            if (k < nh) {
+                if (tid == 32 && ok) issue_s(h);
+                if (ok) s_issued = k + 1;
+            }
             const float Dh = D_ep;
 #pragma unroll
             for (int tb = 0; tb < NT; ++tb) {
@@ -686,6 +704,8 @@ __global__ void __launch_bounds__(kThreadsWide, 1) tc_k5_kernel(const Params p, 
         // ---- x_k landed: keep this thread's D x slices, zero padded rows
         ok = mbar_wait(&bar_x, (uint32_t)(k & 1)) && ok;
         if (ok) x_landed = k + 1;
+        ok = mbar_wait(&bar_s, (uint32_t)(k & 1)) && ok;
+        if (ok) s_landed = k + 1;
 #pragma unroll
         for (int tb = 0; tb < NT; ++tb) {
             const int t = tb * 128 + 32 * q4 + lane;
@@ -697,28 +717,36 @@ __global__ void __launch_bounds__(kThreadsWide, 1) tc_k5_kernel(const Params p, 
             zero_rows_from(xs, Q, vrows);
             fence_async_smem();
         }
-        // ---- one barrier: W_k stored, accumulators of k-1 read, x_k in place
+        // ---- one barrier: W_k stored, accumulators of k-1 read, x_k in place.  The
+        // two issuing threads sit in warps 4 and 5, whose rows carry the fewest
+        // W entries (two of their three units lie above the diagonal when q4 < 2).
         tc_fence_before();
         ok = __syncthreads_and(ok ? 1 : 0) != 0;
         tc_fence_after();
-        if (tid == 0 && ok) {
+        if (tid == 128 && ok) {
             const uint32_t id = idesc_bf16(128, 64, false, true);
-            const uint32_t ib = idesc_bf16(128, 64, false, false);
-            for (int tb = 0; tb < NT; ++tb) {
-                const uint32_t wc = WCOL + 64 * (tb * (tb + 1) / 2);
-                for (int ks = 0; ks < 8 * (tb + 1); ++ks)
-                    mma_bf16_tmem_a(tm + OCOL + tb * 64, tm + wc + 8 * ks, sdesc_mnmajor(smem_u32(xs), ks, XB), id,
+            if (NT == 2)
+                for (int ks = 0; ks < 16; ++ks)
+                    mma_bf16_tmem_a(tm + OCOL + 64, tm + W1COL + 8 * ks, sdesc_mnmajor(smem_u32(xs), ks, XB), id,
                                     ks > 0);
+            for (int ks = 0; ks < 8; ++ks)
+                mma_bf16_tmem_a(tm + OCOL, tm + W0COL + 64 * (k & 1) + 8 * ks, sdesc_mnmajor(smem_u32(xs), ks, XB),
+                                id, ks > 0);
+            mma_commit(&bar_o);
+        }
+        if (tid == 160 && ok) {
+            const uint32_t ib = idesc_bf16(128, 64, false, false);
+            for (int tb = 0; tb < NT; ++tb)
                 for (int ks = 0; ks < kN / 16; ++ks)
                     mma_bf16(tm + BCOL + tb * 64, sdesc_kmajor(smem_u32(Cs + tb * kTile), ks, RB),
                              sdesc_kmajor(smem_u32(Ss), ks, SB), ib, ks > 0);
-            }
-            mma_commit(&bar_mma);
+            mma_commit(&bar_b);
         }
     }
     if (!ok && tid == 0) flag_timeout(p);
     // a load issued for a head that was never waited for has to land before exit
     if (x_issued > x_landed) mbar_wait(&bar_x, (uint32_t)((x_issued - 1) & 1));
+    if (s_issued > s_landed) mbar_wait(&bar_s, (uint32_t)((s_issued - 1) & 1));
     tc_sync();
     if (warp == 0) tmem_dealloc(tm, NCOL);
 }
