@@ -44,7 +44,7 @@ constexpr int kTile = 16384;  // one [128 rows][64] bf16 SW128 tile
 constexpr int kStatusTimeout = 5;
 
 struct TcMaps {
-    CUtensorMap x, dy, B, C, st, dst, cb, cbt, dcb;
+    CUtensorMap x, dy, B, C, st, dst, cb, cbt, dcb, part;
 };
 
 __device__ __forceinline__ uint8_t *align1024(uint8_t *p) {
@@ -2099,20 +2099,44 @@ __global__ void __launch_bounds__(kThreadsWide + 32, 1) tc_bwd_dbc_kernel(const 
     tc_fence_after();
     if (tid < NCONS) {
         if (ok) {
-            for (int tb = 0; tb < NT; ++tb) {
-                const int t = tb * 128 + 32 * q4 + lane;
-                for (int r0 = 64 * hf; r0 < 64 * hf + 64; r0 += 32) {
-                    float v[32];
-                    tmem_ld32(tmem_addr(tm, 32 * q4, tb * 128 + r0), v);
-                    float4 *dC = reinterpret_cast<float4 *>(outC + (size_t)t * kN + r0);
+            // fp32 partials through the (now idle) stage area: 128-row x 32-column
+            // boxes in the 128-byte swizzled layout of the store's tensor map (so
+            // the row-per-thread shared stores do not collide on banks), written
+            // out by TMA, dC first, then dB
+            constexpr int NBOX = NT * 4;  // boxes per output
+            const int row = 32 * q4 + lane;
+            const long long rows_out = (long long)p.b * p.n * p.G * Q;
+            const long long rbase = (((long long)bi * p.n + c) * p.G + g) * Q;
+#pragma unroll 1
+            for (int which = 0; which < 2; ++which) {
+                uint8_t *boxes = sm + (NT == 2 ? 0 : which * NBOX * kTile);
+                if (which == 1 && NT == 2) {  // the dC boxes must have been read out first
+                    if (tid == 0) bulk_wait_read_all();
+                    bar_sync_n(1, NCONS);
+                }
+#pragma unroll 1
+                for (int tb = 0; tb < NT; ++tb)
+#pragma unroll 1
+                    for (int r0 = 64 * hf; r0 < 64 * hf + 64; r0 += 32) {
+                        float v[32];
+                        tmem_ld32(tmem_addr(tm, 32 * q4, (which ? DBCOL : 0) + tb * 128 + r0), v);
+                        const uint32_t bb = smem_u32(boxes + (tb * 4 + r0 / 32) * kTile) + (uint32_t)row * 128u;
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) dC[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
-                    tmem_ld32(tmem_addr(tm, 32 * q4, DBCOL + tb * 128 + r0), v);
-                    float4 *dB = reinterpret_cast<float4 *>(outB + (size_t)t * kN + r0);
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) dB[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+                        for (int c4 = 0; c4 < 8; ++c4)
+                            st_shared_v4(bb + (uint32_t)((c4 ^ (row & 7)) * 16), __float_as_uint(v[4 * c4]),
+                                         __float_as_uint(v[4 * c4 + 1]), __float_as_uint(v[4 * c4 + 2]),
+                                         __float_as_uint(v[4 * c4 + 3]));
+                    }
+                fence_async_smem();
+                bar_sync_n(1, NCONS);
+                if (tid == 0) {
+                    const long long y0 = ((long long)slice * 2 + which) * rows_out + rbase;
+                    for (int bx = 0; bx < NBOX; ++bx)
+                        tma_store_2d(&maps.part, boxes + bx * kTile, 32 * (bx & 3), (int)(y0 + 128 * (bx >> 2)));
+                    bulk_commit();
                 }
             }
+            if (tid == 0) bulk_wait_all();
         } else if (tid == 0) {
             flag_timeout(p);
         }
@@ -2175,11 +2199,11 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 cudaError_t encode(CUtensorMap *m, const void *base, int rank, const cuuint64_t *dims, const cuuint64_t *strides,
-                   const cuuint32_t *box) {
+                   const cuuint32_t *box, CUtensorMapDataType dtype = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) {
     auto fn = encode_fn();
     if (!fn) return cudaErrorNotSupported;
     cuuint32_t es[4] = {1, 1, 1, 1};
-    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank, const_cast<void *>(base), dims, strides,
+    CUresult r = fn(m, dtype, (cuuint32_t)rank, const_cast<void *>(base), dims, strides,
                     box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                     CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
@@ -2223,6 +2247,14 @@ cudaError_t make_maps(const Params &p, TcMaps *mp, bool backward) {
             if ((e = encode(&mp->dcb, p.d_cb_bf, 2, dims, strides, box)) != cudaSuccess) return e;
         }
         if ((e = map_tokens(&mp->dy, p.dy, p.b, p.L, p.H, kP)) != cudaSuccess) return e;
+        if (p.dBC_part) {  // G2 fp32 partials [nslice * 2 * b*n*G*Q rows][N]: boxes of 32 columns x 128 rows
+            cuuint64_t dims[2] = {(cuuint64_t)kN, (cuuint64_t)p.nslice * 2 * p.b * p.n * p.G * p.Q};
+            cuuint64_t strides[1] = {(cuuint64_t)kN * 4};
+            cuuint32_t box[2] = {32, 128};
+            if ((e = encode(&mp->part, p.dBC_part, 2, dims, strides, box, CU_TENSOR_MAP_DATA_TYPE_FLOAT32)) !=
+                cudaSuccess)
+                return e;
+        }
         if (p.dstates_bf && (e = map_states(&mp->dst, p.dstates_bf, (long long)p.b * p.n * p.H)) != cudaSuccess)
             return e;
     }
