@@ -44,7 +44,7 @@ constexpr int kTile = 16384;  // one [128 rows][64] bf16 SW128 tile
 constexpr int kStatusTimeout = 5;
 
 struct TcMaps {
-    CUtensorMap x, dy, B, C, st, dst, cb, cbt, dcb, part;
+    CUtensorMap x, dy, B, C, st, dst, cb, cbt, dcb, part, dx;
 };
 
 __device__ __forceinline__ uint8_t *align1024(uint8_t *p) {
@@ -950,8 +950,11 @@ __global__ void __launch_bounds__(kThreadsWide + 32, 1) tc_bwd_blue_kernel(const
 //   dx       += bbs[s] U[s, p]                        (dx holds the ORANGE and skip terms)
 //   ddt_main += d_bbs exp(cumA_last - cumA)           (the K3 part of ddt)
 //   d_delta   = d_bbs dt exp(cumA_last - cumA),  dcum_main -= d_delta   (the K3 part of d cumA)
-// Runs after the ORANGE kernel; its read-modify-writes are prefetched at the
-// top of each head so the global loads overlap the TMA wait and the MMA.
+// Runs after the ORANGE kernel.  The dx tile of a head (which holds the ORANGE
+// and skip terms) comes in by TMA, is updated in place in shared memory and
+// goes back out by a TMA tile store; the next head's tile is fetched once that
+// store has read the buffer.  The per-token sums are read-modify-written
+// directly (coalesced), prefetched at the top of each head.
 template <int Q>
 __global__ void __launch_bounds__(kThreadsWide, 1) tc_bwd_k3_kernel(const Params p, const __grid_constant__ TcMaps maps) {
     constexpr int NT = Q / 128;
@@ -961,10 +964,10 @@ __global__ void __launch_bounds__(kThreadsWide, 1) tc_bwd_k3_kernel(const Params
     constexpr int NSC = 3;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = align1024(smem_raw);
-    uint8_t *Bs = sm, *stg = Bs + 2 * RB;
-    float *fbuf = reinterpret_cast<float *>(stg + 2 * STG);  // [NSC][3Q]: dts, dec_end, (spare)
+    uint8_t *Bs = sm, *stg = Bs + 2 * RB, *dxs = stg + 2 * STG;
+    float *fbuf = reinterpret_cast<float *>(dxs + XB);  // [NSC][3Q]: dts, dec_end, (spare)
     float *dbbp = fbuf + NSC * 3 * Q;                        // [2][Q]
-    __shared__ uint64_t bar_res, bar_x[2], bar_mma[2];
+    __shared__ uint64_t bar_res, bar_x[2], bar_mma[2], bar_dx;
     __shared__ uint32_t s_tmem;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int q4 = warp & 3, hf = warp >> 2;
@@ -1005,6 +1008,10 @@ __global__ void __launch_bounds__(kThreadsWide, 1) tc_bwd_k3_kernel(const Params
             f[Q + tid] = __expf(r_end - r_cum);
         }
     };
+    auto issue_dx = [&](int k) {  // thread 0: the dx tile of head k
+        mbar_arrive_expect_tx(&bar_dx, XB);
+        for (int j = 0; j < NT; ++j) tma_load_4d(dxs + j * kTile, &maps.dx, &bar_dx, 0, h_begin + k, t0 + 128 * j, bi);
+    };
     auto issue = [&](int k) {
         const int h = h_begin + k, st = k & 1;
         uint8_t *xs = stg + st * STG, *dis = xs + XB;
@@ -1019,6 +1026,7 @@ __global__ void __launch_bounds__(kThreadsWide, 1) tc_bwd_k3_kernel(const Params
         mbar_init(&bar_x[1], 1);
         mbar_init(&bar_mma[0], 1);
         mbar_init(&bar_mma[1], 1);
+        mbar_init(&bar_dx, 1);
         mbar_fence_init();
     }
     if (warp == 0) tmem_alloc(&s_tmem, NCOL);
@@ -1031,6 +1039,7 @@ __global__ void __launch_bounds__(kThreadsWide, 1) tc_bwd_k3_kernel(const Params
                 tma_load_4d(Bs + rb * RB + j * kTile, &maps.B, &bar_res, 64 * rb, g, t0 + 128 * j, bi);
         issue(0);
         if (nh > 1) issue(1);
+        issue_dx(0);
     }
     fetch(0);
     stash(0);
@@ -1039,7 +1048,7 @@ __global__ void __launch_bounds__(kThreadsWide, 1) tc_bwd_k3_kernel(const Params
         stash(1);
     }
     if (nh > 2) fetch(2);
-    int issued = nh > 1 ? 2 : 1, landed = 0;
+    int issued = nh > 1 ? 2 : 1, landed = 0, dx_issued = 1, dx_landed = 0;
     bool ok = wait_all(&bar_res, 0, true);
     if (ok && vrows < Q) {
         zero_rows_from(Bs, Q, vrows);
@@ -1052,17 +1061,12 @@ __global__ void __launch_bounds__(kThreadsWide, 1) tc_bwd_k3_kernel(const Params
         const float *f = fbuf + (k % NSC) * 3 * Q;
         const float *dts = f, *dec = f + Q;
         const size_t cbase = ix_chunk(p, bi, h, c) * Q;
-        // prefetch this head's read-modify-write operands (dx rows, per-token sums)
-        uint4 dxr[NT][4];
-#pragma unroll
-        for (int mb = 0; mb < NT; ++mb) {
-            const int s = mb * 128 + 32 * q4 + lane;
-            if (t0 + s < p.L && s < vrows) {
-                const uint4 *src = reinterpret_cast<const uint4 *>(DX + ix_x(p, bi, t0 + s, h, 32 * hf));
-#pragma unroll
-                for (int c8 = 0; c8 < 4; ++c8) dxr[mb][c8] = src[c8];
-            }
+        if (tid == 0 && k > 0) {  // the store of head k - 1's tile has read the buffer: fetch head k's
+            bulk_wait_read_all();
+            issue_dx(k);
         }
+        if (k > 0) dx_issued = k + 1;
+        // prefetch this head's per-token sums
         float ddt_pre[(Q + kThreadsWide - 1) / kThreadsWide], dcum_pre[(Q + kThreadsWide - 1) / kThreadsWide];
 #pragma unroll
         for (int i = 0; i < (Q + kThreadsWide - 1) / kThreadsWide; ++i) {
@@ -1098,6 +1102,8 @@ __global__ void __launch_bounds__(kThreadsWide, 1) tc_bwd_k3_kernel(const Params
         }
         ok = mbar_wait(&bar_mma[st], (uint32_t)((k >> 1) & 1)) && ok;
         tc_fence_after();
+        ok = mbar_wait(&bar_dx, (uint32_t)(k & 1)) && ok;
+        if (ok) dx_landed = k + 1;
         for (int mb = 0; mb < NT; ++mb) {
             const int s = mb * 128 + 32 * q4 + lane;
             float u[32];
@@ -1112,23 +1118,30 @@ __global__ void __launch_bounds__(kThreadsWide, 1) tc_bwd_k3_kernel(const Params
                         bf_lo(xv.z) * uu[4] + bf_hi(xv.z) * uu[5] + bf_lo(xv.w) * uu[6] + bf_hi(xv.w) * uu[7];
             }
             dbbp[hf * Q + s] = part;
-            if (t0 + s < p.L && s < vrows) {
+            if (s < vrows) {  // rows past valid_len keep the ORANGE kernel's zeros
                 const float bbs = dts[s] * dec[s];
+                const uint32_t db = smem_u32(dxs + mb * kTile);
+                const int row = s & 127;
 #pragma unroll
                 for (int c8 = 0; c8 < 4; ++c8) {
-                    const uint4 pv = dxr[mb][c8];
-                    float *a = u + 8 * c8;
-                    a[0] = a[0] * bbs + bf_lo(pv.x); a[1] = a[1] * bbs + bf_hi(pv.x);
-                    a[2] = a[2] * bbs + bf_lo(pv.y); a[3] = a[3] * bbs + bf_hi(pv.y);
-                    a[4] = a[4] * bbs + bf_lo(pv.z); a[5] = a[5] * bbs + bf_hi(pv.z);
-                    a[6] = a[6] * bbs + bf_lo(pv.w); a[7] = a[7] * bbs + bf_hi(pv.w);
+                    const uint32_t ad = db + sw128_chunk(row, 4 * hf + c8);
+                    const uint4 pv = ld_shared_v4(ad);
+                    const float *a = u + 8 * c8;
+                    st_shared_v4(ad, pack_bf2(a[0] * bbs + bf_lo(pv.x), a[1] * bbs + bf_hi(pv.x)),
+                                 pack_bf2(a[2] * bbs + bf_lo(pv.y), a[3] * bbs + bf_hi(pv.y)),
+                                 pack_bf2(a[4] * bbs + bf_lo(pv.z), a[5] * bbs + bf_hi(pv.z)),
+                                 pack_bf2(a[6] * bbs + bf_lo(pv.w), a[7] * bbs + bf_hi(pv.w)));
                 }
-                store_row32_bf16(DX + ix_x(p, bi, t0 + s, h, 32 * hf), u);
             }
         }
+        fence_async_smem();
         tc_fence_before();
         ok = __syncthreads_and(ok ? 1 : 0) != 0;  // d_bbs halves complete; stage st no longer read
         tc_fence_after();
+        if (tid == 0 && ok) {  // the updated dx tile goes out (rows past the sequence end are clipped)
+            for (int j = 0; j < NT; ++j) tma_store_4d(&maps.dx, dxs + j * kTile, 0, h, t0 + 128 * j, bi);
+            bulk_commit();
+        }
         if (tid == 0 && k + 2 < nh) issue(k + 2);
         if (k + 2 < nh) issued = k + 3;
 #pragma unroll
@@ -1146,6 +1159,8 @@ __global__ void __launch_bounds__(kThreadsWide, 1) tc_bwd_k3_kernel(const Params
     if (!ok && tid == 0) flag_timeout(p);
     // loads issued for heads that were never waited for have to land before exit
     for (int k = landed; k < issued; ++k) mbar_wait(&bar_x[k & 1], (uint32_t)((k >> 1) & 1));
+    if (dx_issued > dx_landed) mbar_wait(&bar_dx, (uint32_t)((dx_issued - 1) & 1));
+    if (tid == 0) bulk_wait_all();
     tc_sync();
     if (warp == 0) tmem_dealloc(tm, NCOL);
 }
@@ -2247,6 +2262,7 @@ cudaError_t make_maps(const Params &p, TcMaps *mp, bool backward) {
             if ((e = encode(&mp->dcb, p.d_cb_bf, 2, dims, strides, box)) != cudaSuccess) return e;
         }
         if ((e = map_tokens(&mp->dy, p.dy, p.b, p.L, p.H, kP)) != cudaSuccess) return e;
+        if (p.dx && (e = map_tokens(&mp->dx, p.dx, p.b, p.L, p.H, kP)) != cudaSuccess) return e;
         if (p.dBC_part) {  // G2 fp32 partials [nslice * 2 * b*n*G*Q rows][N]: boxes of 32 columns x 128 rows
             cuuint64_t dims[2] = {(cuuint64_t)kN, (cuuint64_t)p.nslice * 2 * p.b * p.n * p.G * p.Q};
             cuuint64_t strides[1] = {(cuuint64_t)kN * 4};
@@ -2279,7 +2295,7 @@ constexpr size_t smem_k5(int Q) {
 }
 constexpr size_t smem_blue(int Q) { return 1024 + 2 * (size_t)Q * 128 + 3 * ((size_t)Q * 128 + 2 * 64 * 128); }
 constexpr size_t smem_k3bwd(int Q) {
-    return 1024 + 2 * (size_t)Q * 128 + 2 * ((size_t)Q * 128 + 2 * 64 * 128) + 4 * (3 * 3 * Q + 2 * Q);
+    return 1024 + 2 * (size_t)Q * 128 + 2 * ((size_t)Q * 128 + 2 * 64 * 128) + (size_t)Q * 128 + 4 * (3 * 3 * Q + 2 * Q);
 }
 // Padded above half of the SM's shared memory: a CTA holding 512 TMEM columns
 // must never share its SM with another CTA of the same kernel.
