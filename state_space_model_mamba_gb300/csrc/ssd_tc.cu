@@ -1167,8 +1167,10 @@ __global__ void __launch_bounds__(kThreadsWide, 1) tc_bwd_k3_kernel(const Params
 
 // ====================================================================== ORANGE backward
 // CTA per (b, chunk, group, head slice), 256 threads, looping over the slice's
-// heads; thread 0 refills the CB^T copy and x as soon as the previous head's
-// MMAs complete (every thread waits for them anyway), dy two heads ahead.  The ORANGE block of the backward is
+// heads; thread 0 refills x as soon as the previous head's MMAs complete
+// (every thread waits for them anyway), dy a head ahead.  A head's dx rows are
+// staged in its dy buffer once the epilogue has read dy, and leave by TMA tile
+// stores at the next head's first barrier.  The ORANGE block of the backward is
 // restated so that every reduction becomes a per-row dot product of two MMA
 // outputs (thread = row of the chunk):
 //   M^T[s, t]   = CB^T[s, t] exp(cumA_t - cumA_s)   (t >= s, 0 above): built per
@@ -1204,7 +1206,7 @@ __global__ void __launch_bounds__(kThreadsWide, 1) tc_bwd_orange_kernel(const Pa
     uint8_t *sm = align1024(smem_raw);
     uint8_t *Mt = sm, *xs = Mt + NCBT * kTile, *dys = xs + XB;  // dys: 2 buffers
     float *fbuf = reinterpret_cast<float *>(dys + 2 * XB);       // [NSC][FST]
-    __shared__ uint64_t bar_cb, bar_x, bar_dy[2], bar_mma;
+    __shared__ uint64_t bar_cb, bar_x, bar_dy[2], bar_a, bar_mma;
     __shared__ uint32_t s_tmem;
     __shared__ int s_x_issued, s_dy_issued, s_landed;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -1242,6 +1244,7 @@ __global__ void __launch_bounds__(kThreadsWide, 1) tc_bwd_orange_kernel(const Pa
         mbar_init(&bar_x, 1);
         mbar_init(&bar_dy[0], 1);
         mbar_init(&bar_dy[1], 1);
+        mbar_init(&bar_a, 1);
         mbar_init(&bar_mma, 1);
         mbar_fence_init();
         s_x_issued = 0;
@@ -1446,7 +1449,11 @@ __global__ void __launch_bounds__(kThreadsWide, 1) tc_bwd_orange_kernel(const Pa
             }
             if (tid == 0) {
                 s_landed = k + 1;
-                if (k + 1 < nh) issue_dy(k + 1);  // its buffer was last read by head k - 1's epilogue
+                if (k > 0) {  // head k - 1's dx, staged in dy buffer (k - 1) & 1 by its epilogue
+                    for (int j = 0; j < NT; ++j)
+                        tma_store_4d(&maps.dx, dys + (db ^ 1) * XB + j * kTile, 0, h - 1, t0 + 128 * j, bi);
+                    bulk_commit();
+                }
             }
             if (NT == 2 && tid == 192) {  // warp 6's phase-B units are the lightest
                 // dx'[1] = M^T[s-block 1] dy[t >= 128];  yo[1] = (s-block 1 part)
@@ -1457,6 +1464,7 @@ __global__ void __launch_bounds__(kThreadsWide, 1) tc_bwd_orange_kernel(const Pa
                 for (int ks = 0; ks < 8; ++ks)
                     mma_bf16(tm + 128 + 64, sdesc_mnmajor(smem_u32(tile_of(1, 2)), ks, kTile),
                              sdesc_mnmajor(smem_u32(xs) + 128 * 128, ks, XB), ib, ks > 0);
+                mma_commit(&bar_a);
             }
             if (k + 2 < nh) {  // buffer (k + 2) % NSC was last read by head k - 1
                 stash(k + 2);
@@ -1480,10 +1488,14 @@ __global__ void __launch_bounds__(kThreadsWide, 1) tc_bwd_orange_kernel(const Pa
                         mma_bf16(tm + 128 + 64 * tb, sdesc_mnmajor(smem_u32(tile_of(0, 2 * tb)), ks, kTile),
                                  sdesc_mnmajor(smem_u32(xs), ks, XB), ib, tb == 1 || ks > 0);
                 mma_commit(&bar_mma);
+                // the store of head k - 1's dx has read its buffer: dy of head k + 1 goes there
+                if (k > 0) bulk_wait_read_all();
+                if (k + 1 < nh) issue_dy(k + 1);
             }
             if (k + 1 < nh) derive(k + 1);  // while the MMAs run (raw scalars visible since barrier 1)
             // ---- epilogue of head k (row i)
             okk = mbar_wait(&bar_mma, (uint32_t)(k & 1));
+            if (NT == 2) okk = mbar_wait(&bar_a, (uint32_t)(k & 1)) && okk;  // dy may now be overwritten
             tc_fence_after();
             if (!okk) ok = false;
             if (tid == 0 && okk && k + 1 < nh) issue_x(k + 1);  // x is free once the MMAs are done
@@ -1520,11 +1532,11 @@ __global__ void __launch_bounds__(kThreadsWide, 1) tc_bwd_orange_kernel(const Pa
                             o[4 * c8 + j] = valid ? pack_bf2(o2.x, o2.y) : 0u;
                         }
                     }
-                    if (t0 + i < p.L) {
-                        uint4 *dst = reinterpret_cast<uint4 *>(DX + ix_x(p, bi, t0 + i, h, 32 * hh));
+                    // dx row i over dy row i (read into registers above, by this thread only)
 #pragma unroll
-                        for (int c = 0; c < 4; ++c) dst[c] = make_uint4(o[4 * c], o[4 * c + 1], o[4 * c + 2], o[4 * c + 3]);
-                    }
+                    for (int c4 = 0; c4 < 4; ++c4)
+                        st_shared_v4(yb + sw128_chunk(i, 4 * hh + c4), o[4 * c4], o[4 * c4 + 1], o[4 * c4 + 2],
+                                     o[4 * c4 + 3]);
                 }
 #pragma unroll
                 for (int hh = 0; hh < 2; ++hh) {
@@ -1543,6 +1555,7 @@ __global__ void __launch_bounds__(kThreadsWide, 1) tc_bwd_orange_kernel(const Pa
                 p.ddt_main[cbase + i] = valid ? ddo2.x + ddo2.y : 0.f;  // the K3 backward adds its terms
                 p.dcum_main[cbase + i] = valid ? (tgt2.x + tgt2.y) - (src2.x + src2.y) : 0.f;
             }
+            fence_async_smem();  // the staged dx rows are read by the next head's TMA store
             float dd = dd2.x + dd2.y;
             dd = warp_sum(dd);
             if (lane == 0) p.dD_part[(((size_t)bi * p.n + c) * p.H + h) * p.dD_per + warp] = dd;
@@ -1552,6 +1565,12 @@ __global__ void __launch_bounds__(kThreadsWide, 1) tc_bwd_orange_kernel(const Pa
     ok = __syncthreads_and(ok ? 1 : 0) != 0;
     tc_fence_after();
     if (!ok && tid == 0) flag_timeout(p);
+    if (ok && tid == 0) {  // the last head's dx
+        for (int j = 0; j < NT; ++j)
+            tma_store_4d(&maps.dx, dys + ((nh - 1) & 1) * XB + j * kTile, 0, h_begin + nh - 1, t0 + 128 * j, bi);
+        bulk_commit();
+    }
+    if (tid == 0) bulk_wait_all();
     // loads issued for heads that were never consumed have to land before exit
     if (tid == 0) {
         mbar_wait(&bar_cb, 0);  // landed long ago unless the kernel gave up early
