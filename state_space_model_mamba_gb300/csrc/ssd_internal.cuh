@@ -131,7 +131,8 @@ template <typename T> cudaError_t launch_simt_bwd_group(const Params &p, cudaStr
 
 // Geometry constants of the CUDA-core kernels that size workspace buffers.
 constexpr int kK4Threads = 128;             // threads per block of the state-passing kernels
-constexpr int kK4Vec = 16;                  // state entries per thread of the state-passing kernels
+constexpr int kK4Vec = 16;                   // state entries per thread of the state-passing kernels
+constexpr int kMaxQ = 256;                   // largest supported chunk length
 constexpr int kMainRows = 16;               // source rows per block of the backward main kernel
 
 }  // namespace ssd

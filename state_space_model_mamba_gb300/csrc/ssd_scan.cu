@@ -12,9 +12,11 @@ namespace ssd {
 
 // ------------------------------------------------------------------ K1 forward
 // One warp per (b, h, chunk): inclusive warp-shuffle scan of dt*A over the
-// chunk's Q tokens, 32 at a time with a running carry.  Tokens at or past the
-// sample's valid length contribute dt = 0.  (The grid has b*H*n*32 >= n_count
-// threads, so the counter clear needs no extra launch.)
+// chunk's Q tokens, 32 at a time with a running carry.  All of the warp's loads
+// are issued before the first scan step (Q <= 256: at most 8 per lane), so
+// their latencies overlap.  Tokens at or past the sample's valid length
+// contribute dt = 0.  (The grid has b*H*n*32 >= n_count threads, so the
+// counter clear needs no extra launch.)
 __global__ void k1_chunk_cumsum(Params p) {
     const size_t gid = blockIdx.x * (size_t)blockDim.x + threadIdx.x;
     // the backward's first kernel also clears the d_cb arrival counters
@@ -27,18 +29,25 @@ __global__ void k1_chunk_cumsum(Params p) {
     const float Ah = p.A[h];
     const float *dtrow = p.dt + ix_dt(p, bi, h, 0);
     float *out = p.cumA + (size_t)warp * p.Q;
+    float v[kMaxQ / 32];
+#pragma unroll
+    for (int sg = 0; sg < kMaxQ / 32; ++sg) {
+        const int q = sg * 32 + lane, t = c * p.Q + q;
+        v[sg] = (q < p.Q && t < V) ? dtrow[t] * Ah : 0.f;
+    }
     float carry = 0.f;
-    for (int q0 = 0; q0 < p.Q; q0 += 32) {
-        const int q = q0 + lane, t = c * p.Q + q;
-        float v = (q < p.Q && t < V) ? dtrow[t] * Ah : 0.f;
+#pragma unroll
+    for (int sg = 0; sg < kMaxQ / 32; ++sg) {
+        if (sg * 32 >= p.Q) break;
+        float u = v[sg];
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
-            const float u = __shfl_up_sync(0xffffffffu, v, o);
-            if (lane >= o) v += u;
+            const float w = __shfl_up_sync(0xffffffffu, u, o);
+            if (lane >= o) u += w;
         }
-        v += carry;
-        if (q < p.Q) out[q] = v;
-        carry = __shfl_sync(0xffffffffu, v, 31);
+        u += carry;
+        if (sg * 32 + lane < p.Q) out[sg * 32 + lane] = u;
+        carry = __shfl_sync(0xffffffffu, u, 31);
     }
     if (lane == 0) p.endA[warp] = carry;
 }
@@ -268,34 +277,43 @@ __global__ void bwd_k1_chunk_cumsum(Params p) {
     const int V = valid_len_of(p, bi);
     const float Ah = p.A[h];
     const size_t base = (size_t)warp * p.Q;
-    // chunk-end terms
+    constexpr int NS = kMaxQ / 32;
+    // every load of the warp first (at most 8 tokens per lane), then the scans
+    float v[NS], dtt[NS], ddm[NS];
     float endterm = 0.f;
+#pragma unroll
+    for (int sg = 0; sg < NS; ++sg) {
+        const int q = sg * 32 + lane, t = c * p.Q + q;
+        const bool in = q < p.Q;
+        v[sg] = in ? p.dcum_blue[base + q] + p.dcum_main[base + q] : 0.f;
+        endterm += in ? p.d_delta[base + q] : 0.f;
+        const bool valid = in && t < V;
+        dtt[sg] = valid ? p.dt[ix_dt(p, bi, h, t)] : 0.f;
+        ddm[sg] = valid ? p.ddt_main[base + q] : 0.f;
+    }
+    // chunk-end terms: the K4 partials and the K3 sum of d_delta
     for (int k = lane; k < p.k4_nblk; k += 32) endterm += p.d_endA_part[(size_t)warp * p.k4_nblk + k];
-    for (int q = lane; q < p.Q; q += 32) endterm += p.d_delta[base + q];
     endterm = warp_sum(endterm);
     float carry = 0.f, dA_acc = 0.f;
-    const int nseg = (p.Q + 31) / 32;
-    for (int sg = nseg - 1; sg >= 0; --sg) {
+#pragma unroll
+    for (int sg = NS - 1; sg >= 0; --sg) {
+        if (sg * 32 >= p.Q) continue;
         const int q = sg * 32 + lane;
-        float v = 0.f;
-        if (q < p.Q) {
-            v = p.dcum_blue[base + q] + p.dcum_main[base + q];
-            if (q == p.Q - 1) v += endterm;
-        }
+        float u = v[sg];
+        if (q == p.Q - 1) u += endterm;
         // inclusive suffix scan within the 32 lanes
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
-            const float u = __shfl_down_sync(0xffffffffu, v, o);
-            if (lane + o < 32) v += u;
+            const float w = __shfl_down_sync(0xffffffffu, u, o);
+            if (lane + o < 32) u += w;
         }
-        v += carry;
-        carry = __shfl_sync(0xffffffffu, v, 0);
+        u += carry;
+        carry = __shfl_sync(0xffffffffu, u, 0);
         const int t = c * p.Q + q;
         if (q < p.Q && t < p.L) {
             const bool valid = t < V;
-            const float dtt = valid ? p.dt[ix_dt(p, bi, h, t)] : 0.f;
-            p.ddt[ix_dt(p, bi, h, t)] = valid ? p.ddt_main[base + q] + v * Ah : 0.f;
-            dA_acc += v * dtt;
+            p.ddt[ix_dt(p, bi, h, t)] = valid ? ddm[sg] + u * Ah : 0.f;
+            dA_acc += u * dtt[sg];
         }
     }
     dA_acc = warp_sum(dA_acc);
