@@ -44,7 +44,7 @@ constexpr int kTile = 16384;  // one [128 rows][64] bf16 SW128 tile
 constexpr int kStatusTimeout = 5;
 
 struct TcMaps {
-    CUtensorMap x, dy, B, C, st, dst, cb, cbt, dcb, part, dx;
+    CUtensorMap x, dy, B, C, st, dst, cb, cbt, dcb, part, dx, y;
 };
 
 __device__ __forceinline__ uint8_t *align1024(uint8_t *p) {
@@ -430,10 +430,11 @@ __global__ void __launch_bounds__(kThreadsWide + 32, 1) tc_k3_kernel(const Param
 // tiles stay resident in shared memory.  One thread issues the ORANGE MMAs and
 // another the BLUE MMAs of a head, each committing to its own mbarrier.  W of
 // t-block 0 has two TMEM buffers, so the next head's t-block-0 units (and its
-// scalar tables) are built while this head's ORANGE MMAs run; its t-block-1
-// units follow once they complete, while the BLUE MMAs may still run.  x is
-// refilled by TMA as soon as the ORANGE MMAs complete, s_in once the BLUE ones
-// do.  Per-head scalars are prefetched two heads ahead.  Per 128-row t-block tb:
+// scalar tables) are built while this head's ORANGE MMAs run.  Once both MMA
+// groups of the previous head are done its epilogue runs, writing y into the
+// (now dead) x buffer, from which a TMA tile store takes it; x and s_in of this
+// head are then fetched and land while its t-block-1 units are built.
+// Per-head scalars are prefetched two heads ahead.  Per 128-row t-block tb:
 //   ORANGE (TMEM cols tb*64):        W[tb] (A operand in TMEM) x  (x MN-major)
 //   BLUE   (TMEM cols NT*64+tb*64):  C[tb] (K-major)            s_in (K-major)
 // y = ORANGE + exp(cumA_t) * BLUE + D x, W[t, s] = CB[t, s] exp(cumA_t - cumA_s) dt_s
@@ -645,13 +646,53 @@ __global__ void __launch_bounds__(kThreadsWide, 1) tc_k5_kernel(const Params p, 
             if (k + 1 < nh) derive((k + 1) % NSC);
         }
         if (k > 0) {
-            // ORANGE MMAs of head k-1 done: the t-block 1 W region and the x buffer are free
+            // both MMA groups of head k-1 done: W of t-block 1, x, s_in and the accumulators are free
             ok = mbar_wait(&bar_o, (uint32_t)((k - 1) & 1)) && ok;
+            ok = mbar_wait(&bar_b, (uint32_t)((k - 1) & 1)) && ok;
             tc_fence_after();
-            if (k < nh) {
-                if (tid == 0 && ok) issue_x(h);
-                if (ok) x_issued = k + 1;
+            // ---- epilogue of head k - 1: y rows into the x buffer
+            const float Dh = D_ep;
+#pragma unroll
+            for (int tb = 0; tb < NT; ++tb) {
+                const int t = tb * 128 + 32 * q4 + lane;
+                float o[32], bl[32];
+                tmem_ld32(tmem_addr(tm, 32 * q4, OCOL + tb * 64 + hf * 32), o);
+                tmem_ld32(tmem_addr(tm, 32 * q4, BCOL + tb * 64 + hf * 32), bl);
+                const float e = ep_ep[tb];
+                const bool valid = t < vrows;
+                const uint32_t yb = smem_u32(xs);
+#pragma unroll
+                for (int c8 = 0; c8 < 4; ++c8) {
+                    const uint4 u = xr[tb][c8];
+                    const uint32_t xw[4] = {u.x, u.y, u.z, u.w};
+                    uint32_t yw[4];
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const float y0 = o[8 * c8 + 2 * j] + e * bl[8 * c8 + 2 * j] + Dh * bf_lo(xw[j]);
+                        const float y1 = o[8 * c8 + 2 * j + 1] + e * bl[8 * c8 + 2 * j + 1] + Dh * bf_hi(xw[j]);
+                        yw[j] = valid ? pack_bf2(y0, y1) : 0u;
+                    }
+                    st_shared_v4(yb + sw128_chunk(t, 4 * hf + c8), yw[0], yw[1], yw[2], yw[3]);
+                }
             }
+            fence_async_smem();
+            tc_fence_before();
+            ok = __syncthreads_and(ok ? 1 : 0) != 0;
+            tc_fence_after();
+            if (tid == 0 && ok) {  // y of head k - 1 out (rows past the sequence end are clipped); x of head k in
+                for (int j = 0; j < NT; ++j) tma_store_4d(&maps.y, xs + j * kTile, 0, h - 1, t0 + 128 * j, bi);
+                bulk_commit();
+                if (k < nh) {
+                    bulk_wait_read_all();
+                    issue_x(h);
+                }
+            }
+            if (tid == 32 && ok && k < nh) issue_s(h);
+            if (ok && k < nh) {
+                x_issued = k + 1;
+                s_issued = k + 1;
+            }
+            if (!ok) break;
         }
         if (NT == 2 && k < nh) {
             if (hf == 0) {
@@ -660,41 +701,6 @@ __global__ void __launch_bounds__(kThreadsWide, 1) tc_k5_kernel(const Params p, 
             } else {
                 build(1, dq == 0 ? 3 : 2, W1COL);
                 build(1, 2 + dq, W1COL);
-            }
-        }
-        // ---- epilogue of head k - 1
-        if (k > 0) {
-            // BLUE MMAs of head k-1 done: the accumulators are final, the s_in buffer is free
-            ok = mbar_wait(&bar_b, (uint32_t)((k - 1) & 1)) && ok;
-            tc_fence_after();
-            if (k < nh) {
-                if (tid == 32 && ok) issue_s(h);
-                if (ok) s_issued = k + 1;
-            }
-            const float Dh = D_ep;
-#pragma unroll
-            for (int tb = 0; tb < NT; ++tb) {
-                const int t = tb * 128 + 32 * q4 + lane;
-                float o[32], bl[32];
-                tmem_ld32(tmem_addr(tm, 32 * q4, OCOL + tb * 64 + hf * 32), o);
-                tmem_ld32(tmem_addr(tm, 32 * q4, BCOL + tb * 64 + hf * 32), bl);
-                if (t0 + t < p.L) {
-                    if (t < vrows) {
-                        const float e = ep_ep[tb];
-#pragma unroll
-                        for (int c8 = 0; c8 < 4; ++c8) {
-                            const uint4 u = xr[tb][c8];
-                            const float xv[8] = {bf_lo(u.x), bf_hi(u.x), bf_lo(u.y), bf_hi(u.y),
-                                                 bf_lo(u.z), bf_hi(u.z), bf_lo(u.w), bf_hi(u.w)};
-#pragma unroll
-                            for (int j = 0; j < 8; ++j) o[8 * c8 + j] += e * bl[8 * c8 + j] + Dh * xv[j];
-                        }
-                    } else {
-#pragma unroll
-                        for (int j = 0; j < 32; ++j) o[j] = 0.f;
-                    }
-                    store_row32_bf16(Y + ix_x(p, bi, t0 + t, h - 1, 32 * hf), o);
-                }
             }
         }
         if (k == nh) break;
@@ -747,6 +753,7 @@ __global__ void __launch_bounds__(kThreadsWide, 1) tc_k5_kernel(const Params p, 
     // a load issued for a head that was never waited for has to land before exit
     if (x_issued > x_landed) mbar_wait(&bar_x, (uint32_t)((x_issued - 1) & 1));
     if (s_issued > s_landed) mbar_wait(&bar_s, (uint32_t)((s_issued - 1) & 1));
+    if (tid == 0) bulk_wait_all();
     tc_sync();
     if (warp == 0) tmem_dealloc(tm, NCOL);
 }
@@ -2266,6 +2273,7 @@ cudaError_t make_maps(const Params &p, TcMaps *mp, bool backward) {
     if ((e = map_tokens(&mp->B, p.B, p.b, p.L, p.G, kN)) != cudaSuccess) return e;
     if ((e = map_tokens(&mp->C, p.C, p.b, p.L, p.G, kN)) != cudaSuccess) return e;
     if (p.states_bf && (e = map_states(&mp->st, p.states_bf, (long long)p.b * p.n * p.H)) != cudaSuccess) return e;
+    if (!backward && p.y && (e = map_tokens(&mp->y, p.y, p.b, p.L, p.H, kP)) != cudaSuccess) return e;
     if (p.CBh) {  // CB and CB^T, bf16 [b*n*G*Q rows][Q]: boxes of 64 columns x 128 rows
         cuuint64_t dims[2] = {(cuuint64_t)p.Q, (cuuint64_t)p.b * p.n * p.G * p.Q};
         cuuint64_t strides[1] = {(cuuint64_t)p.Q * 2};
