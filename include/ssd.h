@@ -134,11 +134,17 @@ ssd_status ssd_workspace_status(const void *workspace, size_t workspace_bytes, v
  * silently when the array is full.  ssd_profile_end deactivates it and
  * returns how many events were recorded (2 per kernel); ssd_profile_name(i)
  * names the i-th recorded kernel (i < 4096).  Timing events add no device
- * work besides the records themselves. */
+ * work besides the records themselves.
+ *
+ * ssd_profile_only: restricts the recording to kernels whose name (as
+ * ssd_profile_name reports it) equals `name`; NULL or "" records every
+ * kernel again.  The string is copied (at most 63 characters).  Applies to
+ * the calling host thread until changed. */
 int ssd_last_launch_count(void);
 ssd_status ssd_profile_begin(void **events, int capacity);
 int ssd_profile_end(void);
 const char *ssd_profile_name(int i);
+void ssd_profile_only(const char *name);
 
 /* ---- Forward without any device allocation (no counterpart on the pages) ----
  *

@@ -37,10 +37,12 @@ struct Recorder {
     const char *names[4096];
 };
 thread_local Recorder g_rec;
+thread_local char g_rec_only[64] = "";  // record only this kernel ("" = all)
 
 cudaError_t mark_start(const char *name, cudaStream_t s) {
     ++g_launches;
     if (!g_rec.ev || g_rec.n + 2 > g_rec.cap) return cudaSuccess;
+    if (g_rec_only[0] && strcmp(name, g_rec_only) != 0) return cudaSuccess;
     g_rec.names[(g_rec.n / 2) % 4096] = name;
     return cudaEventRecord(g_rec.ev[g_rec.n++], s);
 }
@@ -408,6 +410,10 @@ int ssd_profile_end(void) {
     g_rec.ev = nullptr;
     g_rec.cap = 0;
     return n;
+}
+
+void ssd_profile_only(const char *name) {
+    snprintf(g_rec_only, sizeof(g_rec_only), "%s", name ? name : "");
 }
 
 const char *ssd_profile_name(int i) {

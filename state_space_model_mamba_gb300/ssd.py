@@ -25,7 +25,8 @@ STATUS = {0: "SSD_OK", 1: "SSD_ERR_INVALID_ARG", 2: "SSD_ERR_UNSUPPORTED",
           3: "SSD_ERR_WORKSPACE", 4: "SSD_ERR_CUDA", 5: "SSD_ERR_TIMEOUT"}
 EXPORTED = ("ssd_supported", "ssd_workspace_bytes", "ssd_forward", "ssd_backward",
             "ssd_workspace_status", "ssd_status_str", "ssd_last_error", "ssd_version",
-            "ssd_last_launch_count", "ssd_profile_begin", "ssd_profile_end", "ssd_profile_name")
+            "ssd_last_launch_count", "ssd_profile_begin", "ssd_profile_end", "ssd_profile_name",
+            "ssd_profile_only")
 
 
 class SsdDims(ctypes.Structure):
@@ -80,6 +81,8 @@ def load_library(path: str | None = None):
         lib.ssd_profile_end.restype = i32
         lib.ssd_profile_name.argtypes = [i32]
         lib.ssd_profile_name.restype = ctypes.c_char_p
+        lib.ssd_profile_only.argtypes = [ctypes.c_char_p]
+        lib.ssd_profile_only.restype = None
         if path is None:
             _lib = lib
         return lib
@@ -239,7 +242,8 @@ class KernelTimer:
     active (on the launching stream).  ``durations()`` returns a list of
     (kernel name, milliseconds) in launch order after a synchronize."""
 
-    def __init__(self, capacity_kernels: int):
+    def __init__(self, capacity_kernels: int, only: str | None = None):
+        self.only = only  # record only the kernel of this name (None: every kernel)
         self.events = [torch.cuda.Event(enable_timing=True) for _ in range(2 * capacity_kernels)]
         for e in self.events:
             e.record()  # materialise the underlying cudaEvent_t
@@ -248,11 +252,15 @@ class KernelTimer:
         self.n = 0
 
     def __enter__(self):
-        _check(load_library().ssd_profile_begin(self._arr, len(self.events)))
+        lib = load_library()
+        lib.ssd_profile_only(self.only.encode() if self.only else None)
+        _check(lib.ssd_profile_begin(self._arr, len(self.events)))
         return self
 
     def __exit__(self, *exc):
-        self.n = int(load_library().ssd_profile_end())
+        lib = load_library()
+        self.n = int(lib.ssd_profile_end())
+        lib.ssd_profile_only(None)
         return False
 
     def names(self, count: int) -> list:
@@ -267,7 +275,9 @@ class KernelTimer:
         names = self.names(k)
         out = []
         for i in range(k):
-            if pattern:
+            if self.only:
+                nm = self.only
+            elif pattern:
                 nm = pattern[i % len(pattern)]
             else:
                 nm = names[i] if i < len(names) else ""
