@@ -759,15 +759,17 @@ __global__ void __launch_bounds__(kThreadsWide, 1) tc_k5_kernel(const Params p, 
 }
 
 // ====================================================================== BLUE backward
-// CTA per (b, chunk, group, head slice): 8 consumer warps and one TMA producer
+// CTA per (b, chunk, group, head slice): 8 consumer warps and one producer
 // warp; C stays resident, (dy, s_in) stream through a ring of NST stages.  Per head
 //   d_ch[l, p]     = dy[l, p] exp(cumA_l)   (row l scaled in place by consumer thread l,
 //                                            which keeps it in registers for the dot below)
 //   d_s_in[r, p]   = sum_l C[l, r] d_ch[l, p]   (A = C MN-major, B = d_ch MN-major)
 //   u[l, p]        = sum_r C[l, r] s_in[p, r]   (A = C K-major,  B = s_in K-major)
 //   d_cumA_blue[l] = sum_p d_ch[l, p] u[l, p]
-// into one of two TMEM buffers, so the MMAs of head k overlap the epilogue of
-// head k - 1.
+// into one of two TMEM buffers.  The producer issues the TMA refills and the
+// MMAs: head k's once every consumer warp has scaled its rows and left the
+// epilogue of head k - 2 (two mbarriers the warps arrive on), so no CTA-wide
+// barrier sits in the loop and the MMAs of head k overlap the epilogue of k - 1.
 template <int Q>
 __global__ void __launch_bounds__(kThreadsWide + 32, 1) tc_bwd_blue_kernel(const Params p, const __grid_constant__ TcMaps maps) {
     constexpr int NT = Q / 128;
@@ -779,7 +781,7 @@ __global__ void __launch_bounds__(kThreadsWide + 32, 1) tc_bwd_blue_kernel(const
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = align1024(smem_raw);
     uint8_t *Cs = sm, *stg = sm + 2 * RB;
-    __shared__ uint64_t bar_res, bar_x[NST], bar_free[NST], bar_mma[2];
+    __shared__ uint64_t bar_res, bar_x[NST], bar_free[NST], bar_scaled[NST], bar_mma[2], bar_tfree[2];
     __shared__ uint32_t s_tmem;
     __shared__ int s_issued, s_landed, s_perr;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -807,9 +809,12 @@ __global__ void __launch_bounds__(kThreadsWide + 32, 1) tc_bwd_blue_kernel(const
         for (int i = 0; i < NST; ++i) {
             mbar_init(&bar_x[i], 1);
             mbar_init(&bar_free[i], 1);
+            mbar_init(&bar_scaled[i], NCONS / 32);
         }
-        mbar_init(&bar_mma[0], 1);
-        mbar_init(&bar_mma[1], 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&bar_mma[i], 1);
+            mbar_init(&bar_tfree[i], NCONS / 32);
+        }
         mbar_fence_init();
         s_issued = 0;
         s_landed = 0;
@@ -820,24 +825,56 @@ __global__ void __launch_bounds__(kThreadsWide + 32, 1) tc_bwd_blue_kernel(const
     const uint32_t tm = s_tmem;
     bool ok = true;
     if (warp == NCONS / 32) {
-        // ---- producer: C once, then (dy_k, s_in_k) into stage k % NST once head k - NST's MMAs are done
+        // ---- producer: C once; (dy_k, s_in_k) into stage k % NST once head k - NST's
+        // MMAs are done; head k's MMAs once it is scaled and TMEM buffer k & 1 is free
         if (lane == 0) {
-            mbar_arrive_expect_tx(&bar_res, 2 * RB);
-            for (int rb = 0; rb < 2; ++rb)
-                for (int j = 0; j < NT; ++j)
-                    tma_load_4d(Cs + rb * RB + j * kTile, &maps.C, &bar_res, 64 * rb, g, t0 + 128 * j, bi);
-            for (int k = 0; k < nh; ++k) {
+            auto load = [&](int k) {
                 const int st = k % NST, h = h_begin + k;
-                if (k >= NST && !mbar_wait(&bar_free[st], (uint32_t)(((k - NST) / NST) & 1))) {
-                    s_perr = 1;
-                    break;
-                }
                 uint8_t *dys = stg + st * STG, *sis = dys + XB;
                 const int sidx = (bi * p.n + c) * p.H + h;
                 mbar_arrive_expect_tx(&bar_x[st], STG);
                 for (int j = 0; j < NT; ++j) tma_load_4d(dys + j * kTile, &maps.dy, &bar_x[st], 0, h, t0 + 128 * j, bi);
                 for (int rb = 0; rb < 2; ++rb) tma_load_3d(sis + rb * SB, &maps.st, &bar_x[st], 64 * rb, 0, sidx);
                 s_issued = k + 1;
+            };
+            mbar_arrive_expect_tx(&bar_res, 2 * RB);
+            for (int rb = 0; rb < 2; ++rb)
+                for (int j = 0; j < NT; ++j)
+                    tma_load_4d(Cs + rb * RB + j * kTile, &maps.C, &bar_res, 64 * rb, g, t0 + 128 * j, bi);
+            for (int k = 0; k < NST && k < nh; ++k) load(k);
+            for (int k = 0; k < nh; ++k) {
+                const int st = k % NST;
+                if (!mbar_wait(&bar_scaled[st], (uint32_t)((k / NST) & 1)) || s_perr) {
+                    s_perr = 1;
+                    break;
+                }
+                s_landed = k + 1;
+                // the stage of head k - 1 is free once its MMAs are done: head k - 1 + NST goes there
+                if (k >= 1 && k - 1 + NST < nh) {
+                    if (!mbar_wait(&bar_free[(k - 1) % NST], (uint32_t)(((k - 1) / NST) & 1))) {
+                        s_perr = 1;
+                        break;
+                    }
+                    load(k - 1 + NST);
+                }
+                if (k >= 2 && !mbar_wait(&bar_tfree[k & 1], (uint32_t)(((k - 2) >> 1) & 1))) {
+                    s_perr = 1;
+                    break;
+                }
+                tc_fence_after();
+                uint8_t *dys = stg + st * STG, *sis = dys + XB;
+                const uint32_t buf = BUF * (k & 1);
+                const uint32_t i1 = idesc_bf16(128, 64, true, true);
+                for (int ks = 0; ks < Q / 16; ++ks)
+                    mma_bf16(tm + buf, sdesc_mnmajor(smem_u32(Cs), ks, RB), sdesc_mnmajor(smem_u32(dys), ks, XB), i1,
+                             ks > 0);
+                const uint32_t i2 = idesc_bf16(128, 64, false, false);
+                for (int tb = 0; tb < NT; ++tb)
+                    for (int ks = 0; ks < kN / 16; ++ks)
+                        mma_bf16(tm + buf + 64 + tb * 64, sdesc_kmajor(smem_u32(Cs + tb * kTile), ks, RB),
+                                 sdesc_kmajor(smem_u32(sis), ks, SB), i2, ks > 0);
+                mma_commit(&bar_mma[k & 1]);
+                mma_commit(&bar_free[st]);
             }
         }
     } else {
@@ -859,15 +896,15 @@ __global__ void __launch_bounds__(kThreadsWide + 32, 1) tc_bwd_blue_kernel(const
         uint4 dch[8], dch_prev[8];  // scaled dy row t of the current / previous head
 #pragma unroll
         for (int i = 0; i < 8; ++i) dch_prev[i] = dch[i] = make_uint4(0, 0, 0, 0);
-        for (int k = 0; k <= nh; ++k) {
+        for (int k = 0; k <= nh && ok; ++k) {
             if (k < nh) {
                 const int st = k % NST;
-                uint8_t *dys = stg + st * STG, *sis = dys + XB;
+                uint8_t *dys = stg + st * STG;
                 const float e_row = __expf(c_cur);
                 c_cur = c_nx;
                 if (k + 2 < nh) c_nx = fetch(k + 2);
-                bool okk = ok && mbar_wait(&bar_x[st], (uint32_t)((k / NST) & 1));
-                if (okk && t < Q) {
+                ok = __all_sync(0xffffffffu, mbar_wait(&bar_x[st], (uint32_t)((k / NST) & 1)) && ok);  // warp-uniform
+                if (ok && t < Q) {
                     const uint32_t base = smem_u32(dys);
 #pragma unroll
                     for (int c8 = 0; c8 < 8; ++c8) {
@@ -884,45 +921,36 @@ __global__ void __launch_bounds__(kThreadsWide + 32, 1) tc_bwd_blue_kernel(const
                         dch[c8] = v;
                     }
                 }
+                if (!ok) s_perr = 1;
                 fence_async_smem();
-                tc_fence_before();
-                okk = bar_and(1, NCONS, okk);  // also: epilogue k - 2 has left TMEM buffer k & 1
-                tc_fence_after();
-                if (!okk) {
-                    ok = false;
-                    break;
-                }
-                if (tid == 0) {
-                    s_landed = k + 1;
-                    const uint32_t buf = BUF * (k & 1);
-                    const uint32_t i1 = idesc_bf16(128, 64, true, true);
-                    for (int ks = 0; ks < Q / 16; ++ks)
-                        mma_bf16(tm + buf, sdesc_mnmajor(smem_u32(Cs), ks, RB), sdesc_mnmajor(smem_u32(dys), ks, XB), i1,
-                                 ks > 0);
-                    const uint32_t i2 = idesc_bf16(128, 64, false, false);
-                    for (int tb = 0; tb < NT; ++tb)
-                        for (int ks = 0; ks < kN / 16; ++ks)
-                            mma_bf16(tm + buf + 64 + tb * 64, sdesc_kmajor(smem_u32(Cs + tb * kTile), ks, RB),
-                                     sdesc_kmajor(smem_u32(sis), ks, SB), i2, ks > 0);
-                    mma_commit(&bar_mma[k & 1]);
-                    mma_commit(&bar_free[st]);
-                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bar_scaled[st]);  // the producer issues head k's MMAs
             }
             if (k > 0) {
                 // ---- epilogue of head k - 1
                 const int kk = k - 1, h = h_begin + kk;
                 const uint32_t buf = BUF * (kk & 1);
-                ok = mbar_wait(&bar_mma[kk & 1], (uint32_t)((kk >> 1) & 1)) && ok;
+                ok = __all_sync(0xffffffffu, mbar_wait(&bar_mma[kk & 1], (uint32_t)((kk >> 1) & 1)) && ok);
+                if (!ok) {
+                    s_perr = 1;
+                    break;
+                }
                 tc_fence_after();
                 float v[32];
                 tmem_ld32(tmem_addr(tm, 32 * q4, buf + 32 * hf), v);
+                float u[64];
+                if (t < Q) {  // warp w holds rows 128 (w / 4) + 32 (w % 4) + lane of u: its own t
+                    tmem_ld32(tmem_addr(tm, 32 * q4, buf + 64 + 64 * hf), u);
+                    tmem_ld32(tmem_addr(tm, 32 * q4, buf + 64 + 64 * hf + 32), u + 32);
+                }
+                // TMEM buffer kk & 1 read: the MMAs of head k + 1 may overwrite it
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bar_tfree[kk & 1]);
                 bf16 *dsin = p.dstates_bf + ix_state(p, bi, c, h);
 #pragma unroll
                 for (int j = 0; j < 32; ++j) dsin[(size_t)(32 * hf + j) * kN + r] = __float2bfloat16_rn(v[j]);
-                if (t < Q) {  // warp w holds rows 128 (w / 4) + 32 (w % 4) + lane of u: its own t
-                    float u[64];
-                    tmem_ld32(tmem_addr(tm, 32 * q4, buf + 64 + 64 * hf), u);
-                    tmem_ld32(tmem_addr(tm, 32 * q4, buf + 64 + 64 * hf + 32), u + 32);
+                if (t < Q) {
                     float acc = 0.f;
 #pragma unroll
                     for (int c8 = 0; c8 < 8; ++c8) {
@@ -944,6 +972,8 @@ __global__ void __launch_bounds__(kThreadsWide + 32, 1) tc_bwd_blue_kernel(const
     if (!ok && tid == 0) flag_timeout(p);
     if (tid == 0)
         for (int k = s_landed; k < s_issued; ++k) mbar_wait(&bar_x[k % NST], (uint32_t)((k / NST) & 1));
+    // the last heads' MMAs (each commit covers the producer's earlier ones)
+    if (tid == 0 && s_landed > 0) mbar_wait(&bar_free[(s_landed - 1) % NST], (uint32_t)(((s_landed - 1) / NST) & 1));
     tc_sync();
     if (warp == 0) tmem_dealloc(tm, 512);
 }
