@@ -1243,7 +1243,7 @@ __global__ void __launch_bounds__(kThreadsWide, 1) tc_bwd_orange_kernel(const Pa
     uint8_t *sm = align1024(smem_raw);
     uint8_t *Mt = sm, *xs = Mt + NCBT * kTile, *dys = xs + XB;  // dys: 2 buffers
     float *fbuf = reinterpret_cast<float *>(dys + 2 * XB);       // [NSC][FST]
-    __shared__ uint64_t bar_cb, bar_x, bar_dy[2], bar_a, bar_mma;
+    __shared__ uint64_t bar_cb, bar_x, bar_dy[2], bar_mma;
     __shared__ uint32_t s_tmem;
     __shared__ int s_x_issued, s_dy_issued, s_landed;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -1281,8 +1281,7 @@ __global__ void __launch_bounds__(kThreadsWide, 1) tc_bwd_orange_kernel(const Pa
         mbar_init(&bar_x, 1);
         mbar_init(&bar_dy[0], 1);
         mbar_init(&bar_dy[1], 1);
-        mbar_init(&bar_a, 1);
-        mbar_init(&bar_mma, 1);
+        mbar_init(&bar_mma, 2);
         mbar_fence_init();
         s_x_issued = 0;
         s_dy_issued = 0;
@@ -1501,7 +1500,6 @@ __global__ void __launch_bounds__(kThreadsWide, 1) tc_bwd_orange_kernel(const Pa
                 for (int ks = 0; ks < 8; ++ks)
                     mma_bf16(tm + 128 + 64, sdesc_mnmajor(smem_u32(tile_of(1, 2)), ks, kTile),
                              sdesc_mnmajor(smem_u32(xs) + 128 * 128, ks, XB), ib, ks > 0);
-                mma_commit(&bar_a);
             }
             if (k + 2 < nh) {  // buffer (k + 2) % NSC was last read by head k - 1
                 stash(k + 2);
@@ -1514,25 +1512,32 @@ __global__ void __launch_bounds__(kThreadsWide, 1) tc_bwd_orange_kernel(const Pa
             tc_fence_before();
             okk = bar_and(1, NCONS, true);
             tc_fence_after();
-            if (tid == 0) {
-                // dx'[0] = M^T[s-block 0] dy;  yo[0] = M[t-block 0, s-block 0] (dt x);  yo[1] += s-block 0 part
-                const uint32_t ia = idesc_bf16(128, 64, false, true), ib = idesc_bf16(128, 64, true, true);
+            // The s-block 0 MMAs, split between two issuing threads in warps 6 and 7 (the
+            // lightest in this phase), each committing to bar_mma (two arrivals): the
+            // commit of thread 192 also covers its s-block 1 MMAs issued above.
+            if (tid == 224) {  // dx'[0] = M^T[s-block 0] dy
+                const uint32_t ia = idesc_bf16(128, 64, false, true);
                 for (int ks = 0; ks < Q / 16; ++ks)
                     mma_bf16(tm, sdesc_kmajor(smem_u32(tile_of(0, 0)), ks, kTile), sdesc_mnmajor(smem_u32(dyb), ks, XB),
                              ia, ks > 0);
+                mma_commit(&bar_mma);
+            }
+            if (tid == 192) {  // yo[0] = M[t-block 0, s-block 0] (dt x);  yo[1] += s-block 0 part
+                const uint32_t ib = idesc_bf16(128, 64, true, true);
                 for (int tb = 0; tb < NT; ++tb)
                     for (int ks = 0; ks < 8; ++ks)
                         mma_bf16(tm + 128 + 64 * tb, sdesc_mnmajor(smem_u32(tile_of(0, 2 * tb)), ks, kTile),
                                  sdesc_mnmajor(smem_u32(xs), ks, XB), ib, tb == 1 || ks > 0);
                 mma_commit(&bar_mma);
+            }
+            if (tid == 0) {
                 // the store of head k - 1's dx has read its buffer: dy of head k + 1 goes there
                 if (k > 0) bulk_wait_read_all();
                 if (k + 1 < nh) issue_dy(k + 1);
             }
             if (k + 1 < nh) derive(k + 1);  // while the MMAs run (raw scalars visible since barrier 1)
-            // ---- epilogue of head k (row i)
+            // ---- epilogue of head k (row i): every MMA of the head is done, so dy may be overwritten
             okk = mbar_wait(&bar_mma, (uint32_t)(k & 1));
-            if (NT == 2) okk = mbar_wait(&bar_a, (uint32_t)(k & 1)) && okk;  // dy may now be overwritten
             tc_fence_after();
             if (!okk) ok = false;
             if (tid == 0 && okk && k + 1 < nh) issue_x(k + 1);  // x is free once the MMAs are done
