@@ -282,8 +282,11 @@ __global__ void __launch_bounds__(kThreadsWide) tc_k2_kernel(const Params p, con
 // as D[r, p] (M = dstate; A = B, MN-major; B operand = scaled x, MN-major)
 // into one of two TMEM buffers, so the MMA of head k overlaps the epilogue of
 // head k - 1.  Consumer thread t scales row t of x (scalars fetched into
-// registers two heads ahead); the producer refills a stage once the MMA that
-// read it completes.  The scale sits on x, not B, so B is shared by all heads.
+// registers two heads ahead).  The producer refills a stage once the MMA that
+// read it completes and issues head k's MMA once every consumer warp has
+// scaled its rows and left the epilogue of head k - 2 (mbarriers the warps
+// arrive on; no CTA-wide barrier in the loop).  The scale sits on x, not B, so
+// B is shared by all heads.
 template <int Q>
 __global__ void __launch_bounds__(kThreadsWide + 32, 1) tc_k3_kernel(const Params p, const __grid_constant__ TcMaps maps) {
     constexpr int NT = Q / 128;
@@ -293,7 +296,7 @@ __global__ void __launch_bounds__(kThreadsWide + 32, 1) tc_k3_kernel(const Param
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = align1024(smem_raw);
     uint8_t *Bs = sm, *xst = sm + 2 * RB;  // B: 2 r-blocks of Q rows; x: NST stages
-    __shared__ uint64_t bar_res, bar_x[NST], bar_free[NST], bar_mma[2];
+    __shared__ uint64_t bar_res, bar_x[NST], bar_free[NST], bar_scaled[NST], bar_mma[2], bar_tfree[2];
     __shared__ uint32_t s_tmem;
     __shared__ int s_issued, s_landed, s_perr;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -319,9 +322,12 @@ __global__ void __launch_bounds__(kThreadsWide + 32, 1) tc_k3_kernel(const Param
         for (int i = 0; i < NST; ++i) {
             mbar_init(&bar_x[i], 1);
             mbar_init(&bar_free[i], 1);
+            mbar_init(&bar_scaled[i], NCONS / 32);
         }
-        mbar_init(&bar_mma[0], 1);
-        mbar_init(&bar_mma[1], 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&bar_mma[i], 1);
+            mbar_init(&bar_tfree[i], NCONS / 32);
+        }
         mbar_fence_init();
         s_issued = 0;
         s_landed = 0;
@@ -332,22 +338,47 @@ __global__ void __launch_bounds__(kThreadsWide + 32, 1) tc_k3_kernel(const Param
     const uint32_t tm = s_tmem;
     bool ok = true;
     if (warp == NCONS / 32) {
-        // ---- producer: B once, then x_k into stage k % NST once head k - NST's MMA is done
+        // ---- producer: B once; x_k into stage k % NST once head k - NST's MMA is
+        // done; head k's MMA once it is scaled and TMEM buffer k & 1 is free
         if (lane == 0) {
-            mbar_arrive_expect_tx(&bar_res, 2 * RB);
-            for (int rb = 0; rb < 2; ++rb)
-                for (int j = 0; j < NT; ++j)
-                    tma_load_4d(Bs + rb * RB + j * kTile, &maps.B, &bar_res, 64 * rb, g, t0 + 128 * j, bi);
-            for (int k = 0; k < nh; ++k) {
+            auto load = [&](int k) {
                 const int st = k % NST;
-                if (k >= NST && !mbar_wait(&bar_free[st], (uint32_t)(((k - NST) / NST) & 1))) {
-                    s_perr = 1;
-                    break;
-                }
                 mbar_arrive_expect_tx(&bar_x[st], XB);
                 for (int j = 0; j < NT; ++j)
                     tma_load_4d(xst + st * XB + j * kTile, &maps.x, &bar_x[st], 0, h_begin + k, t0 + 128 * j, bi);
                 s_issued = k + 1;
+            };
+            mbar_arrive_expect_tx(&bar_res, 2 * RB);
+            for (int rb = 0; rb < 2; ++rb)
+                for (int j = 0; j < NT; ++j)
+                    tma_load_4d(Bs + rb * RB + j * kTile, &maps.B, &bar_res, 64 * rb, g, t0 + 128 * j, bi);
+            for (int k = 0; k < NST && k < nh; ++k) load(k);
+            for (int k = 0; k < nh; ++k) {
+                const int st = k % NST;
+                if (!mbar_wait(&bar_scaled[st], (uint32_t)((k / NST) & 1)) || s_perr) {
+                    s_perr = 1;
+                    break;
+                }
+                s_landed = k + 1;
+                // the stage of head k - 1 is free once its MMA is done: head k - 1 + NST goes there
+                if (k >= 1 && k - 1 + NST < nh) {
+                    if (!mbar_wait(&bar_free[(k - 1) % NST], (uint32_t)(((k - 1) / NST) & 1))) {
+                        s_perr = 1;
+                        break;
+                    }
+                    load(k - 1 + NST);
+                }
+                if (k >= 2 && !mbar_wait(&bar_tfree[k & 1], (uint32_t)(((k - 2) >> 1) & 1))) {
+                    s_perr = 1;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t idesc = idesc_bf16(128, 64, true, true);
+                for (int ks = 0; ks < Q / 16; ++ks)
+                    mma_bf16(tm + 64 * (k & 1), sdesc_mnmajor(smem_u32(Bs), ks, RB),
+                             sdesc_mnmajor(smem_u32(xst + st * XB), ks, XB), idesc, ks > 0);
+                mma_commit(&bar_mma[k & 1]);
+                mma_commit(&bar_free[st]);
             }
         }
     } else {
@@ -371,7 +402,7 @@ __global__ void __launch_bounds__(kThreadsWide + 32, 1) tc_k3_kernel(const Param
         // epilogue mapping: TMEM lane = dstate r, columns = headdim p
         const int q4 = warp & 3, hf = warp >> 2;
         const int r = 32 * q4 + lane;
-        for (int k = 0; k <= nh; ++k) {
+        for (int k = 0; k <= nh && ok; ++k) {
             if (k < nh) {
                 const int st = k % NST;
                 uint8_t *xs = xst + st * XB;
@@ -380,33 +411,28 @@ __global__ void __launch_bounds__(kThreadsWide + 32, 1) tc_k3_kernel(const Param
                 d_cur = d_nx;
                 e_cur = e_nx;
                 if (k + 2 < nh) fetch(k + 2, c_nx, d_nx, e_nx);
-                bool okk = ok && mbar_wait(&bar_x[st], (uint32_t)((k / NST) & 1));
-                if (okk && t < Q) scale_row_bf16(xs, t, b_row, valid);
+                ok = __all_sync(0xffffffffu, mbar_wait(&bar_x[st], (uint32_t)((k / NST) & 1)) && ok);  // warp-uniform
+                if (ok && t < Q) scale_row_bf16(xs, t, b_row, valid);
+                if (!ok) s_perr = 1;
                 fence_async_smem();
-                tc_fence_before();
-                okk = bar_and(1, NCONS, okk);  // also: epilogue k - 2 has left TMEM buffer k & 1
-                tc_fence_after();
-                if (!okk) {
-                    ok = false;
-                    break;
-                }
-                if (tid == 0) {
-                    s_landed = k + 1;
-                    const uint32_t idesc = idesc_bf16(128, 64, true, true);
-                    for (int ks = 0; ks < Q / 16; ++ks)
-                        mma_bf16(tm + 64 * (k & 1), sdesc_mnmajor(smem_u32(Bs), ks, RB), sdesc_mnmajor(smem_u32(xs), ks, XB),
-                                 idesc, ks > 0);
-                    mma_commit(&bar_mma[k & 1]);
-                    mma_commit(&bar_free[st]);
-                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bar_scaled[st]);  // the producer issues head k's MMA
             }
             if (k > 0) {
                 // ---- epilogue of head k - 1
                 const int kk = k - 1;
-                ok = mbar_wait(&bar_mma[kk & 1], (uint32_t)((kk >> 1) & 1)) && ok;
+                ok = __all_sync(0xffffffffu, mbar_wait(&bar_mma[kk & 1], (uint32_t)((kk >> 1) & 1)) && ok);
+                if (!ok) {
+                    s_perr = 1;
+                    break;
+                }
                 tc_fence_after();
                 float v[32];
                 tmem_ld32(tmem_addr(tm, 32 * q4, 64 * (kk & 1) + 32 * hf), v);
+                // TMEM buffer kk & 1 read: the MMA of head k + 1 may overwrite it
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bar_tfree[kk & 1]);
                 bf16 *out = p.states_bf + ix_state(p, bi, c, h_begin + kk);
 #pragma unroll
                 for (int j = 0; j < 32; ++j) out[(size_t)(32 * hf + j) * kN + r] = __float2bfloat16_rn(v[j]);
@@ -417,9 +443,11 @@ __global__ void __launch_bounds__(kThreadsWide + 32, 1) tc_k3_kernel(const Param
     ok = __syncthreads_and(ok && s_perr == 0 ? 1 : 0) != 0;
     tc_fence_after();
     if (!ok && tid == 0) flag_timeout(p);
-    // loads issued for heads that were never consumed have to land before exit
+    // loads issued for heads that were never consumed have to land before exit,
+    // and the last MMA (its commit covers the producer's earlier ones)
     if (tid == 0)
         for (int k = s_landed; k < s_issued; ++k) mbar_wait(&bar_x[k % NST], (uint32_t)((k / NST) & 1));
+    if (tid == 0 && s_landed > 0) mbar_wait(&bar_free[(s_landed - 1) % NST], (uint32_t)(((s_landed - 1) / NST) & 1));
     tc_sync();
     if (warp == 0) tmem_dealloc(tm, 128);
 }
