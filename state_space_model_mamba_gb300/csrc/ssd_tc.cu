@@ -256,22 +256,35 @@ __global__ void __launch_bounds__(kThreadsWide) tc_k2_kernel(const Params p, con
     ok = wait_all(&bar_mma, 0, ok);
     tc_fence_after();
     if (ok) {
-        const int r = 128 * tb + 32 * q4 + lane;  // CB row t, or CB^T row s
-        bf16 *cb = p.CBh + ix_cb(p, bi, c, g) + (size_t)r * Q;
-        bf16 *cbt = p.CBt + ix_cb(p, bi, c, g) + (size_t)r * Q + 128 * tb;
+        // 64-column pieces, bf16, staged over the (now dead) operand tiles in the
+        // 128-byte swizzled layout of the CB / CB^T maps and written by TMA
+        const int row = 32 * q4 + lane;
         const int npc = (N1 + N2) / 64;
 #pragma unroll 1
         for (int j = hf; j < npc; j += 2) {
             float v[64];
             tmem_ld64(tmem_addr(tm, 32 * q4, 64 * j), v);
-            bf16 *dst = 64 * j < N1 ? cb + 64 * j : cbt + (64 * j - N1);
-            store_row32_bf16(dst, v);
-            store_row32_bf16(dst + 32, v + 32);
+            const uint32_t base = smem_u32(sm + j * kTile) + (uint32_t)row * 128u;
+#pragma unroll
+            for (int c8 = 0; c8 < 8; ++c8)
+                st_shared_v4(base + (uint32_t)((c8 ^ (row & 7)) * 16), pack_bf2(v[8 * c8], v[8 * c8 + 1]),
+                             pack_bf2(v[8 * c8 + 2], v[8 * c8 + 3]), pack_bf2(v[8 * c8 + 4], v[8 * c8 + 5]),
+                             pack_bf2(v[8 * c8 + 6], v[8 * c8 + 7]));
         }
+        fence_async_smem();
     } else if (tid == 0) {
         flag_timeout(p);
     }
     tc_sync();
+    if (ok && tid == 0) {
+        const int row0 = ((bi * p.n + c) * p.G + g) * Q + 128 * tb;
+        for (int j = 0; j < (N1 + N2) / 64; ++j) {
+            if (64 * j < N1) tma_store_2d(&maps.cb, sm + j * kTile, 64 * j, row0);
+            else tma_store_2d(&maps.cbt, sm + j * kTile, 128 * tb + 64 * j - N1, row0);
+        }
+        bulk_commit();
+        bulk_wait_all();
+    }
     if (warp == 0) tmem_dealloc(tm, NCOL);
 }
 
