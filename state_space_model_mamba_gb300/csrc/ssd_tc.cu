@@ -679,12 +679,6 @@ __global__ void __launch_bounds__(kThreadsWide, 1) tc_k5_kernel(const Params p, 
             for (int tb = 0; tb < NT; ++tb) ep_k[tb] = __expf(cum[tb * 128 + 32 * q4 + lane]);
             // t-block 0 into its spare buffer: the ORANGE MMAs of head k - 2 read it last
             build(0, hf == 0 ? dq : 1 - dq, W0COL + 64 * (k & 1));
-            // prefetch raw scalars of head k + 2, derive those of head k + 1 (raw visible since the last barrier)
-            if (k + 2 < nh) {
-                stash((k + 2) % NSC);
-                if (k + 3 < nh) fetch(k + 3);
-            }
-            if (k + 1 < nh) derive((k + 1) % NSC);
         }
         if (k > 0) {
             // both MMA groups of head k-1 done: W of t-block 1, x, s_in and the accumulators are free
@@ -734,6 +728,15 @@ __global__ void __launch_bounds__(kThreadsWide, 1) tc_k5_kernel(const Params p, 
                 s_issued = k + 1;
             }
             if (!ok) break;
+        }
+        if (k < nh) {
+            // prefetch raw scalars of head k + 2, derive those of head k + 1 (raw visible
+            // since the last barrier), after x of head k has been requested
+            if (k + 2 < nh) {
+                stash((k + 2) % NSC);
+                if (k + 3 < nh) fetch(k + 3);
+            }
+            if (k + 1 < nh) derive((k + 1) % NSC);
         }
         if (NT == 2 && k < nh) {
             if (hf == 0) {
