@@ -1254,18 +1254,21 @@ __global__ void __launch_bounds__(kThreadsWide, 1) tc_bwd_k3_kernel(const Params
 // stores at the next head's first barrier.  The ORANGE block of the backward is
 // restated so that every reduction becomes a per-row dot product of two MMA
 // outputs (thread = row of the chunk):
-//   M^T[s, t]   = CB^T[s, t] exp(cumA_t - cumA_s)   (t >= s, 0 above): built per
-//                 head in shared memory from a copy of CB^T kept in TMEM
-//   dx'[s, p]   = sum_t M^T[s, t] dy[t, p]           (A = M^T K-major,  B = dy MN-major)
-//   yo[t, p]    = sum_s M^T[s, t] dt_s x[s, p]       (A = M^T MN-major, B = dt*x MN-major)
-//   ddt_orange[s] = sum_p x[s, p] dx'[s, p]          (= sum_t dW[t, s] CB[t, s] decay[t, s])
-//   dx[s, p]    = dt_s dx'[s, p] + D dy[s, p]        (= sum_t W[t, s] dy[t, p] + D dy[s, p])
-//   tgt[t]      = sum_p dy[t, p] yo[t, p]            (= sum_s dW[t, s] W[t, s])
-//   src[s]      = sum_p (dt x)[s, p] dx'[s, p]       (= sum_t dW[t, s] W[t, s])
-// with dW = dy x^T and W = M diag(dt); the page's column sums over targets and
-// the row sums over sources reduce to these because dW is a product.  tgt and
-// src use the same bf16 operands (M^T and dt x as the MMAs saw them), so their
-// sums over the chunk cancel to fp32 rounding as the page's do.  M^T is
+//   W^T[s, t]   = dt_s CB^T[s, t] exp(cumA_t - cumA_s)   (t >= s, 0 above): built
+//                 per head in shared memory from a copy of CB^T kept in TMEM
+//   z[s, p]     = sum_t W^T[s, t] dy[t, p]          (A = W^T K-major,  B = dy MN-major)
+//   yo[t, p]    = sum_s W^T[s, t] x[s, p]           (A = W^T MN-major, B = x MN-major)
+//   dx[s, p]    = z[s, p] + D dy[s, p]              (= sum_t W[t, s] dy[t, p] + D dy[s, p])
+//   src[s]      = sum_p x[s, p] z[s, p]             (= sum_t dW[t, s] W[t, s])
+//   tgt[t]      = sum_p dy[t, p] yo[t, p]           (= sum_s dW[t, s] W[t, s])
+//   ddt_orange[s] = src[s] / dt_s                   (= sum_t dW[t, s] CB[t, s] decay[t, s])
+// with dW = dy x^T; the page's column sums over targets and the row sums over
+// sources reduce to these because dW is a product.  tgt and src are sums of the
+// same bf16 products (W^T, x and dy as the MMAs saw them), so their sums over
+// the chunk cancel to fp32 rounding as the page's do.  A valid token whose dt
+// is exactly 0 is scaled by 1e-30 instead (its W entries stay below any bf16
+// rounding of the others, and ddt_orange stays defined); rows past valid_len
+// are zero.  W^T is
 // built in two halves (s-block 1, then s-block 0) so the first half's MMAs run
 // while the second half is built.  The decay is factored through 64-group
 // pivots off the diagonal groups and 16-wide sub-block pivots inside them (all
@@ -1275,7 +1278,7 @@ template <int Q>
 __global__ void __launch_bounds__(kThreadsWide, 1) tc_bwd_orange_kernel(const Params p, const __grid_constant__ TcMaps maps) {
     constexpr int NT = Q / 128;
     constexpr uint32_t XB = Q * 128;
-    constexpr int NCBT = NT == 2 ? 6 : 2;  // M^T tiles: s-block 0 Q/64, s-block 1 Q/64 - 2
+    constexpr int NCBT = NT == 2 ? 6 : 2;  // W^T tiles: s-block 0 Q/64, s-block 1 Q/64 - 2
     constexpr int NCONS = kThreadsWide;
     constexpr int NSC = 3;                 // scalar buffers: staged two heads ahead
     // per-head tables (32-bit words): cum Q | dt Q | E pairs 192 | E16 pairs 16 x 32 | piv 8 | piv16 16 | D 4
@@ -1317,7 +1320,7 @@ __global__ void __launch_bounds__(kThreadsWide, 1) tc_bwd_orange_kernel(const Pa
         }
         return;
     }
-    auto tile_of = [&](int mb, int tj) -> uint8_t * {  // M^T tile of s-block mb, t-tile tj (tj >= 2 mb)
+    auto tile_of = [&](int mb, int tj) -> uint8_t * {  // W^T tile of s-block mb, t-tile tj (tj >= 2 mb)
         return Mt + (mb == 0 ? tj : (Q / 64) + tj - 2) * kTile;
     };
     if (tid == 0) {
@@ -1333,7 +1336,7 @@ __global__ void __launch_bounds__(kThreadsWide, 1) tc_bwd_orange_kernel(const Pa
     }
     if (warp == 0) tmem_alloc(&s_tmem, 512);
     tc_sync();
-    const uint32_t tm = s_tmem;  // dx'[mb] at 64 mb, yo[tb] at 128 + 64 tb, CB^T at 256
+    const uint32_t tm = s_tmem;  // z[mb] at 64 mb, yo[tb] at 128 + 64 tb, CB^T at 256
     bool ok = true;
     const int cbrow = ((bi * p.n + c) * p.G + g) * Q;
     auto issue_x = [&](int k) {  // thread 0: x of head k
@@ -1348,7 +1351,7 @@ __global__ void __launch_bounds__(kThreadsWide, 1) tc_bwd_orange_kernel(const Pa
             tma_load_4d(dys + b * XB + j * kTile, &maps.dy, &bar_dy[b], 0, h_begin + k, t0 + 128 * j, bi);
         s_dy_issued = k + 1;
     };
-    if (tid == 0) {  // CB^T once (staged through the M^T buffer into TMEM), then the head ring
+    if (tid == 0) {  // CB^T once (staged through the W^T buffer into TMEM), then the head ring
         mbar_arrive_expect_tx(&bar_cb, NCBT * kTile);
         for (int mb = 0; mb < NT; ++mb)
             for (int tj = 2 * mb; tj < Q / 64; ++tj)
@@ -1401,7 +1404,7 @@ __global__ void __launch_bounds__(kThreadsWide, 1) tc_bwd_orange_kernel(const Pa
             if (i < Q / 64) f[POFF + i] = f[64 * i + 63];
             if (i < Q / 16) f[P16OFF + i] = f[16 * i + 15];
         };
-        // M^T[s, t] for row s of t-tile tj: CB^T from TMEM, scaled as packed bf16 pairs
+        // W^T[s, t] for row s of t-tile tj: CB^T from TMEM, scaled as packed bf16 pairs
         // (off the row's own 16-wide sub-block), written to the shared-memory tile
         const int q4 = warp & 3;  // this warp's TMEM lane quarter (= row s % 128 / 32)
         auto cb_col = [&](int mb, int tj) -> uint32_t { return (mb == 0 ? CBCOL0 : CBCOL1) + 32 * (tj - 2 * mb); };
@@ -1410,6 +1413,11 @@ __global__ void __launch_bounds__(kThreadsWide, 1) tc_bwd_orange_kernel(const Pa
         // in registers, so the sub-block's direct exponentials need no lane-dependent
         // TMEM column.
         uint32_t cbown[8];
+        // the scale of row s of W^T: dt_s on valid tokens (1e-30 for an exact 0), 0 past valid_len
+        auto row_dt = [&](const float *f, int s) -> float {
+            const float d = f[Q + s];
+            return s < vrows ? (d != 0.f ? d : 1e-30f) : 0.f;
+        };
         auto transform = [&](const float *f, int s, int tj) {
             const int sg = s >> 6, row = s & 127, mb = s >> 7;
             const uint32_t base = smem_u32(tile_of(mb, tj));
@@ -1425,7 +1433,8 @@ __global__ void __launch_bounds__(kThreadsWide, 1) tc_bwd_orange_kernel(const Pa
             // off the diagonal group: column table of the 64-group pivot; on it: column table
             // of the row's 16-wide sub-block pivot (0 up to and including that sub-block)
             const bool diag = tj == sg;
-            const float fr = __expf((diag ? f[P16OFF + (s >> 4)] : f[POFF + sg]) - cs);
+            const float dsc = row_dt(f, s);
+            const float fr = __expf((diag ? f[P16OFF + (s >> 4)] : f[POFF + sg]) - cs) * dsc;
             const uint32_t fr2 = pack_bf2(fr, fr);
             const uint32_t *Erow = diag ? f2 + E16OFF + 32 * (s >> 4) - 32 * sg
                                         : f2 + E2OFF + (sg == 0 ? 0 : (sg == 1 ? 96 : 160)) - 32 * (sg + 1);
@@ -1443,7 +1452,7 @@ __global__ void __launch_bounds__(kThreadsWide, 1) tc_bwd_orange_kernel(const Pa
                 for (int j = 0; j < 16; ++j) {
                     const uint32_t pr = cbown[j >> 1];
                     const float cv = (j & 1) ? bf_hi(pr) : bf_lo(pr);
-                    w[j] = t16 + j >= s ? cv * __expf(f[t16 + j] - cs) : 0.f;
+                    w[j] = t16 + j >= s ? cv * __expf(f[t16 + j] - cs) * dsc : 0.f;
                 }
                 st_shared_v4(base + sw128_chunk(row, 2 * us), pack_bf2(w[0], w[1]), pack_bf2(w[2], w[3]),
                              pack_bf2(w[4], w[5]), pack_bf2(w[6], w[7]));
@@ -1499,12 +1508,11 @@ __global__ void __launch_bounds__(kThreadsWide, 1) tc_bwd_orange_kernel(const Pa
             const int h = h_begin + k, db = k & 1;
             const float *f = fbuf + (k % NSC) * FST;
             uint8_t *dyb = dys + db * XB;
-            // ---- head k's tiles landed: keep row i of x and dy, stage dt * x, zero padding
+            // ---- head k's tiles landed: keep row i of x, zero padded rows of x and dy
             bool okk = ok && mbar_wait(&bar_x, (uint32_t)(k & 1));
             okk = okk && mbar_wait(&bar_dy[db], (uint32_t)((k >> 1) & 1));
             uint4 xr[8];  // row i of x; dy row i stays in shared memory until the epilogue
             if (i < Q) {
-                const float dti = f[Q + i];
                 const uint32_t xb = smem_u32(xs), yb = smem_u32(dyb);
 #pragma unroll
                 for (int c8 = 0; c8 < 8; ++c8) {
@@ -1512,12 +1520,13 @@ __global__ void __launch_bounds__(kThreadsWide, 1) tc_bwd_orange_kernel(const Pa
                     uint4 xv = make_uint4(0, 0, 0, 0);
                     if (valid && okk) xv = ld_shared_v4(ax);
                     xr[c8] = xv;
-                    st_shared_v4(ax, pack_bf2(bf_lo(xv.x) * dti, bf_hi(xv.x) * dti), pack_bf2(bf_lo(xv.y) * dti, bf_hi(xv.y) * dti),
-                                 pack_bf2(bf_lo(xv.z) * dti, bf_hi(xv.z) * dti), pack_bf2(bf_lo(xv.w) * dti, bf_hi(xv.w) * dti));
-                    if (!valid) st_shared_v4(ay, 0u, 0u, 0u, 0u);
+                    if (!valid) {  // padding never reaches an MMA (non-finite values included)
+                        st_shared_v4(ax, 0u, 0u, 0u, 0u);
+                        st_shared_v4(ay, 0u, 0u, 0u, 0u);
+                    }
                 }
             }
-            // ---- M^T, s-block 1 first (its MMAs run while s-block 0 is built)
+            // ---- W^T, s-block 1 first (its MMAs run while s-block 0 is built)
             if (NT == 2 && okk) transform(f, 128 + r, 2 + hi);
             fence_async_smem();
             tc_fence_before();
@@ -1536,7 +1545,7 @@ __global__ void __launch_bounds__(kThreadsWide, 1) tc_bwd_orange_kernel(const Pa
                 }
             }
             if (NT == 2 && tid == 192) {  // warp 6's phase-B units are the lightest
-                // dx'[1] = M^T[s-block 1] dy[t >= 128];  yo[1] = (s-block 1 part)
+                // z[1] = W^T[s-block 1] dy[t >= 128];  yo[1] = (s-block 1 part)
                 const uint32_t ia = idesc_bf16(128, 64, false, true), ib = idesc_bf16(128, 64, true, true);
                 for (int ks = 0; ks < 8; ++ks)
                     mma_bf16(tm + 64, sdesc_kmajor(smem_u32(tile_of(1, 2)), ks, kTile),
@@ -1549,7 +1558,7 @@ __global__ void __launch_bounds__(kThreadsWide, 1) tc_bwd_orange_kernel(const Pa
                 stash(k + 2);
                 if (k + 3 < nh) fetch(k + 3);
             }
-            // ---- M^T, s-block 0
+            // ---- W^T, s-block 0
             transform(f, r, 1 - hi);
             if (NT == 2) transform(f, r, 3 - hi);
             fence_async_smem();
@@ -1559,14 +1568,14 @@ __global__ void __launch_bounds__(kThreadsWide, 1) tc_bwd_orange_kernel(const Pa
             // The s-block 0 MMAs, split between two issuing threads in warps 6 and 7 (the
             // lightest in this phase), each committing to bar_mma (two arrivals): the
             // commit of thread 192 also covers its s-block 1 MMAs issued above.
-            if (tid == 224) {  // dx'[0] = M^T[s-block 0] dy
+            if (tid == 224) {  // z[0] = W^T[s-block 0] dy
                 const uint32_t ia = idesc_bf16(128, 64, false, true);
                 for (int ks = 0; ks < Q / 16; ++ks)
                     mma_bf16(tm, sdesc_kmajor(smem_u32(tile_of(0, 0)), ks, kTile), sdesc_mnmajor(smem_u32(dyb), ks, XB),
                              ia, ks > 0);
                 mma_commit(&bar_mma);
             }
-            if (tid == 192) {  // yo[0] = M[t-block 0, s-block 0] (dt x);  yo[1] += s-block 0 part
+            if (tid == 192) {  // yo[0] = W[t-block 0, s-block 0] x;  yo[1] += s-block 0 part
                 const uint32_t ib = idesc_bf16(128, 64, true, true);
                 for (int tb = 0; tb < NT; ++tb)
                     for (int ks = 0; ks < 8; ++ks)
@@ -1585,11 +1594,11 @@ __global__ void __launch_bounds__(kThreadsWide, 1) tc_bwd_orange_kernel(const Pa
             tc_fence_after();
             if (!okk) ok = false;
             if (tid == 0 && okk && k + 1 < nh) issue_x(k + 1);  // x is free once the MMAs are done
-            const float dti = i < Q ? f[Q + i] : 0.f, Dh = f[DOFF];
-            const float2 dti2 = make_float2(dti, dti), Dh2 = make_float2(Dh, Dh);
-            float2 ddo2 = make_float2(0.f, 0.f), src2 = ddo2, dd2 = ddo2, tgt2 = ddo2;
+            const float Dh = f[DOFF];
+            const float2 Dh2 = make_float2(Dh, Dh);
+            float2 src2 = make_float2(0.f, 0.f), dd2 = src2, tgt2 = src2;
             if (i < Q) {
-                // dx'[i]: TMEM block blk (= i / 128), lanes 32 q4 + lane
+                // z[i]: TMEM block blk (= i / 128), lanes 32 q4 + lane
                 const uint32_t yb = smem_u32(dyb);
                 uint4 dyr[8];
 #pragma unroll
@@ -1607,14 +1616,9 @@ __global__ void __launch_bounds__(kThreadsWide, 1) tc_bwd_orange_kernel(const Pa
                         for (int j = 0; j < 4; ++j) {
                             const float2 x2 = bf2_to_f2(xw[j]), y2 = bf2_to_f2(yw[j]);
                             const float2 z2 = make_float2(z[8 * c8 + 2 * j], z[8 * c8 + 2 * j + 1]);
-                            // dt * x exactly as the yo MMA saw it (bf16), so that sum_t tgt and
-                            // sum_s src are sums of the same products and cancel to fp32 rounding
-                            const float2 xp = fmul2(x2, dti2);
-                            const float2 xd2 = bf2_to_f2(pack_bf2(xp.x, xp.y));
-                            ddo2 = ffma2(x2, z2, ddo2);
-                            src2 = ffma2(xd2, z2, src2);
+                            src2 = ffma2(x2, z2, src2);
                             dd2 = ffma2(x2, y2, dd2);
-                            const float2 o2 = ffma2(dti2, z2, fmul2(Dh2, y2));
+                            const float2 o2 = ffma2(Dh2, y2, z2);
                             o[4 * c8 + j] = valid ? pack_bf2(o2.x, o2.y) : 0u;
                         }
                     }
@@ -1638,8 +1642,9 @@ __global__ void __launch_bounds__(kThreadsWide, 1) tc_bwd_orange_kernel(const Pa
                     }
                 }
                 const size_t cbase = ix_chunk(p, bi, h, c) * Q;
-                p.ddt_main[cbase + i] = valid ? ddo2.x + ddo2.y : 0.f;  // the K3 backward adds its terms
-                p.dcum_main[cbase + i] = valid ? (tgt2.x + tgt2.y) - (src2.x + src2.y) : 0.f;
+                const float src = src2.x + src2.y;
+                p.ddt_main[cbase + i] = valid ? src / row_dt(f, i) : 0.f;  // the K3 backward adds its terms
+                p.dcum_main[cbase + i] = valid ? (tgt2.x + tgt2.y) - src : 0.f;
             }
             fence_async_smem();  // the staged dx rows are read by the next head's TMA store
             float dd = dd2.x + dd2.y;
