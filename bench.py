@@ -98,7 +98,6 @@ def kernel_costs(w, tc: bool) -> dict:
         "bwd_group": (b * n * G * 4.0 * tri * N + b * n * H * 4.0 * Q * P * N,
                       2 * x_b + 2 * sts * st + 4 * bc_b + 2 * cum_b),
         "bwd_k1_chunk_cumsum": (0.0, 4 * cum_b + 8 * tok_h),
-        "bwd_finalize": (0.0, 4 * b * H * n * 2),
     }
     return c
 

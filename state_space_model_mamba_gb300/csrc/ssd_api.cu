@@ -85,7 +85,7 @@ size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
 struct Layout {
     size_t status, cumA, endA, CB, states, states_bf, dstates, dstates_bf;
     size_t dcum_blue, dcum_main, d_delta, ddt_main, d_endA_part, dD_part, dA_part, d_cb, dBC_part;
-    size_t d_cb_bf, cb_count;
+    size_t d_cb_bf, cb_count, fin_count;
     int n_count;
     size_t total;
     int k4_nblk, dD_per, nslice, nslice_cb, nslice_k5, nslice_k3;
@@ -135,6 +135,7 @@ Layout make_layout(const ssd_dims &d, ssd_dtype dt, bool backward) {
         lo.d_cb_bf = tc ? take(2 * b * n * G * Q * Q) : 0;
         lo.n_count = tc ? (int)(b * n * G * ((Q / 128) * (Q / 128 + 1) / 2)) : 0;
         lo.cb_count = tc ? take(4 * (size_t)lo.n_count) : 0;
+        lo.fin_count = take(4 * H);
     }
     lo.total = off;
     return lo;
@@ -205,6 +206,7 @@ Params base_params(const ssd_dims &d, const Layout &lo, void *ws) {
         p.dBC_part = lo.dBC_part ? f(lo.dBC_part) : nullptr;
         p.d_cb_bf = lo.d_cb_bf ? (bf16 *)(w + lo.d_cb_bf) : nullptr;
         p.cb_count = lo.cb_count ? (int *)(w + lo.cb_count) : nullptr;
+        p.fin_count = lo.fin_count ? (int *)(w + lo.fin_count) : nullptr;
         p.n_count = lo.n_count;
     }
     p.k4_nblk = lo.k4_nblk;
@@ -390,7 +392,6 @@ ssd_status ssd_backward(const ssd_dims *dims, ssd_dtype dtype, const void *x, co
         }
     }
     SSD_LAUNCH("bwd_k1_chunk_cumsum", launch_bwd_k1(p, s), 1);
-    SSD_LAUNCH("bwd_finalize", launch_bwd_finalize(p, s), 1);
     return SSD_OK;
 }
 

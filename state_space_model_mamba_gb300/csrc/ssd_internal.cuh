@@ -46,6 +46,7 @@ struct Params {
     int nslice_cb;
     bf16 *d_cb_bf;       // [b, n, G, Q, Q] summed d_cb in bf16 (tensor-core group path)
     int *cb_count;       // [n_count] arrival counters of the d_cb partial blocks
+    int *fin_count;      // [H] arrival counters of the K1-backward warps of each head
     int n_count;
     float *dBC_part;     // [nslice, 2, b, n, G, Q, N]  (tensor-core group path)
     int nslice;
@@ -119,7 +120,6 @@ cudaError_t launch_k1_cumsum(const Params &p, cudaStream_t s);
 cudaError_t launch_k4_state_passing(const Params &p, bool write_final, cudaStream_t s);
 cudaError_t launch_bwd_k4(const Params &p, cudaStream_t s);
 cudaError_t launch_bwd_k1(const Params &p, cudaStream_t s);
-cudaError_t launch_bwd_finalize(const Params &p, cudaStream_t s);
 
 // CUDA-core kernels for the contractions (ssd_simt.cu), T = float or bf16.
 template <typename T> cudaError_t launch_simt_k2(const Params &p, cudaStream_t s);

@@ -19,8 +19,9 @@ namespace ssd {
 // counter clear needs no extra launch.)
 __global__ void k1_chunk_cumsum(Params p) {
     const size_t gid = blockIdx.x * (size_t)blockDim.x + threadIdx.x;
-    // the backward's first kernel also clears the d_cb arrival counters
+    // the backward's first kernel also clears the arrival counters
     if (p.cb_count && gid < (size_t)p.n_count) p.cb_count[gid] = 0;
+    if (p.fin_count && gid < (size_t)p.H) p.fin_count[gid] = 0;
     const int warp = (int)(gid >> 5);
     const int lane = threadIdx.x & 31;
     if (warp >= p.b * p.H * p.n) return;
@@ -268,7 +269,8 @@ cudaError_t launch_bwd_k4(const Params &p, cudaStream_t s) {
 // plus, at the chunk's last position, the K4 term d_endA and the K3 term
 // sum_l d_delta[l].  d_da = suffix sum of d_cumA (reverse warp scan);
 // ddt = ddt_main + d_da * A on valid tokens (0 past valid_len); the dA partial
-// of the chunk is sum_l d_da[l] * dt_eff[l].
+// of the chunk is sum_l d_da[l] * dt_eff[l].  The last warp of a head to finish
+// reduces the head's dA and dD partials (fixed order).
 __global__ void bwd_k1_chunk_cumsum(Params p) {
     const int warp = (int)((blockIdx.x * (size_t)blockDim.x + threadIdx.x) >> 5);
     const int lane = threadIdx.x & 31;
@@ -317,36 +319,37 @@ __global__ void bwd_k1_chunk_cumsum(Params p) {
         }
     }
     dA_acc = warp_sum(dA_acc);
-    if (lane == 0) p.dA_part[warp] = dA_acc;
+    // dA[h], dD[h]: the last warp of head h to finish sums the head's partials
+    // (its b * n dA partials, and the dD partials the ORANGE kernel wrote) in a
+    // fixed order, so the result does not depend on which warp that is
+    int last = 0;
+    if (lane == 0) {
+        p.dA_part[warp] = dA_acc;
+        __threadfence();
+        last = atomicAdd(p.fin_count + h, 1) == p.b * p.n - 1;
+    }
+    if (!__shfl_sync(0xffffffffu, last, 0)) return;
+    __threadfence();
+    float a = 0.f, d = 0.f;
+    for (int i = lane; i < p.b * p.n; i += 32) {
+        const int bb = i / p.n, cc = i % p.n;
+        a += __ldcg(p.dA_part + ix_chunk(p, bb, h, cc));
+        const float *dp = p.dD_part + (((size_t)bb * p.n + cc) * p.H + h) * p.dD_per;
+        for (int k = 0; k < p.dD_per; ++k) d += __ldcg(dp + k);
+    }
+    a = warp_sum(a);
+    d = warp_sum(d);
+    if (lane == 0) {
+        p.dA[h] = a;
+        p.dD[h] = d;
+        p.fin_count[h] = 0;  // ready for the next call
+    }
 }
 
 cudaError_t launch_bwd_k1(const Params &p, cudaStream_t s) {
     const long long warps = (long long)p.b * p.H * p.n;
     const int threads = 256;
     bwd_k1_chunk_cumsum<<<(unsigned)((warps * 32 + threads - 1) / threads), threads, 0, s>>>(p);
-    return cudaGetLastError();
-}
-
-// ------------------------------------------------------------------ dA / dD
-// One block per head; fixed-order sums of the per-(b, chunk) partials.
-__global__ void bwd_finalize(Params p) {
-    __shared__ float red[32];
-    const int h = blockIdx.x;
-    float a = 0.f, d = 0.f;
-    for (int i = threadIdx.x; i < p.b * p.n; i += blockDim.x) {
-        const int bi = i / p.n, c = i % p.n;
-        a += p.dA_part[ix_chunk(p, bi, h, c)];
-        const float *dp = p.dD_part + (((size_t)bi * p.n + c) * p.H + h) * p.dD_per;
-        for (int k = 0; k < p.dD_per; ++k) d += dp[k];
-    }
-    a = block_sum(a, red);
-    if (threadIdx.x == 0) p.dA[h] = a;
-    d = block_sum(d, red);
-    if (threadIdx.x == 0) p.dD[h] = d;
-}
-
-cudaError_t launch_bwd_finalize(const Params &p, cudaStream_t s) {
-    bwd_finalize<<<p.H, 256, 0, s>>>(p);
     return cudaGetLastError();
 }
 
