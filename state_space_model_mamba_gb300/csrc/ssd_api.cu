@@ -53,9 +53,10 @@ cudaError_t mark_end(cudaStream_t s) {
 }
 
 // A second stream per device, so that K2 (CB, which only K5 and the ORANGE
-// backward read) runs beside K1 instead of after it.  The caller's stream
-// forks to it and joins back through two events; the lock covers the
-// record / wait pairs, so concurrent callers never wait on each other's record.
+// backward read) runs on the SMs that K3, K4 and the BLUE backward leave idle
+// instead of between them.  The caller's stream forks to it and joins back
+// through two events; the lock is held from the fork to the join, so concurrent
+// callers never wait on each other's record.
 struct SideStream {
     cudaStream_t st = nullptr;
     cudaEvent_t fork = nullptr, join = nullptr;
@@ -234,12 +235,13 @@ Params base_params(const ssd_dims &d, const Layout &lo, void *ws) {
     } while (0)
 
 template <typename T>
-ssd_status run_forward_chain(const Params &p, bool tc, bool write_final, cudaStream_t s) {
+ssd_status run_forward_chain(const Params &p, bool tc, bool write_final, cudaStream_t s, SideStream *sd) {
+    SSD_LAUNCH("k1_chunk_cumsum", launch_k1_cumsum(p, s), 1);
     if (tc) {
-        // K2 on the side stream beside K1; K3 starts once both are done
-        std::lock_guard<std::mutex> lock(g_side_mu);
-        SideStream *sd = nullptr;
-        SSD_TRY(side_stream(&sd));
+        SSD_LAUNCH("k3_state_tc", launch_tc_k3(p, s), 1);
+        // K2 (CB, read first by K5 or the ORANGE backward) on the side stream, forked
+        // after K1 and enqueued after K3, so that K3's CTAs are placed first and K2's
+        // fill the SMs K3 leaves idle; the caller joins before the first reader
         SSD_TRY(cudaEventRecord(sd->fork, s));
         SSD_TRY(cudaStreamWaitEvent(sd->st, sd->fork, 0));
         {
@@ -247,13 +249,6 @@ ssd_status run_forward_chain(const Params &p, bool tc, bool write_final, cudaStr
             SSD_LAUNCH("k2_cb_tc", launch_tc_k2(p, s), 1);
         }
         SSD_TRY(cudaEventRecord(sd->join, sd->st));
-        SSD_LAUNCH("k1_chunk_cumsum", launch_k1_cumsum(p, s), 1);
-        SSD_TRY(cudaStreamWaitEvent(s, sd->join, 0));
-    } else {
-        SSD_LAUNCH("k1_chunk_cumsum", launch_k1_cumsum(p, s), 1);
-    }
-    if (tc) {
-        SSD_LAUNCH("k3_state_tc", launch_tc_k3(p, s), 1);
     } else {
         SSD_LAUNCH("k2_cb_simt", launch_simt_k2<T>(p, s), 1);
         SSD_LAUNCH("k3_state_simt", launch_simt_k3<T>(p, s), 1);
@@ -324,14 +319,25 @@ ssd_status ssd_forward(const ssd_dims *dims, ssd_dtype dtype, const void *x, con
     g_launches = 0;
     SSD_TRY(cudaMemsetAsync(p.status, 0, sizeof(int), s));
     if (dtype == SSD_F32) {
-        st = run_forward_chain<float>(p, false, true, s);
+        st = run_forward_chain<float>(p, false, true, s, nullptr);
         if (st != SSD_OK) return st;
         SSD_LAUNCH("k5_scan_simt", launch_simt_k5<float>(p, s), 1);
     } else {
-        st = run_forward_chain<bf16>(p, tc, true, s);
+        // the side stream's fork / join records stay paired under the lock
+        std::unique_lock<std::mutex> lock(g_side_mu, std::defer_lock);
+        SideStream *sd = nullptr;
+        if (tc) {
+            lock.lock();
+            SSD_TRY(side_stream(&sd));
+        }
+        st = run_forward_chain<bf16>(p, tc, true, s, sd);
         if (st != SSD_OK) return st;
-        if (tc) SSD_LAUNCH("k5_scan_tc", launch_tc_k5(p, s), 1);
-        else SSD_LAUNCH("k5_scan_simt", launch_simt_k5<bf16>(p, s), 1);
+        if (tc) {
+            SSD_TRY(cudaStreamWaitEvent(s, sd->join, 0));  // CB
+            SSD_LAUNCH("k5_scan_tc", launch_tc_k5(p, s), 1);
+        } else {
+            SSD_LAUNCH("k5_scan_simt", launch_simt_k5<bf16>(p, s), 1);
+        }
     }
     return SSD_OK;
 }
@@ -367,18 +373,25 @@ ssd_status ssd_backward(const ssd_dims *dims, ssd_dtype dtype, const void *x, co
     g_launches = 0;
     SSD_TRY(cudaMemsetAsync(p.status, 0, sizeof(int), s));
     if (dtype == SSD_F32) {
-        st = run_forward_chain<float>(p, false, false, s);
+        st = run_forward_chain<float>(p, false, false, s, nullptr);
         if (st != SSD_OK) return st;
         SSD_LAUNCH("bwd_blue_simt", launch_simt_bwd_blue<float>(p, s), 2);
         SSD_LAUNCH("bwd_k4_state_passing", launch_bwd_k4(p, s), 1);
         SSD_LAUNCH("bwd_main_simt", launch_simt_bwd_main<float>(p, s), 1);
         SSD_LAUNCH("bwd_group_simt", launch_simt_bwd_group<float>(p, s), 2);
     } else {
-        st = run_forward_chain<bf16>(p, tc, false, s);
+        std::unique_lock<std::mutex> lock(g_side_mu, std::defer_lock);
+        SideStream *sd = nullptr;
+        if (tc) {
+            lock.lock();
+            SSD_TRY(side_stream(&sd));
+        }
+        st = run_forward_chain<bf16>(p, tc, false, s, sd);
         if (st != SSD_OK) return st;
         if (tc) {
             SSD_LAUNCH("bwd_blue_tc", launch_tc_bwd_blue(p, s), 1);
             SSD_LAUNCH("bwd_k4_state_passing", launch_bwd_k4(p, s), 1);
+            SSD_TRY(cudaStreamWaitEvent(s, sd->join, 0));  // CB^T
             SSD_LAUNCH("bwd_orange_tc", launch_tc_bwd_orange(p, s), 1);
             SSD_LAUNCH("bwd_k3_tc", launch_tc_bwd_k3(p, s), 1);
             SSD_LAUNCH("bwd_dcb_tc", launch_tc_bwd_dcb(p, s), 1);

@@ -2291,11 +2291,22 @@ __global__ void tc_bwd_dbc_reduce(const Params p) {
     if (valid) {
         const size_t pstride = (size_t)p.b * p.n * p.G * Q * kN;
         const size_t off = ((((size_t)bi * p.n + c) * p.G + g) * Q + q) * kN + 4 * r4;
-        for (int sl = 0; sl < p.nslice; ++sl) {
-            const float4 a = *reinterpret_cast<const float4 *>(p.dBC_part + (sl * 2 + 0) * pstride + off);
-            const float4 b = *reinterpret_cast<const float4 *>(p.dBC_part + (sl * 2 + 1) * pstride + off);
-            sc.x += a.x; sc.y += a.y; sc.z += a.z; sc.w += a.w;
-            sb.x += b.x; sb.y += b.y; sb.z += b.z; sb.w += b.w;
+        // up to 8 slices' loads in flight before they are summed (in slice order)
+#pragma unroll 1
+        for (int s0 = 0; s0 < p.nslice; s0 += 8) {
+            float4 av[8], bv[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                if (s0 + j < p.nslice) {
+                    av[j] = __ldcs(reinterpret_cast<const float4 *>(p.dBC_part + ((s0 + j) * 2 + 0) * pstride + off));
+                    bv[j] = __ldcs(reinterpret_cast<const float4 *>(p.dBC_part + ((s0 + j) * 2 + 1) * pstride + off));
+                }
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                if (s0 + j < p.nslice) {
+                    sc.x += av[j].x; sc.y += av[j].y; sc.z += av[j].z; sc.w += av[j].w;
+                    sb.x += bv[j].x; sb.y += bv[j].y; sb.z += bv[j].z; sb.w += bv[j].w;
+                }
         }
     }
     const size_t o = ix_bc(p, bi, t, g, 4 * r4);
