@@ -2156,6 +2156,15 @@ __global__ void __launch_bounds__(kThreadsWide + 32, 1) tc_bwd_dbc_kernel(const 
             if (nh > 1) issue(1);
             for (int k = 0; k < nh; ++k) {
                 const int st = k & 1;
+                // stage (k + 1) & 1 held head k - 1: refill it as soon as that head's MMAs are
+                // done (issued just before), while the consumers are still scaling head k
+                if (k >= 1 && k + 1 < nh) {
+                    if (!mbar_wait(&bar_mma[(k - 1) & 1], (uint32_t)(((k - 1) >> 1) & 1))) {
+                        s_perr = 1;
+                        break;
+                    }
+                    issue(k + 1);
+                }
                 if (!mbar_wait(&bar_scaled[st], (uint32_t)((k >> 1) & 1)) || s_perr) {
                     s_perr = 1;
                     break;
@@ -2174,13 +2183,6 @@ __global__ void __launch_bounds__(kThreadsWide + 32, 1) tc_bwd_dbc_kernel(const 
                                  sdesc_mnmajor(smem_u32(dis), ks, SB), id, acc);
                     }
                 mma_commit(&bar_mma[st]);
-                if (k >= 1 && k + 1 < nh) {  // stage (k + 1) & 1 was read by head k - 1's MMAs
-                    if (!mbar_wait(&bar_mma[(k - 1) & 1], (uint32_t)(((k - 1) >> 1) & 1))) {
-                        s_perr = 1;
-                        break;
-                    }
-                    issue(k + 1);
-                }
             }
         }
     } else if (ok) {
