@@ -482,8 +482,10 @@ __global__ void __launch_bounds__(kThreadsWide + 32, 1) tc_k3_kernel(const Param
 // (s <= t), stored to TMEM as packed bf16 pairs.  The decay is factored
 // through pivots (both factors <= 1): cumA[64 sb + 63] for a 64 x 64 block
 // strictly below the diagonal, cumA[16 v + 15] for a 16-wide sub-block left of
-// the row's own inside a diagonal block; only the row's own 16-wide sub-block
-// takes direct exponentials.
+// the row's own inside a diagonal block.  The row's own 16-wide sub-block is
+// factored through its first position when the sub-block's whole decay span
+// stays below e^64 (a row factor <= 1 times a column factor <= e^64, both
+// finite in bf16); a sub-block with a larger span takes direct exponentials.
 template <int Q>
 __global__ void __launch_bounds__(kThreadsWide, 1) tc_k5_kernel(const Params p, const __grid_constant__ TcMaps maps) {
     constexpr int NT = Q / 128;
@@ -496,9 +498,11 @@ __global__ void __launch_bounds__(kThreadsWide, 1) tc_k5_kernel(const Params p, 
     constexpr uint32_t OCOL = 0, BCOL = NT * 64, W1COL = 2 * NT * 64, W0COL = W1COL + (NT - 1) * 128;
     static_assert(W0COL + 128 == NCOL, "K5 TMEM columns");
     constexpr int NSC = 3;              // scalar buffers: staged two heads ahead
-    // per-head tables (32-bit words): cum Q | dt Q | gcol pairs Q/2 | T16 pairs (Q/64) x 4 x 32 | piv 8
+    // per-head tables (32-bit words): cum Q | dt Q | gcol pairs Q/2 | T16 pairs (Q/64) x 4 x 32 | piv 8 |
+    // own-sub-block pairs Q/2 | own-sub-block fast flags Q/16
     constexpr int GOFF = 2 * Q, TOFF = GOFF + Q / 2, POFF = TOFF + (Q / 64) * 128;
-    constexpr int FST = POFF + 8;
+    constexpr int OOFF = POFF + 8, FLOFF = OOFF + Q / 2;
+    constexpr int FST = FLOFF + Q / 16;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = align1024(smem_raw);
     uint8_t *Cs = sm, *CBs = Cs + 2 * RB, *xs = CBs + NWT * kTile, *Ss = xs + XB;
@@ -567,6 +571,13 @@ __global__ void __launch_bounds__(kThreadsWide, 1) tc_k5_kernel(const Params p, 
             f2[TOFF + e] = pack_bf2(lo, hi);
         }
         for (int j = tid; j < Q / 64; j += kThreadsWide) f[POFF + j] = f[64 * j + 63];
+        //   own[s] = dt_s exp(cumA[16 v] - cumA_s) for s in sub-block v (>= 1, <= e^64 where used)
+        for (int e = tid; e < Q / 2; e += kThreadsWide) {
+            const int s = 2 * e;
+            const float pv = f[s & ~15];
+            f2[OOFF + e] = pack_bf2(f[Q + s] * __expf(pv - f[s]), f[Q + s + 1] * __expf(pv - f[s + 1]));
+        }
+        for (int v = tid; v < Q / 16; v += kThreadsWide) f[FLOFF + v] = f[16 * v] - f[16 * v + 15] < 64.f ? 1.f : 0.f;
     };
     auto issue_x = [&](int h) {
         mbar_arrive_expect_tx(&bar_x, XB);
@@ -655,17 +666,31 @@ __global__ void __launch_bounds__(kThreadsWide, 1) tc_k5_kernel(const Params p, 
                     pk[4 * c8 + 2] = bmul2(bmul2(cv.z, gv.z), er2);
                     pk[4 * c8 + 3] = bmul2(bmul2(cv.w, gv.w), er2);
                 }
-                if (diag) {  // the row's own 16-wide sub-block: direct exponentials, 0 for s > t
+                if (diag) {  // the row's own 16-wide sub-block, 0 for s > t
                     const uint4 c0 = ld_shared_v4(cbb + sw128_chunk(row, 2 * u));
                     const uint4 c1 = ld_shared_v4(cbb + sw128_chunk(row, 2 * u + 1));
                     const uint32_t cw[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
                     uint32_t own[8];
+                    if (f[FLOFF + (t >> 4)] != 0.f) {  // factored through cumA[t16]
+                        const float ro = __expf(ct - cum[t16]);
+                        const uint32_t ro2 = pack_bf2(ro, ro);
+                        const uint4 o0 = *reinterpret_cast<const uint4 *>(f2 + OOFF + (t16 >> 1));
+                        const uint4 o1 = *reinterpret_cast<const uint4 *>(f2 + OOFF + (t16 >> 1) + 4);
+                        const uint32_t ow[8] = {o0.x, o0.y, o0.z, o0.w, o1.x, o1.y, o1.z, o1.w};
+                        const int tt = t & 15;
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        const int s0 = t16 + 2 * j;
-                        const float w0 = s0 <= t ? bf_lo(cw[j]) * __expf(ct - cum[s0]) * dts[s0] : 0.f;
-                        const float w1 = s0 + 1 <= t ? bf_hi(cw[j]) * __expf(ct - cum[s0 + 1]) * dts[s0 + 1] : 0.f;
-                        own[j] = pack_bf2(w0, w1);
+                        for (int j = 0; j < 8; ++j) {
+                            const uint32_t m = (2 * j <= tt ? 0x0000FFFFu : 0u) | (2 * j + 1 <= tt ? 0xFFFF0000u : 0u);
+                            own[j] = bmul2(bmul2(cw[j], ow[j]), ro2) & m;
+                        }
+                    } else {  // direct exponentials
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) {
+                            const int s0 = t16 + 2 * j;
+                            const float w0 = s0 <= t ? bf_lo(cw[j]) * __expf(ct - cum[s0]) * dts[s0] : 0.f;
+                            const float w1 = s0 + 1 <= t ? bf_hi(cw[j]) * __expf(ct - cum[s0 + 1]) * dts[s0 + 1] : 0.f;
+                            own[j] = pack_bf2(w0, w1);
+                        }
                     }
 #pragma unroll
                     for (int j = 0; j < 32; ++j) pk[j] = (j >> 3) == u ? own[j & 7] : pk[j];
@@ -2415,7 +2440,7 @@ constexpr size_t smem_k2(int Q) { return Q == 128 ? 80 * 1024 : 1024 + 4 * (size
 constexpr size_t smem_k3(int Q) { return 1024 + 2 * (size_t)Q * 128 + 4 * (size_t)Q * 128; }
 constexpr size_t smem_k5(int Q) {
     return 1024 + 3 * (size_t)Q * 128 + 2 * 64 * 128 + (size_t)kTile * (Q / 128) * (Q / 128 + 1) +
-           4 * 3 * (2 * Q + Q / 2 + (Q / 64) * 128 + 8);
+           4 * 3 * (2 * Q + Q / 2 + (Q / 64) * 128 + 8 + Q / 2 + Q / 16);
 }
 constexpr size_t smem_blue(int Q) { return 1024 + 2 * (size_t)Q * 128 + 3 * ((size_t)Q * 128 + 2 * 64 * 128); }
 constexpr size_t smem_k3bwd(int Q) {
