@@ -1297,7 +1297,9 @@ __global__ void __launch_bounds__(kThreadsWide, 1) tc_bwd_k3_kernel(const Params
 // built in two halves (s-block 1, then s-block 0) so the first half's MMAs run
 // while the second half is built.  The decay is factored through 64-group
 // pivots off the diagonal groups and 16-wide sub-block pivots inside them (all
-// factors <= 1).  This kernel writes dx, ddt_main, dcum_main and the dD
+// factors <= 1).  The row's own 16-wide sub-block is factored through its last
+// position (a row factor <= 1, a column factor <= e^64) when its decay span is
+// below e^64, one exponential per element otherwise.  This kernel writes dx, ddt_main, dcum_main and the dD
 // partials first; the K3 backward kernel runs after it and adds its terms.
 template <int Q>
 __global__ void __launch_bounds__(kThreadsWide, 1) tc_bwd_orange_kernel(const Params p, const __grid_constant__ TcMaps maps) {
@@ -1306,10 +1308,12 @@ __global__ void __launch_bounds__(kThreadsWide, 1) tc_bwd_orange_kernel(const Pa
     constexpr int NCBT = NT == 2 ? 6 : 2;  // W^T tiles: s-block 0 Q/64, s-block 1 Q/64 - 2
     constexpr int NCONS = kThreadsWide;
     constexpr int NSC = 3;                 // scalar buffers: staged two heads ahead
-    // per-head tables (32-bit words): cum Q | dt Q | E pairs 192 | E16 pairs 16 x 32 | piv 8 | piv16 16 | D 4
+    // per-head tables (32-bit words): cum Q | dt Q | E pairs 192 | E16 pairs 16 x 32 | piv 8 | piv16 16 | D 4 |
+    // own-sub-block column pairs Q/2 | own-sub-block fast flags Q/16
     constexpr int E2OFF = 2 * Q, E16OFF = E2OFF + 192, POFF = E16OFF + 512, P16OFF = POFF + 8;
     constexpr int DOFF = P16OFF + 16;
-    constexpr int FST = DOFF + 4;
+    constexpr int OOFF = DOFF + 4, FLOFF = OOFF + Q / 2;
+    constexpr int FST = FLOFF + Q / 16;
     constexpr uint32_t CBCOL0 = 256, CBCOL1 = 384;  // CB^T resident in TMEM (packed bf16 pairs)
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = align1024(smem_raw);
@@ -1428,6 +1432,13 @@ __global__ void __launch_bounds__(kThreadsWide, 1) tc_bwd_orange_kernel(const Pa
             }
             if (i < Q / 64) f[POFF + i] = f[64 * i + 63];
             if (i < Q / 16) f[P16OFF + i] = f[16 * i + 15];
+            // own sub-block: O[t] = exp(cumA_t - cumA[t | 15]) (>= 1, <= e^64 where used)
+            for (int e = i; e < Q / 2; e += NCONS) {
+                const int t = 2 * e;
+                const float pv = f[t | 15];
+                f2[OOFF + e] = pack_bf2(__expf(f[t] - pv), __expf(f[t + 1] - pv));
+            }
+            if (i < Q / 16) f[FLOFF + i] = f[16 * i] - f[16 * i + 15] < 64.f ? 1.f : 0.f;
         };
         // W^T[s, t] for row s of t-tile tj: CB^T from TMEM, scaled as packed bf16 pairs
         // (off the row's own 16-wide sub-block), written to the shared-memory tile
@@ -1470,19 +1481,35 @@ __global__ void __launch_bounds__(kThreadsWide, 1) tc_bwd_orange_kernel(const Pa
                              bmul2(bmul2(cb[4 * c8 + 1], e.y), fr2), bmul2(bmul2(cb[4 * c8 + 2], e.z), fr2),
                              bmul2(bmul2(cb[4 * c8 + 3], e.w), fr2));
             }
-            if (diag) {  // the row's own 16-wide sub-block: direct exponentials, 0 for t < s
+            if (diag) {  // the row's own 16-wide sub-block, 0 for t < s
                 const int t16 = s & ~15, us = (s & 63) >> 4;
-                float w[16];
+                uint32_t w2[8];
+                if (f[FLOFF + (s >> 4)] != 0.f) {
+                    // span below e^64: factored through cumA[t16 + 15], row factor (<= 1) x column table
+                    const float ro = __expf(f[t16 + 15] - cs) * dsc;
+                    const uint32_t ro2 = pack_bf2(ro, ro);
+                    const uint4 o0 = *reinterpret_cast<const uint4 *>(f2 + OOFF + (t16 >> 1));
+                    const uint4 o1 = *reinterpret_cast<const uint4 *>(f2 + OOFF + (t16 >> 1) + 4);
+                    const uint32_t ow[8] = {o0.x, o0.y, o0.z, o0.w, o1.x, o1.y, o1.z, o1.w};
+                    const int ss = s & 15;
 #pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    const uint32_t pr = cbown[j >> 1];
-                    const float cv = (j & 1) ? bf_hi(pr) : bf_lo(pr);
-                    w[j] = t16 + j >= s ? cv * __expf(f[t16 + j] - cs) * dsc : 0.f;
+                    for (int j = 0; j < 8; ++j) {
+                        const uint32_t m = (2 * j >= ss ? 0x0000FFFFu : 0u) | (2 * j + 1 >= ss ? 0xFFFF0000u : 0u);
+                        w2[j] = bmul2(bmul2(cbown[j], ow[j]), ro2) & m;
+                    }
+                } else {  // direct exponentials
+                    float w[16];
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        const uint32_t pr = cbown[j >> 1];
+                        const float cv = (j & 1) ? bf_hi(pr) : bf_lo(pr);
+                        w[j] = t16 + j >= s ? cv * __expf(f[t16 + j] - cs) * dsc : 0.f;
+                    }
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) w2[j] = pack_bf2(w[2 * j], w[2 * j + 1]);
                 }
-                st_shared_v4(base + sw128_chunk(row, 2 * us), pack_bf2(w[0], w[1]), pack_bf2(w[2], w[3]),
-                             pack_bf2(w[4], w[5]), pack_bf2(w[6], w[7]));
-                st_shared_v4(base + sw128_chunk(row, 2 * us + 1), pack_bf2(w[8], w[9]), pack_bf2(w[10], w[11]),
-                             pack_bf2(w[12], w[13]), pack_bf2(w[14], w[15]));
+                st_shared_v4(base + sw128_chunk(row, 2 * us), w2[0], w2[1], w2[2], w2[3]);
+                st_shared_v4(base + sw128_chunk(row, 2 * us + 1), w2[4], w2[5], w2[6], w2[7]);
             }
         };
         // CB^T: shared-memory tiles (TMA) -> TMEM, by the threads that later transform each row
@@ -2448,11 +2475,10 @@ constexpr size_t smem_k3bwd(int Q) {
 }
 // Padded above half of the SM's shared memory: a CTA holding 512 TMEM columns
 // must never share its SM with another CTA of the same kernel.
-constexpr size_t smem_orange(int Q) {
-    return 1024 + (size_t)kTile * (Q == 256 ? 6 : 2) + 3 * (size_t)Q * 128 + 4 * 3 * (2 * Q + 732) > 120 * 1024
-               ? 1024 + (size_t)kTile * (Q == 256 ? 6 : 2) + 3 * (size_t)Q * 128 + 4 * 3 * (2 * Q + 732)
-               : 120 * 1024;
+constexpr size_t smem_orange_raw(int Q) {
+    return 1024 + (size_t)kTile * (Q == 256 ? 6 : 2) + 3 * (size_t)Q * 128 + 4 * 3 * (2 * Q + 732 + Q / 2 + Q / 16);
 }
+constexpr size_t smem_orange(int Q) { return smem_orange_raw(Q) > 120 * 1024 ? smem_orange_raw(Q) : 120 * 1024; }
 // Padded above a third of the SM's shared memory: two CTAs of 256 TMEM columns
 // each may share an SM, a third must not.
 constexpr size_t smem_dcb(int Q) {
