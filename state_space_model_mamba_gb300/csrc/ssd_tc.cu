@@ -1745,7 +1745,9 @@ __global__ void __launch_bounds__(kThreadsWide, 2) tc_bwd_dcb_kernel(const Param
     constexpr int NBLK = NT * (NT + 1) / 2;
     constexpr uint32_t STG = 2 * kTile;  // dy rows of the t-block, x rows of the s-block
     constexpr int NSC = 3;               // scalar buffers
-    constexpr int FST = (5 * Q + Q / 64 + Q / 16 + 3) & ~3;
+    // own-sub-block column table and fast flags after the pivots (16-byte aligned)
+    constexpr int OWNOFF = (5 * Q + Q / 64 + Q / 16 + 3) & ~3, FLOFF = OWNOFF + Q;
+    constexpr int FST = (FLOFF + Q / 16 + 3) & ~3;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = align1024(smem_raw);
     float *fbuf = reinterpret_cast<float *>(sm + 2 * STG);  // [NSC][cum | dt | g | g64 | g16 | piv64 | piv16]
@@ -1811,6 +1813,9 @@ __global__ void __launch_bounds__(kThreadsWide, 2) tc_bwd_dcb_kernel(const Param
                 f[4 * Q + l] = d * __expf(f[l | 15] - cl);
                 if ((l & 63) == 63) f[5 * Q + (l >> 6)] = cl;
                 if ((l & 15) == 15) f[5 * Q + Q / 64 + (l >> 4)] = cl;
+                // own sub-block: dt_s exp(cumA[16 v] - cumA_s) (>= 0, <= e^64 dt_s where used)
+                f[OWNOFF + l] = d * __expf(f[l & ~15] - cl);
+                if ((l & 15) == 0) f[FLOFF + (l >> 4)] = f[l] - f[l + 15] < 64.f ? 1.f : 0.f;
             } else {
                 f[2 * Q + l] = d * __expf(f[128 * sk + 127] - cl);
             }
@@ -1994,10 +1999,24 @@ __global__ void __launch_bounds__(kThreadsWide, 2) tc_bwd_dcb_kernel(const Param
                                 av[4 * i + 3] = fmaf(dv[4 * i + 3] * gq.w, e, av[4 * i + 3]);
                             }
                         } else if (v16 == u16) {
+                            if (f[FLOFF + (t >> 4)] != 0.f) {
+                                // span below e^64: factored through cumA[16 v] (row factor <= 1)
+                                const float e = __expf(ct - f[sv]);
+                                const float4 *gv = reinterpret_cast<const float4 *>(f + OWNOFF + sv);
 #pragma unroll
-                            for (int i = 0; i < 16; ++i) {
-                                const int s = sv + i;
-                                if (s <= t) av[i] = fmaf(dv[i] * f[Q + s], __expf(ct - f[s]), av[i]);
+                                for (int i = 0; i < 4; ++i) {
+                                    const float4 gq = gv[i];
+                                    const float g4[4] = {gq.x, gq.y, gq.z, gq.w};
+#pragma unroll
+                                    for (int c4 = 0; c4 < 4; ++c4)
+                                        if (sv + 4 * i + c4 <= t) av[4 * i + c4] = fmaf(dv[4 * i + c4] * g4[c4], e, av[4 * i + c4]);
+                                }
+                            } else {
+#pragma unroll
+                                for (int i = 0; i < 16; ++i) {
+                                    const int s = sv + i;
+                                    if (s <= t) av[i] = fmaf(dv[i] * f[Q + s], __expf(ct - f[s]), av[i]);
+                                }
                             }
                         }
                     }
@@ -2481,10 +2500,10 @@ constexpr size_t smem_orange_raw(int Q) {
 constexpr size_t smem_orange(int Q) { return smem_orange_raw(Q) > 120 * 1024 ? smem_orange_raw(Q) : 120 * 1024; }
 // Padded above a third of the SM's shared memory: two CTAs of 256 TMEM columns
 // each may share an SM, a third must not.
+constexpr size_t dcb_fst(int Q) { return (((5 * Q + Q / 64 + Q / 16 + 3) & ~3) + Q + Q / 16 + 3) & ~3; }
 constexpr size_t smem_dcb(int Q) {
-    return 1024 + 4 * (size_t)kTile + 4 * 3 * (size_t)((5 * Q + Q / 64 + Q / 16 + 3) & ~3) > 80 * 1024
-               ? 1024 + 4 * (size_t)kTile + 4 * 3 * (size_t)((5 * Q + Q / 64 + Q / 16 + 3) & ~3)
-               : 80 * 1024;
+    return 1024 + 4 * (size_t)kTile + 4 * 3 * dcb_fst(Q) > 80 * 1024 ? 1024 + 4 * (size_t)kTile + 4 * 3 * dcb_fst(Q)
+                                                                   : 80 * 1024;
 }
 constexpr size_t smem_dbc(int Q) {
     return 1024 + 2 * (2 * (size_t)Q * 128 + 4 * 64 * 128) + 4 * 4 * Q;
