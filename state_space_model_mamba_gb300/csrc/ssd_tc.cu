@@ -1273,8 +1273,10 @@ __global__ void __launch_bounds__(kThreadsWide, 1) tc_bwd_k3_kernel(const Params
 
 // ====================================================================== ORANGE backward
 // CTA per (b, chunk, group, head slice), 256 threads, looping over the slice's
-// heads; thread 0 refills x as soon as the previous head's MMAs complete
-// (every thread waits for them anyway), dy a head ahead.  A head's dx rows are
+// heads.  x arrives in two 128-row halves: the lower half (read by the last
+// MMAs of a head) has two buffers and is fetched a head ahead; the upper half
+// (read only by the first MMAs) has one, refilled as soon as those complete.
+// dy has two buffers and is fetched a head ahead.  A head's dx rows are
 // staged in its dy buffer once the epilogue has read dy, and leave by TMA tile
 // stores at the next head's first barrier.  The ORANGE block of the backward is
 // restated so that every reduction becomes a per-row dot product of two MMA
@@ -1317,11 +1319,13 @@ __global__ void __launch_bounds__(kThreadsWide, 1) tc_bwd_orange_kernel(const Pa
     constexpr uint32_t CBCOL0 = 256, CBCOL1 = 384;  // CB^T resident in TMEM (packed bf16 pairs)
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = align1024(smem_raw);
-    uint8_t *Mt = sm, *xs = Mt + NCBT * kTile, *dys = xs + XB;  // dys: 2 buffers
+    constexpr int XSL = NT == 2 ? 3 : 2;  // x half tiles: lower half x 2, upper half
+    uint8_t *Mt = sm, *xs = Mt + NCBT * kTile, *dys = xs + XSL * kTile;  // dys: 2 buffers
+    uint8_t *xhi = xs + 2 * kTile;                                        // upper half of x (Q = 256)
     float *fbuf = reinterpret_cast<float *>(dys + 2 * XB);       // [NSC][FST]
-    __shared__ uint64_t bar_cb, bar_x, bar_dy[2], bar_mma;
+    __shared__ uint64_t bar_cb, bar_xlo[2], bar_xhi, bar_a, bar_dy[2], bar_mma;
     __shared__ uint32_t s_tmem;
-    __shared__ int s_x_issued, s_dy_issued, s_landed;
+    __shared__ int s_lo_issued, s_hi_issued, s_dy_issued, s_landed;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     int idx = blockIdx.x;
     const int slice = idx % p.nslice_k5;
@@ -1354,12 +1358,16 @@ __global__ void __launch_bounds__(kThreadsWide, 1) tc_bwd_orange_kernel(const Pa
     };
     if (tid == 0) {
         mbar_init(&bar_cb, 1);
-        mbar_init(&bar_x, 1);
+        mbar_init(&bar_xlo[0], 1);
+        mbar_init(&bar_xlo[1], 1);
+        mbar_init(&bar_xhi, 1);
+        mbar_init(&bar_a, 1);
         mbar_init(&bar_dy[0], 1);
         mbar_init(&bar_dy[1], 1);
         mbar_init(&bar_mma, 2);
         mbar_fence_init();
-        s_x_issued = 0;
+        s_lo_issued = 0;
+        s_hi_issued = 0;
         s_dy_issued = 0;
         s_landed = 0;
     }
@@ -1368,10 +1376,15 @@ __global__ void __launch_bounds__(kThreadsWide, 1) tc_bwd_orange_kernel(const Pa
     const uint32_t tm = s_tmem;  // z[mb] at 64 mb, yo[tb] at 128 + 64 tb, CB^T at 256
     bool ok = true;
     const int cbrow = ((bi * p.n + c) * p.G + g) * Q;
-    auto issue_x = [&](int k) {  // thread 0: x of head k
-        mbar_arrive_expect_tx(&bar_x, XB);
-        for (int j = 0; j < NT; ++j) tma_load_4d(xs + j * kTile, &maps.x, &bar_x, 0, h_begin + k, t0 + 128 * j, bi);
-        s_x_issued = k + 1;
+    auto issue_xlo = [&](int k) {  // rows 0..127 of x of head k into buffer k & 1
+        mbar_arrive_expect_tx(&bar_xlo[k & 1], kTile);
+        tma_load_4d(xs + (k & 1) * kTile, &maps.x, &bar_xlo[k & 1], 0, h_begin + k, t0, bi);
+        s_lo_issued = k + 1;
+    };
+    auto issue_xhi = [&](int k) {  // rows 128..255 of x of head k
+        mbar_arrive_expect_tx(&bar_xhi, kTile);
+        tma_load_4d(xhi, &maps.x, &bar_xhi, 0, h_begin + k, t0 + 128, bi);
+        s_hi_issued = k + 1;
     };
     auto issue_dy = [&](int k) {  // thread 0: dy of head k into buffer k & 1
         const int b = k & 1;
@@ -1385,7 +1398,9 @@ __global__ void __launch_bounds__(kThreadsWide, 1) tc_bwd_orange_kernel(const Pa
         for (int mb = 0; mb < NT; ++mb)
             for (int tj = 2 * mb; tj < Q / 64; ++tj)
                 tma_load_2d(tile_of(mb, tj), &maps.cbt, &bar_cb, 64 * tj, cbrow + 128 * mb);
-        issue_x(0);
+        issue_xlo(0);
+        if (NT == 2) issue_xhi(0);
+        if (nh > 1) issue_xlo(1);
         issue_dy(0);
     }
     {
@@ -1561,14 +1576,16 @@ __global__ void __launch_bounds__(kThreadsWide, 1) tc_bwd_orange_kernel(const Pa
             const float *f = fbuf + (k % NSC) * FST;
             uint8_t *dyb = dys + db * XB;
             // ---- head k's tiles landed: keep row i of x, zero padded rows of x and dy
-            bool okk = ok && mbar_wait(&bar_x, (uint32_t)(k & 1));
+            bool okk = ok && mbar_wait(&bar_xlo[db], (uint32_t)((k >> 1) & 1));
+            if (NT == 2) okk = okk && mbar_wait(&bar_xhi, (uint32_t)(k & 1));
+            uint8_t *xlo = xs + db * kTile;
             okk = okk && mbar_wait(&bar_dy[db], (uint32_t)((k >> 1) & 1));
             uint4 xr[8];  // row i of x; dy row i stays in shared memory until the epilogue
             if (i < Q) {
-                const uint32_t xb = smem_u32(xs), yb = smem_u32(dyb);
+                const uint32_t xb = smem_u32(i < 128 ? xlo : xhi), yb = smem_u32(dyb);
 #pragma unroll
                 for (int c8 = 0; c8 < 8; ++c8) {
-                    const uint32_t ax = xb + sw128_chunk(i, c8), ay = yb + sw128_chunk(i, c8);
+                    const uint32_t ax = xb + sw128_chunk(i & 127, c8), ay = yb + sw128_chunk(i, c8);
                     uint4 xv = make_uint4(0, 0, 0, 0);
                     if (valid && okk) xv = ld_shared_v4(ax);
                     xr[c8] = xv;
@@ -1604,7 +1621,8 @@ __global__ void __launch_bounds__(kThreadsWide, 1) tc_bwd_orange_kernel(const Pa
                              sdesc_mnmajor(smem_u32(dyb) + 128 * 128, ks, XB), ia, ks > 0);
                 for (int ks = 0; ks < 8; ++ks)
                     mma_bf16(tm + 128 + 64, sdesc_mnmajor(smem_u32(tile_of(1, 2)), ks, kTile),
-                             sdesc_mnmajor(smem_u32(xs) + 128 * 128, ks, XB), ib, ks > 0);
+                             sdesc_mnmajor(smem_u32(xhi), ks, kTile), ib, ks > 0);
+                mma_commit(&bar_a);  // the upper half of x is free once these complete
             }
             if (k + 2 < nh) {  // buffer (k + 2) % NSC was last read by head k - 1
                 stash(k + 2);
@@ -1632,8 +1650,12 @@ __global__ void __launch_bounds__(kThreadsWide, 1) tc_bwd_orange_kernel(const Pa
                 for (int tb = 0; tb < NT; ++tb)
                     for (int ks = 0; ks < 8; ++ks)
                         mma_bf16(tm + 128 + 64 * tb, sdesc_mnmajor(smem_u32(tile_of(0, 2 * tb)), ks, kTile),
-                                 sdesc_mnmajor(smem_u32(xs), ks, XB), ib, tb == 1 || ks > 0);
+                                 sdesc_mnmajor(smem_u32(xlo), ks, kTile), ib, tb == 1 || ks > 0);
                 mma_commit(&bar_mma);
+                if (NT == 2 && k + 1 < nh) {  // the s-block 1 MMAs (issued a phase ago) are done: next upper half
+                    if (mbar_wait(&bar_a, (uint32_t)(k & 1))) issue_xhi(k + 1);
+                    else ok = false;
+                }
             }
             if (tid == 0) {
                 // the store of head k - 1's dx has read its buffer: dy of head k + 1 goes there
@@ -1645,7 +1667,7 @@ __global__ void __launch_bounds__(kThreadsWide, 1) tc_bwd_orange_kernel(const Pa
             okk = mbar_wait(&bar_mma, (uint32_t)(k & 1));
             tc_fence_after();
             if (!okk) ok = false;
-            if (tid == 0 && okk && k + 1 < nh) issue_x(k + 1);  // x is free once the MMAs are done
+            if (tid == 0 && okk && k + 2 < nh) issue_xlo(k + 2);  // the lower-half buffer of head k is free
             const float Dh = f[DOFF];
             const float2 Dh2 = make_float2(Dh, Dh);
             float2 src2 = make_float2(0.f, 0.f), dd2 = src2, tgt2 = src2;
@@ -1717,7 +1739,9 @@ __global__ void __launch_bounds__(kThreadsWide, 1) tc_bwd_orange_kernel(const Pa
     // loads issued for heads that were never consumed have to land before exit
     if (tid == 0) {
         mbar_wait(&bar_cb, 0);  // landed long ago unless the kernel gave up early
-        if (s_x_issued > s_landed) mbar_wait(&bar_x, (uint32_t)((s_x_issued - 1) & 1));
+        for (int k = s_landed; k < s_lo_issued; ++k) mbar_wait(&bar_xlo[k & 1], (uint32_t)((k >> 1) & 1));
+        if (s_hi_issued > s_landed) mbar_wait(&bar_xhi, (uint32_t)((s_hi_issued - 1) & 1));
+        if (NT == 2 && s_landed > 0) mbar_wait(&bar_a, (uint32_t)((s_landed - 1) & 1));
         for (int k = s_landed; k < s_dy_issued; ++k) mbar_wait(&bar_dy[k & 1], (uint32_t)((k >> 1) & 1));
     }
     tc_sync();
@@ -2494,8 +2518,10 @@ constexpr size_t smem_k3bwd(int Q) {
 }
 // Padded above half of the SM's shared memory: a CTA holding 512 TMEM columns
 // must never share its SM with another CTA of the same kernel.
+// W^T tiles | x half tiles (Q = 256: two lower, one upper; Q = 128: two) | dy x 2 | scalar tables
 constexpr size_t smem_orange_raw(int Q) {
-    return 1024 + (size_t)kTile * (Q == 256 ? 6 : 2) + 3 * (size_t)Q * 128 + 4 * 3 * (2 * Q + 732 + Q / 2 + Q / 16);
+    return 1024 + (size_t)kTile * (Q == 256 ? 6 : 2) + (size_t)kTile * (Q == 256 ? 3 : 2) + 2 * (size_t)Q * 128 +
+           4 * 3 * (2 * Q + 732 + Q / 2 + Q / 16);
 }
 constexpr size_t smem_orange(int Q) { return smem_orange_raw(Q) > 120 * 1024 ? smem_orange_raw(Q) : 120 * 1024; }
 // Padded above a third of the SM's shared memory: two CTAs of 256 TMEM columns
