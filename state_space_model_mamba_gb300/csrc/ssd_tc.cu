@@ -44,7 +44,7 @@ constexpr int kTile = 16384;  // one [128 rows][64] bf16 SW128 tile
 constexpr int kStatusTimeout = 5;
 
 struct TcMaps {
-    CUtensorMap x, dy, B, C, st, dst, cb, cbt, dcb, part, dx, y;
+    CUtensorMap x, dy, B, C, st, dst, cb, cbt, dcb, part, dx, y, cb64;
 };
 
 __device__ __forceinline__ uint8_t *align1024(uint8_t *p) {
@@ -471,10 +471,13 @@ __global__ void __launch_bounds__(kThreadsWide + 32, 1) tc_k3_kernel(const Param
 // tiles stay resident in shared memory.  One thread issues the ORANGE MMAs and
 // another the BLUE MMAs of a head, each committing to its own mbarrier.  W of
 // t-block 0 has two TMEM buffers, so the next head's t-block-0 units (and its
-// scalar tables) are built while this head's ORANGE MMAs run.  Once both MMA
-// groups of the previous head are done its epilogue runs, writing y into the
-// (now dead) x buffer, from which a TMA tile store takes it; x and s_in of this
-// head are then fetched and land while its t-block-1 units are built.
+// scalar tables) are built while this head's ORANGE MMAs run.  x of this head
+// is requested as soon as the previous head's ORANGE MMAs are done; once its
+// BLUE MMAs are done too, the previous head's epilogue writes y into a staging
+// tile and the (now dead) s_in buffer, from which TMA tile stores take it, and
+// s_in of this head follows.  The CB tiles whose upper 64 rows are zero (the
+// upper 64-column group of each diagonal 128-block) are kept as 64-row tiles,
+// which makes room for the staging tile.
 // Per-head scalars are prefetched two heads ahead.  Per 128-row t-block tb:
 //   ORANGE (TMEM cols tb*64):        W[tb] (A operand in TMEM) x  (x MN-major)
 //   BLUE   (TMEM cols NT*64+tb*64):  C[tb] (K-major)            s_in (K-major)
@@ -505,8 +508,15 @@ __global__ void __launch_bounds__(kThreadsWide, 1) tc_k5_kernel(const Params p, 
     constexpr int FST = FLOFF + Q / 16;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = align1024(smem_raw);
-    uint8_t *Cs = sm, *CBs = Cs + 2 * RB, *xs = CBs + NWT * kTile, *Ss = xs + XB;
-    float *fbuf = reinterpret_cast<float *>(Ss + 2 * SB);  // [NSC][FST]
+    // C | CB tiles (NWT - NT full, NT lower halves) | x | s_in | y staging tile | scalar tables
+    uint8_t *Cs = sm, *CBf = Cs + 2 * RB, *CBh = CBf + (NWT - NT) * kTile, *xs = CBh + NT * (kTile / 2);
+    uint8_t *Ss = xs + XB, *Ys = Ss + 2 * SB;
+    float *fbuf = reinterpret_cast<float *>(Ys + kTile);  // [NSC][FST]
+    // CB tile (t-block tb, 64-column group sb): its upper 64 rows are zero when sb = 2 tb + 1, and
+    // only its lower half is stored, addressed as if the whole tile were there (rows >= 64 read)
+    auto cb_tile = [&](int tb, int sb) -> uint8_t * {
+        return sb == 2 * tb + 1 ? CBh + tb * (kTile / 2) - kTile / 2 : CBf + (tb * (tb + 1) + sb - tb) * kTile;
+    };
     __shared__ uint64_t bar_res, bar_x, bar_s, bar_o, bar_b;
     __shared__ uint32_t s_tmem;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -600,14 +610,18 @@ __global__ void __launch_bounds__(kThreadsWide, 1) tc_k5_kernel(const Params p, 
     tc_sync();
     const uint32_t tm = s_tmem;
     if (tid == 0) {
-        mbar_arrive_expect_tx(&bar_res, 2 * RB + NWT * kTile);
+        mbar_arrive_expect_tx(&bar_res, 2 * RB + (NWT - NT) * kTile + NT * (kTile / 2));
         const int cbrow = ((bi * p.n + c) * p.G + g) * Q;
         for (int j = 0; j < NT; ++j)
             for (int rb = 0; rb < 2; ++rb)
                 tma_load_4d(Cs + rb * RB + j * kTile, &maps.C, &bar_res, 64 * rb, g, t0 + 128 * j, bi);
         for (int tb = 0; tb < NT; ++tb)
-            for (int sb = 0; sb < 2 * (tb + 1); ++sb)
-                tma_load_2d(CBs + (tb * (tb + 1) + sb) * kTile, &maps.cb, &bar_res, 64 * sb, cbrow + 128 * tb);
+            for (int sb = 0; sb < 2 * (tb + 1); ++sb) {
+                if (sb == 2 * tb + 1)
+                    tma_load_2d(CBh + tb * (kTile / 2), &maps.cb64, &bar_res, 64 * sb, cbrow + 128 * tb + 64);
+                else
+                    tma_load_2d(cb_tile(tb, sb), &maps.cb, &bar_res, 64 * sb, cbrow + 128 * tb);
+            }
         issue_x(h_begin);
         issue_s(h_begin);
     }
@@ -648,7 +662,7 @@ __global__ void __launch_bounds__(kThreadsWide, 1) tc_k5_kernel(const Params p, 
 #pragma unroll
                 for (int j = 0; j < 32; ++j) pk[j] = 0u;
             } else {
-                const uint32_t cbb = smem_u32(CBs + (tb * (tb + 1) + sb) * kTile);
+                const uint32_t cbb = smem_u32(cb_tile(tb, sb));
                 const bool diag = sb == tr;
                 const int u = (t & 63) >> 4, t16 = t & ~15;
                 const float ct = cum[t];
@@ -706,11 +720,17 @@ __global__ void __launch_bounds__(kThreadsWide, 1) tc_k5_kernel(const Params p, 
             build(0, hf == 0 ? dq : 1 - dq, W0COL + 64 * (k & 1));
         }
         if (k > 0) {
-            // both MMA groups of head k-1 done: W of t-block 1, x, s_in and the accumulators are free
+            // ORANGE MMAs of head k-1 done: W of t-block 1 and the x buffer are free
             ok = mbar_wait(&bar_o, (uint32_t)((k - 1) & 1)) && ok;
+            if (k < nh) {
+                if (tid == 0 && ok) issue_x(h);
+                if (ok) x_issued = k + 1;
+            }
+            // BLUE MMAs done too: the accumulators are final, the s_in buffer is free
             ok = mbar_wait(&bar_b, (uint32_t)((k - 1) & 1)) && ok;
             tc_fence_after();
-            // ---- epilogue of head k - 1: y rows into the x buffer
+            // ---- epilogue of head k - 1: y rows of t-block 0 into the staging tile, of t-block 1
+            // into the s_in buffer
             const float Dh = D_ep;
 #pragma unroll
             for (int tb = 0; tb < NT; ++tb) {
@@ -720,7 +740,7 @@ __global__ void __launch_bounds__(kThreadsWide, 1) tc_k5_kernel(const Params p, 
                 tmem_ld32(tmem_addr(tm, 32 * q4, BCOL + tb * 64 + hf * 32), bl);
                 const float e = ep_ep[tb];
                 const bool valid = t < vrows;
-                const uint32_t yb = smem_u32(xs);
+                const uint32_t yb = smem_u32(tb == 0 ? Ys : Ss) - (uint32_t)(tb * kTile);  // row t of the tile
 #pragma unroll
                 for (int c8 = 0; c8 < 4; ++c8) {
                     const uint4 u = xr[tb][c8];
@@ -739,19 +759,15 @@ __global__ void __launch_bounds__(kThreadsWide, 1) tc_k5_kernel(const Params p, 
             tc_fence_before();
             ok = __syncthreads_and(ok ? 1 : 0) != 0;
             tc_fence_after();
-            if (tid == 0 && ok) {  // y of head k - 1 out (rows past the sequence end are clipped); x of head k in
-                for (int j = 0; j < NT; ++j) tma_store_4d(&maps.y, xs + j * kTile, 0, h - 1, t0 + 128 * j, bi);
+            if (tid == 0 && ok) {  // y of head k - 1 out (rows past the sequence end are clipped); s_in of head k in
+                for (int j = 0; j < NT; ++j) tma_store_4d(&maps.y, j == 0 ? Ys : Ss, 0, h - 1, t0 + 128 * j, bi);
                 bulk_commit();
                 if (k < nh) {
                     bulk_wait_read_all();
-                    issue_x(h);
+                    issue_s(h);
                 }
             }
-            if (tid == 32 && ok && k < nh) issue_s(h);
-            if (ok && k < nh) {
-                x_issued = k + 1;
-                s_issued = k + 1;
-            }
+            if (ok && k < nh) s_issued = k + 1;
             if (!ok) break;
         }
         if (k < nh) {
@@ -2472,6 +2488,8 @@ cudaError_t make_maps(const Params &p, TcMaps *mp, bool backward) {
         cuuint32_t box[2] = {64, 128};
         if ((e = encode(&mp->cb, p.CBh, 2, dims, strides, box)) != cudaSuccess) return e;
         if ((e = encode(&mp->cbt, p.CBt, 2, dims, strides, box)) != cudaSuccess) return e;
+        cuuint32_t box64[2] = {64, 64};  // the lower halves of the tiles whose upper halves are zero
+        if ((e = encode(&mp->cb64, p.CBh, 2, dims, strides, box64)) != cudaSuccess) return e;
     }
     if (backward) {
         if (p.d_cb_bf) {  // summed d_cb, bf16 [b*n*G*Q rows][Q]: boxes of 64 columns x 128 rows
@@ -2508,8 +2526,10 @@ cudaError_t launch(K kernel, unsigned grid, size_t smem, cudaStream_t s, const P
 // Q = 128 holds 256 TMEM columns per CTA: padded so that at most two CTAs share an SM.
 constexpr size_t smem_k2(int Q) { return Q == 128 ? 80 * 1024 : 1024 + 4 * (size_t)Q * 128; }
 constexpr size_t smem_k3(int Q) { return 1024 + 2 * (size_t)Q * 128 + 4 * (size_t)Q * 128; }
+// C | CB tiles (full ones and lower halves) | x | s_in | y staging tile | scalar tables
 constexpr size_t smem_k5(int Q) {
-    return 1024 + 3 * (size_t)Q * 128 + 2 * 64 * 128 + (size_t)kTile * (Q / 128) * (Q / 128 + 1) +
+    return 1024 + 3 * (size_t)Q * 128 + 2 * 64 * 128 +
+           (size_t)kTile * ((Q / 128) * (Q / 128 + 1) - Q / 128) + (size_t)(kTile / 2) * (Q / 128) + kTile +
            4 * 3 * (2 * Q + Q / 2 + (Q / 64) * 128 + 8 + Q / 2 + Q / 16);
 }
 constexpr size_t smem_blue(int Q) { return 1024 + 2 * (size_t)Q * 128 + 3 * ((size_t)Q * 128 + 2 * 64 * 128); }
