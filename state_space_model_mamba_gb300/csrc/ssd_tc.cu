@@ -298,8 +298,10 @@ __global__ void __launch_bounds__(kThreadsWide) tc_k2_kernel(const Params p, con
 // registers two heads ahead).  The producer refills a stage once the MMA that
 // read it completes and issues head k's MMA once every consumer warp has
 // scaled its rows and left the epilogue of head k - 2 (mbarriers the warps
-// arrive on; no CTA-wide barrier in the loop).  The scale sits on x, not B, so
-// B is shared by all heads.
+// arrive on).  The scale sits on x, not B, so B is shared by all heads.  The
+// bf16 state of a head is staged in one of two swizzled shared tiles and
+// written by TMA tile stores (a row-per-thread epilogue would store 2 bytes
+// per lane per column).
 template <int Q>
 __global__ void __launch_bounds__(kThreadsWide + 32, 1) tc_k3_kernel(const Params p, const __grid_constant__ TcMaps maps) {
     constexpr int NT = Q / 128;
@@ -309,6 +311,8 @@ __global__ void __launch_bounds__(kThreadsWide + 32, 1) tc_k3_kernel(const Param
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = align1024(smem_raw);
     uint8_t *Bs = sm, *xst = sm + 2 * RB;  // B: 2 r-blocks of Q rows; x: NST stages
+    uint8_t *stg = xst + NST * XB;         // two [P][N] bf16 state tiles (two 64 x 64 boxes each)
+    constexpr uint32_t STT = kP * kN * 2;
     __shared__ uint64_t bar_res, bar_x[NST], bar_free[NST], bar_scaled[NST], bar_mma[2], bar_tfree[2];
     __shared__ uint32_t s_tmem;
     __shared__ int s_issued, s_landed, s_perr;
@@ -415,7 +419,9 @@ __global__ void __launch_bounds__(kThreadsWide + 32, 1) tc_k3_kernel(const Param
         // epilogue mapping: TMEM lane = dstate r, columns = headdim p
         const int q4 = warp & 3, hf = warp >> 2;
         const int r = 32 * q4 + lane;
-        for (int k = 0; k <= nh && ok; ++k) {
+        // the loop ends only on a CTA-uniform status (the named barriers below
+        // need every consumer warp), so no warp leaves early
+        for (int k = 0; k <= nh; ++k) {
             if (k < nh) {
                 const int st = k % NST;
                 uint8_t *xs = xst + st * XB;
@@ -435,10 +441,6 @@ __global__ void __launch_bounds__(kThreadsWide + 32, 1) tc_k3_kernel(const Param
                 // ---- epilogue of head k - 1
                 const int kk = k - 1;
                 ok = __all_sync(0xffffffffu, mbar_wait(&bar_mma[kk & 1], (uint32_t)((kk >> 1) & 1)) && ok);
-                if (!ok) {
-                    s_perr = 1;
-                    break;
-                }
                 tc_fence_after();
                 float v[32];
                 tmem_ld32(tmem_addr(tm, 32 * q4, 64 * (kk & 1) + 32 * hf), v);
@@ -446,9 +448,32 @@ __global__ void __launch_bounds__(kThreadsWide + 32, 1) tc_k3_kernel(const Param
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&bar_tfree[kk & 1]);
-                bf16 *out = p.states_bf + ix_state(p, bi, c, h_begin + kk);
+                // state tile kk & 1 is free once the store of head kk - 2 has read it
+                uint8_t *stile = stg + (kk & 1) * STT;
+                if (tid == 0 && kk >= 2) bulk_wait_read_1();
+                ok = bar_and(2, NCONS, ok);
+                if (ok) {  // element (p, r): box r / 64, row p, 16-byte chunk (r % 64) / 8 swizzled by p
+                    const uint32_t base = smem_u32(stile) + (uint32_t)(r >> 6) * (STT / 2);
+                    const int rc = r & 63;
 #pragma unroll
-                for (int j = 0; j < 32; ++j) out[(size_t)(32 * hf + j) * kN + r] = __float2bfloat16_rn(v[j]);
+                    for (int j = 0; j < 32; ++j) {
+                        const int pp = 32 * hf + j;
+                        const uint32_t a = base + (uint32_t)pp * 128u + (uint32_t)((((rc >> 3) ^ (pp & 7)) << 4) + (rc & 7) * 2);
+                        st_shared_u16(a, __bfloat16_as_ushort(__float2bfloat16_rn(v[j])));
+                    }
+                    fence_async_smem();
+                }
+                ok = bar_and(2, NCONS, ok);
+                if (!ok) {
+                    s_perr = 1;
+                    break;
+                }
+                if (tid == 0) {
+                    const int sidx = (bi * p.n + c) * p.H + h_begin + kk;
+                    tma_store_3d(&maps.st, stile, 0, 0, sidx);
+                    tma_store_3d(&maps.st, stile + STT / 2, 64, 0, sidx);
+                    bulk_commit();
+                }
             }
         }
     }
@@ -461,6 +486,7 @@ __global__ void __launch_bounds__(kThreadsWide + 32, 1) tc_k3_kernel(const Param
     if (tid == 0)
         for (int k = s_landed; k < s_issued; ++k) mbar_wait(&bar_x[k % NST], (uint32_t)((k / NST) & 1));
     if (tid == 0 && s_landed > 0) mbar_wait(&bar_free[(s_landed - 1) % NST], (uint32_t)(((s_landed - 1) / NST) & 1));
+    if (tid == 0) bulk_wait_all();
     tc_sync();
     if (warp == 0) tmem_dealloc(tm, 128);
 }
@@ -2525,7 +2551,8 @@ cudaError_t launch(K kernel, unsigned grid, size_t smem, cudaStream_t s, const P
 
 // Q = 128 holds 256 TMEM columns per CTA: padded so that at most two CTAs share an SM.
 constexpr size_t smem_k2(int Q) { return Q == 128 ? 80 * 1024 : 1024 + 4 * (size_t)Q * 128; }
-constexpr size_t smem_k3(int Q) { return 1024 + 2 * (size_t)Q * 128 + 4 * (size_t)Q * 128; }
+// B | x stages | two bf16 state tiles
+constexpr size_t smem_k3(int Q) { return 1024 + 2 * (size_t)Q * 128 + 4 * (size_t)Q * 128 + 2 * (size_t)kP * kN * 2; }
 // C | CB tiles (full ones and lower halves) | x | s_in | y staging tile | scalar tables
 constexpr size_t smem_k5(int Q) {
     return 1024 + 3 * (size_t)Q * 128 + 2 * 64 * 128 +
