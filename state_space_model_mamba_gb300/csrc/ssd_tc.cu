@@ -1854,19 +1854,21 @@ __global__ void __launch_bounds__(kThreadsWide, 2) tc_bwd_dcb_kernel(const Param
     }
     const bool diag = tb == sk;
     // --- per-head scalars: registers -> shared buffer k % NSC -> derived tables
-    float r_cum = 0.f, r_dt = 0.f;
+    // two register sets (head k in set k & 1), so a head's global loads are
+    // issued two heads before they are staged
+    float r_cum[2] = {0.f, 0.f}, r_dt[2] = {0.f, 0.f};
     auto fetch = [&](int k) {
         if (tid < Q) {
             const int h = h_begin + k;
-            r_cum = p.cumA[ix_chunk(p, bi, h, c) * Q + tid];
-            r_dt = tid < vrows ? p.dt[ix_dt(p, bi, h, t0 + tid)] : 0.f;
+            r_cum[k & 1] = p.cumA[ix_chunk(p, bi, h, c) * Q + tid];
+            r_dt[k & 1] = tid < vrows ? p.dt[ix_dt(p, bi, h, t0 + tid)] : 0.f;
         }
     };
     auto stash = [&](int k) {
         float *f = fbuf + (k % NSC) * FST;
         if (tid < Q) {
-            f[tid] = r_cum;
-            f[Q + tid] = r_dt;
+            f[tid] = r_cum[k & 1];
+            f[Q + tid] = r_dt[k & 1];
         }
     };
     auto derive = [&](int k) {
@@ -1982,6 +1984,7 @@ __global__ void __launch_bounds__(kThreadsWide, 2) tc_bwd_dcb_kernel(const Param
             stash(1);
         }
         if (nh > 2) fetch(2);
+        if (nh > 3) fetch(3);
         __syncthreads();
         if (nh > 0) derive(0);
         // Wait for head k's tiles, zero x rows past valid_len, and (thread 0) issue
@@ -2018,7 +2021,7 @@ __global__ void __launch_bounds__(kThreadsWide, 2) tc_bwd_dcb_kernel(const Param
                 ok = __syncthreads_and(okt ? 1 : 0) != 0;
             }
             if (k + 2 < nh) stash(k + 2);
-            if (k + 3 < nh) fetch(k + 3);
+            if (k + 4 < nh) fetch(k + 4);  // set k & 1, just staged
             if (k + 1 < nh) derive(k + 1);
             okt = ok && mbar_wait(&bar_mma[st], (uint32_t)((k >> 1) & 1));
             tc_fence_after();
