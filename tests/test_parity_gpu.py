@@ -12,9 +12,9 @@ torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
 
 
-def small(b, L, H, P, N, G, seed, valid_len=None, bf16=False, init_std=0.3):
+def small(b, L, H, P, N, G, seed, valid_len=None, bf16=False, init_std=0.3, dt_mu=-2.0):
     return generate_small(b, L, H, P, N, G, seed=seed, init_std=init_std, d_final_std=1.0,
-                          valid_len=valid_len, bf16=bf16)
+                          valid_len=valid_len, bf16=bf16, dt_mu=dt_mu)
 
 
 # ---------------------------------------------------------------- fp32 path
@@ -48,6 +48,18 @@ def test_bf16_q128_several_heads_per_cta():
     inp = small(2, 8192, 8, 64, 128, 2, seed=58, valid_len=[8192, 5000], bf16=True)
     gpu = run_gpu(inp, "bf16", 128)
     compare(gpu, run_oracle(inp), TOL["bf16"], "bf16 Q=128 multi-head")
+    padded_grads_zero(gpu, inp["valid_len"])
+
+
+@pytest.mark.parametrize("Q", [128, 256])
+def test_bf16_strong_decay(Q):
+    # dt ~ softplus(N(0.5, 1)) with |A| up to 16: with these seeds 32 % (Q = 128) and
+    # 75 % (Q = 256) of the 16-token blocks decay by more than e^64 (the tensor-core
+    # kernels then take one exponential per element on the diagonal sub-blocks), the
+    # rest stay below it (factored path), mixed within single heads
+    inp = small(2, 700, 4, 64, 128, 2, seed=70 + Q, valid_len=[517, 700], bf16=True, dt_mu=0.5)
+    gpu = run_gpu(inp, "bf16", Q)
+    compare(gpu, run_oracle(inp), TOL["bf16"], f"bf16 strong decay Q={Q}")
     padded_grads_zero(gpu, inp["valid_len"])
 
 
