@@ -379,6 +379,7 @@ ssd_status ssd_backward(const ssd_dims *dims, ssd_dtype dtype, const void *x, co
         SSD_LAUNCH("bwd_k4_state_passing", launch_bwd_k4(p, s), 1);
         SSD_LAUNCH("bwd_main_simt", launch_simt_bwd_main<float>(p, s), 1);
         SSD_LAUNCH("bwd_group_simt", launch_simt_bwd_group<float>(p, s), 2);
+        SSD_LAUNCH("bwd_k1_chunk_cumsum", launch_bwd_k1(p, s), 1);
     } else {
         std::unique_lock<std::mutex> lock(g_side_mu, std::defer_lock);
         SideStream *sd = nullptr;
@@ -394,17 +395,28 @@ ssd_status ssd_backward(const ssd_dims *dims, ssd_dtype dtype, const void *x, co
             SSD_TRY(cudaStreamWaitEvent(s, sd->join, 0));  // CB^T
             SSD_LAUNCH("bwd_orange_tc", launch_tc_bwd_orange(p, s), 1);
             SSD_LAUNCH("bwd_k3_tc", launch_tc_bwd_k3(p, s), 1);
+            // the K1 backward reads nothing the group kernels write: it runs on the side
+            // stream beside them (enqueued after G1, so that G1's CTAs are placed first
+            // and the K1 backward fills the SMs its second wave leaves idle)
+            SSD_TRY(cudaEventRecord(sd->fork, s));
             SSD_LAUNCH("bwd_dcb_tc", launch_tc_bwd_dcb(p, s), 1);
+            SSD_TRY(cudaStreamWaitEvent(sd->st, sd->fork, 0));
+            {
+                cudaStream_t s = sd->st;
+                SSD_LAUNCH("bwd_k1_chunk_cumsum", launch_bwd_k1(p, s), 1);
+            }
+            SSD_TRY(cudaEventRecord(sd->join, sd->st));
             SSD_LAUNCH("bwd_dbc_tc", launch_tc_bwd_dbc(p, s), 1);
             SSD_LAUNCH("bwd_dbc_reduce_tc", launch_tc_bwd_dbc_reduce(p, s), 1);
+            SSD_TRY(cudaStreamWaitEvent(s, sd->join, 0));  // ddt, dA, dD
         } else {
             SSD_LAUNCH("bwd_blue_simt", launch_simt_bwd_blue<bf16>(p, s), 2);
             SSD_LAUNCH("bwd_k4_state_passing", launch_bwd_k4(p, s), 1);
             SSD_LAUNCH("bwd_main_simt", launch_simt_bwd_main<bf16>(p, s), 1);
             SSD_LAUNCH("bwd_group_simt", launch_simt_bwd_group<bf16>(p, s), 2);
+            SSD_LAUNCH("bwd_k1_chunk_cumsum", launch_bwd_k1(p, s), 1);
         }
     }
-    SSD_LAUNCH("bwd_k1_chunk_cumsum", launch_bwd_k1(p, s), 1);
     return SSD_OK;
 }
 
