@@ -37,6 +37,8 @@ METRIC = "SSD fwd+bwd tokens/sec (2.7B-layer shape, 1 GB300); % of tensor/HBM ro
 UNIT = "tokens/s"
 DEFAULT_WORKLOAD = "mamba2_2p7b"
 L2_BYTES = 129 * 1024 * 1024
+# kernels the library launches on its second stream, beside the caller's chain
+SECOND_STREAM = ("k2_cb_tc", "bwd_dcb_tc", "bwd_dbc_tc", "bwd_dbc_reduce_tc")
 PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
@@ -341,7 +343,9 @@ def run_ours(args, w, rank, world, local_rank):
     per = {}
     for name, ms in ptimer.durations(pattern):
         per.setdefault(name, []).append(ms)
-    top = max(per, key=lambda k: sum(per[k]))
+    # the dominant kernel is taken on the caller's stream: the kernels on the library's
+    # second stream share the SMs with it, so their event spans include that overlap
+    top = max((k for k in per if k not in SECOND_STREAM), key=lambda k: sum(per[k]))
 
     # ---------------- timed region (device time, CUDA events on the launching stream)
     stream = torch.cuda.current_stream(dev)
@@ -372,6 +376,9 @@ def run_ours(args, w, rank, world, local_rank):
     tot_k = sum(sum(v) for v in per.values())
     shares = {k: {"launches": len(v) * args.steps // prof_steps, "avg_us": 1e3 * sum(v) / len(v),
                   "share": sum(v) / tot_k if tot_k else None} for k, v in per.items()}
+    for k in shares:
+        if k in SECOND_STREAM:
+            shares[k]["second_stream"] = True
     shares[top]["avg_us"] = 1e3 * sum(live) / len(live)
     shares[top]["timed_live"] = True
     peaks, peak_src = load_peaks()

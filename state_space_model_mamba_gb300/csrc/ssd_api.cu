@@ -53,13 +53,14 @@ cudaError_t mark_end(cudaStream_t s) {
 }
 
 // A second stream per device, so that K2 (CB, which only K5 and the ORANGE
-// backward read) runs on the SMs that K3, K4 and the BLUE backward leave idle
-// instead of between them.  The caller's stream forks to it and joins back
-// through two events; the lock is held from the fork to the join, so concurrent
-// callers never wait on each other's record.
+// backward read) and the backward's group kernels run on the SMs that the
+// caller's chain leaves idle instead of between its kernels.  The caller's
+// stream forks to it and joins back through events (aux marks the end of the
+// backward's group chain); the lock is held from the fork to the last join, so
+// concurrent callers never wait on each other's record.
 struct SideStream {
     cudaStream_t st = nullptr;
-    cudaEvent_t fork = nullptr, join = nullptr;
+    cudaEvent_t fork = nullptr, join = nullptr, aux = nullptr;
 };
 constexpr int kMaxDevices = 64;
 SideStream g_side[kMaxDevices];
@@ -75,6 +76,7 @@ cudaError_t side_stream(SideStream **out) {
         if ((e = cudaStreamCreateWithFlags(&sd.st, cudaStreamNonBlocking)) != cudaSuccess) return e;
         if ((e = cudaEventCreateWithFlags(&sd.fork, cudaEventDisableTiming)) != cudaSuccess) return e;
         if ((e = cudaEventCreateWithFlags(&sd.join, cudaEventDisableTiming)) != cudaSuccess) return e;
+        if ((e = cudaEventCreateWithFlags(&sd.aux, cudaEventDisableTiming)) != cudaSuccess) return e;
     }
     *out = &sd;
     return cudaSuccess;
@@ -390,25 +392,31 @@ ssd_status ssd_backward(const ssd_dims *dims, ssd_dtype dtype, const void *x, co
         st = run_forward_chain<bf16>(p, tc, false, s, sd);
         if (st != SSD_OK) return st;
         if (tc) {
+            // Two chains from here on.  The group kernels (G1: d_cb; G2: dB, dC partials;
+            // G3: their sum) read only the leaves, cumA, the chunk states and d_intra, and
+            // nothing else reads what they write: they run on the side stream (G1 right
+            // after K2, G2 once the K4 backward has written d_intra) and fill the SMs that
+            // the per-head chain on the caller's stream (BLUE, K4 backward, ORANGE, K3
+            // backward, K1 backward) leaves idle.  The caller's stream joins at the end.
+            {
+                cudaStream_t s = sd->st;
+                SSD_LAUNCH("bwd_dcb_tc", launch_tc_bwd_dcb(p, s), 1);
+            }
             SSD_LAUNCH("bwd_blue_tc", launch_tc_bwd_blue(p, s), 1);
             SSD_LAUNCH("bwd_k4_state_passing", launch_bwd_k4(p, s), 1);
-            SSD_TRY(cudaStreamWaitEvent(s, sd->join, 0));  // CB^T
-            SSD_LAUNCH("bwd_orange_tc", launch_tc_bwd_orange(p, s), 1);
-            SSD_LAUNCH("bwd_k3_tc", launch_tc_bwd_k3(p, s), 1);
-            // the K1 backward reads nothing the group kernels write: it runs on the side
-            // stream beside them (enqueued after G1, so that G1's CTAs are placed first
-            // and the K1 backward fills the SMs its second wave leaves idle)
-            SSD_TRY(cudaEventRecord(sd->fork, s));
-            SSD_LAUNCH("bwd_dcb_tc", launch_tc_bwd_dcb(p, s), 1);
+            SSD_TRY(cudaEventRecord(sd->fork, s));  // d_intra
             SSD_TRY(cudaStreamWaitEvent(sd->st, sd->fork, 0));
             {
                 cudaStream_t s = sd->st;
-                SSD_LAUNCH("bwd_k1_chunk_cumsum", launch_bwd_k1(p, s), 1);
+                SSD_LAUNCH("bwd_dbc_tc", launch_tc_bwd_dbc(p, s), 1);
+                SSD_LAUNCH("bwd_dbc_reduce_tc", launch_tc_bwd_dbc_reduce(p, s), 1);
             }
-            SSD_TRY(cudaEventRecord(sd->join, sd->st));
-            SSD_LAUNCH("bwd_dbc_tc", launch_tc_bwd_dbc(p, s), 1);
-            SSD_LAUNCH("bwd_dbc_reduce_tc", launch_tc_bwd_dbc_reduce(p, s), 1);
-            SSD_TRY(cudaStreamWaitEvent(s, sd->join, 0));  // ddt, dA, dD
+            SSD_TRY(cudaEventRecord(sd->aux, sd->st));
+            SSD_TRY(cudaStreamWaitEvent(s, sd->join, 0));  // CB^T
+            SSD_LAUNCH("bwd_orange_tc", launch_tc_bwd_orange(p, s), 1);
+            SSD_LAUNCH("bwd_k3_tc", launch_tc_bwd_k3(p, s), 1);
+            SSD_LAUNCH("bwd_k1_chunk_cumsum", launch_bwd_k1(p, s), 1);
+            SSD_TRY(cudaStreamWaitEvent(s, sd->aux, 0));  // dB, dC
         } else {
             SSD_LAUNCH("bwd_blue_simt", launch_simt_bwd_blue<bf16>(p, s), 2);
             SSD_LAUNCH("bwd_k4_state_passing", launch_bwd_k4(p, s), 1);
