@@ -343,8 +343,10 @@ def run_ours(args, w, rank, world, local_rank):
     per = {}
     for name, ms in ptimer.durations(pattern):
         per.setdefault(name, []).append(ms)
-    # the dominant kernel is taken on the caller's stream: the kernels on the library's
-    # second stream share the SMs with it, so their event spans include that overlap
+    # (while every kernel is timed the library runs its second-stream kernels on the
+    # caller's stream, so these are standalone durations.)  The dominant kernel is taken
+    # among the caller's-stream kernels: in the timed region below the second-stream
+    # kernels run beside them, and their event spans would include that overlap
     top = max((k for k in per if k not in SECOND_STREAM), key=lambda k: sum(per[k]))
 
     # ---------------- timed region (device time, CUDA events on the launching stream)

@@ -134,7 +134,13 @@ ssd_status ssd_workspace_status(const void *workspace, size_t workspace_bytes, v
  * silently when the array is full.  ssd_profile_end deactivates it and
  * returns how many events were recorded (2 per kernel); ssd_profile_name(i)
  * names the i-th recorded kernel (i < 4096).  Timing events add no device
- * work besides the records themselves.
+ * work besides the records themselves.  While every kernel is recorded (no
+ * ssd_profile_only filter), the kernels the library otherwise runs on its
+ * second stream beside the caller's chain (K2, and the backward's d_cb and
+ * dB/dC kernels) run on the call's stream instead, so that each event pair
+ * brackets one kernel running alone; with a filter the schedule is unchanged
+ * and a second-stream kernel's pair is recorded on that stream, spanning any
+ * overlap with the caller's chain.
  *
  * ssd_profile_only: restricts the recording to kernels whose name (as
  * ssd_profile_name reports it) equals `name`; NULL or "" records every

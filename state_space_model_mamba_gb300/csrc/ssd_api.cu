@@ -62,6 +62,12 @@ struct SideStream {
     cudaStream_t st = nullptr;
     cudaEvent_t fork = nullptr, join = nullptr, aux = nullptr;
 };
+// The stream for the side chain's launches: the caller's own while every launch is
+// being timed (ssd_profile_begin without a ssd_profile_only filter), so that each
+// event pair brackets one kernel running alone; the side stream otherwise.
+cudaStream_t side_or_serial(const SideStream *sd, cudaStream_t s) {
+    return (g_rec.ev && !g_rec_only[0]) ? s : sd->st;
+}
 constexpr int kMaxDevices = 64;
 SideStream g_side[kMaxDevices];
 std::mutex g_side_mu;
@@ -246,8 +252,9 @@ ssd_status run_forward_chain(const Params &p, bool tc, bool write_final, cudaStr
         // fill the SMs K3 leaves idle; the caller joins before the first reader
         SSD_TRY(cudaEventRecord(sd->fork, s));
         SSD_TRY(cudaStreamWaitEvent(sd->st, sd->fork, 0));
+        const cudaStream_t side = side_or_serial(sd, s);
         {
-            cudaStream_t s = sd->st;
+            cudaStream_t s = side;
             SSD_LAUNCH("k2_cb_tc", launch_tc_k2(p, s), 1);
         }
         SSD_TRY(cudaEventRecord(sd->join, sd->st));
@@ -398,8 +405,9 @@ ssd_status ssd_backward(const ssd_dims *dims, ssd_dtype dtype, const void *x, co
             // after K2, G2 once the K4 backward has written d_intra) and fill the SMs that
             // the per-head chain on the caller's stream (BLUE, K4 backward, ORANGE, K3
             // backward, K1 backward) leaves idle.  The caller's stream joins at the end.
+            const cudaStream_t side = side_or_serial(sd, s);
             {
-                cudaStream_t s = sd->st;
+                cudaStream_t s = side;
                 SSD_LAUNCH("bwd_dcb_tc", launch_tc_bwd_dcb(p, s), 1);
             }
             SSD_LAUNCH("bwd_blue_tc", launch_tc_bwd_blue(p, s), 1);
@@ -407,7 +415,7 @@ ssd_status ssd_backward(const ssd_dims *dims, ssd_dtype dtype, const void *x, co
             SSD_TRY(cudaEventRecord(sd->fork, s));  // d_intra
             SSD_TRY(cudaStreamWaitEvent(sd->st, sd->fork, 0));
             {
-                cudaStream_t s = sd->st;
+                cudaStream_t s = side;
                 SSD_LAUNCH("bwd_dbc_tc", launch_tc_bwd_dbc(p, s), 1);
                 SSD_LAUNCH("bwd_dbc_reduce_tc", launch_tc_bwd_dbc_reduce(p, s), 1);
             }
