@@ -48,6 +48,19 @@ def dist_env():
     return int(os.environ.get("RANK", "0")), ws, int(os.environ.get("LOCAL_RANK", "0"))
 
 
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    """The largest `x` over all ranks (the slowest rank's time); `x` itself on
+    one rank.  `device` holds the reduction tensor: the rank's GPU under NCCL,
+    the CPU under gloo."""
+    if world <= 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -364,11 +377,7 @@ def run_ours(args, w, rank, world, local_rank):
         ev1.record(stream)
         torch.cuda.synchronize()
     barrier()
-    ms_total = ev0.elapsed_time(ev1)
-    if world > 1:
-        tt = torch.tensor([ms_total], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms_total = float(tt.item())
+    ms_total = max_over_ranks(ev0.elapsed_time(ev1), world, dev)
     ms_step = ms_total / args.steps
     value = w.tokens * world / (ms_step * 1e-3)
     ssd.workspace_status(ws)
@@ -481,11 +490,7 @@ def run_ours(args, w, rank, world, local_rank):
     e1.record(stream)
     torch.cuda.synchronize()
     barrier()
-    e2e_ms = e0.elapsed_time(e1) / e2e_steps
-    if world > 1:
-        tt = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        e2e_ms = float(tt.item())
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, world, dev)
 
     if rank != 0:
         return None
