@@ -324,8 +324,11 @@ def run_ours(args, w, rank, world, local_rank):
              dB=torch.empty_like(B), dC=torch.empty_like(C), dD=torch.empty_like(D),
              d_init=torch.empty_like(fin))
 
-    def step():
+    def fwd():
         ssd.forward_into(dims, x, dt, A, B, C, D, init, vl, y, fin, ws)
+
+    def step():
+        fwd()
         n1 = ssd.last_launch_count()
         ssd.backward_into(dims, x, dt, A, B, C, D, init, vl, dy, dfin, g["dx"], g["ddt"], g["dA"],
                           g["dB"], g["dC"], g["dD"], g["d_init"], ws)
@@ -382,6 +385,21 @@ def run_ours(args, w, rank, world, local_rank):
     value = w.tokens * world / (ms_step * 1e-3)
     ssd.workspace_status(ws)
 
+    # ---------------- the forward alone, same inputs and timing
+    for _ in range(3):
+        fwd()
+    f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize()
+    f0.record(stream)
+    for _ in range(args.steps):
+        fwd()
+    f1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    fwd_ms = max_over_ranks(f0.elapsed_time(f1) / args.steps, world, dev)
+    ssd.workspace_status(ws)
+
     # the dominant kernel's live durations (timed region); the others from the pass above
     live = [ms for _, ms in timer.durations()]
     tot_k = sum(sum(v) for v in per.values())
@@ -414,6 +432,21 @@ def run_ours(args, w, rank, world, local_rank):
     roof["algorithmic_flops_per_launch"] = flops
     roof["algorithmic_bytes_per_launch"] = byts
     roof["traffic"] = ncu_traffic(top, w.name)
+
+    # the whole step against HBM: the kernels' algorithmic bytes summed over one
+    # step's launches, and the minimum (every leaf, dy and d_final read once per
+    # call, every output written once)
+    step_costs = kernel_costs(w, tc=not any(k.endswith("_simt") for k in pattern))
+    step_bytes = sum(step_costs.get(cost_key(k), (0.0, 0))[1] for k in pattern)
+    nb = lambda *ts: sum(t.numel() * t.element_size() for t in ts if t is not None)
+    leaves = nb(x, dt, A, B, C, D, init, vl)
+    min_bytes = (leaves + nb(y, fin)) + (leaves + nb(dy, dfin) + nb(*g.values()))
+    step_s = ms_step * 1e-3
+    step_roof = {"unit": "GB/s", "peak": peaks["hbm_gbs"],
+                 "algorithmic_bytes": step_bytes, "achieved": step_bytes / step_s / 1e9,
+                 "frac": step_bytes / step_s / 1e9 / peaks["hbm_gbs"],
+                 "minimum_bytes": min_bytes,
+                 "frac_of_minimum": min_bytes / step_s / 1e9 / peaks["hbm_gbs"]}
 
     # ---------------- end to end: pinned host buffers -> device -> host every step.
     # Every step's inputs cross to the device and its results cross back inside the
@@ -504,6 +537,9 @@ def run_ours(args, w, rank, world, local_rank):
                    "l2": f"inputs larger than L2 ({in_bytes / 1e6:.0f} MB > {L2_BYTES / 1e6:.0f} MB); no flush",
                    "step": "ssd_forward + ssd_backward (recompute), inputs resident in HBM"},
         "roofline": roof,
+        "step_roofline": step_roof,
+        "forward": {"value": w.tokens * world / (fwd_ms * 1e-3), "unit": UNIT,
+                    "ms_per_step": fwd_ms, "steps": args.steps},
         "kernels": {k: {kk: (round(vv, 4) if isinstance(vv, float) else vv) for kk, vv in s.items()}
                     for k, s in sorted(shares.items(), key=lambda kv: -kv[1]["share"])},
         "e2e": {"value": w.tokens * world / (e2e_ms * 1e-3), "unit": UNIT,
