@@ -63,6 +63,19 @@ def test_bf16_strong_decay(Q):
     padded_grads_zero(gpu, inp["valid_len"])
 
 
+def test_chunk_length_independence():
+    # the same inputs at chunk 64 (CUDA-core path), 128 and 256 (tensor-core path):
+    # chunking regroups the recurrence exactly, so each result meets the bar against
+    # the oracle and any two agree within the sum of their bars (triangle inequality)
+    inp = small(2, 700, 4, 64, 128, 2, seed=80, valid_len=[517, 700], bf16=True)
+    ref = run_oracle(inp)
+    outs = {Q: run_gpu(inp, "bf16", Q) for Q in (64, 128, 256)}
+    for Q, o in outs.items():
+        compare(o, ref, TOL["bf16"], f"Q={Q}")
+    compare(outs[128], outs[256], 2 * TOL["bf16"], "Q=128 vs Q=256")
+    compare(outs[64], outs[256], 2 * TOL["bf16"], "Q=64 vs Q=256")
+
+
 @pytest.mark.parametrize("N", [64, 128])
 def test_bf16_dstate(N):
     inp = small(1, 512, 2, 64, N, 1, seed=60 + N, bf16=True)
