@@ -48,6 +48,32 @@ def dist_env():
     return int(os.environ.get("RANK", "0")), ws, int(os.environ.get("LOCAL_RANK", "0"))
 
 
+def kernel_table(per: dict, top: str, live: list, steps: int, prof_steps: int, costs: dict,
+                 hbm_gbs: float) -> dict:
+    """Per-kernel entries of the benchmark line.  `per` maps a kernel name to its
+    event durations (ms) over `prof_steps` profiled steps, `live` holds the
+    dominant kernel's durations inside the timed region of `steps` steps.  Each
+    entry: launches in the timed region, mean duration (the live one for `top`),
+    share of the summed profiled time, the fraction of the HBM peak its
+    algorithmic bytes per launch reach at that duration, and whether it runs on
+    the library's second stream."""
+    tot = sum(sum(v) for v in per.values())
+    out = {}
+    for k, v in per.items():
+        e = {"launches": len(v) * steps // prof_steps, "avg_us": 1e3 * sum(v) / len(v),
+             "share": sum(v) / tot if tot else None}
+        if k == top:
+            e["avg_us"] = 1e3 * sum(live) / len(live)
+            e["timed_live"] = True
+        byts = costs.get(cost_key(k), (0.0, 0))[1]
+        if byts and e["avg_us"] > 0:
+            e["hbm_frac"] = byts / (e["avg_us"] * 1e-6) / 1e9 / hbm_gbs
+        if k in SECOND_STREAM:
+            e["second_stream"] = True
+        out[k] = e
+    return out
+
+
 def max_over_ranks(x: float, world: int, device=None) -> float:
     """The largest `x` over all ranks (the slowest rank's time); `x` itself on
     one rank.  `device` holds the reduction tensor: the rank's GPU under NCCL,
@@ -402,15 +428,10 @@ def run_ours(args, w, rank, world, local_rank):
 
     # the dominant kernel's live durations (timed region); the others from the pass above
     live = [ms for _, ms in timer.durations()]
-    tot_k = sum(sum(v) for v in per.values())
-    shares = {k: {"launches": len(v) * args.steps // prof_steps, "avg_us": 1e3 * sum(v) / len(v),
-                  "share": sum(v) / tot_k if tot_k else None} for k, v in per.items()}
-    for k in shares:
-        if k in SECOND_STREAM:
-            shares[k]["second_stream"] = True
-    shares[top]["avg_us"] = 1e3 * sum(live) / len(live)
-    shares[top]["timed_live"] = True
     peaks, peak_src = load_peaks()
+    shares = kernel_table(per, top, live, args.steps, prof_steps,
+                          kernel_costs(w, tc=not any(k.endswith("_simt") for k in pattern)),
+                          peaks["hbm_gbs"])
     costs = kernel_costs(w, tc=not top.endswith("_simt"))
     flops, byts = costs[cost_key(top)]
     avg_s = statistics.mean(live) * 1e-3
