@@ -31,13 +31,19 @@
  * rate used as given; dt is the already-discretised step used as given.
  *
  * Ownership and memory: every pointer is a DEVICE pointer owned by the
- * caller.  The library allocates no memory and keeps no state between calls;
- * scratch lives in the caller's `workspace`, sized by ssd_workspace_bytes().
+ * caller.  The library allocates no device memory and keeps no data between
+ * calls; scratch lives in the caller's `workspace`, sized by
+ * ssd_workspace_bytes().
  * Outputs are overwritten, never accumulated into.  Tensor pointers and the
  * workspace must be 16-byte aligned.
  *
  * Streams and errors: work is enqueued on `stream` (a cudaStream_t; NULL is
  * the legacy default stream) and the call returns without synchronising.
+ * The tensor-core path forks part of its kernels onto a second stream that
+ * the library creates once per device (non-blocking, with three events) and
+ * joins it back into `stream` before returning, so to the caller every call
+ * is ordered on `stream` as if all its kernels ran there; tensor-core calls
+ * from several host threads enqueue one at a time (a lock).
  * Argument errors are detected on the host and returned before anything is
  * enqueued.  Launch failures return SSD_ERR_CUDA.  Kernels that wait on a
  * shared-memory barrier give up after a bounded number of polls and record
