@@ -74,6 +74,30 @@ def kernel_table(per: dict, top: str, live: list, steps: int, prof_steps: int, c
     return out
 
 
+def roofline_entry(kernel: str, flops: float, byts: float, live_ms: float, alone_ms: float,
+                   peaks: dict) -> dict:
+    """The roofline object of the benchmark line for one kernel: its algorithmic
+    work per launch over its mean live launch time in the timed region
+    (`achieved`, `frac`), against the HBM peak, the sustained bf16 tensor peak
+    (when its flops per byte exceed the ridge) or the fp32 FFMA peak (CUDA-core
+    kernels); and the same over its mean time when it runs alone (`alone`)."""
+    ridge = peaks["bf16_tflops_sustained"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
+    if kernel.endswith("_simt") and flops > 0:
+        sm_mhz = peaks.get("sm_max_mhz", 2070.0)
+        bound, unit, work = "alu", "TFLOP/s", flops / 1e12
+        peak = 152 * 128 * 2 * sm_mhz * 1e6 / 1e12                    # fp32 FFMA TFLOP/s
+    elif flops > 0 and flops / max(byts, 1) > ridge:
+        bound, unit, work, peak = "tensor", "TFLOP/s", flops / 1e12, peaks["bf16_tflops_sustained"]
+    else:
+        bound, unit, work, peak = "hbm", "GB/s", byts / 1e9, peaks["hbm_gbs"]
+    achieved = work / (live_ms * 1e-3)
+    alone = work / (alone_ms * 1e-3)
+    return {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
+            "frac": achieved / peak, "kernel": kernel,
+            "algorithmic_flops_per_launch": flops, "algorithmic_bytes_per_launch": byts,
+            "alone": {"avg_us": 1e3 * alone_ms, "achieved": alone, "frac": alone / peak}}
+
+
 def max_over_ranks(x: float, world: int, device=None) -> float:
     """The largest `x` over all ranks (the slowest rank's time); `x` itself on
     one rank.  `device` holds the reduction tensor: the rank's GPU under NCCL,
@@ -434,24 +458,8 @@ def run_ours(args, w, rank, world, local_rank):
                           peaks["hbm_gbs"])
     costs = kernel_costs(w, tc=not top.endswith("_simt"))
     flops, byts = costs[cost_key(top)]
-    avg_s = statistics.mean(live) * 1e-3
-    ridge = peaks["bf16_tflops_sustained"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
-    if top.endswith("_simt") and flops > 0:
-        sm_mhz = peaks.get("sm_max_mhz", 2070.0)
-        alu_peak = 152 * 128 * 2 * sm_mhz * 1e6 / 1e12              # fp32 FFMA TFLOP/s
-        roof = {"bound": "alu", "achieved": flops / avg_s / 1e12, "peak": alu_peak,
-                "unit": "TFLOP/s"}
-    elif flops > 0 and flops / max(byts, 1) > ridge:
-        roof = {"bound": "tensor", "achieved": flops / avg_s / 1e12,
-                "peak": peaks["bf16_tflops_sustained"], "unit": "TFLOP/s"}
-    else:
-        roof = {"bound": "hbm", "achieved": byts / avg_s / 1e9, "peak": peaks["hbm_gbs"],
-                "unit": "GB/s"}
-    roof["frac"] = roof["achieved"] / roof["peak"]
-    roof["kernel"] = top
+    roof = roofline_entry(top, flops, byts, statistics.mean(live), statistics.mean(per[top]), peaks)
     roof["peak_source"] = f"{peak_src} (MEASURED_PEAKS.json)" if peak_src == "measured" else "fallback"
-    roof["algorithmic_flops_per_launch"] = flops
-    roof["algorithmic_bytes_per_launch"] = byts
     roof["traffic"] = ncu_traffic(top, w.name)
 
     # the whole step against HBM: the kernels' algorithmic bytes summed over one

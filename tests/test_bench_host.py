@@ -48,3 +48,29 @@ def test_every_launched_kernel_has_a_cost():
 
 def test_second_stream_names_are_launched_kernels():
     assert set(bench.SECOND_STREAM) <= launch_names()
+
+
+PEAKS = {"hbm_gbs": 6789.0, "bf16_tflops_sustained": 1691.0, "sm_max_mhz": 2070.0}
+
+
+def test_roofline_hbm_bound_live_and_alone():
+    # the ORANGE backward at the 2.7B layer: 528.5 MB and 43.1 GF per launch (below the
+    # ridge of ~249 flop/B), 219 us live beside the group chain, 176 us alone
+    r = bench.roofline_entry("bwd_orange_tc", 43.1e9, 528.5e6, 0.219, 0.176, PEAKS)
+    assert r["bound"] == "hbm" and r["unit"] == "GB/s" and r["peak"] == 6789.0
+    assert r["achieved"] == pytest.approx(528.5e6 / 219e-6 / 1e9)
+    assert r["frac"] == pytest.approx(r["achieved"] / 6789.0)
+    assert r["alone"]["avg_us"] == pytest.approx(176.0)
+    assert r["alone"]["frac"] == pytest.approx(528.5e6 / 176e-6 / 1e9 / 6789.0)
+    assert r["kernel"] == "bwd_orange_tc" and r["algorithmic_bytes_per_launch"] == 528.5e6
+
+
+def test_roofline_tensor_and_alu_bounds():
+    r = bench.roofline_entry("k_tc", 1e12, 1e9, 1.0, 0.5, PEAKS)       # 1000 flop/B > ridge
+    assert r["bound"] == "tensor" and r["unit"] == "TFLOP/s"
+    assert r["achieved"] == pytest.approx(1000.0) and r["alone"]["achieved"] == pytest.approx(2000.0)
+    assert r["frac"] == pytest.approx(1000.0 / 1691.0)
+    r = bench.roofline_entry("k_simt", 1e9, 1e9, 1.0, 1.0, PEAKS)     # CUDA-core kernel
+    assert r["bound"] == "alu" and r["peak"] == pytest.approx(152 * 128 * 2 * 2070e6 / 1e12)
+    r = bench.roofline_entry("k1_chunk_cumsum", 0.0, 1e7, 0.01, 0.01, PEAKS)
+    assert r["bound"] == "hbm" and r["achieved"] == pytest.approx(1000.0)
