@@ -163,6 +163,9 @@ def kernel_costs(w, tc: bool) -> dict:
         "bwd_group": (b * n * G * 4.0 * tri * N + b * n * H * 4.0 * Q * P * N,
                       2 * x_b + 2 * sts * st + 4 * bc_b + 2 * cum_b),
         "bwd_k1_chunk_cumsum": (0.0, 4 * cum_b + 8 * tok_h),
+        # debug check (SSD_FLAG_CHECK_FINITE, never timed): reads the backward's outputs,
+        # cumA, endA and the chunk states and their gradients once
+        "check_finite": (0.0, x_b + 4 * tok_h + 2 * bc_b + cum_b + 4 * b * H * n + 2 * sts * st),
     }
     return c
 

@@ -31,9 +31,11 @@
  * rate used as given; dt is the already-discretised step used as given.
  *
  * Ownership and memory: every pointer is a DEVICE pointer owned by the
- * caller.  The library allocates no device memory and keeps no data between
- * calls; scratch lives in the caller's `workspace`, sized by
- * ssd_workspace_bytes().
+ * caller.  Apart from one exception, the library allocates no device memory
+ * and keeps no data between calls; scratch lives in the caller's `workspace`,
+ * sized by ssd_workspace_bytes().  The exception is ssd_forward_noalloc (end
+ * of this file): its scratch is a fixed array of SSD_NOALLOC_SCRATCH_BYTES
+ * held on every GPU that loads the library, whose contents outlive each call.
  * Outputs are overwritten, never accumulated into.  Tensor pointers and the
  * workspace must be 16-byte aligned.
  *
@@ -45,10 +47,17 @@
  * is ordered on `stream` as if all its kernels ran there; tensor-core calls
  * from several host threads enqueue one at a time (a lock).
  * Argument errors are detected on the host and returned before anything is
- * enqueued.  Launch failures return SSD_ERR_CUDA.  Kernels that wait on a
- * shared-memory barrier give up after a bounded number of polls and record
- * SSD_ERR_TIMEOUT in a status word inside the workspace, readable with
- * ssd_workspace_status() after the stream has been synchronised.
+ * enqueued.  Launch failures return SSD_ERR_CUDA.  Three conditions can only be
+ * seen on the device; each call clears the first 16 bytes of its workspace
+ * (its status words) and the kernels record them there, readable with
+ * ssd_workspace_status() once the call's work has finished:
+ *   - a wait on a shared-memory barrier that gives up after its time limit
+ *     (SSD_ERR_TIMEOUT; the call's outputs are then undefined);
+ *   - valid_len entries outside [0, seqlen]: such an entry is clamped into the
+ *     range, the call completes with the clamped value, and the count of
+ *     clamped entries is reported (SSD_ERR_INVALID_ARG);
+ *   - with SSD_FLAG_CHECK_FINITE, NaN or infinite values in any output or in
+ *     the intermediates the call writes in full (SSD_ERR_NONFINITE).
  */
 #ifndef SSD_GB300_H
 #define SSD_GB300_H
@@ -66,7 +75,8 @@ typedef enum {
     SSD_ERR_UNSUPPORTED = 2,  /* shape outside the supported range (see ssd_supported) */
     SSD_ERR_WORKSPACE = 3,    /* workspace smaller than ssd_workspace_bytes() */
     SSD_ERR_CUDA = 4,         /* a CUDA call or kernel launch failed */
-    SSD_ERR_TIMEOUT = 5       /* a bounded device-side wait expired */
+    SSD_ERR_TIMEOUT = 5,      /* a bounded device-side wait expired */
+    SSD_ERR_NONFINITE = 6     /* SSD_FLAG_CHECK_FINITE found NaN / Inf values */
 } ssd_status;
 
 typedef enum {
@@ -78,6 +88,13 @@ typedef enum {
 #define SSD_FLAG_NONE 0u
 #define SSD_FLAG_SIMT 1u   /* SSD_BF16 only: use the CUDA-core kernels instead of
                               the tcgen05 tensor-core kernels for the contractions */
+#define SSD_FLAG_CHECK_FINITE 2u  /* debug: one extra kernel at the end of the call
+                              counts NaN / Inf elements of every output and of
+                              cumA, endA, the chunk states (and, in the backward,
+                              the chunk-state gradients); ssd_workspace_status then
+                              returns SSD_ERR_NONFINITE.  The page passes every
+                              intermediate of combined_backward through `san`;
+                              this flag is that check.  Off: no cost at all. */
 
 typedef struct {
     int64_t batch;      /* b  >= 1 */
@@ -103,8 +120,18 @@ ssd_status ssd_supported(const ssd_dims *dims, ssd_dtype dtype);
 size_t ssd_workspace_bytes(const ssd_dims *dims, ssd_dtype dtype, int backward);
 
 /* Forward: y (and optionally final_state).
+ * burn-mamba, "combined_backward.rs": the forward intermediates that its
+ * "RECOMPUTE FORWARD INTERMEDIATES" block rebuilds (K1 k1_ssd_chunk_cumsum,
+ * K2 k2_ssd_bmm, K3 k3_ssd_chunk_state_extended, K4 k4_ssd_state_passing)
+ * followed by the chunk scan whose pieces its "BLUE backward" (C times the
+ * chunk-input state, scaled by exp(cumA)), "ORANGE backward" (the causal
+ * C.B^T decay-weighted sum over earlier tokens, scaled by dt) and "SKIP
+ * backward" (D x) blocks differentiate.
  *   init_state   may be NULL (zeros);  valid_len may be NULL (= seqlen);
- *   final_state  may be NULL (not written). */
+ *   final_state  may be NULL (not written).
+ *   Errors: SSD_ERR_INVALID_ARG / _UNSUPPORTED / _WORKSPACE before any work is
+ *   enqueued; SSD_ERR_CUDA if a launch fails (work already enqueued by the
+ *   call may then have run).  Device-side conditions: ssd_workspace_status. */
 ssd_status ssd_forward(const ssd_dims *dims, ssd_dtype dtype,
                        const void *x, const float *dt, const float *A,
                        const void *B, const void *C, const float *D,
@@ -113,8 +140,16 @@ ssd_status ssd_forward(const ssd_dims *dims, ssd_dtype dtype,
                        void *workspace, size_t workspace_bytes, void *stream);
 
 /* Backward with recompute: gradients of <dy,y> + <d_final_state,final_state>.
+ * burn-mamba, "combined_backward.rs": the function combined_backward(d_y,
+ * d_final, x, dt, b, c, d, initial_state, a_decay) and its result struct
+ * CombinedGrads, whose fields d_x, d_dt, d_b, d_c, d_d, d_initial_state and
+ * d_a_decay are the outputs dx, ddt, dB, dC, dD, d_init_state and dA here
+ * (B and C per group instead of per head: their gradients are summed over the
+ * group's heads).  Like the page, it saves nothing from the forward: every
+ * intermediate is recomputed from the leaves.
  *   d_final_state may be NULL (zeros);  d_init_state may be NULL (not written).
- *   dA and dD are reduced over batch and time in a fixed order (deterministic). */
+ *   dA and dD are reduced over batch and time in a fixed order (deterministic).
+ *   Errors: as ssd_forward. */
 ssd_status ssd_backward(const ssd_dims *dims, ssd_dtype dtype,
                         const void *x, const float *dt, const float *A,
                         const void *B, const void *C, const float *D,
@@ -124,8 +159,11 @@ ssd_status ssd_backward(const ssd_dims *dims, ssd_dtype dtype,
                         float *d_init_state,
                         void *workspace, size_t workspace_bytes, void *stream);
 
-/* Reads (synchronously, on `stream`) the device status word that the last
- * call on this workspace left: SSD_OK or SSD_ERR_TIMEOUT. */
+/* Reads (synchronously, on `stream`) the status words that the last call on
+ * this workspace left and returns, in this order of precedence:
+ * SSD_ERR_TIMEOUT, SSD_ERR_NONFINITE (with the count in ssd_last_error()),
+ * SSD_ERR_INVALID_ARG for clamped valid_len entries (count in
+ * ssd_last_error()), else SSD_OK.  workspace_bytes must be >= 16. */
 ssd_status ssd_workspace_status(const void *workspace, size_t workspace_bytes, void *stream);
 
 /* ---- Diagnostics (no counterpart on the pages; used by the benchmark) ----
@@ -175,7 +213,11 @@ void ssd_profile_only(const char *name);
  *    enqueued.
  *  - First call per device: it looks up the array's device address for the
  *    current device (cudaGetSymbolAddress, which may load the library's code
- *    onto that device).  Make that first call before any stream capture.
+ *    onto that device).  Make that first call before any stream capture.  The
+ *    address is kept per CUDA context: after a device reset (a new primary
+ *    context) the next call looks it up again, and is again a first call.
+ *  - Status: the call's status words (see the file header) live at the start
+ *    of the array; read them with ssd_noalloc_status() on the same device.
  *  - Sharing: every call on a device uses the same array and leaves its
  *    contents behind; the call clears what must start at zero itself.  Calls
  *    whose GPU work overlaps (different streams, or different host threads
@@ -188,6 +230,12 @@ ssd_status ssd_forward_noalloc(const ssd_dims *dims, ssd_dtype dtype,
                                const void *B, const void *C, const float *D,
                                const float *init_state, const int32_t *valid_len,
                                void *y, float *final_state, void *stream);
+
+/* Status of the last ssd_forward_noalloc call on the current device, as
+ * ssd_workspace_status() reports it for a workspace (synchronises `stream`;
+ * allocates nothing).  SSD_ERR_INVALID_ARG with "no call yet" in
+ * ssd_last_error() if the array has not been used on this device. */
+ssd_status ssd_noalloc_status(void *stream);
 
 /* Static description of a status code. */
 const char *ssd_status_str(ssd_status status);

@@ -10,6 +10,7 @@
 #include <mutex>
 
 #include "ssd.h"
+#include "ssd_check.cuh"
 #include "ssd_internal.cuh"
 #include "ssd_tc.cuh"
 
@@ -121,7 +122,7 @@ Layout make_layout(const ssd_dims &d, ssd_dtype dt, bool backward) {
     lo.nslice_k3 = tc ? tc_k3_slices(d) : 1;
     size_t off = 0;
     auto take = [&](size_t bytes) { size_t o = off; off += align_up(bytes); return o; };
-    lo.status = take(16);
+    lo.status = take(sizeof(int) * kStatusWords);
     lo.cumA = take(4 * tok);
     lo.endA = take(4 * b * H * n);
     lo.CB = take(4 * b * n * G * Q * Q);
@@ -156,7 +157,8 @@ ssd_status validate_dims(const ssd_dims *d, ssd_dtype dt) {
     if (!d) return fail(SSD_ERR_INVALID_ARG, "dims is NULL");
     if (dt != SSD_F32 && dt != SSD_BF16) return fail(SSD_ERR_INVALID_ARG, "unknown dtype %d", (int)dt);
     if (d->reserved != 0) return fail(SSD_ERR_INVALID_ARG, "dims.reserved must be 0");
-    if (d->flags & ~(uint32_t)SSD_FLAG_SIMT) return fail(SSD_ERR_INVALID_ARG, "unknown flags 0x%x", d->flags);
+    if (d->flags & ~(uint32_t)(SSD_FLAG_SIMT | SSD_FLAG_CHECK_FINITE))
+        return fail(SSD_ERR_INVALID_ARG, "unknown flags 0x%x", d->flags);
     if (d->batch < 1 || d->seqlen < 1 || d->nheads < 1 || d->headdim < 1 || d->dstate < 1 ||
         d->ngroups < 1 || d->chunk_len < 1)
         return fail(SSD_ERR_INVALID_ARG, "every dimension must be >= 1");
@@ -266,9 +268,34 @@ ssd_status run_forward_chain(const Params &p, bool tc, bool write_final, cudaStr
     return SSD_OK;
 }
 
+// The SSD_FLAG_CHECK_FINITE regions shared by both calls: cumA, endA and the
+// chunk states (every element written by K1 / K3 / K4 on both paths).
+void add_intermediates(CheckList &l, const Params &p) {
+    const size_t nst = (size_t)p.b * p.n * p.H * p.P * p.N;
+    l.r[l.n++] = {p.cumA, (size_t)p.b * p.H * p.n * p.Q, 0};
+    l.r[l.n++] = {p.endA, (size_t)p.b * p.H * p.n, 0};
+    if (p.states) l.r[l.n++] = {p.states, nst, 0};
+    if (p.states_bf) l.r[l.n++] = {p.states_bf, nst, 1};
+}
+
 }  // namespace
 
 void record_error(const char *msg) { snprintf(g_last_error, sizeof(g_last_error), "%s", msg); }
+
+ssd_status read_status_words(const void *words, cudaStream_t s) {
+    int v[kStatusWords] = {0, 0, 0, 0};
+    SSD_TRY(cudaMemcpyAsync(v, words, sizeof(v), cudaMemcpyDeviceToHost, s));
+    SSD_TRY(cudaStreamSynchronize(s));
+    if (v[kStatusCode] == SSD_ERR_TIMEOUT) return fail(SSD_ERR_TIMEOUT, "a device-side wait gave up");
+    if (v[kStatusCode] != SSD_OK) return fail(SSD_ERR_CUDA, "unexpected device status %d", v[kStatusCode]);
+    if (v[kStatusNonFinite] > 0)
+        return fail(SSD_ERR_NONFINITE, "%d non-finite values in the call's outputs or intermediates",
+                    v[kStatusNonFinite]);
+    if (v[kStatusValidLen] > 0)
+        return fail(SSD_ERR_INVALID_ARG, "%d valid_len entries outside [0, seqlen] were clamped",
+                    v[kStatusValidLen]);
+    return SSD_OK;
+}
 
 }  // namespace ssd
 
@@ -288,6 +315,7 @@ const char *ssd_status_str(ssd_status st) {
         case SSD_ERR_WORKSPACE: return "workspace too small";
         case SSD_ERR_CUDA: return "CUDA error";
         case SSD_ERR_TIMEOUT: return "device-side wait timed out";
+        case SSD_ERR_NONFINITE: return "non-finite values found";
     }
     return "unknown status";
 }
@@ -326,7 +354,7 @@ ssd_status ssd_forward(const ssd_dims *dims, ssd_dtype dtype, const void *x, con
     p.valid_len = valid_len; p.y = y; p.final_state = final_state;
     cudaStream_t s = (cudaStream_t)stream;
     g_launches = 0;
-    SSD_TRY(cudaMemsetAsync(p.status, 0, sizeof(int), s));
+    SSD_TRY(cudaMemsetAsync(p.status, 0, sizeof(int) * kStatusWords, s));
     if (dtype == SSD_F32) {
         st = run_forward_chain<float>(p, false, true, s, nullptr);
         if (st != SSD_OK) return st;
@@ -347,6 +375,16 @@ ssd_status ssd_forward(const ssd_dims *dims, ssd_dtype dtype, const void *x, con
         } else {
             SSD_LAUNCH("k5_scan_simt", launch_simt_k5<bf16>(p, s), 1);
         }
+    }
+    if (dims->flags & SSD_FLAG_CHECK_FINITE) {
+        const size_t tokens = (size_t)p.b * p.L, xe = tokens * p.H * p.P;
+        const int bf = dtype == SSD_BF16;
+        CheckList l;
+        l.n = 0;
+        l.r[l.n++] = {y, xe, bf};
+        if (final_state) l.r[l.n++] = {final_state, (size_t)p.b * p.H * p.P * p.N, 0};
+        add_intermediates(l, p);
+        SSD_LAUNCH("check_finite", launch_check_finite(l, p.status + kStatusNonFinite, s), 1);
     }
     return SSD_OK;
 }
@@ -380,7 +418,7 @@ ssd_status ssd_backward(const ssd_dims *dims, ssd_dtype dtype, const void *x, co
     p.dA = dA; p.dB = dB; p.dC = dC; p.dD = dD; p.d_init = d_init_state;
     cudaStream_t s = (cudaStream_t)stream;
     g_launches = 0;
-    SSD_TRY(cudaMemsetAsync(p.status, 0, sizeof(int), s));
+    SSD_TRY(cudaMemsetAsync(p.status, 0, sizeof(int) * kStatusWords, s));
     if (dtype == SSD_F32) {
         st = run_forward_chain<float>(p, false, false, s, nullptr);
         if (st != SSD_OK) return st;
@@ -433,6 +471,24 @@ ssd_status ssd_backward(const ssd_dims *dims, ssd_dtype dtype, const void *x, co
             SSD_LAUNCH("bwd_k1_chunk_cumsum", launch_bwd_k1(p, s), 1);
         }
     }
+    if (dims->flags & SSD_FLAG_CHECK_FINITE) {
+        const size_t tokens = (size_t)p.b * p.L, xe = tokens * p.H * p.P, bce = tokens * p.G * p.N;
+        const size_t nst = (size_t)p.b * p.n * p.H * p.P * p.N;
+        const int bf = dtype == SSD_BF16;
+        CheckList l;
+        l.n = 0;
+        l.r[l.n++] = {dx, xe, bf};
+        l.r[l.n++] = {ddt, (size_t)p.b * p.H * p.L, 0};
+        l.r[l.n++] = {dA, (size_t)p.H, 0};
+        l.r[l.n++] = {dB, bce, bf};
+        l.r[l.n++] = {dC, bce, bf};
+        l.r[l.n++] = {dD, (size_t)p.H, 0};
+        if (d_init_state) l.r[l.n++] = {d_init_state, (size_t)p.b * p.H * p.P * p.N, 0};
+        add_intermediates(l, p);
+        if (p.dstates) l.r[l.n++] = {p.dstates, nst, 0};
+        if (p.dstates_bf) l.r[l.n++] = {p.dstates_bf, nst, 1};
+        SSD_LAUNCH("check_finite", launch_check_finite(l, p.status + kStatusNonFinite, s), 1);
+    }
     return SSD_OK;
 }
 
@@ -465,14 +521,9 @@ const char *ssd_profile_name(int i) {
 
 ssd_status ssd_workspace_status(const void *workspace, size_t workspace_bytes, void *stream) {
     g_last_error[0] = 0;
-    if (!workspace || workspace_bytes < 16) return fail(SSD_ERR_INVALID_ARG, "bad workspace");
-    int v = 0;
-    cudaStream_t s = (cudaStream_t)stream;
-    SSD_TRY(cudaMemcpyAsync(&v, workspace, sizeof(int), cudaMemcpyDeviceToHost, s));
-    SSD_TRY(cudaStreamSynchronize(s));
-    if (v == SSD_OK) return SSD_OK;
-    if (v == SSD_ERR_TIMEOUT) return fail(SSD_ERR_TIMEOUT, "a device-side wait gave up");
-    return fail(SSD_ERR_CUDA, "unexpected device status %d", v);
+    if (!workspace || workspace_bytes < sizeof(int) * kStatusWords)
+        return fail(SSD_ERR_INVALID_ARG, "bad workspace");
+    return read_status_words(workspace, (cudaStream_t)stream);
 }
 
 }  // extern "C"

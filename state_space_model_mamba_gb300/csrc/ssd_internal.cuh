@@ -11,6 +11,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "ssd.h"
+
 namespace ssd {
 
 typedef __nv_bfloat16 bf16;
@@ -52,10 +54,17 @@ struct Params {
     int nslice;
     int nslice_k5;       // head slices of the persistent per-group kernels (tensor-core path)
     int nslice_k3;       // head slices of the streaming K3 / BLUE kernels (tensor-core path)
-    int *status;         // device status word (SSD_OK / SSD_ERR_TIMEOUT)
+    int *status;         // device status words, kStatusWords ints (below)
 };
 
+// The workspace's status words (cleared by every call before its first kernel):
+//   [kStatusCode]      SSD_OK, or SSD_ERR_TIMEOUT once a bounded wait gave up
+//   [kStatusValidLen]  number of valid_len entries outside [0, seqlen] (clamped)
+//   [kStatusNonFinite] non-finite elements seen by the SSD_FLAG_CHECK_FINITE check
+constexpr int kStatusCode = 0, kStatusValidLen = 1, kStatusNonFinite = 2, kStatusWords = 4;
+
 // ---------------------------------------------------------------- small helpers
+// valid_len[bi] clamped to [0, L] (an entry outside is counted by K1, below).
 __device__ __forceinline__ int valid_len_of(const Params &p, int bi) {
     int V = p.L;
     if (p.valid_len) {
@@ -63,6 +72,13 @@ __device__ __forceinline__ int valid_len_of(const Params &p, int bi) {
         V = V < 0 ? 0 : (V > p.L ? p.L : V);
     }
     return V;
+}
+
+// True when valid_len[bi] lies outside [0, L] (the kernels then use the clamped value).
+__device__ __forceinline__ bool valid_len_out_of_range(const Params &p, int bi) {
+    if (!p.valid_len) return false;
+    const int V = p.valid_len[bi];
+    return V < 0 || V > p.L;
 }
 
 __device__ __forceinline__ float ldf(const float *a, size_t i) { return a[i]; }
@@ -113,6 +129,9 @@ __device__ __forceinline__ float block_sum(float v, float *red) {
 
 // Sets the message ssd_last_error() returns on the calling host thread.
 void record_error(const char *msg);
+// Reads kStatusWords device ints at `words` (synchronising `s`) and turns them
+// into the status ssd_workspace_status reports.
+ssd_status read_status_words(const void *words, cudaStream_t s);
 
 // ---------------------------------------------------------------- launchers
 // Shared by both execution paths (ssd_scan.cu).

@@ -15,7 +15,8 @@ namespace ssd {
 // chunk's Q tokens, 32 at a time with a running carry.  All of the warp's loads
 // are issued before the first scan step (Q <= 256: at most 8 per lane), so
 // their latencies overlap.  Tokens at or past the sample's valid length
-// contribute dt = 0.  (The grid has b*H*n*32 >= n_count threads, so the
+// contribute dt = 0; a valid_len entry outside [0, L] is clamped and counted
+// in the status words.  (The grid has b*H*n*32 >= n_count threads, so the
 // counter clear needs no extra launch.)
 __global__ void k1_chunk_cumsum(Params p) {
     const size_t gid = blockIdx.x * (size_t)blockDim.x + threadIdx.x;
@@ -27,6 +28,9 @@ __global__ void k1_chunk_cumsum(Params p) {
     if (warp >= p.b * p.H * p.n) return;
     const int c = warp % p.n, bh = warp / p.n, h = bh % p.H, bi = bh / p.H;
     const int V = valid_len_of(p, bi);
+    // one warp per sample reports a valid_len entry outside [0, L] (it is clamped)
+    if (h == 0 && c == 0 && lane == 0 && valid_len_out_of_range(p, bi))
+        atomicAdd(p.status + kStatusValidLen, 1);
     const float Ah = p.A[h];
     const float *dtrow = p.dt + ix_dt(p, bi, h, 0);
     float *out = p.cumA + (size_t)warp * p.Q;

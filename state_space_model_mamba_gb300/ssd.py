@@ -21,12 +21,15 @@ LIB_PATH = os.path.join(_PKG, "lib", "libssd.so")
 
 SSD_F32, SSD_BF16 = 0, 1
 SSD_FLAG_SIMT = 1
+SSD_FLAG_CHECK_FINITE = 2
+SSD_OK, SSD_ERR_INVALID_ARG, SSD_ERR_UNSUPPORTED, SSD_ERR_WORKSPACE = 0, 1, 2, 3
+SSD_ERR_CUDA, SSD_ERR_TIMEOUT, SSD_ERR_NONFINITE = 4, 5, 6
 STATUS = {0: "SSD_OK", 1: "SSD_ERR_INVALID_ARG", 2: "SSD_ERR_UNSUPPORTED",
-          3: "SSD_ERR_WORKSPACE", 4: "SSD_ERR_CUDA", 5: "SSD_ERR_TIMEOUT"}
+          3: "SSD_ERR_WORKSPACE", 4: "SSD_ERR_CUDA", 5: "SSD_ERR_TIMEOUT", 6: "SSD_ERR_NONFINITE"}
 EXPORTED = ("ssd_supported", "ssd_workspace_bytes", "ssd_forward", "ssd_backward",
             "ssd_workspace_status", "ssd_status_str", "ssd_last_error", "ssd_version",
             "ssd_last_launch_count", "ssd_profile_begin", "ssd_profile_end", "ssd_profile_name",
-            "ssd_profile_only")
+            "ssd_profile_only", "ssd_forward_noalloc", "ssd_noalloc_status")
 
 
 class SsdDims(ctypes.Structure):
@@ -83,6 +86,10 @@ def load_library(path: str | None = None):
         lib.ssd_profile_name.restype = ctypes.c_char_p
         lib.ssd_profile_only.argtypes = [ctypes.c_char_p]
         lib.ssd_profile_only.restype = None
+        lib.ssd_forward_noalloc.argtypes = [dims_p, i32] + [vp] * 10 + [vp]
+        lib.ssd_forward_noalloc.restype = i32
+        lib.ssd_noalloc_status.argtypes = [vp]
+        lib.ssd_noalloc_status.restype = i32
         if path is None:
             _lib = lib
         return lib
@@ -103,10 +110,12 @@ class Dims:
     ngroups: int
     chunk_len: int
     simt: bool = False
+    check_finite: bool = False
 
     def c(self) -> SsdDims:
+        flags = (SSD_FLAG_SIMT if self.simt else 0) | (SSD_FLAG_CHECK_FINITE if self.check_finite else 0)
         return SsdDims(self.batch, self.seqlen, self.nheads, self.headdim, self.dstate,
-                       self.ngroups, self.chunk_len, SSD_FLAG_SIMT if self.simt else 0, 0)
+                       self.ngroups, self.chunk_len, flags, 0)
 
 
 def _dtype_code(t: torch.Tensor) -> int:
@@ -117,10 +126,11 @@ def _dtype_code(t: torch.Tensor) -> int:
     raise TypeError(f"x must be float32 or bfloat16, got {t.dtype}")
 
 
-def dims_of(x: torch.Tensor, B: torch.Tensor, chunk_len: int, simt: bool = False) -> Dims:
+def dims_of(x: torch.Tensor, B: torch.Tensor, chunk_len: int, simt: bool = False,
+            check_finite: bool = False) -> Dims:
     b, L, H, P = x.shape
     G, N = B.shape[2], B.shape[3]
-    return Dims(b, L, H, P, N, G, int(chunk_len), simt)
+    return Dims(b, L, H, P, N, G, int(chunk_len), simt, check_finite)
 
 
 def supported(dims: Dims, dtype_code: int) -> bool:
@@ -187,31 +197,38 @@ def backward_into(dims: Dims, x, dt, A, B, C, D, init_state, valid_len, dy, d_fi
 
 
 def ssd_forward(x, dt, A, B, C, D, chunk_len, init_state=None, valid_len=None,
-                return_final_state=True, simt=False):
+                return_final_state=True, simt=False, check_finite=False, check_status=False):
     """Forward of the chunked selective scan.  Returns ``(y, final_state)``.
 
     x [b,L,H,P] (fp32 or bf16), dt [b,H,L] fp32, A [H] fp32, B/C [b,L,G,N]
     (x's dtype), D [H] fp32, init_state [b,H,P,N] fp32 or None,
-    valid_len int32 [b] or None.
+    valid_len int32 [b] or None.  ``check_finite`` sets SSD_FLAG_CHECK_FINITE;
+    with it or ``check_status`` the call synchronises and raises SsdError when
+    the device reported a condition (timeout, non-finite values, clamped
+    valid_len entries).
     """
     _check_inputs(x, dt, A, B, C, D, init_state, valid_len, x.dtype)
-    dims = dims_of(x, B, chunk_len, simt)
+    dims = dims_of(x, B, chunk_len, simt, check_finite)
     code = _dtype_code(x)
     y = torch.empty_like(x)
     fin = (torch.empty(x.shape[0], x.shape[2], x.shape[3], B.shape[3], device=x.device,
                        dtype=torch.float32) if return_final_state else None)
     ws = alloc_workspace(dims, code, False, x.device)
     forward_into(dims, x, dt, A, B, C, D, init_state, valid_len, y, fin, ws)
+    if check_finite or check_status:
+        workspace_status(ws)
     return y, fin
 
 
 def ssd_backward(x, dt, A, B, C, D, chunk_len, dy, d_final_state=None, init_state=None,
-                 valid_len=None, want_d_init=True, simt=False):
-    """Recompute backward.  Returns a dict with dx, ddt, dA, dB, dC, dD, d_init."""
+                 valid_len=None, want_d_init=True, simt=False, check_finite=False,
+                 check_status=False):
+    """Recompute backward.  Returns a dict with dx, ddt, dA, dB, dC, dD, d_init.
+    ``check_finite`` / ``check_status`` as in :func:`ssd_forward`."""
     _check_inputs(x, dt, A, B, C, D, init_state, valid_len, x.dtype)
     if tuple(dy.shape) != tuple(x.shape) or dy.dtype != x.dtype or not dy.is_contiguous():
         raise ValueError("dy must match x in shape and dtype and be contiguous")
-    dims = dims_of(x, B, chunk_len, simt)
+    dims = dims_of(x, B, chunk_len, simt, check_finite)
     code = _dtype_code(x)
     b, L, H, P = x.shape
     N = B.shape[3]
@@ -223,13 +240,23 @@ def ssd_backward(x, dt, A, B, C, D, chunk_len, dy, d_final_state=None, init_stat
     ws = alloc_workspace(dims, code, True, dev)
     backward_into(dims, x, dt, A, B, C, D, init_state, valid_len, dy, d_final_state, out["dx"],
                   out["ddt"], out["dA"], out["dB"], out["dC"], out["dD"], out["d_init"], ws)
+    if check_finite or check_status:
+        workspace_status(ws)
     return out
 
 
 def workspace_status(workspace: torch.Tensor) -> None:
-    """Raise if the last call on ``workspace`` recorded a device-side timeout."""
+    """Raise SsdError if the last call on ``workspace`` recorded a device-side
+    condition: a timeout, non-finite values (SSD_FLAG_CHECK_FINITE) or clamped
+    valid_len entries.  Synchronises the current stream."""
     _check(load_library().ssd_workspace_status(_ptr(workspace), workspace.numel(),
                                                _stream_ptr(workspace.device)))
+
+
+def noalloc_status(device=None) -> None:
+    """Raise SsdError if the last ssd_forward_noalloc call on the current
+    device recorded a device-side condition (as :func:`workspace_status`)."""
+    _check(load_library().ssd_noalloc_status(_stream_ptr(device)))
 
 
 def last_launch_count() -> int:

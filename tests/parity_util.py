@@ -52,10 +52,72 @@ def normrel(a, b):
     return float(np.linalg.norm(a - b) / max(np.linalg.norm(b), 1e-30))
 
 
-def compare(gpu, ref, tol, label=""):
+# A tile's normwise error is taken against max(its own reference norm, this
+# fraction of the root-mean-square reference norm of the tensor's tiles), so a
+# tile whose reference is nearly zero is judged against a typical tile's size
+# instead of its own.
+TILE_FLOOR = 0.1
+
+
+def _tile_view(key, a, chunk):
+    """Reshape one output into (tiles, elements per tile) without copying where
+    the sequence length is a multiple of the chunk.  Tiles: (b, chunk, head) of
+    y and dx; (b, head, chunk) of ddt; (b, chunk, group) of dB and dC; (b, head)
+    of final_state and d_init; one element of dA and dD."""
+    a = np.asarray(a, np.float64)
+    if key in ("dA", "dD"):
+        return a.reshape(-1, 1), None
+    if key in ("final_state", "d_init"):
+        return a.reshape(a.shape[0] * a.shape[1], -1), None
+    seq_axis = 2 if key == "ddt" else 1
+    L = a.shape[seq_axis]
+    n = -(-L // chunk)
+    if n * chunk != L:
+        pad = [(0, 0)] * a.ndim
+        pad[seq_axis] = (0, n * chunk - L)
+        a = np.pad(a, pad)
+    if key == "ddt":                          # [b, H, L] -> (b, H, n) tiles of Q
+        b, H = a.shape[:2]
+        return a.reshape(b * H * n, chunk), None
+    b, _, X, Y = a.shape                      # [b, L, X, Y] -> tiles (b, n, X) of Q x Y
+    return a.reshape(b, n, chunk, X, Y), (2, 4)
+
+
+def tile_errors(gpu_a, ref_a, key, chunk):
+    """Normwise relative error of every tile (see _tile_view), each against
+    max(tile reference norm, TILE_FLOOR x RMS tile reference norm)."""
+    g, axes = _tile_view(key, gpu_a, chunk)
+    r, _ = _tile_view(key, ref_a, chunk)
+    if axes is None:
+        num = np.sum((g - r) ** 2, axis=1)
+        den = np.sum(r ** 2, axis=1)
+    else:                                     # per batch entry, to bound the temporaries
+        num = np.stack([np.sum((g[i] - r[i]) ** 2, axis=(1, 3)) for i in range(g.shape[0])])
+        den = np.stack([np.sum(r[i] ** 2, axis=(1, 3)) for i in range(r.shape[0])])
+    num, den = num.ravel(), den.ravel()
+    floor = TILE_FLOOR ** 2 * max(float(np.mean(den)), 1e-60)
+    return np.sqrt(num / np.maximum(den, floor))
+
+
+def compare(gpu, ref, tol, label="", chunk=None):
+    """Normwise relative error of every output against the bar; with `chunk`,
+    also the normwise error of every tile (tile_errors) against the same bar,
+    so that one wrong tile of a large tensor cannot hide in the whole norm.
+    Returns {key: whole-tensor error} and, with `chunk`, {key + "/tile": worst
+    tile error}."""
     errs = {k: normrel(gpu[k], ref[k]) for k in OUT_KEYS if k in gpu and k in ref}
     bad = {k: v for k, v in errs.items() if not v <= tol}
     assert not bad, f"{label}: normwise rel. error above {tol}: {bad} (all: {errs})"
+    if chunk is not None:
+        worst = {}
+        for k in OUT_KEYS:
+            if k in gpu and k in ref:
+                te = tile_errors(gpu[k], ref[k], k, chunk)
+                i = int(np.argmax(te))
+                worst[k] = (float(te[i]), i)
+        bad = {k: v for k, v in worst.items() if not v[0] <= tol}
+        assert not bad, f"{label}: tile error above {tol} (key: (error, tile index)): {bad}"
+        errs.update({k + "/tile": v[0] for k, v in worst.items()})
     return errs
 
 

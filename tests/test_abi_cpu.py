@@ -39,8 +39,8 @@ def test_every_declared_symbol_is_exported(lib):
 
 def test_version_and_status_strings(lib):
     assert lib.ssd_version() >= 10000
-    for code in range(6):
-        assert lib.ssd_status_str(code)
+    for code in range(7):
+        assert lib.ssd_status_str(code) and lib.ssd_status_str(code) != b"unknown status"
     assert lib.ssd_status_str(99) == b"unknown status"
 
 
@@ -79,6 +79,20 @@ def test_workspace_sizes(lib):
 def test_supported_rejects(lib, kw, code):
     assert lib.ssd_supported(ctypes.byref(_dims(**kw)), ssd.SSD_BF16) == code
     assert lib.ssd_last_error()
+
+
+def test_flags_accepted(lib):
+    for flags in (ssd.SSD_FLAG_SIMT, ssd.SSD_FLAG_CHECK_FINITE, ssd.SSD_FLAG_SIMT | ssd.SSD_FLAG_CHECK_FINITE):
+        assert lib.ssd_supported(ctypes.byref(_dims(flags=flags)), ssd.SSD_BF16) == 0
+    # the check adds no workspace
+    base = lib.ssd_workspace_bytes(ctypes.byref(_dims()), ssd.SSD_BF16, 1)
+    chk = lib.ssd_workspace_bytes(ctypes.byref(_dims(flags=ssd.SSD_FLAG_CHECK_FINITE)), ssd.SSD_BF16, 1)
+    assert base == chk
+
+
+def test_status_query_arguments(lib):
+    assert lib.ssd_workspace_status(None, 1 << 20, None) == 1
+    assert lib.ssd_workspace_status(ctypes.c_void_p(0x10000), 8, None) == 1
 
 
 def test_supported_accepts_workloads(lib):

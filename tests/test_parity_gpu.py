@@ -1,12 +1,15 @@
 """GPU parity: the CUDA path (through the C ABI) against the fp64 CPU oracle,
 element by element, on seeded inputs.  Bars: normwise relative error <= 1e-4
 on the fp32 path and <= 2e-2 on the bf16 path, for y, final_state and every
-gradient; padded positions exactly 0."""
+gradient, both over each whole tensor and over each tile of it ((b, chunk,
+head) of y / dx, (b, head, chunk) of ddt, (b, chunk, group) of dB / dC, (b,
+head) of the states, one element of dA / dD); padded positions exactly 0."""
 import numpy as np
 import pytest
 
+from state_space_model_mamba_gb300 import ssd
 from state_space_model_mamba_gb300.inputs import WORKLOADS, generate, generate_small
-from parity_util import TOL, compare, padded_grads_zero, run_gpu, run_oracle
+from parity_util import TOL, compare, padded_grads_zero, run_gpu, run_oracle, to_device
 
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
@@ -22,14 +25,14 @@ def small(b, L, H, P, N, G, seed, valid_len=None, bf16=False, init_std=0.3, dt_m
 def test_fp32_small_ragged_grouped(Q):
     inp = small(2, 200, 4, 16, 32, 2, seed=40 + Q, valid_len=[150, 200])
     gpu = run_gpu(inp, "f32", Q)
-    compare(gpu, run_oracle(inp), TOL["f32"], f"f32 Q={Q}")
+    compare(gpu, run_oracle(inp), TOL["f32"], f"f32 Q={Q}", chunk=Q)
     padded_grads_zero(gpu, inp["valid_len"])
 
 
 def test_fp32_tiny_workload():
     w = WORKLOADS["tiny_f32"]
     inp = generate(w)
-    compare(run_gpu(inp, "f32", w.chunk_len), run_oracle(inp), TOL["f32"], "tiny")
+    compare(run_gpu(inp, "f32", w.chunk_len), run_oracle(inp), TOL["f32"], "tiny", chunk=w.chunk_len)
 
 
 # ---------------------------------------------------------------- bf16 path
@@ -38,7 +41,7 @@ def test_fp32_tiny_workload():
 def test_bf16_small_ragged_grouped(Q, simt):
     inp = small(2, 700, 4, 64, 128, 2, seed=50 + Q, valid_len=[517, 700], bf16=True)
     gpu = run_gpu(inp, "bf16", Q, simt=simt)
-    compare(gpu, run_oracle(inp), TOL["bf16"], f"bf16 Q={Q} simt={simt}")
+    compare(gpu, run_oracle(inp), TOL["bf16"], f"bf16 Q={Q} simt={simt}", chunk=Q)
     padded_grads_zero(gpu, inp["valid_len"])
 
 
@@ -47,7 +50,7 @@ def test_bf16_q128_several_heads_per_cta():
     # heads (the small cases above give each CTA one head), ragged and grouped
     inp = small(2, 8192, 8, 64, 128, 2, seed=58, valid_len=[8192, 5000], bf16=True)
     gpu = run_gpu(inp, "bf16", 128)
-    compare(gpu, run_oracle(inp), TOL["bf16"], "bf16 Q=128 multi-head")
+    compare(gpu, run_oracle(inp), TOL["bf16"], "bf16 Q=128 multi-head", chunk=128)
     padded_grads_zero(gpu, inp["valid_len"])
 
 
@@ -59,7 +62,7 @@ def test_bf16_strong_decay(Q):
     # rest stay below it (factored path), mixed within single heads
     inp = small(2, 700, 4, 64, 128, 2, seed=70 + Q, valid_len=[517, 700], bf16=True, dt_mu=0.5)
     gpu = run_gpu(inp, "bf16", Q)
-    compare(gpu, run_oracle(inp), TOL["bf16"], f"bf16 strong decay Q={Q}")
+    compare(gpu, run_oracle(inp), TOL["bf16"], f"bf16 strong decay Q={Q}", chunk=Q)
     padded_grads_zero(gpu, inp["valid_len"])
 
 
@@ -71,7 +74,7 @@ def test_chunk_length_independence():
     ref = run_oracle(inp)
     outs = {Q: run_gpu(inp, "bf16", Q) for Q in (64, 128, 256)}
     for Q, o in outs.items():
-        compare(o, ref, TOL["bf16"], f"Q={Q}")
+        compare(o, ref, TOL["bf16"], f"Q={Q}", chunk=256)
     compare(outs[128], outs[256], 2 * TOL["bf16"], "Q=128 vs Q=256")
     compare(outs[64], outs[256], 2 * TOL["bf16"], "Q=64 vs Q=256")
 
@@ -79,14 +82,14 @@ def test_chunk_length_independence():
 @pytest.mark.parametrize("N", [64, 128])
 def test_bf16_dstate(N):
     inp = small(1, 512, 2, 64, N, 1, seed=60 + N, bf16=True)
-    compare(run_gpu(inp, "bf16", 256), run_oracle(inp), TOL["bf16"], f"bf16 N={N}")
+    compare(run_gpu(inp, "bf16", 256), run_oracle(inp), TOL["bf16"], f"bf16 N={N}", chunk=256)
 
 
 # ---------------------------------------------------------------- edge cases
 def test_edge_single_token_and_empty_sample():
     inp = small(3, 1, 2, 8, 8, 1, seed=70, valid_len=[1, 0, 1])
     gpu = run_gpu(inp, "f32", 16)
-    compare(gpu, run_oracle(inp), TOL["f32"], "L=1")
+    compare(gpu, run_oracle(inp), TOL["f32"], "L=1", chunk=16)
     assert np.all(gpu["y"][1] == 0) and np.all(gpu["dx"][1] == 0)
     # an empty sample passes the initial state through and its gradient back
     np.testing.assert_allclose(gpu["final_state"][1], inp["init"][1], rtol=0, atol=0)
@@ -95,14 +98,14 @@ def test_edge_single_token_and_empty_sample():
 
 def test_edge_seqlen_below_chunk():
     inp = small(2, 37, 2, 64, 64, 1, seed=71, bf16=True)
-    compare(run_gpu(inp, "bf16", 256), run_oracle(inp), TOL["bf16"], "L<Q")
+    compare(run_gpu(inp, "bf16", 256), run_oracle(inp), TOL["bf16"], "L<Q", chunk=256)
 
 
 def test_edge_all_padding_chunks_skipped():
     # second sample valid for one token: whole chunks past valid_len
     inp = small(2, 1024, 2, 64, 128, 1, seed=72, valid_len=[1024, 1], bf16=True)
     gpu = run_gpu(inp, "bf16", 256)
-    compare(gpu, run_oracle(inp), TOL["bf16"], "valid_len=1")
+    compare(gpu, run_oracle(inp), TOL["bf16"], "valid_len=1", chunk=256)
     padded_grads_zero(gpu, inp["valid_len"])
 
 
@@ -120,6 +123,104 @@ def test_workload_full_size(name):
     w = WORKLOADS[name]
     inp = generate(w)
     gpu = run_gpu(inp, w.dtype, w.chunk_len)
-    errs = compare(gpu, run_oracle(inp), TOL[w.dtype], name)
+    errs = compare(gpu, run_oracle(inp), TOL[w.dtype], name, chunk=w.chunk_len)
     padded_grads_zero(gpu, inp["valid_len"])
     print(name, {k: f"{v:.2e}" for k, v in errs.items()})
+
+
+# ---------------------------------------------------------------- degenerate values of the method
+# The ORANGE backward folds dt into its operand and recovers ddt by a division,
+# and the decay factors are split through pivots: exact zeros, tiny steps and a
+# head without decay exercise each on the tensor-core path (P = 64, N = 128,
+# Q = 256), against the oracle.
+def _degenerate(kind, seed):
+    inp = small(2, 700, 4, 64, 128, 2, seed=seed, valid_len=[517, 700], bf16=True)
+    rng = np.random.default_rng(seed + 1)
+    if kind in ("dt_zero", "dt_tiny"):
+        pick = rng.random(inp["dt"].shape) < 0.05
+        if kind == "dt_zero":
+            inp["dt"][pick] = 0.0
+        else:
+            inp["dt"][pick] = (10.0 ** rng.uniform(-30.0, -20.0, size=int(pick.sum()))).astype(np.float32)
+    elif kind == "A_zero":
+        inp["A"][1] = 0.0
+    return inp
+
+
+@pytest.mark.parametrize("kind", ["dt_zero", "dt_tiny", "A_zero"])
+def test_degenerate_values_tensor_cores(kind):
+    inp = _degenerate(kind, seed={"dt_zero": 120, "dt_tiny": 121, "A_zero": 122}[kind])
+    gpu = run_gpu(inp, "bf16", 256)
+    errs = compare(gpu, run_oracle(inp), TOL["bf16"], kind, chunk=256)
+    padded_grads_zero(gpu, inp["valid_len"])
+    for k, v in gpu.items():
+        assert np.isfinite(v).all(), k
+    print(kind, {k: f"{v:.2e}" for k, v in errs.items()})
+
+
+# ---------------------------------------------------------------- device-side status
+def _status_case(seed=130, valid_len=None):
+    inp = small(2, 300, 4, 64, 128, 2, seed=seed, valid_len=valid_len, bf16=True)
+    return to_device(inp, "bf16")
+
+
+def test_status_words_map_to_codes():
+    """The status words at the start of a workspace turn into the documented
+    codes, in order of precedence (timeout, non-finite, clamped valid_len)."""
+    ws = torch.zeros(1024, dtype=torch.uint8, device="cuda")
+    words = ws[:16].view(torch.int32)
+    ssd.workspace_status(ws)                                   # all clear
+    for vals, code, text in [((0, 3, 0, 0), ssd.SSD_ERR_INVALID_ARG, "clamped"),
+                             ((0, 3, 7, 0), ssd.SSD_ERR_NONFINITE, "7 non-finite"),
+                             ((5, 3, 7, 0), ssd.SSD_ERR_TIMEOUT, "gave up")]:
+        words.copy_(torch.tensor(vals, dtype=torch.int32))
+        with pytest.raises(ssd.SsdError) as e:
+            ssd.workspace_status(ws)
+        assert e.value.code == code and text in str(e.value)
+
+
+@pytest.mark.parametrize("simt", [False, True])
+def test_check_finite_flags_nan_input(simt):
+    d = _status_case()
+    # clean inputs: the check runs (one more launch) and finds nothing
+    ssd.ssd_forward(d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"], 256, simt=simt, check_finite=True)
+    n_clean = ssd.last_launch_count()
+    ssd.ssd_backward(d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"], 256, d["dy"], simt=simt,
+                     check_finite=True)
+    ssd.ssd_forward(d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"], 256, simt=simt)
+    assert ssd.last_launch_count() == n_clean - 1
+    # one NaN in x reaches y and dx: the flag reports it, nothing else changes
+    x = d["x"].clone()
+    x[0, 5, 1, 3] = float("nan")
+    with pytest.raises(ssd.SsdError) as e:
+        ssd.ssd_forward(x, d["dt"], d["A"], d["B"], d["C"], d["D"], 256, simt=simt, check_finite=True)
+    assert e.value.code == ssd.SSD_ERR_NONFINITE
+    with pytest.raises(ssd.SsdError) as e:
+        ssd.ssd_backward(x, d["dt"], d["A"], d["B"], d["C"], d["D"], 256, d["dy"], simt=simt,
+                         check_finite=True)
+    assert e.value.code == ssd.SSD_ERR_NONFINITE
+    # without the flag the same call reports nothing
+    ssd.ssd_forward(x, d["dt"], d["A"], d["B"], d["C"], d["D"], 256, simt=simt, check_status=True)
+
+
+def test_valid_len_out_of_range_is_clamped_and_reported():
+    L = 300
+    d = _status_case(valid_len=[L, 120])
+    over = torch.tensor([L + 5, -3], dtype=torch.int32, device="cuda")
+    clamped = torch.tensor([L, 0], dtype=torch.int32, device="cuda")
+    args = (d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"], 256)
+    with pytest.raises(ssd.SsdError) as e:
+        ssd.ssd_forward(*args, valid_len=over, check_status=True)
+    assert e.value.code == ssd.SSD_ERR_INVALID_ARG and "2 valid_len entries" in str(e.value)
+    with pytest.raises(ssd.SsdError) as e:
+        ssd.ssd_backward(*args, d["dy"], valid_len=over, check_status=True)
+    assert e.value.code == ssd.SSD_ERR_INVALID_ARG
+    # the call still completes, with the clamped lengths
+    y1, f1 = ssd.ssd_forward(*args, valid_len=over)
+    y2, f2 = ssd.ssd_forward(*args, valid_len=clamped, check_status=True)
+    g1 = ssd.ssd_backward(*args, d["dy"], valid_len=over)
+    g2 = ssd.ssd_backward(*args, d["dy"], valid_len=clamped, check_status=True)
+    torch.cuda.synchronize()
+    assert torch.equal(y1, y2) and torch.equal(f1, f2)
+    for k in g1:
+        assert torch.equal(g1[k], g2[k]), k

@@ -67,6 +67,7 @@ def test_noalloc_forward_matches_ssd_forward_twice(dtype, shape, Q, valid):
         rc = fn(ctypes.byref(dims), code, ptr(d["x"]), ptr(d["dt"]), ptr(d["A"]), ptr(d["B"]),
                 ptr(d["C"]), ptr(d["D"]), ptr(d["init"]), ptr(d["valid_len"]), ptr(y), ptr(fin), stream)
         assert rc == 0, lib.ssd_last_error().decode()
+        ssd.noalloc_status()                     # the call's status words: nothing recorded
         torch.cuda.synchronize()
         ey = normrel(y.double().cpu().numpy(), y_ref.double().cpu().numpy())
         ef = normrel(fin.double().cpu().numpy(), f_ref.double().cpu().numpy())
