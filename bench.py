@@ -7,12 +7,16 @@ seqlen 8192, nheads 80, headdim 64, dstate 128, ngroups 1, chunk 256; bf16
 x/B/C/dy, fp32 dt/A/D), synthetic seeded inputs resident in HBM.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME] [--profile-case forward|step]
 
 Prints one JSON line (rank 0).  Under torchrun (N > 1) every rank runs an
 independent replica of the workload (the scan has no data-path exchange) and
 `value` is the tokens all ranks processed divided by the slowest rank's time.
 `--impl reference` times the CPU oracle (plain fp64 recurrence) on the host
-cores on a bounded sample of the same workload.
+cores on a bounded sample of the same workload.  `--profile-case` is the
+light run that ncu captures are taken on: W + K forward calls (or whole
+steps) on resident inputs, then a short line; no per-kernel pass, no end-to-end
+leg, no CPU baseline.
 """
 from __future__ import annotations
 
@@ -349,6 +353,54 @@ def run_reference(args, w, rank, world):
     }
 
 
+def run_profile_case(args, w, local_rank):
+    """W warm-up and K timed forward calls (or fwd + bwd steps) on resident
+    inputs, for ncu captures: nothing else is launched."""
+    import torch
+
+    from state_space_model_mamba_gb300 import ssd
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    inp = generate(w)
+    bf = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+
+    def up(a, dt=torch.float32):
+        return None if a is None else torch.from_numpy(np.ascontiguousarray(a)).to(dev, dt)
+
+    x, B, C, dy = up(inp["x"], bf), up(inp["B"], bf), up(inp["C"], bf), up(inp["dy"], bf)
+    dt, A, D, init, dfin = up(inp["dt"]), up(inp["A"]), up(inp["D"]), up(inp["init"]), up(inp["d_final"])
+    vl = None if inp["valid_len"] is None else torch.from_numpy(inp["valid_len"]).to(dev)
+    dims = ssd.dims_of(x, B, w.chunk_len)
+    code = ssd.SSD_BF16 if w.dtype == "bf16" else ssd.SSD_F32
+    bwd = args.profile_case == "step"
+    ws = ssd.alloc_workspace(dims, code, bwd, dev)
+    y = torch.empty_like(x)
+    fin = torch.empty(w.batch, w.nheads, w.headdim, w.dstate, device=dev)
+    g = dict(dx=torch.empty_like(x), ddt=torch.empty_like(dt), dA=torch.empty_like(A),
+             dB=torch.empty_like(B), dC=torch.empty_like(C), dD=torch.empty_like(D),
+             d_init=torch.empty_like(fin))
+
+    def one():
+        ssd.forward_into(dims, x, dt, A, B, C, D, init, vl, y, fin, ws)
+        if bwd:
+            ssd.backward_into(dims, x, dt, A, B, C, D, init, vl, dy, dfin, g["dx"], g["ddt"], g["dA"],
+                              g["dB"], g["dC"], g["dD"], g["d_init"], ws)
+
+    for _ in range(args.warmup):
+        one()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        one()
+    e1.record()
+    torch.cuda.synchronize()
+    ssd.workspace_status(ws)
+    ms = e0.elapsed_time(e1) / args.steps
+    return {"profile_case": args.profile_case, "workload": w.name, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_call": ms, "device_bytes": torch.cuda.max_memory_allocated(dev)}
+
+
 def run_ours(args, w, rank, world, local_rank):
     import torch
     import torch.distributed as dist
@@ -572,6 +624,10 @@ def run_ours(args, w, rank, world, local_rank):
         "step_roofline": step_roof,
         "forward": {"value": w.tokens * world / (fwd_ms * 1e-3), "unit": UNIT,
                     "ms_per_step": fwd_ms, "steps": args.steps},
+        "valid_tokens": (None if inp["valid_len"] is None else {
+            "per_step": int(np.sum(inp["valid_len"])) * world,
+            "value": int(np.sum(inp["valid_len"])) * world / (ms_step * 1e-3), "unit": UNIT,
+            "forward_value": int(np.sum(inp["valid_len"])) * world / (fwd_ms * 1e-3)}),
         "kernels": {k: {kk: (round(vv, 4) if isinstance(vv, float) else vv) for kk, vv in s.items()}
                     for k, s in sorted(shares.items(), key=lambda kv: -kv[1]["share"])},
         "e2e": {"value": w.tokens * world / (e2e_ms * 1e-3), "unit": UNIT,
@@ -595,6 +651,8 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--profile-case", choices=("forward", "step"), default=None,
+                    help="light run for ncu captures (see the module docstring)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -607,6 +665,11 @@ def main():
         if backend == "nccl":
             torch.cuda.set_device(local_rank)
         dist.init_process_group(backend=backend)
+    if args.profile_case:
+        if world > 1:
+            ap.error("--profile-case runs on one GPU")
+        print(json.dumps(run_profile_case(args, w, local_rank)), flush=True)
+        return
     if args.impl == "reference":
         line = run_reference(args, w, rank, world)
     else:

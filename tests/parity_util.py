@@ -59,14 +59,20 @@ def normrel(a, b):
 TILE_FLOOR = 0.1
 
 
+# Outputs checked tile by tile.  dA and dD are not: each entry is a sum over
+# the whole batch and sequence of terms that largely cancel (the two sides of
+# the d cumA identity), so one entry's relative error reflects that
+# cancellation, not a local mistake; a wholly wrong entry still moves the
+# whole-tensor norm of these [H] vectors far past the bar.
+TILED_KEYS = ("y", "final_state", "dx", "ddt", "dB", "dC", "d_init")
+
+
 def _tile_view(key, a, chunk):
     """Reshape one output into (tiles, elements per tile) without copying where
     the sequence length is a multiple of the chunk.  Tiles: (b, chunk, head) of
     y and dx; (b, head, chunk) of ddt; (b, chunk, group) of dB and dC; (b, head)
-    of final_state and d_init; one element of dA and dD."""
+    of final_state and d_init."""
     a = np.asarray(a, np.float64)
-    if key in ("dA", "dD"):
-        return a.reshape(-1, 1), None
     if key in ("final_state", "d_init"):
         return a.reshape(a.shape[0] * a.shape[1], -1), None
     seq_axis = 2 if key == "ddt" else 1
@@ -110,7 +116,7 @@ def compare(gpu, ref, tol, label="", chunk=None):
     assert not bad, f"{label}: normwise rel. error above {tol}: {bad} (all: {errs})"
     if chunk is not None:
         worst = {}
-        for k in OUT_KEYS:
+        for k in TILED_KEYS:
             if k in gpu and k in ref:
                 te = tile_errors(gpu[k], ref[k], k, chunk)
                 i = int(np.argmax(te))

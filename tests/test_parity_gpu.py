@@ -3,7 +3,7 @@ element by element, on seeded inputs.  Bars: normwise relative error <= 1e-4
 on the fp32 path and <= 2e-2 on the bf16 path, for y, final_state and every
 gradient, both over each whole tensor and over each tile of it ((b, chunk,
 head) of y / dx, (b, head, chunk) of ddt, (b, chunk, group) of dB / dC, (b,
-head) of the states, one element of dA / dD); padded positions exactly 0."""
+head) of the states; dA and dD whole); padded positions exactly 0."""
 import numpy as np
 import pytest
 
