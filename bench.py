@@ -148,8 +148,13 @@ def kernel_costs(w, tc: bool) -> dict:
         "k2_cb": (2.0 * b * n * G * tri * N, 2 * bc_b + cb_b * (2 if tc else 1)),   # CB and CB^T on tc
         "k3_state": (2.0 * b * n * H * Q * P * N, x_b + bc_b + 4 * tok_h + cum_b + sts * st),
         "k4_state_passing": (2.0 * st, 2 * sts * st + 4 * b * H * n),
-        "k5_scan": (b * n * H * (2.0 * Q * P * N + 2.0 * tri * P),
-                    2 * x_b + bc_b + cb_b + sts * st + cum_b + 4 * tok_h),
+        # fused K1 + K3 + K4 (tensor-core path): reads x, B, dt (and init), writes cumA, endA,
+        # the bf16 chunk-input states (and the final state); the intra states stay on chip
+        "state_scan": (2.0 * b * n * H * Q * P * N + 2.0 * st,
+                       x_b + bc_b + 4 * tok_h + cum_b + 4 * b * H * n + sts * st + 2 * 4 * b * H * P * N),
+        # K5; on the tensor-core path it computes CB itself (K2's flops, B read instead of CB)
+        "k5_scan": (b * n * H * (2.0 * Q * P * N + 2.0 * tri * P) + (2.0 * b * n * G * tri * N if tc else 0.0),
+                    2 * x_b + bc_b + (bc_b if tc else cb_b) + sts * st + cum_b + 4 * tok_h),
         "bwd_blue": (b * n * H * 4.0 * Q * P * N, x_b + bc_b + 2 * sts * st + 2 * cum_b),
         "bwd_k4_state_passing": (4.0 * st, 3 * sts * st + 4 * b * H * n),
         "bwd_main": (b * n * H * (4.0 * tri * P + 2.0 * Q * P * N),
@@ -370,7 +375,7 @@ def run_profile_case(args, w, local_rank):
     x, B, C, dy = up(inp["x"], bf), up(inp["B"], bf), up(inp["C"], bf), up(inp["dy"], bf)
     dt, A, D, init, dfin = up(inp["dt"]), up(inp["A"]), up(inp["D"]), up(inp["init"]), up(inp["d_final"])
     vl = None if inp["valid_len"] is None else torch.from_numpy(inp["valid_len"]).to(dev)
-    dims = ssd.dims_of(x, B, w.chunk_len)
+    dims = ssd.dims_of(x, B, w.chunk_len, split_scan=args.split_scan)
     code = ssd.SSD_BF16 if w.dtype == "bf16" else ssd.SSD_F32
     bwd = args.profile_case == "step"
     ws = ssd.alloc_workspace(dims, code, bwd, dev)
@@ -419,7 +424,7 @@ def run_ours(args, w, rank, world, local_rank):
     dt, A, D = up(inp["dt"]), up(inp["A"]), up(inp["D"])
     init, dfin = up(inp["init"]), up(inp["d_final"])
     vl = None if inp["valid_len"] is None else torch.from_numpy(inp["valid_len"]).to(dev)
-    dims = ssd.dims_of(x, B, w.chunk_len)
+    dims = ssd.dims_of(x, B, w.chunk_len, split_scan=args.split_scan)
     code = ssd.SSD_BF16 if w.dtype == "bf16" else ssd.SSD_F32
     ws = torch.empty(max(ssd.workspace_bytes(dims, code, True),
                          ssd.workspace_bytes(dims, code, False)), dtype=torch.uint8, device=dev)
@@ -619,7 +624,8 @@ def run_ours(args, w, rank, world, local_rank):
         "config": {"workload": w.name, **w.dims(),
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "l2": f"inputs larger than L2 ({in_bytes / 1e6:.0f} MB > {L2_BYTES / 1e6:.0f} MB); no flush",
-                   "step": "ssd_forward + ssd_backward (recompute), inputs resident in HBM"},
+                   "step": "ssd_forward + ssd_backward (recompute), inputs resident in HBM",
+                   "chunk_states": "split (K3 + K4)" if args.split_scan else "library default"},
         "roofline": roof,
         "step_roofline": step_roof,
         "forward": {"value": w.tokens * world / (fwd_ms * 1e-3), "unit": UNIT,
@@ -650,6 +656,8 @@ def main():
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--split-scan", action="store_true",
+                    help="chunk states by the chunk-parallel K3 and a separate K4 pass (SSD_FLAG_SPLIT_SCAN)")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--profile-case", choices=("forward", "step"), default=None,
                     help="light run for ncu captures (see the module docstring)")

@@ -88,6 +88,13 @@ typedef enum {
 #define SSD_FLAG_NONE 0u
 #define SSD_FLAG_SIMT 1u   /* SSD_BF16 only: use the CUDA-core kernels instead of
                               the tcgen05 tensor-core kernels for the contractions */
+#define SSD_FLAG_SPLIT_SCAN 4u     /* tensor-core path: compute the chunk states
+                              with the chunk-parallel K3 and a separate K4 pass
+                              (the intra-chunk states round-trip through the
+                              workspace) even where the fused chunk-state scan,
+                              which carries the state on chip along each (b, h)
+                              chain, would be chosen; the scan is chosen when
+                              batch * nheads >= 64.  Same results up to rounding. */
 #define SSD_FLAG_CHECK_FINITE 2u  /* debug: one extra kernel at the end of the call
                               counts NaN / Inf elements of every output and of
                               cumA, endA, the chunk states (and, in the backward,

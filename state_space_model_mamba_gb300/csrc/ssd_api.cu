@@ -105,6 +105,14 @@ bool use_tensor_cores(const ssd_dims &d, ssd_dtype dt) {
     return dt == SSD_BF16 && !(d.flags & SSD_FLAG_SIMT) && tc_supported(d.headdim, d.dstate, d.chunk_len);
 }
 
+// The fused chunk-state scan (K1 + K3 + K4, one CTA per (b, head pair) walking
+// the chunks in order) needs enough (b, h) chains to fill the GPU; with few,
+// long chains the chunk-parallel K3 and the separate K4 pass are faster.
+constexpr long long kMinScanChains = 64;
+bool use_fused_scan(const Params &p, const ssd_dims &d) {
+    return !(d.flags & SSD_FLAG_SPLIT_SCAN) && (long long)p.b * p.H >= kMinScanChains;
+}
+
 Layout make_layout(const ssd_dims &d, ssd_dtype dt, bool backward) {
     Layout lo;
     memset(&lo, 0, sizeof(lo));
@@ -125,7 +133,9 @@ Layout make_layout(const ssd_dims &d, ssd_dtype dt, bool backward) {
     lo.status = take(sizeof(int) * kStatusWords);
     lo.cumA = take(4 * tok);
     lo.endA = take(4 * b * H * n);
-    lo.CB = take(4 * b * n * G * Q * Q);
+    // CB: fp32 on the CUDA-core path; bf16 CB and CB^T on the tensor-core path, where
+    // only the backward stores them (the forward's K5 computes CB itself)
+    lo.CB = (tc && !backward) ? 0 : take(4 * b * n * G * Q * Q);
     // chunk states: fp32 on the CUDA-core path, bf16 only on the tensor-core path
     lo.states = tc ? 0 : take(4 * nst);
     lo.states_bf = tc ? take(2 * nst) : 0;
@@ -157,7 +167,7 @@ ssd_status validate_dims(const ssd_dims *d, ssd_dtype dt) {
     if (!d) return fail(SSD_ERR_INVALID_ARG, "dims is NULL");
     if (dt != SSD_F32 && dt != SSD_BF16) return fail(SSD_ERR_INVALID_ARG, "unknown dtype %d", (int)dt);
     if (d->reserved != 0) return fail(SSD_ERR_INVALID_ARG, "dims.reserved must be 0");
-    if (d->flags & ~(uint32_t)(SSD_FLAG_SIMT | SSD_FLAG_CHECK_FINITE))
+    if (d->flags & ~(uint32_t)(SSD_FLAG_SIMT | SSD_FLAG_CHECK_FINITE | SSD_FLAG_SPLIT_SCAN))
         return fail(SSD_ERR_INVALID_ARG, "unknown flags 0x%x", d->flags);
     if (d->batch < 1 || d->seqlen < 1 || d->nheads < 1 || d->headdim < 1 || d->dstate < 1 ||
         d->ngroups < 1 || d->chunk_len < 1)
@@ -198,9 +208,11 @@ Params base_params(const ssd_dims &d, const Layout &lo, void *ws) {
     p.status = (int *)(w + lo.status);
     p.cumA = f(lo.cumA);
     p.endA = f(lo.endA);
-    p.CB = f(lo.CB);
-    p.CBh = (bf16 *)(w + lo.CB);
-    p.CBt = p.CBh + (size_t)p.b * p.n * p.G * p.Q * p.Q;
+    if (lo.CB) {
+        p.CB = f(lo.CB);
+        p.CBh = (bf16 *)(w + lo.CB);
+        p.CBt = p.CBh + (size_t)p.b * p.n * p.G * p.Q * p.Q;
+    }
     p.states = lo.states ? f(lo.states) : nullptr;
     p.states_bf = lo.states_bf ? (bf16 *)(w + lo.states_bf) : nullptr;
     if (lo.dcum_blue) {  // backward layout
@@ -245,25 +257,34 @@ Params base_params(const ssd_dims &d, const Layout &lo, void *ws) {
     } while (0)
 
 template <typename T>
-ssd_status run_forward_chain(const Params &p, bool tc, bool write_final, cudaStream_t s, SideStream *sd) {
-    SSD_LAUNCH("k1_chunk_cumsum", launch_k1_cumsum(p, s), 1);
+ssd_status run_forward_chain(const Params &p, const ssd_dims &d, bool tc, bool write_final, cudaStream_t s,
+                             SideStream *sd) {
     if (tc) {
-        SSD_LAUNCH("k3_state_tc", launch_tc_k3(p, s), 1);
-        // K2 (CB, read first by K5 or the ORANGE backward) on the side stream, forked
-        // after K1 and enqueued after K3, so that K3's CTAs are placed first and K2's
-        // fill the SMs K3 leaves idle; the caller joins before the first reader
-        SSD_TRY(cudaEventRecord(sd->fork, s));
-        SSD_TRY(cudaStreamWaitEvent(sd->st, sd->fork, 0));
-        const cudaStream_t side = side_or_serial(sd, s);
-        {
-            cudaStream_t s = side;
-            SSD_LAUNCH("k2_cb_tc", launch_tc_k2(p, s), 1);
+        if (use_fused_scan(p, d)) {
+            // K1, K3 and K4 in one pass per (b, h) chain: the intra-chunk states stay on chip
+            SSD_LAUNCH("state_scan_tc", launch_tc_state_scan(p, write_final, s), 1);
+        } else {
+            SSD_LAUNCH("k1_chunk_cumsum", launch_k1_cumsum(p, s), 1);
+            SSD_LAUNCH("k3_state_tc", launch_tc_k3(p, s), 1);
         }
-        SSD_TRY(cudaEventRecord(sd->join, sd->st));
-    } else {
-        SSD_LAUNCH("k2_cb_simt", launch_simt_k2<T>(p, s), 1);
-        SSD_LAUNCH("k3_state_simt", launch_simt_k3<T>(p, s), 1);
+        if (sd) {
+            // K2 (CB and CB^T for the ORANGE backward) on the side stream, forked once
+            // the chunk states are enqueued; the caller joins before the first reader
+            SSD_TRY(cudaEventRecord(sd->fork, s));
+            SSD_TRY(cudaStreamWaitEvent(sd->st, sd->fork, 0));
+            const cudaStream_t side = side_or_serial(sd, s);
+            {
+                cudaStream_t s = side;
+                SSD_LAUNCH("k2_cb_tc", launch_tc_k2(p, s), 1);
+            }
+            SSD_TRY(cudaEventRecord(sd->join, sd->st));
+        }
+        if (!use_fused_scan(p, d)) SSD_LAUNCH("k4_state_passing", launch_k4_state_passing(p, write_final, s), 1);
+        return SSD_OK;
     }
+    SSD_LAUNCH("k1_chunk_cumsum", launch_k1_cumsum(p, s), 1);
+    SSD_LAUNCH("k2_cb_simt", launch_simt_k2<T>(p, s), 1);
+    SSD_LAUNCH("k3_state_simt", launch_simt_k3<T>(p, s), 1);
     SSD_LAUNCH("k4_state_passing", launch_k4_state_passing(p, write_final, s), 1);
     return SSD_OK;
 }
@@ -356,25 +377,19 @@ ssd_status ssd_forward(const ssd_dims *dims, ssd_dtype dtype, const void *x, con
     g_launches = 0;
     SSD_TRY(cudaMemsetAsync(p.status, 0, sizeof(int) * kStatusWords, s));
     if (dtype == SSD_F32) {
-        st = run_forward_chain<float>(p, false, true, s, nullptr);
+        st = run_forward_chain<float>(p, *dims, false, true, s, nullptr);
         if (st != SSD_OK) return st;
         SSD_LAUNCH("k5_scan_simt", launch_simt_k5<float>(p, s), 1);
-    } else {
-        // the side stream's fork / join records stay paired under the lock
-        std::unique_lock<std::mutex> lock(g_side_mu, std::defer_lock);
-        SideStream *sd = nullptr;
-        if (tc) {
-            lock.lock();
-            SSD_TRY(side_stream(&sd));
-        }
-        st = run_forward_chain<bf16>(p, tc, true, s, sd);
+    } else if (tc) {
+        // on the caller's stream: the chunk states (one fused scan per (b, h) chain,
+        // or K1, K3, K4), then K5 with K2 computed inside it
+        st = run_forward_chain<bf16>(p, *dims, true, true, s, nullptr);
         if (st != SSD_OK) return st;
-        if (tc) {
-            SSD_TRY(cudaStreamWaitEvent(s, sd->join, 0));  // CB
-            SSD_LAUNCH("k5_scan_tc", launch_tc_k5(p, s), 1);
-        } else {
-            SSD_LAUNCH("k5_scan_simt", launch_simt_k5<bf16>(p, s), 1);
-        }
+        SSD_LAUNCH("k5_scan_tc", launch_tc_k5(p, s), 1);
+    } else {
+        st = run_forward_chain<bf16>(p, *dims, false, true, s, nullptr);
+        if (st != SSD_OK) return st;
+        SSD_LAUNCH("k5_scan_simt", launch_simt_k5<bf16>(p, s), 1);
     }
     if (dims->flags & SSD_FLAG_CHECK_FINITE) {
         const size_t tokens = (size_t)p.b * p.L, xe = tokens * p.H * p.P;
@@ -420,7 +435,7 @@ ssd_status ssd_backward(const ssd_dims *dims, ssd_dtype dtype, const void *x, co
     g_launches = 0;
     SSD_TRY(cudaMemsetAsync(p.status, 0, sizeof(int) * kStatusWords, s));
     if (dtype == SSD_F32) {
-        st = run_forward_chain<float>(p, false, false, s, nullptr);
+        st = run_forward_chain<float>(p, *dims, false, false, s, nullptr);
         if (st != SSD_OK) return st;
         SSD_LAUNCH("bwd_blue_simt", launch_simt_bwd_blue<float>(p, s), 2);
         SSD_LAUNCH("bwd_k4_state_passing", launch_bwd_k4(p, s), 1);
@@ -434,7 +449,7 @@ ssd_status ssd_backward(const ssd_dims *dims, ssd_dtype dtype, const void *x, co
             lock.lock();
             SSD_TRY(side_stream(&sd));
         }
-        st = run_forward_chain<bf16>(p, tc, false, s, sd);
+        st = run_forward_chain<bf16>(p, *dims, tc, false, s, sd);
         if (st != SSD_OK) return st;
         if (tc) {
             // Two chains from here on.  The group kernels (G1: d_cb; G2: dB, dC partials;

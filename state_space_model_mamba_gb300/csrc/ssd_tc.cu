@@ -45,7 +45,10 @@ constexpr int kStatusTimeout = 5;
 
 struct TcMaps {
     CUtensorMap x, dy, B, C, st, dst, cb, cbt, dcb, part, dx, y, cb64;
+    CUtensorMap xs, Bs;    // chunk-state scan: x of 1 or 2 heads, both halves of B, 128 tokens
 };
+
+constexpr int kScanConsumers = 512;  // consumer threads of the chunk-state scan
 
 __device__ __forceinline__ uint8_t *align1024(uint8_t *p) {
     return (uint8_t *)(((uintptr_t)p + 1023) & ~(uintptr_t)1023);
@@ -491,6 +494,326 @@ __global__ void __launch_bounds__(kThreadsWide + 32, 1) tc_k3_kernel(const Param
     if (warp == 0) tmem_dealloc(tm, 128);
 }
 
+// ====================================================================== fused K1 + K3 + K4
+// The chunk-state scan: CTA per (b, pair of heads of one group) -- or per
+// (b, head) when the problem has few heads -- looping over the chunks in
+// order with the running states in registers, so that the intra-chunk states
+// never leave the SM (burn-mamba, "combined_backward.rs": the K1 recompute of
+// dA = dt * A and its inclusive cumsum, k3_ssd_chunk_state_extended, and the
+// K4 recurrence s_{i+1} = exp(dA_end_i) s_i + intra_i).  Per chunk c and head e:
+//   cumA   inclusive cumsum of dt * A over the chunk (each lane sums Q / 32
+//          consecutive tokens, a warp scan adds the lanes' sums), written to
+//          the workspace with endA = cumA[Q - 1], and bbs = dt exp(endA - cumA)
+//          into a table;
+//   intra  intra[r, p] = sum_l B[l, r] (bbs[l] x[l, p]): one MMA accumulation
+//          over 128-token sub-stages (M = dstate, A = B, B = the scaled x of
+//          the CTA's heads side by side, N = 64 per head, both MN-major) into
+//          one of two TMEM buffers, so the MMAs of chunk c overlap the
+//          epilogue of chunk c - 1;
+//   carry  s_in_c = s goes to the workspace in bf16 for K5 and the backward,
+//          then s <- exp(endA_c) s + intra_c in fp32 registers: consumer thread
+//          (warp w, lane quadrant q4 = w % 4, column quarter cq = w / 4) keeps the
+//          16 entries (p = 16 cq + j, r = 32 q4 + lane) of each head.
+// Roles, handing over through mbarriers only (no CTA-wide barrier in the loop):
+// 16 consumer warps scale the x rows of each sub-stage and run the carry; one
+// thread issues the MMAs, one issues the TMA loads (one box for the x of both
+// heads, one for both 64-column halves of B) into a ring of NSS stages, and
+// one warp per head runs the scans up to NTAB chunks ahead.  The chain over chunks is
+// serial, so the kernel lives on the depth of its ring: one CTA per SM, and
+// two heads per CTA when there are enough heads to fill the SMs that way,
+// which halves the B traffic.  Chunks wholly past valid_len load nothing:
+// their cumA and endA are 0 and the states pass through them unchanged.
+template <int HPC>
+struct ScanGeom {
+    static constexpr uint32_t XS = 128 * 128;             // x of one head, one sub-stage: [128 tokens][64]
+    static constexpr uint32_t BS = 128 * 128;             // one 64-column half of B of a sub-stage
+    static constexpr uint32_t SST = HPC * XS + 2 * BS;    // one stage
+    static constexpr int NSS = HPC == 2 ? 3 : 4;          // ring depth
+    static constexpr int NTAB = 4;                        // chunks of scan tables
+    static constexpr size_t smem = 1024 + (size_t)NSS * SST;
+};
+
+template <int Q, int HPC>
+__global__ void __launch_bounds__(kScanConsumers + 128, 1)
+    tc_state_scan_kernel(const Params p, const __grid_constant__ TcMaps maps, int write_final) {
+    using Gm = ScanGeom<HPC>;
+    constexpr int SPC = Q / 128;  // 128-token sub-stages per chunk
+    constexpr int NSS = Gm::NSS, NTAB = Gm::NTAB;
+    constexpr uint32_t XS = Gm::XS, BS = Gm::BS, SST = Gm::SST;
+    constexpr uint32_t BOFF = HPC * XS;   // B within a stage
+    constexpr int NCW = kScanConsumers / 32;  // consumer warps
+    constexpr int W_MMA = NCW, W_LOAD = NCW + 1, W_SCAN = NCW + 2;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *ring = align1024(smem_raw);
+    __shared__ uint64_t bar_full[NSS], bar_scaled[NSS], bar_free[NSS], bar_mma[2], bar_tfree[2];
+    __shared__ uint64_t bar_tab[NTAB], bar_tabfree[NTAB];
+    __shared__ uint32_t s_tmem;
+    __shared__ int s_issued, s_mma, s_perr;
+    __shared__ float s_bbs[NTAB][HPC][Q];
+    __shared__ float s_ea[NTAB][HPC];
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    // CTA -> (b, group, first head); a group with an odd head count ends in a one-head CTA
+    const int cpg = (p.hpg + HPC - 1) / HPC;  // CTAs per (b, group)
+    const int bg = blockIdx.x / cpg, g = bg % p.G, bi = bg / p.G;
+    const int h0 = g * p.hpg + (blockIdx.x % cpg) * HPC;
+    const int nh = min(HPC, g * p.hpg + p.hpg - h0);
+    const int V = valid_len_of(p, bi);
+    const int nv = (V + Q - 1) / Q;  // chunks holding a valid token (a prefix)
+    const int U = nv * SPC;          // sub-stages loaded and multiplied
+    // the backward's first kernel also clears the arrival counters
+    {
+        const int gs = gridDim.x * blockDim.x, i0 = blockIdx.x * blockDim.x + tid;
+        if (p.cb_count)
+            for (int i = i0; i < p.n_count; i += gs) p.cb_count[i] = 0;
+        if (p.fin_count)
+            for (int i = i0; i < p.H; i += gs) p.fin_count[i] = 0;
+    }
+    // one CTA per sample reports a valid_len entry outside [0, L] (it is clamped)
+    if (h0 == 0 && tid == 0 && valid_len_out_of_range(p, bi)) atomicAdd(p.status + kStatusValidLen, 1);
+    if (tid == 0) {
+        for (int i = 0; i < NSS; ++i) {
+            mbar_init(&bar_full[i], 1);
+            mbar_init(&bar_scaled[i], NCW);
+            mbar_init(&bar_free[i], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&bar_mma[i], 1);
+            mbar_init(&bar_tfree[i], NCW);
+        }
+        for (int i = 0; i < NTAB; ++i) {
+            mbar_init(&bar_tab[i], 32 * HPC);
+            mbar_init(&bar_tabfree[i], NCW);
+        }
+        mbar_fence_init();
+        s_issued = 0;
+        s_mma = 0;
+        s_perr = 0;
+    }
+    // TMEM: buffer k & 1 at columns 64 HPC (k & 1), head e at + 64 e
+    constexpr uint32_t NCOL = HPC == 2 ? 256 : 128;
+    if (warp == 0) tmem_alloc(&s_tmem, NCOL);
+    tc_sync();
+    const uint32_t tm = s_tmem;
+    bool ok = true;
+    if (warp == W_MMA) {
+        // ---- MMA issuer: sub-stage u once every consumer warp has scaled it
+        if (lane == 0) {
+            const uint32_t idesc = idesc_bf16(128, 64 * nh, true, true);
+            for (int u = 0; u < U; ++u) {
+                const int st = u % NSS, k = u / SPC, j = u % SPC;
+                if (!mbar_wait(&bar_scaled[st], (uint32_t)((u / NSS) & 1)) || s_perr) {
+                    s_perr = 1;
+                    break;
+                }
+                // TMEM buffer k & 1 is free once the epilogue of chunk k - 2 has read it
+                if (j == 0 && k >= 2 && !mbar_wait(&bar_tfree[k & 1], (uint32_t)(((k - 2) >> 1) & 1))) {
+                    s_perr = 1;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t base = smem_u32(ring + st * SST);
+                for (int ks = 0; ks < 8; ++ks)
+                    mma_bf16(tm + 64 * HPC * (k & 1), sdesc_mnmajor(base + BOFF, ks, BS), sdesc_mnmajor(base, ks, XS),
+                             idesc, j > 0 || ks > 0);
+                mma_commit(&bar_free[st]);
+                if (j == SPC - 1) mma_commit(&bar_mma[k & 1]);
+                s_mma = u + 1;
+            }
+        }
+    } else if (warp == W_LOAD) {
+        // ---- TMA loader: stage u % NSS once the MMAs of sub-stage u - NSS are done
+        if (lane == 0) {
+            for (int u = 0; u < U; ++u) {
+                const int st = u % NSS, t = (u / SPC) * Q + 128 * (u % SPC);
+                if (u >= NSS && !mbar_wait(&bar_free[st], (uint32_t)((u / NSS - 1) & 1))) {
+                    s_perr = 1;
+                    break;
+                }
+                uint8_t *dst = ring + st * SST;
+                mbar_arrive_expect_tx(&bar_full[st], SST);
+                tma_load_4d(dst, &maps.xs, &bar_full[st], 0, t, h0, bi);
+                tma_load_5d(dst + BOFF, &maps.Bs, &bar_full[st], 0, t, 0, g, bi);
+                s_issued = u + 1;
+            }
+        }
+    } else if (warp >= W_SCAN) {
+        // ---- scans: warp W_SCAN + e scans head e of chunk c into table c % NTAB, up to
+        // NTAB chunks ahead.  Lane l holds tokens TPL l .. TPL l + TPL - 1: their dt
+        // (fetched a chunk ahead), a sequential sum, a warp scan of the lanes' sums.
+        constexpr int TPL = Q / 32;
+        const int e = warp - W_SCAN;
+        const bool live = e < nh;
+        const float Ah = live ? p.A[h0 + e] : 0.f;
+        const float *dtrow = p.dt + ix_dt(p, bi, live ? h0 + e : h0, 0);
+        auto fetch = [&](int c, float *v) {
+            const int vr = min(Q, V - c * Q);
+#pragma unroll
+            for (int i = 0; i < TPL; ++i) {
+                const int q = TPL * lane + i;
+                v[i] = (live && q < vr) ? dtrow[c * Q + q] : 0.f;
+            }
+        };
+        float vn[TPL];
+        fetch(0, vn);
+        for (int c = 0; c < p.n; ++c) {
+            const int slot = c % NTAB;
+            float v[TPL];
+#pragma unroll
+            for (int i = 0; i < TPL; ++i) v[i] = vn[i];
+            if (c + 1 < p.n) fetch(c + 1, vn);
+            if (c >= NTAB && !__all_sync(0xffffffffu, mbar_wait(&bar_tabfree[slot], (uint32_t)((c / NTAB - 1) & 1)))) {
+                s_perr = 1;
+                break;
+            }
+            if (live) {
+                const int vr = min(Q, V - c * Q);
+                float cum[TPL], run = 0.f;
+#pragma unroll
+                for (int i = 0; i < TPL; ++i) {
+                    run += v[i] * Ah;
+                    cum[i] = run;
+                }
+                float incl = run;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const float w = __shfl_up_sync(0xffffffffu, incl, o);
+                    if (lane >= o) incl += w;
+                }
+                const float pre = incl - run, endA = __shfl_sync(0xffffffffu, incl, 31);
+                const size_t ck = ix_chunk(p, bi, h0 + e, c);
+#pragma unroll
+                for (int i = 0; i < TPL; ++i) {
+                    const int q = TPL * lane + i;
+                    const float cq = cum[i] + pre;
+                    p.cumA[ck * Q + q] = cq;
+                    s_bbs[slot][e][q] = q < vr ? v[i] * __expf(endA - cq) : 0.f;
+                }
+                if (lane == 0) {
+                    p.endA[ck] = endA;
+                    s_ea[slot][e] = __expf(endA);
+                }
+            }
+            mbar_arrive(&bar_tab[slot]);
+        }
+    } else if (warp < NCW) {
+        // ---- consumers
+        const int q4 = warp & 3, cq = warp >> 2;
+        const int r = 32 * q4 + lane;
+        float s[HPC][16];
+#pragma unroll
+        for (int e = 0; e < HPC; ++e) {
+            const size_t bh = (size_t)bi * p.H + h0 + e;
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+                s[e][j] = (p.init && e < nh) ? p.init[(bh * kP + 16 * cq + j) * kN + r] : 0.f;
+        }
+        for (int c = 0; c <= p.n && ok; ++c) {
+            if (c < p.n) {
+                const int slot = c % NTAB, vr = min(Q, V - c * Q);
+                ok = __all_sync(0xffffffffu, mbar_wait(&bar_tab[slot], (uint32_t)((c / NTAB) & 1)));
+                // ---- K3 operands: scale x rows by bbs (packed bf16 pairs), zero rows past valid_len
+                for (int j = 0; j < SPC && c < nv && ok; ++j) {
+                    const int u = c * SPC + j, st = u % NSS;
+                    const uint32_t sb = smem_u32(ring + st * SST);
+                    ok = __all_sync(0xffffffffu, mbar_wait(&bar_full[st], (uint32_t)((u / NSS) & 1)));
+                    if (!ok) break;
+                    // thread: row tid / 4 of the sub-stage, 16-byte chunks 2 (tid % 4) and + 1
+                    const int row = tid >> 2, tl = 128 * j + row;
+                    const bool vrow = tl < vr;
+                    const uint32_t off = (uint32_t)row * 128u + (uint32_t)(tid & 3) * 32u;
+#pragma unroll
+                    for (int e = 0; e < HPC; ++e) {
+                        if (e >= nh) break;
+                        const uint32_t a = sb + e * XS + off;
+                        if (!vrow) {
+                            st_shared_v4(a, 0u, 0u, 0u, 0u);
+                            st_shared_v4(a + 16u, 0u, 0u, 0u, 0u);
+                            continue;
+                        }
+                        const float f = s_bbs[slot][e][tl];
+                        const uint32_t f2 = pack_bf2(f, f);
+                        const uint4 v0 = ld_shared_v4(a), v1 = ld_shared_v4(a + 16u);
+                        st_shared_v4(a, bmul2(v0.x, f2), bmul2(v0.y, f2), bmul2(v0.z, f2), bmul2(v0.w, f2));
+                        st_shared_v4(a + 16u, bmul2(v1.x, f2), bmul2(v1.y, f2), bmul2(v1.z, f2), bmul2(v1.w, f2));
+                    }
+                    if (!vrow) {  // B rows past valid_len (both halves)
+#pragma unroll
+                        for (int q = 0; q < 4; ++q)
+                            st_shared_v4(sb + BOFF + (uint32_t)(q >> 1) * BS + off + (uint32_t)(q & 1) * 16u, 0u, 0u,
+                                         0u, 0u);
+                    }
+                    fence_async_smem();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&bar_scaled[st]);  // the MMA thread issues the sub-stage
+                }
+                if (!ok) break;
+            }
+            if (c > 0) {
+                // ---- K4 step of chunk k = c - 1: s_in_k = s out, s <- exp(endA_k) s + intra_k
+                const int k = c - 1, kslot = k % NTAB;
+                float v[HPC][16];
+                if (k < nv) {
+                    ok = __all_sync(0xffffffffu, mbar_wait(&bar_mma[k & 1], (uint32_t)((k >> 1) & 1)));
+                    if (!ok) break;
+                    tc_fence_after();
+#pragma unroll
+                    for (int e = 0; e < HPC; ++e) {
+                        if (e < nh) tmem_ld16(tmem_addr(tm, 32 * q4, 64 * (HPC * (k & 1) + e) + 16 * cq), v[e]);
+                        else {
+#pragma unroll
+                            for (int j = 0; j < 16; ++j) v[e][j] = 0.f;
+                        }
+                    }
+                    // TMEM buffer k & 1 read: the MMAs of chunk k + 2 may overwrite it
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&bar_tfree[k & 1]);
+                } else {
+#pragma unroll
+                    for (int e = 0; e < HPC; ++e)
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) v[e][j] = 0.f;
+                }
+#pragma unroll
+                for (int e = 0; e < HPC; ++e) {
+                    if (e >= nh) break;
+                    // s_in_k: for each p the warp's lanes write 32 consecutive r (64 bytes)
+                    bf16 *dst = p.states_bf + ix_state(p, bi, k, h0 + e) + (size_t)(16 * cq) * kN + r;
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) dst[(size_t)j * kN] = __float2bfloat16_rn(s[e][j]);
+                    const float a = s_ea[kslot][e];
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) s[e][j] = fmaf(a, s[e][j], v[e][j]);
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bar_tabfree[kslot]);  // table of chunk k no longer read
+            }
+        }
+        if (!ok) s_perr = 1;
+        if (ok && write_final && p.final_state) {
+#pragma unroll
+            for (int e = 0; e < HPC; ++e) {
+                if (e >= nh) break;
+                const size_t bh = (size_t)bi * p.H + h0 + e;
+#pragma unroll
+                for (int j = 0; j < 16; ++j) p.final_state[(bh * kP + 16 * cq + j) * kN + r] = s[e][j];
+            }
+        }
+    }
+    tc_fence_before();
+    ok = __syncthreads_and(ok && s_perr == 0 ? 1 : 0) != 0;
+    tc_fence_after();
+    if (!ok && tid == 0) flag_timeout(p);
+    if (tid == 0) {
+        // the latest load of every stage has to land before exit (one not consumed
+        // after an error), and the last MMAs have to complete (they complete in order)
+        for (int u = max(0, s_issued - NSS); u < s_issued; ++u) mbar_wait(&bar_full[u % NSS], (uint32_t)((u / NSS) & 1));
+        if (s_mma > 0) mbar_wait(&bar_free[(s_mma - 1) % NSS], (uint32_t)(((s_mma - 1) / NSS) & 1));
+    }
+    tc_sync();
+    if (warp == 0) tmem_dealloc(tm, NCOL);
+}
+
 // ====================================================================== K5
 // CTA per (b, chunk, group, head slice), 256 threads, looping over the slice's
 // heads with one CTA barrier per head.  C (BLUE's A operand) and the bf16 CB
@@ -543,7 +866,7 @@ __global__ void __launch_bounds__(kThreadsWide, 1) tc_k5_kernel(const Params p, 
     auto cb_tile = [&](int tb, int sb) -> uint8_t * {
         return sb == 2 * tb + 1 ? CBh + tb * (kTile / 2) - kTile / 2 : CBf + (tb * (tb + 1) + sb - tb) * kTile;
     };
-    __shared__ uint64_t bar_res, bar_x, bar_s, bar_o, bar_b;
+    __shared__ uint64_t bar_res, bar_x, bar_s, bar_o, bar_b, bar_cb;
     __shared__ uint32_t s_tmem;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int q4 = warp & 3, hf = warp >> 2;
@@ -630,26 +953,33 @@ __global__ void __launch_bounds__(kThreadsWide, 1) tc_k5_kernel(const Params p, 
         mbar_init(&bar_s, 1);
         mbar_init(&bar_o, 1);
         mbar_init(&bar_b, 1);
+        mbar_init(&bar_cb, 1);
         mbar_fence_init();
     }
     if (warp == 0) tmem_alloc(&s_tmem, NCOL);
     tc_sync();
     const uint32_t tm = s_tmem;
+    // ---- K2 prologue: CB = C B^T of the chunk and group (burn-mamba "K2 -- CB
+    // matrix used in K5 ORANGE"), once per CTA for all of its heads.  C and B
+    // come in by TMA (B into the CB tile region when it fits there, else into
+    // the x / s_in / staging region, and then the first head's x and s_in wait
+    // until CB is out of TMEM); per t-block tb one MMA accumulation (both
+    // operands K-major) gives CB[t, s] for s < 128 (tb + 1) in TMEM columns
+    // [64 tb (tb + 1), 64 (tb + 1) (tb + 2)), which the threads round to bf16
+    // into the swizzled CB tiles the W build reads.
+    constexpr bool B_IN_CB = (NWT - NT) * kTile + NT * (kTile / 2) >= 2 * RB;
+    uint8_t *Bsm = B_IN_CB ? CBf : xs;
     if (tid == 0) {
-        mbar_arrive_expect_tx(&bar_res, 2 * RB + (NWT - NT) * kTile + NT * (kTile / 2));
-        const int cbrow = ((bi * p.n + c) * p.G + g) * Q;
+        mbar_arrive_expect_tx(&bar_res, 4 * RB);
         for (int j = 0; j < NT; ++j)
-            for (int rb = 0; rb < 2; ++rb)
+            for (int rb = 0; rb < 2; ++rb) {
                 tma_load_4d(Cs + rb * RB + j * kTile, &maps.C, &bar_res, 64 * rb, g, t0 + 128 * j, bi);
-        for (int tb = 0; tb < NT; ++tb)
-            for (int sb = 0; sb < 2 * (tb + 1); ++sb) {
-                if (sb == 2 * tb + 1)
-                    tma_load_2d(CBh + tb * (kTile / 2), &maps.cb64, &bar_res, 64 * sb, cbrow + 128 * tb + 64);
-                else
-                    tma_load_2d(cb_tile(tb, sb), &maps.cb, &bar_res, 64 * sb, cbrow + 128 * tb);
+                tma_load_4d(Bsm + rb * RB + j * kTile, &maps.B, &bar_res, 64 * rb, g, t0 + 128 * j, bi);
             }
-        issue_x(h_begin);
-        issue_s(h_begin);
+        if (B_IN_CB) {
+            issue_x(h_begin);
+            issue_s(h_begin);
+        }
     }
     fetch(0);
     stash(0);
@@ -658,13 +988,53 @@ __global__ void __launch_bounds__(kThreadsWide, 1) tc_k5_kernel(const Params p, 
         stash(1);
     }
     if (nh > 2) fetch(2);
-    int x_issued = 1, x_landed = 0, s_issued = 1, s_landed = 0;
     bool ok = wait_all(&bar_res, 0, true);  // publishes the raw scalars of heads 0 and 1
     if (ok && vrows < Q) {
-        zero_rows_from(Cs, Q, vrows);
-        zero_rows_from(Cs + RB, Q, vrows);
-        fence_async_smem();
+        for (int rb = 0; rb < 2; ++rb) {
+            zero_rows_from(Cs + rb * RB, Q, vrows);
+            zero_rows_from(Bsm + rb * RB, Q, vrows);
+        }
     }
+    fence_async_smem();
+    tc_sync();
+    if (tid == 0 && ok) {
+        for (int tb = 0; tb < NT; ++tb) {
+            const uint32_t id = idesc_bf16(128, 128 * (tb + 1), false, false);
+            for (int ks = 0; ks < kN / 16; ++ks)
+                mma_bf16(tm + (uint32_t)(64 * tb * (tb + 1)), sdesc_kmajor(smem_u32(Cs + tb * kTile), ks, RB),
+                         sdesc_kmajor(smem_u32(Bsm), ks, RB), id, ks > 0);
+        }
+        mma_commit(&bar_cb);
+    }
+    ok = wait_all(&bar_cb, 0, ok);
+    tc_fence_after();
+    if (ok) {
+        // warps of a lane quadrant take alternate 64-column pieces; the upper 64
+        // rows of the half tiles are zero and not stored
+        const int row = 32 * q4 + lane;
+#pragma unroll
+        for (int tb = 0; tb < NT; ++tb)
+            for (int sb = hf; sb < 2 * (tb + 1); sb += 2) {
+                if (sb == 2 * tb + 1 && q4 < 2) continue;
+                float v[64];
+                tmem_ld64(tmem_addr(tm, 32 * q4, 64 * tb * (tb + 1) + 64 * sb), v);
+                const uint32_t base = smem_u32(cb_tile(tb, sb)) + (uint32_t)row * 128u;
+#pragma unroll
+                for (int c8 = 0; c8 < 8; ++c8)
+                    st_shared_v4(base + (uint32_t)((c8 ^ (row & 7)) << 4), pack_bf2(v[8 * c8], v[8 * c8 + 1]),
+                                 pack_bf2(v[8 * c8 + 2], v[8 * c8 + 3]), pack_bf2(v[8 * c8 + 4], v[8 * c8 + 5]),
+                                 pack_bf2(v[8 * c8 + 6], v[8 * c8 + 7]));
+            }
+    }
+    // CB tiles visible, CB out of TMEM, B dead
+    tc_fence_before();
+    ok = __syncthreads_and(ok ? 1 : 0) != 0;
+    tc_fence_after();
+    if (!B_IN_CB && tid == 0 && ok) {
+        issue_x(h_begin);
+        issue_s(h_begin);
+    }
+    int x_issued = B_IN_CB || ok ? 1 : 0, x_landed = 0, s_issued = x_issued, s_landed = 0;
     derive(0);
     __syncthreads();
     uint4 xr[NT][4];  // this thread's D x slices of the head whose epilogue comes next
@@ -2480,18 +2850,18 @@ cudaError_t encode(CUtensorMap *m, const void *base, int rank, const cuuint64_t 
                    const cuuint32_t *box, CUtensorMapDataType dtype = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) {
     auto fn = encode_fn();
     if (!fn) return cudaErrorNotSupported;
-    cuuint32_t es[4] = {1, 1, 1, 1};
+    cuuint32_t es[5] = {1, 1, 1, 1, 1};
     CUresult r = fn(m, dtype, (cuuint32_t)rank, const_cast<void *>(base), dims, strides,
                     box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                     CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-// [b, L, H or G, 64 or 128] bf16 activations: boxes of 64 columns x 128 tokens.
-cudaError_t map_tokens(CUtensorMap *m, const void *base, int b, int L, int heads, int width) {
+// [b, L, H or G, 64 or 128] bf16 activations: boxes of 64 columns x `tokens` tokens.
+cudaError_t map_tokens(CUtensorMap *m, const void *base, int b, int L, int heads, int width, int tokens = 128) {
     cuuint64_t dims[4] = {(cuuint64_t)width, (cuuint64_t)heads, (cuuint64_t)L, (cuuint64_t)b};
     cuuint64_t strides[3] = {(cuuint64_t)width * 2, (cuuint64_t)heads * width * 2, (cuuint64_t)L * heads * width * 2};
-    cuuint32_t box[4] = {64, 1, 128, 1};
+    cuuint32_t box[4] = {64, 1, (cuuint32_t)tokens, 1};
     return encode(m, base, 4, dims, strides, box);
 }
 
@@ -2503,12 +2873,29 @@ cudaError_t map_states(CUtensorMap *m, const void *base, long long count) {
     return encode(m, base, 3, dims, strides, box);
 }
 
+// Heads per CTA of the chunk-state scan (one CTA per SM): one while the (b, head)
+// chains fit the 152 SMs in one wave, else two (sharing B), which halves the waves.
+int scan_heads_per_cta(const Params &p) { return (long long)p.b * p.H > 152 ? 2 : 1; }
+
 cudaError_t make_maps(const Params &p, TcMaps *mp, bool backward) {
     memset(mp, 0, sizeof(*mp));
     cudaError_t e;
     if ((e = map_tokens(&mp->x, p.x, p.b, p.L, p.H, kP)) != cudaSuccess) return e;
     if ((e = map_tokens(&mp->B, p.B, p.b, p.L, p.G, kN)) != cudaSuccess) return e;
     if ((e = map_tokens(&mp->C, p.C, p.b, p.L, p.G, kN)) != cudaSuccess) return e;
+    {  // x as [b][head][token][64] boxes of (1 or 2 heads) x 128 tokens: dims (p, token, head, b)
+        const int hpc = scan_heads_per_cta(p);
+        cuuint64_t dims[4] = {(cuuint64_t)kP, (cuuint64_t)p.L, (cuuint64_t)p.H, (cuuint64_t)p.b};
+        cuuint64_t strides[3] = {(cuuint64_t)p.H * kP * 2, (cuuint64_t)kP * 2, (cuuint64_t)p.L * p.H * kP * 2};
+        cuuint32_t box[4] = {64, 128, (cuuint32_t)hpc, 1};
+        if ((e = encode(&mp->xs, p.x, 4, dims, strides, box)) != cudaSuccess) return e;
+    }
+    {  // B as [half][token][64] boxes of 2 halves x 128 tokens: dims (column, token, half, group, b)
+        cuuint64_t dims[5] = {64, (cuuint64_t)p.L, 2, (cuuint64_t)p.G, (cuuint64_t)p.b};
+        cuuint64_t strides[4] = {(cuuint64_t)p.G * kN * 2, 128, (cuuint64_t)kN * 2, (cuuint64_t)p.L * p.G * kN * 2};
+        cuuint32_t box[5] = {64, 128, 2, 1, 1};
+        if ((e = encode(&mp->Bs, p.B, 5, dims, strides, box)) != cudaSuccess) return e;
+    }
     if (p.states_bf && (e = map_states(&mp->st, p.states_bf, (long long)p.b * p.n * p.H)) != cudaSuccess) return e;
     if (!backward && p.y && (e = map_tokens(&mp->y, p.y, p.b, p.L, p.H, kP)) != cudaSuccess) return e;
     if (p.CBh) {  // CB and CB^T, bf16 [b*n*G*Q rows][Q]: boxes of 64 columns x 128 rows
@@ -2590,6 +2977,9 @@ static_assert(smem_k2(256) > 116 * 1024, "K2 (512 TMEM columns): one CTA per SM"
 static_assert(smem_k2(128) >= 1024 + 4 * 128 * 128 && 3 * (smem_k2(128) + 1024) > 233472,
               "K2 at Q = 128 (256 TMEM columns): at most two CTAs per SM");
 static_assert(smem_k5(256) <= 232448 && smem_k5(256) > 116 * 1024, "K5: one CTA per SM");
+static_assert(ScanGeom<2>::smem + 4 * (4 * 2 * 256 + 2 * 4) + 512 <= 232448 &&
+                  ScanGeom<1>::smem + 4 * (4 * 1 * 256 + 4) + 512 <= 232448,
+              "chunk-state scan shared memory");
 static_assert(smem_k3(256) <= 232448 && smem_blue(256) <= 232448, "K3 / BLUE shared memory");
 static_assert(smem_blue(128) > 116 * 1024, "BLUE (512 TMEM columns): one CTA per SM");
 static_assert(smem_dbc(256) <= 232448, "group backward shared memory");
@@ -2694,6 +3084,27 @@ cudaError_t launch_tc_k3(const Params &p, cudaStream_t s) {
 #define CALL(Q) launch(tc_k3_kernel<Q>, grid, smem_k3(Q), s, p, m, kThreadsWide + 32)
     return SSD_TC_DISPATCH(p.Q, CALL);
 #undef CALL
+}
+
+
+template <int Q, int HPC>
+cudaError_t launch_scan(const Params &p, const TcMaps &m, bool write_final, cudaStream_t s) {
+    auto kernel = tc_state_scan_kernel<Q, HPC>;
+    const size_t smem = ScanGeom<HPC>::smem;
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    const unsigned grid = (unsigned)(p.b * p.G * ((p.hpg + HPC - 1) / HPC));
+    kernel<<<grid, kScanConsumers + 32 * (2 + HPC), smem, s>>>(p, m, write_final ? 1 : 0);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_tc_state_scan(const Params &p, bool write_final, cudaStream_t s) {
+    TcMaps m;
+    cudaError_t e = make_maps(p, &m, false);
+    if (e != cudaSuccess) return e;
+    const int hpc = scan_heads_per_cta(p);
+    if (p.Q == 256) return hpc == 2 ? launch_scan<256, 2>(p, m, write_final, s) : launch_scan<256, 1>(p, m, write_final, s);
+    return hpc == 2 ? launch_scan<128, 2>(p, m, write_final, s) : launch_scan<128, 1>(p, m, write_final, s);
 }
 
 cudaError_t launch_tc_k5(const Params &p, cudaStream_t s) {

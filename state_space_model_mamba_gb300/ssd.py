@@ -22,6 +22,7 @@ LIB_PATH = os.path.join(_PKG, "lib", "libssd.so")
 SSD_F32, SSD_BF16 = 0, 1
 SSD_FLAG_SIMT = 1
 SSD_FLAG_CHECK_FINITE = 2
+SSD_FLAG_SPLIT_SCAN = 4
 SSD_OK, SSD_ERR_INVALID_ARG, SSD_ERR_UNSUPPORTED, SSD_ERR_WORKSPACE = 0, 1, 2, 3
 SSD_ERR_CUDA, SSD_ERR_TIMEOUT, SSD_ERR_NONFINITE = 4, 5, 6
 STATUS = {0: "SSD_OK", 1: "SSD_ERR_INVALID_ARG", 2: "SSD_ERR_UNSUPPORTED",
@@ -111,9 +112,11 @@ class Dims:
     chunk_len: int
     simt: bool = False
     check_finite: bool = False
+    split_scan: bool = False
 
     def c(self) -> SsdDims:
-        flags = (SSD_FLAG_SIMT if self.simt else 0) | (SSD_FLAG_CHECK_FINITE if self.check_finite else 0)
+        flags = ((SSD_FLAG_SIMT if self.simt else 0) | (SSD_FLAG_CHECK_FINITE if self.check_finite else 0)
+                 | (SSD_FLAG_SPLIT_SCAN if self.split_scan else 0))
         return SsdDims(self.batch, self.seqlen, self.nheads, self.headdim, self.dstate,
                        self.ngroups, self.chunk_len, flags, 0)
 
@@ -127,10 +130,10 @@ def _dtype_code(t: torch.Tensor) -> int:
 
 
 def dims_of(x: torch.Tensor, B: torch.Tensor, chunk_len: int, simt: bool = False,
-            check_finite: bool = False) -> Dims:
+            check_finite: bool = False, split_scan: bool = False) -> Dims:
     b, L, H, P = x.shape
     G, N = B.shape[2], B.shape[3]
-    return Dims(b, L, H, P, N, G, int(chunk_len), simt, check_finite)
+    return Dims(b, L, H, P, N, G, int(chunk_len), simt, check_finite, split_scan)
 
 
 def supported(dims: Dims, dtype_code: int) -> bool:
@@ -197,7 +200,8 @@ def backward_into(dims: Dims, x, dt, A, B, C, D, init_state, valid_len, dy, d_fi
 
 
 def ssd_forward(x, dt, A, B, C, D, chunk_len, init_state=None, valid_len=None,
-                return_final_state=True, simt=False, check_finite=False, check_status=False):
+                return_final_state=True, simt=False, check_finite=False, check_status=False,
+                split_scan=False):
     """Forward of the chunked selective scan.  Returns ``(y, final_state)``.
 
     x [b,L,H,P] (fp32 or bf16), dt [b,H,L] fp32, A [H] fp32, B/C [b,L,G,N]
@@ -205,10 +209,11 @@ def ssd_forward(x, dt, A, B, C, D, chunk_len, init_state=None, valid_len=None,
     valid_len int32 [b] or None.  ``check_finite`` sets SSD_FLAG_CHECK_FINITE;
     with it or ``check_status`` the call synchronises and raises SsdError when
     the device reported a condition (timeout, non-finite values, clamped
-    valid_len entries).
+    valid_len entries).  ``split_scan`` sets SSD_FLAG_SPLIT_SCAN (chunk states by
+    the chunk-parallel K3 and a separate K4 pass instead of the fused scan).
     """
     _check_inputs(x, dt, A, B, C, D, init_state, valid_len, x.dtype)
-    dims = dims_of(x, B, chunk_len, simt, check_finite)
+    dims = dims_of(x, B, chunk_len, simt, check_finite, split_scan)
     code = _dtype_code(x)
     y = torch.empty_like(x)
     fin = (torch.empty(x.shape[0], x.shape[2], x.shape[3], B.shape[3], device=x.device,
@@ -221,14 +226,14 @@ def ssd_forward(x, dt, A, B, C, D, chunk_len, init_state=None, valid_len=None,
 
 
 def ssd_backward(x, dt, A, B, C, D, chunk_len, dy, d_final_state=None, init_state=None,
-                 valid_len=None, want_d_init=True, simt=False, check_finite=False,
+                 valid_len=None, want_d_init=True, simt=False, check_finite=False, split_scan=False,
                  check_status=False):
     """Recompute backward.  Returns a dict with dx, ddt, dA, dB, dC, dD, d_init.
     ``check_finite`` / ``check_status`` as in :func:`ssd_forward`."""
     _check_inputs(x, dt, A, B, C, D, init_state, valid_len, x.dtype)
     if tuple(dy.shape) != tuple(x.shape) or dy.dtype != x.dtype or not dy.is_contiguous():
         raise ValueError("dy must match x in shape and dtype and be contiguous")
-    dims = dims_of(x, B, chunk_len, simt, check_finite)
+    dims = dims_of(x, B, chunk_len, simt, check_finite, split_scan)
     code = _dtype_code(x)
     b, L, H, P = x.shape
     N = B.shape[3]

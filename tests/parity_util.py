@@ -22,15 +22,16 @@ def to_device(inp, dtype: str, device="cuda"):
                 torch.from_numpy(np.asarray(inp["valid_len"], np.int32)).to(device))
 
 
-def run_gpu(inp, dtype: str, chunk_len: int, simt=False, backward=True):
+def run_gpu(inp, dtype: str, chunk_len: int, simt=False, backward=True, split_scan=False):
     d = to_device(inp, dtype)
     y, fin = ssd.ssd_forward(d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"], chunk_len,
-                             init_state=d["init"], valid_len=d["valid_len"], simt=simt)
+                             init_state=d["init"], valid_len=d["valid_len"], simt=simt,
+                             split_scan=split_scan)
     out = {"y": y, "final_state": fin}
     if backward:
         g = ssd.ssd_backward(d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"], chunk_len, d["dy"],
                              d_final_state=d["d_final"], init_state=d["init"],
-                             valid_len=d["valid_len"], simt=simt)
+                             valid_len=d["valid_len"], simt=simt, split_scan=split_scan)
         out.update(g)
     torch.cuda.synchronize()
     return {k: v.double().cpu().numpy() for k, v in out.items() if v is not None}

@@ -117,6 +117,26 @@ def test_backward_is_deterministic():
         assert np.array_equal(a[k], b[k]), k
 
 
+# ---------------------------------------------------------------- the two chunk-state paths
+# The fused chunk-state scan (K1 + K3 + K4 along each (b, h) chain) is chosen
+# when batch * nheads >= 64, with two heads per CTA above 152 chains;
+# SSD_FLAG_SPLIT_SCAN forces the chunk-parallel K3 and the separate K4 pass.
+# Groups of an odd head count end in a one-head CTA of the two-head scan;
+# ragged valid lengths (one sample empty, one ending inside a chunk) and a
+# sequence length that is not a multiple of the chunk exercise the skipped
+# chunks and the partial last sub-stage.
+@pytest.mark.parametrize("split", [False, True])
+@pytest.mark.parametrize("Q,b,H,G", [(256, 5, 33, 3), (128, 5, 33, 3), (256, 2, 40, 2), (128, 2, 40, 2)])
+def test_bf16_chunk_state_paths(Q, b, H, G, split):
+    vl = [700, 0, 389, 512, 1] if b == 5 else [389, 700]
+    inp = generate_small(b, 700, H, 64, 128, G, seed=170 + Q + H, init_std=0.3, d_final_std=1.0,
+                         valid_len=vl, bf16=True)
+    gpu = run_gpu(inp, "bf16", Q, split_scan=split)
+    errs = compare(gpu, run_oracle(inp), TOL["bf16"], f"Q={Q} b={b} H={H} split={split}", chunk=Q)
+    padded_grads_zero(gpu, inp["valid_len"])
+    print(f"Q={Q} b={b} H={H} split={split}", {k: f"{v:.2e}" for k, v in errs.items()})
+
+
 # ---------------------------------------------------------------- full-size workloads
 @pytest.mark.parametrize("name", ["mamba2_130m", "mamba2_2p7b", "grouped_padded", "long_seq"])
 def test_workload_full_size(name):
