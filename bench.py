@@ -8,6 +8,7 @@ x/B/C/dy, fp32 dt/A/D), synthetic seeded inputs resident in HBM.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                     [--workload NAME] [--profile-case forward|step]
+                    [--op quat_scan|ydiag_siso|ydiag_mimo4]
 
 Prints one JSON line (rank 0).  Under torchrun (N > 1) every rank runs an
 independent replica of the workload (the scan has no data-path exchange) and
@@ -648,6 +649,141 @@ def run_ours(args, w, rank, world, local_rank):
     return line
 
 
+# ----------------------------------------------------------------------------- other ops
+# `--op NAME` measures one of the library's other entry points on its workload
+# (inputs resident in HBM and larger than L2, CUDA events on the launching
+# stream, W warm-up and K timed calls of forward and backward each) and prints
+# one line with its own metric, the HBM roofline of the op and the oracle
+# timed on the host cores on a bounded sample.
+OPS = ("quat_scan", "ydiag_siso", "ydiag_mimo4")
+
+
+def _event_time(fn, warmup: int, steps: int) -> float:
+    """Mean milliseconds per call of fn over `steps` calls after `warmup`."""
+    import torch
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(steps):
+        fn()
+    e1.record()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / steps
+
+
+def _wall_rate(fn, units: float, target_s: float) -> tuple:
+    """Units per second of the CPU function fn (repeated to about target_s)."""
+    t0 = time.perf_counter()
+    reps = 0
+    while True:
+        fn()
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= target_s or el * (reps + 1) / reps > 3 * target_s:
+            return units * reps / el, reps, el
+
+
+def run_op(args, local_rank):
+    import ctypes
+
+    import torch
+
+    from oracle import mamba3 as om3
+    from state_space_model_mamba_gb300 import mamba3, ssd
+    from state_space_model_mamba_gb300.inputs import MAMBA3_WORKLOADS, generate_diag, generate_quat
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    lib = mamba3._lib()
+    stream = lambda: ctypes.c_void_p(torch.cuda.current_stream(dev).cuda_stream)
+    P_ = lambda t: ctypes.c_void_p(t.data_ptr())
+    peaks, peak_src = load_peaks()
+    clocks = ClockSampler(local_rank)
+    up = lambda a, dt=torch.float32: torch.from_numpy(np.ascontiguousarray(a)).to(dev, dt)
+    if args.op == "quat_scan":
+        w = MAMBA3_WORKLOADS["quat_scan_2p7b"]
+        inp = generate_quat(w)
+        q, init, dcum = up(inp["q"]), up(inp["init"]), up(inp["d_cum"])
+        cum, dq, dinit = torch.empty_like(q), torch.empty_like(q), torch.empty_like(init)
+        wsf, wsb = mamba3.quat_workspace(q, False), mamba3.quat_workspace(q, True)
+        b, L, H, J, _ = q.shape
+
+        def fwd():
+            ssd._check(lib.m3_quat_cumprod(P_(q), P_(init), P_(cum), b, L, H, J, P_(wsf), wsf.numel(), stream()))
+
+        def bwd():
+            ssd._check(lib.m3_quat_cumprod_backward(P_(q), P_(init), P_(dcum), P_(dq), P_(dinit), b, L, H, J,
+                                                    P_(wsb), wsb.numel(), stream()))
+        bytes_f = 2 * q.nbytes + init.nbytes
+        bytes_b = 3 * q.nbytes + 2 * init.nbytes
+        tokens = w.tokens
+        config = {"workload": w.name, "batch": b, "seqlen": L, "nheads": H, "nblocks": J, "dtype": "f32"}
+        kernels = {"forward": "quat_seg_product + quat_seg_scan", "backward": "quat_bwd_segments + quat_bwd_apply"}
+        hs = 8  # oracle sample: batch 0, 8 heads
+
+        def cpu():
+            om3.quat_cumprod(inp["q"][:1, :, :hs], inp["init"][:1, :hs])
+            om3.quat_cumprod_backward_closed(inp["q"][:1, :, :hs], inp["init"][:1, :hs], inp["d_cum"][:1, :, :hs])
+        cpu_units, cpu_scale = L * hs / H, 1.0
+        sample = f"fp64 NumPy oracle fwd + closed-form bwd on batch 0, heads 0..{hs - 1} of {H}, all {L} steps; scaled to tokens/s of all heads"
+        metric = "Mamba-3 quaternion cumprod scan fwd+bwd tokens/sec (2.7B-layer tokens and heads, 1 GB300)"
+    else:
+        w = MAMBA3_WORKLOADS["ydiag_siso_2p7b" if args.op == "ydiag_siso" else "ydiag_mimo4"]
+        inp = generate_diag(w)
+        V, B, C, dY = (up(inp[k], torch.bfloat16) for k in ("V", "B", "C", "dY"))
+        g = up(inp["gamma"])
+        y, dV, dB, dC, dg = torch.empty_like(V), torch.empty_like(V), torch.empty_like(B), torch.empty_like(C), torch.empty_like(g)
+        T, m, H, Pd = V.shape
+        N = B.shape[3]
+
+        def fwd():
+            ssd._check(lib.m3_y_diag(ssd.SSD_BF16, P_(V), P_(B), P_(C), P_(g), P_(y), T, m, H, Pd, N, stream()))
+
+        def bwd():
+            ssd._check(lib.m3_y_diag_backward(ssd.SSD_BF16, P_(dY), P_(V), P_(B), P_(C), P_(g), P_(dV), P_(dB),
+                                              P_(dC), P_(dg), T, m, H, Pd, N, stream()))
+        bytes_f = 2 * V.nbytes + B.nbytes + C.nbytes + g.nbytes
+        bytes_b = 3 * V.nbytes + 2 * B.nbytes + 2 * C.nbytes + 2 * g.nbytes
+        tokens = T
+        config = {"workload": w.name, "tokens": T, "mimo": m, "nheads": H, "headdim": Pd, "dstate": N, "dtype": "bf16"}
+        kernels = {"forward": f"y_diag_fwd<bf16, {m}>", "backward": f"y_diag_bwd<bf16, {m}>"}
+        ts = 2048
+
+        def cpu():
+            sl = lambda a: a[:ts]
+            om3.y_diag(sl(inp["V"]), sl(inp["B"]), sl(inp["C"]), sl(inp["gamma"]))
+            om3.y_diag_vjp(sl(inp["dY"]), sl(inp["V"]), sl(inp["B"]), sl(inp["C"]), sl(inp["gamma"]))
+        cpu_units = ts
+        sample = f"fp64 NumPy oracle fwd + bwd on tokens 0..{ts - 1} of {T}, all heads"
+        metric = f"Mamba-3 gamma correction ({'SISO' if m == 1 else f'MIMO rank {m}'}) fwd+bwd tokens/sec (1 GB300)"
+    with clocks:
+        tf = _event_time(fwd, args.warmup, args.steps)
+        tb = _event_time(bwd, args.warmup, args.steps)
+    hbm = peaks["hbm_gbs"]
+    rate_cpu, reps, el = _wall_rate(cpu, cpu_units, min(args.cpu_seconds, 10.0))
+    cores = int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
+    return {
+        "metric": metric, "value": tokens / ((tf + tb) * 1e-3), "unit": UNIT, "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": tf + tb, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": config["dtype"], "data": "synthetic", "op": args.op,
+        "config": {**config, "l2": "inputs larger than L2; no flush"},
+        "forward": {"ms": tf, "tokens_per_s": tokens / (tf * 1e-3), "algorithmic_bytes": bytes_f,
+                    "achieved_gbs": bytes_f / (tf * 1e-3) / 1e9, "kernels": kernels["forward"]},
+        "backward": {"ms": tb, "tokens_per_s": tokens / (tb * 1e-3), "algorithmic_bytes": bytes_b,
+                     "achieved_gbs": bytes_b / (tb * 1e-3) / 1e9, "kernels": kernels["backward"]},
+        "roofline": {"bound": "hbm", "unit": "GB/s", "peak": hbm,
+                     "peak_source": f"{peak_src} (MEASURED_PEAKS.json)" if peak_src == "measured" else "fallback",
+                     "achieved": bytes_b / (tb * 1e-3) / 1e9, "frac": bytes_b / (tb * 1e-3) / 1e9 / hbm,
+                     "kernel": "backward (the longer of the two)", "traffic": None},
+        "gpu_launches": 4 * args.steps if args.op == "quat_scan" else 2 * args.steps,
+        "clocks": clocks.summary(),
+        "cpu_baseline": {"value": rate_cpu, "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": f"{sample}; {reps} repetition(s), {el:.1f} s; NumPy on one core "
+                                   f"({cores} available)"},
+    }
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -661,9 +797,14 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--profile-case", choices=("forward", "step"), default=None,
                     help="light run for ncu captures (see the module docstring)")
+    ap.add_argument("--op", choices=OPS, default=None,
+                    help="measure another entry point of the library (see run_op)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.op:
+        print(json.dumps(run_op(args, int(os.environ.get("LOCAL_RANK", "0")))), flush=True)
+        return
     rank, world, local_rank = dist_env()
     w = WORKLOADS[args.workload]
     if world > 1:

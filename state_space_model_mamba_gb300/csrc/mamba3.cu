@@ -1,0 +1,463 @@
+// mamba3.cu -- the Mamba-3 pieces of include/mamba3.h: the quaternion
+// cumulative-product scan with its closed-form recompute backward (burn-mamba,
+// "mamba3/quat_scan/backward.rs", "Gradient math") and the same-step gamma
+// correction with its backward (burn-mamba,
+// "mamba3/single_ssd/ssd/serial_recalculated/diag.rs").  Both are HBM-bound
+// streams: coalesced 16-byte (quaternion) or pair loads, fp32 arithmetic.
+//
+// Quaternion scan.  A chain is one (b, h, j); its L steps are cut into
+// segments of kSeg steps so that b * L / kSeg * H * J threads share the work.
+//   forward:  pass 1, per segment: the product of its steps;
+//             pass 2, per segment: the carry (init times the earlier segments'
+//             products, in order), then its steps from that carry.
+//   backward: pass 1, per segment: the local prefix products LP (from the
+//             identity at the segment start), their product, and
+//             T = sum_s conj(LP[s]) (x) d_cum[s];
+//             pass 2, per segment: the carry P_in (product of the earlier
+//             segments), the suffix sum from the later segments
+//             sum_{later} conj(P_in') (x) T', then one forward walk in which
+//             S[t] = suffix + conj(P_in) (x) (T - running sum of the segment's
+//             terms before t) -- the page's reverse cumsum without a reverse
+//             walk -- and G, d_q as on the page.
+#include <cuda_bf16.h>
+#include <stdio.h>
+
+#include "mamba3.h"
+#include "ssd_internal.cuh"
+
+namespace ssd {
+namespace {
+
+constexpr int kSeg = 128;  // steps per segment of the quaternion scan
+
+struct Qt {
+    float w, x, y, z;
+};
+__device__ __forceinline__ Qt qmul(Qt a, Qt b) {
+    return {a.w * b.w - a.x * b.x - a.y * b.y - a.z * b.z, a.w * b.x + a.x * b.w + a.y * b.z - a.z * b.y,
+            a.w * b.y - a.x * b.z + a.y * b.w + a.z * b.x, a.w * b.z + a.x * b.y - a.y * b.x + a.z * b.w};
+}
+__device__ __forceinline__ Qt qconj(Qt a) { return {a.w, -a.x, -a.y, -a.z}; }
+__device__ __forceinline__ Qt qadd(Qt a, Qt b) { return {a.w + b.w, a.x + b.x, a.y + b.y, a.z + b.z}; }
+__device__ __forceinline__ Qt qsub(Qt a, Qt b) { return {a.w - b.w, a.x - b.x, a.y - b.y, a.z - b.z}; }
+__device__ __forceinline__ Qt qld(const float *p) {
+    const float4 v = __ldg(reinterpret_cast<const float4 *>(p));
+    return {v.x, v.y, v.z, v.w};
+}
+__device__ __forceinline__ void qst(float *p, Qt a) { *reinterpret_cast<float4 *>(p) = make_float4(a.w, a.x, a.y, a.z); }
+__device__ __forceinline__ Qt qone() { return {1.f, 0.f, 0.f, 0.f}; }
+__device__ __forceinline__ Qt qzero() { return {0.f, 0.f, 0.f, 0.f}; }
+
+struct QShape {
+    long long b, L, C, S;  // C = H * J chains per sample, S segments
+};
+
+// thread -> (sample, segment, chain), the chain fastest (coalesced 16-byte accesses)
+__device__ __forceinline__ bool qmap(const QShape &s, long long &bi, long long &sg, long long &c) {
+    const long long idx = blockIdx.x * (long long)blockDim.x + threadIdx.x;
+    if (idx >= s.b * s.S * s.C) return false;
+    c = idx % s.C;
+    sg = (idx / s.C) % s.S;
+    bi = idx / (s.C * s.S);
+    return true;
+}
+
+__global__ void quat_seg_product(const float *__restrict__ q, float *__restrict__ segp, QShape s) {
+    long long bi, sg, c;
+    if (!qmap(s, bi, sg, c)) return;
+    const long long t0 = sg * kSeg, t1 = min(s.L, t0 + kSeg);
+    const float *qp = q + ((bi * s.L + t0) * s.C + c) * 4;
+    Qt acc = qone();
+#pragma unroll 8
+    for (long long t = t0; t < t1; ++t, qp += s.C * 4) acc = qmul(qld(qp), acc);
+    qst(segp + ((bi * s.S + sg) * s.C + c) * 4, acc);
+}
+
+__global__ void quat_seg_scan(const float *__restrict__ q, const float *__restrict__ init,
+                              const float *__restrict__ segp, float *__restrict__ cum, QShape s) {
+    long long bi, sg, c;
+    if (!qmap(s, bi, sg, c)) return;
+    Qt carry = init ? qld(init + (bi * s.C + c) * 4) : qone();
+    for (long long k = 0; k < sg; ++k) carry = qmul(qld(segp + ((bi * s.S + k) * s.C + c) * 4), carry);
+    const long long t0 = sg * kSeg, t1 = min(s.L, t0 + kSeg);
+    const long long off = ((bi * s.L + t0) * s.C + c) * 4;
+    const float *qp = q + off;
+    float *cp = cum + off;
+#pragma unroll 8
+    for (long long t = t0; t < t1; ++t, qp += s.C * 4, cp += s.C * 4) {
+        carry = qmul(qld(qp), carry);
+        qst(cp, carry);
+    }
+}
+
+__global__ void quat_bwd_segments(const float *__restrict__ q, const float *__restrict__ d_cum,
+                                  float *__restrict__ segp, float *__restrict__ segT, QShape s) {
+    long long bi, sg, c;
+    if (!qmap(s, bi, sg, c)) return;
+    const long long t0 = sg * kSeg, t1 = min(s.L, t0 + kSeg);
+    const long long off = ((bi * s.L + t0) * s.C + c) * 4;
+    const float *qp = q + off, *dp = d_cum + off;
+    Qt lp = qone(), acc = qzero();
+#pragma unroll 4
+    for (long long t = t0; t < t1; ++t, qp += s.C * 4, dp += s.C * 4) {
+        lp = qmul(qld(qp), lp);
+        acc = qadd(acc, qmul(qconj(lp), qld(dp)));
+    }
+    const long long so = ((bi * s.S + sg) * s.C + c) * 4;
+    qst(segp + so, lp);
+    qst(segT + so, acc);
+}
+
+__global__ void quat_bwd_apply(const float *__restrict__ q, const float *__restrict__ init,
+                               const float *__restrict__ d_cum, const float *__restrict__ segp,
+                               const float *__restrict__ segT, float *__restrict__ d_q, float *__restrict__ d_init,
+                               QShape s) {
+    long long bi, sg, c;
+    if (!qmap(s, bi, sg, c)) return;
+    // carry into the segment (product of the earlier segments, without init) and
+    // the later segments' part of the reverse cumsum
+    Qt prod = qone(), p_in = qone(), later = qzero();
+    for (long long k = 0; k < s.S; ++k) {
+        const long long so = ((bi * s.S + k) * s.C + c) * 4;
+        if (k == sg) p_in = prod;
+        else if (k > sg) later = qadd(later, qmul(qconj(prod), qld(segT + so)));
+        prod = qmul(qld(segp + so), prod);  // product of segments 0 .. k
+    }
+    const Qt own = qld(segT + ((bi * s.S + sg) * s.C + c) * 4);
+    const Qt in = init ? qld(init + (bi * s.C + c) * 4) : qone();
+    const Qt cin = qconj(p_in);
+    const long long t0 = sg * kSeg, t1 = min(s.L, t0 + kSeg);
+    const long long off = ((bi * s.L + t0) * s.C + c) * 4;
+    const float *qp = q + off, *dp = d_cum + off;
+    float *gp = d_q + off;
+    Qt lp = qone(), run = qzero(), p_prev = p_in;
+#pragma unroll 4
+    for (long long t = t0; t < t1; ++t, qp += s.C * 4, dp += s.C * 4, gp += s.C * 4) {
+        const Qt S_t = qadd(later, qmul(cin, qsub(own, run)));  // sum_{s >= t} conj(P[s]) (x) d_cum[s]
+        lp = qmul(qld(qp), lp);
+        const Qt P_t = qmul(lp, p_in);
+        const Qt G = qmul(P_t, S_t);
+        qst(gp, qmul(G, qconj(qmul(p_prev, in))));  // cum[t-1] = P[t-1] (x) init
+        run = qadd(run, qmul(qconj(lp), qld(dp)));
+        if (t == 0 && d_init) qst(d_init + (bi * s.C + c) * 4, S_t);
+        p_prev = P_t;
+    }
+}
+
+// ---------------------------------------------------------------- gamma correction
+template <typename T>
+struct Pair;
+template <>
+struct Pair<float> {
+    static __device__ __forceinline__ float2 ld(const float *p) { return __ldg(reinterpret_cast<const float2 *>(p)); }
+    static __device__ __forceinline__ void st(float *p, float2 v) { *reinterpret_cast<float2 *>(p) = v; }
+};
+template <>
+struct Pair<bf16> {
+    static __device__ __forceinline__ float2 ld(const bf16 *p) {
+        return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(p));
+    }
+    static __device__ __forceinline__ void st(bf16 *p, float2 v) {
+        *reinterpret_cast<__nv_bfloat162 *>(p) = __floats2bfloat162_rn(v.x, v.y);
+    }
+};
+
+struct DShape {
+    long long T;
+    int H, P, N;
+};
+
+// one warp per (token, head); lanes take pairs of the state / head axis, the
+// m x m products are reduced across the warp
+template <typename T, int M>
+__device__ __forceinline__ void qk_of(const T *C, const T *B, const DShape &s, long long t, int h, int lane,
+                                      float (&qk)[M][M]) {
+#pragma unroll
+    for (int o = 0; o < M; ++o)
+#pragma unroll
+        for (int i = 0; i < M; ++i) qk[o][i] = 0.f;
+    for (int e = 2 * lane; e < s.N; e += 64) {
+        float2 cv[M], bv[M];
+#pragma unroll
+        for (int i = 0; i < M; ++i) {
+            const long long row = ((t * M + i) * s.H + h) * (long long)s.N + e;
+            cv[i] = Pair<T>::ld(C + row);
+            bv[i] = Pair<T>::ld(B + row);
+        }
+#pragma unroll
+        for (int o = 0; o < M; ++o)
+#pragma unroll
+            for (int i = 0; i < M; ++i) qk[o][i] += cv[o].x * bv[i].x + cv[o].y * bv[i].y;
+    }
+#pragma unroll
+    for (int o = 0; o < M; ++o)
+#pragma unroll
+        for (int i = 0; i < M; ++i) qk[o][i] = warp_sum(qk[o][i]);
+}
+
+template <typename T, int M>
+__global__ void y_diag_fwd(const T *__restrict__ V, const T *__restrict__ B, const T *__restrict__ C,
+                           const float *__restrict__ gamma, T *__restrict__ y, DShape s) {
+    const long long w = (blockIdx.x * (long long)blockDim.x + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    if (w >= s.T * s.H) return;
+    const int h = (int)(w % s.H);
+    const long long t = w / s.H;
+    float qk[M][M];
+    qk_of<T, M>(C, B, s, t, h, lane, qk);
+    const float g = gamma[w];
+    for (int e = 2 * lane; e < s.P; e += 64) {
+        float2 vv[M];
+#pragma unroll
+        for (int i = 0; i < M; ++i) vv[i] = Pair<T>::ld(V + ((t * M + i) * s.H + h) * (long long)s.P + e);
+#pragma unroll
+        for (int o = 0; o < M; ++o) {
+            float2 a = make_float2(0.f, 0.f);
+#pragma unroll
+            for (int i = 0; i < M; ++i) {
+                a.x += qk[o][i] * vv[i].x;
+                a.y += qk[o][i] * vv[i].y;
+            }
+            Pair<T>::st(y + ((t * M + o) * s.H + h) * (long long)s.P + e, make_float2(g * a.x, g * a.y));
+        }
+    }
+}
+
+template <typename T, int M>
+__global__ void y_diag_bwd(const T *__restrict__ dY, const T *__restrict__ V, const T *__restrict__ B,
+                           const T *__restrict__ C, const float *__restrict__ gamma, T *__restrict__ dV,
+                           T *__restrict__ dB, T *__restrict__ dC, float *__restrict__ d_gamma, DShape s) {
+    const long long w = (blockIdx.x * (long long)blockDim.x + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    if (w >= s.T * s.H) return;
+    const int h = (int)(w % s.H);
+    const long long t = w / s.H;
+    float qk[M][M], dyv[M][M];
+    qk_of<T, M>(C, B, s, t, h, lane, qk);
+    // dyv[o, i] = sum_p dY[o, p] V[i, p]
+#pragma unroll
+    for (int o = 0; o < M; ++o)
+#pragma unroll
+        for (int i = 0; i < M; ++i) dyv[o][i] = 0.f;
+    for (int e = 2 * lane; e < s.P; e += 64) {
+        float2 dv[M], vv[M];
+#pragma unroll
+        for (int i = 0; i < M; ++i) {
+            const long long row = ((t * M + i) * s.H + h) * (long long)s.P + e;
+            dv[i] = Pair<T>::ld(dY + row);
+            vv[i] = Pair<T>::ld(V + row);
+        }
+#pragma unroll
+        for (int o = 0; o < M; ++o)
+#pragma unroll
+            for (int i = 0; i < M; ++i) dyv[o][i] += dv[o].x * vv[i].x + dv[o].y * vv[i].y;
+    }
+    float dg = 0.f;
+#pragma unroll
+    for (int o = 0; o < M; ++o)
+#pragma unroll
+        for (int i = 0; i < M; ++i) {
+            dyv[o][i] = warp_sum(dyv[o][i]);
+            dg += qk[o][i] * dyv[o][i];
+        }
+    const float g = gamma[w];
+    if (lane == 0) d_gamma[w] = dg;
+    // dV[i, p] = g sum_o qk[o, i] dY[o, p]
+    for (int e = 2 * lane; e < s.P; e += 64) {
+        float2 dv[M];
+#pragma unroll
+        for (int o = 0; o < M; ++o) dv[o] = Pair<T>::ld(dY + ((t * M + o) * s.H + h) * (long long)s.P + e);
+#pragma unroll
+        for (int i = 0; i < M; ++i) {
+            float2 a = make_float2(0.f, 0.f);
+#pragma unroll
+            for (int o = 0; o < M; ++o) {
+                a.x += qk[o][i] * dv[o].x;
+                a.y += qk[o][i] * dv[o].y;
+            }
+            Pair<T>::st(dV + ((t * M + i) * s.H + h) * (long long)s.P + e, make_float2(g * a.x, g * a.y));
+        }
+    }
+    // d_qk = g dyv;  dC[o, r] = sum_i d_qk[o, i] B[i, r];  dB[i, r] = sum_o d_qk[o, i] C[o, r]
+    for (int e = 2 * lane; e < s.N; e += 64) {
+        float2 cv[M], bv[M];
+#pragma unroll
+        for (int i = 0; i < M; ++i) {
+            const long long row = ((t * M + i) * s.H + h) * (long long)s.N + e;
+            cv[i] = Pair<T>::ld(C + row);
+            bv[i] = Pair<T>::ld(B + row);
+        }
+#pragma unroll
+        for (int o = 0; o < M; ++o) {
+            float2 a = make_float2(0.f, 0.f), b2 = make_float2(0.f, 0.f);
+#pragma unroll
+            for (int i = 0; i < M; ++i) {
+                a.x += dyv[o][i] * bv[i].x;
+                a.y += dyv[o][i] * bv[i].y;
+                b2.x += dyv[i][o] * cv[i].x;
+                b2.y += dyv[i][o] * cv[i].y;
+            }
+            const long long row = ((t * M + o) * s.H + h) * (long long)s.N + e;
+            Pair<T>::st(dC + row, make_float2(g * a.x, g * a.y));
+            Pair<T>::st(dB + row, make_float2(g * b2.x, g * b2.y));
+        }
+    }
+}
+
+// ---------------------------------------------------------------- host side
+ssd_status m3_fail(ssd_status st, const char *msg) {
+    record_error(msg);
+    return st;
+}
+bool al16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
+
+ssd_status quat_check(const void *const *ptrs, int nreq, int64_t b, int64_t L, int64_t H, int64_t J) {
+    if (b < 1 || L < 1 || H < 1 || J < 1) return m3_fail(SSD_ERR_INVALID_ARG, "every dimension must be >= 1");
+    if ((double)b * L * H * J * 4 > 4.0e15) return m3_fail(SSD_ERR_UNSUPPORTED, "problem too large");
+    for (int i = 0; i < nreq; ++i)
+        if (!ptrs[i] || !al16(ptrs[i])) return m3_fail(SSD_ERR_INVALID_ARG, "a required pointer is NULL or not 16-byte aligned");
+    return SSD_OK;
+}
+
+QShape qshape(int64_t b, int64_t L, int64_t H, int64_t J) {
+    return QShape{b, L, H * J, (L + kSeg - 1) / kSeg};
+}
+
+unsigned qgrid(const QShape &s) { return (unsigned)((s.b * s.S * s.C + 255) / 256); }
+
+template <typename T, int M>
+cudaError_t launch_y_fwd(const DShape &s, const void *V, const void *B, const void *C, const float *g, void *y,
+                         cudaStream_t st) {
+    const long long threads = s.T * s.H * 32;
+    y_diag_fwd<T, M><<<(unsigned)((threads + 255) / 256), 256, 0, st>>>(
+        (const T *)V, (const T *)B, (const T *)C, g, (T *)y, s);
+    return cudaGetLastError();
+}
+template <typename T, int M>
+cudaError_t launch_y_bwd(const DShape &s, const void *dY, const void *V, const void *B, const void *C,
+                         const float *g, void *dV, void *dB, void *dC, float *dg, cudaStream_t st) {
+    const long long threads = s.T * s.H * 32;
+    y_diag_bwd<T, M><<<(unsigned)((threads + 255) / 256), 256, 0, st>>>(
+        (const T *)dY, (const T *)V, (const T *)B, (const T *)C, g, (T *)dV, (T *)dB, (T *)dC, dg, s);
+    return cudaGetLastError();
+}
+
+ssd_status y_check(ssd_dtype dtype, const void *const *ptrs, int n, int64_t T, int64_t m, int64_t H, int64_t P,
+                   int64_t N) {
+    if (dtype != SSD_F32 && dtype != SSD_BF16) return m3_fail(SSD_ERR_INVALID_ARG, "unknown dtype");
+    if (T < 1 || m < 1 || H < 1 || P < 1 || N < 1) return m3_fail(SSD_ERR_INVALID_ARG, "every dimension must be >= 1");
+    if (m > 4) return m3_fail(SSD_ERR_UNSUPPORTED, "mimo rank above 4");
+    if ((P & 1) || (N & 1)) return m3_fail(SSD_ERR_UNSUPPORTED, "headdim and dstate must be even");
+    if (P > (1 << 20) || N > (1 << 20) || H > (1 << 20) || (double)T * H * 32 > 4.0e18)
+        return m3_fail(SSD_ERR_UNSUPPORTED, "problem too large");
+    for (int i = 0; i < n; ++i)
+        if (!ptrs[i] || !al16(ptrs[i])) return m3_fail(SSD_ERR_INVALID_ARG, "a required pointer is NULL or not 16-byte aligned");
+    return SSD_OK;
+}
+
+ssd_status cuda_status(cudaError_t e) {
+    if (e == cudaSuccess) return SSD_OK;
+    char msg[256];
+    snprintf(msg, sizeof(msg), "launch failed: %s", cudaGetErrorString(e));
+    return m3_fail(SSD_ERR_CUDA, msg);
+}
+
+}  // namespace
+}  // namespace ssd
+
+using namespace ssd;
+
+extern "C" {
+
+size_t m3_quat_workspace_bytes(int64_t b, int64_t L, int64_t H, int64_t J, int backward) {
+    if (b < 1 || L < 1 || H < 1 || J < 1) return 0;
+    const QShape s = qshape(b, L, H, J);
+    return (size_t)(backward ? 2 : 1) * (size_t)(s.b * s.S * s.C * 4) * sizeof(float);
+}
+
+ssd_status m3_quat_cumprod(const float *q, const float *init, float *cum, int64_t b, int64_t L, int64_t H,
+                           int64_t J, void *workspace, size_t workspace_bytes, void *stream) {
+    record_error("");
+    const void *req[] = {q, cum, workspace};
+    ssd_status st = quat_check(req, 3, b, L, H, J);
+    if (st != SSD_OK) return st;
+    if (init && !al16(init)) return m3_fail(SSD_ERR_INVALID_ARG, "init is not 16-byte aligned");
+    if (workspace_bytes < m3_quat_workspace_bytes(b, L, H, J, 0)) return m3_fail(SSD_ERR_WORKSPACE, "workspace too small");
+    const QShape s = qshape(b, L, H, J);
+    cudaStream_t cs = (cudaStream_t)stream;
+    float *segp = (float *)workspace;
+    quat_seg_product<<<qgrid(s), 256, 0, cs>>>(q, segp, s);
+    quat_seg_scan<<<qgrid(s), 256, 0, cs>>>(q, init, segp, cum, s);
+    return cuda_status(cudaGetLastError());
+}
+
+ssd_status m3_quat_cumprod_backward(const float *q, const float *init, const float *d_cum, float *d_q,
+                                    float *d_init, int64_t b, int64_t L, int64_t H, int64_t J, void *workspace,
+                                    size_t workspace_bytes, void *stream) {
+    record_error("");
+    const void *req[] = {q, d_cum, d_q, workspace};
+    ssd_status st = quat_check(req, 4, b, L, H, J);
+    if (st != SSD_OK) return st;
+    if ((init && !al16(init)) || (d_init && !al16(d_init)))
+        return m3_fail(SSD_ERR_INVALID_ARG, "init / d_init is not 16-byte aligned");
+    if (workspace_bytes < m3_quat_workspace_bytes(b, L, H, J, 1)) return m3_fail(SSD_ERR_WORKSPACE, "workspace too small");
+    const QShape s = qshape(b, L, H, J);
+    cudaStream_t cs = (cudaStream_t)stream;
+    float *segp = (float *)workspace, *segT = segp + s.b * s.S * s.C * 4;
+    quat_bwd_segments<<<qgrid(s), 256, 0, cs>>>(q, d_cum, segp, segT, s);
+    quat_bwd_apply<<<qgrid(s), 256, 0, cs>>>(q, init, d_cum, segp, segT, d_q, d_init, s);
+    return cuda_status(cudaGetLastError());
+}
+
+ssd_status m3_y_diag(ssd_dtype dtype, const void *V, const void *B, const void *C, const float *gamma, void *y,
+                     int64_t T, int64_t m, int64_t H, int64_t P, int64_t N, void *stream) {
+    record_error("");
+    const void *req[] = {V, B, C, gamma, y};
+    ssd_status st = y_check(dtype, req, 5, T, m, H, P, N);
+    if (st != SSD_OK) return st;
+    const DShape s{T, (int)H, (int)P, (int)N};
+    cudaStream_t cs = (cudaStream_t)stream;
+    cudaError_t e;
+#define Y_FWD(TY)                                                              \
+    switch (m) {                                                               \
+        case 1: e = launch_y_fwd<TY, 1>(s, V, B, C, gamma, y, cs); break;      \
+        case 2: e = launch_y_fwd<TY, 2>(s, V, B, C, gamma, y, cs); break;      \
+        case 3: e = launch_y_fwd<TY, 3>(s, V, B, C, gamma, y, cs); break;      \
+        default: e = launch_y_fwd<TY, 4>(s, V, B, C, gamma, y, cs); break;     \
+    }
+    if (dtype == SSD_F32) {
+        Y_FWD(float)
+    } else {
+        Y_FWD(bf16)
+    }
+#undef Y_FWD
+    return cuda_status(e);
+}
+
+ssd_status m3_y_diag_backward(ssd_dtype dtype, const void *dY, const void *V, const void *B, const void *C,
+                              const float *gamma, void *dV, void *dB, void *dC, float *d_gamma, int64_t T,
+                              int64_t m, int64_t H, int64_t P, int64_t N, void *stream) {
+    record_error("");
+    const void *req[] = {dY, V, B, C, gamma, dV, dB, dC, d_gamma};
+    ssd_status st = y_check(dtype, req, 9, T, m, H, P, N);
+    if (st != SSD_OK) return st;
+    const DShape s{T, (int)H, (int)P, (int)N};
+    cudaStream_t cs = (cudaStream_t)stream;
+    cudaError_t e;
+#define Y_BWD(TY)                                                                                \
+    switch (m) {                                                                                 \
+        case 1: e = launch_y_bwd<TY, 1>(s, dY, V, B, C, gamma, dV, dB, dC, d_gamma, cs); break;  \
+        case 2: e = launch_y_bwd<TY, 2>(s, dY, V, B, C, gamma, dV, dB, dC, d_gamma, cs); break;  \
+        case 3: e = launch_y_bwd<TY, 3>(s, dY, V, B, C, gamma, dV, dB, dC, d_gamma, cs); break;  \
+        default: e = launch_y_bwd<TY, 4>(s, dY, V, B, C, gamma, dV, dB, dC, d_gamma, cs); break; \
+    }
+    if (dtype == SSD_F32) {
+        Y_BWD(float)
+    } else {
+        Y_BWD(bf16)
+    }
+#undef Y_BWD
+    return cuda_status(e);
+}
+
+}  // extern "C"

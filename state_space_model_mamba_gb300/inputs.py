@@ -124,3 +124,78 @@ def generate_small(b, L, H, P, N, G, seed=0, dt_mu=-2.0, init_std=0.0, d_final_s
     if valid_len is not None:
         out["valid_len"] = np.asarray(valid_len, np.int32)
     return out
+
+
+# ---------------------------------------------------------------- Mamba-3 pieces
+# Quaternion scan: per step a unit quaternion (cos(phi/2), sin(phi/2) u) with a
+# uniformly random axis u and phi ~ N(0, angle_std^2), drawn in fp64 and stored
+# in fp32; init a random unit quaternion; d_cum ~ N(0, 1).  Draw order: axis,
+# phi, init axis, init angle, d_cum.
+# Gamma correction: V, B, C, dY ~ N(0, 1) (rounded to bf16 values when the
+# workload stores bf16), gamma ~ U(0, 1).  Draw order: V, B, C, gamma, dY.
+@dataclass(frozen=True)
+class QuatWorkload:
+    name: str
+    batch: int
+    seqlen: int
+    nheads: int
+    nblocks: int           # quaternion blocks per head (J)
+    angle_std: float = 0.3
+    seed: int = 2000
+
+    @property
+    def tokens(self) -> int:
+        return self.batch * self.seqlen
+
+
+@dataclass(frozen=True)
+class DiagWorkload:
+    name: str
+    tokens: int            # the page's (b, n, l) axes flattened
+    mimo: int              # m
+    nheads: int
+    headdim: int
+    dstate: int
+    dtype: str = "bf16"
+    seed: int = 3000
+
+
+# at the Mamba-2 2.7B layer's token count (2 x 8192) and head count
+MAMBA3_WORKLOADS = {
+    "quat_scan_2p7b": QuatWorkload("quat_scan_2p7b", 2, 8192, 80, 8, seed=2001),
+    "ydiag_siso_2p7b": DiagWorkload("ydiag_siso_2p7b", 16384, 1, 80, 64, 128, seed=3001),
+    "ydiag_mimo4": DiagWorkload("ydiag_mimo4", 16384, 4, 16, 64, 128, seed=3002),
+}
+
+
+def _unit_quaternions(rng, shape, angle_std):
+    axis = rng.standard_normal(shape + (3,))
+    axis /= np.linalg.norm(axis, axis=-1, keepdims=True)
+    phi = rng.standard_normal(shape) * angle_std
+    q = np.concatenate([np.cos(phi / 2)[..., None], np.sin(phi / 2)[..., None] * axis], axis=-1)
+    return q.astype(np.float32)
+
+
+def generate_quat(w: QuatWorkload, seed: int | None = None) -> dict:
+    """q, d_cum [b, L, H, J, 4] and init [b, H, J, 4], fp32."""
+    rng = np.random.default_rng(w.seed if seed is None else seed)
+    b, L, H, J = w.batch, w.seqlen, w.nheads, w.nblocks
+    q = _unit_quaternions(rng, (b, L, H, J), w.angle_std)
+    init = _unit_quaternions(rng, (b, H, J), 1.0)
+    d_cum = rng.standard_normal((b, L, H, J, 4), dtype=np.float32)
+    return dict(q=q, init=init, d_cum=d_cum)
+
+
+def generate_diag(w: DiagWorkload, seed: int | None = None) -> dict:
+    """V, dY [T, m, H, P]; B, C [T, m, H, N]; gamma [T, H]; fp32 arrays."""
+    rng = np.random.default_rng(w.seed if seed is None else seed)
+    T, m, H, P, N = w.tokens, w.mimo, w.nheads, w.headdim, w.dstate
+    f32 = np.float32
+    V = rng.standard_normal((T, m, H, P), dtype=f32)
+    B = rng.standard_normal((T, m, H, N), dtype=f32)
+    C = rng.standard_normal((T, m, H, N), dtype=f32)
+    gamma = rng.uniform(0.0, 1.0, (T, H)).astype(f32)
+    dY = rng.standard_normal((T, m, H, P), dtype=f32)
+    if w.dtype == "bf16":
+        V, B, C, dY = (round_to_bf16(a) for a in (V, B, C, dY))
+    return dict(V=V, B=B, C=C, gamma=gamma, dY=dY)

@@ -25,7 +25,7 @@ def declared_functions():
         if fn.endswith(".h"):
             text = open(os.path.join(ROOT, "include", fn)).read()
             text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-            names += re.findall(r"\b(ssd_[a-z_]+)\s*\(", text)
+            names += re.findall(r"\b((?:ssd|m3)_[a-z0-9_]+)\s*\(", text)
     return sorted(set(names))
 
 
@@ -35,6 +35,28 @@ def test_every_declared_symbol_is_exported(lib):
     for n in names:
         assert hasattr(lib, n), f"{n} declared in include/ but not exported"
     assert set(ssd.EXPORTED) <= set(names)
+    from state_space_model_mamba_gb300 import mamba3
+    assert set(mamba3.EXPORTED) <= set(names)
+
+
+def test_mamba3_calls_reject_bad_arguments_before_launch(lib):
+    from state_space_model_mamba_gb300 import mamba3
+    m = mamba3._lib()
+    buf = ctypes.c_void_p(1 << 20)  # never dereferenced: every call below fails validation first
+    assert m.m3_quat_workspace_bytes(2, 300, 3, 2, 0) == 2 * 3 * 6 * 16
+    assert m.m3_quat_workspace_bytes(2, 300, 3, 2, 1) == 2 * 2 * 3 * 6 * 16
+    assert m.m3_quat_workspace_bytes(0, 300, 3, 2, 0) == 0
+    assert m.m3_quat_cumprod(None, None, buf, 1, 8, 1, 1, buf, 1 << 20, None) == ssd.SSD_ERR_INVALID_ARG
+    assert m.m3_quat_cumprod(buf, None, buf, 1, 0, 1, 1, buf, 1 << 20, None) == ssd.SSD_ERR_INVALID_ARG
+    assert m.m3_quat_cumprod(buf, None, buf, 1, 300, 1, 1, buf, 16, None) == ssd.SSD_ERR_WORKSPACE
+    assert m.m3_quat_cumprod_backward(buf, None, ctypes.c_void_p((1 << 20) + 4), buf, None, 1, 8, 1, 1, buf,
+                                      1 << 20, None) == ssd.SSD_ERR_INVALID_ARG
+    args = [buf] * 5
+    assert m.m3_y_diag(ssd.SSD_BF16, *args, 4, 5, 2, 64, 128, None) == ssd.SSD_ERR_UNSUPPORTED
+    assert m.m3_y_diag(ssd.SSD_BF16, *args, 4, 1, 2, 63, 128, None) == ssd.SSD_ERR_UNSUPPORTED
+    assert m.m3_y_diag(7, *args, 4, 1, 2, 64, 128, None) == ssd.SSD_ERR_INVALID_ARG
+    assert m.m3_y_diag_backward(ssd.SSD_F32, *([buf] * 8), None, 4, 1, 2, 64, 128, None) == ssd.SSD_ERR_INVALID_ARG
+    assert b"NULL" in lib.ssd_last_error()
 
 
 def test_version_and_status_strings(lib):
