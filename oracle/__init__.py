@@ -51,6 +51,8 @@ def _bind(lib):
                                         + [dp] * 7 + [ctypes.c_int])
     lib.ssd_oracle_backward.restype = ctypes.c_int
     lib.ssd_oracle_num_threads.restype = ctypes.c_int
+    lib.ssd_oracle_state_moments.argtypes = [i64] * 6 + [dp] * 5 + [ip, dp, dp, ctypes.c_int]
+    lib.ssd_oracle_state_moments.restype = ctypes.c_int
     return lib
 
 
@@ -139,6 +141,23 @@ def backward(x, dt, A, B, C, D, init, valid_len, dy, d_final=None, nthreads=0, l
     if rc != 0:
         raise RuntimeError(f"ssd_oracle_backward failed with code {rc}")
     return out
+
+
+def state_moments(x, dt, A, B, init=None, valid_len=None, nthreads=0, lib=None):
+    """Raw moments of the per-token states (the states after each valid token):
+    m2 [b,H,N,N] = sum_t S_t^T S_t, m1 [b,H,N] = sum_t sum_p S_t[p,:], and the
+    sample count per sample, valid_len * P (int64 [b])."""
+    x, dt, A, B, init = map(_f64, (x, dt, A, B, init))
+    nb, L, H, P, N, G = _dims(x, B, None)
+    vl = None if valid_len is None else np.ascontiguousarray(valid_len, dtype=np.int32)
+    m2 = np.empty((nb, H, N, N), np.float64)
+    m1 = np.empty((nb, H, N), np.float64)
+    rc = (lib or _load()).ssd_oracle_state_moments(nb, L, H, P, N, G, _ptr(x), _ptr(dt), _ptr(A), _ptr(B),
+                                                   _ptr(init), _ptr(vl), _ptr(m2), _ptr(m1), int(nthreads))
+    if rc != 0:
+        raise RuntimeError(f"ssd_oracle_state_moments failed with code {rc}")
+    V = np.full(nb, L, np.int64) if vl is None else np.clip(vl.astype(np.int64), 0, L)
+    return m2, m1, V * P
 
 
 def loss(y, final, dy, d_final):

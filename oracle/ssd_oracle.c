@@ -293,3 +293,61 @@ int ssd_oracle_backward(int64_t nb, int64_t L, int64_t H, int64_t P, int64_t N, 
     free(dD_part);
     return err;
 }
+
+/*
+ * Raw moments of the per-token states (burn-mamba, "modules/state_moments.rs",
+ * StateMoments: each state row, one (token, p) pair, is a sample in R^N).  For
+ * every (b, h), with S_t the state after token t of the recurrence above
+ * (t < V = valid_len[b]):
+ *
+ *     m2[b,h] = sum_t S_t^T S_t            (N x N; the transpose pools the P rows)
+ *     m1[b,h] = sum_t sum_p S_t[p, :]      (N)
+ *
+ * The sample count of a (b, h) slice is V * P.  Layouts: m2 [b, H, N, N],
+ * m1 [b, H, N]; the other arguments as ssd_oracle_forward.
+ */
+int ssd_oracle_state_moments(int64_t nb, int64_t L, int64_t H, int64_t P, int64_t N, int64_t G,
+                             const double *x, const double *dt, const double *A, const double *Bm,
+                             const double *init, const int32_t *valid_len, double *m2, double *m1,
+                             int nthreads) {
+    if (check_dims(nb, L, H, P, N, G)) return 1;
+    const int64_t hpg = H / G;
+    const int64_t ntask = nb * H;
+    int err = 0;
+    if (nthreads <= 0) nthreads = ssd_oracle_num_threads();
+#pragma omp parallel for schedule(dynamic, 1) num_threads(nthreads)
+    for (int64_t task = 0; task < ntask; ++task) {
+        const int64_t bi = task / H, h = task % H, g = h / hpg;
+        const int64_t V = clamp_len(valid_len, bi, L);
+        double *S = (double *)malloc(sizeof(double) * P * N);
+        if (!S) {
+#pragma omp atomic write
+            err = 2;
+            continue;
+        }
+        if (init)
+            memcpy(S, init + (bi * H + h) * P * N, sizeof(double) * P * N);
+        else
+            memset(S, 0, sizeof(double) * P * N);
+        double *M2 = m2 + task * N * N, *M1 = m1 + task * N;
+        memset(M2, 0, sizeof(double) * N * N);
+        memset(M1, 0, sizeof(double) * N);
+        for (int64_t t = 0; t < V; ++t) {
+            const double dtt = dt[(bi * H + h) * L + t];
+            step_state(S, P, N, exp(dtt * A[h]), dtt, x + ((bi * L + t) * H + h) * P,
+                       Bm + ((bi * L + t) * G + g) * N);
+            for (int64_t p = 0; p < P; ++p) {
+                const double *row = S + p * N;
+                for (int64_t r = 0; r < N; ++r) {
+                    M1[r] += row[r];
+                    const double v = row[r];
+                    double *mr = M2 + r * N;
+                    for (int64_t r2 = 0; r2 < N; ++r2) mr[r2] += v * row[r2];
+                }
+            }
+        }
+        free(S);
+    }
+    return err;
+}
+

@@ -151,6 +151,8 @@ template <>
 struct Pair<float> {
     static __device__ __forceinline__ float2 ld(const float *p) { return __ldg(reinterpret_cast<const float2 *>(p)); }
     static __device__ __forceinline__ void st(float *p, float2 v) { *reinterpret_cast<float2 *>(p) = v; }
+    static __device__ __forceinline__ float4 ld4(const float *p) { return __ldg(reinterpret_cast<const float4 *>(p)); }
+    static __device__ __forceinline__ void st4(float *p, float4 v) { *reinterpret_cast<float4 *>(p) = v; }
 };
 template <>
 struct Pair<bf16> {
@@ -160,7 +162,21 @@ struct Pair<bf16> {
     static __device__ __forceinline__ void st(bf16 *p, float2 v) {
         *reinterpret_cast<__nv_bfloat162 *>(p) = __floats2bfloat162_rn(v.x, v.y);
     }
+    static __device__ __forceinline__ float4 ld4(const bf16 *p) {
+        const uint2 u = __ldg(reinterpret_cast<const uint2 *>(p));
+        const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&u.x));
+        const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&u.y));
+        return make_float4(a.x, a.y, b.x, b.y);
+    }
+    static __device__ __forceinline__ void st4(bf16 *p, float4 v) {
+        __nv_bfloat162 a = __floats2bfloat162_rn(v.x, v.y), b = __floats2bfloat162_rn(v.z, v.w);
+        uint2 u;
+        u.x = *reinterpret_cast<uint32_t *>(&a);
+        u.y = *reinterpret_cast<uint32_t *>(&b);
+        *reinterpret_cast<uint2 *>(p) = u;
+    }
 };
+__device__ __forceinline__ float dot4(float4 a, float4 b) { return a.x * b.x + a.y * b.y + a.z * b.z + a.w * b.w; }
 
 struct DShape {
     long long T;
@@ -176,18 +192,34 @@ __device__ __forceinline__ void qk_of(const T *C, const T *B, const DShape &s, l
     for (int o = 0; o < M; ++o)
 #pragma unroll
         for (int i = 0; i < M; ++i) qk[o][i] = 0.f;
-    for (int e = 2 * lane; e < s.N; e += 64) {
-        float2 cv[M], bv[M];
+    if ((s.N & 3) == 0) {  // 8- or 16-byte loads: four elements per lane
+        for (int e = 4 * lane; e < s.N; e += 128) {
+            float4 cv[M], bv[M];
 #pragma unroll
-        for (int i = 0; i < M; ++i) {
-            const long long row = ((t * M + i) * s.H + h) * (long long)s.N + e;
-            cv[i] = Pair<T>::ld(C + row);
-            bv[i] = Pair<T>::ld(B + row);
+            for (int i = 0; i < M; ++i) {
+                const long long row = ((t * M + i) * s.H + h) * (long long)s.N + e;
+                cv[i] = Pair<T>::ld4(C + row);
+                bv[i] = Pair<T>::ld4(B + row);
+            }
+#pragma unroll
+            for (int o = 0; o < M; ++o)
+#pragma unroll
+                for (int i = 0; i < M; ++i) qk[o][i] += dot4(cv[o], bv[i]);
         }
+    } else {
+        for (int e = 2 * lane; e < s.N; e += 64) {
+            float2 cv[M], bv[M];
 #pragma unroll
-        for (int o = 0; o < M; ++o)
+            for (int i = 0; i < M; ++i) {
+                const long long row = ((t * M + i) * s.H + h) * (long long)s.N + e;
+                cv[i] = Pair<T>::ld(C + row);
+                bv[i] = Pair<T>::ld(B + row);
+            }
 #pragma unroll
-            for (int i = 0; i < M; ++i) qk[o][i] += cv[o].x * bv[i].x + cv[o].y * bv[i].y;
+            for (int o = 0; o < M; ++o)
+#pragma unroll
+                for (int i = 0; i < M; ++i) qk[o][i] += cv[o].x * bv[i].x + cv[o].y * bv[i].y;
+        }
     }
 #pragma unroll
     for (int o = 0; o < M; ++o)
@@ -279,27 +311,57 @@ __global__ void y_diag_bwd(const T *__restrict__ dY, const T *__restrict__ V, co
         }
     }
     // d_qk = g dyv;  dC[o, r] = sum_i d_qk[o, i] B[i, r];  dB[i, r] = sum_o d_qk[o, i] C[o, r]
-    for (int e = 2 * lane; e < s.N; e += 64) {
-        float2 cv[M], bv[M];
-#pragma unroll
-        for (int i = 0; i < M; ++i) {
-            const long long row = ((t * M + i) * s.H + h) * (long long)s.N + e;
-            cv[i] = Pair<T>::ld(C + row);
-            bv[i] = Pair<T>::ld(B + row);
-        }
-#pragma unroll
-        for (int o = 0; o < M; ++o) {
-            float2 a = make_float2(0.f, 0.f), b2 = make_float2(0.f, 0.f);
+    if ((s.N & 3) == 0) {
+        for (int e = 4 * lane; e < s.N; e += 128) {
+            float4 cv[M], bv[M];
 #pragma unroll
             for (int i = 0; i < M; ++i) {
-                a.x += dyv[o][i] * bv[i].x;
-                a.y += dyv[o][i] * bv[i].y;
-                b2.x += dyv[i][o] * cv[i].x;
-                b2.y += dyv[i][o] * cv[i].y;
+                const long long row = ((t * M + i) * s.H + h) * (long long)s.N + e;
+                cv[i] = Pair<T>::ld4(C + row);
+                bv[i] = Pair<T>::ld4(B + row);
             }
-            const long long row = ((t * M + o) * s.H + h) * (long long)s.N + e;
-            Pair<T>::st(dC + row, make_float2(g * a.x, g * a.y));
-            Pair<T>::st(dB + row, make_float2(g * b2.x, g * b2.y));
+#pragma unroll
+            for (int o = 0; o < M; ++o) {
+                float4 a = make_float4(0.f, 0.f, 0.f, 0.f), b2 = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                for (int i = 0; i < M; ++i) {
+                    a.x += dyv[o][i] * bv[i].x;
+                    a.y += dyv[o][i] * bv[i].y;
+                    a.z += dyv[o][i] * bv[i].z;
+                    a.w += dyv[o][i] * bv[i].w;
+                    b2.x += dyv[i][o] * cv[i].x;
+                    b2.y += dyv[i][o] * cv[i].y;
+                    b2.z += dyv[i][o] * cv[i].z;
+                    b2.w += dyv[i][o] * cv[i].w;
+                }
+                const long long row = ((t * M + o) * s.H + h) * (long long)s.N + e;
+                Pair<T>::st4(dC + row, make_float4(g * a.x, g * a.y, g * a.z, g * a.w));
+                Pair<T>::st4(dB + row, make_float4(g * b2.x, g * b2.y, g * b2.z, g * b2.w));
+            }
+        }
+    } else {
+        for (int e = 2 * lane; e < s.N; e += 64) {
+            float2 cv[M], bv[M];
+#pragma unroll
+            for (int i = 0; i < M; ++i) {
+                const long long row = ((t * M + i) * s.H + h) * (long long)s.N + e;
+                cv[i] = Pair<T>::ld(C + row);
+                bv[i] = Pair<T>::ld(B + row);
+            }
+#pragma unroll
+            for (int o = 0; o < M; ++o) {
+                float2 a = make_float2(0.f, 0.f), b2 = make_float2(0.f, 0.f);
+#pragma unroll
+                for (int i = 0; i < M; ++i) {
+                    a.x += dyv[o][i] * bv[i].x;
+                    a.y += dyv[o][i] * bv[i].y;
+                    b2.x += dyv[i][o] * cv[i].x;
+                    b2.y += dyv[i][o] * cv[i].y;
+                }
+                const long long row = ((t * M + o) * s.H + h) * (long long)s.N + e;
+                Pair<T>::st(dC + row, make_float2(g * a.x, g * a.y));
+                Pair<T>::st(dB + row, make_float2(g * b2.x, g * b2.y));
+            }
         }
     }
 }
