@@ -8,7 +8,7 @@ x/B/C/dy, fp32 dt/A/D), synthetic seeded inputs resident in HBM.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                     [--workload NAME] [--profile-case forward|step]
-                    [--op quat_scan|ydiag_siso|ydiag_mimo4]
+                    [--op quat_scan|ydiag_siso|ydiag_mimo4|state_moments]
 
 Prints one JSON line (rank 0).  Under torchrun (N > 1) every rank runs an
 independent replica of the workload (the scan has no data-path exchange) and
@@ -173,6 +173,12 @@ def kernel_costs(w, tc: bool) -> dict:
         "bwd_group": (b * n * G * 4.0 * tri * N + b * n * H * 4.0 * Q * P * N,
                       2 * x_b + 2 * sts * st + 4 * bc_b + 2 * cum_b),
         "bwd_k1_chunk_cumsum": (0.0, 4 * cum_b + 8 * tok_h),
+        # state moments (128-token chunks): G = X X^T, Y = F B + (2 alpha X) s, A += B^T Y + c0 s^T s;
+        # reads x, B, the bf16 chunk-input states, cumA and dt, writes the fp32 range partials
+        "moments": (b * -(-L // 128) * H * 2.0 * 128 * 128 * (64 + 2 * (128 + 64)) * (P * N / (64 * 128)),
+                    x_b + bc_b + 2 * b * -(-L // 128) * H * P * N + 8 * b * H * -(-L // 128) * 128
+                    + 4 * b * H * (N * N + N)),
+        "moments_reduce": (0.0, 2 * 4 * b * H * (N * N + N)),
         # debug check (SSD_FLAG_CHECK_FINITE, never timed): reads the backward's outputs,
         # cumA, endA and the chunk states and their gradients once
         "check_finite": (0.0, x_b + 4 * tok_h + 2 * bc_b + cum_b + 4 * b * H * n + 2 * sts * st),
@@ -655,7 +661,7 @@ def run_ours(args, w, rank, world, local_rank):
 # stream, W warm-up and K timed calls of forward and backward each) and prints
 # one line with its own metric, the HBM roofline of the op and the oracle
 # timed on the host cores on a bounded sample.
-OPS = ("quat_scan", "ydiag_siso", "ydiag_mimo4")
+OPS = ("quat_scan", "ydiag_siso", "ydiag_mimo4", "state_moments")
 
 
 def _event_time(fn, warmup: int, steps: int) -> float:
@@ -701,6 +707,8 @@ def run_op(args, local_rank):
     peaks, peak_src = load_peaks()
     clocks = ClockSampler(local_rank)
     up = lambda a, dt=torch.float32: torch.from_numpy(np.ascontiguousarray(a)).to(dev, dt)
+    if args.op == "state_moments":
+        return run_moments(args, dev, peaks, peak_src, clocks)
     if args.op == "quat_scan":
         w = MAMBA3_WORKLOADS["quat_scan_2p7b"]
         inp = generate_quat(w)
@@ -782,6 +790,76 @@ def run_op(args, local_rank):
                          "sample": f"{sample}; {reps} repetition(s), {el:.1f} s; NumPy on one core "
                                    f"({cores} available)"},
     }
+
+
+def run_moments(args, dev, peaks, peak_src, clocks):
+    """ssd_state_moments on the 2.7B layer (chunk states recomputed at chunk 128,
+    then the closed-form moments and the fixed-order reduction), one call per
+    step; the tensor-core moment kernel also timed alone with its own events."""
+    import torch
+
+    import oracle
+    from state_space_model_mamba_gb300 import ssd
+    w = WORKLOADS["mamba2_2p7b"]
+    inp = generate(w)
+    up = lambda a, dt=torch.float32: torch.from_numpy(np.ascontiguousarray(a)).to(dev, dt)
+    x, B = up(inp["x"], torch.bfloat16), up(inp["B"], torch.bfloat16)
+    dt, A = up(inp["dt"]), up(inp["A"])
+    b, L, H, P = x.shape
+    N = B.shape[3]
+    m2 = torch.empty(b, H, N, N, device=dev)
+    m1 = torch.empty(b, H, N, device=dev)
+    cnt = torch.empty(b, device=dev, dtype=torch.int64)
+    dims = ssd.dims_of(x, B, 128)
+    lib = ssd.load_library()
+    ws = torch.empty(lib.ssd_moments_workspace_bytes(ctypes_byref(dims), ssd.SSD_BF16), dtype=torch.uint8, device=dev)
+
+    def call():
+        ssd._check(lib.ssd_state_moments(ctypes_byref(dims), ssd.SSD_BF16, ssd._ptr(x), ssd._ptr(dt), ssd._ptr(A),
+                                         ssd._ptr(B), None, None, ssd._ptr(m2), ssd._ptr(m1), ssd._ptr(cnt),
+                                         ssd._ptr(ws), ws.numel(), ssd._stream_ptr(dev)))
+    with clocks:
+        t = _event_time(call, args.warmup, args.steps)
+        timer = ssd.KernelTimer(capacity_kernels=args.steps + 4, only="moments_tc")
+        with timer:
+            for _ in range(args.steps):
+                call()
+        live = [ms for _, ms in timer.durations()]
+    ssd.workspace_status(ws)
+    costs = kernel_costs(w, tc=True)
+    flops, byts = costs["moments"]
+    km = statistics.mean(live)
+    peak = peaks["bf16_tflops_sustained"]
+    hs = 2
+
+    def cpu():
+        oracle.state_moments(inp["x"][:1, :, :hs], inp["dt"][:1, :hs], inp["A"][:hs], inp["B"][:1])
+    rate_cpu, reps, el = _wall_rate(cpu, L * hs / H, min(args.cpu_seconds, 15.0))
+    return {
+        "metric": "Mamba-2 state moments (m2, m1 of every per-token state) tokens/sec (2.7B-layer shape, 1 GB300)",
+        "value": w.tokens / (t * 1e-3), "unit": UNIT, "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": t, "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic", "op": args.op,
+        "config": {"workload": w.name, **w.dims(), "moment_chunk": 128,
+                   "l2": "inputs larger than L2; no flush",
+                   "step": "ssd_state_moments: chunk states at chunk 128, closed-form moments, range reduction"},
+        "roofline": {"bound": "tensor", "unit": "TFLOP/s", "peak": peak,
+                     "peak_source": f"{peak_src} sustained bf16 (MEASURED_PEAKS.json)" if peak_src == "measured" else "fallback",
+                     "achieved": flops / (km * 1e-3) / 1e12, "frac": flops / (km * 1e-3) / 1e12 / peak,
+                     "kernel": "moments_tc", "avg_us": km * 1e3, "algorithmic_flops_per_launch": flops,
+                     "algorithmic_bytes_per_launch": byts, "hbm_frac": byts / (km * 1e-3) / 1e9 / peaks["hbm_gbs"],
+                     "traffic": None},
+        "gpu_launches": (lib.ssd_last_launch_count()) * args.steps,
+        "clocks": clocks.summary(),
+        "cpu_baseline": {"value": rate_cpu, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
+                         "sample": f"fp64 C oracle (per-token states, OpenMP) on batch 0, heads 0..{hs - 1} of {H}, "
+                                   f"all {L} tokens; {reps} repetition(s), {el:.1f} s; scaled to tokens/s of all heads"},
+    }
+
+
+def ctypes_byref(dims):
+    import ctypes
+    return ctypes.byref(dims.c())
 
 
 def main():

@@ -253,6 +253,48 @@ const char *ssd_last_error(void);
 /* ABI version (major * 10000 + minor * 100 + patch). */
 int ssd_version(void);
 
+/* ---------------------------------------------------------------- state moments
+ * Raw first and second moments of every per-token state of the forward
+ * (burn-mamba, "modules/state_moments.rs": StateMoments, produced in closed
+ * form for Mamba-2 by Mamba2SsdInput::state_moments).  Each state row -- one
+ * (token, p) pair of S_t in R^{P x N}, S_t the state after token t < valid_len
+ * -- is one sample in R^N:
+ *   m2[b, h] = sum_t S_t^T S_t      [b, H, N, N] fp32
+ *   m1[b, h] = sum_t sum_p S_t[p,:] [b, H, N] fp32
+ *   count[b] = valid_len[b] * P     int64 (device), or NULL
+ * Computed without forming any per-token state: the chunk-input states are
+ * recomputed from the leaves (x, dt, A, B, init; C and D do not enter) at
+ * chunk 128 whatever dims->chunk_len says, then each 128-token chunk adds
+ * c0 s^T s + U^T D B + B^T D U + B^T (K o G) B (see the kernel) by three
+ * tensor-core products.  SSD_BF16 with headdim 64 and dstate 128 only
+ * (SSD_ERR_UNSUPPORTED otherwise).  Workspace from ssd_moments_workspace_bytes;
+ * m2, m1 overwritten; status words as ssd_forward's (ssd_workspace_status). */
+size_t ssd_moments_workspace_bytes(const ssd_dims *dims, ssd_dtype dtype);
+ssd_status ssd_state_moments(const ssd_dims *dims, ssd_dtype dtype, const void *x, const float *dt,
+                             const float *A, const void *B, const float *init_state,
+                             const int32_t *valid_len, float *m2, float *m1, int64_t *count,
+                             void *workspace, size_t workspace_bytes, void *stream);
+
+/* Participation ratio of pooled state moments (StateMoments::pr / ::pr_complex
+ * / ::trace): per (b, h), Sigma = m2 / n, minus mu mu^T with mu = m1 / n when
+ * `center`; PR = tr(Sigma)^2 / tr(Sigma^2) evaluated, as the page does, on
+ * Sigma / max(tr Sigma, FLT_MIN) with the denominator floored at 1e-12.  With a
+ * complex or quaternionic `pairing` the state axis is read as realified
+ * coordinates and tr(Sigma^2) is that of the Hermitian moment (one complex or
+ * quaternion direction counts once; unrotated coordinates join as a real
+ * block).  `pool_batch` first sums m2, m1 and count over the batch (the page's
+ * pool_batch); outputs are then [1, H].  trace[b, h] = tr(m2) / n (the raw mean
+ * squared state magnitude), or NULL.  All pointers are device pointers;
+ * N = dstate <= 224; num = complex pairs or quaternion blocks (ignored for
+ * SSD_PAIR_REAL).  PR of a slice with no samples is not defined (NaN/Inf). */
+#define SSD_PAIR_REAL 0
+#define SSD_PAIR_COMPLEX_INTERLEAVED 1  /* coordinate 2a real, 2a+1 imaginary part of pair a */
+#define SSD_PAIR_COMPLEX_HALF_HALF 2    /* coordinate a real, N/2 + a imaginary part of pair a */
+#define SSD_PAIR_QUATERNION 3           /* coordinates 4j .. 4j+3: quaternion block j (w, x, y, z) */
+ssd_status ssd_state_pr(const float *m2, const float *m1, const int64_t *count, int64_t batch,
+                        int64_t nheads, int64_t dstate, int center, int pairing, int64_t num,
+                        int pool_batch, float *pr, float *trace, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -289,6 +289,50 @@ ssd_status run_forward_chain(const Params &p, const ssd_dims &d, bool tc, bool w
     return SSD_OK;
 }
 
+// Chunk ranges per (b, h) of the state-moment kernel (one CTA per SM): the
+// count that minimises waves x (chunks per range + the CTA's fixed cost, about
+// two chunks), fewest ranges on ties.
+int moment_ranges(const ssd_dims &d) {
+    const long long bh = d.batch * d.nheads, n = (d.seqlen + 127) / 128;
+    long long best = 1, best_cost = -1;
+    for (long long r = 1; r <= n; ++r) {
+        const long long cost = ((bh * r + 151) / 152) * ((n + r - 1) / r + 2);
+        if (best_cost < 0 || cost < best_cost) {
+            best = r;
+            best_cost = cost;
+        }
+    }
+    return (int)best;
+}
+
+struct MomentLayout {
+    ssd_dims d;  // the caller's dims at chunk 128
+    Layout lo;   // the forward's workspace at chunk 128
+    size_t A, m1, total;
+    int ranges;
+};
+
+MomentLayout moment_layout(const ssd_dims &dims, ssd_dtype dt) {
+    MomentLayout m;
+    m.d = dims;
+    m.d.chunk_len = 128;
+    m.lo = make_layout(m.d, dt, false);
+    m.ranges = moment_ranges(m.d);
+    const size_t bhn = (size_t)dims.batch * dims.nheads * dims.dstate;
+    m.A = m.lo.total;
+    m.m1 = m.A + align_up(4 * (size_t)m.ranges * bhn * dims.dstate);
+    m.total = m.m1 + align_up(4 * (size_t)m.ranges * bhn);
+    return m;
+}
+
+ssd_status moments_supported(const ssd_dims *d, ssd_dtype dt) {
+    ssd_status st = validate_dims(d, dt);
+    if (st != SSD_OK) return st;
+    if (dt != SSD_BF16 || (d->flags & SSD_FLAG_SIMT) || !tc_supported(d->headdim, d->dstate, 128))
+        return fail(SSD_ERR_UNSUPPORTED, "state moments run on the tensor-core path: SSD_BF16, headdim 64, dstate 128");
+    return SSD_OK;
+}
+
 // The SSD_FLAG_CHECK_FINITE regions shared by both calls: cumA, endA and the
 // chunk states (every element written by K1 / K3 / K4 on both paths).
 void add_intermediates(CheckList &l, const Params &p) {
@@ -504,6 +548,81 @@ ssd_status ssd_backward(const ssd_dims *dims, ssd_dtype dtype, const void *x, co
         if (p.dstates_bf) l.r[l.n++] = {p.dstates_bf, nst, 1};
         SSD_LAUNCH("check_finite", launch_check_finite(l, p.status + kStatusNonFinite, s), 1);
     }
+    return SSD_OK;
+}
+
+size_t ssd_moments_workspace_bytes(const ssd_dims *dims, ssd_dtype dtype) {
+    if (moments_supported(dims, dtype) != SSD_OK) return 0;
+    return moment_layout(*dims, dtype).total;
+}
+
+ssd_status ssd_state_moments(const ssd_dims *dims, ssd_dtype dtype, const void *x, const float *dt,
+                             const float *A, const void *B, const float *init_state,
+                             const int32_t *valid_len, float *m2, float *m1, int64_t *count,
+                             void *workspace, size_t workspace_bytes, void *stream) {
+    g_last_error[0] = 0;
+    ssd_status st = moments_supported(dims, dtype);
+    if (st != SSD_OK) return st;
+    const void *req[] = {x, dt, A, B, m2, m1, workspace};
+    const char *names[] = {"x", "dt", "A", "B", "m2", "m1", "workspace"};
+    for (int i = 0; i < 7; ++i) {
+        if (!req[i]) return fail(SSD_ERR_INVALID_ARG, "%s is NULL", names[i]);
+        if (!aligned16(req[i])) return fail(SSD_ERR_INVALID_ARG, "%s is not 16-byte aligned", names[i]);
+    }
+    if ((init_state && !aligned16(init_state)) || (count && ((uintptr_t)count & 7u)))
+        return fail(SSD_ERR_INVALID_ARG, "init_state must be 16-byte and count 8-byte aligned");
+    const MomentLayout ml = moment_layout(*dims, dtype);
+    if (workspace_bytes < ml.total)
+        return fail(SSD_ERR_WORKSPACE, "workspace %zu < required %zu", workspace_bytes, ml.total);
+    Params p = base_params(ml.d, ml.lo, workspace);
+    p.x = x; p.dt = dt; p.A = A; p.B = B; p.init = init_state; p.valid_len = valid_len;
+    p.mom_A = (float *)((char *)workspace + ml.A);
+    p.mom_m1 = (float *)((char *)workspace + ml.m1);
+    p.mom_ranges = ml.ranges;
+    cudaStream_t s = (cudaStream_t)stream;
+    g_launches = 0;
+    SSD_TRY(cudaMemsetAsync(p.status, 0, sizeof(int) * kStatusWords, s));
+    // the chunk-input states at chunk 128 (fused scan or K1 + K3 + K4), then the moments
+    st = run_forward_chain<bf16>(p, ml.d, true, false, s, nullptr);
+    if (st != SSD_OK) return st;
+    SSD_LAUNCH("moments_tc", launch_tc_moments(p, s), 1);
+    SSD_LAUNCH("moments_reduce", launch_moments_reduce(p, m2, m1, count, s), 1);
+    if (dims->flags & SSD_FLAG_CHECK_FINITE) {
+        CheckList l;
+        l.n = 0;
+        l.r[l.n++] = {m2, (size_t)p.b * p.H * p.N * p.N, 0};
+        l.r[l.n++] = {m1, (size_t)p.b * p.H * p.N, 0};
+        add_intermediates(l, p);
+        SSD_LAUNCH("check_finite", launch_check_finite(l, p.status + kStatusNonFinite, s), 1);
+    }
+    return SSD_OK;
+}
+
+ssd_status ssd_state_pr(const float *m2, const float *m1, const int64_t *count, int64_t batch,
+                        int64_t nheads, int64_t dstate, int center, int pairing, int64_t num,
+                        int pool_batch, float *pr, float *trace, void *stream) {
+    g_last_error[0] = 0;
+    if (!m2 || !m1 || !count || !pr) return fail(SSD_ERR_INVALID_ARG, "m2, m1, count and pr are required");
+    if (batch < 1 || nheads < 1 || dstate < 1) return fail(SSD_ERR_INVALID_ARG, "every dimension must be >= 1");
+    if (dstate > 224) return fail(SSD_ERR_UNSUPPORTED, "dstate %lld above 224", (long long)dstate);
+    if (batch * nheads > (1LL << 30)) return fail(SSD_ERR_UNSUPPORTED, "problem too large");
+    const int64_t N = dstate;
+    switch (pairing) {
+        case SSD_PAIR_REAL: num = 0; break;
+        case SSD_PAIR_COMPLEX_INTERLEAVED:
+            if (num < 1 || 2 * num > N) return fail(SSD_ERR_INVALID_ARG, "interleaved pairing exceeds dstate");
+            break;
+        case SSD_PAIR_COMPLEX_HALF_HALF:
+            if (num < 1 || num > N / 2) return fail(SSD_ERR_INVALID_ARG, "half-and-half pairing exceeds dstate / 2");
+            break;
+        case SSD_PAIR_QUATERNION:
+            if (num < 1 || 4 * num > N) return fail(SSD_ERR_INVALID_ARG, "quaternion pairing exceeds dstate");
+            break;
+        default: return fail(SSD_ERR_INVALID_ARG, "unknown pairing %d", pairing);
+    }
+    cudaStream_t s = (cudaStream_t)stream;
+    SSD_TRY(launch_state_pr(m2, m1, count, (int)batch, (int)nheads, (int)N, center ? 1 : 0, pairing, (int)num,
+                            pool_batch ? 1 : 0, pr, trace, s));
     return SSD_OK;
 }
 

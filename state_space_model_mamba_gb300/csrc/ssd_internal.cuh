@@ -55,6 +55,9 @@ struct Params {
     int nslice_k5;       // head slices of the persistent per-group kernels (tensor-core path)
     int nslice_k3;       // head slices of the streaming K3 / BLUE kernels (tensor-core path)
     int *status;         // device status words, kStatusWords ints (below)
+    float *mom_A;        // [mom_ranges, b, H, N, N] state-moment partials (A stored transposed)
+    float *mom_m1;       // [mom_ranges, b, H, N]
+    int mom_ranges;      // chunk ranges per (b, h) of the state-moment kernel
 };
 
 // The workspace's status words (cleared by every call before its first kernel):
@@ -147,6 +150,14 @@ template <typename T> cudaError_t launch_simt_k5(const Params &p, cudaStream_t s
 template <typename T> cudaError_t launch_simt_bwd_blue(const Params &p, cudaStream_t s);
 template <typename T> cudaError_t launch_simt_bwd_main(const Params &p, cudaStream_t s);
 template <typename T> cudaError_t launch_simt_bwd_group(const Params &p, cudaStream_t s);
+
+// State moments (ssd_moments.cu): sum of the per-range partials into m2 / m1 /
+// count, and the participation ratio of pooled moments.
+constexpr int kMomN = 128;  // dstate of the tensor-core state-moment kernel
+cudaError_t launch_moments_reduce(const Params &p, float *m2, float *m1, int64_t *count, cudaStream_t s);
+cudaError_t launch_state_pr(const float *m2, const float *m1, const int64_t *count, int nb, int H, int N,
+                            int center, int pairing, int num, int pool, float *pr, float *trace_out,
+                            cudaStream_t s);
 
 // Geometry constants of the CUDA-core kernels that size workspace buffers.
 constexpr int kK4Threads = 128;             // threads per block of the state-passing kernels

@@ -2831,6 +2831,348 @@ __global__ void tc_bwd_dbc_reduce(const Params p) {
     *reinterpret_cast<uint2 *>((bf16 *)p.dB + o) = ub;
 }
 
+// ====================================================================== state moments
+// Raw moments of the per-token states (burn-mamba, "modules/state_moments.rs":
+// m2 = sum_t S_t^T S_t over the valid tokens, pooling the P rows of each
+// state, and m1 = sum_t sum_p S_t[p, :]) in closed form per 128-token chunk,
+// so that no per-token state is formed.  CTA per (b, h, range of chunks), 256
+// threads; the chunk-input states s come from the chunk-state scan run at
+// chunk 128.  With c = cumA, S_t = exp(c_t) s + sum_{u <= t} w_tu x_u B_u^T,
+// w_tu = exp(c_t - c_u) dt_u, the chunk's sum over its valid tokens t < vr is
+//   c0 s^T s + U^T D B + B^T D U + B^T (K o G) B,
+//   U = X s, D = diag(alpha), alpha_u = dt_u exp(c_u) sigma_u, c0 = sum_t exp(2 c_t),
+//   G = X X^T, K[u, v] = sum_{t >= max(u, v)} w_tu w_tv
+//                      = dt_u dt_v sigma_m exp(2 c_m - c_u - c_v), m = max(u, v),
+//   sigma_m = sum_{t = m}^{vr - 1} exp(2 (c_t - c_m))  (every exponent <= 0).
+// Three MMAs per chunk (bf16 operands, fp32 in TMEM):
+//   MMA1  G = X X^T                                (TMEM columns 0..127)
+//   MMA2  Y = F B + (2 alpha o X) s,  F = K o G    (columns 128..255)
+//   MMA3  A += B^T Y + (sqrt(c0) s)^T (sqrt(c0) s) (columns 256..383, over all chunks)
+// so that A + A^T = 2 (chunk sums): the range's partial A (stored transposed)
+// and m1 go to the workspace and ssd_moments_reduce sums the ranges in order
+// and symmetrises.  m1 += sum_u beta_u (sum_p x_u[p]) B_u + (sum_t exp(c_t)) sum_p s[p, :]
+// with beta_u = dt_u tau_u, tau_u = sum_{t >= u} exp(c_t - c_u), on the CUDA
+// cores.  sigma and tau are suffix sums of the recurrences
+// sigma_t = 1 + exp(2 (c_{t+1} - c_t)) sigma_{t+1}, tau_t = 1 + exp(c_{t+1} - c_t) tau_{t+1}:
+// one warp composes their affine maps (four tokens per lane, then a suffix scan
+// across the lanes).
+__device__ __forceinline__ void affine_compose(float &A1, float &B1, float A2, float B2) {
+    // (x -> B1 + A1 x) after (x -> B2 + A2 x)
+    B1 = fmaf(A1, B2, B1);
+    A1 = A1 * A2;
+}
+
+__global__ void __launch_bounds__(kThreadsWide, 1) tc_moments_kernel(const Params p, const __grid_constant__ TcMaps maps) {
+    constexpr int Q = 128;
+    constexpr uint32_t XT = 128 * 128;  // [128 tokens][64] bf16
+    constexpr uint32_t BT = 2 * XT;     // B: two 64-column halves
+    constexpr uint32_t ST = 64 * 128;   // one [64 p][64 r] half of s
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *sm = align1024(smem_raw);
+    uint8_t *Xs = sm, *Bs = Xs + 2 * XT, *Ss = Bs + 2 * BT, *Fs = Ss + 2 * ST, *XAs = Fs + 2 * XT;
+    uint8_t *Ys = XAs + XT, *Ssc = Ys + 2 * XT;
+    __shared__ uint64_t bar_xb[2], bar_s, bar_g, bar_y, bar_a;
+    __shared__ uint32_t s_tmem;
+    __shared__ float t_c[Q], t_dt[Q], t_ds[Q], t_al2[Q], t_w1[Q], t_rs[Q];
+    __shared__ float s_c0, s_asum;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int q4 = warp & 3, hf = warp >> 2;
+    int idx = blockIdx.x;
+    const int range = idx % p.mom_ranges;
+    const int bh = idx / p.mom_ranges, h = bh % p.H, bi = bh / p.H, g = h / p.hpg;
+    const int V = valid_len_of(p, bi);
+    const int nv = (V + Q - 1) / Q;
+    const int per = (p.n + p.mom_ranges - 1) / p.mom_ranges;
+    const int c_begin = range * per, c_end = min(nv, c_begin + per);
+    const int nk = max(0, c_end - c_begin);
+    float *Apart = p.mom_A + ((size_t)range * p.b * p.H + bh) * (size_t)kN * kN;
+    float *m1part = p.mom_m1 + ((size_t)range * p.b * p.H + bh) * kN;
+    if (nk == 0) {
+        for (int i = tid; i < kN * kN; i += blockDim.x) Apart[i] = 0.f;
+        if (tid < kN) m1part[tid] = 0.f;
+        return;
+    }
+    auto issue_xb = [&](int k) {
+        const int c = c_begin + k, buf = k & 1;
+        mbar_arrive_expect_tx(&bar_xb[buf], XT + BT);
+        tma_load_4d(Xs + buf * XT, &maps.x, &bar_xb[buf], 0, h, Q * c, bi);
+        for (int rb = 0; rb < 2; ++rb) tma_load_4d(Bs + buf * BT + rb * XT, &maps.B, &bar_xb[buf], 64 * rb, g, Q * c, bi);
+    };
+    auto issue_s = [&](int k) {
+        const int sidx = (bi * p.n + c_begin + k) * p.H + h;
+        mbar_arrive_expect_tx(&bar_s, 2 * ST);
+        for (int rb = 0; rb < 2; ++rb) tma_load_3d(Ss + rb * ST, &maps.st, &bar_s, 64 * rb, 0, sidx);
+    };
+    if (tid == 0) {
+        mbar_init(&bar_xb[0], 1);
+        mbar_init(&bar_xb[1], 1);
+        mbar_init(&bar_s, 1);
+        mbar_init(&bar_g, 1);
+        mbar_init(&bar_y, 1);
+        mbar_init(&bar_a, 1);
+        mbar_fence_init();
+    }
+    if (warp == 0) tmem_alloc(&s_tmem, 512);
+    tc_sync();
+    const uint32_t tm = s_tmem;
+    if (tid == 0) {
+        issue_xb(0);
+        issue_s(0);
+    }
+    // per-token scalars of the next chunk, one token per thread (t < 128)
+    float r_c = 0.f, r_dt = 0.f;
+    auto fetch = [&](int k) {
+        const int c = c_begin + k, vr = min(Q, V - Q * c);
+        if (tid < Q) {
+            r_c = p.cumA[ix_chunk(p, bi, h, c) * Q + tid];
+            r_dt = tid < vr ? p.dt[ix_dt(p, bi, h, Q * c + tid)] : 0.f;
+        }
+    };
+    fetch(0);
+    float m1_acc = 0.f;  // thread r < 128: m1[r] of this range
+    bool ok = true;
+    int xb_issued = 1, s_issued = 1, xb_landed = 0, s_landed = 0;
+    for (int k = 0; k < nk && ok; ++k) {
+        const int c = c_begin + k, vr = min(Q, V - Q * c), buf = k & 1;
+        uint8_t *Xb = Xs + buf * XT, *Bb = Bs + buf * BT;
+        // MMA3 of chunk k - 1 done: its buffers (Ys, Ssc, and X, B of buffer (k - 1) & 1) are free
+        if (k > 0) ok = wait_all(&bar_a, (uint32_t)((k - 1) & 1), ok);
+        tc_fence_after();
+        if (tid == 0 && ok && k + 1 < nk) {
+            issue_xb(k + 1);
+            xb_issued = k + 2;
+        }
+        const float cur_c = r_c, cur_dt = r_dt;
+        if (k + 1 < nk) fetch(k + 1);
+        ok = wait_all(&bar_xb[buf], (uint32_t)((k >> 1) & 1), ok);
+        if (ok) xb_landed = k + 1;
+        ok = wait_all(&bar_s, (uint32_t)(k & 1), ok);
+        if (ok) s_landed = k + 1;
+        if (!ok) break;
+        if (vr < Q) {  // rows past valid_len may hold anything: zero them (a select)
+            zero_rows_from(Xb, Q, vr);
+            zero_rows_from(Bb, Q, vr);
+            zero_rows_from(Bb + XT, Q, vr);
+        }
+        fence_async_smem();
+        tc_sync();
+        if (tid == 0) {  // MMA1: G = X X^T (both operands the K-major X tile)
+            const uint32_t id = idesc_bf16(128, 128, false, false);
+            for (int ks = 0; ks < kP / 16; ++ks)
+                mma_bf16(tm, sdesc_kmajor(smem_u32(Xb), ks, XT), sdesc_kmajor(smem_u32(Xb), ks, XT), id, ks > 0);
+            mma_commit(&bar_g);
+        }
+        // ---- scalar tables
+        if (tid < Q) {
+            t_c[tid] = cur_c;
+            t_dt[tid] = cur_dt;
+            const uint32_t rowb = smem_u32(Xb) + (uint32_t)tid * 128u;
+            float rs = 0.f;
+#pragma unroll
+            for (int c8 = 0; c8 < 8; ++c8) {
+                const uint4 u = ld_shared_v4(rowb + (uint32_t)c8 * 16u);
+                rs += bf_lo(u.x) + bf_hi(u.x) + bf_lo(u.y) + bf_hi(u.y) + bf_lo(u.z) + bf_hi(u.z) + bf_lo(u.w) + bf_hi(u.w);
+            }
+            t_rs[tid] = rs;
+        }
+        __syncthreads();
+        if (warp == 0) {
+            // suffix recurrences over the valid tokens; lane l owns tokens 4 l .. 4 l + 3
+            float sA = 1.f, sB = 0.f, uA = 1.f, uB = 0.f;  // lane map (identity)
+            float e2[4], e1[4];
+#pragma unroll
+            for (int i = 3; i >= 0; --i) {
+                const int t = 4 * lane + i;
+                float a2 = 0.f, a1 = 0.f, b = 0.f;  // token map x -> b + a x
+                if (t < vr - 1) {
+                    const float d = t_c[t + 1] - t_c[t];
+                    a2 = __expf(2.f * d);
+                    a1 = __expf(d);
+                    b = 1.f;
+                } else if (t == vr - 1) {
+                    b = 1.f;
+                }
+                e2[i] = a2;
+                e1[i] = a1;
+                // lane map = token map after the maps of the lane's later tokens
+                float tA = a2, tB = b;
+                affine_compose(tA, tB, sA, sB);
+                sA = tA;
+                sB = tB;
+                float vA = a1, vB = b;
+                affine_compose(vA, vB, uA, uB);
+                uA = vA;
+                uB = vB;
+            }
+            // inclusive suffix scan of the lane maps: lane l gets map_l after ... after map_31
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const float oA = __shfl_down_sync(0xffffffffu, sA, o), oB = __shfl_down_sync(0xffffffffu, sB, o);
+                const float pA = __shfl_down_sync(0xffffffffu, uA, o), pB = __shfl_down_sync(0xffffffffu, uB, o);
+                if (lane + o < 32) {
+                    affine_compose(sA, sB, oA, oB);
+                    affine_compose(uA, uB, pA, pB);
+                }
+            }
+            // value entering the lane's last token: the next lane's suffix applied to 0
+            float sig = __shfl_down_sync(0xffffffffu, sB, 1), tau = __shfl_down_sync(0xffffffffu, uB, 1);
+            if (lane == 31) sig = tau = 0.f;
+            float c0 = 0.f, asum = 0.f;
+#pragma unroll
+            for (int i = 3; i >= 0; --i) {
+                const int t = 4 * lane + i;
+                const bool valid = t < vr;
+                sig = valid ? fmaf(e2[i], sig, 1.f) : 0.f;
+                tau = valid ? fmaf(e1[i], tau, 1.f) : 0.f;
+                const float ec = valid ? __expf(t_c[t]) : 0.f, dt = t_dt[t];
+                t_ds[t] = dt * sig;
+                t_al2[t] = 2.f * dt * ec * sig;
+                t_w1[t] = dt * tau * t_rs[t];
+                c0 += ec * ec;
+                asum += ec;
+            }
+            c0 = warp_sum(c0);
+            asum = warp_sum(asum);
+            if (lane == 0) {
+                s_c0 = c0;
+                s_asum = asum;
+            }
+        }
+        __syncthreads();
+        // ---- A operand (2 alpha o X) and sqrt(c0) s
+        {
+            const uint32_t xb = smem_u32(Xb), xa = smem_u32(XAs);
+            for (int i = tid; i < Q * 8; i += blockDim.x) {
+                const int row = i >> 3;
+                const uint32_t off = (uint32_t)i * 16u;
+                if (row >= vr) {
+                    st_shared_v4(xa + off, 0u, 0u, 0u, 0u);
+                    continue;
+                }
+                const uint32_t f2 = pack_bf2(t_al2[row], t_al2[row]);
+                const uint4 v = ld_shared_v4(xb + off);
+                st_shared_v4(xa + off, bmul2(v.x, f2), bmul2(v.y, f2), bmul2(v.z, f2), bmul2(v.w, f2));
+            }
+            const float sq = sqrtf(s_c0);
+            const uint32_t f2 = pack_bf2(sq, sq), ss = smem_u32(Ss), sc = smem_u32(Ssc);
+            for (int i = tid; i < 2 * ST / 16; i += blockDim.x) {
+                const uint4 v = ld_shared_v4(ss + (uint32_t)i * 16u);
+                st_shared_v4(sc + (uint32_t)i * 16u, bmul2(v.x, f2), bmul2(v.y, f2), bmul2(v.z, f2), bmul2(v.w, f2));
+            }
+        }
+        // ---- F = K o G into the K-major A tile (row u, K-block hf)
+        ok = wait_all(&bar_g, (uint32_t)(k & 1), ok);
+        tc_fence_after();
+        if (ok) {
+            const int u = 32 * q4 + lane;
+            float gv[64];
+            tmem_ld64(tmem_addr(tm, 32 * q4, 64 * hf), gv);
+            const float cu = t_c[u], dtu = t_dt[u], dsu = t_ds[u];
+            const bool vu = u < vr;
+            const uint32_t rowf = smem_u32(Fs) + (uint32_t)hf * XT + (uint32_t)u * 128u;
+#pragma unroll
+            for (int c8 = 0; c8 < 8; ++c8) {
+                float f[8];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const int v = 64 * hf + 8 * c8 + j;
+                    const float cv = t_c[v];
+                    const float val = v <= u ? gv[8 * c8 + j] * dsu * t_dt[v] * __expf(cu - cv)
+                                             : gv[8 * c8 + j] * dtu * t_ds[v] * __expf(cv - cu);
+                    f[j] = (vu && v < vr) ? val : 0.f;
+                }
+                st_shared_v4(rowf + (uint32_t)(((c8 ^ (u & 7)) & 7) << 4), pack_bf2(f[0], f[1]), pack_bf2(f[2], f[3]),
+                             pack_bf2(f[4], f[5]), pack_bf2(f[6], f[7]));
+            }
+        }
+        fence_async_smem();
+        tc_fence_before();
+        ok = __syncthreads_and(ok ? 1 : 0) != 0;
+        tc_fence_after();
+        if (!ok) break;
+        if (tid == 0) {  // MMA2: Y = F B + (2 alpha o X) s
+            const uint32_t id = idesc_bf16(128, 128, false, true);
+            for (int ks = 0; ks < 8; ++ks)
+                mma_bf16(tm + 128, sdesc_kmajor(smem_u32(Fs), ks, XT), sdesc_mnmajor(smem_u32(Bb), ks, XT), id, ks > 0);
+            for (int ks = 0; ks < kP / 16; ++ks)
+                mma_bf16(tm + 128, sdesc_kmajor(smem_u32(XAs), ks, XT), sdesc_mnmajor(smem_u32(Ss), ks, ST), id, true);
+            mma_commit(&bar_y);
+        }
+        // ---- m1 (CUDA cores, beside MMA2): thread r
+        if (tid < kN) {
+            const int r = tid, rc = r & 63;
+            const uint32_t bb = smem_u32(Bb) + (uint32_t)(r >> 6) * XT, sb = smem_u32(Ss) + (uint32_t)(r >> 6) * ST;
+            float a = 0.f, sp = 0.f;
+            for (int u = 0; u < vr; ++u) {
+                unsigned short hv;
+                asm volatile("ld.shared.u16 %0, [%1];" : "=h"(hv) : "r"(bb + sw128_elem(u, rc)));
+                a = fmaf(t_w1[u], __bfloat162float(__ushort_as_bfloat16(hv)), a);
+            }
+            for (int pp = 0; pp < kP; ++pp) {
+                unsigned short hv;
+                asm volatile("ld.shared.u16 %0, [%1];" : "=h"(hv) : "r"(sb + sw128_elem(pp, rc)));
+                sp += __bfloat162float(__ushort_as_bfloat16(hv));
+            }
+            m1_acc += a + s_asum * sp;
+        }
+        // ---- Y into the MN-major B tile of MMA3 (row u, 64-column block hf)
+        ok = wait_all(&bar_y, (uint32_t)(k & 1), ok);
+        tc_fence_after();
+        if (ok) {
+            const int u = 32 * q4 + lane;
+            float yv[64];
+            tmem_ld64(tmem_addr(tm, 32 * q4, 128 + 64 * hf), yv);
+            const uint32_t rowy = smem_u32(Ys) + (uint32_t)hf * XT + (uint32_t)u * 128u;
+#pragma unroll
+            for (int c8 = 0; c8 < 8; ++c8)
+                st_shared_v4(rowy + (uint32_t)(((c8 ^ (u & 7)) & 7) << 4), pack_bf2(yv[8 * c8], yv[8 * c8 + 1]),
+                             pack_bf2(yv[8 * c8 + 2], yv[8 * c8 + 3]), pack_bf2(yv[8 * c8 + 4], yv[8 * c8 + 5]),
+                             pack_bf2(yv[8 * c8 + 6], yv[8 * c8 + 7]));
+        }
+        fence_async_smem();
+        tc_fence_before();
+        ok = __syncthreads_and(ok ? 1 : 0) != 0;
+        tc_fence_after();
+        if (!ok) break;
+        if (tid == 0) {
+            // s of the next chunk (MMA2 and the m1 loop have read this one)
+            if (k + 1 < nk) {
+                issue_s(k + 1);
+                s_issued = k + 2;
+            }
+            // MMA3: A += B^T Y + (sqrt(c0) s)^T (sqrt(c0) s)
+            const uint32_t id = idesc_bf16(128, 128, true, true);
+            for (int ks = 0; ks < 8; ++ks)
+                mma_bf16(tm + 256, sdesc_mnmajor(smem_u32(Bb), ks, XT), sdesc_mnmajor(smem_u32(Ys), ks, XT), id,
+                         k > 0 || ks > 0);
+            for (int ks = 0; ks < kP / 16; ++ks)
+                mma_bf16(tm + 256, sdesc_mnmajor(smem_u32(Ssc), ks, ST), sdesc_mnmajor(smem_u32(Ssc), ks, ST), id, true);
+            mma_commit(&bar_a);
+        }
+    }
+    if (ok) ok = wait_all(&bar_a, (uint32_t)((nk - 1) & 1), ok);
+    tc_fence_after();
+    if (ok) {
+        // the range's A, transposed (coalesced: lanes hold consecutive r), and m1
+        const int r = 32 * q4 + lane;
+        float av[64];
+        tmem_ld64(tmem_addr(tm, 32 * q4, 256 + 64 * hf), av);
+#pragma unroll
+        for (int j = 0; j < 64; ++j) Apart[(size_t)(64 * hf + j) * kN + r] = av[j];
+        if (tid < kN) m1part[tid] = m1_acc;
+    } else if (tid == 0) {
+        flag_timeout(p);
+    }
+    // loads issued for chunks that were never waited for have to land before exit
+    if (tid == 0) {
+        if (xb_issued > xb_landed)
+            for (int k = xb_landed; k < xb_issued; ++k) mbar_wait(&bar_xb[k & 1], (uint32_t)((k >> 1) & 1));
+        if (s_issued > s_landed) mbar_wait(&bar_s, (uint32_t)((s_issued - 1) & 1));
+    }
+    tc_sync();
+    if (warp == 0) tmem_dealloc(tm, 512);
+}
+
 // ====================================================================== host side
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -2943,6 +3285,8 @@ cudaError_t launch(K kernel, unsigned grid, size_t smem, cudaStream_t s, const P
 constexpr size_t smem_k2(int Q) { return Q == 128 ? 80 * 1024 : 1024 + 4 * (size_t)Q * 128; }
 // B | x stages | two bf16 state tiles
 constexpr size_t smem_k3(int Q) { return 1024 + 2 * (size_t)Q * 128 + 4 * (size_t)Q * 128 + 2 * (size_t)kP * kN * 2; }
+// X x 2 | B x 2 | s | F | 2 alpha X | Y | sqrt(c0) s (one CTA per SM: 512 TMEM columns)
+constexpr size_t smem_moments() { return 1024 + (size_t)(2 + 4 + 1 + 2 + 1 + 2) * 128 * 128 + 2 * 64 * 128; }
 // C | CB tiles (full ones and lower halves) | x | s_in | y staging tile | scalar tables
 constexpr size_t smem_k5(int Q) {
     return 1024 + 3 * (size_t)Q * 128 + 2 * 64 * 128 +
@@ -2977,6 +3321,7 @@ static_assert(smem_k2(256) > 116 * 1024, "K2 (512 TMEM columns): one CTA per SM"
 static_assert(smem_k2(128) >= 1024 + 4 * 128 * 128 && 3 * (smem_k2(128) + 1024) > 233472,
               "K2 at Q = 128 (256 TMEM columns): at most two CTAs per SM");
 static_assert(smem_k5(256) <= 232448 && smem_k5(256) > 116 * 1024, "K5: one CTA per SM");
+static_assert(smem_moments() + 6 * 128 * 4 + 64 <= 232448 && smem_moments() > 116 * 1024, "moments: one CTA per SM");
 static_assert(ScanGeom<2>::smem + 4 * (4 * 2 * 256 + 2 * 4) + 512 <= 232448 &&
                   ScanGeom<1>::smem + 4 * (4 * 1 * 256 + 4) + 512 <= 232448,
               "chunk-state scan shared memory");
@@ -3105,6 +3450,14 @@ cudaError_t launch_tc_state_scan(const Params &p, bool write_final, cudaStream_t
     const int hpc = scan_heads_per_cta(p);
     if (p.Q == 256) return hpc == 2 ? launch_scan<256, 2>(p, m, write_final, s) : launch_scan<256, 1>(p, m, write_final, s);
     return hpc == 2 ? launch_scan<128, 2>(p, m, write_final, s) : launch_scan<128, 1>(p, m, write_final, s);
+}
+
+cudaError_t launch_tc_moments(const Params &p, cudaStream_t s) {
+    TcMaps m;
+    cudaError_t e = make_maps(p, &m, false);
+    if (e != cudaSuccess) return e;
+    const unsigned grid = (unsigned)(p.b * p.H * p.mom_ranges);
+    return launch(tc_moments_kernel, grid, smem_moments(), s, p, m, kThreadsWide);
 }
 
 cudaError_t launch_tc_k5(const Params &p, cudaStream_t s) {

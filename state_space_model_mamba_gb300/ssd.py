@@ -30,7 +30,9 @@ STATUS = {0: "SSD_OK", 1: "SSD_ERR_INVALID_ARG", 2: "SSD_ERR_UNSUPPORTED",
 EXPORTED = ("ssd_supported", "ssd_workspace_bytes", "ssd_forward", "ssd_backward",
             "ssd_workspace_status", "ssd_status_str", "ssd_last_error", "ssd_version",
             "ssd_last_launch_count", "ssd_profile_begin", "ssd_profile_end", "ssd_profile_name",
-            "ssd_profile_only", "ssd_forward_noalloc", "ssd_noalloc_status")
+            "ssd_profile_only", "ssd_forward_noalloc", "ssd_noalloc_status",
+            "ssd_moments_workspace_bytes", "ssd_state_moments", "ssd_state_pr")
+SSD_PAIR_REAL, SSD_PAIR_COMPLEX_INTERLEAVED, SSD_PAIR_COMPLEX_HALF_HALF, SSD_PAIR_QUATERNION = 0, 1, 2, 3
 
 
 class SsdDims(ctypes.Structure):
@@ -91,6 +93,13 @@ def load_library(path: str | None = None):
         lib.ssd_forward_noalloc.restype = i32
         lib.ssd_noalloc_status.argtypes = [vp]
         lib.ssd_noalloc_status.restype = i32
+        lib.ssd_moments_workspace_bytes.argtypes = [dims_p, i32]
+        lib.ssd_moments_workspace_bytes.restype = sz
+        lib.ssd_state_moments.argtypes = [dims_p, i32] + [vp] * 9 + [vp, sz, vp]
+        lib.ssd_state_moments.restype = i32
+        i64 = ctypes.c_int64
+        lib.ssd_state_pr.argtypes = [vp] * 3 + [i64] * 3 + [i32, i32, i64, i32, vp, vp, vp]
+        lib.ssd_state_pr.restype = i32
         if path is None:
             _lib = lib
         return lib
@@ -248,6 +257,42 @@ def ssd_backward(x, dt, A, B, C, D, chunk_len, dy, d_final_state=None, init_stat
     if check_finite or check_status:
         workspace_status(ws)
     return out
+
+
+def state_moments(x, dt, A, B, init_state=None, valid_len=None, check_status=False, split_scan=False):
+    """Raw moments of the per-token states: returns (m2 [b,H,N,N], m1 [b,H,N],
+    count int64 [b]).  x, B bf16; dt, A, init fp32 (as ssd_forward)."""
+    _check_inputs(x, dt, A, B, B, A, init_state, valid_len, x.dtype)
+    dims = dims_of(x, B, 128, split_scan=split_scan)
+    code = _dtype_code(x)
+    b, L, H, P = x.shape
+    N = B.shape[3]
+    dev = x.device
+    m2 = torch.empty(b, H, N, N, device=dev, dtype=torch.float32)
+    m1 = torch.empty(b, H, N, device=dev, dtype=torch.float32)
+    count = torch.empty(b, device=dev, dtype=torch.int64)
+    lib = load_library()
+    n = lib.ssd_moments_workspace_bytes(ctypes.byref(dims.c()), code)
+    if n == 0:
+        _check(lib.ssd_supported(ctypes.byref(dims.c()), code) or SSD_ERR_UNSUPPORTED)
+    ws = torch.empty(n, dtype=torch.uint8, device=dev)
+    _check(lib.ssd_state_moments(ctypes.byref(dims.c()), code, _ptr(x), _ptr(dt), _ptr(A), _ptr(B),
+                                 _ptr(init_state), _ptr(valid_len), _ptr(m2), _ptr(m1), _ptr(count),
+                                 _ptr(ws), ws.numel(), _stream_ptr(dev)))
+    if check_status:
+        workspace_status(ws)
+    return m2, m1, count
+
+
+def state_pr(m2, m1, count, center=False, pairing=SSD_PAIR_REAL, num=0, pool_batch=False):
+    """Participation ratio [b or 1, H] and trace of pooled state moments."""
+    b, H, N, _ = m2.shape
+    nb = 1 if pool_batch else b
+    pr = torch.empty(nb, H, device=m2.device, dtype=torch.float32)
+    tr = torch.empty(nb, H, device=m2.device, dtype=torch.float32)
+    _check(load_library().ssd_state_pr(_ptr(m2), _ptr(m1), _ptr(count), b, H, N, int(center), int(pairing),
+                                       int(num), int(pool_batch), _ptr(pr), _ptr(tr), _stream_ptr(m2.device)))
+    return pr, tr
 
 
 def workspace_status(workspace: torch.Tensor) -> None:
