@@ -2851,8 +2851,9 @@ __global__ void tc_bwd_dbc_reduce(const Params p) {
 // so that A + A^T = 2 (chunk sums): the range's partial A (stored transposed)
 // and m1 go to the workspace and ssd_moments_reduce sums the ranges in order
 // and symmetrises.  m1 += sum_u beta_u (sum_p x_u[p]) B_u + (sum_t exp(c_t)) sum_p s[p, :]
-// with beta_u = dt_u tau_u, tau_u = sum_{t >= u} exp(c_t - c_u), on the CUDA
-// cores.  sigma and tau are suffix sums of the recurrences
+// with beta_u = dt_u tau_u, tau_u = sum_{t >= u} exp(c_t - c_u), rides along
+// MMA3 as a 144th column (w1 = beta * row sums of x beside Y, and
+// sum exp(c) / sqrt(c0) beside sqrt(c0) s).  sigma and tau are suffix sums of the recurrences
 // sigma_t = 1 + exp(2 (c_{t+1} - c_t)) sigma_{t+1}, tau_t = 1 + exp(c_{t+1} - c_t) tau_{t+1}:
 // one warp composes their affine maps (four tokens per lane, then a suffix scan
 // across the lanes).
@@ -2862,21 +2863,31 @@ __device__ __forceinline__ void affine_compose(float &A1, float &B1, float A2, f
     A1 = A1 * A2;
 }
 
-__global__ void __launch_bounds__(kThreadsWide, 1) tc_moments_kernel(const Params p, const __grid_constant__ TcMaps maps) {
+constexpr int kMomMain = 512;     // 16 warps: 4 per TMEM lane quadrant
+constexpr int kMomThreads = kMomMain + 128;  // + 4 scalar warps, a chunk ahead
+
+__global__ void __launch_bounds__(kMomThreads, 1) tc_moments_kernel(const Params p, const __grid_constant__ TcMaps maps) {
     constexpr int Q = 128;
     constexpr uint32_t XT = 128 * 128;  // [128 tokens][64] bf16
     constexpr uint32_t BT = 2 * XT;     // B: two 64-column halves
     constexpr uint32_t ST = 64 * 128;   // one [64 p][64 r] half of s
+    constexpr int ISSUER = 128;         // the thread that issues TMA and MMAs (warp 4: not a scan warp)
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = align1024(smem_raw);
-    uint8_t *Xs = sm, *Bs = Xs + 2 * XT, *Ss = Bs + 2 * BT, *Fs = Ss + 2 * ST, *XAs = Fs + 2 * XT;
-    uint8_t *Ys = XAs + XT, *Ssc = Ys + 2 * XT;
-    __shared__ uint64_t bar_xb[2], bar_s, bar_g, bar_y, bar_a;
+    // X x 2 | B x 2 | s | sqrt(c0) s | F | Y | 2 alpha X.  MMA3 reads N = 144 columns:
+    // Y's two blocks then the (dead by then) 2 alpha X tile holding the w1 column,
+    // and sqrt(c0) s's two blocks then the (dead) first 8 KB of F holding the
+    // sum_t exp(c_t) / sqrt(c0) column; column 128 of A accumulates m1.
+    uint8_t *Xs = sm, *Bs = Xs + 2 * XT, *Ss = Bs + 2 * BT, *Ssc = Ss + 2 * ST, *Fs = Ssc + 2 * ST;
+    uint8_t *Ys = Fs + 2 * XT, *XAs = Ys + 2 * XT;
+    __shared__ uint64_t bar_xb[2], bar_s, bar_g, bar_y, bar_a, bar_tab[2], bar_tabfree[2];
     __shared__ uint32_t s_tmem;
-    __shared__ float t_c[Q], t_dt[Q], t_ds[Q], t_al2[Q], t_w1[Q], t_rs[Q];
-    __shared__ float s_c0, s_asum;
+    // per-chunk tables, double-buffered: written by the scalar warps a chunk ahead
+    __shared__ float t_c[2][Q], t_dt[2][Q], t_ds[2][Q], t_al2[2][Q], t_w1[2][Q], t_rs[Q];
+    __shared__ float s_c0[2], s_asum[2];
+    __shared__ int s_abort;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int q4 = warp & 3, hf = warp >> 2;
+    const int q4 = warp & 3, cq = warp >> 2;  // TMEM lane quadrant, 32-column quarter
     int idx = blockIdx.x;
     const int range = idx % p.mom_ranges;
     const int bh = idx / p.mom_ranges, h = bh % p.H, bi = bh / p.H, g = h / p.hpg;
@@ -2910,187 +2921,222 @@ __global__ void __launch_bounds__(kThreadsWide, 1) tc_moments_kernel(const Param
         mbar_init(&bar_g, 1);
         mbar_init(&bar_y, 1);
         mbar_init(&bar_a, 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&bar_tab[i], 1);
+            mbar_init(&bar_tabfree[i], 1);
+        }
         mbar_fence_init();
+        s_abort = 0;
     }
     if (warp == 0) tmem_alloc(&s_tmem, 512);
     tc_sync();
     const uint32_t tm = s_tmem;
-    if (tid == 0) {
+    if (tid == ISSUER) {
         issue_xb(0);
         issue_s(0);
     }
-    // per-token scalars of the next chunk, one token per thread (t < 128)
-    float r_c = 0.f, r_dt = 0.f;
-    auto fetch = [&](int k) {
-        const int c = c_begin + k, vr = min(Q, V - Q * c);
-        if (tid < Q) {
-            r_c = p.cumA[ix_chunk(p, bi, h, c) * Q + tid];
-            r_dt = tid < vr ? p.dt[ix_dt(p, bi, h, Q * c + tid)] : 0.f;
-        }
-    };
-    fetch(0);
-    float m1_acc = 0.f;  // thread r < 128: m1[r] of this range
     bool ok = true;
     int xb_issued = 1, s_issued = 1, xb_landed = 0, s_landed = 0;
+    // barriers of the main group (the scalar warps run their own loop)
+    auto main_sync = [&]() {
+        tc_fence_before();
+        bar_sync_n(1, kMomMain);
+        tc_fence_after();
+    };
+    auto main_wait = [&](uint64_t *bar, uint32_t parity, bool okv) {
+        const bool r = okv ? mbar_wait(bar, parity) : false;
+        return bar_and(1, kMomMain, r);
+    };
+    if (tid >= kMomMain) {
+        // ---- scalar warps: the tables of chunk k into slot k & 1 (t = token)
+        const int t = tid - kMomMain, sw = (tid - kMomMain) >> 5;
+        float r_c = 0.f, r_dt = 0.f;
+        auto fetch = [&](int k) {
+            const int c = c_begin + k, vr = min(Q, V - Q * c);
+            r_c = p.cumA[ix_chunk(p, bi, h, c) * Q + t];
+            r_dt = t < vr ? p.dt[ix_dt(p, bi, h, Q * c + t)] : 0.f;
+        };
+        fetch(0);
+        bool sok = true;
+        for (int k = 0; k < nk; ++k) {
+            const int c = c_begin + k, vr = min(Q, V - Q * c), sl = k & 1;
+            const float cur_c = r_c, cur_dt = r_dt;
+            if (k + 1 < nk) fetch(k + 1);
+            // the main group has finished with the tables of chunk k - 2
+            if (k >= 2) sok = sok && mbar_wait(&bar_tabfree[sl], (uint32_t)(((k - 2) >> 1) & 1));
+            // X of chunk k (its rows past valid_len are not read)
+            sok = sok && mbar_wait(&bar_xb[k & 1], (uint32_t)((k >> 1) & 1));
+            sok = bar_and(2, 128, sok);
+            if (!sok) break;
+            t_c[sl][t] = cur_c;
+            t_dt[sl][t] = cur_dt;
+            float rs = 0.f;
+            if (t < vr) {
+                const uint32_t rowb = smem_u32(Xs + (k & 1) * XT) + (uint32_t)t * 128u;
+                float r4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int c8 = 0; c8 < 8; ++c8) {
+                    const uint4 u = ld_shared_v4(rowb + (uint32_t)c8 * 16u);
+                    r4[c8 & 3] += (bf_lo(u.x) + bf_hi(u.x)) + (bf_lo(u.y) + bf_hi(u.y)) + (bf_lo(u.z) + bf_hi(u.z)) +
+                                  (bf_lo(u.w) + bf_hi(u.w));
+                }
+                rs = (r4[0] + r4[1]) + (r4[2] + r4[3]);
+            }
+            t_rs[t] = rs;
+            bar_sync_n(2, 128);
+            if (sw == 0) {
+                const int lane_ = t;
+                // suffix recurrences over the valid tokens; lane l owns tokens 4 l .. 4 l + 3
+                float sA = 1.f, sB = 0.f, uA = 1.f, uB = 0.f;  // lane map (identity)
+                float e2[4], e1[4];
+#pragma unroll
+                for (int i = 3; i >= 0; --i) {
+                    const int t = 4 * lane_ + i;
+                    float a2 = 0.f, a1 = 0.f, b = 0.f;  // token map x -> b + a x
+                    if (t < vr - 1) {
+                        const float d = t_c[sl][t + 1] - t_c[sl][t];
+                        a2 = __expf(2.f * d);
+                        a1 = __expf(d);
+                        b = 1.f;
+                    } else if (t == vr - 1) {
+                        b = 1.f;
+                    }
+                    e2[i] = a2;
+                    e1[i] = a1;
+                    // lane map = token map after the maps of the lane's later tokens
+                    float tA = a2, tB = b;
+                    affine_compose(tA, tB, sA, sB);
+                    sA = tA;
+                    sB = tB;
+                    float vA = a1, vB = b;
+                    affine_compose(vA, vB, uA, uB);
+                    uA = vA;
+                    uB = vB;
+                }
+                // inclusive suffix scan of the lane maps: lane l gets map_l after ... after map_31
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const float oA = __shfl_down_sync(0xffffffffu, sA, o), oB = __shfl_down_sync(0xffffffffu, sB, o);
+                    const float pA = __shfl_down_sync(0xffffffffu, uA, o), pB = __shfl_down_sync(0xffffffffu, uB, o);
+                    if (lane_ + o < 32) {
+                        affine_compose(sA, sB, oA, oB);
+                        affine_compose(uA, uB, pA, pB);
+                    }
+                }
+                // value entering the lane's last token: the next lane's suffix applied to 0
+                float sig = __shfl_down_sync(0xffffffffu, sB, 1), tau = __shfl_down_sync(0xffffffffu, uB, 1);
+                if (lane_ == 31) sig = tau = 0.f;
+                float c0 = 0.f, asum = 0.f;
+#pragma unroll
+                for (int i = 3; i >= 0; --i) {
+                    const int t = 4 * lane_ + i;
+                    const bool valid = t < vr;
+                    sig = valid ? fmaf(e2[i], sig, 1.f) : 0.f;
+                    tau = valid ? fmaf(e1[i], tau, 1.f) : 0.f;
+                    const float ec = valid ? __expf(t_c[sl][t]) : 0.f, dt = t_dt[sl][t];
+                    t_ds[sl][t] = dt * sig;
+                    t_al2[sl][t] = 2.f * dt * ec * sig;
+                    t_w1[sl][t] = dt * tau * t_rs[t];
+                    c0 += ec * ec;
+                    asum += ec;
+                }
+                c0 = warp_sum(c0);
+                asum = warp_sum(asum);
+                if (lane_ == 0) {
+                    s_c0[sl] = c0;
+                    s_asum[sl] = asum;
+                }
+            }
+            bar_sync_n(2, 128);
+            if (t == 0) mbar_arrive(&bar_tab[sl]);
+        }
+        if (!sok) s_abort = 1;
+    } else {
     for (int k = 0; k < nk && ok; ++k) {
         const int c = c_begin + k, vr = min(Q, V - Q * c), buf = k & 1;
         uint8_t *Xb = Xs + buf * XT, *Bb = Bs + buf * BT;
-        // MMA3 of chunk k - 1 done: its buffers (Ys, Ssc, and X, B of buffer (k - 1) & 1) are free
-        if (k > 0) ok = wait_all(&bar_a, (uint32_t)((k - 1) & 1), ok);
+        // MMA3 of chunk k - 1 done: Y, sqrt(c0) s, F, 2 alpha X and the X, B of buffer (k - 1) & 1 are free
+        const int sl = k & 1;
+        if (k > 0) ok = main_wait(&bar_a, (uint32_t)((k - 1) & 1), ok);
         tc_fence_after();
-        if (tid == 0 && ok && k + 1 < nk) {
+        if (tid == ISSUER && ok && k + 1 < nk) {
             issue_xb(k + 1);
             xb_issued = k + 2;
         }
-        const float cur_c = r_c, cur_dt = r_dt;
-        if (k + 1 < nk) fetch(k + 1);
-        ok = wait_all(&bar_xb[buf], (uint32_t)((k >> 1) & 1), ok);
+        ok = main_wait(&bar_xb[buf], (uint32_t)((k >> 1) & 1), ok);
         if (ok) xb_landed = k + 1;
-        ok = wait_all(&bar_s, (uint32_t)(k & 1), ok);
+        ok = main_wait(&bar_s, (uint32_t)(k & 1), ok);
         if (ok) s_landed = k + 1;
         if (!ok) break;
         if (vr < Q) {  // rows past valid_len may hold anything: zero them (a select)
-            zero_rows_from(Xb, Q, vr);
-            zero_rows_from(Bb, Q, vr);
-            zero_rows_from(Bb + XT, Q, vr);
+            zero_rows_from_n(Xb, Q, vr, kMomMain);
+            zero_rows_from_n(Bb, Q, vr, kMomMain);
+            zero_rows_from_n(Bb + XT, Q, vr, kMomMain);
         }
         fence_async_smem();
-        tc_sync();
-        if (tid == 0) {  // MMA1: G = X X^T (both operands the K-major X tile)
+        main_sync();
+        if (tid == ISSUER) {  // MMA1: G = X X^T (both operands the K-major X tile)
             const uint32_t id = idesc_bf16(128, 128, false, false);
             for (int ks = 0; ks < kP / 16; ++ks)
                 mma_bf16(tm, sdesc_kmajor(smem_u32(Xb), ks, XT), sdesc_kmajor(smem_u32(Xb), ks, XT), id, ks > 0);
             mma_commit(&bar_g);
         }
-        // ---- scalar tables
-        if (tid < Q) {
-            t_c[tid] = cur_c;
-            t_dt[tid] = cur_dt;
-            const uint32_t rowb = smem_u32(Xb) + (uint32_t)tid * 128u;
-            float rs = 0.f;
-#pragma unroll
-            for (int c8 = 0; c8 < 8; ++c8) {
-                const uint4 u = ld_shared_v4(rowb + (uint32_t)c8 * 16u);
-                rs += bf_lo(u.x) + bf_hi(u.x) + bf_lo(u.y) + bf_hi(u.y) + bf_lo(u.z) + bf_hi(u.z) + bf_lo(u.w) + bf_hi(u.w);
-            }
-            t_rs[tid] = rs;
-        }
-        __syncthreads();
-        if (warp == 0) {
-            // suffix recurrences over the valid tokens; lane l owns tokens 4 l .. 4 l + 3
-            float sA = 1.f, sB = 0.f, uA = 1.f, uB = 0.f;  // lane map (identity)
-            float e2[4], e1[4];
-#pragma unroll
-            for (int i = 3; i >= 0; --i) {
-                const int t = 4 * lane + i;
-                float a2 = 0.f, a1 = 0.f, b = 0.f;  // token map x -> b + a x
-                if (t < vr - 1) {
-                    const float d = t_c[t + 1] - t_c[t];
-                    a2 = __expf(2.f * d);
-                    a1 = __expf(d);
-                    b = 1.f;
-                } else if (t == vr - 1) {
-                    b = 1.f;
-                }
-                e2[i] = a2;
-                e1[i] = a1;
-                // lane map = token map after the maps of the lane's later tokens
-                float tA = a2, tB = b;
-                affine_compose(tA, tB, sA, sB);
-                sA = tA;
-                sB = tB;
-                float vA = a1, vB = b;
-                affine_compose(vA, vB, uA, uB);
-                uA = vA;
-                uB = vB;
-            }
-            // inclusive suffix scan of the lane maps: lane l gets map_l after ... after map_31
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const float oA = __shfl_down_sync(0xffffffffu, sA, o), oB = __shfl_down_sync(0xffffffffu, sB, o);
-                const float pA = __shfl_down_sync(0xffffffffu, uA, o), pB = __shfl_down_sync(0xffffffffu, uB, o);
-                if (lane + o < 32) {
-                    affine_compose(sA, sB, oA, oB);
-                    affine_compose(uA, uB, pA, pB);
-                }
-            }
-            // value entering the lane's last token: the next lane's suffix applied to 0
-            float sig = __shfl_down_sync(0xffffffffu, sB, 1), tau = __shfl_down_sync(0xffffffffu, uB, 1);
-            if (lane == 31) sig = tau = 0.f;
-            float c0 = 0.f, asum = 0.f;
-#pragma unroll
-            for (int i = 3; i >= 0; --i) {
-                const int t = 4 * lane + i;
-                const bool valid = t < vr;
-                sig = valid ? fmaf(e2[i], sig, 1.f) : 0.f;
-                tau = valid ? fmaf(e1[i], tau, 1.f) : 0.f;
-                const float ec = valid ? __expf(t_c[t]) : 0.f, dt = t_dt[t];
-                t_ds[t] = dt * sig;
-                t_al2[t] = 2.f * dt * ec * sig;
-                t_w1[t] = dt * tau * t_rs[t];
-                c0 += ec * ec;
-                asum += ec;
-            }
-            c0 = warp_sum(c0);
-            asum = warp_sum(asum);
-            if (lane == 0) {
-                s_c0 = c0;
-                s_asum = asum;
-            }
-        }
-        __syncthreads();
+        // ---- the chunk's tables (the scalar warps)
+        ok = main_wait(&bar_tab[sl], (uint32_t)((k >> 1) & 1), ok);
+        if (!ok) break;
         // ---- A operand (2 alpha o X) and sqrt(c0) s
         {
             const uint32_t xb = smem_u32(Xb), xa = smem_u32(XAs);
-            for (int i = tid; i < Q * 8; i += blockDim.x) {
+            for (int i = tid; i < Q * 8; i += kMomMain) {
                 const int row = i >> 3;
                 const uint32_t off = (uint32_t)i * 16u;
                 if (row >= vr) {
                     st_shared_v4(xa + off, 0u, 0u, 0u, 0u);
                     continue;
                 }
-                const uint32_t f2 = pack_bf2(t_al2[row], t_al2[row]);
+                const uint32_t f2 = pack_bf2(t_al2[sl][row], t_al2[sl][row]);
                 const uint4 v = ld_shared_v4(xb + off);
                 st_shared_v4(xa + off, bmul2(v.x, f2), bmul2(v.y, f2), bmul2(v.z, f2), bmul2(v.w, f2));
             }
-            const float sq = sqrtf(s_c0);
+            const float sq = sqrtf(s_c0[sl]);
             const uint32_t f2 = pack_bf2(sq, sq), ss = smem_u32(Ss), sc = smem_u32(Ssc);
-            for (int i = tid; i < 2 * ST / 16; i += blockDim.x) {
+            for (int i = tid; i < 2 * ST / 16; i += kMomMain) {
                 const uint4 v = ld_shared_v4(ss + (uint32_t)i * 16u);
                 st_shared_v4(sc + (uint32_t)i * 16u, bmul2(v.x, f2), bmul2(v.y, f2), bmul2(v.z, f2), bmul2(v.w, f2));
             }
         }
-        // ---- F = K o G into the K-major A tile (row u, K-block hf)
-        ok = wait_all(&bar_g, (uint32_t)(k & 1), ok);
+        // ---- F = K o G into the K-major A tile: row u, columns 32 cq .. 32 cq + 31
+        ok = main_wait(&bar_g, (uint32_t)(k & 1), ok);
         tc_fence_after();
         if (ok) {
             const int u = 32 * q4 + lane;
-            float gv[64];
-            tmem_ld64(tmem_addr(tm, 32 * q4, 64 * hf), gv);
-            const float cu = t_c[u], dtu = t_dt[u], dsu = t_ds[u];
+            float gv[32];
+            tmem_ld32(tmem_addr(tm, 32 * q4, 32 * cq), gv);
+            const float cu = t_c[sl][u], dtu = t_dt[sl][u], dsu = t_ds[sl][u];
             const bool vu = u < vr;
-            const uint32_t rowf = smem_u32(Fs) + (uint32_t)hf * XT + (uint32_t)u * 128u;
+            const uint32_t rowf = smem_u32(Fs) + (uint32_t)(cq >> 1) * XT + (uint32_t)u * 128u;
 #pragma unroll
-            for (int c8 = 0; c8 < 8; ++c8) {
+            for (int c4 = 0; c4 < 4; ++c4) {
                 float f[8];
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
-                    const int v = 64 * hf + 8 * c8 + j;
-                    const float cv = t_c[v];
-                    const float val = v <= u ? gv[8 * c8 + j] * dsu * t_dt[v] * __expf(cu - cv)
-                                             : gv[8 * c8 + j] * dtu * t_ds[v] * __expf(cv - cu);
-                    f[j] = (vu && v < vr) ? val : 0.f;
+                    const int v = 32 * cq + 8 * c4 + j;
+                    // exp(2 c_m - c_u - c_v) = exp(-|c_u - c_v|); the sigma_m dt factor sits on the later token
+                    const float e = __expf(-fabsf(cu - t_c[sl][v]));
+                    const float fac = v <= u ? dsu * t_dt[sl][v] : dtu * t_ds[sl][v];
+                    f[j] = (vu && v < vr) ? gv[8 * c4 + j] * e * fac : 0.f;
                 }
+                const int c8 = 4 * (cq & 1) + c4;
                 st_shared_v4(rowf + (uint32_t)(((c8 ^ (u & 7)) & 7) << 4), pack_bf2(f[0], f[1]), pack_bf2(f[2], f[3]),
                              pack_bf2(f[4], f[5]), pack_bf2(f[6], f[7]));
             }
         }
         fence_async_smem();
         tc_fence_before();
-        ok = __syncthreads_and(ok ? 1 : 0) != 0;
+        ok = bar_and(1, kMomMain, ok);
         tc_fence_after();
         if (!ok) break;
-        if (tid == 0) {  // MMA2: Y = F B + (2 alpha o X) s
+        if (tid == ISSUER) {  // MMA2: Y = F B + (2 alpha o X) s
             const uint32_t id = idesc_bf16(128, 128, false, true);
             for (int ks = 0; ks < 8; ++ks)
                 mma_bf16(tm + 128, sdesc_kmajor(smem_u32(Fs), ks, XT), sdesc_mnmajor(smem_u32(Bb), ks, XT), id, ks > 0);
@@ -3098,50 +3144,48 @@ __global__ void __launch_bounds__(kThreadsWide, 1) tc_moments_kernel(const Param
                 mma_bf16(tm + 128, sdesc_kmajor(smem_u32(XAs), ks, XT), sdesc_mnmajor(smem_u32(Ss), ks, ST), id, true);
             mma_commit(&bar_y);
         }
-        // ---- m1 (CUDA cores, beside MMA2): thread r
-        if (tid < kN) {
-            const int r = tid, rc = r & 63;
-            const uint32_t bb = smem_u32(Bb) + (uint32_t)(r >> 6) * XT, sb = smem_u32(Ss) + (uint32_t)(r >> 6) * ST;
-            float a = 0.f, sp = 0.f;
-            for (int u = 0; u < vr; ++u) {
-                unsigned short hv;
-                asm volatile("ld.shared.u16 %0, [%1];" : "=h"(hv) : "r"(bb + sw128_elem(u, rc)));
-                a = fmaf(t_w1[u], __bfloat162float(__ushort_as_bfloat16(hv)), a);
-            }
-            for (int pp = 0; pp < kP; ++pp) {
-                unsigned short hv;
-                asm volatile("ld.shared.u16 %0, [%1];" : "=h"(hv) : "r"(sb + sw128_elem(pp, rc)));
-                sp += __bfloat162float(__ushort_as_bfloat16(hv));
-            }
-            m1_acc += a + s_asum * sp;
-        }
-        // ---- Y into the MN-major B tile of MMA3 (row u, 64-column block hf)
-        ok = wait_all(&bar_y, (uint32_t)(k & 1), ok);
+        // ---- Y into the MN-major B tile of MMA3 (row u, columns 32 cq ..), and the two
+        // extra columns: w1 beside Y (in the 2 alpha X tile), sum exp(c) / sqrt(c0) beside sqrt(c0) s
+        ok = main_wait(&bar_y, (uint32_t)(k & 1), ok);
         tc_fence_after();
         if (ok) {
             const int u = 32 * q4 + lane;
-            float yv[64];
-            tmem_ld64(tmem_addr(tm, 32 * q4, 128 + 64 * hf), yv);
-            const uint32_t rowy = smem_u32(Ys) + (uint32_t)hf * XT + (uint32_t)u * 128u;
+            float yv[32];
+            tmem_ld32(tmem_addr(tm, 32 * q4, 128 + 32 * cq), yv);
+            const uint32_t rowy = smem_u32(Ys) + (uint32_t)(cq >> 1) * XT + (uint32_t)u * 128u;
 #pragma unroll
-            for (int c8 = 0; c8 < 8; ++c8)
-                st_shared_v4(rowy + (uint32_t)(((c8 ^ (u & 7)) & 7) << 4), pack_bf2(yv[8 * c8], yv[8 * c8 + 1]),
-                             pack_bf2(yv[8 * c8 + 2], yv[8 * c8 + 3]), pack_bf2(yv[8 * c8 + 4], yv[8 * c8 + 5]),
-                             pack_bf2(yv[8 * c8 + 6], yv[8 * c8 + 7]));
+            for (int c4 = 0; c4 < 4; ++c4) {
+                const int c8 = 4 * (cq & 1) + c4;
+                st_shared_v4(rowy + (uint32_t)(((c8 ^ (u & 7)) & 7) << 4), pack_bf2(yv[8 * c4], yv[8 * c4 + 1]),
+                             pack_bf2(yv[8 * c4 + 2], yv[8 * c4 + 3]), pack_bf2(yv[8 * c4 + 4], yv[8 * c4 + 5]),
+                             pack_bf2(yv[8 * c4 + 6], yv[8 * c4 + 7]));
+            }
+            if (tid < Q) {  // row u of the third Y block: (w1[u], 0, ..., 0) over columns 0 .. 15
+                const uint32_t row = smem_u32(XAs) + (uint32_t)tid * 128u;
+                st_shared_v4(row + (uint32_t)(((0 ^ (tid & 7)) & 7) << 4), pack_bf2(t_w1[sl][tid], 0.f), 0u, 0u, 0u);
+                st_shared_v4(row + (uint32_t)(((1 ^ (tid & 7)) & 7) << 4), 0u, 0u, 0u, 0u);
+            } else if (tid < Q + kP) {  // row p of the third sqrt(c0) s block: sum exp(c) / sqrt(c0)
+                const int pp = tid - Q;
+                const uint32_t row = smem_u32(Fs) + (uint32_t)pp * 128u;
+                st_shared_v4(row + (uint32_t)(((0 ^ (pp & 7)) & 7) << 4), pack_bf2(s_asum[sl] / sqrtf(s_c0[sl]), 0.f),
+                             0u, 0u, 0u);
+                st_shared_v4(row + (uint32_t)(((1 ^ (pp & 7)) & 7) << 4), 0u, 0u, 0u, 0u);
+            }
         }
         fence_async_smem();
         tc_fence_before();
-        ok = __syncthreads_and(ok ? 1 : 0) != 0;
+        ok = bar_and(1, kMomMain, ok);
         tc_fence_after();
         if (!ok) break;
-        if (tid == 0) {
-            // s of the next chunk (MMA2 and the m1 loop have read this one)
+        if (tid == 0) mbar_arrive(&bar_tabfree[sl]);  // the tables of chunk k are no longer read
+        if (tid == ISSUER) {
+            // s of the next chunk (MMA2 has read this one; sqrt(c0) s is a copy)
             if (k + 1 < nk) {
                 issue_s(k + 1);
                 s_issued = k + 2;
             }
-            // MMA3: A += B^T Y + (sqrt(c0) s)^T (sqrt(c0) s)
-            const uint32_t id = idesc_bf16(128, 128, true, true);
+            // MMA3: [A | m1] += B^T [Y | w1] + (sqrt(c0) s)^T [sqrt(c0) s | sum exp(c) / sqrt(c0)]
+            const uint32_t id = idesc_bf16(128, 144, true, true);
             for (int ks = 0; ks < 8; ++ks)
                 mma_bf16(tm + 256, sdesc_mnmajor(smem_u32(Bb), ks, XT), sdesc_mnmajor(smem_u32(Ys), ks, XT), id,
                          k > 0 || ks > 0);
@@ -3150,21 +3194,27 @@ __global__ void __launch_bounds__(kThreadsWide, 1) tc_moments_kernel(const Param
             mma_commit(&bar_a);
         }
     }
-    if (ok) ok = wait_all(&bar_a, (uint32_t)((nk - 1) & 1), ok);
+    if (ok) ok = main_wait(&bar_a, (uint32_t)((nk - 1) & 1), ok);
     tc_fence_after();
+    if (ok && s_abort) ok = false;
     if (ok) {
-        // the range's A, transposed (coalesced: lanes hold consecutive r), and m1
+        // the range's A, transposed (coalesced: lanes hold consecutive r), and m1 (column 128)
         const int r = 32 * q4 + lane;
-        float av[64];
-        tmem_ld64(tmem_addr(tm, 32 * q4, 256 + 64 * hf), av);
+        float av[32];
+        tmem_ld32(tmem_addr(tm, 32 * q4, 256 + 32 * cq), av);
 #pragma unroll
-        for (int j = 0; j < 64; ++j) Apart[(size_t)(64 * hf + j) * kN + r] = av[j];
-        if (tid < kN) m1part[tid] = m1_acc;
+        for (int j = 0; j < 32; ++j) Apart[(size_t)(32 * cq + j) * kN + r] = av[j];
+        if (cq == 0) {
+            float mv[16];
+            tmem_ld16(tmem_addr(tm, 32 * q4, 256 + 128), mv);
+            m1part[r] = mv[0];
+        }
     } else if (tid == 0) {
         flag_timeout(p);
     }
+    }  // main group
     // loads issued for chunks that were never waited for have to land before exit
-    if (tid == 0) {
+    if (tid == ISSUER) {
         if (xb_issued > xb_landed)
             for (int k = xb_landed; k < xb_issued; ++k) mbar_wait(&bar_xb[k & 1], (uint32_t)((k >> 1) & 1));
         if (s_issued > s_landed) mbar_wait(&bar_s, (uint32_t)((s_issued - 1) & 1));
@@ -3285,7 +3335,7 @@ cudaError_t launch(K kernel, unsigned grid, size_t smem, cudaStream_t s, const P
 constexpr size_t smem_k2(int Q) { return Q == 128 ? 80 * 1024 : 1024 + 4 * (size_t)Q * 128; }
 // B | x stages | two bf16 state tiles
 constexpr size_t smem_k3(int Q) { return 1024 + 2 * (size_t)Q * 128 + 4 * (size_t)Q * 128 + 2 * (size_t)kP * kN * 2; }
-// X x 2 | B x 2 | s | F | 2 alpha X | Y | sqrt(c0) s (one CTA per SM: 512 TMEM columns)
+// X x 2 | B x 2 | s | sqrt(c0) s | F | Y | 2 alpha X (one CTA per SM: 512 TMEM columns)
 constexpr size_t smem_moments() { return 1024 + (size_t)(2 + 4 + 1 + 2 + 1 + 2) * 128 * 128 + 2 * 64 * 128; }
 // C | CB tiles (full ones and lower halves) | x | s_in | y staging tile | scalar tables
 constexpr size_t smem_k5(int Q) {
@@ -3457,7 +3507,7 @@ cudaError_t launch_tc_moments(const Params &p, cudaStream_t s) {
     cudaError_t e = make_maps(p, &m, false);
     if (e != cudaSuccess) return e;
     const unsigned grid = (unsigned)(p.b * p.H * p.mom_ranges);
-    return launch(tc_moments_kernel, grid, smem_moments(), s, p, m, kThreadsWide);
+    return launch(tc_moments_kernel, grid, smem_moments(), s, p, m, kMomThreads);
 }
 
 cudaError_t launch_tc_k5(const Params &p, cudaStream_t s) {
