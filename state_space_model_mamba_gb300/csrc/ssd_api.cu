@@ -7,7 +7,10 @@
 #include <stdio.h>
 #include <string.h>
 
+#include <map>
+#include <memory>
 #include <mutex>
+#include <utility>
 
 #include "ssd.h"
 #include "ssd_check.cuh"
@@ -53,39 +56,44 @@ cudaError_t mark_end(cudaStream_t s) {
     return cudaEventRecord(g_rec.ev[g_rec.n++], s);
 }
 
-// A second stream per device, so that K2 (CB, which only K5 and the ORANGE
-// backward read) and the backward's group kernels run on the SMs that the
-// caller's chain leaves idle instead of between its kernels.  The caller's
-// stream forks to it and joins back through events (aux marks the end of the
-// backward's group chain); the lock is held from the fork to the last join, so
-// concurrent callers never wait on each other's record.
+// A second stream per (device, caller stream), so that the backward's K2 (CB
+// and CB^T, which only the ORANGE backward reads) and group kernels run on the
+// SMs that the caller's chain leaves idle instead of between its kernels.  The
+// caller's stream forks to it and joins back through events (aux marks the end
+// of the group chain).  Each caller stream has its own side stream and lock, so
+// callers on different streams neither serialise their enqueue nor queue their
+// side kernels behind one another; the lock (held from the fork to the last
+// join) only orders calls that share a caller stream.  Side streams and their
+// events live until the process exits, one set per caller stream seen.
 struct SideStream {
     cudaStream_t st = nullptr;
     cudaEvent_t fork = nullptr, join = nullptr, aux = nullptr;
+    std::mutex mu;
 };
 // The stream for the side chain's launches: the caller's own while every launch is
 // being timed (ssd_profile_begin without a ssd_profile_only filter), so that each
 // event pair brackets one kernel running alone; the side stream otherwise.
-cudaStream_t side_or_serial(const SideStream *sd, cudaStream_t s) {
+cudaStream_t side_stream_for(const SideStream *sd, cudaStream_t s) {
     return (g_rec.ev && !g_rec_only[0]) ? s : sd->st;
 }
-constexpr int kMaxDevices = 64;
-SideStream g_side[kMaxDevices];
-std::mutex g_side_mu;
+std::mutex g_side_mu;  // guards the table below (lookup and insertion only)
+std::map<std::pair<int, cudaStream_t>, std::unique_ptr<SideStream>> g_side;
 
-cudaError_t side_stream(SideStream **out) {
+cudaError_t side_stream(cudaStream_t caller, SideStream **out) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-    SideStream &sd = g_side[dev];
-    if (!sd.st) {
-        if ((e = cudaStreamCreateWithFlags(&sd.st, cudaStreamNonBlocking)) != cudaSuccess) return e;
-        if ((e = cudaEventCreateWithFlags(&sd.fork, cudaEventDisableTiming)) != cudaSuccess) return e;
-        if ((e = cudaEventCreateWithFlags(&sd.join, cudaEventDisableTiming)) != cudaSuccess) return e;
-        if ((e = cudaEventCreateWithFlags(&sd.aux, cudaEventDisableTiming)) != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lock(g_side_mu);
+    std::unique_ptr<SideStream> &slot = g_side[std::make_pair(dev, caller)];
+    if (!slot) {
+        std::unique_ptr<SideStream> sd(new SideStream);
+        if ((e = cudaStreamCreateWithFlags(&sd->st, cudaStreamNonBlocking)) != cudaSuccess) return e;
+        if ((e = cudaEventCreateWithFlags(&sd->fork, cudaEventDisableTiming)) != cudaSuccess) return e;
+        if ((e = cudaEventCreateWithFlags(&sd->join, cudaEventDisableTiming)) != cudaSuccess) return e;
+        if ((e = cudaEventCreateWithFlags(&sd->aux, cudaEventDisableTiming)) != cudaSuccess) return e;
+        slot = std::move(sd);
     }
-    *out = &sd;
+    *out = slot.get();
     return cudaSuccess;
 }
 
@@ -272,7 +280,7 @@ ssd_status run_forward_chain(const Params &p, const ssd_dims &d, bool tc, bool w
             // the chunk states are enqueued; the caller joins before the first reader
             SSD_TRY(cudaEventRecord(sd->fork, s));
             SSD_TRY(cudaStreamWaitEvent(sd->st, sd->fork, 0));
-            const cudaStream_t side = side_or_serial(sd, s);
+            const cudaStream_t side = side_stream_for(sd, s);
             {
                 cudaStream_t s = side;
                 SSD_LAUNCH("k2_cb_tc", launch_tc_k2(p, s), 1);
@@ -487,11 +495,11 @@ ssd_status ssd_backward(const ssd_dims *dims, ssd_dtype dtype, const void *x, co
         SSD_LAUNCH("bwd_group_simt", launch_simt_bwd_group<float>(p, s), 2);
         SSD_LAUNCH("bwd_k1_chunk_cumsum", launch_bwd_k1(p, s), 1);
     } else {
-        std::unique_lock<std::mutex> lock(g_side_mu, std::defer_lock);
         SideStream *sd = nullptr;
+        std::unique_lock<std::mutex> lock;
         if (tc) {
-            lock.lock();
-            SSD_TRY(side_stream(&sd));
+            SSD_TRY(side_stream(s, &sd));
+            lock = std::unique_lock<std::mutex>(sd->mu);  // orders calls sharing this caller stream
         }
         st = run_forward_chain<bf16>(p, *dims, tc, false, s, sd);
         if (st != SSD_OK) return st;
@@ -502,7 +510,7 @@ ssd_status ssd_backward(const ssd_dims *dims, ssd_dtype dtype, const void *x, co
             // after K2, G2 once the K4 backward has written d_intra) and fill the SMs that
             // the per-head chain on the caller's stream (BLUE, K4 backward, ORANGE, K3
             // backward, K1 backward) leaves idle.  The caller's stream joins at the end.
-            const cudaStream_t side = side_or_serial(sd, s);
+            const cudaStream_t side = side_stream_for(sd, s);
             {
                 cudaStream_t s = side;
                 SSD_LAUNCH("bwd_dcb_tc", launch_tc_bwd_dcb(p, s), 1);

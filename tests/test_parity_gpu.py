@@ -244,3 +244,26 @@ def test_valid_len_out_of_range_is_clamped_and_reported():
     assert torch.equal(y1, y2) and torch.equal(f1, f2)
     for k in g1:
         assert torch.equal(g1[k], g2[k]), k
+
+
+# ---------------------------------------------------------------- independent callers
+def test_two_caller_streams_concurrently():
+    """Two backward calls with their own workspaces on two caller streams, enqueued
+    back to back without synchronising: each has its own second stream, and both
+    match the oracle."""
+    from parity_util import to_device
+    inps = [small(2, 700, 4, 64, 128, 2, seed=s, valid_len=[517, 700], bf16=True) for s in (300, 301)]
+    devs = [to_device(i, "bf16") for i in inps]
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    outs = [None, None]
+    for k in range(2):
+        with torch.cuda.stream(streams[k]):
+            d = devs[k]
+            outs[k] = ssd.ssd_backward(d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"], 256, d["dy"],
+                                       d_final_state=d["d_final"], init_state=d["init"], valid_len=d["valid_len"])
+    torch.cuda.synchronize()
+    for k in range(2):
+        gpu = {n: v.double().cpu().numpy() for n, v in outs[k].items() if v is not None}
+        ref = run_oracle(inps[k])
+        ref = {n: ref[n] for n in gpu}
+        compare(gpu, ref, TOL["bf16"], f"stream {k}", chunk=256)
