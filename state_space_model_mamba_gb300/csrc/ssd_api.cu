@@ -121,6 +121,19 @@ bool use_fused_scan(const Params &p, const ssd_dims &d) {
     return !(d.flags & SSD_FLAG_SPLIT_SCAN) && (long long)p.b * p.H >= kMinScanChains;
 }
 
+// In the backward the scan's chains may leave SMs idle (the 2.7B layer: 80 CTAs
+// on 152 SMs); then K2 and the d_cb kernel, which read cumA but no chunk state,
+// run beside it on the side stream.  Measured on GB300: 80 CTAs gain 2.7% of the
+// step; 96 CTAs of the 130M layer (a 0.24 ms step) lose 3% to the extra launch
+// on the critical path; 256 CTAs fill the GPU and lose 3%.  Hence at most 60%.
+bool overlap_scan(const Params &p) {
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return false;
+    return 5 * tc_state_scan_ctas(p) <= 3LL * sms;
+}
+
 Layout make_layout(const ssd_dims &d, ssd_dtype dt, bool backward) {
     Layout lo;
     memset(&lo, 0, sizeof(lo));
@@ -268,6 +281,24 @@ template <typename T>
 ssd_status run_forward_chain(const Params &p, const ssd_dims &d, bool tc, bool write_final, cudaStream_t s,
                              SideStream *sd) {
     if (tc) {
+        if (use_fused_scan(p, d) && sd && overlap_scan(p)) {
+            // backward with a small scan grid: K1 first, so that the side chain (K2, then
+            // the caller's G1, which reads cumA but no chunk state) runs on the SMs the
+            // scan leaves idle; the scan then reads cumA instead of computing it
+            SSD_LAUNCH("k1_chunk_cumsum", launch_k1_cumsum(p, s), 1);
+            SSD_TRY(cudaEventRecord(sd->fork, s));
+            SSD_TRY(cudaStreamWaitEvent(sd->st, sd->fork, 0));
+            const cudaStream_t side = side_stream_for(sd, s);
+            {
+                cudaStream_t s = side;
+                SSD_LAUNCH("k2_cb_tc", launch_tc_k2(p, s), 1);
+            }
+            SSD_TRY(cudaEventRecord(sd->join, sd->st));
+            Params q = p;
+            q.cumA_given = 1;
+            SSD_LAUNCH("state_scan_tc", launch_tc_state_scan(q, write_final, s), 1);
+            return SSD_OK;
+        }
         if (use_fused_scan(p, d)) {
             // K1, K3 and K4 in one pass per (b, h) chain: the intra-chunk states stay on chip
             SSD_LAUNCH("state_scan_tc", launch_tc_state_scan(p, write_final, s), 1);
@@ -507,9 +538,11 @@ ssd_status ssd_backward(const ssd_dims *dims, ssd_dtype dtype, const void *x, co
             // Two chains from here on.  The group kernels (G1: d_cb; G2: dB, dC partials;
             // G3: their sum) read only the leaves, cumA, the chunk states and d_intra, and
             // nothing else reads what they write: they run on the side stream (G1 right
-            // after K2, G2 once the K4 backward has written d_intra) and fill the SMs that
-            // the per-head chain on the caller's stream (BLUE, K4 backward, ORANGE, K3
-            // backward, K1 backward) leaves idle.  The caller's stream joins at the end.
+            // after K2 -- with a small fused-scan grid both follow K1 and run beside the scan, since
+            // G1 reads cumA but no chunk state -- G2 once the K4 backward has written
+            // d_intra) and fill the SMs that the per-head chain on the caller's stream
+            // (scan, BLUE, K4 backward, ORANGE, K3 backward, K1 backward) leaves idle.
+            // The caller's stream joins at the end.
             const cudaStream_t side = side_stream_for(sd, s);
             {
                 cudaStream_t s = side;

@@ -58,6 +58,7 @@ struct Params {
     float *mom_A;        // [mom_ranges, b, H, N, N] state-moment partials (A stored transposed)
     float *mom_m1;       // [mom_ranges, b, H, N]
     int mom_ranges;      // chunk ranges per (b, h) of the state-moment kernel
+    int cumA_given;      // the chunk-state scan reads cumA / endA (K1 ran before it)
 };
 
 // The workspace's status words (cleared by every call before its first kernel):

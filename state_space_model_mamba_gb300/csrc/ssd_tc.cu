@@ -560,16 +560,17 @@ __global__ void __launch_bounds__(kScanConsumers + 128, 1)
     const int V = valid_len_of(p, bi);
     const int nv = (V + Q - 1) / Q;  // chunks holding a valid token (a prefix)
     const int U = nv * SPC;          // sub-stages loaded and multiplied
-    // the backward's first kernel also clears the arrival counters
-    {
+    // the backward's first kernel also clears the arrival counters (unless K1 ran first:
+    // then K1 did that, reported valid_len, and wrote cumA / endA, which the scan reads)
+    if (!p.cumA_given) {
         const int gs = gridDim.x * blockDim.x, i0 = blockIdx.x * blockDim.x + tid;
         if (p.cb_count)
             for (int i = i0; i < p.n_count; i += gs) p.cb_count[i] = 0;
         if (p.fin_count)
             for (int i = i0; i < p.H; i += gs) p.fin_count[i] = 0;
+        // one CTA per sample reports a valid_len entry outside [0, L] (it is clamped)
+        if (h0 == 0 && tid == 0 && valid_len_out_of_range(p, bi)) atomicAdd(p.status + kStatusValidLen, 1);
     }
-    // one CTA per sample reports a valid_len entry outside [0, L] (it is clamped)
-    if (h0 == 0 && tid == 0 && valid_len_out_of_range(p, bi)) atomicAdd(p.status + kStatusValidLen, 1);
     if (tid == 0) {
         for (int i = 0; i < NSS; ++i) {
             mbar_init(&bar_full[i], 1);
@@ -665,7 +666,17 @@ __global__ void __launch_bounds__(kScanConsumers + 128, 1)
                 s_perr = 1;
                 break;
             }
-            if (live) {
+            if (live && p.cumA_given) {  // K1 has written cumA and endA: read them
+                const int vr = min(Q, V - c * Q);
+                const size_t ck = ix_chunk(p, bi, h0 + e, c);
+                const float endA = p.endA[ck];
+#pragma unroll
+                for (int i = 0; i < TPL; ++i) {
+                    const int q = TPL * lane + i;
+                    s_bbs[slot][e][q] = q < vr ? v[i] * __expf(endA - p.cumA[ck * Q + q]) : 0.f;
+                }
+                if (lane == 0) s_ea[slot][e] = __expf(endA);
+            } else if (live) {
                 const int vr = min(Q, V - c * Q);
                 float cum[TPL], run = 0.f;
 #pragma unroll
@@ -3491,6 +3502,11 @@ cudaError_t launch_scan(const Params &p, const TcMaps &m, bool write_final, cuda
     const unsigned grid = (unsigned)(p.b * p.G * ((p.hpg + HPC - 1) / HPC));
     kernel<<<grid, kScanConsumers + 32 * (2 + HPC), smem, s>>>(p, m, write_final ? 1 : 0);
     return cudaGetLastError();
+}
+
+long long tc_state_scan_ctas(const Params &p) {
+    const int hpc = scan_heads_per_cta(p);
+    return (long long)p.b * p.G * ((p.hpg + hpc - 1) / hpc);
 }
 
 cudaError_t launch_tc_state_scan(const Params &p, bool write_final, cudaStream_t s) {

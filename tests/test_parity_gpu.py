@@ -125,10 +125,14 @@ def test_backward_is_deterministic():
 # ragged valid lengths (one sample empty, one ending inside a chunk) and a
 # sequence length that is not a multiple of the chunk exercise the skipped
 # chunks and the partial last sub-stage.
+# The fused scan's backward has two schedules: with a grid of at most 60% of the
+# SMs (90 and 80 CTAs here) K2 and d_cb run beside it and it reads cumA; with a
+# larger grid (100 CTAs: b = 4, H = 25) it computes cumA itself.
 @pytest.mark.parametrize("split", [False, True])
-@pytest.mark.parametrize("Q,b,H,G", [(256, 5, 33, 3), (128, 5, 33, 3), (256, 2, 40, 2), (128, 2, 40, 2)])
+@pytest.mark.parametrize("Q,b,H,G", [(256, 5, 33, 3), (128, 5, 33, 3), (256, 2, 40, 2), (128, 2, 40, 2),
+                                     (256, 4, 25, 1)])
 def test_bf16_chunk_state_paths(Q, b, H, G, split):
-    vl = [700, 0, 389, 512, 1] if b == 5 else [389, 700]
+    vl = {5: [700, 0, 389, 512, 1], 4: [700, 0, 389, 1], 2: [389, 700]}[b]
     inp = generate_small(b, 700, H, 64, 128, G, seed=170 + Q + H, init_std=0.3, d_final_std=1.0,
                          valid_len=vl, bf16=True)
     gpu = run_gpu(inp, "bf16", Q, split_scan=split)
