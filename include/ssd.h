@@ -244,6 +244,24 @@ ssd_status ssd_forward_noalloc(const ssd_dims *dims, ssd_dtype dtype,
  * ssd_last_error() if the array has not been used on this device. */
 ssd_status ssd_noalloc_status(void *stream);
 
+/* Self-test of the device-side timeout path (no counterpart on the pages).
+ * Every wait of the library's kernels is a bounded wait on a shared-memory
+ * barrier that gives up after 2 s and records SSD_ERR_TIMEOUT in the call's
+ * status words.  This call runs that same wait in a one-thread kernel, on a
+ * barrier that one arrival completes (arrive = 1) or that nothing completes
+ * (arrive = 0), with a limit of limit_us microseconds (1 <= limit_us <=
+ * 2,000,000), after clearing the workspace's status words.  With arrive = 0
+ * the wait runs out, the kernel records the timeout and returns, the stream
+ * and context stay usable, and ssd_workspace_status then returns
+ * SSD_ERR_TIMEOUT; with arrive = 1 it returns SSD_OK.  The kernel holds no
+ * copies or tensor memory, so giving up leaves nothing in flight.
+ *   workspace: device memory, workspace_bytes >= 16 (only the status words are
+ *   written);  stream: cudaStream_t or NULL.
+ *   Errors: SSD_ERR_INVALID_ARG (before any work) for a bad workspace, limit
+ *   or arrive; SSD_ERR_CUDA if the launch fails. */
+ssd_status ssd_wait_selftest(void *workspace, size_t workspace_bytes, uint32_t limit_us, int arrive,
+                             void *stream);
+
 /* Static description of a status code. */
 const char *ssd_status_str(ssd_status status);
 

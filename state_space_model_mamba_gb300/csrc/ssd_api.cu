@@ -667,6 +667,19 @@ ssd_status ssd_state_pr(const float *m2, const float *m1, const int64_t *count, 
     return SSD_OK;
 }
 
+ssd_status ssd_wait_selftest(void *workspace, size_t workspace_bytes, uint32_t limit_us, int arrive,
+                             void *stream) {
+    g_last_error[0] = 0;
+    if (!workspace || workspace_bytes < sizeof(int) * kStatusWords) return fail(SSD_ERR_INVALID_ARG, "bad workspace");
+    if (limit_us < 1 || limit_us > 2000000) return fail(SSD_ERR_INVALID_ARG, "limit_us must be in [1, 2000000]");
+    if (arrive != 0 && arrive != 1) return fail(SSD_ERR_INVALID_ARG, "arrive must be 0 or 1");
+    cudaStream_t s = (cudaStream_t)stream;
+    SSD_TRY(cudaMemsetAsync(workspace, 0, sizeof(int) * kStatusWords, s));
+    SSD_TRY(launch_wait_selftest((int *)workspace, 1000ull * limit_us, arrive, s));
+    g_launches = 1;
+    return SSD_OK;
+}
+
 int ssd_last_launch_count(void) { return g_launches; }
 
 ssd_status ssd_profile_begin(void **events, int capacity) {

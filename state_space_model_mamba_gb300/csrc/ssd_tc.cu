@@ -3394,6 +3394,19 @@ static_assert(3 * (smem_dcb(128) + 1024) > 233472 && 2 * (smem_dcb(256) + 1024) 
 static_assert(2 * (size_t)256 * 256 + 2 * 256 * 128 <= 2 * (2 * (size_t)256 * 128 + 4 * 64 * 128),
               "d_cb + B tile must fit the two long-K stages");
 
+
+// The bounded wait of the kernels above, on a barrier that one arrival
+// completes (arrive = 1) or that nothing completes (arrive = 0), with the
+// caller's limit; a timeout is recorded in the status word as they record it.
+// One thread, no copies or tensor-memory in flight: giving up is always safe.
+__global__ void wait_selftest_kernel(Params p, uint64_t limit_ns, int arrive) {
+    __shared__ __align__(8) uint64_t bar;
+    mbar_init(&bar, 1);
+    mbar_fence_init();
+    if (arrive) mbar_arrive(&bar);
+    if (!mbar_wait(&bar, 0, limit_ns)) flag_timeout(p);
+}
+
 }  // namespace
 
 bool tc_supported(int64_t P, int64_t N, int64_t Q) { return P == kP && N == kN && (Q == 128 || Q == 256); }
@@ -3591,6 +3604,14 @@ cudaError_t launch_tc_bwd_dbc_reduce(const Params &p, cudaStream_t s) {
     const unsigned grid = (unsigned)((nvec + 255) / 256);
     if (p.Q == 256) tc_bwd_dbc_reduce<256><<<grid, 256, 0, s>>>(p);
     else tc_bwd_dbc_reduce<128><<<grid, 256, 0, s>>>(p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_wait_selftest(int *status, uint64_t limit_ns, int arrive, cudaStream_t s) {
+    Params p;
+    memset(&p, 0, sizeof(p));
+    p.status = status;
+    wait_selftest_kernel<<<1, 1, 0, s>>>(p, limit_ns, arrive);
     return cudaGetLastError();
 }
 

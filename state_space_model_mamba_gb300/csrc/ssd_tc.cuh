@@ -22,6 +22,8 @@ int tc_group_slices(const ssd_dims &d);
 cudaError_t launch_tc_state_scan(const Params &p, bool write_final, cudaStream_t s);
 // CTAs of the chunk-state scan's grid (one per (b, group, head pair or head))
 long long tc_state_scan_ctas(const Params &p);
+// one bounded wait (the kernels' own) that gives up after limit_ns unless arrive
+cudaError_t launch_wait_selftest(int *status, uint64_t limit_ns, int arrive, cudaStream_t s);
 // Closed-form state moments per (b, h, chunk range): partial A and m1 into p.mom_A, p.mom_m1.
 cudaError_t launch_tc_moments(const Params &p, cudaStream_t s);
 cudaError_t launch_tc_k2(const Params &p, cudaStream_t s);

@@ -105,14 +105,14 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
     return t;
 }
 // Bounded wait: returns false (and the caller records a timeout) if the phase
-// has not completed within `limit_ns` nanoseconds.
+// has not completed within `limit_ns` nanoseconds (the kernels: 2 s).
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint64_t limit_ns = kWaitLimitNs) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_timer_ns();
     for (uint32_t it = 0;; ++it) {
         if (mbar_try_wait(bar, parity)) return true;
-        if ((it & 63u) == 63u && global_timer_ns() - t0 > kWaitLimitNs) return false;
+        if ((it & 63u) == 63u && global_timer_ns() - t0 > limit_ns) return false;
     }
 }
 

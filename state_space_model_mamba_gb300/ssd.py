@@ -31,7 +31,7 @@ EXPORTED = ("ssd_supported", "ssd_workspace_bytes", "ssd_forward", "ssd_backward
             "ssd_workspace_status", "ssd_status_str", "ssd_last_error", "ssd_version",
             "ssd_last_launch_count", "ssd_profile_begin", "ssd_profile_end", "ssd_profile_name",
             "ssd_profile_only", "ssd_forward_noalloc", "ssd_noalloc_status",
-            "ssd_moments_workspace_bytes", "ssd_state_moments", "ssd_state_pr")
+            "ssd_moments_workspace_bytes", "ssd_state_moments", "ssd_state_pr", "ssd_wait_selftest")
 SSD_PAIR_REAL, SSD_PAIR_COMPLEX_INTERLEAVED, SSD_PAIR_COMPLEX_HALF_HALF, SSD_PAIR_QUATERNION = 0, 1, 2, 3
 
 
@@ -77,6 +77,8 @@ def load_library(path: str | None = None):
         lib.ssd_backward.restype = i32
         lib.ssd_workspace_status.argtypes = [vp, sz, vp]
         lib.ssd_workspace_status.restype = i32
+        lib.ssd_wait_selftest.argtypes = [vp, sz, ctypes.c_uint32, i32, vp]
+        lib.ssd_wait_selftest.restype = i32
         lib.ssd_status_str.argtypes = [i32]
         lib.ssd_status_str.restype = ctypes.c_char_p
         lib.ssd_last_error.restype = ctypes.c_char_p
@@ -301,6 +303,15 @@ def workspace_status(workspace: torch.Tensor) -> None:
     valid_len entries.  Synchronises the current stream."""
     _check(load_library().ssd_workspace_status(_ptr(workspace), workspace.numel(),
                                                _stream_ptr(workspace.device)))
+
+
+def wait_selftest(workspace: torch.Tensor, limit_us: int, arrive: bool) -> None:
+    """Run the kernels' bounded device wait on a barrier that one arrival
+    completes (``arrive``) or that nothing completes, giving up after
+    ``limit_us`` microseconds; :func:`workspace_status` then reports the
+    timeout (ssd_wait_selftest)."""
+    _check(load_library().ssd_wait_selftest(_ptr(workspace), workspace.numel(), int(limit_us), int(arrive),
+                                            _stream_ptr(workspace.device)))
 
 
 def noalloc_status(device=None) -> None:

@@ -22,16 +22,17 @@ def to_device(inp, dtype: str, device="cuda"):
                 torch.from_numpy(np.asarray(inp["valid_len"], np.int32)).to(device))
 
 
-def run_gpu(inp, dtype: str, chunk_len: int, simt=False, backward=True, split_scan=False):
+def run_gpu(inp, dtype: str, chunk_len: int, simt=False, backward=True, split_scan=False, check_status=False):
     d = to_device(inp, dtype)
     y, fin = ssd.ssd_forward(d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"], chunk_len,
                              init_state=d["init"], valid_len=d["valid_len"], simt=simt,
-                             split_scan=split_scan)
+                             split_scan=split_scan, check_status=check_status)
     out = {"y": y, "final_state": fin}
     if backward:
         g = ssd.ssd_backward(d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"], chunk_len, d["dy"],
                              d_final_state=d["d_final"], init_state=d["init"],
-                             valid_len=d["valid_len"], simt=simt, split_scan=split_scan)
+                             valid_len=d["valid_len"], simt=simt, split_scan=split_scan,
+                             check_status=check_status)
         out.update(g)
     torch.cuda.synchronize()
     return {k: v.double().cpu().numpy() for k, v in out.items() if v is not None}

@@ -115,6 +115,11 @@ def test_flags_accepted(lib):
 def test_status_query_arguments(lib):
     assert lib.ssd_workspace_status(None, 1 << 20, None) == 1
     assert lib.ssd_workspace_status(ctypes.c_void_p(0x10000), 8, None) == 1
+    fake = ctypes.c_void_p(0x10000)  # never dereferenced: validation fails first
+    assert lib.ssd_wait_selftest(None, 64, 1000, 0, None) == 1
+    assert lib.ssd_wait_selftest(fake, 8, 1000, 0, None) == 1
+    for limit_us, arrive in ((0, 0), (2000001, 0), (1000, 2), (1000, -1)):
+        assert lib.ssd_wait_selftest(fake, 64, limit_us, arrive, None) == 1
 
 
 def test_supported_accepts_workloads(lib):

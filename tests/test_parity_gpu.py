@@ -250,6 +250,28 @@ def test_valid_len_out_of_range_is_clamped_and_reported():
         assert torch.equal(g1[k], g2[k]), k
 
 
+def test_bounded_wait_runs_out_and_the_timeout_reaches_the_caller():
+    """The kernels' bounded wait, on a barrier that nothing completes, gives up
+    after its limit; the kernel records the timeout and returns; the host reads
+    SSD_ERR_TIMEOUT; and the context is still usable: a forward and backward
+    enqueued on the same stream right after match the oracle with a clear status."""
+    import time
+    ws = torch.zeros(64, dtype=torch.uint8, device="cuda")
+    ssd.wait_selftest(ws, limit_us=200000, arrive=True)   # one arrival completes it
+    ssd.workspace_status(ws)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    ssd.wait_selftest(ws, limit_us=50000, arrive=False)    # nothing does: 50 ms, then give up
+    with pytest.raises(ssd.SsdError) as e:
+        ssd.workspace_status(ws)
+    waited = time.perf_counter() - t0
+    assert e.value.code == ssd.SSD_ERR_TIMEOUT and "gave up" in str(e.value)
+    assert 0.05 <= waited < 5.0, waited
+    inp = small(2, 300, 4, 64, 128, 2, seed=131, valid_len=[300, 77], bf16=True)
+    gpu = run_gpu(inp, "bf16", 256, check_status=True)
+    compare(gpu, run_oracle(inp), TOL["bf16"], "after a timed-out wait", chunk=256)
+
+
 # ---------------------------------------------------------------- independent callers
 def test_two_caller_streams_concurrently():
     """Two backward calls with their own workspaces on two caller streams, enqueued
