@@ -49,6 +49,8 @@ struct TcMaps {
 };
 
 constexpr int kScanConsumers = 512;  // consumer threads of the chunk-state scan
+// tokens per sub-stage of the chunk-state scan: 64 with two heads per CTA, 128 with one
+__host__ __device__ constexpr int scan_tok(int hpc) { return hpc == 2 ? 64 : 128; }
 
 __device__ __forceinline__ uint8_t *align1024(uint8_t *p) {
     return (uint8_t *)(((uintptr_t)p + 1023) & ~(uintptr_t)1023);
@@ -506,7 +508,7 @@ __global__ void __launch_bounds__(kThreadsWide + 32, 1) tc_k3_kernel(const Param
 //          the workspace with endA = cumA[Q - 1], and bbs = dt exp(endA - cumA)
 //          into a table;
 //   intra  intra[r, p] = sum_l B[l, r] (bbs[l] x[l, p]): one MMA accumulation
-//          over 128-token sub-stages (M = dstate, A = B, B = the scaled x of
+//          over sub-stages of 64 or 128 tokens (M = dstate, A = B, B = the scaled x of
 //          the CTA's heads side by side, N = 64 per head, both MN-major) into
 //          one of two TMEM buffers, so the MMAs of chunk c overlap the
 //          epilogue of chunk c - 1;
@@ -521,14 +523,16 @@ __global__ void __launch_bounds__(kThreadsWide + 32, 1) tc_k3_kernel(const Param
 // one warp per head runs the scans up to NTAB chunks ahead.  The chain over chunks is
 // serial, so the kernel lives on the depth of its ring: one CTA per SM, and
 // two heads per CTA when there are enough heads to fill the SMs that way,
-// which halves the B traffic.  Chunks wholly past valid_len load nothing:
+// which halves the B traffic; then 64-token sub-stages (a ring six deep),
+// else 128-token ones (four deep), the faster of the two in each case on GB300.  Chunks wholly past valid_len load nothing:
 // their cumA and endA are 0 and the states pass through them unchanged.
 template <int HPC>
 struct ScanGeom {
-    static constexpr uint32_t XS = 128 * 128;             // x of one head, one sub-stage: [128 tokens][64]
-    static constexpr uint32_t BS = 128 * 128;             // one 64-column half of B of a sub-stage
+    static constexpr int TOK = scan_tok(HPC);              // tokens per sub-stage
+    static constexpr uint32_t XS = TOK * 128;              // x of one head, one sub-stage: [TOK tokens][64]
+    static constexpr uint32_t BS = TOK * 128;              // one 64-column half of B of a sub-stage
     static constexpr uint32_t SST = HPC * XS + 2 * BS;    // one stage
-    static constexpr int NSS = HPC == 2 ? 3 : 4;          // ring depth
+    static constexpr int NSS = HPC == 2 ? 6 : 4;          // ring depth (192 KB)
     static constexpr int NTAB = 4;                        // chunks of scan tables
     static constexpr size_t smem = 1024 + (size_t)NSS * SST;
 };
@@ -537,12 +541,14 @@ template <int Q, int HPC>
 __global__ void __launch_bounds__(kScanConsumers + 128, 1)
     tc_state_scan_kernel(const Params p, const __grid_constant__ TcMaps maps, int write_final) {
     using Gm = ScanGeom<HPC>;
-    constexpr int SPC = Q / 128;  // 128-token sub-stages per chunk
+    constexpr int TOK = Gm::TOK;
+    constexpr int SPC = Q / TOK;  // sub-stages per chunk
     constexpr int NSS = Gm::NSS, NTAB = Gm::NTAB;
     constexpr uint32_t XS = Gm::XS, BS = Gm::BS, SST = Gm::SST;
     constexpr uint32_t BOFF = HPC * XS;   // B within a stage
     constexpr int NCW = kScanConsumers / 32;  // consumer warps
     constexpr int W_MMA = NCW, W_LOAD = NCW + 1, W_SCAN = NCW + 2;
+    constexpr int NPX = HPC * TOK * 8, NPB = 2 * TOK * 8;  // 16-byte pieces of x, of B per sub-stage
     extern __shared__ uint8_t smem_raw[];
     uint8_t *ring = align1024(smem_raw);
     __shared__ uint64_t bar_full[NSS], bar_scaled[NSS], bar_free[NSS], bar_mma[2], bar_tfree[2];
@@ -613,7 +619,7 @@ __global__ void __launch_bounds__(kScanConsumers + 128, 1)
                 }
                 tc_fence_after();
                 const uint32_t base = smem_u32(ring + st * SST);
-                for (int ks = 0; ks < 8; ++ks)
+                for (int ks = 0; ks < TOK / 16; ++ks)
                     mma_bf16(tm + 64 * HPC * (k & 1), sdesc_mnmajor(base + BOFF, ks, BS), sdesc_mnmajor(base, ks, XS),
                              idesc, j > 0 || ks > 0);
                 mma_commit(&bar_free[st]);
@@ -625,7 +631,7 @@ __global__ void __launch_bounds__(kScanConsumers + 128, 1)
         // ---- TMA loader: stage u % NSS once the MMAs of sub-stage u - NSS are done
         if (lane == 0) {
             for (int u = 0; u < U; ++u) {
-                const int st = u % NSS, t = (u / SPC) * Q + 128 * (u % SPC);
+                const int st = u % NSS, t = (u / SPC) * Q + TOK * (u % SPC);
                 if (u >= NSS && !mbar_wait(&bar_free[st], (uint32_t)((u / NSS - 1) & 1))) {
                     s_perr = 1;
                     break;
@@ -639,8 +645,9 @@ __global__ void __launch_bounds__(kScanConsumers + 128, 1)
         }
     } else if (warp >= W_SCAN) {
         // ---- scans: warp W_SCAN + e scans head e of chunk c into table c % NTAB, up to
-        // NTAB chunks ahead.  Lane l holds tokens TPL l .. TPL l + TPL - 1: their dt
-        // (fetched a chunk ahead), a sequential sum, a warp scan of the lanes' sums.
+        // NTAB chunks ahead.  Lane l holds tokens 32 i + l (i < TPL), so that the dt
+        // loads (a chunk ahead), the cumA stores and the table stores are whole
+        // 128-byte rows: one warp scan per 32 tokens, carried across the chunk.
         constexpr int TPL = Q / 32;
         const int e = warp - W_SCAN;
         const bool live = e < nh;
@@ -650,7 +657,7 @@ __global__ void __launch_bounds__(kScanConsumers + 128, 1)
             const int vr = min(Q, V - c * Q);
 #pragma unroll
             for (int i = 0; i < TPL; ++i) {
-                const int q = TPL * lane + i;
+                const int q = 32 * i + lane;
                 v[i] = (live && q < vr) ? dtrow[c * Q + q] : 0.f;
             }
         };
@@ -672,7 +679,7 @@ __global__ void __launch_bounds__(kScanConsumers + 128, 1)
                 const float endA = p.endA[ck];
 #pragma unroll
                 for (int i = 0; i < TPL; ++i) {
-                    const int q = TPL * lane + i;
+                    const int q = 32 * i + lane;
                     s_bbs[slot][e][q] = q < vr ? v[i] * __expf(endA - p.cumA[ck * Q + q]) : 0.f;
                 }
                 if (lane == 0) s_ea[slot][e] = __expf(endA);
@@ -681,23 +688,22 @@ __global__ void __launch_bounds__(kScanConsumers + 128, 1)
                 float cum[TPL], run = 0.f;
 #pragma unroll
                 for (int i = 0; i < TPL; ++i) {
-                    run += v[i] * Ah;
-                    cum[i] = run;
-                }
-                float incl = run;
+                    float incl = v[i] * Ah;
 #pragma unroll
-                for (int o = 1; o < 32; o <<= 1) {
-                    const float w = __shfl_up_sync(0xffffffffu, incl, o);
-                    if (lane >= o) incl += w;
+                    for (int o = 1; o < 32; o <<= 1) {
+                        const float w = __shfl_up_sync(0xffffffffu, incl, o);
+                        if (lane >= o) incl += w;
+                    }
+                    cum[i] = run + incl;
+                    run += __shfl_sync(0xffffffffu, incl, 31);
                 }
-                const float pre = incl - run, endA = __shfl_sync(0xffffffffu, incl, 31);
+                const float endA = run;
                 const size_t ck = ix_chunk(p, bi, h0 + e, c);
 #pragma unroll
                 for (int i = 0; i < TPL; ++i) {
-                    const int q = TPL * lane + i;
-                    const float cq = cum[i] + pre;
-                    p.cumA[ck * Q + q] = cq;
-                    s_bbs[slot][e][q] = q < vr ? v[i] * __expf(endA - cq) : 0.f;
+                    const int q = 32 * i + lane;
+                    p.cumA[ck * Q + q] = cum[i];
+                    s_bbs[slot][e][q] = q < vr ? v[i] * __expf(endA - cum[i]) : 0.f;
                 }
                 if (lane == 0) {
                     p.endA[ck] = endA;
@@ -722,36 +728,38 @@ __global__ void __launch_bounds__(kScanConsumers + 128, 1)
             if (c < p.n) {
                 const int slot = c % NTAB, vr = min(Q, V - c * Q);
                 ok = __all_sync(0xffffffffu, mbar_wait(&bar_tab[slot], (uint32_t)((c / NTAB) & 1)));
-                // ---- K3 operands: scale x rows by bbs (packed bf16 pairs), zero rows past valid_len
+                // ---- K3 operands: scale x rows by bbs (packed bf16 pairs), zero rows past valid_len.
+                // Thread i takes the 16-byte pieces i, i + 512, ... (32 consecutive pieces:
+                // four whole 128-byte rows, no bank conflict; the 128-byte swizzle permutes
+                // pieces within a row, so one scale per row).
                 for (int j = 0; j < SPC && c < nv && ok; ++j) {
                     const int u = c * SPC + j, st = u % NSS;
                     const uint32_t sb = smem_u32(ring + st * SST);
                     ok = __all_sync(0xffffffffu, mbar_wait(&bar_full[st], (uint32_t)((u / NSS) & 1)));
                     if (!ok) break;
-                    // thread: row tid / 4 of the sub-stage, 16-byte chunks 2 (tid % 4) and + 1
-                    const int row = tid >> 2, tl = 128 * j + row;
-                    const bool vrow = tl < vr;
-                    const uint32_t off = (uint32_t)row * 128u + (uint32_t)(tid & 3) * 32u;
 #pragma unroll
-                    for (int e = 0; e < HPC; ++e) {
-                        if (e >= nh) break;
-                        const uint32_t a = sb + e * XS + off;
-                        if (!vrow) {
+                    for (int pi = tid; pi < NPX; pi += kScanConsumers) {
+                        const int e = pi / (TOK * 8), row = (pi >> 3) % TOK, tl = TOK * j + row;
+                        if (e >= nh) continue;
+                        const uint32_t a = sb + e * XS + (uint32_t)row * 128u + (uint32_t)(pi & 7) * 16u;
+                        if (tl >= vr) {
                             st_shared_v4(a, 0u, 0u, 0u, 0u);
-                            st_shared_v4(a + 16u, 0u, 0u, 0u, 0u);
                             continue;
                         }
                         const float f = s_bbs[slot][e][tl];
                         const uint32_t f2 = pack_bf2(f, f);
-                        const uint4 v0 = ld_shared_v4(a), v1 = ld_shared_v4(a + 16u);
+                        const uint4 v0 = ld_shared_v4(a);
                         st_shared_v4(a, bmul2(v0.x, f2), bmul2(v0.y, f2), bmul2(v0.z, f2), bmul2(v0.w, f2));
-                        st_shared_v4(a + 16u, bmul2(v1.x, f2), bmul2(v1.y, f2), bmul2(v1.z, f2), bmul2(v1.w, f2));
                     }
-                    if (!vrow) {  // B rows past valid_len (both halves)
+                    if (TOK * j + TOK > vr) {  // B rows past valid_len (both halves)
 #pragma unroll
-                        for (int q = 0; q < 4; ++q)
-                            st_shared_v4(sb + BOFF + (uint32_t)(q >> 1) * BS + off + (uint32_t)(q & 1) * 16u, 0u, 0u,
-                                         0u, 0u);
+                        for (int pi = tid; pi < NPB; pi += kScanConsumers) {
+                            const int row = (pi >> 3) % TOK;
+                            if (TOK * j + row >= vr)
+                                st_shared_v4(sb + BOFF + (uint32_t)(pi / (TOK * 8)) * BS + (uint32_t)row * 128u +
+                                                 (uint32_t)(pi & 7) * 16u,
+                                             0u, 0u, 0u, 0u);
+                        }
                     }
                     fence_async_smem();
                     __syncwarp();
@@ -760,41 +768,39 @@ __global__ void __launch_bounds__(kScanConsumers + 128, 1)
                 if (!ok) break;
             }
             if (c > 0) {
-                // ---- K4 step of chunk k = c - 1: s_in_k = s out, s <- exp(endA_k) s + intra_k
+                // ---- K4 step of chunk k = c - 1: s_in_k = s out, s <- exp(endA_k) s + intra_k,
+                // one head at a time (16 accumulator values live at once)
                 const int k = c - 1, kslot = k % NTAB;
-                float v[HPC][16];
-                if (k < nv) {
+                const bool live = k < nv;
+                if (live) {
                     ok = __all_sync(0xffffffffu, mbar_wait(&bar_mma[k & 1], (uint32_t)((k >> 1) & 1)));
                     if (!ok) break;
                     tc_fence_after();
+                }
 #pragma unroll
-                    for (int e = 0; e < HPC; ++e) {
-                        if (e < nh) tmem_ld16(tmem_addr(tm, 32 * q4, 64 * (HPC * (k & 1) + e) + 16 * cq), v[e]);
-                        else {
+                for (int e = 0; e < HPC; ++e) {
+                    float v[16];
+                    if (live && e < nh) {
+                        tmem_ld16(tmem_addr(tm, 32 * q4, 64 * (HPC * (k & 1) + e) + 16 * cq), v);
+                    } else {
 #pragma unroll
-                            for (int j = 0; j < 16; ++j) v[e][j] = 0.f;
-                        }
+                        for (int j = 0; j < 16; ++j) v[j] = 0.f;
                     }
+                    if (e < nh) {
+                        // s_in_k: for each p the warp's lanes write 32 consecutive r (64 bytes)
+                        bf16 *dst = p.states_bf + ix_state(p, bi, k, h0 + e) + (size_t)(16 * cq) * kN + r;
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) dst[(size_t)j * kN] = __float2bfloat16_rn(s[e][j]);
+                        const float a = s_ea[kslot][e];
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) s[e][j] = fmaf(a, s[e][j], v[j]);
+                    }
+                }
+                if (live) {
                     // TMEM buffer k & 1 read: the MMAs of chunk k + 2 may overwrite it
                     tc_fence_before();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&bar_tfree[k & 1]);
-                } else {
-#pragma unroll
-                    for (int e = 0; e < HPC; ++e)
-#pragma unroll
-                        for (int j = 0; j < 16; ++j) v[e][j] = 0.f;
-                }
-#pragma unroll
-                for (int e = 0; e < HPC; ++e) {
-                    if (e >= nh) break;
-                    // s_in_k: for each p the warp's lanes write 32 consecutive r (64 bytes)
-                    bf16 *dst = p.states_bf + ix_state(p, bi, k, h0 + e) + (size_t)(16 * cq) * kN + r;
-#pragma unroll
-                    for (int j = 0; j < 16; ++j) dst[(size_t)j * kN] = __float2bfloat16_rn(s[e][j]);
-                    const float a = s_ea[kslot][e];
-#pragma unroll
-                    for (int j = 0; j < 16; ++j) s[e][j] = fmaf(a, s[e][j], v[e][j]);
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&bar_tabfree[kslot]);  // table of chunk k no longer read
@@ -3286,17 +3292,17 @@ cudaError_t make_maps(const Params &p, TcMaps *mp, bool backward) {
     if ((e = map_tokens(&mp->x, p.x, p.b, p.L, p.H, kP)) != cudaSuccess) return e;
     if ((e = map_tokens(&mp->B, p.B, p.b, p.L, p.G, kN)) != cudaSuccess) return e;
     if ((e = map_tokens(&mp->C, p.C, p.b, p.L, p.G, kN)) != cudaSuccess) return e;
-    {  // x as [b][head][token][64] boxes of (1 or 2 heads) x 128 tokens: dims (p, token, head, b)
+    {  // x as [b][head][token][64] boxes of (1 or 2 heads) x 128 or 64 tokens: dims (p, token, head, b)
         const int hpc = scan_heads_per_cta(p);
         cuuint64_t dims[4] = {(cuuint64_t)kP, (cuuint64_t)p.L, (cuuint64_t)p.H, (cuuint64_t)p.b};
         cuuint64_t strides[3] = {(cuuint64_t)p.H * kP * 2, (cuuint64_t)kP * 2, (cuuint64_t)p.L * p.H * kP * 2};
-        cuuint32_t box[4] = {64, 128, (cuuint32_t)hpc, 1};
+        cuuint32_t box[4] = {64, (cuuint32_t)scan_tok(hpc), (cuuint32_t)hpc, 1};
         if ((e = encode(&mp->xs, p.x, 4, dims, strides, box)) != cudaSuccess) return e;
     }
-    {  // B as [half][token][64] boxes of 2 halves x 128 tokens: dims (column, token, half, group, b)
+    {  // B as [half][token][64] boxes of 2 halves x the scan's sub-stage: dims (column, token, half, group, b)
         cuuint64_t dims[5] = {64, (cuuint64_t)p.L, 2, (cuuint64_t)p.G, (cuuint64_t)p.b};
         cuuint64_t strides[4] = {(cuuint64_t)p.G * kN * 2, 128, (cuuint64_t)kN * 2, (cuuint64_t)p.L * p.G * kN * 2};
-        cuuint32_t box[5] = {64, 128, 2, 1, 1};
+        cuuint32_t box[5] = {64, (cuuint32_t)scan_tok(scan_heads_per_cta(p)), 2, 1, 1};
         if ((e = encode(&mp->Bs, p.B, 5, dims, strides, box)) != cudaSuccess) return e;
     }
     if (p.states_bf && (e = map_states(&mp->st, p.states_bf, (long long)p.b * p.n * p.H)) != cudaSuccess) return e;
