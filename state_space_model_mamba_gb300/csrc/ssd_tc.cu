@@ -2184,7 +2184,8 @@ __global__ void __launch_bounds__(kThreadsWide, 1) tc_bwd_orange_kernel(const Pa
 //   d_cb[t, s] = sum_h dt_h[s] exp(cumA_h[t] - cumA_h[s]) dW_h[t, s]     (s <= t)
 // where dW_h = dy_h x_h^T is one MMA per head into one of two TMEM buffers, so
 // the MMA of head k + 1 runs during the epilogue of head k.  dy / x tiles come
-// through a two-stage TMA ring; per-head scalars are fetched into registers
+// through a three-stage TMA ring (head k + 3 is requested once MMA k is done, so
+// a load has two heads' work to land in); per-head scalars are fetched into registers
 // three heads ahead and staged in shared memory.  The slices' fp32 partials
 // are summed, in slice order, by the last CTA of the block to finish, which
 // writes d_cb in bf16 (the operand type of the next kernel).  The decay is factored through pivots, both factors <= 1:
@@ -2197,14 +2198,15 @@ __global__ void __launch_bounds__(kThreadsWide, 2) tc_bwd_dcb_kernel(const Param
     constexpr int NT = Q / 128;
     constexpr int NBLK = NT * (NT + 1) / 2;
     constexpr uint32_t STG = 2 * kTile;  // dy rows of the t-block, x rows of the s-block
+    constexpr int NST = 3;               // TMA stages: head k + 3 is requested once MMA k is done
     constexpr int NSC = 3;               // scalar buffers
     // own-sub-block column table and fast flags after the pivots (16-byte aligned)
-    constexpr int OWNOFF = (5 * Q + Q / 64 + Q / 16 + 3) & ~3, FLOFF = OWNOFF + Q;
+    constexpr int OWNOFF = (4 * Q + Q / 64 + Q / 16 + 3) & ~3, FLOFF = OWNOFF + Q;
     constexpr int FST = (FLOFF + Q / 16 + 3) & ~3;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = align1024(smem_raw);
-    float *fbuf = reinterpret_cast<float *>(sm + 2 * STG);  // [NSC][cum | dt | g | g64 | g16 | piv64 | piv16]
-    __shared__ uint64_t bar_tma[2], bar_mma[2];
+    float *fbuf = reinterpret_cast<float *>(sm + NST * STG);  // [NSC][cum | dt | g64 | g16 | piv64 | piv16 | own | flags]
+    __shared__ uint64_t bar_tma[NST], bar_mma[NST];
     __shared__ uint32_t s_tmem;
     __shared__ int s_last;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -2258,51 +2260,41 @@ __global__ void __launch_bounds__(kThreadsWide, 2) tc_bwd_dcb_kernel(const Param
             f[Q + tid] = r_dt[k & 1];
         }
     };
-    auto derive = [&](int k) {
+    auto derive = [&](int k) {  // diagonal blocks only
         float *f = fbuf + (k % NSC) * FST;
         const int l = 128 * sk + (tid & 127);  // a column of this block
         if (tid < 128) {
             const float cl = f[l], d = f[Q + l];
-            if (diag) {
-                f[3 * Q + l] = d * __expf(f[l | 63] - cl);
-                f[4 * Q + l] = d * __expf(f[l | 15] - cl);
-                if ((l & 63) == 63) f[5 * Q + (l >> 6)] = cl;
-                if ((l & 15) == 15) f[5 * Q + Q / 64 + (l >> 4)] = cl;
-                // own sub-block: dt_s exp(cumA[16 v] - cumA_s) (>= 0, <= e^64 dt_s where used)
-                f[OWNOFF + l] = d * __expf(f[l & ~15] - cl);
-                if ((l & 15) == 0) f[FLOFF + (l >> 4)] = f[l] - f[l + 15] < 64.f ? 1.f : 0.f;
-            } else {
-                f[2 * Q + l] = d * __expf(f[128 * sk + 127] - cl);
-            }
+            f[2 * Q + l] = d * __expf(f[l | 63] - cl);
+            f[3 * Q + l] = d * __expf(f[l | 15] - cl);
+            if ((l & 63) == 63) f[4 * Q + (l >> 6)] = cl;
+            if ((l & 15) == 15) f[4 * Q + Q / 64 + (l >> 4)] = cl;
+            // own sub-block: dt_s exp(cumA[16 v] - cumA_s) (>= 0, <= e^64 dt_s where used)
+            f[OWNOFF + l] = d * __expf(f[l & ~15] - cl);
+            if ((l & 15) == 0) f[FLOFF + (l >> 4)] = f[l] - f[l + 15] < 64.f ? 1.f : 0.f;
         }
     };
     const int xrow = vrows - 128 * sk;  // valid rows of the x tile (> 0)
     auto issue = [&](int k) {
-        const int h = h_begin + k, st = k & 1;
+        const int h = h_begin + k, st = k % NST;
         uint8_t *dys = sm + st * STG, *xs = dys + kTile;
         mbar_arrive_expect_tx(&bar_tma[st], STG);
         tma_load_4d(dys, &maps.dy, &bar_tma[st], 0, h, t0 + 128 * tb, bi);
         tma_load_4d(xs, &maps.x, &bar_tma[st], 0, h, t0 + 128 * sk, bi);
     };
     if (tid == 0) {
-        mbar_init(&bar_tma[0], 1);
-        mbar_init(&bar_tma[1], 1);
-        mbar_init(&bar_mma[0], 1);
-        mbar_init(&bar_mma[1], 1);
+        for (int i = 0; i < NST; ++i) {
+            mbar_init(&bar_tma[i], 1);
+            mbar_init(&bar_mma[i], 1);
+        }
         mbar_fence_init();
     }
     if (warp == 0) tmem_alloc(&s_tmem, 256);
     tc_sync();
     const uint32_t tm = s_tmem;
     int issued = 0, landed = 0;  // TMA bookkeeping of thread 0
-    if (tid == 0 && nh > 0) {
-        issue(0);
-        issued = 1;
-        if (nh > 1) {
-            issue(1);
-            issued = 2;
-        }
-    }
+    if (tid == 0)
+        for (; issued < min(nh, NST); ++issued) issue(issued);
     bool ok = true, okt = true;
     if (!diag) {
         // ---- the block below the diagonal: its pivot P = cumA[128 sk + 127] (the last
@@ -2325,13 +2317,13 @@ __global__ void __launch_bounds__(kThreadsWide, 2) tc_bwd_dcb_kernel(const Param
         if (nh > 0) fetch_o(0, cr, dr, pr);
         if (nh > 1) fetch_o(1, cn, dn, pn);
         for (int k = 0; k < nh && ok; ++k) {
-            const int st = k & 1;
+            const int st = k % NST;
             const float fct = on_dy ? __expf(cr - pr) : dr * __expf(pr - cr);
             cr = cn;
             dr = dn;
             pr = pn;
             if (k + 2 < nh) fetch_o(k + 2, cn, dn, pn);
-            const bool okk = mbar_wait(&bar_tma[st], (uint32_t)((k >> 1) & 1));
+            const bool okk = mbar_wait(&bar_tma[st], (uint32_t)((k / NST) & 1));
             if (tid == 0 && okk) landed = k + 1;
             if (okk) scale_row_bf16x2(sm + st * STG + (on_dy ? 0 : kTile), r, fct, rv);
             fence_async_smem();
@@ -2345,17 +2337,19 @@ __global__ void __launch_bounds__(kThreadsWide, 2) tc_bwd_dcb_kernel(const Param
                 for (int ks = 0; ks < kP / 16; ++ks)
                     mma_bf16(tm, sdesc_kmajor(dys, ks, kTile), sdesc_kmajor(xs, ks, kTile), id, k > 0 || ks > 0);
                 mma_commit(&bar_mma[st]);
-                if (k + 2 < nh) {  // stage st takes head k + 2 once MMA k has read it
-                    if (mbar_wait(&bar_mma[st], (uint32_t)((k >> 1) & 1))) {
-                        issue(k + 2);
-                        issued = k + 3;
+                // the stage of head k - 1 takes head k - 1 + NST once MMA k - 1 has read it
+                // (MMA k stays queued behind it meanwhile)
+                if (k >= 1 && k - 1 + NST < nh) {
+                    if (mbar_wait(&bar_mma[(k - 1) % NST], (uint32_t)(((k - 1) / NST) & 1))) {
+                        issue(k - 1 + NST);
+                        issued = k + NST;
                     } else {
                         okt = false;
                     }
                 }
             }
         }
-        if (ok && nh > 0) okt = mbar_wait(&bar_mma[(nh - 1) & 1], (uint32_t)(((nh - 1) >> 1) & 1)) && okt;
+        if (ok && nh > 0) okt = mbar_wait(&bar_mma[(nh - 1) % NST], (uint32_t)(((nh - 1) / NST) & 1)) && okt;
         tc_fence_after();
         if (ok && nh > 0) {
             tmem_ld32(tmem_addr(tm, 32 * q4, colp(0)), acc);
@@ -2377,8 +2371,8 @@ __global__ void __launch_bounds__(kThreadsWide, 2) tc_bwd_dcb_kernel(const Param
         // Wait for head k's tiles, zero x rows past valid_len, and (thread 0) issue
         // dW_k into TMEM buffer k & 1.  Returns a CTA-uniform status.
         auto land_and_mma = [&](int k, bool ok_in) -> bool {
-            const int st = k & 1;
-            bool ok = ok_in && mbar_wait(&bar_tma[st], (uint32_t)((k >> 1) & 1));
+            const int st = k % NST, tb2 = k & 1;  // TMA stage, TMEM buffer
+            bool ok = ok_in && mbar_wait(&bar_tma[st], (uint32_t)((k / NST) & 1));
             if (tid == 0 && ok) landed = k + 1;
             if (ok && xrow < 128) {
                 zero_rows_from(sm + st * STG + kTile, 128, xrow);
@@ -2392,8 +2386,8 @@ __global__ void __launch_bounds__(kThreadsWide, 2) tc_bwd_dcb_kernel(const Param
                 const uint32_t id = idesc_bf16(128, 128, false, false);
 #pragma unroll
                 for (int ks = 0; ks < kP / 16; ++ks)
-                    mma_bf16(tm + 128 * st, sdesc_kmajor(dys, ks, kTile), sdesc_kmajor(xs, ks, kTile), id, ks > 0);
-                mma_commit(&bar_mma[st]);
+                    mma_bf16(tm + 128 * tb2, sdesc_kmajor(dys, ks, kTile), sdesc_kmajor(xs, ks, kTile), id, ks > 0);
+                mma_commit(&bar_mma[tb2]);
             }
             return ok;
         };
@@ -2412,9 +2406,9 @@ __global__ void __launch_bounds__(kThreadsWide, 2) tc_bwd_dcb_kernel(const Param
             if (k + 1 < nh) derive(k + 1);
             okt = ok && mbar_wait(&bar_mma[st], (uint32_t)((k >> 1) & 1));
             tc_fence_after();
-            if (tid == 0 && okt && k + 2 < nh) {
-                issue(k + 2);  // stage st is free: MMA k has read it
-                issued = k + 3;
+            if (tid == 0 && okt && k + NST < nh) {
+                issue(k + NST);  // the stage of head k is free: MMA k has read it
+                issued = k + NST + 1;
             }
             const float *f = fbuf + (k % NSC) * FST;
             const float ct = f[t];
@@ -2427,8 +2421,8 @@ __global__ void __launch_bounds__(kThreadsWide, 2) tc_bwd_dcb_kernel(const Param
                 float *a = acc + 32 * half;
                 if (row_ok && (!diag || half < tr)) {
                     // one pivot for all 32 columns
-                    const float e = __expf(ct - (diag ? f[5 * Q + (s0 >> 6)] : f[128 * sk + 127]));
-                    const float4 *gv = reinterpret_cast<const float4 *>(f + (diag ? 3 : 2) * Q + s0);
+                    const float e = __expf(ct - (diag ? f[4 * Q + (s0 >> 6)] : f[128 * sk + 127]));
+                    const float4 *gv = reinterpret_cast<const float4 *>(f + 2 * Q + s0);
 #pragma unroll
                     for (int i = 0; i < 8; ++i) {
                         const float4 gq = gv[i];
@@ -2444,8 +2438,8 @@ __global__ void __launch_bounds__(kThreadsWide, 2) tc_bwd_dcb_kernel(const Param
                         float *av = a + 16 * v2;
                         const float *dv = dw + 16 * v2;
                         if (v16 < u16) {
-                            const float e = __expf(ct - f[5 * Q + Q / 64 + (sv >> 4)]);
-                            const float4 *gv = reinterpret_cast<const float4 *>(f + 4 * Q + sv);
+                            const float e = __expf(ct - f[4 * Q + Q / 64 + (sv >> 4)]);
+                            const float4 *gv = reinterpret_cast<const float4 *>(f + 3 * Q + sv);
 #pragma unroll
                             for (int i = 0; i < 4; ++i) {
                                 const float4 gq = gv[i];
@@ -2485,7 +2479,7 @@ __global__ void __launch_bounds__(kThreadsWide, 2) tc_bwd_dcb_kernel(const Param
     tc_fence_after();
     if (!ok && tid == 0) flag_timeout(p);
     if (tid == 0)
-        for (int k = landed; k < issued; ++k) mbar_wait(&bar_tma[k & 1], (uint32_t)((k >> 1) & 1));
+        for (int k = landed; k < issued; ++k) mbar_wait(&bar_tma[k % NST], (uint32_t)((k / NST) & 1));
     tc_sync();
     if (warp == 0) tmem_dealloc(tm, 256);
     if (!ok) return;
@@ -3342,7 +3336,10 @@ cudaError_t make_maps(const Params &p, TcMaps *mp, bool backward) {
 template <typename K>
 cudaError_t launch(K kernel, unsigned grid, size_t smem, cudaStream_t s, const Params &p, const TcMaps &maps,
                    int threads = kThreads) {
+    // every kernel here sizes its CTAs against the whole 228 KB: ask for that carveout
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
     if (e != cudaSuccess) return e;
     kernel<<<grid, threads, smem, s>>>(p, maps);
     return cudaGetLastError();
@@ -3374,9 +3371,9 @@ constexpr size_t smem_orange_raw(int Q) {
 constexpr size_t smem_orange(int Q) { return smem_orange_raw(Q) > 120 * 1024 ? smem_orange_raw(Q) : 120 * 1024; }
 // Padded above a third of the SM's shared memory: two CTAs of 256 TMEM columns
 // each may share an SM, a third must not.
-constexpr size_t dcb_fst(int Q) { return (((5 * Q + Q / 64 + Q / 16 + 3) & ~3) + Q + Q / 16 + 3) & ~3; }
+constexpr size_t dcb_fst(int Q) { return (((4 * Q + Q / 64 + Q / 16 + 3) & ~3) + Q + Q / 16 + 3) & ~3; }
 constexpr size_t smem_dcb(int Q) {
-    return 1024 + 4 * (size_t)kTile + 4 * 3 * dcb_fst(Q) > 80 * 1024 ? 1024 + 4 * (size_t)kTile + 4 * 3 * dcb_fst(Q)
+    return 1024 + 6 * (size_t)kTile + 4 * 3 * dcb_fst(Q) > 80 * 1024 ? 1024 + 6 * (size_t)kTile + 4 * 3 * dcb_fst(Q)
                                                                    : 80 * 1024;
 }
 constexpr size_t smem_dbc(int Q) {
@@ -3517,6 +3514,8 @@ cudaError_t launch_scan(const Params &p, const TcMaps &m, bool write_final, cuda
     auto kernel = tc_state_scan_kernel<Q, HPC>;
     const size_t smem = ScanGeom<HPC>::smem;
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
     if (e != cudaSuccess) return e;
     const unsigned grid = (unsigned)(p.b * p.G * ((p.hpg + HPC - 1) / HPC));
     kernel<<<grid, kScanConsumers + 32 * (2 + HPC), smem, s>>>(p, m, write_final ? 1 : 0);
