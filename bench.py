@@ -755,7 +755,7 @@ def run_op(args, local_rank):
         bytes_b = 3 * V.nbytes + 2 * B.nbytes + 2 * C.nbytes + 2 * g.nbytes
         tokens = T
         config = {"workload": w.name, "tokens": T, "mimo": m, "nheads": H, "headdim": Pd, "dstate": N, "dtype": "bf16"}
-        kernels = {"forward": f"y_diag_fwd<bf16, {m}>", "backward": f"y_diag_bwd<bf16, {m}>"}
+        kernels = {"forward": f"y_diag_fwd_fast<bf16, {m}>", "backward": f"y_diag_bwd_fast<bf16, {m}>"}
         ts = 2048
 
         def cpu():

@@ -366,12 +366,123 @@ __global__ void y_diag_bwd(const T *__restrict__ dY, const T *__restrict__ V, co
     }
 }
 
+// The same two kernels when the state axis fits one 4-wide piece per lane
+// (N <= 128, N % 4 == 0) and the head axis one pair per lane (P <= 64, P
+// even): every row the warp needs is loaded at the start, so a warp waits for
+// one memory round trip instead of two (forward) or four (backward), and
+// nothing is read twice.
+template <typename T, int M>
+__global__ void y_diag_fwd_fast(const T *__restrict__ V, const T *__restrict__ B, const T *__restrict__ C,
+                                const float *__restrict__ gamma, T *__restrict__ y, DShape s) {
+    const long long w = (blockIdx.x * (long long)blockDim.x + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    if (w >= s.T * s.H) return;
+    const int h = (int)(w % s.H);
+    const long long t = w / s.H;
+    const bool hn = 4 * lane < s.N, hp = 2 * lane < s.P;
+    float4 cv[M], bv[M];
+    float2 vv[M];
+#pragma unroll
+    for (int i = 0; i < M; ++i) {
+        const long long rn = ((t * M + i) * s.H + h) * (long long)s.N + 4 * lane;
+        const long long rp = ((t * M + i) * s.H + h) * (long long)s.P + 2 * lane;
+        cv[i] = hn ? Pair<T>::ld4(C + rn) : make_float4(0.f, 0.f, 0.f, 0.f);
+        bv[i] = hn ? Pair<T>::ld4(B + rn) : make_float4(0.f, 0.f, 0.f, 0.f);
+        vv[i] = hp ? Pair<T>::ld(V + rp) : make_float2(0.f, 0.f);
+    }
+    const float g = gamma[w];
+    float qk[M][M];
+#pragma unroll
+    for (int o = 0; o < M; ++o)
+#pragma unroll
+        for (int i = 0; i < M; ++i) qk[o][i] = warp_sum(dot4(cv[o], bv[i]));
+    if (!hp) return;
+#pragma unroll
+    for (int o = 0; o < M; ++o) {
+        float2 a = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int i = 0; i < M; ++i) {
+            a.x += qk[o][i] * vv[i].x;
+            a.y += qk[o][i] * vv[i].y;
+        }
+        Pair<T>::st(y + ((t * M + o) * s.H + h) * (long long)s.P + 2 * lane, make_float2(g * a.x, g * a.y));
+    }
+}
+
+template <typename T, int M>
+__global__ void y_diag_bwd_fast(const T *__restrict__ dY, const T *__restrict__ V, const T *__restrict__ B,
+                                const T *__restrict__ C, const float *__restrict__ gamma, T *__restrict__ dV,
+                                T *__restrict__ dB, T *__restrict__ dC, float *__restrict__ d_gamma, DShape s) {
+    const long long w = (blockIdx.x * (long long)blockDim.x + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    if (w >= s.T * s.H) return;
+    const int h = (int)(w % s.H);
+    const long long t = w / s.H;
+    const bool hn = 4 * lane < s.N, hp = 2 * lane < s.P;
+    float4 cv[M], bv[M];
+    float2 dv[M], vv[M];
+#pragma unroll
+    for (int i = 0; i < M; ++i) {
+        const long long rn = ((t * M + i) * s.H + h) * (long long)s.N + 4 * lane;
+        const long long rp = ((t * M + i) * s.H + h) * (long long)s.P + 2 * lane;
+        cv[i] = hn ? Pair<T>::ld4(C + rn) : make_float4(0.f, 0.f, 0.f, 0.f);
+        bv[i] = hn ? Pair<T>::ld4(B + rn) : make_float4(0.f, 0.f, 0.f, 0.f);
+        dv[i] = hp ? Pair<T>::ld(dY + rp) : make_float2(0.f, 0.f);
+        vv[i] = hp ? Pair<T>::ld(V + rp) : make_float2(0.f, 0.f);
+    }
+    const float g = gamma[w];
+    float qk[M][M], dyv[M][M];
+    float dg = 0.f;
+#pragma unroll
+    for (int o = 0; o < M; ++o)
+#pragma unroll
+        for (int i = 0; i < M; ++i) {
+            qk[o][i] = warp_sum(dot4(cv[o], bv[i]));
+            dyv[o][i] = warp_sum(dv[o].x * vv[i].x + dv[o].y * vv[i].y);
+            dg += qk[o][i] * dyv[o][i];
+        }
+    if (lane == 0) d_gamma[w] = dg;
+    if (hp) {  // dV[i, p] = g sum_o qk[o, i] dY[o, p]
+#pragma unroll
+        for (int i = 0; i < M; ++i) {
+            float2 a = make_float2(0.f, 0.f);
+#pragma unroll
+            for (int o = 0; o < M; ++o) {
+                a.x += qk[o][i] * dv[o].x;
+                a.y += qk[o][i] * dv[o].y;
+            }
+            Pair<T>::st(dV + ((t * M + i) * s.H + h) * (long long)s.P + 2 * lane, make_float2(g * a.x, g * a.y));
+        }
+    }
+    if (hn) {  // d_qk = g dyv;  dC[o, r] = sum_i d_qk[o, i] B[i, r];  dB[o, r] = sum_i d_qk[i, o] C[i, r]
+#pragma unroll
+        for (int o = 0; o < M; ++o) {
+            float4 a = make_float4(0.f, 0.f, 0.f, 0.f), b2 = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int i = 0; i < M; ++i) {
+                a.x += dyv[o][i] * bv[i].x;
+                a.y += dyv[o][i] * bv[i].y;
+                a.z += dyv[o][i] * bv[i].z;
+                a.w += dyv[o][i] * bv[i].w;
+                b2.x += dyv[i][o] * cv[i].x;
+                b2.y += dyv[i][o] * cv[i].y;
+                b2.z += dyv[i][o] * cv[i].z;
+                b2.w += dyv[i][o] * cv[i].w;
+            }
+            const long long row = ((t * M + o) * s.H + h) * (long long)s.N + 4 * lane;
+            Pair<T>::st4(dC + row, make_float4(g * a.x, g * a.y, g * a.z, g * a.w));
+            Pair<T>::st4(dB + row, make_float4(g * b2.x, g * b2.y, g * b2.z, g * b2.w));
+        }
+    }
+}
+
 // ---------------------------------------------------------------- host side
 ssd_status m3_fail(ssd_status st, const char *msg) {
     record_error(msg);
     return st;
 }
 bool al16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
+bool y_diag_fits_lanes(const DShape &s) { return s.N <= 128 && (s.N & 3) == 0 && s.P <= 64 && (s.P & 1) == 0; }
 
 ssd_status quat_check(const void *const *ptrs, int nreq, int64_t b, int64_t L, int64_t H, int64_t J) {
     if (b < 1 || L < 1 || H < 1 || J < 1) return m3_fail(SSD_ERR_INVALID_ARG, "every dimension must be >= 1");
@@ -391,16 +502,24 @@ template <typename T, int M>
 cudaError_t launch_y_fwd(const DShape &s, const void *V, const void *B, const void *C, const float *g, void *y,
                          cudaStream_t st) {
     const long long threads = s.T * s.H * 32;
-    y_diag_fwd<T, M><<<(unsigned)((threads + 255) / 256), 256, 0, st>>>(
-        (const T *)V, (const T *)B, (const T *)C, g, (T *)y, s);
+    const unsigned grid = (unsigned)((threads + 255) / 256);
+    if (y_diag_fits_lanes(s))
+        y_diag_fwd_fast<T, M><<<grid, 256, 0, st>>>((const T *)V, (const T *)B, (const T *)C, g, (T *)y, s);
+    else
+        y_diag_fwd<T, M><<<grid, 256, 0, st>>>((const T *)V, (const T *)B, (const T *)C, g, (T *)y, s);
     return cudaGetLastError();
 }
 template <typename T, int M>
 cudaError_t launch_y_bwd(const DShape &s, const void *dY, const void *V, const void *B, const void *C,
                          const float *g, void *dV, void *dB, void *dC, float *dg, cudaStream_t st) {
     const long long threads = s.T * s.H * 32;
-    y_diag_bwd<T, M><<<(unsigned)((threads + 255) / 256), 256, 0, st>>>(
-        (const T *)dY, (const T *)V, (const T *)B, (const T *)C, g, (T *)dV, (T *)dB, (T *)dC, dg, s);
+    const unsigned grid = (unsigned)((threads + 255) / 256);
+    if (y_diag_fits_lanes(s))
+        y_diag_bwd_fast<T, M><<<grid, 256, 0, st>>>((const T *)dY, (const T *)V, (const T *)B, (const T *)C, g,
+                                                    (T *)dV, (T *)dB, (T *)dC, dg, s);
+    else
+        y_diag_bwd<T, M><<<grid, 256, 0, st>>>((const T *)dY, (const T *)V, (const T *)B, (const T *)C, g,
+                                               (T *)dV, (T *)dB, (T *)dC, dg, s);
     return cudaGetLastError();
 }
 
