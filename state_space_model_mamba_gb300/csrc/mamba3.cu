@@ -8,14 +8,18 @@
 // Quaternion scan.  A chain is one (b, h, j); its L steps are cut into
 // segments of kSeg steps so that b * L / kSeg * H * J threads share the work.
 //   forward:  pass 1, per segment: the product of its steps;
-//             pass 2, per segment: the carry (init times the earlier segments'
-//             products, in order), then its steps from that carry.
+//             carries, one warp per chain: the carry into each segment (init
+//             times the earlier segments' products, in order) by a warp scan
+//             whose combine is the ordered product, written over pass 1's
+//             products;
+//             pass 2, per segment: its steps from that carry.
 //   backward: pass 1, per segment: the local prefix products LP (from the
 //             identity at the segment start), their product, and
 //             T = sum_s conj(LP[s]) (x) d_cum[s];
-//             pass 2, per segment: the carry P_in (product of the earlier
-//             segments), the suffix sum from the later segments
-//             sum_{later} conj(P_in') (x) T', then one forward walk in which
+//             carries, one warp per chain: P_in (product of the earlier
+//             segments) and the suffix sum over the later segments
+//             sum_{later} conj(P_in') (x) T';
+//             pass 2, per segment: one forward walk in which
 //             S[t] = suffix + conj(P_in) (x) (T - running sum of the segment's
 //             terms before t) -- the page's reverse cumsum without a reverse
 //             walk -- and G, d_q as on the page.
@@ -28,7 +32,7 @@
 namespace ssd {
 namespace {
 
-constexpr int kSeg = 128;  // steps per segment of the quaternion scan
+constexpr int kSeg = 32;  // steps per segment of the quaternion scan
 
 struct Qt {
     float w, x, y, z;
@@ -45,6 +49,18 @@ __device__ __forceinline__ Qt qld(const float *p) {
     return {v.x, v.y, v.z, v.w};
 }
 __device__ __forceinline__ void qst(float *p, Qt a) { *reinterpret_cast<float4 *>(p) = make_float4(a.w, a.x, a.y, a.z); }
+__device__ __forceinline__ Qt qld_rw(const float *p) {  // plain load: data this kernel also writes
+    const float4 v = *reinterpret_cast<const float4 *>(p);
+    return {v.x, v.y, v.z, v.w};
+}
+__device__ __forceinline__ Qt qshfl_up(Qt a, int o) {
+    return {__shfl_up_sync(0xffffffffu, a.w, o), __shfl_up_sync(0xffffffffu, a.x, o),
+            __shfl_up_sync(0xffffffffu, a.y, o), __shfl_up_sync(0xffffffffu, a.z, o)};
+}
+__device__ __forceinline__ Qt qshfl_down(Qt a, int o) {
+    return {__shfl_down_sync(0xffffffffu, a.w, o), __shfl_down_sync(0xffffffffu, a.x, o),
+            __shfl_down_sync(0xffffffffu, a.y, o), __shfl_down_sync(0xffffffffu, a.z, o)};
+}
 __device__ __forceinline__ Qt qone() { return {1.f, 0.f, 0.f, 0.f}; }
 __device__ __forceinline__ Qt qzero() { return {0.f, 0.f, 0.f, 0.f}; }
 
@@ -73,12 +89,55 @@ __global__ void quat_seg_product(const float *__restrict__ q, float *__restrict_
     qst(segp + ((bi * s.S + sg) * s.C + c) * 4, acc);
 }
 
-__global__ void quat_seg_scan(const float *__restrict__ q, const float *__restrict__ init,
-                              const float *__restrict__ segp, float *__restrict__ cum, QShape s) {
+// One warp per chain (b, c): lane l takes segments [l K, l K + K), K = ceil(S / 32).
+// The product of a lane's segments, a warp scan in lane order (later (x) earlier),
+// then a walk that overwrites each segment's product with the carry into it.
+// The segments are read in batches of kCB into registers, every load of a batch
+// before any store; a lane with one batch (K <= kCB) reads them once.
+constexpr int kCB = 8;
+
+__global__ void quat_seg_carry(float *__restrict__ segp, const float *__restrict__ init, QShape s) {
+    const long long wid = (blockIdx.x * (long long)blockDim.x + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    if (wid >= s.b * s.C) return;  // warp-uniform
+    const long long c = wid % s.C, bi = wid / s.C;
+    const long long K = (s.S + 31) / 32, k0 = lane * K, k1 = min(s.S, k0 + K);
+    auto at = [&](long long k) { return ((bi * s.S + k) * s.C + c) * 4; };
+    Qt v[kCB];
+    Qt a = qone();
+    for (long long kb = k0; kb < k1; kb += kCB) {
+#pragma unroll
+        for (int i = 0; i < kCB; ++i) v[i] = kb + i < k1 ? qld_rw(segp + at(kb + i)) : qone();
+#pragma unroll
+        for (int i = 0; i < kCB; ++i) a = qmul(v[i], a);
+    }
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const Qt y = qshfl_up(a, o);
+        if (lane >= o) a = qmul(a, y);
+    }
+    Qt run = qshfl_up(a, 1);  // the earlier lanes' segments
+    if (lane == 0) run = qone();
+    const Qt in = init ? qld(init + (bi * s.C + c) * 4) : qone();
+    const bool reuse = k1 - k0 <= kCB;
+    for (long long kb = k0; kb < k1; kb += kCB) {
+        if (!reuse) {
+#pragma unroll
+            for (int i = 0; i < kCB; ++i) v[i] = kb + i < k1 ? qld_rw(segp + at(kb + i)) : qone();
+        }
+#pragma unroll
+        for (int i = 0; i < kCB; ++i) {
+            if (kb + i < k1) qst(segp + at(kb + i), qmul(run, in));
+            run = qmul(v[i], run);
+        }
+    }
+}
+
+__global__ void quat_seg_scan(const float *__restrict__ q, const float *__restrict__ carries,
+                              float *__restrict__ cum, QShape s) {
     long long bi, sg, c;
     if (!qmap(s, bi, sg, c)) return;
-    Qt carry = init ? qld(init + (bi * s.C + c) * 4) : qone();
-    for (long long k = 0; k < sg; ++k) carry = qmul(qld(segp + ((bi * s.S + k) * s.C + c) * 4), carry);
+    Qt carry = qld(carries + ((bi * s.S + sg) * s.C + c) * 4);
     const long long t0 = sg * kSeg, t1 = min(s.L, t0 + kSeg);
     const long long off = ((bi * s.L + t0) * s.C + c) * 4;
     const float *qp = q + off;
@@ -108,22 +167,91 @@ __global__ void quat_bwd_segments(const float *__restrict__ q, const float *__re
     qst(segT + so, acc);
 }
 
-__global__ void quat_bwd_apply(const float *__restrict__ q, const float *__restrict__ init,
-                               const float *__restrict__ d_cum, const float *__restrict__ segp,
-                               const float *__restrict__ segT, float *__restrict__ d_q, float *__restrict__ d_init,
+// One warp per chain, lanes over segments as in quat_seg_carry: segp's products
+// become P_in[k] (the product of segments 0 .. k-1, without init), and
+// later[k] = sum_{k' > k} conj(P_in[k']) (x) T[k'] (a suffix sum over lanes, then
+// a reverse walk over the lane's own segments).  A lane with one batch of
+// segments holds its products, P_in and T in registers throughout.
+__global__ void quat_bwd_carry(float *__restrict__ segp, const float *__restrict__ segT, float *__restrict__ later,
                                QShape s) {
+    const long long wid = (blockIdx.x * (long long)blockDim.x + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    if (wid >= s.b * s.C) return;  // warp-uniform
+    const long long c = wid % s.C, bi = wid / s.C;
+    const long long K = (s.S + 31) / 32, k0 = lane * K, k1 = min(s.S, k0 + K);
+    auto at = [&](long long k) { return ((bi * s.S + k) * s.C + c) * 4; };
+    const bool reuse = k1 - k0 <= kCB;
+    Qt v[kCB], tv[kCB], pin[kCB];
+    Qt a = qone();
+    for (long long kb = k0; kb < k1; kb += kCB) {
+#pragma unroll
+        for (int i = 0; i < kCB; ++i) {
+            v[i] = kb + i < k1 ? qld_rw(segp + at(kb + i)) : qone();
+            tv[i] = kb + i < k1 ? qld(segT + at(kb + i)) : qzero();
+        }
+#pragma unroll
+        for (int i = 0; i < kCB; ++i) a = qmul(v[i], a);
+    }
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const Qt y = qshfl_up(a, o);
+        if (lane >= o) a = qmul(a, y);
+    }
+    Qt run = qshfl_up(a, 1);
+    if (lane == 0) run = qone();
+    Qt u = qzero();  // sum over the lane's segments of conj(P_in) (x) T
+    for (long long kb = k0; kb < k1; kb += kCB) {
+        if (!reuse) {
+#pragma unroll
+            for (int i = 0; i < kCB; ++i) {
+                v[i] = kb + i < k1 ? qld_rw(segp + at(kb + i)) : qone();
+                tv[i] = kb + i < k1 ? qld(segT + at(kb + i)) : qzero();
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < kCB; ++i) {
+            pin[i] = run;
+            if (kb + i < k1) qst(segp + at(kb + i), run);
+            u = qadd(u, qmul(qconj(run), tv[i]));
+            run = qmul(v[i], run);
+        }
+    }
+    Qt r = u;  // inclusive suffix sum over lanes, then exclusive
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const Qt y = qshfl_down(r, o);
+        if (lane + o < 32) r = qadd(r, y);
+    }
+    r = qsub(r, u);
+    // the lane's segments in reverse, batch by batch from the last
+    const long long nb = (k1 - k0 + kCB - 1) / kCB;
+    for (long long bb = nb - 1; bb >= 0; --bb) {
+        const long long kb = k0 + bb * kCB;
+        if (!reuse) {
+#pragma unroll
+            for (int i = 0; i < kCB; ++i) {
+                pin[i] = kb + i < k1 ? qld_rw(segp + at(kb + i)) : qone();
+                tv[i] = kb + i < k1 ? qld(segT + at(kb + i)) : qzero();
+            }
+        }
+#pragma unroll
+        for (int i = kCB - 1; i >= 0; --i) {
+            if (kb + i < k1) {
+                qst(later + at(kb + i), r);
+                r = qadd(r, qmul(qconj(pin[i]), tv[i]));
+            }
+        }
+    }
+}
+
+__global__ void quat_bwd_apply(const float *__restrict__ q, const float *__restrict__ init,
+                               const float *__restrict__ d_cum, const float *__restrict__ p_ins,
+                               const float *__restrict__ segT, const float *__restrict__ laters,
+                               float *__restrict__ d_q, float *__restrict__ d_init, QShape s) {
     long long bi, sg, c;
     if (!qmap(s, bi, sg, c)) return;
-    // carry into the segment (product of the earlier segments, without init) and
-    // the later segments' part of the reverse cumsum
-    Qt prod = qone(), p_in = qone(), later = qzero();
-    for (long long k = 0; k < s.S; ++k) {
-        const long long so = ((bi * s.S + k) * s.C + c) * 4;
-        if (k == sg) p_in = prod;
-        else if (k > sg) later = qadd(later, qmul(qconj(prod), qld(segT + so)));
-        prod = qmul(qld(segp + so), prod);  // product of segments 0 .. k
-    }
-    const Qt own = qld(segT + ((bi * s.S + sg) * s.C + c) * 4);
+    const long long so = ((bi * s.S + sg) * s.C + c) * 4;
+    const Qt p_in = qld(p_ins + so), later = qld(laters + so), own = qld(segT + so);
     const Qt in = init ? qld(init + (bi * s.C + c) * 4) : qone();
     const Qt cin = qconj(p_in);
     const long long t0 = sg * kSeg, t1 = min(s.L, t0 + kSeg);
@@ -497,6 +625,7 @@ QShape qshape(int64_t b, int64_t L, int64_t H, int64_t J) {
 }
 
 unsigned qgrid(const QShape &s) { return (unsigned)((s.b * s.S * s.C + 255) / 256); }
+unsigned cgrid(const QShape &s) { return (unsigned)((s.b * s.C * 32 + 255) / 256); }  // a warp per chain
 
 template <typename T, int M>
 cudaError_t launch_y_fwd(const DShape &s, const void *V, const void *B, const void *C, const float *g, void *y,
@@ -553,7 +682,7 @@ extern "C" {
 size_t m3_quat_workspace_bytes(int64_t b, int64_t L, int64_t H, int64_t J, int backward) {
     if (b < 1 || L < 1 || H < 1 || J < 1) return 0;
     const QShape s = qshape(b, L, H, J);
-    return (size_t)(backward ? 2 : 1) * (size_t)(s.b * s.S * s.C * 4) * sizeof(float);
+    return (size_t)(backward ? 3 : 1) * (size_t)(s.b * s.S * s.C * 4) * sizeof(float);
 }
 
 ssd_status m3_quat_cumprod(const float *q, const float *init, float *cum, int64_t b, int64_t L, int64_t H,
@@ -568,7 +697,8 @@ ssd_status m3_quat_cumprod(const float *q, const float *init, float *cum, int64_
     cudaStream_t cs = (cudaStream_t)stream;
     float *segp = (float *)workspace;
     quat_seg_product<<<qgrid(s), 256, 0, cs>>>(q, segp, s);
-    quat_seg_scan<<<qgrid(s), 256, 0, cs>>>(q, init, segp, cum, s);
+    quat_seg_carry<<<cgrid(s), 256, 0, cs>>>(segp, init, s);
+    quat_seg_scan<<<qgrid(s), 256, 0, cs>>>(q, segp, cum, s);
     return cuda_status(cudaGetLastError());
 }
 
@@ -584,9 +714,10 @@ ssd_status m3_quat_cumprod_backward(const float *q, const float *init, const flo
     if (workspace_bytes < m3_quat_workspace_bytes(b, L, H, J, 1)) return m3_fail(SSD_ERR_WORKSPACE, "workspace too small");
     const QShape s = qshape(b, L, H, J);
     cudaStream_t cs = (cudaStream_t)stream;
-    float *segp = (float *)workspace, *segT = segp + s.b * s.S * s.C * 4;
+    float *segp = (float *)workspace, *segT = segp + s.b * s.S * s.C * 4, *later = segT + s.b * s.S * s.C * 4;
     quat_bwd_segments<<<qgrid(s), 256, 0, cs>>>(q, d_cum, segp, segT, s);
-    quat_bwd_apply<<<qgrid(s), 256, 0, cs>>>(q, init, d_cum, segp, segT, d_q, d_init, s);
+    quat_bwd_carry<<<cgrid(s), 256, 0, cs>>>(segp, segT, later, s);
+    quat_bwd_apply<<<qgrid(s), 256, 0, cs>>>(q, init, d_cum, segp, segT, later, d_q, d_init, s);
     return cuda_status(cudaGetLastError());
 }
 

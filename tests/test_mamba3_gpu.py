@@ -44,7 +44,10 @@ def m3():
 
 
 # ---------------------------------------------------------------- quaternion scan
-QUAT_SHAPES = [(1, 1, 1, 1), (2, 127, 3, 2), (2, 128, 2, 3), (1, 129, 4, 1), (3, 700, 5, 2), (1, 2049, 2, 8)]
+# ragged segment tails, one segment, many; 9000 steps give a lane more than
+# eight segments in the per-chain carry kernels (their batched path)
+QUAT_SHAPES = [(1, 1, 1, 1), (2, 127, 3, 2), (2, 128, 2, 3), (1, 129, 4, 1), (3, 700, 5, 2), (1, 2049, 2, 8),
+               (1, 9000, 1, 2)]
 
 
 @pytest.mark.parametrize("shape", QUAT_SHAPES)
