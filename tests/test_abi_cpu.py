@@ -43,8 +43,9 @@ def test_mamba3_calls_reject_bad_arguments_before_launch(lib):
     from state_space_model_mamba_gb300 import mamba3
     m = mamba3._lib()
     buf = ctypes.c_void_p(1 << 20)  # never dereferenced: every call below fails validation first
-    assert m.m3_quat_workspace_bytes(2, 300, 3, 2, 0) == 2 * 3 * 6 * 16
-    assert m.m3_quat_workspace_bytes(2, 300, 3, 2, 1) == 2 * 2 * 3 * 6 * 16
+    # one quaternion per (sample, 32-step segment, chain); three arrays of them for the backward
+    assert m.m3_quat_workspace_bytes(2, 300, 3, 2, 0) == 2 * 10 * 6 * 16
+    assert m.m3_quat_workspace_bytes(2, 300, 3, 2, 1) == 3 * 2 * 10 * 6 * 16
     assert m.m3_quat_workspace_bytes(0, 300, 3, 2, 0) == 0
     assert m.m3_quat_cumprod(None, None, buf, 1, 8, 1, 1, buf, 1 << 20, None) == ssd.SSD_ERR_INVALID_ARG
     assert m.m3_quat_cumprod(buf, None, buf, 1, 0, 1, 1, buf, 1 << 20, None) == ssd.SSD_ERR_INVALID_ARG
