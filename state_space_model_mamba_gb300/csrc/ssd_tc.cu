@@ -1721,10 +1721,13 @@ __global__ void __launch_bounds__(kThreadsWide, 1) tc_bwd_k3_kernel(const Params
 // with dW = dy x^T; the page's column sums over targets and the row sums over
 // sources reduce to these because dW is a product.  tgt and src are sums of the
 // same bf16 products (W^T, x and dy as the MMAs saw them), so their sums over
-// the chunk cancel to fp32 rounding as the page's do.  A valid token whose dt
-// is exactly 0 is scaled by 1e-30 instead (its W entries stay below any bf16
-// rounding of the others, and ddt_orange stays defined); rows past valid_len
-// are zero.  W^T is
+// the chunk cancel to fp32 rounding as the page's do.  A valid token whose
+// |dt| is below 2^-30 (an exact 0 included) scales its row by 2^-30 instead,
+// and ddt_orange divides by the same: the row factors of the factored decay
+// reach e^-64, and with the scale e^-64 * 2^-30 is still a normal bf16, where
+// a smaller scale would flush the row's near-diagonal entries to zero; the
+// row's entries stay 1e-6 below those of an ordinary dt, far under bf16
+// rounding of the others.  Rows past valid_len are zero.  W^T is
 // built in two halves (s-block 1, then s-block 0) so the first half's MMAs run
 // while the second half is built.  The decay is factored through 64-group
 // pivots off the diagonal groups and 16-wide sub-block pivots inside them (all
@@ -1893,10 +1896,10 @@ __global__ void __launch_bounds__(kThreadsWide, 1) tc_bwd_orange_kernel(const Pa
         // in registers, so the sub-block's direct exponentials need no lane-dependent
         // TMEM column.
         uint32_t cbown[8];
-        // the scale of row s of W^T: dt_s on valid tokens (1e-30 for an exact 0), 0 past valid_len
+        // the scale of row s of W^T: dt_s on valid tokens (+-2^-30 where |dt_s| < 2^-30), 0 past valid_len
         auto row_dt = [&](const float *f, int s) -> float {
             const float d = f[Q + s];
-            return s < vrows ? (d != 0.f ? d : 1e-30f) : 0.f;
+            return s < vrows ? (fabsf(d) >= 0x1p-30f ? d : (d < 0.f ? -0x1p-30f : 0x1p-30f)) : 0.f;
         };
         auto transform = [&](const float *f, int s, int tj) {
             const int sg = s >> 6, row = s & 127, mb = s >> 7;

@@ -156,9 +156,11 @@ def test_workload_full_size(name):
 # The ORANGE backward folds dt into its operand and recovers ddt by a division,
 # and the decay factors are split through pivots: exact zeros, tiny steps and a
 # head without decay exercise each on the tensor-core path (P = 64, N = 128,
-# Q = 256), against the oracle.
-def _degenerate(kind, seed):
-    inp = small(2, 700, 4, 64, 128, 2, seed=seed, valid_len=[517, 700], bf16=True)
+# Q = 256), against the oracle.  4 heads take the K1 / K3 / K4 chunk states;
+# 40 take the fused chunk-state scan (and, in the backward, its schedule that
+# reads K1's cumA).
+def _degenerate(kind, seed, H=4):
+    inp = small(2, 700, H, 64, 128, 2, seed=seed, valid_len=[517, 700], bf16=True)
     rng = np.random.default_rng(seed + 1)
     if kind in ("dt_zero", "dt_tiny"):
         pick = rng.random(inp["dt"].shape) < 0.05
@@ -171,15 +173,16 @@ def _degenerate(kind, seed):
     return inp
 
 
+@pytest.mark.parametrize("H", [4, 40])
 @pytest.mark.parametrize("kind", ["dt_zero", "dt_tiny", "A_zero"])
-def test_degenerate_values_tensor_cores(kind):
-    inp = _degenerate(kind, seed={"dt_zero": 120, "dt_tiny": 121, "A_zero": 122}[kind])
+def test_degenerate_values_tensor_cores(kind, H):
+    inp = _degenerate(kind, seed={"dt_zero": 120, "dt_tiny": 121, "A_zero": 122}[kind] + H, H=H)
     gpu = run_gpu(inp, "bf16", 256)
     errs = compare(gpu, run_oracle(inp), TOL["bf16"], kind, chunk=256)
     padded_grads_zero(gpu, inp["valid_len"])
     for k, v in gpu.items():
         assert np.isfinite(v).all(), k
-    print(kind, {k: f"{v:.2e}" for k, v in errs.items()})
+    print(kind, H, {k: f"{v:.2e}" for k, v in errs.items()})
 
 
 # ---------------------------------------------------------------- device-side status
