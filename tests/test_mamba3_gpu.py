@@ -123,3 +123,47 @@ def test_y_diag_full_size(m3, name):
         errs[nm] = check(a.float().cpu().numpy(), r, 2e-2, nm, 3)
     errs["d_gamma"] = check(dg.cpu().numpy(), rg, 2e-2, "d_gamma", 1)
     print(name, {k: f"{v[0]:.2e}/{v[1]:.2e}" for k, v in errs.items()})
+
+
+
+def host(t):
+    return t.float().cpu().numpy()
+
+
+@pytest.mark.parametrize("i", range(6))
+def test_quat_scan_random_shapes(m3, i):
+    """Random batch, length (up to ~19k steps: several carry batches per lane), heads, blocks."""
+    rng = np.random.default_rng(9700 + i)
+    b, L, H, J = int(rng.integers(1, 4)), int(rng.integers(1, 20000)), int(rng.integers(1, 5)), int(rng.integers(1, 5))
+    qi = generate_quat(QuatWorkload("r", b, L, H, J, seed=9710 + i), seed=None)
+    with_init = bool(i % 2)
+    init = qi["init"] if with_init else np.tile(np.array([1, 0, 0, 0], np.float32), (b, H, J, 1))
+    gin = dev(qi["init"]) if with_init else None
+    cum = m3.quat_cumprod(dev(qi["q"]), gin)
+    d_q, d_init = m3.quat_cumprod_backward(dev(qi["q"]), gin, dev(qi["d_cum"]))
+    torch.cuda.synchronize()
+    rq, ri = om3.quat_cumprod_backward_closed(qi["q"], init, qi["d_cum"])
+    check(host(cum), om3.quat_cumprod(qi["q"], init), 1e-4, "cum", 2)
+    check(host(d_q), rq, 1e-4, "d_q", 2)
+    check(host(d_init), ri, 1e-4, "d_init", 1)
+
+
+@pytest.mark.parametrize("i", range(8))
+def test_y_diag_random_shapes(m3, i):
+    """Random token count, rank, heads and (P, N): the one-piece-per-lane kernels and the looping ones."""
+    rng = np.random.default_rng(9800 + i)
+    T, m, H = int(rng.integers(1, 3000)), int(rng.integers(1, 5)), int(rng.integers(1, 9))
+    P, N = int(rng.choice([2, 6, 32, 64, 66, 130])), int(rng.choice([4, 10, 64, 128, 132]))
+    dtype = "bf16" if i % 2 == 0 else "f32"
+    di = generate_diag(DiagWorkload("r", T, m, H, P, N, dtype=dtype, seed=9810 + i))
+    tdt = torch.bfloat16 if dtype == "bf16" else torch.float32
+    V, B, C, dY = (dev(di[k], tdt) for k in ("V", "B", "C", "dY"))
+    g = dev(di["gamma"])
+    y = m3.y_diag(V, B, C, g)
+    grads = m3.y_diag_backward(dY, V, B, C, g)
+    torch.cuda.synchronize()
+    tol = 2e-2 if dtype == "bf16" else 1e-4
+    check(host(y), om3.y_diag(di["V"], di["B"], di["C"], di["gamma"]), tol, "y", 1)
+    for name, a, r in zip(("dV", "dB", "dC", "d_gamma"), grads,
+                          om3.y_diag_vjp(di["dY"], di["V"], di["B"], di["C"], di["gamma"])):
+        check(host(a), r, tol, name, 1)

@@ -80,6 +80,21 @@ def test_state_moments_full_size_head_sample():
     print("mamba2_2p7b heads 0-3", f"m2 {e2[0]:.2e}/{e2[1]:.2e}", f"m1 {e1[0]:.2e}/{e1[1]:.2e}")
 
 
+@pytest.mark.parametrize("i", range(8))
+def test_state_moments_random_shapes(i):
+    """Random batch, length, groups, heads and ragged valid lengths; both chunk-state paths."""
+    rng = np.random.default_rng(9500 + i)
+    b, L, G = int(rng.integers(1, 4)), int(rng.integers(1, 1200)), int(rng.choice([1, 2]))
+    H = G * int(rng.integers(1, 24))
+    vl = [int(v) for v in rng.integers(0, L + 1, size=b)] if rng.random() < 0.6 else None
+    inp = generate_small(b, L, H, 64, 128, G, seed=9600 + i, init_std=0.3, valid_len=vl, bf16=True)
+    m2, m1, n = gpu_moments(inp, split=bool(i % 2))
+    r2, r1, rn = oracle.state_moments(inp["x"], inp["dt"], inp["A"], inp["B"], inp["init"], inp["valid_len"])
+    assert list(n) == list(rn)
+    slicewise(m2, r2, 2e-2, "m2")
+    slicewise(m1, r1, 2e-2, "m1")
+
+
 PAIRINGS = [(0, 0), (1, 40), (1, 64), (2, 16), (2, 64), (3, 8), (3, 32)]
 
 
