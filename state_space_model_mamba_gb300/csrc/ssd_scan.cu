@@ -133,15 +133,16 @@ __device__ __forceinline__ void store16(bf16 *dst, const float *v) {
     q[1] = make_uint4(w[4], w[5], w[6], w[7]);
 }
 
-// chunks read ahead: bounded by registers (the grid must stay one wave)
-template <typename S>
-__host__ __device__ constexpr int k4_ahead_fwd() { return sizeof(S) == 2 ? 4 : 2; }
-template <typename S>
-__host__ __device__ constexpr int k4_ahead_bwd() { return sizeof(S) == 2 ? 4 : 2; }
+// Chunks read ahead (U): bounded by registers, since the grid must stay one
+// wave.  A grid of at most one block per SM (few (b, h) chains: the 131k-token
+// workload has 32, 128 blocks) takes a deep read-ahead and the registers it
+// needs; larger grids keep five blocks per SM and a short one.  MB: the blocks
+// per SM the launch bounds promise.
+constexpr int k4_min_blocks(int U, int bytes) { return U * bytes >= 32 ? 1 : (U * bytes >= 16 ? 2 : 5); }
 
-template <typename S>
-__global__ void __launch_bounds__(kK4Threads, 5) k4_state_passing(Params p, S *st, int write_final) {
-    constexpr int U = k4_ahead_fwd<S>();
+template <typename S, int U>
+__global__ void __launch_bounds__(kK4Threads, k4_min_blocks(U, sizeof(S)))
+    k4_state_passing(Params p, S *st, int write_final) {
     const size_t PN = (size_t)p.P * p.N, nvec = PN / kVec;
     const size_t gid = blockIdx.x * (size_t)blockDim.x + threadIdx.x;
     if (gid >= (size_t)p.b * p.H * nvec) return;
@@ -186,13 +187,27 @@ __global__ void __launch_bounds__(kK4Threads, 5) k4_state_passing(Params p, S *s
     if (write_final && p.final_state) store16(p.final_state + bh * PN + kVec * e, s);
 }
 
+// blocks per SM of a K4 grid on this device (1: at most one block on every SM)
+static int k4_per_sm(long long blocks) {
+    int dev = 0, sms = 152;
+    if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    return (int)((blocks + sms - 1) / sms);
+}
+
 cudaError_t launch_k4_state_passing(const Params &p, bool write_final, cudaStream_t s) {
     const long long nthr = (long long)p.b * p.H * ((long long)p.P * p.N / kVec);
     const long long blocks = (nthr + kK4Threads - 1) / kK4Threads;
-    if (p.states)
-        k4_state_passing<float><<<(unsigned)blocks, kK4Threads, 0, s>>>(p, p.states, write_final ? 1 : 0);
-    else
-        k4_state_passing<bf16><<<(unsigned)blocks, kK4Threads, 0, s>>>(p, p.states_bf, write_final ? 1 : 0);
+    const int per_sm = k4_per_sm(blocks), wf = write_final ? 1 : 0;
+    const unsigned g = (unsigned)blocks;
+    if (p.states) {  // fp32 states: 16 registers per chunk read ahead
+        if (per_sm <= 1) k4_state_passing<float, 8><<<g, kK4Threads, 0, s>>>(p, p.states, wf);
+        else if (per_sm <= 2) k4_state_passing<float, 4><<<g, kK4Threads, 0, s>>>(p, p.states, wf);
+        else k4_state_passing<float, 2><<<g, kK4Threads, 0, s>>>(p, p.states, wf);
+    } else {         // bf16 states: 8 registers per chunk
+        if (per_sm <= 1) k4_state_passing<bf16, 16><<<g, kK4Threads, 0, s>>>(p, p.states_bf, wf);
+        else if (per_sm <= 2) k4_state_passing<bf16, 8><<<g, kK4Threads, 0, s>>>(p, p.states_bf, wf);
+        else k4_state_passing<bf16, 4><<<g, kK4Threads, 0, s>>>(p, p.states_bf, wf);
+    }
     return cudaGetLastError();
 }
 
@@ -205,9 +220,8 @@ cudaError_t launch_k4_state_passing(const Params &p, bool write_final, cudaStrea
 // (b, h, chunk), summed in a fixed order by the K1 backward), so the chunk
 // loop has no block barrier.  `dst` holds d_s_in on entry and d_intra on
 // exit; `st` holds s_in.
-template <typename S>
-__global__ void __launch_bounds__(kK4Threads, 5) bwd_k4_state_passing(Params p, S *dst, const S *st) {
-    constexpr int U = k4_ahead_bwd<S>();
+template <typename S, int U, int MB>
+__global__ void __launch_bounds__(kK4Threads, MB) bwd_k4_state_passing(Params p, S *dst, const S *st) {
     const size_t PN = (size_t)p.P * p.N, nvec = PN / kVec;
     const int nblk = (int)((nvec + kK4Threads - 1) / kK4Threads);
     const int bh = blockIdx.x / nblk, slab = blockIdx.x % nblk;
@@ -261,10 +275,16 @@ __global__ void __launch_bounds__(kK4Threads, 5) bwd_k4_state_passing(Params p, 
 cudaError_t launch_bwd_k4(const Params &p, cudaStream_t s) {
     const long long nvec = (long long)p.P * p.N / kVec;
     const long long blocks = (long long)p.b * p.H * ((nvec + kK4Threads - 1) / kK4Threads);
-    if (p.dstates)
-        bwd_k4_state_passing<float><<<(unsigned)blocks, kK4Threads, 0, s>>>(p, p.dstates, p.states);
-    else
-        bwd_k4_state_passing<bf16><<<(unsigned)blocks, kK4Threads, 0, s>>>(p, p.dstates_bf, p.states_bf);
+    const int per_sm = k4_per_sm(blocks);
+    const unsigned g = (unsigned)blocks;
+    // two chunks (d_s_in and s_in) per step read ahead; one block per SM: deep, else five per SM
+    if (p.dstates) {
+        if (per_sm <= 1) bwd_k4_state_passing<float, 4, 1><<<g, kK4Threads, 0, s>>>(p, p.dstates, p.states);
+        else bwd_k4_state_passing<float, 2, 5><<<g, kK4Threads, 0, s>>>(p, p.dstates, p.states);
+    } else {
+        if (per_sm <= 1) bwd_k4_state_passing<bf16, 8, 1><<<g, kK4Threads, 0, s>>>(p, p.dstates_bf, p.states_bf);
+        else bwd_k4_state_passing<bf16, 4, 5><<<g, kK4Threads, 0, s>>>(p, p.dstates_bf, p.states_bf);
+    }
     return cudaGetLastError();
 }
 
