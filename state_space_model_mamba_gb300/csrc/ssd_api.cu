@@ -104,6 +104,8 @@ struct Layout {
     size_t status, cumA, endA, CB, states, states_bf, dstates, dstates_bf;
     size_t dcum_blue, dcum_main, d_delta, ddt_main, d_endA_part, dD_part, dA_part, d_cb, dBC_part;
     size_t d_cb_bf, cb_count, fin_count;
+    size_t k4s_sync, k4s_agg, k4s_carry, k4s_dec;
+    size_t clear;  // bytes from the workspace's start that every call zeroes (status words, K4 sync)
     int n_count;
     size_t total;
     int k4_nblk, dD_per, nslice, nslice_cb, nslice_k5, nslice_k3;
@@ -152,6 +154,18 @@ Layout make_layout(const ssd_dims &d, ssd_dtype dt, bool backward) {
     size_t off = 0;
     auto take = [&](size_t bytes) { size_t o = off; off += align_up(bytes); return o; };
     lo.status = take(sizeof(int) * kStatusWords);
+    // the segmented state passing's ticket counter and flags follow the status
+    // words, so that one memset clears both
+    const size_t sync_ints = k4_seg_sync_ints(b, H, P, N, n, !tc);
+    lo.k4s_sync = sync_ints ? take(sizeof(int) * sync_ints) : 0;
+    lo.clear = off;
+    if (sync_ints) {
+        const K4SegGeom g = k4_seg_geom(b, H, P, N, n, !tc);
+        const size_t ent = (size_t)kK4Threads * kK4Vec;
+        lo.k4s_agg = take(4 * (size_t)g.pairs * g.K * ent);
+        lo.k4s_carry = take(4 * (size_t)g.pairs * g.KG * ent);
+        lo.k4s_dec = take(4 * (size_t)g.pairs * g.K);
+    }
     lo.cumA = take(4 * tok);
     lo.endA = take(4 * b * H * n);
     // CB: fp32 on the CUDA-core path; bf16 CB and CB^T on the tensor-core path, where
@@ -234,6 +248,10 @@ Params base_params(const ssd_dims &d, const Layout &lo, void *ws) {
         p.CBh = (bf16 *)(w + lo.CB);
         p.CBt = p.CBh + (size_t)p.b * p.n * p.G * p.Q * p.Q;
     }
+    p.k4s_sync = lo.k4s_sync ? (int *)(w + lo.k4s_sync) : nullptr;
+    p.k4s_agg = lo.k4s_agg ? f(lo.k4s_agg) : nullptr;
+    p.k4s_carry = lo.k4s_carry ? f(lo.k4s_carry) : nullptr;
+    p.k4s_dec = lo.k4s_dec ? f(lo.k4s_dec) : nullptr;
     p.states = lo.states ? f(lo.states) : nullptr;
     p.states_bf = lo.states_bf ? (bf16 *)(w + lo.states_bf) : nullptr;
     if (lo.dcum_blue) {  // backward layout
@@ -458,7 +476,7 @@ ssd_status ssd_forward(const ssd_dims *dims, ssd_dtype dtype, const void *x, con
     p.valid_len = valid_len; p.y = y; p.final_state = final_state;
     cudaStream_t s = (cudaStream_t)stream;
     g_launches = 0;
-    SSD_TRY(cudaMemsetAsync(p.status, 0, sizeof(int) * kStatusWords, s));
+    SSD_TRY(cudaMemsetAsync(workspace, 0, lo.clear, s));  // status words and K4 sync
     if (dtype == SSD_F32) {
         st = run_forward_chain<float>(p, *dims, false, true, s, nullptr);
         if (st != SSD_OK) return st;
@@ -516,7 +534,7 @@ ssd_status ssd_backward(const ssd_dims *dims, ssd_dtype dtype, const void *x, co
     p.dA = dA; p.dB = dB; p.dC = dC; p.dD = dD; p.d_init = d_init_state;
     cudaStream_t s = (cudaStream_t)stream;
     g_launches = 0;
-    SSD_TRY(cudaMemsetAsync(p.status, 0, sizeof(int) * kStatusWords, s));
+    SSD_TRY(cudaMemsetAsync(workspace, 0, lo.clear, s));  // status words and K4 sync
     if (dtype == SSD_F32) {
         st = run_forward_chain<float>(p, *dims, false, false, s, nullptr);
         if (st != SSD_OK) return st;
@@ -622,7 +640,7 @@ ssd_status ssd_state_moments(const ssd_dims *dims, ssd_dtype dtype, const void *
     p.mom_ranges = ml.ranges;
     cudaStream_t s = (cudaStream_t)stream;
     g_launches = 0;
-    SSD_TRY(cudaMemsetAsync(p.status, 0, sizeof(int) * kStatusWords, s));
+    SSD_TRY(cudaMemsetAsync(workspace, 0, ml.lo.clear, s));  // status words and K4 sync
     // the chunk-input states at chunk 128 (fused scan or K1 + K3 + K4), then the moments
     st = run_forward_chain<bf16>(p, ml.d, true, false, s, nullptr);
     if (st != SSD_OK) return st;

@@ -59,6 +59,11 @@ struct Params {
     float *mom_m1;       // [mom_ranges, b, H, N]
     int mom_ranges;      // chunk ranges per (b, h) of the state-moment kernel
     int cumA_given;      // the chunk-state scan reads cumA / endA (K1 ran before it)
+    // time-segmented state passing (few, long (b, h) chains; K4SegGeom below)
+    int *k4s_sync;       // ticket counter and ready flags, zeroed by every call with the status words
+    float *k4s_agg;      // [pairs, K, kK4Threads * kK4Vec] each segment's state change from zero
+    float *k4s_carry;    // [pairs, KG, kK4Threads * kK4Vec] carry into each group's first segment
+    float *k4s_dec;      // [pairs, K] each segment's decay (product of its chunks' exp(endA))
 };
 
 // The workspace's status words (cleared by every call before its first kernel):
@@ -165,5 +170,32 @@ constexpr int kK4Threads = 128;             // threads per block of the state-pa
 constexpr int kK4Vec = 16;                   // state entries per thread of the state-passing kernels
 constexpr int kMaxQ = 256;                   // largest supported chunk length
 constexpr int kMainRows = 16;               // source rows per block of the backward main kernel
+
+// Time-segmented state passing (forward).  With few (b, h) chains the
+// chunk-serial K4 grid holds a fraction of the GPU and its speed is set by
+// memory latency; the recurrence s_{c+1} = a_c s_c + v_c is linear, so the
+// chunks are cut into segments of T, each (chain, slice, segment) ticket
+// reduces its segment from a zero state, and the carry into a segment is
+// rebuilt from the earlier segments' reductions in one fixed order
+// (deterministic results).  Used when the chunk-serial grid has at most
+// kK4SegMaxBlocks blocks, P * N fills whole 2048-entry slices and the chains
+// have at least two segments.
+constexpr int kK4SegGroup = 8;               // segments per group (carry published at each group's start)
+constexpr int kK4SegMaxBlocks = 304;         // two 128-thread blocks per SM on a 152-SM GPU
+constexpr int kK4SegSyncHead = 64;           // ints before the ready flags: [0] the ticket counter
+struct K4SegGeom {
+    int on;            // 1: the segmented kernel runs
+    int T;             // chunks per segment
+    int K;             // segments per chain
+    int KG;            // segment groups per chain, ceil(K / kK4SegGroup)
+    int slices;        // kK4Threads-thread slices of one (b, h) state
+    long long pairs;   // b * H * slices
+};
+// Geometry of the forward state passing; fp32_states selects the CUDA-core
+// path's fp32 chunk states.
+K4SegGeom k4_seg_geom(long long b, long long H, long long P, long long N, long long n, bool fp32_states);
+// Ints of the sync region (ticket counter, then the ready flags) for these
+// dims; 0 when the state passing is not segmented.
+size_t k4_seg_sync_ints(long long b, long long H, long long P, long long N, long long n, bool fp32_states);
 
 }  // namespace ssd

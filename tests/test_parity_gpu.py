@@ -141,6 +141,31 @@ def test_bf16_chunk_state_paths(Q, b, H, G, split):
     print(f"Q={Q} b={b} H={H} split={split}", {k: f"{v:.2e}" for k, v in errs.items()})
 
 
+# ---------------------------------------------------------------- time-segmented state passing
+# With few (b, h) chains the forward state passing (and the backward's
+# recompute of it) cuts each chain into segments of chunks (8 per segment on
+# the tensor-core path, 4 with fp32 states) and rebuilds each segment's carry
+# from the earlier segments' reductions, group by group (8 segments a group).
+# These shapes (P * N a multiple of the 2048-entry slice, few chains) give five
+# groups, a partial last segment, ragged valid lengths and an initial state;
+# two runs must agree bit for bit.
+@pytest.mark.parametrize("case", ["tc", "cuda_core"])
+def test_segmented_state_passing_several_groups(case):
+    if case == "tc":
+        inp = small(1, 64 * 300 - 17, 2, 64, 128, 1, seed=190, bf16=True)
+        dtype, Q = "bf16", 64
+    else:
+        inp = small(2, 16 * 150 - 5, 3, 16, 128, 1, seed=191, valid_len=[2395, 1700])
+        dtype, Q = "f32", 16
+    a = run_gpu(inp, dtype, Q)
+    errs = compare(a, run_oracle(inp), TOL[dtype], f"segmented state passing {case}", chunk=Q)
+    padded_grads_zero(a, inp["valid_len"])
+    b = run_gpu(inp, dtype, Q)
+    for k in a:
+        assert np.array_equal(a[k], b[k]), k
+    print(case, {k: f"{v:.2e}" for k, v in errs.items()})
+
+
 # ---------------------------------------------------------------- full-size workloads
 @pytest.mark.parametrize("name", ["mamba2_130m", "mamba2_2p7b", "grouped_padded", "long_seq"])
 def test_workload_full_size(name):
