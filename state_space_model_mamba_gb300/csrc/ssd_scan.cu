@@ -382,11 +382,12 @@ __device__ __forceinline__ void seg_st_pub(float *blk, const float *v) {
 }
 
 // Publishes this thread's 16 values at blk (every thread), then the flag (the
-// barrier orders every thread's stores before thread 0's release store).
+// barrier orders every thread's stores before the release store, which warp 1
+// issues so that warp 0, which waits on flags next, does not stall on it).
 __device__ __forceinline__ void seg_publish(float *blk, const float *v, int *flag) {
     seg_st_pub(blk, v);
     __syncthreads();
-    if (threadIdx.x == 0) st_release(flag, 1);
+    if (threadIdx.x == 32) st_release(flag, 1);
 }
 
 // Step 2: the carry into segment r of `pair` (16 entries of this thread), from
@@ -417,27 +418,33 @@ __device__ void seg_carry(const Params &p, const SegDev &g, long long pair, int 
 #pragma unroll
         for (int i = 0; i < kVec; ++i) c[i] = 0.f;
     }
-    // the fold's loads are issued together (at most kK4SegGroup segments), a
-    // quarter of the 16 entries at a time, then applied in segment order
+    // the fold's loads are issued together (at most kK4SegGroup segments), half
+    // of the 16 entries at a time, then applied in segment order
     const int m = r - start;
     float dd[kK4SegGroup];
 #pragma unroll
     for (int jj = 0; jj < kK4SegGroup; ++jj) dd[jj] = jj < m ? __ldcg(p.k4s_dec + (size_t)pair * g.K + start + jj) : 0.f;
     const float4 *q0 = reinterpret_cast<const float4 *>(p.k4s_agg + ((size_t)pair * g.K + start) * kSegSlice);
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-        float4 t[kK4SegGroup];
+    for (int k2 = 0; k2 < 4; k2 += 2) {
+        float4 t[2][kK4SegGroup];
 #pragma unroll
-        for (int jj = 0; jj < kK4SegGroup; ++jj)
-            if (jj < m) t[jj] = __ldcg(q0 + (size_t)jj * (kSegSlice / 4) + k * kK4Threads + threadIdx.x);
+        for (int h = 0; h < 2; ++h)
 #pragma unroll
-        for (int jj = 0; jj < kK4SegGroup; ++jj)
-            if (jj < m) {
-                c[4 * k] = fmaf(dd[jj], c[4 * k], t[jj].x);
-                c[4 * k + 1] = fmaf(dd[jj], c[4 * k + 1], t[jj].y);
-                c[4 * k + 2] = fmaf(dd[jj], c[4 * k + 2], t[jj].z);
-                c[4 * k + 3] = fmaf(dd[jj], c[4 * k + 3], t[jj].w);
-            }
+            for (int jj = 0; jj < kK4SegGroup; ++jj)
+                if (jj < m) t[h][jj] = __ldcg(q0 + (size_t)jj * (kSegSlice / 4) + (k2 + h) * kK4Threads + threadIdx.x);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int k = k2 + h;
+#pragma unroll
+            for (int jj = 0; jj < kK4SegGroup; ++jj)
+                if (jj < m) {
+                    c[4 * k] = fmaf(dd[jj], c[4 * k], t[h][jj].x);
+                    c[4 * k + 1] = fmaf(dd[jj], c[4 * k + 1], t[h][jj].y);
+                    c[4 * k + 2] = fmaf(dd[jj], c[4 * k + 2], t[h][jj].z);
+                    c[4 * k + 3] = fmaf(dd[jj], c[4 * k + 3], t[h][jj].w);
+                }
+        }
     }
     if (r > 0 && r % G == 0 && r < g.K - 1)
         seg_publish(p.k4s_carry + ((size_t)pair * g.KG + r / G) * kSegSlice, c, g.carryflag + pair * g.KG + r / G);
@@ -514,6 +521,10 @@ __global__ void __launch_bounds__(kK4Threads, 3) k4_state_passing_seg(Params p, 
     long long t = seg_draw(g, &tk[slot]);
     if (t < total) issue(t, buf);
     while (t < total) {
+        // the next ticket's atomic goes out first; its value is needed only
+        // after the reduction (so its round trip overlaps the copy wait)
+        int nxt = 0;
+        if (threadIdx.x == 0) nxt = atomicAdd(g.ticket, 1);
         const SegPos q = seg_pos(p, g, t);
         const long long pair = t % g.pairs;
         const int c0 = q.r * T;
@@ -537,13 +548,17 @@ __global__ void __launch_bounds__(kK4Threads, 3) k4_state_passing_seg(Params p, 
                 for (int i = 0; i < kVec; ++i) acc[i] = fmaf(a[u], acc[i], x[i]);
             }
         }
+        // (the slot was last read before the previous iteration's barriers)
+        slot ^= 1;
+        if (threadIdx.x == 0) tk[slot] = nxt;
         if (q.r < g.K - 1) {
             if (threadIdx.x == 0) p.k4s_dec[(size_t)pair * g.K + q.r] = dec;
             seg_publish(p.k4s_agg + ((size_t)pair * g.K + q.r) * kSegSlice, acc, g.aggflag + pair * g.K + q.r);
+        } else {
+            __syncthreads();
         }
         // the next segment's copies go out now
-        slot ^= 1;
-        const long long t2 = seg_draw(g, &tk[slot]);
+        const long long t2 = tk[slot];
         if (t2 < total) issue(t2, buf ^ 1);
         // 2. the carry in
         float sv[kVec];
