@@ -325,55 +325,11 @@ __device__ __forceinline__ long long seg_draw(const SegDev &g, int *sh) {
     return *sh;
 }
 
-// ---- this thread's 16 entries of a slice, 16-byte pieces (see above)
+// ---- this thread's 16 entries of a slice, 16-byte pieces (see above): the
+// chunk-serial kernels' helpers with e = threadIdx.x address them from the
+// slice's first entry
 template <typename S>
 __host__ __device__ constexpr int seg_pieces() { return kVec * (int)sizeof(S) / 16; }
-// Entries of a chunk state S (bf16 / fp32) written from v[16].
-template <typename S>
-__device__ __forceinline__ void seg_st_state(S *slice, const float *v) {
-    constexpr int PC = seg_pieces<S>(), EP = kVec / PC;
-#pragma unroll
-    for (int q = 0; q < PC; ++q) {
-        S *dst = slice + (size_t)(q * kK4Threads + threadIdx.x) * EP;
-        if constexpr (sizeof(S) == 4) {
-            *reinterpret_cast<float4 *>(dst) = make_float4(v[q * EP], v[q * EP + 1], v[q * EP + 2], v[q * EP + 3]);
-        } else {
-            uint32_t w[4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                __nv_bfloat162 h2 = __floats2bfloat162_rn(v[q * EP + 2 * i], v[q * EP + 2 * i + 1]);
-                w[i] = *reinterpret_cast<uint32_t *>(&h2);
-            }
-            *reinterpret_cast<uint4 *>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
-        }
-    }
-}
-// fp32 values (initial state, final state and their gradients) at the entries
-// a state of type S maps to this thread.
-template <typename S>
-__device__ __forceinline__ void seg_ld_f32(const float *slice, float *v) {
-    constexpr int PC = seg_pieces<S>(), EP = kVec / PC;
-#pragma unroll
-    for (int q = 0; q < PC; ++q) {
-        const float4 *src = reinterpret_cast<const float4 *>(slice + (size_t)(q * kK4Threads + threadIdx.x) * EP);
-#pragma unroll
-        for (int k = 0; k < EP / 4; ++k) {
-            const float4 x = src[k];
-            v[q * EP + 4 * k] = x.x; v[q * EP + 4 * k + 1] = x.y; v[q * EP + 4 * k + 2] = x.z; v[q * EP + 4 * k + 3] = x.w;
-        }
-    }
-}
-template <typename S>
-__device__ __forceinline__ void seg_st_f32(float *slice, const float *v) {
-    constexpr int PC = seg_pieces<S>(), EP = kVec / PC;
-#pragma unroll
-    for (int q = 0; q < PC; ++q) {
-        float4 *dst = reinterpret_cast<float4 *>(slice + (size_t)(q * kK4Threads + threadIdx.x) * EP);
-#pragma unroll
-        for (int k = 0; k < EP / 4; ++k)
-            dst[k] = make_float4(v[q * EP + 4 * k], v[q * EP + 4 * k + 1], v[q * EP + 4 * k + 2], v[q * EP + 4 * k + 3]);
-    }
-}
 // The published 16 fp32 values of a ticket: 2048 floats as [4][128 threads] float4.
 __device__ __forceinline__ void seg_st_pub(float *blk, const float *v) {
     float4 *d = reinterpret_cast<float4 *>(blk);
@@ -413,7 +369,7 @@ __device__ void seg_carry(const Params &p, const SegDev &g, long long pair, int 
             c[4 * k] = t.x; c[4 * k + 1] = t.y; c[4 * k + 2] = t.z; c[4 * k + 3] = t.w;
         }
     } else if (base) {
-        seg_ld_f32<S>(base, c);
+        ld_f32<S, true>(base, threadIdx.x, c);
     } else {
 #pragma unroll
         for (int i = 0; i < kVec; ++i) c[i] = 0.f;
@@ -466,11 +422,10 @@ __device__ __forceinline__ void cp_async_wait_all() {
 // Copies this thread's pieces of one chunk's slice into slot `slot`.
 template <typename S>
 __device__ __forceinline__ void seg_stage(uint4 *sm, int slot, const S *slice) {
-    constexpr int PC = seg_pieces<S>(), EP = kVec / PC;
+    constexpr int PC = seg_pieces<S>();
 #pragma unroll
     for (int q = 0; q < PC; ++q)
-        cp_async16(sm + ((size_t)slot * PC + q) * kK4Threads + threadIdx.x,
-                   slice + (size_t)(q * kK4Threads + threadIdx.x) * EP);
+        cp_async16(sm + ((size_t)slot * PC + q) * kK4Threads + threadIdx.x, slice + piece_off<S, true>(threadIdx.x, q));
 }
 template <typename S>
 __device__ __forceinline__ void seg_unpack(const uint4 *sm, int slot, float *v) {
@@ -568,14 +523,14 @@ __global__ void __launch_bounds__(kK4Threads, 3) k4_state_passing_seg(Params p, 
         for (int u = 0; u < T; ++u) {
             const int c = c0 + u;
             if (c < p.n) {
-                seg_st_state<S>(st + ix_state(p, q.bi, c, q.h) + soff, sv);
+                st_vals<S, true>(st + ix_state(p, q.bi, c, q.h) + soff, threadIdx.x, sv);
                 float x[kVec];
                 seg_unpack<S>(seg_sm, buf * T + u, x);
 #pragma unroll
                 for (int i = 0; i < kVec; ++i) sv[i] = fmaf(a[u], sv[i], x[i]);
             }
         }
-        if (q.r == g.K - 1 && write_final && p.final_state) seg_st_f32<S>(p.final_state + q.bh * PN + soff, sv);
+        if (q.r == g.K - 1 && write_final && p.final_state) st_f32<S, true>(p.final_state + q.bh * PN + soff, threadIdx.x, sv);
         t = t2;
         buf ^= 1;
     }
@@ -606,7 +561,9 @@ K4SegGeom k4_seg_geom(long long b, long long H, long long P, long long N, long l
     g.T = fp32_states ? 4 : 8;
     g.K = (int)((n + g.T - 1) / g.T);
     g.KG = (g.K + kK4SegGroup - 1) / kK4SegGroup;
-    g.on = (P * N) % (kK4Threads * kVec) == 0 && g.pairs <= kK4SegMaxBlocks && g.K >= 2;
+    // (the 32-bit ticket counter ends at the tickets plus one per block)
+    g.on = (P * N) % (kK4Threads * kVec) == 0 && g.pairs <= kK4SegMaxBlocks && g.K >= 2 &&
+           g.pairs * (long long)g.K <= (1LL << 30);
     return g;
 }
 
