@@ -41,18 +41,23 @@
  *
  * Streams and errors: work is enqueued on `stream` (a cudaStream_t; NULL is
  * the legacy default stream) and the call returns without synchronising.
- * The tensor-core path forks part of its kernels onto a second stream that
- * the library creates once per device (non-blocking, with three events) and
- * joins it back into `stream` before returning, so to the caller every call
- * is ordered on `stream` as if all its kernels ran there; tensor-core calls
- * from several host threads enqueue one at a time (a lock).
+ * The tensor-core backward forks part of its kernels onto a second stream
+ * that the library creates once per (device, caller stream) pair
+ * (non-blocking, with three events, kept until the process exits) and joins
+ * it back into `stream` before returning, so to the caller every call is
+ * ordered on `stream` as if all its kernels ran there.  Calls that share a
+ * caller stream enqueue one at a time (a lock per caller stream); calls on
+ * different streams do not wait for each other.
  * Argument errors are detected on the host and returned before anything is
  * enqueued.  Launch failures return SSD_ERR_CUDA.  Three conditions can only be
- * seen on the device; each call clears the first 16 bytes of its workspace
- * (its status words) and the kernels record them there, readable with
+ * seen on the device; each call clears the start of its workspace (its status
+ * words in the first 16 bytes, and, when few long (batch, head) chains take
+ * the time-segmented state passing, that pass's ticket counter and ready
+ * flags after them) and the kernels record them there, readable with
  * ssd_workspace_status() once the call's work has finished:
- *   - a wait on a shared-memory barrier that gives up after its time limit
- *     (SSD_ERR_TIMEOUT; the call's outputs are then undefined);
+ *   - a wait on a shared-memory barrier, or on another block's ready flag,
+ *     that gives up after its time limit (SSD_ERR_TIMEOUT; the call's outputs
+ *     are then undefined);
  *   - valid_len entries outside [0, seqlen]: such an entry is clamped into the
  *     range, the call completes with the clamped value, and the count of
  *     clamped entries is reported (SSD_ERR_INVALID_ARG);
