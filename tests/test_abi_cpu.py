@@ -89,6 +89,48 @@ def test_workspace_sizes(lib):
     assert r > f
 
 
+def _forward_workspace(b, L, H, P, N, Q, fp32_states):
+    """The forward's workspace as documented: 256-byte aligned regions for the
+    status words, (segmented state passing only) its ticket counter and ready
+    flags, per-segment reductions, group carries and decays, then cumA, endA,
+    the CB region (CUDA-core path only) and the chunk states."""
+    al = lambda v: (v + 255) // 256 * 256
+    n = -(-L // Q)
+    slices = -(-(P * N // 16) // 128)
+    pairs = b * H * slices
+    T = 4 if fp32_states else 8
+    K = -(-n // T)
+    KG = -(-K // 8)
+    seg = (P * N) % 2048 == 0 and pairs <= 304 and K >= 2
+    total = al(16)
+    if seg:
+        total += al(4 * (64 + pairs * (K + KG))) + al(4 * pairs * K * 2048) + al(4 * pairs * KG * 2048) + al(4 * pairs * K)
+    total += al(4 * b * H * n * Q) + al(4 * b * H * n)
+    if fp32_states:
+        total += al(4 * b * n * Q * Q)                       # fp32 CB, one group
+    total += al((4 if fp32_states else 2) * b * n * H * P * N)
+    return total, seg
+
+
+@pytest.mark.parametrize("shape", [
+    dict(batch=1, seqlen=131072, nheads=32),                 # 32 chains of 512 chunks: segmented
+    dict(batch=1, seqlen=131072, nheads=32, flags=ssd.SSD_FLAG_SIMT),  # fp32 states: segmented
+    dict(batch=1, seqlen=131072, nheads=76),                 # 304 blocks: segmented
+    dict(batch=1, seqlen=131072, nheads=80),                 # 320 blocks: chunk-serial
+    dict(batch=1, seqlen=2048, nheads=2),                    # one segment per chain: chunk-serial
+    # P * N below one slice (and outside the tensor-core shapes: fp32 states): chunk-serial
+    dict(batch=1, seqlen=8192, nheads=2, headdim=32, dstate=32),
+])
+def test_forward_workspace_layout_and_segmented_state_passing(lib, shape):
+    kw = dict(shape)
+    d = _dims(**kw)
+    simt = bool(kw.get("flags", 0) & ssd.SSD_FLAG_SIMT) or (d.headdim, d.dstate) != (64, 128)
+    want, seg = _forward_workspace(d.batch, d.seqlen, d.nheads, d.headdim, d.dstate, d.chunk_len, simt)
+    assert lib.ssd_workspace_bytes(ctypes.byref(d), ssd.SSD_BF16, 0) == want
+    expect_seg = {(32, 131072): True, (76, 131072): True}.get((d.nheads, d.seqlen), False)
+    assert seg == expect_seg
+
+
 @pytest.mark.parametrize("kw,code", [
     (dict(ngroups=3), ssd.SSD_BF16 and 1),
     (dict(chunk_len=100), 2),
