@@ -273,7 +273,7 @@ __global__ void __launch_bounds__(kK4Threads, k4_min_blocks(U, sizeof(S)))
 // Tickets are drawn from a counter in segment order, so a ticket waits only
 // on smaller ones.  Waits are bounded (2 s); on expiry the call's status
 // records SSD_ERR_TIMEOUT and the block goes on with what it has.
-// Measured on the 131k-token sequence (GB300): 152 us against 389 us for the
+// Measured on the 131k-token sequence (GB300): 137 us against 389 us for the
 // chunk-serial kernel.  The backward keeps its chunk-serial kernel, which ran
 // faster there than this scheme in reverse chunk order (207 against 271 us).
 //
